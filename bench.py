@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Benchmark of the k-quant x q8_1 contraction on GB300.
+
+One "step" is one pass of the whole hot path over one batch of synthetic
+input: q8_1 quantization of every distinct activation, then the GEMV (decode)
+or MMQ (prefill) of every weight that reads it, residual adds fused.
+
+Workloads (benchmark configurations; shapes of the named models, synthetic
+data of the stated distributions):
+  0  single Q4_K GEMV 4096 x 4096, M = 1
+  1  Llama-3-8B decode layer, M = 1: QKV 6144x4096, attn-out 4096x4096 (+res),
+     gate||up 28672x4096 (one q8_1 activation), down 4096x14336 (+res)   [default]
+  2  Q6_K output head 128256 x 4096, M = 1
+  3  config 1 + config 2 at M = 4
+  4  Qwen2-7B prefill MMQ at M = 2048: QKV 4608x3584, attn-out 3584x3584 (+res),
+     gate||up 37888x3584, down 3584x18944 (+res)
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
+graphs (programmatic dependent launch between the kernels), bracketed by a
+barrier and torch.cuda.synchronize(), timed with CUDA events on the launching
+stream.  Weight copies rotate between steps so the working set exceeds L2.
+`--impl reference` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "Q4_K/Q6_K GEMV weight GB/s (% of HBM peak); prefill MMQ int8 TOPS"
+L2_BYTES = 129 * 2 ** 20
+BYTES_PER_SB = {"q4k": 144, "q6k": 210}
+
+CONFIGS = {
+    0: dict(name="single Q4_K GEMV 4096x4096, batch 1", M=1, kind="gemv",
+            gemms=[("w", "q4k", 4096, 4096, False, "x")]),
+    1: dict(name="Llama-3-8B decode layer, batch 1 (Q4_K)", M=1, kind="gemv",
+            gemms=[(n, "q4k", N, K, r, s) for (n, N, K, r, s) in synth.LLAMA3_8B_LAYER]),
+    2: dict(name="Q6_K output head 128256x4096, batch 1", M=1, kind="gemv",
+            gemms=[("head", "q6k", 128256, 4096, False, "x_head")]),
+    3: dict(name="Llama-3-8B decode layer + Q6_K head, 4 sequences", M=4, kind="gemv",
+            gemms=[(n, "q4k", N, K, r, s) for (n, N, K, r, s) in synth.LLAMA3_8B_LAYER]
+            + [("head", "q6k", 128256, 4096, False, "x_head")]),
+    4: dict(name="Qwen2-7B prefill MMQ, 2048 tokens (Q4_K)", M=2048, kind="mmq",
+            gemms=[(n, "q4k", N, K, r, s) for (n, N, K, r, s) in synth.QWEN2_7B_PREFILL]),
+}
+
+
+def weight_bytes(cfg) -> int:
+    return sum(N * (K // 256) * BYTES_PER_SB[q] for (_, q, N, K, _, _) in cfg["gemms"])
+
+
+def int_ops(cfg) -> int:
+    return sum(2 * cfg["M"] * N * K for (_, _, N, K, _, _) in cfg["gemms"])
+
+
+def slots(cfg):
+    """activation slots in step order with their K"""
+    out = []
+    for (_, _, _, K, _, s) in cfg["gemms"]:
+        if s not in [a for a, _ in out]:
+            out.append((s, K))
+    return out
+
+
+# ------------------------------------------------------------------ workload
+
+class Workload:
+    """Device buffers for one configuration: repacked weights (several copies),
+    f32 activations and residuals, q8_1 buffers and outputs."""
+
+    def __init__(self, cfg_id: int, seed: int = 0, copies: int | None = None, device="cuda"):
+        import quantized_q8_activation_gb300 as qk
+        self.qk = qk
+        self.cfg_id = cfg_id
+        self.cfg = cfg = CONFIGS[cfg_id]
+        self.M = M = cfg["M"]
+        wb = weight_bytes(cfg)
+        if copies is None:
+            copies = max(1, -(-3 * L2_BYTES // wb))         # working set >= 3 x L2
+        self.copies = copies
+        self.host_w, self.w = {}, [dict() for _ in range(copies)]
+        for (name, q, N, K, _, _) in cfg["gemms"]:
+            hw = synth.weights(q, N, K, seed=seed, tag=name)
+            self.host_w[name] = hw
+            g = torch.from_numpy(hw).to(device)
+            for c in range(copies):
+                self.w[c][name] = qk.repack(qk.Q4_K if q == "q4k" else qk.Q6_K, g, N, K)
+            del g
+        self.host_x = {s: synth.activations(M, K, seed=seed, tag=s) for s, K in slots(cfg)}
+        self.x = {s: torch.from_numpy(v).to(device) for s, v in self.host_x.items()}
+        self.q8 = {s: qk.empty_q8_1(M, K, device) for s, K in slots(cfg)}
+        self.host_r, self.r, self.y = {}, {}, {}
+        for (name, _, N, _, res, _) in cfg["gemms"]:
+            if res:
+                self.host_r[name] = synth.residual(M, N, seed=seed, tag=name)
+                self.r[name] = torch.from_numpy(self.host_r[name]).to(device)
+            self.y[name] = torch.empty((M, N), dtype=torch.float32, device=device)
+        torch.cuda.synchronize()
+
+    def step(self, copy: int, pdl: bool = True, stream=None, events=None):
+        """Enqueue one step on `stream`.  With `events` (a list), every GEMV/MMQ
+        launch is bracketed by a pair of recorded CUDA events."""
+        qk, cfg = self.qk, self.cfg
+        done = set()
+        for (name, q, N, K, res, s) in cfg["gemms"]:
+            if s not in done:
+                codes, scales = self.q8[s]
+                qk.quantize_q8_1(self.x[s], codes, scales, pdl=pdl, stream=stream)
+                done.add(s)
+            codes, scales = self.q8[s]
+            fn = (qk.mmq_q4k if cfg["kind"] == "mmq" else qk.gemv_q4k if q == "q4k" else qk.gemv_q6k)
+            if events is not None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            fn(self.w[copy][name], codes, scales, N, K, residual=self.r.get(name), y=self.y[name],
+               pdl=pdl, stream=stream)
+            if events is not None:
+                e1.record(stream)
+                events.append((name, q, N, K, e0, e1))
+
+    def launches_per_step(self) -> int:
+        return len(slots(self.cfg)) + len(self.cfg["gemms"])
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.dev)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        else:
+            self.lines = []
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def barrier_max(value: float, ws: int, device):
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_step(cfg, host_w, host_x, host_r, threads: int, m_rows=None):
+    """One step of the workload on the CPU oracle (quantize + every contraction).
+    m_rows limits the activation rows (bounded sample for the prefill config)."""
+    import oracle
+    q8 = {}
+    for s, x in host_x.items():
+        xx = x if m_rows is None else x[:m_rows]
+        c, d, _ = oracle.quantize_q8_1(xx)
+        q8[s] = (c, d)
+    for (name, q, N, K, res, s) in cfg["gemms"]:
+        c, d = q8[s]
+        r = host_r.get(name)
+        if r is not None and m_rows is not None:
+            r = r[:m_rows]
+        oracle.gemm(oracle.Q4_K if q == "q4k" else oracle.Q6_K, host_w[name], N, K, c, d, residual=r,
+                    threads=threads)
+
+
+def cpu_baseline(wl_host, cfg, budget_s: float = 12.0):
+    """Time the oracle as it stands on the host cores; bounded sample."""
+    threads = os.cpu_count() or 1
+    host_w, host_x, host_r = wl_host
+    if cfg["kind"] == "mmq":
+        m_rows = 8                                      # 8 of the 2048 tokens per sample step
+        units = int_ops(cfg) * m_rows / cfg["M"]
+        unit, scale = "TOPS", 1e12
+        sample = f"{m_rows} of {cfg['M']} activation rows of every GEMM per step (quantize + contraction)"
+    else:
+        m_rows = None
+        units = weight_bytes(cfg)
+        unit, scale = "GB/s", 1e9
+        sample = "the full step (quantize + every contraction) per sample"
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_step(cfg, host_w, host_x, host_r, threads, m_rows)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s or n >= 50:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": units * n / dt / scale, "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"{n} x {sample}; {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------- main arms
+
+def run_reference(args, ws, rank):
+    """The oracle on the host cores, on our arm's config/metric/unit."""
+    if rank != 0:
+        return
+    cfg = CONFIGS[args.config]
+    host_w = {name: synth.weights(q, N, K, seed=0, tag=name) for (name, q, N, K, _, _) in cfg["gemms"]}
+    host_x = {s: synth.activations(cfg["M"], K, seed=0, tag=s) for s, K in slots(cfg)}
+    host_r = {name: synth.residual(cfg["M"], N, seed=0, tag=name) for (name, _, N, _, res, _) in cfg["gemms"] if res}
+    threads = os.cpu_count() or 1
+    m_rows = 8 if cfg["kind"] == "mmq" else None
+    for _ in range(args.warmup):
+        oracle_step(cfg, host_w, host_x, host_r, threads, m_rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(cfg, host_w, host_x, host_r, threads, m_rows)
+    dt = time.perf_counter() - t0
+    if cfg["kind"] == "mmq":
+        value = int_ops(cfg) * (m_rows / cfg["M"]) * args.steps / dt / 1e12
+        unit = "TOPS"
+        sample = f"{m_rows} of {cfg['M']} activation rows per step"
+    else:
+        value = weight_bytes(cfg) * args.steps / dt / 1e9
+        unit = "GB/s"
+        sample = "full step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg["name"], "M": cfg["M"]},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import quantized_q8_activation_gb300 as qk
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    qk.build()
+    qk.lib()
+    cfg = CONFIGS[args.config]
+    wl = Workload(args.config, seed=0, copies=args.copies)
+    stream = torch.cuda.Stream(device)
+    C = wl.copies
+    S = C * max(1, -(-args.graph_steps // C))        # steps per graph, a multiple of the copy count
+
+    def steps(n, start=0, events=None, pdl=True):
+        for i in range(n):
+            wl.step((start + i) % C, pdl=pdl, stream=stream, events=events)
+
+    # warm-up (also settles per-kernel attributes before any capture)
+    with torch.cuda.stream(stream):
+        steps(max(args.warmup, 1))
+    torch.cuda.synchronize()
+    g_main = capture(lambda: steps(S), stream)
+    rem = args.steps % S
+    g_rem = capture(lambda: steps(rem), stream) if rem else None
+    nrep = args.steps // S
+    g_main.replay()                                     # one untimed replay of the graph itself
+    torch.cuda.synchronize()
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(nrep):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    ms = barrier_max(ms, ws, device)
+    ms_step = ms / args.steps
+
+    # per-launch durations of the contraction kernels (events around each launch)
+    # (eager launches queued behind a GPU-side sleep, so the GPU runs them back to back)
+    evs = []
+    n_ev = min(S, 4 * C * max(1, 10 // C))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(200_000_000)
+        steps(n_ev, events=evs, pdl=False)
+    torch.cuda.synchronize()
+    per_kernel = {}
+    for (name, q, N, K, a, b) in evs:
+        key = "mmq_q4k" if cfg["kind"] == "mmq" else ("gemv_q4k" if q == "q4k" else "gemv_q6k")
+        d = per_kernel.setdefault(key, {"ms": 0.0, "n": 0, "bytes": 0, "ops": 0})
+        d["ms"] += a.elapsed_time(b)
+        d["n"] += 1
+        d["bytes"] += N * (K // 256) * BYTES_PER_SB[q]
+        d["ops"] += 2 * cfg["M"] * N * K
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
+    dk = per_kernel[dom]
+    hbm, bf16, peak_src = peaks()
+
+    if cfg["kind"] == "mmq":
+        units = int_ops(cfg)
+        value = units * ws / (ms_step * 1e-3) / 1e12
+        unit = "TOPS"
+        achieved = dk["ops"] / (dk["ms"] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                "frac": achieved / bf16, "traffic": None, "kernel": dom,
+                "peak_note": f"bf16 dense ({peak_src}); no int8 peak is measured on this part",
+                "avg_launch_us": dk["ms"] / dk["n"] * 1e3}
+    else:
+        units = weight_bytes(cfg)
+        value = units * ws / (ms_step * 1e-3) / 1e9
+        unit = "GB/s"
+        achieved = dk["bytes"] / (dk["ms"] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": None, "kernel": dom, "peak_note": f"hbm_gbs ({peak_src}, burst copy)",
+                "avg_launch_us": dk["ms"] / dk["n"] * 1e3}
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    h2d = {s: torch.from_numpy(v).pin_memory() for s, v in wl.host_x.items()}
+    h2r = {n: torch.from_numpy(v).pin_memory() for n, v in wl.host_r.items()}
+    d2h = {n: torch.empty(tuple(t.shape), dtype=torch.float32).pin_memory() for n, t in wl.y.items()}
+    h2d_bytes = sum(t.numel() * 4 for t in h2d.values()) + sum(t.numel() * 4 for t in h2r.values())
+    d2h_bytes = sum(t.numel() * 4 for t in d2h.values())
+
+    def e2e_step(i):
+        for s, t in h2d.items():
+            wl.x[s].copy_(t, non_blocking=True)
+        for n, t in h2r.items():
+            wl.r[n].copy_(t, non_blocking=True)
+        wl.step(i % C, pdl=True, stream=stream)
+        for n, t in d2h.items():
+            t.copy_(wl.y[n], non_blocking=True)
+
+    e2e_steps = min(args.steps, max(S, 200))
+    g_e2e = capture(lambda: [e2e_step(i) for i in range(S)], stream)
+    g_e2e.replay()
+    torch.cuda.synchronize()
+    reps = max(1, e2e_steps // S)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g_e2e.replay()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / (reps * S)
+    e2e_s = barrier_max(e2e_s, ws, device)
+    e2e_value = (units * ws / e2e_s / (1e12 if unit == "TOPS" else 1e9))
+
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic (seeded; distributions of the benchmark definition)",
+            "config": {"workload": cfg["name"], "config_id": args.config, "M": cfg["M"],
+                       "weight_bytes_per_step": weight_bytes(cfg), "int_ops_per_step": int_ops(cfg),
+                       "l2": f"inputs larger than L2: {C} rotating weight copies, "
+                             f"{C * weight_bytes(cfg) / 1e6:.0f} MB working set",
+                       "graph_steps": S, "pdl": True, "parallelism": f"replicas x{ws}"},
+            "hbm_frac": (value / ws) / hbm if unit == "GB/s" else None,
+            "roofline": roof,
+            "per_kernel": {k: {"launches": v["n"], "avg_us": v["ms"] / v["n"] * 1e3,
+                               "share": v["ms"] / sum(x["ms"] for x in per_kernel.values())}
+                           for k, v in per_kernel.items()},
+            "clocks": clk.summary(),
+            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d_bytes,
+                    "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": wl.launches_per_step() * args.steps}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline((wl.host_w, wl.host_x, wl.host_r), cfg, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default per config: about a second of GPU work)")
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, choices=sorted(CONFIGS))
+    ap.add_argument("--copies", type=int, default=None, help="weight copies rotated between steps")
+    ap.add_argument("--graph-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100}[args.config]
+    args.graph_steps = max(1, min(args.graph_steps, args.steps))
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank)
+        else:
+            run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

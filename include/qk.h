@@ -1,0 +1,199 @@
+/*
+ * qk.h -- C ABI of the GB300 (sm_103a) k-quant x q8_1 contraction library.
+ *
+ * The library computes the hot path of Q4_K_M LLM inference:
+ *   1. quantize f32 activations to q8_1 blocks          (qk_quantize_q8_1)
+ *   2. once, at load time, repack GGUF Q4_K / Q6_K weights into the device
+ *      layout below                                       (qk_repack)
+ *   3. y = x_q8 . W^T (+ r) for a few activation rows     (qk_gemv_q4k, qk_gemv_q6k)
+ *   4. the same for many rows (prefill)                   (qk_mmq_q4k)
+ * with y[m][n] = sum_k w[n][k] * xhat[m][k] (+ r[m][n]), xhat = d_a * q_a the
+ * dequantized q8_1 activation and w the dequantized weight.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must be device memory of the current
+ *    CUDA device (or managed memory); host pointers are never accepted in
+ *    their place.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ *  - The caller owns all memory.  No call allocates, frees or keeps a
+ *    pointer after it returns; every compute call is asynchronous on
+ *    `stream`.  The library keeps no per-call state.
+ *  - Arguments are validated on the host before anything is launched.  On
+ *    a validation error nothing is launched and a negative QK_E_* status is
+ *    returned.  QK_E_CUDA means a CUDA runtime call failed (the launch
+ *    itself, or a kernel attribute call); errors of earlier asynchronous
+ *    work on the stream can also surface there.
+ *  - Matrices are row-major.  N = output rows of W, K = reduction length,
+ *    M = activation rows (tokens).  K must be a positive multiple of 256.
+ *  - Floating point is IEEE: no fast-math; reductions run in a fixed order,
+ *    so results are identical from run to run on the same device.
+ */
+#ifndef QK_H
+#define QK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+#define QK_OK 0
+#define QK_E_NULL (-1)      /* a required pointer is NULL                     */
+#define QK_E_SHAPE (-2)     /* M, N or K out of range, or K % 256 != 0        */
+#define QK_E_ALIGN (-3)     /* a pointer or leading dimension is misaligned   */
+#define QK_E_ALIAS (-4)     /* an output overlaps an input it may not overlap */
+#define QK_E_TYPE (-5)      /* unknown quantization type                      */
+#define QK_E_WORKSPACE (-6) /* workspace too small                            */
+#define QK_E_CUDA (-7)      /* a CUDA runtime call failed                     */
+
+/* quantization types for qk_repacked_bytes / qk_repack */
+#define QK_TYPE_Q4_K 1
+#define QK_TYPE_Q6_K 2
+
+/* flags for the compute calls */
+#define QK_LAUNCH_PDL 1u
+/*
+ * QK_LAUNCH_PDL: launch with programmatic dependent launch, so the kernel
+ * can start while the previous kernel on the stream is still running.  The
+ * kernel waits for that kernel (and so for everything before it) to finish
+ * before it reads any activation, scale or residual or writes any output.
+ * A GEMV or MMQ launched this way may read its weight buffer `w` EARLY: the
+ * caller guarantees that no work still in flight on the stream writes `w`
+ * (e.g. qk_repack must have completed, or have been followed by another
+ * launch, before the first PDL launch that reads its output).  Without the
+ * flag every call is ordinary stream-ordered work.
+ */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int qk_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *qk_status_string(int status);
+
+/* ==================================================================== q8_1
+ * q8_1 activation blocks (leone-cuda "CUDA kernel design": each q8_1 block
+ * stores 32 signed codes, an f16 scale and an f16 source sum; minfer
+ * "15 . The CUDA backend" sec. 2.3 quantizes the activations once per
+ * matmul in a small prepass).
+ *
+ * Layout of a quantized M x K activation (two caller buffers):
+ *   codes:  int8   [M][K]      row-major, row stride K
+ *   scales: half2  [M][K/32]   (.x = d, .y = s) as IEEE binary16
+ * For block b of row m (values x[32b .. 32b+31]):
+ *   amax = max |x_i| (binary32), d = amax / 127 (binary32 division),
+ *   q_i  = roundf(x_i / d) in [-127, 127] (ties away from zero; 0 if d == 0),
+ *   s    = d * sum_i q_i (binary32),
+ *   stored d and s are binary16, round to nearest even, saturating at
+ *   +-65504.
+ */
+
+/* Sizes of the two q8_1 buffers for an M x K activation. */
+int qk_q8_1_bytes(int64_t M, int64_t K, size_t *codes_bytes, size_t *scales_bytes);
+
+/*
+ * x:      device, float [M][ldx], 16-byte aligned, ldx % 4 == 0, ldx >= K.
+ * codes:  device, int8 [M][K], 16-byte aligned.
+ * scales: device, half2 [M][K/32], 16-byte aligned.
+ * M >= 0 (0 launches nothing), K % 32 == 0 and K > 0.  Outputs must not
+ * overlap x.  Codes and scales match the definition above bit for bit.
+ */
+int qk_quantize_q8_1(const float *x, int64_t ldx, int64_t M, int64_t K,
+                     int8_t *codes, void *scales, unsigned flags, void *stream);
+
+/* ================================================================== repack
+ * Load-time lossless repack of GGUF k-quant weights into the device layout
+ * that the GEMV and MMQ kernels stream with aligned 16-byte loads (leone-cuda
+ * "CUDA kernel design" splits Q4_K codes from metadata; minfer "15 . The CUDA
+ * backend" sec. 3.2.2 pads Q6_K's 210-byte blocks for aligned loads -- this
+ * layout splits Q6_K into planes instead and adds no padding).
+ *
+ * GGUF input: row-major [N][K/256] superblocks;
+ *   Q4_K 144 B: f16 d, f16 dmin, 12 B packed 6-bit scales/mins, 128 B codes;
+ *   Q6_K 210 B: 128 B low 4 bits, 64 B high 2 bits, 16 int8 scales, f16 d.
+ * Output (B = K/256 superblocks per row, same total byte count):
+ *   Q4_K: codes plane [0, N*B*128): row n at n*B*128, cut into steps of up
+ *           to 8 superblocks at 1024*s; step s holds G = 4*nsb groups
+ *           (nsb = min(8, B-8s)); group u is code bytes 32g..32g+31 (g = u%4)
+ *           of superblock 8s+u/4, its first 16 bytes at 16u and its last 16
+ *           at 16G+16u.
+ *         meta plane [N*B*128, N*B*144): 16 B per superblock: d, dmin
+ *           (binary16, as in GGUF), then for g = 0..3 a 24-bit little-endian
+ *           record at bytes 4+3g: sc[2g] | sc[2g+1]<<6 | m[2g]<<12 | m[2g+1]<<18.
+ *   Q6_K: ql plane [0, N*B*128): row n at n*B*128, steps of up to 8
+ *           superblocks at 1024*s with L = 4*nsb lanes; lane u is superblock
+ *           8s+u/4 with p = u%4, h = p/2, e = p%2; GGUF ql[64h+16e ..+16] at
+ *           16u and ql[64h+32+16e ..+16] at 16L+16u.
+ *         qh plane [N*B*128, N*B*192): GGUF qh, 64 B per superblock.
+ *         scale plane [N*B*192, N*B*208): 16 B per superblock, byte 4p+t =
+ *           GGUF sc[8h + e + 2t] (p = 2h+e).
+ *         d plane [N*B*208, N*B*210): binary16 d per superblock.
+ */
+
+/* Bytes of the repacked weight (== GGUF bytes: N*K/256*144 or *210). */
+int qk_repacked_bytes(int qtype, int64_t N, int64_t K, size_t *bytes);
+
+/*
+ * gguf: device, GGUF superblocks as above, 16-byte aligned.
+ * dst:  device, qk_repacked_bytes() bytes, 16-byte aligned, must not
+ *       overlap gguf.  N >= 1, K % 256 == 0.  Never launched with PDL.
+ */
+int qk_repack(int qtype, const void *gguf, int64_t N, int64_t K, void *dst, void *stream);
+
+/* ==================================================================== GEMV
+ * Decode GEMV, M = 1..8 activation rows sharing one pass over the weight
+ * (minfer "15 . The CUDA backend" sec. 3.2.5 multi-token MMVQ; cajeta.dev
+ * "xpu walkthrough" sec. 4.2 batched Cols kernels: one pass over a weight
+ * row serves every sequence).  The integer dot of each 32-value q8_1 block
+ * with the weight codes is exact; the weight scales (d*sc, dmin*m for Q4_K,
+ * d*sc for Q6_K) and the activation scale are applied in binary32 per
+ * 32-value block (per 16-value block for Q6_K), the Q4_K min term using the
+ * exact integer sum of the block's codes (leone-cuda "CUDA kernel design":
+ * the minimum correction comes from the same codes).  Per-lane partial sums
+ * are combined by a fixed shuffle tree.
+ *
+ * w:        device, qk_repack() output for this qtype, 16-byte aligned.
+ * codes:    device, int8 [M][K] q8_1 codes, 16-byte aligned.
+ * scales:   device, half2 [M][K/32] q8_1 (d, s), 16-byte aligned (only d
+ *           is read).
+ * residual: device float [M][N] or NULL; may be equal to y (in-place
+ *           accumulate: y += W x).  Added in binary32 when the row is written
+ *           (leone-cuda "CUDA kernel design": the GEMV can add a residual as
+ *           it writes an output row).
+ * y:        device float [M][N], 4-byte aligned; must not overlap w, codes,
+ *           scales, or residual unless residual == y.
+ * Ranges: 1 <= M <= 8, 1 <= N <= 2^31-1, K % 256 == 0, 256 <= K and
+ * M*K <= 163840 (the q8_1 activation is staged in shared memory).
+ */
+int qk_gemv_q4k(const void *w, const int8_t *codes, const void *scales,
+                int64_t M, int64_t N, int64_t K,
+                const float *residual, float *y, unsigned flags, void *stream);
+
+int qk_gemv_q6k(const void *w, const int8_t *codes, const void *scales,
+                int64_t M, int64_t N, int64_t K,
+                const float *residual, float *y, unsigned flags, void *stream);
+
+/* ===================================================================== MMQ
+ * Prefill contraction of many activation rows with a Q4_K weight: quantized
+ * weight bytes go straight to tensor-core MMA with integer-exact operands,
+ * and the float scales are folded outside the integer accumulation (minfer
+ * "15 . The CUDA backend" sec. 2.3 and 3.2.6).
+ *
+ * w, codes, scales, residual, y: as for qk_gemv_q4k.
+ * Ranges: M >= 1, N >= 1, K % 256 == 0, K >= 256.  (M == 0 is a no-op.)
+ * workspace: device scratch of qk_mmq_workspace_bytes() bytes, 256-byte
+ *   aligned, or NULL when that size is 0.  Not read before written.
+ */
+int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
+
+int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales,
+               int64_t M, int64_t N, int64_t K,
+               const float *residual, float *y,
+               void *workspace, size_t workspace_bytes,
+               unsigned flags, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QK_H */

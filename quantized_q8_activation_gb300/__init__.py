@@ -1,0 +1,207 @@
+"""Python binding of the GB300 k-quant x q8_1 contraction library (libqk.so).
+
+Argument marshalling only: every computation runs in the CUDA kernels behind
+the C ABI declared in include/qk.h.  PyTorch provides device memory and
+streams.  There is no CPU fallback: if the shared library is missing or a
+call fails, an exception is raised.
+
+Typical use::
+
+    import quantized_q8_activation_gb300 as qk
+    w = qk.repack(qk.Q4_K, gguf_bytes_on_device, N, K)      # once, at load
+    codes, scales = qk.quantize_q8_1(x)                      # x: float32 [M][K] on cuda
+    y = qk.gemv_q4k(w, codes, scales, N, K, residual=r)      # M <= 8
+    y = qk.mmq_q4k(w, codes, scales, N, K)                   # any M
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+Q4_K = 1
+Q6_K = 2
+LAUNCH_PDL = 1
+
+QK_OK = 0
+STATUS = {0: "QK_OK", -1: "QK_E_NULL", -2: "QK_E_SHAPE", -3: "QK_E_ALIGN", -4: "QK_E_ALIAS",
+          -5: "QK_E_TYPE", -6: "QK_E_WORKSPACE", -7: "QK_E_CUDA"}
+
+# every symbol include/qk.h declares
+EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1", "qk_repacked_bytes",
+           "qk_repack", "qk_gemv_q4k", "qk_gemv_q6k", "qk_mmq_workspace_bytes", "qk_mmq_q4k"]
+
+_lib = None
+_lock = threading.Lock()
+
+
+class QKError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def build(force: bool = False) -> str:
+    """Compile libqk.so for sm_103a (nvcc)."""
+    return _build.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libqk.so not built ({path}); call quantized_q8_activation_gb300.build()")
+            L = ctypes.CDLL(path)
+            i64, p, u = ctypes.c_int64, ctypes.c_void_p, ctypes.c_uint
+            szp = ctypes.POINTER(ctypes.c_size_t)
+            L.qk_version.restype = ctypes.c_int
+            L.qk_status_string.argtypes = [ctypes.c_int]
+            L.qk_status_string.restype = ctypes.c_char_p
+            L.qk_q8_1_bytes.argtypes = [i64, i64, szp, szp]
+            L.qk_quantize_q8_1.argtypes = [p, i64, i64, i64, p, p, u, p]
+            L.qk_repacked_bytes.argtypes = [ctypes.c_int, i64, i64, szp]
+            L.qk_repack.argtypes = [ctypes.c_int, p, i64, i64, p, p]
+            L.qk_gemv_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
+            L.qk_gemv_q6k.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
+            L.qk_mmq_workspace_bytes.argtypes = [i64, i64, i64, szp]
+            L.qk_mmq_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
+            for name in EXPORTS:
+                getattr(L, name).restype = ctypes.c_int if name != "qk_status_string" else ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().qk_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != QK_OK:
+        raise QKError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _p(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _cuda(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ------------------------------------------------------------------- sizes
+
+def q8_1_bytes(M: int, K: int) -> tuple[int, int]:
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().qk_q8_1_bytes(M, K, ctypes.byref(c), ctypes.byref(s)), "qk_q8_1_bytes")
+    return c.value, s.value
+
+
+def repacked_bytes(qtype: int, N: int, K: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().qk_repacked_bytes(qtype, N, K, ctypes.byref(b)), "qk_repacked_bytes")
+    return b.value
+
+
+def mmq_workspace_bytes(M: int, N: int, K: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().qk_mmq_workspace_bytes(M, N, K, ctypes.byref(b)), "qk_mmq_workspace_bytes")
+    return b.value
+
+
+# --------------------------------------------------------------- operations
+
+def empty_q8_1(M: int, K: int, device="cuda"):
+    """Uninitialised q8_1 buffers: codes int8 [M][K], scales float16 [M][K/32][2] (d, s)."""
+    return (torch.empty((M, K), dtype=torch.int8, device=device),
+            torch.empty((M, K // 32, 2), dtype=torch.float16, device=device))
+
+
+def quantize_q8_1(x: torch.Tensor, codes=None, scales=None, pdl: bool = False, stream=None):
+    """x: float32 [M][K] (rows may be strided) -> (codes, scales)."""
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    if x.dtype != torch.float32 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("x must be a float32 CUDA tensor with unit stride along K")
+    M, K = x.shape
+    if codes is None or scales is None:
+        codes, scales = empty_q8_1(M, K, x.device)
+    _cuda(codes, "codes"), _cuda(scales, "scales")
+    st = lib().qk_quantize_q8_1(x.data_ptr(), x.stride(0) if M > 1 else K, M, K, codes.data_ptr(),
+                                scales.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
+    _check(st, "qk_quantize_q8_1")
+    return codes, scales
+
+
+def repack(qtype: int, gguf: torch.Tensor, N: int, K: int, out=None, stream=None) -> torch.Tensor:
+    """GGUF superblocks (uint8 CUDA tensor) -> repacked device weight (uint8)."""
+    _cuda(gguf, "gguf")
+    nbytes = repacked_bytes(qtype, N, K)
+    if gguf.numel() * gguf.element_size() < nbytes:
+        raise ValueError("gguf buffer smaller than N*K/256 superblocks")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=gguf.device)
+    _cuda(out, "out")
+    _check(lib().qk_repack(qtype, gguf.data_ptr(), N, K, out.data_ptr(), _stream(stream)), "qk_repack")
+    return out
+
+
+def _gemv(fn, name, w, codes, scales, N, K, residual, y, pdl, stream):
+    M = codes.shape[0]
+    for t, n in ((w, "w"), (codes, "codes"), (scales, "scales")):
+        _cuda(t, n)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=codes.device)
+    _cuda(y, "y")
+    if residual is not None:
+        _cuda(residual, "residual")
+    st = fn(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
+            LAUNCH_PDL if pdl else 0, _stream(stream))
+    _check(st, name)
+    return y
+
+
+def gemv_q4k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
+    """y[M][N] = xhat . W^T (+ residual) over a repacked Q4_K weight, 1 <= M <= 8."""
+    return _gemv(lib().qk_gemv_q4k, "qk_gemv_q4k", w, codes, scales, N, K, residual, y, pdl, stream)
+
+
+def gemv_q6k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
+    """y[M][N] = xhat . W^T (+ residual) over a repacked Q6_K weight, 1 <= M <= 8."""
+    return _gemv(lib().qk_gemv_q6k, "qk_gemv_q6k", w, codes, scales, N, K, residual, y, pdl, stream)
+
+
+def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None):
+    """Prefill contraction over a repacked Q4_K weight, any M."""
+    M = codes.shape[0]
+    for t, n in ((w, "w"), (codes, "codes"), (scales, "scales")):
+        _cuda(t, n)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=codes.device)
+    need = mmq_workspace_bytes(M, N, K)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=codes.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().qk_mmq_q4k(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
+                          _p(workspace), wsb, LAUNCH_PDL if pdl else 0, _stream(stream))
+    _check(st, "qk_mmq_q4k")
+    return y

@@ -1,0 +1,91 @@
+// qk_quantize.cu -- f32 activations -> q8_1 blocks.
+//
+// Method: leone-cuda "CUDA kernel design" (a q8_1 block holds 32 signed
+// codes, an f16 scale and an f16 source sum; the activation is quantized once
+// per GEMV input) with d = amax/127 and s = d*sum(q).  Each lane handles four
+// consecutive values (one 16-byte load), eight lanes one 32-value block; the
+// block max and the integer code sum are exact 8-lane shuffle reductions.
+// HBM-bound: 4 bytes read and 1.125 bytes written per value.
+#include "qk_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;              // 32 q8_1 blocks per CTA
+
+__global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(const float *__restrict__ x, int64_t ldx,
+                                                                 int64_t nblocks, int nb_row,
+                                                                 int8_t *__restrict__ codes,
+                                                                 __half2 *__restrict__ scales, int64_t K)
+{
+    qk::pdl_wait();                         // x may come from the previous kernel
+    qk::pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t blk = (int64_t)blockIdx.x * (kThreads / 8) + (threadIdx.x >> 3);   // q8_1 block id
+    const bool live = blk < nblocks;
+    const int64_t m = live ? blk / nb_row : 0;
+    const int b = live ? (int)(blk - m * nb_row) : 0;
+    const int sub = lane & 7;               // lane within the block's 8-lane group
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live) v = *reinterpret_cast<const float4 *>(x + m * ldx + 32 * b + 4 * sub);
+
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+
+    const float d = __fdiv_rn(amax, 127.0f);
+    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+    if (d > 0.0f) {
+        q0 = (int)roundf(__fdiv_rn(v.x, d));
+        q1 = (int)roundf(__fdiv_rn(v.y, d));
+        q2 = (int)roundf(__fdiv_rn(v.z, d));
+        q3 = (int)roundf(__fdiv_rn(v.w, d));
+    }
+    int sum = q0 + q1 + q2 + q3;
+    sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+
+    if (live) {
+        const uint32_t packed = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
+                                ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
+        *reinterpret_cast<uint32_t *>(codes + m * K + 32 * b + 4 * sub) = packed;
+        if (sub == 0) {
+            const float s = __fmul_rn(d, (float)sum);
+            scales[blk] = __halves2half2(qk::f16_sat(d), qk::f16_sat(s));
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" int qk_q8_1_bytes(int64_t M, int64_t K, size_t *codes_bytes, size_t *scales_bytes)
+{
+    if (!codes_bytes || !scales_bytes) return QK_E_NULL;
+    if (M < 0 || K <= 0 || K % 32 != 0) return QK_E_SHAPE;
+    *codes_bytes = (size_t)M * (size_t)K;
+    *scales_bytes = (size_t)M * (size_t)(K / 32) * 4;
+    return QK_OK;
+}
+
+extern "C" int qk_quantize_q8_1(const float *x, int64_t ldx, int64_t M, int64_t K, int8_t *codes,
+                                void *scales, unsigned flags, void *stream)
+{
+    if (M < 0 || K <= 0 || K % 32 != 0 || ldx < K || K > (int64_t)1 << 30) return QK_E_SHAPE;
+    if (M == 0) return QK_OK;
+    if (!x || !codes || !scales) return QK_E_NULL;
+    if (!qk::aligned(x, 16) || ldx % 4 != 0 || !qk::aligned(codes, 16) || !qk::aligned(scales, 16))
+        return QK_E_ALIGN;
+    const size_t xbytes = ((size_t)(M - 1) * (size_t)ldx + (size_t)K) * 4;
+    const size_t cbytes = (size_t)M * (size_t)K, sbytes = (size_t)M * (size_t)(K / 32) * 4;
+    if (qk::overlaps(x, xbytes, codes, cbytes) || qk::overlaps(x, xbytes, scales, sbytes) ||
+        qk::overlaps(codes, cbytes, scales, sbytes))
+        return QK_E_ALIAS;
+    const int nb_row = (int)(K / 32);
+    const int64_t nblocks = M * nb_row;
+    const int64_t grid = (nblocks + kThreads / 8 - 1) / (kThreads / 8);
+    if (grid > 0x7fffffffLL) return QK_E_SHAPE;
+    return qk::launch(quantize_q8_1_kernel, dim3((unsigned)grid), dim3(kThreads), 0, (cudaStream_t)stream,
+                      (flags & QK_LAUNCH_PDL) != 0, x, ldx, nblocks, nb_row, codes,
+                      reinterpret_cast<__half2 *>(scales), K);
+}

@@ -1,0 +1,118 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library must load, export every function include/qk.h declares, and
+reject bad arguments on the host with the documented status codes before
+anything is launched.  No call here reaches a CUDA launch: fake device
+pointers are only compared and never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_q8_activation_gb300 as qk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qk.h")
+
+P = 0x7F0000000000          # fake, 256-byte aligned device addresses
+E_NULL, E_SHAPE, E_ALIGN, E_ALIAS, E_TYPE = -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def L():
+    qk.build()
+    return qk.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qk_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(qk.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    assert L.qk_version() >= 100
+    for st in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert len(qk.status_string(st)) > 0
+    assert qk.status_string(-99) == "unknown status"
+
+
+def test_sizes(L):
+    assert qk.q8_1_bytes(4, 4096) == (4 * 4096, 4 * 128 * 4)
+    assert qk.repacked_bytes(qk.Q4_K, 4096, 4096) == 4096 * 16 * 144
+    assert qk.repacked_bytes(qk.Q6_K, 128256, 4096) == 430940160
+    with pytest.raises(qk.QKError):
+        qk.repacked_bytes(qk.Q4_K, 10, 100)
+    with pytest.raises(qk.QKError):
+        qk.repacked_bytes(7, 10, 256)
+    assert qk.mmq_workspace_bytes(2048, 4608, 3584) >= 0
+
+
+def call_gemv(L, fn, w=P, codes=P + 0x10000000, scales=P + 0x20000000, M=1, N=64, K=256, r=None,
+              y=P + 0x30000000):
+    return getattr(L, fn)(w, codes, scales, M, N, K, r, y, 0, None)
+
+
+@pytest.mark.parametrize("fn", ["qk_gemv_q4k", "qk_gemv_q6k"])
+def test_gemv_rejects(L, fn):
+    assert call_gemv(L, fn, w=None) == E_NULL
+    assert call_gemv(L, fn, y=None) == E_NULL
+    assert call_gemv(L, fn, K=100) == E_SHAPE
+    assert call_gemv(L, fn, K=0) == E_SHAPE
+    assert call_gemv(L, fn, M=0) == E_SHAPE
+    assert call_gemv(L, fn, M=9) == E_SHAPE
+    assert call_gemv(L, fn, N=0) == E_SHAPE
+    assert call_gemv(L, fn, M=8, K=256 * 81) == E_SHAPE           # activation too large for shared memory
+    assert call_gemv(L, fn, w=P + 8) == E_ALIGN
+    assert call_gemv(L, fn, codes=P + 0x10000004) == E_ALIGN
+    assert call_gemv(L, fn, y=P + 0x30000002) == E_ALIGN
+    assert call_gemv(L, fn, y=P + 64) == E_ALIAS                   # y inside the weight
+    assert call_gemv(L, fn, r=P + 0x30000000 + 4) == E_ALIAS       # residual partially overlaps y
+
+
+def test_quantize_rejects(L):
+    f = L.qk_quantize_q8_1
+    x, c, s = P, P + 0x10000000, P + 0x20000000
+    assert f(x, 256, 1, 100, c, s, 0, None) == E_SHAPE
+    assert f(x, 128, 1, 256, c, s, 0, None) == E_SHAPE             # ldx < K
+    assert f(x, 256, 0, 256, c, s, 0, None) == 0                   # M = 0: nothing to do
+    assert f(None, 256, 1, 256, c, s, 0, None) == E_NULL
+    assert f(x + 4, 256, 1, 256, c, s, 0, None) == E_ALIGN
+    assert f(x, 258, 2, 256, c, s, 0, None) == E_ALIGN             # ldx % 4 != 0
+    assert f(x, 256, 1, 256, x + 512, s, 0, None) == E_ALIAS       # codes inside x
+
+
+def test_repack_rejects(L):
+    f = L.qk_repack
+    assert f(3, P, 4, 256, P + 0x10000000, None) == E_TYPE
+    assert f(qk.Q4_K, P, 4, 300, P + 0x10000000, None) == E_SHAPE
+    assert f(qk.Q4_K, None, 4, 256, P + 0x10000000, None) == E_NULL
+    assert f(qk.Q6_K, P + 2, 4, 256, P + 0x10000000, None) == E_ALIGN
+    assert f(qk.Q4_K, P, 4, 256, P + 144, None) == E_ALIAS
+
+
+def test_mmq_rejects(L):
+    f = L.qk_mmq_q4k
+    w, c, s, y = P, P + 0x10000000, P + 0x20000000, P + 0x30000000
+    assert f(w, c, s, 0, 64, 256, None, y, None, 0, 0, None) == 0   # M = 0: nothing to do
+    assert f(w, c, s, 16, 64, 320, None, y, None, 0, 0, None) == E_SHAPE
+    assert f(None, c, s, 16, 64, 256, None, y, None, 0, 0, None) == E_NULL
+    assert f(w, c + 1, s, 16, 64, 256, None, y, None, 0, 0, None) == E_ALIGN
+    assert f(w, c, s, 16, 64, 256, None, c, None, 0, 0, None) == E_ALIAS
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    with pytest.raises(ValueError):
+        qk.quantize_q8_1(torch.zeros(1, 256))

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars (set by the method's definition):
+  - q8_1 codes and binary16 scales: bit for bit.
+  - device weight layout: byte for byte against the oracle's statement of it.
+  - GEMV / MMQ outputs: |y_gpu - y_ref| <= 1e-4 * sum_k |w * xhat| per
+    output, plus 2^-22 * |r| for the binary32 residual add.
+Shapes span several tiles and ragged tails (rows, superblock steps, M).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+qk = None
+QT = {"q4k": (1, oracle.Q4_K), "q6k": (2, oracle.Q6_K)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    global qk
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_q8_activation_gb300 as m
+    m.build()
+    m.lib()
+    qk = m
+    yield
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def weights(qt, N, K, seed):
+    w = synth.weights(qt, N, K, seed=seed)
+    return w, qk.repack(QT[qt][0], dev(w), N, K)
+
+
+def q8(x_np):
+    codes, scales = qk.quantize_q8_1(dev(x_np))
+    return codes, scales
+
+
+def q8_host(codes, scales):
+    c = codes.cpu().numpy()
+    d = scales.cpu().numpy()[:, :, 0].view(np.uint16).copy()
+    return c, d
+
+
+def check(y_gpu, y_ref, ab, r=None, what=""):
+    y_gpu = np.asarray(y_gpu, np.float64)
+    tol = 1e-4 * ab
+    if r is not None:
+        tol = tol + 2.0 ** -22 * np.abs(np.asarray(r, np.float64))
+    err = np.abs(y_gpu - y_ref)
+    bad = err > tol
+    assert not bad.any(), f"{what}: {bad.sum()} outputs out of bound; worst err/tol " \
+                          f"{np.max(err / np.maximum(tol, 1e-300)):.3g}"
+
+
+# ---------------------------------------------------------------------- q8_1
+
+@pytest.mark.parametrize("M,K", [(1, 256), (1, 4096), (3, 4096), (2, 14336), (4, 3584), (7, 32 * 13)])
+def test_quantize_bitexact(M, K):
+    x = synth.activations(M, K, seed=M + K) * np.float32(3.0)
+    x[0, :32] = 0.0                                  # an all-zero block
+    x[-1, 32:64] = np.float32(1e-30)                 # tiny values (subnormal scale)
+    if K >= 128:
+        x[0, 64:96] = np.float32(7.25)               # constant block
+    codes, scales = q8(x)
+    c_ref, d_ref, s_ref = oracle.quantize_q8_1(x)
+    c, sc = codes.cpu().numpy(), scales.cpu().numpy().view(np.uint16)
+    assert np.array_equal(c, c_ref)
+    assert np.array_equal(sc[:, :, 0], d_ref)
+    assert np.array_equal(sc[:, :, 1], s_ref)
+
+
+def test_quantize_golden_ties_and_strided_rows():
+    x = np.zeros((2, 64), np.float32)
+    x[0, :8] = [127.0, -63.5, 0.5, -0.5, 1.5, 2.5, -2.5, 63.49]
+    x[1, :] = 0.3
+    big = np.zeros((2, 96), np.float32)
+    big[:, :64] = x                                   # rows with stride 96
+    xt = dev(big)[:, :64]
+    codes, scales = qk.quantize_q8_1(xt)
+    c_ref, d_ref, s_ref = oracle.quantize_q8_1(x)
+    assert codes.cpu().numpy()[0, :8].tolist() == [127, -64, 1, -1, 2, 3, -3, 63]
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    sc = scales.cpu().numpy().view(np.uint16)
+    assert np.array_equal(sc[:, :, 0], d_ref) and np.array_equal(sc[:, :, 1], s_ref)
+    assert int(sc[1, 0, 0]) == 0x18D6 and int(sc[1, 0, 1]) == 0x48CD
+
+
+def test_quantize_saturates_large_blocks():
+    x = np.full((1, 32), 1.0e7, np.float32)
+    codes, scales = q8(x)
+    c_ref, d_ref, s_ref = oracle.quantize_q8_1(x)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    sc = scales.cpu().numpy().view(np.uint16)
+    assert int(sc[0, 0, 0]) == int(d_ref[0, 0]) == 0x7BFF
+    assert int(sc[0, 0, 1]) == int(s_ref[0, 0]) == 0x7BFF
+
+
+# -------------------------------------------------------------------- repack
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+@pytest.mark.parametrize("N,K", [(1, 256), (3, 2304), (5, 4096), (2, 256 * 17), (9, 256 * 8)])
+def test_repack_bitexact(qt, N, K):
+    w, wr = weights(qt, N, K, seed=N * 7 + K)
+    assert np.array_equal(wr.cpu().numpy(), oracle.repack(QT[qt][1], w, N, K))
+
+
+# ---------------------------------------------------------------------- GEMV
+
+def gemv(qt, *a, **kw):
+    return (qk.gemv_q4k if qt == "q4k" else qk.gemv_q6k)(*a, **kw)
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("N,K", [(1, 256), (37, 2304), (300, 4096), (130, 256 * 11)])
+def test_gemv_parity(qt, M, N, K):
+    w, wr = weights(qt, N, K, seed=M + N + K)
+    x = synth.activations(M, K, seed=N)
+    codes, scales = q8(x)
+    c, d = q8_host(codes, scales)
+    y = gemv(qt, wr, codes, scales, N, K).cpu().numpy()
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+    check(y, y_ref, ab, what=f"{qt} M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+@pytest.mark.parametrize("mode", ["separate", "inplace", "pdl"])
+def test_gemv_residual(qt, mode):
+    M, N, K = 4, 515, 4096
+    w, wr = weights(qt, N, K, seed=11)
+    x = synth.activations(M, K, seed=12)
+    r = synth.residual(M, N, seed=13)
+    codes, scales = q8(x)
+    c, d = q8_host(codes, scales)
+    rt = dev(r)
+    if mode == "inplace":
+        y = gemv(qt, wr, codes, scales, N, K, residual=rt, y=rt)
+    else:
+        y = gemv(qt, wr, codes, scales, N, K, residual=rt, pdl=(mode == "pdl"))
+    torch.cuda.synchronize()
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d, residual=r)
+    check(y.cpu().numpy(), y_ref, ab, r, what=f"{qt} residual {mode}")
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+def test_gemv_edges(qt):
+    # zero activation gives the residual exactly; one-hot activation gives a scaled column
+    N, K = 33, 512
+    w, wr = weights(qt, N, K, seed=21)
+    r = synth.residual(1, N, seed=22)
+    codes, scales = q8(np.zeros((1, K), np.float32))
+    y = gemv(qt, wr, codes, scales, N, K, residual=dev(r)).cpu().numpy()
+    assert np.array_equal(y, r)
+    x = np.zeros((1, K), np.float32)
+    x[0, 300] = 2.0
+    codes, scales = q8(x)
+    c, d = q8_host(codes, scales)
+    y = gemv(qt, wr, codes, scales, N, K).cpu().numpy()
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+    check(y, y_ref, ab, what="one-hot")
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+def test_gemv_max_activation(qt):
+    M, K, N = 8, 20480, 40                      # M*K at the documented limit
+    w, wr = weights(qt, N, K, seed=31)
+    x = synth.activations(M, K, seed=32)
+    codes, scales = q8(x)
+    c, d = q8_host(codes, scales)
+    y = gemv(qt, wr, codes, scales, N, K).cpu().numpy()
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+    check(y, y_ref, ab, what="max M*K")
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+def test_gemv_deterministic_and_guard_band(qt):
+    M, N, K = 3, 1000, 4096
+    w, wr = weights(qt, N, K, seed=41)
+    codes, scales = q8(synth.activations(M, K, seed=42))
+    guard = torch.full((M * N + 1024,), 1234.5, dtype=torch.float32, device="cuda")
+    y1 = guard[:M * N].view(M, N)
+    gemv(qt, wr, codes, scales, N, K, y=y1)
+    y2 = gemv(qt, wr, codes, scales, N, K)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert torch.all(guard[M * N:] == 1234.5)
+
+
+# ----------------------------------------------------------------------- MMQ
+
+@pytest.mark.parametrize("M,N,K", [(1, 64, 256), (17, 130, 512), (64, 128, 2304), (130, 300, 4096),
+                                   (200, 77, 768), (65, 129, 256 * 9)])
+def test_mmq_parity(M, N, K):
+    w, wr = weights("q4k", N, K, seed=M * 3 + N + K)
+    x = synth.activations(M, K, seed=M)
+    codes, scales = q8(x)
+    c, d = q8_host(codes, scales)
+    y = qk.mmq_q4k(wr, codes, scales, N, K).cpu().numpy()
+    y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d)
+    check(y, y_ref, ab, what=f"mmq M={M} N={N} K={K}")
+
+
+def test_mmq_residual_inplace_deterministic():
+    M, N, K = 96, 200, 1024
+    w, wr = weights("q4k", N, K, seed=51)
+    codes, scales = q8(synth.activations(M, K, seed=52))
+    c, d = q8_host(codes, scales)
+    r = synth.residual(M, N, seed=53)
+    rt = dev(r)
+    y = qk.mmq_q4k(wr, codes, scales, N, K, residual=rt, y=rt)
+    y2 = qk.mmq_q4k(wr, codes, scales, N, K, residual=dev(r), pdl=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
+    y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d, residual=r)
+    check(y.cpu().numpy(), y_ref, ab, r, what="mmq residual")
