@@ -110,28 +110,38 @@ class Workload:
             self.y[name] = torch.empty((M, N), dtype=torch.float32, device=device)
         torch.cuda.synchronize()
 
-    def step(self, copy: int, pdl: bool = True, stream=None, events=None):
-        """Enqueue one step on `stream`.  With `events` (a list), every GEMV/MMQ
-        launch is bracketed by a pair of recorded CUDA events."""
+    def step(self, copy: int, pdl: bool = True, stream=None, events=None, fused: bool = True):
+        """Enqueue one step on `stream`.  Decode steps with `fused` quantize each
+        activation inside its GEMV (qk_gemv_*_f32); otherwise a q8_1 quantize
+        kernel runs once per activation before its consumers.  With `events`
+        (a list), every GEMV/MMQ launch is bracketed by recorded CUDA events."""
         qk, cfg = self.qk, self.cfg
+        fused = fused and cfg["kind"] == "gemv"
         done = set()
         for (name, q, N, K, res, s) in cfg["gemms"]:
-            if s not in done:
+            if not fused and s not in done:
                 codes, scales = self.q8[s]
                 qk.quantize_q8_1(self.x[s], codes, scales, pdl=pdl, stream=stream)
                 done.add(s)
             codes, scales = self.q8[s]
-            fn = (qk.mmq_q4k if cfg["kind"] == "mmq" else qk.gemv_q4k if q == "q4k" else qk.gemv_q6k)
             if events is not None:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-            fn(self.w[copy][name], codes, scales, N, K, residual=self.r.get(name), y=self.y[name],
-               pdl=pdl, stream=stream)
+            if fused:
+                fn = qk.gemv_q4k_f32 if q == "q4k" else qk.gemv_q6k_f32
+                fn(self.w[copy][name], self.x[s], N, K, residual=self.r.get(name), y=self.y[name],
+                   pdl=pdl, stream=stream)
+            else:
+                fn = qk.mmq_q4k if cfg["kind"] == "mmq" else qk.gemv_q4k if q == "q4k" else qk.gemv_q6k
+                fn(self.w[copy][name], codes, scales, N, K, residual=self.r.get(name), y=self.y[name],
+                   pdl=pdl, stream=stream)
             if events is not None:
                 e1.record(stream)
                 events.append((name, q, N, K, e0, e1))
 
-    def launches_per_step(self) -> int:
+    def launches_per_step(self, fused: bool = True) -> int:
+        if fused and self.cfg["kind"] == "gemv":
+            return len(self.cfg["gemms"])
         return len(slots(self.cfg)) + len(self.cfg["gemms"])
 
 
@@ -322,9 +332,11 @@ def run_ours(args, ws, rank, local):
     C = wl.copies
     S = C * max(1, -(-args.graph_steps // C))        # steps per graph, a multiple of the copy count
 
-    def steps(n, start=0, events=None, pdl=True):
+    fused = not args.unfused
+
+    def steps(n, start=0, events=None, pdl=True, fused=fused):
         for i in range(n):
-            wl.step((start + i) % C, pdl=pdl, stream=stream, events=events)
+            wl.step((start + i) % C, pdl=pdl, stream=stream, events=events, fused=fused)
 
     # warm-up (also settles per-kernel attributes before any capture)
     with torch.cuda.stream(stream):
@@ -354,6 +366,23 @@ def run_ours(args, ws, rank, local):
     ms = barrier_max(ms, ws, device)
     ms_step = ms / args.steps
 
+    # the other front end, for reference: same step with q8_1 quantize kernels (or fused, if --unfused)
+    alt_ms_step = None
+    if cfg["kind"] == "gemv":
+        g_alt = capture(lambda: steps(S, fused=not fused), stream)
+        g_alt.replay()
+        torch.cuda.synchronize()
+        reps = max(1, min(nrep, 50))
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a0.record(stream)
+            for _ in range(reps):
+                g_alt.replay()
+            a1.record(stream)
+        torch.cuda.synchronize()
+        alt_ms_step = a0.elapsed_time(a1) / (reps * S)
+        del g_alt
+
     # per-launch durations of the contraction kernels (events around each launch)
     # (eager launches queued behind a GPU-side sleep, so the GPU runs them back to back)
     evs = []
@@ -366,6 +395,8 @@ def run_ours(args, ws, rank, local):
     per_kernel = {}
     for (name, q, N, K, a, b) in evs:
         key = "mmq_q4k" if cfg["kind"] == "mmq" else ("gemv_q4k" if q == "q4k" else "gemv_q6k")
+        if cfg["kind"] == "gemv" and fused:
+            key += "_f32"
         d = per_kernel.setdefault(key, {"ms": 0.0, "n": 0, "bytes": 0, "ops": 0})
         d["ms"] += a.elapsed_time(b)
         d["n"] += 1
@@ -433,7 +464,10 @@ def run_ours(args, ws, rank, local):
                        "weight_bytes_per_step": weight_bytes(cfg), "int_ops_per_step": int_ops(cfg),
                        "l2": f"inputs larger than L2: {C} rotating weight copies, "
                              f"{C * weight_bytes(cfg) / 1e6:.0f} MB working set",
-                       "graph_steps": S, "pdl": True, "parallelism": f"replicas x{ws}"},
+                       "graph_steps": S, "pdl": True, "parallelism": f"replicas x{ws}",
+                       "front_end": ("q8_1 quantization inside each GEMV (qk_gemv_*_f32)" if fused and
+                                     cfg["kind"] == "gemv" else "qk_quantize_q8_1 kernel per activation")},
+            "alt_front_end_ms_per_step": alt_ms_step,
             "hbm_frac": (value / ws) / hbm if unit == "GB/s" else None,
             "roofline": roof,
             "per_kernel": {k: {"launches": v["n"], "avg_us": v["ms"] / v["n"] * 1e3,
@@ -442,7 +476,7 @@ def run_ours(args, ws, rank, local):
             "clocks": clk.summary(),
             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d_bytes,
                     "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_s * 1e3},
-            "gpu_launches": wl.launches_per_step() * args.steps}
+            "gpu_launches": wl.launches_per_step(fused) * args.steps}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline((wl.host_w, wl.host_x, wl.host_r), cfg, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -461,6 +495,8 @@ def main():
     ap.add_argument("--graph-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="decode: run the q8_1 quantize kernel before each GEMV instead of quantizing in the GEMV")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100}[args.config]

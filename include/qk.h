@@ -162,8 +162,9 @@ int qk_repack(int qtype, const void *gguf, int64_t N, int64_t K, void *dst, void
  *           it writes an output row).
  * y:        device float [M][N], 4-byte aligned; must not overlap w, codes,
  *           scales, or residual unless residual == y.
- * Ranges: 1 <= M <= 8, 1 <= N <= 2^31-1, K % 256 == 0, 256 <= K and
- * M*K <= 163840 (the q8_1 activation is staged in shared memory).
+ * Ranges: 1 <= M <= 8, 1 <= N <= 2^31-1, K % 256 == 0, 256 <= K, and
+ * M*K <= 81920 for Q4_K, M*K <= 40960 for Q6_K (the q8_1 activation is
+ * staged in shared memory next to the weight streaming buffers).
  */
 int qk_gemv_q4k(const void *w, const int8_t *codes, const void *scales,
                 int64_t M, int64_t N, int64_t K,
@@ -172,6 +173,32 @@ int qk_gemv_q4k(const void *w, const int8_t *codes, const void *scales,
 int qk_gemv_q6k(const void *w, const int8_t *codes, const void *scales,
                 int64_t M, int64_t N, int64_t K,
                 const float *residual, float *y, unsigned flags, void *stream);
+
+/*
+ * Same GEMVs with the q8_1 quantization of the activation done inside the
+ * kernel (every CTA quantizes x into shared memory with the same arithmetic
+ * as qk_quantize_q8_1, so the codes are bit-identical).  For decode, where an
+ * activation of a few thousand values feeds one GEMV, this removes the
+ * quantize kernel and its grid boundary from the chain (leone-cuda "CUDA
+ * kernel design" fuses the q8_1 pack into the producers of GEMV inputs for
+ * the same reason; here the consumer does it).
+ *
+ * x:          device float [M][ldx], 16-byte aligned, ldx % 4 == 0, ldx >= K.
+ * codes_out,  NULL, or device buffers laid out as qk_quantize_q8_1's outputs
+ * scales_out: (16-byte aligned) that receive the q8_1 codes and scales the
+ *             kernel computed; both NULL or both non-NULL.
+ * w, residual, y, M, N, K, flags: as for qk_gemv_q4k / qk_gemv_q6k.  y must
+ * not overlap x; codes_out / scales_out must not overlap any other argument.
+ */
+int qk_gemv_q4k_f32(const void *w, const float *x, int64_t ldx,
+                    int64_t M, int64_t N, int64_t K,
+                    const float *residual, float *y,
+                    int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
+
+int qk_gemv_q6k_f32(const void *w, const float *x, int64_t ldx,
+                    int64_t M, int64_t N, int64_t K,
+                    const float *residual, float *y,
+                    int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
 
 /* ===================================================================== MMQ
  * Prefill contraction of many activation rows with a Q4_K weight: quantized

@@ -33,7 +33,8 @@ STATUS = {0: "QK_OK", -1: "QK_E_NULL", -2: "QK_E_SHAPE", -3: "QK_E_ALIGN", -4: "
 
 # every symbol include/qk.h declares
 EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1", "qk_repacked_bytes",
-           "qk_repack", "qk_gemv_q4k", "qk_gemv_q6k", "qk_mmq_workspace_bytes", "qk_mmq_q4k"]
+           "qk_repack", "qk_gemv_q4k", "qk_gemv_q6k", "qk_gemv_q4k_f32", "qk_gemv_q6k_f32",
+           "qk_mmq_workspace_bytes", "qk_mmq_q4k"]
 
 _lib = None
 _lock = threading.Lock()
@@ -74,6 +75,8 @@ def lib() -> ctypes.CDLL:
             L.qk_repack.argtypes = [ctypes.c_int, p, i64, i64, p, p]
             L.qk_gemv_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
             L.qk_gemv_q6k.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
+            L.qk_gemv_q4k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
+            L.qk_gemv_q6k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
             L.qk_mmq_workspace_bytes.argtypes = [i64, i64, i64, szp]
             L.qk_mmq_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
             for name in EXPORTS:
@@ -188,6 +191,36 @@ def gemv_q4k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=No
 def gemv_q6k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
     """y[M][N] = xhat . W^T (+ residual) over a repacked Q6_K weight, 1 <= M <= 8."""
     return _gemv(lib().qk_gemv_q6k, "qk_gemv_q6k", w, codes, scales, N, K, residual, y, pdl, stream)
+
+
+def _gemv_f32(fn, name, w, x, N, K, residual, y, codes_out, scales_out, pdl, stream):
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    if x.dtype != torch.float32 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("x must be a float32 CUDA tensor with unit stride along K")
+    _cuda(w, "w")
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _cuda(y, "y")
+    if residual is not None:
+        _cuda(residual, "residual")
+    st = fn(w.data_ptr(), x.data_ptr(), x.stride(0) if M > 1 else K, M, N, K, _p(residual), y.data_ptr(),
+            _p(codes_out), _p(scales_out), LAUNCH_PDL if pdl else 0, _stream(stream))
+    _check(st, name)
+    return y
+
+
+def gemv_q4k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+    """GEMV over a repacked Q4_K weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
+    return _gemv_f32(lib().qk_gemv_q4k_f32, "qk_gemv_q4k_f32", w, x, N, K, residual, y, codes_out, scales_out,
+                     pdl, stream)
+
+
+def gemv_q6k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+    """GEMV over a repacked Q6_K weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
+    return _gemv_f32(lib().qk_gemv_q6k_f32, "qk_gemv_q6k_f32", w, x, N, K, residual, y, codes_out, scales_out,
+                     pdl, stream)
 
 
 def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None):

@@ -21,6 +21,22 @@ int sm_count()
     return n;
 }
 
+size_t max_smem_optin()
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 48 * 1024;
+    if (dev < 64) {
+        int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return (size_t)v;
+    }
+    int n = 48 * 1024;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || n < 1)
+        n = 48 * 1024;
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return (size_t)n;
+}
+
 }  // namespace qk
 
 extern "C" int qk_version(void) { return 100; }   // 0.1.0

@@ -50,6 +50,18 @@ inline int launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
 // Number of SMs of the current device (queried once per device id).
 int sm_count();
 
+// Largest dynamic shared memory a CTA may opt in to on the current device.
+size_t max_smem_optin();
+
+// Every kernel of the library asks for the same (maximal) shared-memory
+// carveout, so consecutive kernels never force an L1/shared reconfiguration.
+template <typename Kern>
+inline cudaError_t max_carveout(Kern kern)
+{
+    return cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared);
+}
+
 // ---------------------------------------------------------------- device side
 
 // Wait until the previous grid on the stream has completed and its memory
@@ -100,7 +112,62 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c)
     return d;
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only); `bytes` < 16 zero-fills the rest
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, int bytes = 16)
+{
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gsrc), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // binary32 -> binary16, round to nearest even, saturating at +-65504
 __device__ __forceinline__ __half f16_sat(float v) { return __float2half_rn(fminf(fmaxf(v, -65504.0f), 65504.0f)); }
+
+// roundf(x / d) for the q8_1 code of x, exactly as the IEEE quotient would
+// give it.  Fast path: t = x * r with r = RN(1/d) differs from x/d by at most
+// 2^-23 |x/d| <= 1.6e-5, and RN(x/d) from x/d by at most 7.7e-6 (|x/d| <= 127.5),
+// so unless t lies within 2^-15 of a half-integer both round to the same
+// integer; near a tie (or if 1/d overflowed) the quotient is computed with an
+// IEEE division.
+__device__ __forceinline__ int q81_code(float x, float d, float r)
+{
+    const float t = x * r;
+    const float a = fabsf(t);
+    const float fr = a - truncf(a);
+    if (fabsf(fr - 0.5f) > 3.0517578125e-05f && a < 128.0f) return (int)roundf(t);
+    return (int)roundf(__fdiv_rn(x, d));
+}
+
+// q8_1 quantization of one 32-value block held by 8 consecutive lanes (lane
+// group 8j..8j+7 of the warp, 4 values each, all 32 lanes participating):
+// d = amax/127 (binary32 division), q = roundf(x/d) (0 when d == 0).  Returns
+// this lane's 4 codes packed little-endian; d is the block's binary32 scale and
+// s4 the sum of this lane's 4 codes.  Used by the standalone quantizer and by
+// the GEMV kernels that quantize their activation themselves, so both produce
+// the same codes bit for bit.
+__device__ __forceinline__ uint32_t q81_quant8(float4 v, float &d, int &s4)
+{
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    d = __fdiv_rn(amax, 127.0f);
+    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+    if (d > 0.0f) {
+        const float r = __frcp_rn(d);
+        q0 = q81_code(v.x, d, r);
+        q1 = q81_code(v.y, d, r);
+        q2 = q81_code(v.z, d, r);
+        q3 = q81_code(v.w, d, r);
+    }
+    s4 = q0 + q1 + q2 + q3;
+    return (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) | ((uint32_t)(q2 & 0xff) << 16) |
+           ((uint32_t)(q3 & 0xff) << 24);
+}
+
+// stored binary16 s of a q8_1 block: s = d * sum(q) in binary32, then binary16
+__device__ __forceinline__ __half q81_sum_f16(float d, int sum) { return f16_sat(__fmul_rn(d, (float)sum)); }
 
 }  // namespace qk

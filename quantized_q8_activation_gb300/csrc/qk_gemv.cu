@@ -4,16 +4,24 @@
 // Design (GB300, HBM-bound):
 //  - Persistent grid, one CTA of 16 warps per SM.  Warp w of the grid owns
 //    output rows w, w + W, w + 2W, ... and walks each row in steps of up to
-//    8 superblocks; in a step every lane reads 16-byte chunks so a warp load
-//    covers 512 contiguous bytes of the repacked code plane (qk.h layout).
-//  - Weight loads for the next two steps are in flight while the current
-//    step is computed (ld.global.nc, L1 no-allocate).  With QK_LAUNCH_PDL the
-//    first two steps are issued before griddepcontrol.wait, so weight
-//    streaming overlaps the tail of the previous kernel.
+//    8 superblocks (an "item"); in an item every lane copies 16-byte chunks
+//    so a warp covers 512 contiguous bytes of the repacked code plane per
+//    copy instruction (qk.h layout).
+//  - Each warp streams its items through a private ring of R shared-memory
+//    slots with cp.async (L2 -> SMEM, no register cost), R-1 items in flight
+//    while one is computed; no block-wide barrier inside the loop.  With
+//    QK_LAUNCH_PDL the first R-1 items are issued before griddepcontrol.wait,
+//    so weight streaming overlaps the tail of the previous kernel, and the
+//    kernel lets its successor launch at entry.
 //  - The q8_1 activation (M x K codes) is staged once per CTA in shared
 //    memory with a 16-byte-chunk XOR swizzle that keeps the lanes' 16-byte
 //    reads conflict free; per 32-value block the CTA also stores d_a and the
-//    exact d_a * sum(q_a) (Q4_K) or the 16-value code sums (Q6_K).
+//    exact d_a * sum(q_a) (Q4_K) or per 16 values the -32 bias term (Q6_K).
+//    Two front ends: the q8_1 entry points copy caller-quantized codes; the
+//    _f32 entry points quantize the f32 activation in every CTA with the
+//    library's q8_1 block quantizer (bit-identical codes), which removes the
+//    quantize kernel and its grid boundary from the decode chain and lets
+//    consecutive GEMVs co-reside under programmatic dependent launch.
 //  - Integer dots with dp4a (int32, exact per block), weight scales decoded
 //    in registers, binary32 fold per 32-value (Q4_K) / 16-value (Q6_K)
 //    block, per-lane accumulators combined by a fixed xor-shuffle tree, the
@@ -29,321 +37,601 @@
 
 namespace {
 
-constexpr int kWarps = 16;
-constexpr int kThreads = kWarps * 32;
+// tile constants (compile-time; -D overrides exist for tuning sweeps)
+#ifndef QK_GEMV_WARPS
+#define QK_GEMV_WARPS 16              // warps per CTA for M > 2
+#endif
+#ifndef QK_GEMV_WARPS_SMALL_M
+#define QK_GEMV_WARPS_SMALL_M 16      // warps per CTA for M <= 2
+#endif
+#ifndef QK_GEMV_CTAS_PER_SM
+#define QK_GEMV_CTAS_PER_SM 1
+#endif
+#ifndef QK_GEMV_Q4_RING
+#define QK_GEMV_Q4_RING 3
+#endif
+#ifndef QK_GEMV_Q6_RING
+#define QK_GEMV_Q6_RING 3
+#endif
+// 0: allow the next kernel to launch at entry; 1: after the activation is staged; 2: at exit
+#ifndef QK_GEMV_TRIGGER
+#define QK_GEMV_TRIGGER 0
+#endif
+// warps and CTAs per SM of the f32-input (self-quantizing) kernels for M <= 2
+#ifndef QK_GEMV_WARPS_FUSED
+#define QK_GEMV_WARPS_FUSED 16
+#endif
+#ifndef QK_GEMV_MINB_FUSED
+#define QK_GEMV_MINB_FUSED 1
+#endif
+template <int M, bool FUSED>
+struct Cfg {
+    static constexpr int warps = M > 2 ? QK_GEMV_WARPS : FUSED ? QK_GEMV_WARPS_FUSED : QK_GEMV_WARPS_SMALL_M;
+    static constexpr int threads = warps * 32;
+    static constexpr int minb = (M <= 2 && FUSED) ? QK_GEMV_MINB_FUSED : 1;
+};
+constexpr int kCtasPerSm = QK_GEMV_CTAS_PER_SM;
+constexpr int kRowsPerItem = 2;                                     // rows a lane works on at once
+constexpr int Q4_R = QK_GEMV_Q4_RING, Q4_SLOT = kRowsPerItem * (1024 + 128);       // codes + 8 metadata records
+constexpr int Q6_R = QK_GEMV_Q6_RING, Q6_SLOT = kRowsPerItem * (1024 + 512 + 128); // ql + qh + scales
+static_assert(Q4_R >= 2 && Q6_R >= 2, "ring needs two slots at least");
 
-// 16-byte chunk c of an activation row lives at chunk position swz(c)
+// kernel arguments (one struct: the q8_1 and the f32 front ends share the kernels)
+struct GemvArgs {
+    const uint8_t *w;              // repacked weight
+    const int8_t *codes;           // q8_1 front end: codes [M][K]
+    const __half2 *scales;         //                 scales [M][K/32]
+    const float *x;                // f32 front end: activation [M][ldx]
+    int64_t ldx;
+    int8_t *codes_out;             //                optional copy of the codes it computed
+    __half2 *scales_out;           //                and of the scales
+    int64_t N;
+    int K;
+    const float *residual;
+    float *y;
+};
+
+// 16-byte chunk c of an activation row lives at chunk position swz(c); for
+// c = 128*s + c' (c' < 128), swz(c) = 128*s + swz(c')
 __device__ __forceinline__ int swz(int c) { return c ^ ((c >> 2) & 7); }
 
-__device__ __forceinline__ uint4 lds16(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+__device__ __forceinline__ uint4 lds16(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+__device__ __forceinline__ float f16lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu))); }
+__device__ __forceinline__ float f16hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+__device__ __forceinline__ int sum16(uint4 v)
+{
+    int s = qk::dp4a_ss(v.x, 0x01010101u, 0);
+    s = qk::dp4a_ss(v.y, 0x01010101u, s);
+    s = qk::dp4a_ss(v.z, 0x01010101u, s);
+    return qk::dp4a_ss(v.w, 0x01010101u, s);
+}
 
 // --------------------------------------------------------------- staging
+// One pass over the M x K codes in 16-byte chunks: copy to the swizzled
+// shared-memory image and reduce the chunk's code sum (exact, dp4a).
 
-// Q4_K side data per (m, 32-block): {d_a, d_a * sum(q_a)}; both exact in f32
-template <int M>
+// Q4_K side data per (m, 32-block): {d_a, d_a * sum(q_a)}; odd blocks are the
+// high-nibble sub-blocks whose codes the kernel reads as 16*q, so their d_a
+// is stored divided by 16 (exact).
+template <int M, int NT>
 __device__ void stage_act_q4k(const int8_t *__restrict__ codes, const __half2 *__restrict__ scales, int K,
                               uint8_t *s_codes, float2 *s_sc)
 {
-    const int nchunk = K >> 4;
-    for (int i = threadIdx.x; i < M * nchunk; i += kThreads) {
-        const int m = i / nchunk, c = i - m * nchunk;
-        const uint4 v = *reinterpret_cast<const uint4 *>(codes + (size_t)m * K + 16 * c);
-        *reinterpret_cast<uint4 *>(s_codes + (size_t)m * K + 16 * swz(c)) = v;
-    }
-    const int nb = K >> 5;
-    for (int i = threadIdx.x; i < M * nb; i += kThreads) {
-        const int m = i / nb, b = i - m * nb;
-        const uint4 *p = reinterpret_cast<const uint4 *>(codes + (size_t)m * K + 32 * b);
-        const uint4 a = p[0], c = p[1];
-        int s = 0;
-        s = qk::dp4a_ss(a.x, 0x01010101u, s), s = qk::dp4a_ss(a.y, 0x01010101u, s);
-        s = qk::dp4a_ss(a.z, 0x01010101u, s), s = qk::dp4a_ss(a.w, 0x01010101u, s);
-        s = qk::dp4a_ss(c.x, 0x01010101u, s), s = qk::dp4a_ss(c.y, 0x01010101u, s);
-        s = qk::dp4a_ss(c.z, 0x01010101u, s), s = qk::dp4a_ss(c.w, 0x01010101u, s);
-        const float d = __low2float(scales[(size_t)m * nb + b]);
-        s_sc[m * nb + b] = make_float2(d, d * (float)s);
+    const int nchunk = K >> 4, total = M * nchunk;        // total is even
+    for (int base = 0; base < total; base += NT) {
+        const int i = base + threadIdx.x;
+        const bool ok = i < total;
+        const int m = ok ? i / nchunk : 0, c = ok ? i - m * nchunk : 0;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (ok) {
+            v = *reinterpret_cast<const uint4 *>(codes + (size_t)m * K + 16 * c);
+            *reinterpret_cast<uint4 *>(s_codes + (size_t)m * K + 16 * swz(c)) = v;
+        }
+        int s = sum16(v);
+        s += __shfl_xor_sync(0xffffffffu, s, 1);           // the other half of the 32-value block
+        if (ok && (c & 1) == 0) {
+            const int b = c >> 1;
+            const float d = __low2float(scales[(size_t)m * (K >> 5) + b]);
+            s_sc[m * (K >> 5) + b] = make_float2((b & 1) ? d * 0.0625f : d, d * (float)s);
+        }
     }
 }
 
-// Q6_K side data: d_a per (m, 32-block) and 32 * sum(q_a) per (m, 16-block)
-template <int M>
+// Q6_K side data per (m, 16-value chunk): {d_a, -32 * d_a * sum(q_a)}, the
+// activation scale and the offset term of the weight codes' -32 bias (exact)
+template <int M, int NT>
 __device__ void stage_act_q6k(const int8_t *__restrict__ codes, const __half2 *__restrict__ scales, int K,
-                              uint8_t *s_codes, float *s_d, float *s_s16)
+                              uint8_t *s_codes, float2 *s_c16)
 {
     const int nchunk = K >> 4;
-    for (int i = threadIdx.x; i < M * nchunk; i += kThreads) {
+    for (int i = threadIdx.x; i < M * nchunk; i += NT) {
         const int m = i / nchunk, c = i - m * nchunk;
         const uint4 v = *reinterpret_cast<const uint4 *>(codes + (size_t)m * K + 16 * c);
         *reinterpret_cast<uint4 *>(s_codes + (size_t)m * K + 16 * swz(c)) = v;
-        int s = 0;
-        s = qk::dp4a_ss(v.x, 0x01010101u, s), s = qk::dp4a_ss(v.y, 0x01010101u, s);
-        s = qk::dp4a_ss(v.z, 0x01010101u, s), s = qk::dp4a_ss(v.w, 0x01010101u, s);
-        s_s16[i] = (float)(32 * s);
+        const float d = __low2float(scales[(size_t)m * (K >> 5) + (c >> 1)]);
+        s_c16[i] = make_float2(d, -32.0f * d * (float)sum16(v));
     }
+}
+
+// f32 front end: quantize the activation into the same shared-memory image
+// (Q6 selects the Q6_K side data).  8 lanes per 32-value block, 4 values per
+// lane; CTA 0 also writes the codes and scales out when asked to.
+template <int M, int NT, bool Q6>
+__device__ void stage_quant(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
+{
+    constexpr int U = 8;                                   // loads in flight per thread
+    const int K = a.K, k4n = K >> 2, total = M * k4n;      // total is a multiple of 8
     const int nb = K >> 5;
-    for (int i = threadIdx.x; i < M * nb; i += kThreads) s_d[i] = __low2float(scales[i]);
+    const bool out = a.codes_out != nullptr && blockIdx.x == 0;
+    for (int base = 0; base < total; base += NT * U) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int i = base + u * NT + threadIdx.x;
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < total) {
+                const int m = i / k4n, k4 = i - m * k4n;
+                v[u] = *reinterpret_cast<const float4 *>(a.x + m * a.ldx + 4 * k4);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int i = base + u * NT + threadIdx.x;
+            if (base + u * NT >= total) break;             // uniform: the whole batch row is past the end
+            const bool ok = i < total;
+            const int m = ok ? i / k4n : 0, k4 = ok ? i - m * k4n : 0;
+            float d;
+            int s4;
+            const uint32_t packed = qk::q81_quant8(v[u], d, s4);
+            int s16 = s4 + __shfl_xor_sync(0xffffffffu, s4, 1);
+            s16 += __shfl_xor_sync(0xffffffffu, s16, 2);                  // 16 values (4 lanes)
+            const int s32 = s16 + __shfl_xor_sync(0xffffffffu, s16, 4);   // the 32-value block
+            if (ok) {
+                const int c = k4 >> 2, sub = k4 & 7;
+                *reinterpret_cast<uint32_t *>(s_codes + (size_t)m * K + 16 * swz(c) + 4 * (k4 & 3)) = packed;
+                const __half dh = qk::f16_sat(d);
+                const float da = __half2float(dh);                         // the stored scale is what the dot uses
+                if (!Q6) {
+                    if (sub == 0) {
+                        const int b = k4 >> 3;
+                        s_side[m * nb + b] = make_float2((b & 1) ? da * 0.0625f : da, da * (float)s32);
+                    }
+                } else if ((sub & 3) == 0) {
+                    s_side[m * (K >> 4) + c] = make_float2(da, -32.0f * da * (float)s16);
+                }
+                if (out) {
+                    *reinterpret_cast<uint32_t *>(a.codes_out + (size_t)m * K + 4 * k4) = packed;
+                    if (sub == 0)
+                        a.scales_out[(size_t)m * nb + (k4 >> 3)] = __halves2half2(dh, qk::q81_sum_f16(d, s32));
+                }
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------ row reduce
 
-template <int M>
-__device__ __forceinline__ void finish_row(float (&acc)[M], int lane, int64_t n, int64_t N,
-                                           const float *__restrict__ residual, float *__restrict__ y)
+__device__ __forceinline__ float warp_sum(float v)
 {
-#pragma unroll
-    for (int m = 0; m < M; m++) {
-        float v = acc[m];
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        if (lane == m) {
-            const size_t o = (size_t)m * N + n;
-            y[o] = residual ? __fadd_rn(v, residual[o]) : v;
-        }
-        acc[m] = 0.0f;
-    }
+    v += __shfl_xor_sync(0xffffffffu, v, 16);              // fixed xor tree over the 32 lanes
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    return v;
 }
+
+// ------------------------------------------------------------ work split
+// Rows are taken in groups of P consecutive rows; an item is (group, step s),
+// the step-s bytes of the group's rows.  Bulk: while every warp of the grid
+// can get one, groups are dealt round robin over all W warps (warp w takes
+// groups w, w+W, ...), so at any time the grid streams one contiguous window
+// of the weight.  Tail: the remaining NG mod W groups are split into
+// contiguous ranges per CTA, and each CTA's tail items into equal (+-1)
+// contiguous ranges per warp.  A group whose steps all fall in one warp is
+// written directly; a tail group cut between warps leaves a partial per warp
+// in shared memory, combined in warp order when the CTA is done.
+struct ItemSeq {
+    int64_t g;                     // current item: group g, step s
+    int s;
+    int64_t bulk_left;             // bulk items left, the current one included
+    int64_t tail_g;                // first tail item of this warp
+    int tail_s;
+    int64_t W;
+    __device__ __forceinline__ void next(int nsteps)
+    {
+        if (bulk_left > 0) {
+            if (++s == nsteps) s = 0, g += W;
+            if (--bulk_left == 0) g = tail_g, s = tail_s;
+        } else if (++s == nsteps) {
+            s = 0, ++g;
+        }
+    }
+};
+
+constexpr int P = kRowsPerItem;
+constexpr int kMaxM = 8;
+
+struct Part {                                              // per warp: up to two partial groups
+    float v[2][P][kMaxM];
+    long long g[2];
+};
 
 // ------------------------------------------------------------------ Q4_K
+// slot: [P][1024] code bytes of the step, then [P][8] 16-byte metadata records
 
-struct Q4Item {
-    uint4 c0, c1, mt;
+constexpr int Q4_CODES = 1024, Q4_META = 128;
+
+struct Q4Ops {
+    static constexpr int R = Q4_R, SLOT = Q4_SLOT;
+    static constexpr int SIDE_PER_32 = 8;                 // one float2 per 32-value block
+    struct LaneConst {
+        uint32_t selA, selB;
+        int aoff[4];
+    };
+    __device__ static LaneConst lane_const(int lane)
+    {
+        LaneConst c;
+        const int g = lane & 3;
+        c.selA = g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u;
+        c.selB = g == 0 ? 0x3210u : g == 1 ? 0x3210u : g == 2 ? 0x3410u : 0x3765u;
+#pragma unroll
+        for (int i = 0; i < 4; i++) c.aoff[i] = 16 * ((4 * lane + i) ^ (lane & 7));
+        return c;
+    }
+    // copy item (group starting at row n, step s) into a ring slot; no per-lane register payload
+    __device__ static uint32_t issue(uint8_t *slot, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n, int s,
+                                     int lane)
+    {
+        const int nsb = min(8, B - 8 * s), G = 4 * nsb;
+        const uint8_t *meta = w + N * (int64_t)B * 128;
+#pragma unroll
+        for (int r = 0; r < P; r++) {
+            if (n + r < N) {
+                const uint8_t *src = w + (n + r) * (int64_t)B * 128 + 1024 * s;
+                uint8_t *dst = slot + r * Q4_CODES;
+                if (lane < G) {
+                    qk::cp_async16(dst + 16 * lane, src + 16 * lane);
+                    qk::cp_async16(dst + 16 * G + 16 * lane, src + 16 * G + 16 * lane);
+                }
+                if (lane < nsb)
+                    qk::cp_async16(slot + P * Q4_CODES + r * Q4_META + 16 * lane,
+                                        meta + ((n + r) * B + 8 * s + lane) * 16);
+            }
+        }
+        return 0;
+    }
+    template <int M>
+    __device__ static void compute(const uint8_t *sl, int s, int B, int lane, uint32_t, const LaneConst &lc,
+                                   const uint8_t *s_codes, const float2 *s_sc, int K, float (&acc)[P][M])
+    {
+        const int G = 4 * min(8, B - 8 * s);
+        if (lane >= G) return;
+        uint4 c0[P], c1[P];
+        float d[P], dmin[P], m0[P], m1[P];
+        int sc0[P], sc1[P];
+#pragma unroll
+        for (int r = 0; r < P; r++) {
+            c0[r] = lds16(sl + r * Q4_CODES + 16 * lane);
+            c1[r] = lds16(sl + r * Q4_CODES + 16 * G + 16 * lane);
+            const uint4 mt = lds16(sl + P * Q4_CODES + r * Q4_META + 16 * (lane >> 2));
+            d[r] = f16lo(mt.x);
+            dmin[r] = f16hi(mt.x);
+            // this lane's group record: sc0 | sc1<<6 | m0<<12 | m1<<18
+            const uint32_t rec = __byte_perm(__byte_perm(mt.y, mt.z, lc.selA), mt.w, lc.selB);
+            sc0[r] = rec & 63u;
+            sc1[r] = (rec >> 6) & 63u;
+            m0[r] = (float)((rec >> 12) & 63u);
+            m1[r] = (float)((rec >> 18) & 63u);
+        }
+        const uint8_t *abase = s_codes + 2048 * s;             // activation of this step (chunk 128*s)
+        const float2 *sbase = s_sc + 64 * s + 2 * lane;       // 32-blocks 8*(8s + lane/4) + 2g, +1
+        const int nb = K >> 5;
+#pragma unroll
+        for (int m = 0; m < M; m++) {
+            const uint8_t *ar = abase + (size_t)m * K;
+            const uint4 a0 = lds16(ar + lc.aoff[0]), a1 = lds16(ar + lc.aoff[1]);   // sub-block 2g
+            const uint4 a2 = lds16(ar + lc.aoff[2]), a3 = lds16(ar + lc.aoff[3]);   // sub-block 2g+1
+            const float4 sa = *reinterpret_cast<const float4 *>(sbase + (size_t)m * nb);   // d0 S0 d1/16 S1
+#pragma unroll
+            for (int r = 0; r < P; r++) {
+                const uint4 x0 = c0[r], x1 = c1[r];
+                int il = qk::dp4a_ss(x0.x & 0x0F0F0F0Fu, a0.x, 0), ih = qk::dp4a_us(x0.x & 0xF0F0F0F0u, a2.x, 0);
+                il = qk::dp4a_ss(x0.y & 0x0F0F0F0Fu, a0.y, il), ih = qk::dp4a_us(x0.y & 0xF0F0F0F0u, a2.y, ih);
+                il = qk::dp4a_ss(x0.z & 0x0F0F0F0Fu, a0.z, il), ih = qk::dp4a_us(x0.z & 0xF0F0F0F0u, a2.z, ih);
+                il = qk::dp4a_ss(x0.w & 0x0F0F0F0Fu, a0.w, il), ih = qk::dp4a_us(x0.w & 0xF0F0F0F0u, a2.w, ih);
+                il = qk::dp4a_ss(x1.x & 0x0F0F0F0Fu, a1.x, il), ih = qk::dp4a_us(x1.x & 0xF0F0F0F0u, a3.x, ih);
+                il = qk::dp4a_ss(x1.y & 0x0F0F0F0Fu, a1.y, il), ih = qk::dp4a_us(x1.y & 0xF0F0F0F0u, a3.y, ih);
+                il = qk::dp4a_ss(x1.z & 0x0F0F0F0Fu, a1.z, il), ih = qk::dp4a_us(x1.z & 0xF0F0F0F0u, a3.z, ih);
+                il = qk::dp4a_ss(x1.w & 0x0F0F0F0Fu, a1.w, il), ih = qk::dp4a_us(x1.w & 0xF0F0F0F0u, a3.w, ih);
+                float t = sa.x * (float)(il * sc0[r]);
+                t = fmaf(sa.z, (float)(ih * sc1[r]), t);
+                const float v = fmaf(m1[r], sa.w, m0[r] * sa.y);
+                acc[r][m] = fmaf(d[r], t, fmaf(-dmin[r], v, acc[r][m]));
+            }
+        }
+    }
+    template <int M, int NT, bool FUSED>
+    __device__ static void stage(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
+    {
+        if (FUSED) stage_quant<M, NT, false>(a, s_codes, s_side);
+        else stage_act_q4k<M, NT>(a.codes, a.scales, a.K, s_codes, s_side);
+    }
 };
-
-__device__ __forceinline__ void q4_load(Q4Item &it, const uint8_t *__restrict__ w, int64_t N, int B,
-                                        int64_t n, int s, int lane)
-{
-    const int nsb = min(8, B - 8 * s), G = 4 * nsb;
-    if (n < N && lane < G) {
-        const uint8_t *base = w + n * (int64_t)B * 128 + 1024 * s;
-        it.c0 = qk::ldg_stream16(base + 16 * lane);
-        it.c1 = qk::ldg_stream16(base + 16 * G + 16 * lane);
-        it.mt = qk::ldg_stream16(w + N * (int64_t)B * 128 + (n * B + 8 * s + (lane >> 2)) * 16);
-    } else {
-        it.c0 = it.c1 = it.mt = make_uint4(0, 0, 0, 0);
-    }
-}
-
-template <int M>
-__device__ __forceinline__ void q4_compute(const Q4Item &it, int s, int lane, int K, uint32_t selA, uint32_t selB,
-                                           const uint8_t *s_codes, const float2 *s_sc, float (&acc)[M])
-{
-    // scales: d, dmin and this lane's group record (sc0 | sc1<<6 | m0<<12 | m1<<18)
-    const float d = __half2float(__ushort_as_half((unsigned short)(it.mt.x & 0xffffu)));
-    const float dmin = __half2float(__ushort_as_half((unsigned short)(it.mt.x >> 16)));
-    const uint32_t rec = __byte_perm(__byte_perm(it.mt.y, it.mt.z, selA), it.mt.w, selB);
-    const float dsc0 = d * (float)(rec & 63u);
-    const float dsc1 = d * (float)((rec >> 6) & 63u) * 0.0625f;      // high nibbles are read as 16*q
-    const float dmm0 = dmin * (float)((rec >> 12) & 63u);
-    const float dmm1 = dmin * (float)((rec >> 18) & 63u);
-    const uint32_t lo[8] = {it.c0.x & 0x0F0F0F0Fu, it.c0.y & 0x0F0F0F0Fu, it.c0.z & 0x0F0F0F0Fu,
-                            it.c0.w & 0x0F0F0F0Fu, it.c1.x & 0x0F0F0F0Fu, it.c1.y & 0x0F0F0F0Fu,
-                            it.c1.z & 0x0F0F0F0Fu, it.c1.w & 0x0F0F0F0Fu};
-    const uint32_t hi[8] = {it.c0.x & 0xF0F0F0F0u, it.c0.y & 0xF0F0F0F0u, it.c0.z & 0xF0F0F0F0u,
-                            it.c0.w & 0xF0F0F0F0u, it.c1.x & 0xF0F0F0F0u, it.c1.y & 0xF0F0F0F0u,
-                            it.c1.z & 0xF0F0F0F0u, it.c1.w & 0xF0F0F0F0u};
-    const int c0 = 128 * s + 4 * lane;          // first activation chunk of this lane's group
-    const int kb0 = 64 * s + 2 * lane;          // its first 32-value block
-    const int nb = K >> 5;
-#pragma unroll
-    for (int m = 0; m < M; m++) {
-        const uint8_t *arow = s_codes + (size_t)m * K;
-        const uint4 a0 = lds16(arow + 16 * swz(c0 + 0));     // sub-block 2g, values 0..15
-        const uint4 a1 = lds16(arow + 16 * swz(c0 + 1));     // sub-block 2g, values 16..31
-        const uint4 a2 = lds16(arow + 16 * swz(c0 + 2));     // sub-block 2g+1, values 0..15
-        const uint4 a3 = lds16(arow + 16 * swz(c0 + 3));     // sub-block 2g+1, values 16..31
-        int il = 0, ih = 0;
-        il = qk::dp4a_ss(lo[0], a0.x, il), il = qk::dp4a_ss(lo[1], a0.y, il);
-        il = qk::dp4a_ss(lo[2], a0.z, il), il = qk::dp4a_ss(lo[3], a0.w, il);
-        il = qk::dp4a_ss(lo[4], a1.x, il), il = qk::dp4a_ss(lo[5], a1.y, il);
-        il = qk::dp4a_ss(lo[6], a1.z, il), il = qk::dp4a_ss(lo[7], a1.w, il);
-        ih = qk::dp4a_us(hi[0], a2.x, ih), ih = qk::dp4a_us(hi[1], a2.y, ih);
-        ih = qk::dp4a_us(hi[2], a2.z, ih), ih = qk::dp4a_us(hi[3], a2.w, ih);
-        ih = qk::dp4a_us(hi[4], a3.x, ih), ih = qk::dp4a_us(hi[5], a3.y, ih);
-        ih = qk::dp4a_us(hi[6], a3.z, ih), ih = qk::dp4a_us(hi[7], a3.w, ih);
-        const float4 sc = *reinterpret_cast<const float4 *>(s_sc + (size_t)m * nb + kb0);  // d0 S0 d1 S1
-        float a = acc[m];
-        a = fmaf(sc.x, dsc0 * (float)il, a);
-        a = fmaf(sc.z, dsc1 * (float)ih, a);
-        a = fmaf(-dmm0, sc.y, a);
-        a = fmaf(-dmm1, sc.w, a);
-        acc[m] = a;
-    }
-}
-
-template <int M>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemv_q4k_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ codes,
-                    const __half2 *__restrict__ scales, int64_t N, int K, const float *residual, float *y)
-{
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *s_codes = smem;
-    float2 *s_sc = reinterpret_cast<float2 *>(smem + (size_t)M * K);
-    const int B = K >> 8, nsteps = (B + 7) >> 3;
-    const int lane = threadIdx.x & 31;
-    const int64_t W = (int64_t)gridDim.x * kWarps;
-    const int g = lane & 3;
-    const uint32_t selA = g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u;
-    const uint32_t selB = g == 0 ? 0x3210u : g == 1 ? 0x3210u : g == 2 ? 0x3410u : 0x3765u;
-
-    // item = (row n, step s); items of this warp: rows n0, n0+W, ..., each steps 0..nsteps-1
-    int64_t n_cur = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    int s_cur = 0;
-    int64_t n1 = n_cur, n2;
-    int s1 = 0, s2;
-    if (++s1 == nsteps) s1 = 0, n1 += W;
-    n2 = n1, s2 = s1;
-    if (++s2 == nsteps) s2 = 0, n2 += W;
-
-    Q4Item cur, nx1, nx2;
-    q4_load(cur, w, N, B, n_cur, s_cur, lane);    // weights never depend on the previous kernel
-    q4_load(nx1, w, N, B, n1, s1, lane);
-
-    qk::pdl_wait();
-    stage_act_q4k<M>(codes, scales, K, s_codes, s_sc);
-    __syncthreads();
-    qk::pdl_launch_dependents();
-
-    float acc[M];
-#pragma unroll
-    for (int m = 0; m < M; m++) acc[m] = 0.0f;
-
-    while (n_cur < N) {
-        q4_load(nx2, w, N, B, n2, s2, lane);
-        if (lane < 4 * min(8, B - 8 * s_cur)) q4_compute<M>(cur, s_cur, lane, K, selA, selB, s_codes, s_sc, acc);
-        if (s_cur == nsteps - 1) finish_row<M>(acc, lane, n_cur, N, residual, y);
-        cur = nx1, nx1 = nx2;
-        n_cur = n1, s_cur = s1, n1 = n2, s1 = s2;
-        if (++s2 == nsteps) s2 = 0, n2 += W;
-    }
-}
 
 // ------------------------------------------------------------------ Q6_K
+// slot: [P][1024] ql bytes of the step, [P][512] qh bytes, [P][8] 16-byte scale records
 
-struct Q6Item {
-    uint4 a, b, h;
-    uint32_t sc;
-    uint32_t d;
-};
+constexpr int Q6_QL = 1024, Q6_QH = 512, Q6_SC = 128;
 
-__device__ __forceinline__ void q6_load(Q6Item &it, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n,
-                                        int s, int lane)
-{
-    const int nsb = min(8, B - 8 * s), L = 4 * nsb;
-    if (n < N && lane < L) {
-        const int64_t NB = N * (int64_t)B;
-        const int64_t sb0 = n * B + 8 * s;                       // first superblock of the step
-        const uint8_t *base = w + n * (int64_t)B * 128 + 1024 * s;
-        it.a = qk::ldg_stream16(base + 16 * lane);
-        it.b = qk::ldg_stream16(base + 16 * L + 16 * lane);
-        it.h = qk::ldg_stream16(w + NB * 128 + sb0 * 64 + 16 * lane);
-        it.sc = qk::ldg_stream4(w + NB * 192 + sb0 * 16 + 4 * lane);
-        it.d = qk::ldg_stream2(w + NB * 208 + (sb0 + (lane >> 2)) * 2);
-    } else {
-        it.a = it.b = it.h = make_uint4(0, 0, 0, 0);
-        it.sc = it.d = 0;
-    }
-}
-
-template <int M>
-__device__ __forceinline__ void q6_compute(const Q6Item &it, int s, int lane, int K, const uint8_t *s_codes,
-                                           const float *s_d, const float *s_s16, float (&acc)[M])
-{
-    const float d = __half2float(__ushort_as_half((unsigned short)it.d));
-    float dsc[4];
-#pragma unroll
-    for (int t = 0; t < 4; t++) dsc[t] = d * (float)(int)(int8_t)(it.sc >> (8 * t));
-    // 6-bit codes u = low4 | high2 << 4 in [0, 63]; the -32 offset is applied with the block sums
-    const uint32_t aw[4] = {it.a.x, it.a.y, it.a.z, it.a.w};
-    const uint32_t bw[4] = {it.b.x, it.b.y, it.b.z, it.b.w};
-    const uint32_t hw[4] = {it.h.x, it.h.y, it.h.z, it.h.w};
-    uint32_t u[4][4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-        u[0][j] = (aw[j] & 0x0F0F0F0Fu) | ((hw[j] << 4) & 0x30303030u);
-        u[1][j] = (bw[j] & 0x0F0F0F0Fu) | ((hw[j] << 2) & 0x30303030u);
-        u[2][j] = ((aw[j] >> 4) & 0x0F0F0F0Fu) | (hw[j] & 0x30303030u);
-        u[3][j] = ((bw[j] >> 4) & 0x0F0F0F0Fu) | ((hw[j] >> 2) & 0x30303030u);
-    }
-    const int p = lane & 3, h = p >> 1, e = p & 1;
-    const int cbase = 128 * s + 16 * (lane >> 2) + 8 * h + e;    // activation chunk of quarter t: cbase + 2t
-    const int nb = K >> 5, nc = K >> 4;
-#pragma unroll
-    for (int m = 0; m < M; m++) {
-        const uint8_t *arow = s_codes + (size_t)m * K;
-        float a = acc[m];
+struct Q6Ops {
+    static constexpr int R = Q6_R, SLOT = Q6_SLOT;
+    static constexpr int SIDE_PER_32 = 16;                // one float2 per 16-value chunk
+    struct LaneConst {
+        int qoff[4], coff[4];
+    };
+    __device__ static LaneConst lane_const(int lane)
+    {
+        // lane (superblock lane/4, p = lane%4 = 2h+e) reads activation chunk
+        // 16*(lane/4) + 8h + e + 2t of the step for quarter t
+        LaneConst c;
+        const int p = lane & 3, h = p >> 1, e = p & 1;
 #pragma unroll
         for (int t = 0; t < 4; t++) {
-            const int c = cbase + 2 * t;
-            const uint4 av = lds16(arow + 16 * swz(c));
-            int dot = 0;
-            dot = qk::dp4a_ss(u[t][0], av.x, dot), dot = qk::dp4a_ss(u[t][1], av.y, dot);
-            dot = qk::dp4a_ss(u[t][2], av.z, dot), dot = qk::dp4a_ss(u[t][3], av.w, dot);
-            const float da = s_d[m * nb + (c >> 1)];
-            const float f = (float)dot - s_s16[m * nc + c];          // exact: sum of (u - 32) * q_a
-            a = fmaf(da * dsc[t], f, a);
+            c.coff[t] = 16 * (lane >> 2) + 8 * h + e + 2 * t;
+            c.qoff[t] = 16 * swz(c.coff[t]);
         }
-        acc[m] = a;
+        return c;
     }
+    // copy an item into a ring slot; returns this lane's binary16 d register:
+    // lane 8r+j (j < nsb) holds d of superblock 8s+j of row r (2-byte records)
+    __device__ static uint32_t issue(uint8_t *slot, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n, int s,
+                                     int lane)
+    {
+        uint32_t dv = 0;
+        const int nsb = min(8, B - 8 * s), L = 4 * nsb;
+        const int64_t NB = N * (int64_t)B;
+#pragma unroll
+        for (int r = 0; r < P; r++) {
+            if (n + r < N) {
+                const int64_t sb0 = (n + r) * B + 8 * s;
+                const uint8_t *src = w + (n + r) * (int64_t)B * 128 + 1024 * s;
+                uint8_t *dst = slot + r * Q6_QL;
+                if (lane < L) {
+                    qk::cp_async16(dst + 16 * lane, src + 16 * lane);
+                    qk::cp_async16(dst + 16 * L + 16 * lane, src + 16 * L + 16 * lane);
+                    qk::cp_async16(slot + P * Q6_QL + r * Q6_QH + 16 * lane, w + NB * 128 + sb0 * 64 + 16 * lane);
+                }
+                if (lane < nsb)
+                    qk::cp_async16(slot + P * (Q6_QL + Q6_QH) + r * Q6_SC + 16 * lane,
+                                        w + NB * 192 + (sb0 + lane) * 16);
+                if ((lane >> 3) == r && (lane & 7) < nsb) dv = qk::ldg_stream2(w + NB * 208 + (sb0 + (lane & 7)) * 2);
+            }
+        }
+        return dv;
+    }
+    template <int M>
+    __device__ static void compute(const uint8_t *sl, int s, int B, int lane, uint32_t dreg, const LaneConst &lc,
+                                   const uint8_t *s_codes, const float2 *s_c16, int K, float (&acc)[P][M])
+    {
+        const int L = 4 * min(8, B - 8 * s);
+        float d[P];
+#pragma unroll
+        for (int r = 0; r < P; r++)
+            d[r] = __half2float(__ushort_as_half((unsigned short)__shfl_sync(0xffffffffu, dreg, 8 * r + (lane >> 2))));
+        if (lane >= L) return;
+        // 6-bit codes u = low4 | high2 << 4 in [0, 63]; the -32 offset comes with the staged block sums
+        uint32_t u[P][4][4];
+        float dsc[P][4];
+#pragma unroll
+        for (int r = 0; r < P; r++) {
+            const uint4 a = lds16(sl + r * Q6_QL + 16 * lane), b = lds16(sl + r * Q6_QL + 16 * L + 16 * lane);
+            const uint4 h = lds16(sl + P * Q6_QL + r * Q6_QH + 16 * lane);
+            const uint32_t scw =
+                *reinterpret_cast<const uint32_t *>(sl + P * (Q6_QL + Q6_QH) + r * Q6_SC + 4 * lane);
+#pragma unroll
+            for (int t = 0; t < 4; t++) dsc[r][t] = d[r] * (float)(int)(int8_t)(scw >> (8 * t));
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w}, hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                u[r][0][j] = (aw[j] & 0x0F0F0F0Fu) | ((hw[j] << 4) & 0x30303030u);
+                u[r][1][j] = (bw[j] & 0x0F0F0F0Fu) | ((hw[j] << 2) & 0x30303030u);
+                u[r][2][j] = ((aw[j] >> 4) & 0x0F0F0F0Fu) | (hw[j] & 0x30303030u);
+                u[r][3][j] = ((bw[j] >> 4) & 0x0F0F0F0Fu) | ((hw[j] >> 2) & 0x30303030u);
+            }
+        }
+        const uint8_t *abase = s_codes + 2048 * s;
+        const float2 *cbase = s_c16 + 128 * s;
+        const int nc = K >> 4;
+#pragma unroll
+        for (int m = 0; m < M; m++) {
+            const uint8_t *ar = abase + (size_t)m * K;
+            const float2 *cr = cbase + (size_t)m * nc;
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+                const uint4 av = lds16(ar + lc.qoff[t]);
+                const float2 dc = cr[lc.coff[t]];                    // d_a * (dot - 32 * sum q_a)
+#pragma unroll
+                for (int r = 0; r < P; r++) {
+                    int dot = qk::dp4a_ss(u[r][t][0], av.x, 0);
+                    dot = qk::dp4a_ss(u[r][t][1], av.y, dot);
+                    dot = qk::dp4a_ss(u[r][t][2], av.z, dot);
+                    dot = qk::dp4a_ss(u[r][t][3], av.w, dot);
+                    acc[r][m] = fmaf(dsc[r][t], fmaf(dc.x, (float)dot, dc.y), acc[r][m]);
+                }
+            }
+        }
+    }
+    template <int M, int NT, bool FUSED>
+    __device__ static void stage(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
+    {
+        if (FUSED) stage_quant<M, NT, true>(a, s_codes, s_side);
+        else stage_act_q6k<M, NT>(a.codes, a.scales, a.K, s_codes, s_side);
+    }
+};
+
+// ---------------------------------------------------------------- driver
+
+template <class Ops, int M, bool FUSED>
+__device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
+{
+    constexpr int kWarps = Cfg<M, FUSED>::warps, R = Ops::R;
+    if (QK_GEMV_TRIGGER == 0) qk::pdl_launch_dependents();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t N = a.N;
+    const int K = a.K, B = K >> 8, nsteps = (B + 7) >> 3;
+    const uint8_t *__restrict__ w = a.w;
+    uint8_t *ring = smem + warp * (R * Ops::SLOT);
+    uint8_t *s_codes = smem + kWarps * R * Ops::SLOT;
+    float2 *s_side = reinterpret_cast<float2 *>(s_codes + (size_t)M * K);
+    Part *part = reinterpret_cast<Part *>(s_codes + (size_t)M * K + (size_t)M * (K >> 5) * Ops::SIDE_PER_32);
+    const typename Ops::LaneConst lc = Ops::lane_const(lane);
+
+    // bulk rounds of groups over all W warps, then this CTA's tail groups [ga, gb)
+    // and this warp's tail items [ia, ib) (tail item = group*nsteps + step)
+    const int64_t NG = (N + P - 1) / P;
+    const int64_t W = (int64_t)gridDim.x * kWarps, wg0 = (int64_t)blockIdx.x * kWarps + warp;
+    const int64_t rounds = NG / W, tail0 = rounds * W, NT = NG - tail0;
+    const int64_t ga = tail0 + (int64_t)blockIdx.x * NT / gridDim.x;
+    const int64_t gb = tail0 + ((int64_t)blockIdx.x + 1) * NT / gridDim.x;
+    const int64_t T = (gb - ga) * nsteps;
+    const int64_t ia = (int64_t)warp * T / kWarps, ib = ((int64_t)warp + 1) * T / kWarps;
+    const int64_t total = rounds * nsteps + (ib - ia);
+    ItemSeq rd;
+    rd.W = W;
+    rd.tail_g = ga + ia / nsteps;
+    rd.tail_s = (int)(ia % nsteps);
+    rd.bulk_left = rounds * nsteps;
+    rd.g = rounds > 0 ? wg0 : rd.tail_g;
+    rd.s = rounds > 0 ? 0 : rd.tail_s;
+    ItemSeq wr = rd;
+    if (lane == 0) part[warp].g[0] = part[warp].g[1] = -1;
+
+    // weights never depend on the previous kernel: the first R-1 items are
+    // requested before waiting for it
+    int64_t wi = 0;
+    uint32_t reg[R - 1];
+#pragma unroll
+    for (int j = 0; j < R - 1; j++) {
+        reg[j] = 0;
+        if (wi < total) reg[j] = Ops::issue(ring + j * Ops::SLOT, w, N, B, P * wr.g, wr.s, lane);
+        qk::cp_async_commit();
+        wr.next(nsteps);
+        ++wi;
+    }
+    qk::pdl_wait();
+    Ops::template stage<M, Cfg<M, FUSED>::threads, FUSED>(a, s_codes, s_side);
+    __syncthreads();
+    if (QK_GEMV_TRIGGER == 1) qk::pdl_launch_dependents();
+
+    float acc[P][M];
+#pragma unroll
+    for (int r = 0; r < P; r++)
+#pragma unroll
+        for (int m = 0; m < M; m++) acc[r][m] = 0.0f;
+
+    bool whole = rd.s == 0;             // this warp saw the current group's first step
+    int np = 0;                         // partial groups stored so far
+    int slot = 0, wslot = R - 1;
+    for (int64_t k = 0; k < total; k++) {
+        uint32_t rnew = 0;
+        if (wi < total) rnew = Ops::issue(ring + wslot * Ops::SLOT, w, N, B, P * wr.g, wr.s, lane);
+        qk::cp_async_commit();
+        wr.next(nsteps);
+        ++wi;
+        qk::cp_async_wait<R - 1>();
+        __syncwarp();
+        Ops::template compute<M>(ring + slot * Ops::SLOT, rd.s, B, lane, reg[0], lc, s_codes, s_side, K, acc);
+        __syncwarp();
+        const bool last_step = rd.s == nsteps - 1;
+        if (last_step || k == total - 1) {
+#pragma unroll
+            for (int r = 0; r < P; r++)
+#pragma unroll
+                for (int m = 0; m < M; m++) {
+                    const float v = warp_sum(acc[r][m]);
+                    acc[r][m] = 0.0f;
+                    const int64_t n = P * rd.g + r;
+                    if (whole && last_step) {
+                        if (lane == m && n < N) {
+                            const size_t o = (size_t)m * N + n;
+                            a.y[o] = a.residual ? __fadd_rn(v, a.residual[o]) : v;
+                        }
+                    } else if (lane == 0) {
+                        part[warp].v[np][r][m] = v;
+                    }
+                }
+            if (!(whole && last_step)) {
+                if (lane == 0) part[warp].g[np] = rd.g;
+                ++np;
+            }
+        }
+        rd.next(nsteps);
+        if (last_step || k == total - 1) whole = rd.s == 0;
+#pragma unroll
+        for (int j = 0; j < R - 2; j++) reg[j] = reg[j + 1];
+        reg[R - 2] = rnew;
+        wslot = slot;
+        slot = slot + 1 == R ? 0 : slot + 1;
+    }
+    qk::cp_async_wait<0>();
+    __syncthreads();
+    // groups cut between warps: sum their partials in warp order
+    if (warp == 0 && lane < M * P) {
+        const int m = lane / P, r = lane % P;
+        long long cur = -1;
+        float sum = 0.0f;
+        for (int ww = 0; ww < kWarps; ww++)
+            for (int k = 0; k < 2; k++) {
+                const long long gg = part[ww].g[k];
+                if (gg < 0) continue;
+                if (gg != cur) {
+                    if (cur >= 0 && P * cur + r < N) {
+                        const size_t o = (size_t)m * N + (size_t)(P * cur + r);
+                        a.y[o] = a.residual ? __fadd_rn(sum, a.residual[o]) : sum;
+                    }
+                    cur = gg;
+                    sum = 0.0f;
+                }
+                sum += part[ww].v[k][r][m];
+            }
+        if (cur >= 0 && P * cur + r < N) {
+            const size_t o = (size_t)m * N + (size_t)(P * cur + r);
+            a.y[o] = a.residual ? __fadd_rn(sum, a.residual[o]) : sum;
+        }
+    }
+    if (QK_GEMV_TRIGGER == 2) qk::pdl_launch_dependents();
 }
 
-template <int M>
-__global__ void __launch_bounds__(kThreads, 1)
-    gemv_q6k_kernel(const uint8_t *__restrict__ w, const int8_t *__restrict__ codes,
-                    const __half2 *__restrict__ scales, int64_t N, int K, const float *residual, float *y)
+template <int M, bool FUSED>
+__global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q4k_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t *s_codes = smem;
-    float *s_s16 = reinterpret_cast<float *>(smem + (size_t)M * K);
-    float *s_d = s_s16 + (size_t)M * (K >> 4);
-    const int B = K >> 8, nsteps = (B + 7) >> 3;
-    const int lane = threadIdx.x & 31;
-    const int64_t W = (int64_t)gridDim.x * kWarps;
+    gemv_body<Q4Ops, M, FUSED>(a, smem);
+}
 
-    int64_t n_cur = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    int s_cur = 0;
-    int64_t n1 = n_cur, n2;
-    int s1 = 0, s2;
-    if (++s1 == nsteps) s1 = 0, n1 += W;
-    n2 = n1, s2 = s1;
-    if (++s2 == nsteps) s2 = 0, n2 += W;
-
-    Q6Item cur, nx1, nx2;
-    q6_load(cur, w, N, B, n_cur, s_cur, lane);
-    q6_load(nx1, w, N, B, n1, s1, lane);
-
-    qk::pdl_wait();
-    stage_act_q6k<M>(codes, scales, K, s_codes, s_d, s_s16);
-    __syncthreads();
-    qk::pdl_launch_dependents();
-
-    float acc[M];
-#pragma unroll
-    for (int m = 0; m < M; m++) acc[m] = 0.0f;
-
-    while (n_cur < N) {
-        q6_load(nx2, w, N, B, n2, s2, lane);
-        if (lane < 4 * min(8, B - 8 * s_cur)) q6_compute<M>(cur, s_cur, lane, K, s_codes, s_d, s_s16, acc);
-        if (s_cur == nsteps - 1) finish_row<M>(acc, lane, n_cur, N, residual, y);
-        cur = nx1, nx1 = nx2;
-        n_cur = n1, s_cur = s1, n1 = n2, s1 = s2;
-        if (++s2 == nsteps) s2 = 0, n2 += W;
-    }
+template <int M, bool FUSED>
+__global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q6k_kernel(const GemvArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    gemv_body<Q6Ops, M, FUSED>(a, smem);
 }
 
 // ------------------------------------------------------------------ host
 
-// per (qtype, M) kernel: largest dynamic shared memory opted in so far (per process)
-std::atomic<int> g_smem_set[2][8];
+typedef void (*gemv_fn)(const GemvArgs);
 
-template <typename Kern>
-int set_smem(Kern kern, std::atomic<int> &done, size_t smem)
+// per kernel: largest dynamic shared memory opted in so far (per process)
+std::atomic<int> g_smem_set[2][2][8];
+
+int prepare(gemv_fn kern, std::atomic<int> &done, size_t smem)
 {
     // opt in to more than 48 KB of dynamic shared memory; repeated only when a larger size is needed
     if ((int)smem <= done.load(std::memory_order_relaxed)) return QK_OK;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = qk::max_carveout(kern);
     if (e != cudaSuccess) return QK_E_CUDA;
     int prev = done.load(std::memory_order_relaxed);
     while ((int)smem > prev && !done.compare_exchange_weak(prev, (int)smem)) {
@@ -351,44 +639,95 @@ int set_smem(Kern kern, std::atomic<int> &done, size_t smem)
     return QK_OK;
 }
 
-typedef void (*gemv_fn)(const uint8_t *, const int8_t *, const __half2 *, int64_t, int, const float *, float *);
-
+template <bool FUSED>
 gemv_fn pick(int qtype, int M)
 {
-    static const gemv_fn q4[8] = {gemv_q4k_kernel<1>, gemv_q4k_kernel<2>, gemv_q4k_kernel<3>, gemv_q4k_kernel<4>,
-                                  gemv_q4k_kernel<5>, gemv_q4k_kernel<6>, gemv_q4k_kernel<7>, gemv_q4k_kernel<8>};
-    static const gemv_fn q6[8] = {gemv_q6k_kernel<1>, gemv_q6k_kernel<2>, gemv_q6k_kernel<3>, gemv_q6k_kernel<4>,
-                                  gemv_q6k_kernel<5>, gemv_q6k_kernel<6>, gemv_q6k_kernel<7>, gemv_q6k_kernel<8>};
+    static const gemv_fn q4[8] = {gemv_q4k_kernel<1, FUSED>, gemv_q4k_kernel<2, FUSED>, gemv_q4k_kernel<3, FUSED>,
+                                  gemv_q4k_kernel<4, FUSED>, gemv_q4k_kernel<5, FUSED>, gemv_q4k_kernel<6, FUSED>,
+                                  gemv_q4k_kernel<7, FUSED>, gemv_q4k_kernel<8, FUSED>};
+    static const gemv_fn q6[8] = {gemv_q6k_kernel<1, FUSED>, gemv_q6k_kernel<2, FUSED>, gemv_q6k_kernel<3, FUSED>,
+                                  gemv_q6k_kernel<4, FUSED>, gemv_q6k_kernel<5, FUSED>, gemv_q6k_kernel<6, FUSED>,
+                                  gemv_q6k_kernel<7, FUSED>, gemv_q6k_kernel<8, FUSED>};
     return qtype == QK_TYPE_Q4_K ? q4[M - 1] : q6[M - 1];
 }
 
-int gemv(int qtype, const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N, int64_t K,
-         const float *residual, float *y, unsigned flags, void *stream)
+int warps_for(int M, bool fused)
 {
-    if (M < 1 || M > 8 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || M * K > 163840)
+    return M > 2 ? QK_GEMV_WARPS : fused ? QK_GEMV_WARPS_FUSED : QK_GEMV_WARPS_SMALL_M;
+}
+
+int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, unsigned flags, void *stream)
+{
+    if (M < 1 || M > 8 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 ||
+        M * K > (qtype == QK_TYPE_Q4_K ? 81920 : 40960))
         return QK_E_SHAPE;
-    if (!w || !codes || !scales || !y) return QK_E_NULL;
-    if (!qk::aligned(w, 16) || !qk::aligned(codes, 16) || !qk::aligned(scales, 16) || !qk::aligned(y, 4) ||
-        (residual && !qk::aligned(residual, 4)))
+    if (!a.w || !a.y) return QK_E_NULL;
+    if (fused ? !a.x : (!a.codes || !a.scales)) return QK_E_NULL;
+    if (fused && (a.codes_out == nullptr) != (a.scales_out == nullptr)) return QK_E_NULL;
+    if (fused && a.ldx < K) return QK_E_SHAPE;
+    if (!qk::aligned(a.w, 16) || !qk::aligned(a.y, 4) || (a.residual && !qk::aligned(a.residual, 4)))
+        return QK_E_ALIGN;
+    if (!fused && (!qk::aligned(a.codes, 16) || !qk::aligned(a.scales, 16))) return QK_E_ALIGN;
+    if (fused && (!qk::aligned(a.x, 16) || a.ldx % 4 != 0 || (a.codes_out && !qk::aligned(a.codes_out, 16)) ||
+                  (a.scales_out && !qk::aligned(a.scales_out, 16))))
         return QK_E_ALIGN;
     size_t wbytes = 0;
     qk_repacked_bytes(qtype, N, K, &wbytes);
     const size_t ybytes = (size_t)M * N * 4, cbytes = (size_t)M * K, sbytes = (size_t)M * (K / 32) * 4;
-    if (qk::overlaps(y, ybytes, w, wbytes) || qk::overlaps(y, ybytes, codes, cbytes) ||
-        qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)))
+    const size_t xbytes = fused ? ((size_t)(M - 1) * (size_t)a.ldx + (size_t)K) * 4 : 0;
+    if (qk::overlaps(a.y, ybytes, a.w, wbytes) || qk::overlaps(a.y, ybytes, a.codes, cbytes) ||
+        qk::overlaps(a.y, ybytes, a.scales, sbytes) || qk::overlaps(a.y, ybytes, a.x, xbytes) ||
+        (a.residual != a.y && qk::overlaps(a.y, ybytes, a.residual, ybytes)))
         return QK_E_ALIAS;
-    const size_t smem = qtype == QK_TYPE_Q4_K ? (size_t)M * K + (size_t)M * (K / 32) * 8
-                                              : (size_t)M * K + (size_t)M * (K / 16) * 4 + (size_t)M * (K / 32) * 4;
-    gemv_fn kern = pick(qtype, (int)M);
-    int st = set_smem(kern, g_smem_set[qtype == QK_TYPE_Q4_K ? 0 : 1][M - 1], smem);
+    if (a.codes_out &&
+        (qk::overlaps(a.codes_out, cbytes, a.x, xbytes) || qk::overlaps(a.scales_out, sbytes, a.x, xbytes) ||
+         qk::overlaps(a.codes_out, cbytes, a.y, ybytes) || qk::overlaps(a.scales_out, sbytes, a.y, ybytes) ||
+         qk::overlaps(a.codes_out, cbytes, a.w, wbytes) || qk::overlaps(a.scales_out, sbytes, a.w, wbytes) ||
+         qk::overlaps(a.codes_out, cbytes, a.scales_out, sbytes) ||
+         (a.residual && (qk::overlaps(a.codes_out, cbytes, a.residual, ybytes) ||
+                         qk::overlaps(a.scales_out, sbytes, a.residual, ybytes)))))
+        return QK_E_ALIAS;
+    const int warps = warps_for((int)M, fused);
+    // ring | activation codes | side data | per-warp partials
+    const size_t smem = (size_t)warps * (qtype == QK_TYPE_Q4_K ? Q4_R * Q4_SLOT : Q6_R * Q6_SLOT) +
+                        (size_t)M * K + (size_t)M * (K / 32) * (qtype == QK_TYPE_Q4_K ? 8 : 16) +
+                        (size_t)warps * sizeof(Part);
+    if (smem > qk::max_smem_optin()) return QK_E_SHAPE;
+    gemv_fn kern = fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M);
+    int st = prepare(kern, g_smem_set[qtype == QK_TYPE_Q4_K ? 0 : 1][fused ? 1 : 0][M - 1], smem);
     if (st != QK_OK) return st;
-    const int64_t warps_needed = N;
-    int64_t grid = qk::sm_count();
-    const int64_t max_useful = (warps_needed + kWarps - 1) / kWarps;
-    if (grid > max_useful) grid = max_useful;
-    return qk::launch(kern, dim3((unsigned)grid), dim3(kThreads), smem, (cudaStream_t)stream,
-                      (flags & QK_LAUNCH_PDL) != 0, static_cast<const uint8_t *>(w), codes,
-                      static_cast<const __half2 *>(scales), N, (int)K, residual, y);
+    int64_t grid = (int64_t)kCtasPerSm * qk::sm_count();
+    const int64_t groups = (N + kRowsPerItem - 1) / kRowsPerItem;
+    if (grid > groups) grid = groups;                               // every CTA gets a group at least
+    a.N = N;
+    a.K = (int)K;
+    return qk::launch(kern, dim3((unsigned)grid), dim3(warps * 32), smem, (cudaStream_t)stream,
+                      (flags & QK_LAUNCH_PDL) != 0, a);
+}
+
+GemvArgs q8_args(const void *w, const int8_t *codes, const void *scales, const float *residual, float *y)
+{
+    GemvArgs a = {};
+    a.w = static_cast<const uint8_t *>(w);
+    a.codes = codes;
+    a.scales = static_cast<const __half2 *>(scales);
+    a.residual = residual;
+    a.y = y;
+    return a;
+}
+
+GemvArgs f32_args(const void *w, const float *x, int64_t ldx, const float *residual, float *y, int8_t *codes_out,
+                  void *scales_out)
+{
+    GemvArgs a = {};
+    a.w = static_cast<const uint8_t *>(w);
+    a.x = x;
+    a.ldx = ldx;
+    a.codes_out = codes_out;
+    a.scales_out = static_cast<__half2 *>(scales_out);
+    a.residual = residual;
+    a.y = y;
+    return a;
 }
 
 }  // namespace
@@ -396,11 +735,27 @@ int gemv(int qtype, const void *w, const int8_t *codes, const void *scales, int6
 extern "C" int qk_gemv_q4k(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N,
                            int64_t K, const float *residual, float *y, unsigned flags, void *stream)
 {
-    return gemv(QK_TYPE_Q4_K, w, codes, scales, M, N, K, residual, y, flags, stream);
+    return gemv(QK_TYPE_Q4_K, false, q8_args(w, codes, scales, residual, y), M, N, K, flags, stream);
 }
 
 extern "C" int qk_gemv_q6k(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N,
                            int64_t K, const float *residual, float *y, unsigned flags, void *stream)
 {
-    return gemv(QK_TYPE_Q6_K, w, codes, scales, M, N, K, residual, y, flags, stream);
+    return gemv(QK_TYPE_Q6_K, false, q8_args(w, codes, scales, residual, y), M, N, K, flags, stream);
+}
+
+extern "C" int qk_gemv_q4k_f32(const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                               const float *residual, float *y, int8_t *codes_out, void *scales_out,
+                               unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q4_K, true, f32_args(w, x, ldx, residual, y, codes_out, scales_out), M, N, K, flags,
+                stream);
+}
+
+extern "C" int qk_gemv_q6k_f32(const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                               const float *residual, float *y, int8_t *codes_out, void *scales_out,
+                               unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q6_K, true, f32_args(w, x, ldx, residual, y, codes_out, scales_out), M, N, K, flags,
+                stream);
 }

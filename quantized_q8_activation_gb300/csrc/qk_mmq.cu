@@ -239,7 +239,8 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
         return QK_E_ALIAS;
     static std::atomic<int> smem_set{0};
     if (!smem_set.load()) {
-        if (cudaFuncSetAttribute(mmq_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+        if (cudaFuncSetAttribute(mmq_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess ||
+            qk::max_carveout(mmq_q4k_kernel) != cudaSuccess)
             return QK_E_CUDA;
         smem_set.store(1);
     }

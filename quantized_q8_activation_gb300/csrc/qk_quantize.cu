@@ -8,6 +8,8 @@
 // HBM-bound: 4 bytes read and 1.125 bytes written per value.
 #include "qk_common.cuh"
 
+#include <atomic>
+
 namespace {
 
 constexpr int kThreads = 256;              // 32 q8_1 blocks per CTA
@@ -17,8 +19,8 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(const float *__
                                                                  int8_t *__restrict__ codes,
                                                                  __half2 *__restrict__ scales, int64_t K)
 {
+    qk::pdl_launch_dependents();            // let the consumer start its weight prefetch
     qk::pdl_wait();                         // x may come from the previous kernel
-    qk::pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t blk = (int64_t)blockIdx.x * (kThreads / 8) + (threadIdx.x >> 3);   // q8_1 block id
     const bool live = blk < nblocks;
@@ -27,33 +29,15 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(const float *__
     const int sub = lane & 7;               // lane within the block's 8-lane group
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) v = *reinterpret_cast<const float4 *>(x + m * ldx + 32 * b + 4 * sub);
-
-    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-
-    const float d = __fdiv_rn(amax, 127.0f);
-    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-    if (d > 0.0f) {
-        q0 = (int)roundf(__fdiv_rn(v.x, d));
-        q1 = (int)roundf(__fdiv_rn(v.y, d));
-        q2 = (int)roundf(__fdiv_rn(v.z, d));
-        q3 = (int)roundf(__fdiv_rn(v.w, d));
-    }
-    int sum = q0 + q1 + q2 + q3;
+    float d;
+    int sum;
+    const uint32_t packed = qk::q81_quant8(v, d, sum);
     sum += __shfl_xor_sync(0xffffffffu, sum, 4);
     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-
     if (live) {
-        const uint32_t packed = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) |
-                                ((uint32_t)(q2 & 0xff) << 16) | ((uint32_t)(q3 & 0xff) << 24);
         *reinterpret_cast<uint32_t *>(codes + m * K + 32 * b + 4 * sub) = packed;
-        if (sub == 0) {
-            const float s = __fmul_rn(d, (float)sum);
-            scales[blk] = __halves2half2(qk::f16_sat(d), qk::f16_sat(s));
-        }
+        if (sub == 0) scales[blk] = __halves2half2(qk::f16_sat(d), qk::q81_sum_f16(d, sum));
     }
 }
 
@@ -81,6 +65,11 @@ extern "C" int qk_quantize_q8_1(const float *x, int64_t ldx, int64_t M, int64_t 
     if (qk::overlaps(x, xbytes, codes, cbytes) || qk::overlaps(x, xbytes, scales, sbytes) ||
         qk::overlaps(codes, cbytes, scales, sbytes))
         return QK_E_ALIAS;
+    static std::atomic<int> carveout_set{0};
+    if (!carveout_set.load(std::memory_order_relaxed)) {
+        if (qk::max_carveout(quantize_q8_1_kernel) != cudaSuccess) return QK_E_CUDA;
+        carveout_set.store(1, std::memory_order_relaxed);
+    }
     const int nb_row = (int)(K / 32);
     const int64_t nblocks = M * nb_row;
     const int64_t grid = (nblocks + kThreads / 8 - 1) / (kThreads / 8);

@@ -73,12 +73,28 @@ def test_gemv_rejects(L, fn):
     assert call_gemv(L, fn, M=0) == E_SHAPE
     assert call_gemv(L, fn, M=9) == E_SHAPE
     assert call_gemv(L, fn, N=0) == E_SHAPE
-    assert call_gemv(L, fn, M=8, K=256 * 81) == E_SHAPE           # activation too large for shared memory
+    assert call_gemv(L, fn, M=8, K=256 * (41 if fn == "qk_gemv_q4k" else 21)) == E_SHAPE   # activation too large
+    assert call_gemv(L, fn, M=8, K=256 * (40 if fn == "qk_gemv_q4k" else 20), y=None) == E_NULL  # at the limit
     assert call_gemv(L, fn, w=P + 8) == E_ALIGN
     assert call_gemv(L, fn, codes=P + 0x10000004) == E_ALIGN
     assert call_gemv(L, fn, y=P + 0x30000002) == E_ALIGN
     assert call_gemv(L, fn, y=P + 64) == E_ALIAS                   # y inside the weight
     assert call_gemv(L, fn, r=P + 0x30000000 + 4) == E_ALIAS       # residual partially overlaps y
+
+
+@pytest.mark.parametrize("fn", ["qk_gemv_q4k_f32", "qk_gemv_q6k_f32"])
+def test_gemv_f32_rejects(L, fn):
+    f = getattr(L, fn)
+    w, x, y, c, s = P, P + 0x10000000, P + 0x30000000, P + 0x40000000, P + 0x50000000
+    assert f(w, None, 256, 1, 64, 256, None, y, None, None, 0, None) == E_NULL
+    assert f(w, x, 256, 1, 64, 256, None, y, c, None, 0, None) == E_NULL              # codes_out without scales_out
+    assert f(w, x, 128, 1, 64, 256, None, y, None, None, 0, None) == E_SHAPE          # ldx < K
+    assert f(w, x, 256, 9, 64, 256, None, y, None, None, 0, None) == E_SHAPE
+    assert f(w, x + 4, 256, 1, 64, 256, None, y, None, None, 0, None) == E_ALIGN
+    assert f(w, x, 258, 2, 64, 256, None, y, None, None, 0, None) == E_ALIGN
+    assert f(w, x, 256, 1, 64, 256, None, y, c + 1, s, 0, None) == E_ALIGN
+    assert f(w, x, 256, 1, 64, 256, None, x + 64, None, None, 0, None) == E_ALIAS     # y inside x
+    assert f(w, x, 256, 1, 64, 256, None, y, x, s, 0, None) == E_ALIAS                # codes_out inside x
 
 
 def test_quantize_rejects(L):

@@ -24,23 +24,25 @@ def sample_rows(N, n=24, seed=0):
     return sorted(r for r in rows if 0 <= r < N)
 
 
-@pytest.mark.parametrize("cfg_id", [0, 1, 2, 3, 4])
-def test_config_full_size(cfg_id):
+@pytest.mark.parametrize("cfg_id,fused", [(0, True), (1, True), (2, True), (3, True), (1, False), (3, False),
+                                         (4, False)])
+def test_config_full_size(cfg_id, fused):
     import bench
     wl = bench.Workload(cfg_id, seed=0, copies=1)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        wl.step(0, pdl=True, stream=stream)
-        wl.step(0, pdl=True, stream=stream)          # twice: PDL chaining across steps
+        wl.step(0, pdl=True, stream=stream, fused=fused)
+        wl.step(0, pdl=True, stream=stream, fused=fused)          # twice: PDL chaining across steps
     torch.cuda.synchronize()
     cfg = wl.cfg
     q8 = {}
     for s, x in wl.host_x.items():
         c, d, sref = oracle.quantize_q8_1(x)
-        codes, scales = wl.q8[s]
-        sc = scales.cpu().numpy().view(np.uint16)
-        assert np.array_equal(codes.cpu().numpy(), c), s
-        assert np.array_equal(sc[:, :, 0], d) and np.array_equal(sc[:, :, 1], sref), s
+        if not fused:
+            codes, scales = wl.q8[s]
+            sc = scales.cpu().numpy().view(np.uint16)
+            assert np.array_equal(codes.cpu().numpy(), c), s
+            assert np.array_equal(sc[:, :, 0], d) and np.array_equal(sc[:, :, 1], sref), s
         q8[s] = (c, d)
     for (name, q, N, K, res, s) in cfg["gemms"]:
         y = wl.y[name].cpu().numpy()

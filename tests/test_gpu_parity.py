@@ -173,7 +173,8 @@ def test_gemv_edges(qt):
 
 @pytest.mark.parametrize("qt", ["q4k", "q6k"])
 def test_gemv_max_activation(qt):
-    M, K, N = 8, 20480, 40                      # M*K at the documented limit
+    M, N = 8, 40
+    K = 10240 if qt == "q4k" else 5120           # M*K at the documented limit
     w, wr = weights(qt, N, K, seed=31)
     x = synth.activations(M, K, seed=32)
     codes, scales = q8(x)
@@ -195,6 +196,66 @@ def test_gemv_deterministic_and_guard_band(qt):
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
     assert torch.all(guard[M * N:] == 1234.5)
+
+
+# ----------------------------------------------- GEMV, in-kernel quantization
+
+def gemv_f32(qt, *a, **kw):
+    return (qk.gemv_q4k_f32 if qt == "q4k" else qk.gemv_q6k_f32)(*a, **kw)
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("N,K", [(1, 256), (37, 2304), (300, 4096), (130, 256 * 11)])
+def test_gemv_f32_parity_and_codes(qt, M, N, K):
+    w, wr = weights(qt, N, K, seed=M + 2 * N + K)
+    x = synth.activations(M, K, seed=N + 1) * np.float32(2.0)
+    x[0, :32] = 0.0
+    codes, scales = qk.empty_q8_1(M, K)
+    y = gemv_f32(qt, wr, dev(x), N, K, codes_out=codes, scales_out=scales).cpu().numpy()
+    c_ref, d_ref, s_ref = oracle.quantize_q8_1(x)
+    sc = scales.cpu().numpy().view(np.uint16)
+    assert np.array_equal(codes.cpu().numpy(), c_ref)
+    assert np.array_equal(sc[:, :, 0], d_ref) and np.array_equal(sc[:, :, 1], s_ref)
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c_ref, d_ref)
+    check(y, y_ref, ab, what=f"{qt} f32 M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+@pytest.mark.parametrize("mode", ["separate", "inplace", "pdl", "strided"])
+def test_gemv_f32_residual(qt, mode):
+    M, N, K = 2, 515, 4096
+    w, wr = weights(qt, N, K, seed=61)
+    x = synth.activations(M, K, seed=62)
+    r = synth.residual(M, N, seed=63)
+    rt = dev(r)
+    if mode == "strided":
+        big = np.zeros((M, K + 64), np.float32)
+        big[:, :K] = x
+        xt = dev(big)[:, :K]
+    else:
+        xt = dev(x)
+    if mode == "inplace":
+        y = gemv_f32(qt, wr, xt, N, K, residual=rt, y=rt)
+    else:
+        y = gemv_f32(qt, wr, xt, N, K, residual=rt, pdl=(mode == "pdl"))
+    torch.cuda.synchronize()
+    c_ref, d_ref, _ = oracle.quantize_q8_1(x)
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c_ref, d_ref, residual=r)
+    check(y.cpu().numpy(), y_ref, ab, r, what=f"{qt} f32 residual {mode}")
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+def test_gemv_f32_matches_q8_path_bitwise(qt):
+    # same codes, same kernel body: the two front ends give identical outputs
+    M, N, K = 2, 700, 4096
+    w, wr = weights(qt, N, K, seed=71)
+    x = dev(synth.activations(M, K, seed=72))
+    codes, scales = qk.quantize_q8_1(x)
+    y1 = gemv(qt, wr, codes, scales, N, K)
+    y2 = gemv_f32(qt, wr, x, N, K)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
 
 
 # ----------------------------------------------------------------------- MMQ
