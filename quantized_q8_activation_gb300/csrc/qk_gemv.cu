@@ -140,7 +140,16 @@ __device__ void stage_act_q4k(const int8_t *__restrict__ codes, const __half2 *_
 }
 
 // Q6_K side data per (m, 16-value chunk): {d_a, -32 * d_a * sum(q_a)}, the
-// activation scale and the offset term of the weight codes' -32 bias (exact)
+// activation scale and the offset term of the weight codes' -32 bias (exact).
+// Within each 128-chunk step the entries are stored in the order the lanes
+// read them: chunk 16j + 8h + e + 2t (lane 4j+2h+e, quarter t) at 4*lane + t,
+// so a lane fetches its four entries with two conflict-free 16-byte loads.
+__device__ __forceinline__ int q6_side_pos(int c)
+{
+    const int lo = c & 127;
+    return (c & ~127) + ((((lo >> 4) << 2) + (((lo >> 3) & 1) << 1) + (lo & 1)) << 2) + ((lo >> 1) & 3);
+}
+
 template <int M, int NT>
 __device__ void stage_act_q6k(const int8_t *__restrict__ codes, const __half2 *__restrict__ scales, int K,
                               uint8_t *s_codes, float2 *s_c16)
@@ -151,7 +160,7 @@ __device__ void stage_act_q6k(const int8_t *__restrict__ codes, const __half2 *_
         const uint4 v = *reinterpret_cast<const uint4 *>(codes + (size_t)m * K + 16 * c);
         *reinterpret_cast<uint4 *>(s_codes + (size_t)m * K + 16 * swz(c)) = v;
         const float d = __low2float(scales[(size_t)m * (K >> 5) + (c >> 1)]);
-        s_c16[i] = make_float2(d, -32.0f * d * (float)sum16(v));
+        s_c16[m * nchunk + q6_side_pos(c)] = make_float2(d, -32.0f * d * (float)sum16(v));
     }
 }
 
@@ -199,7 +208,7 @@ __device__ void stage_quant(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
                         s_side[m * nb + b] = make_float2((b & 1) ? da * 0.0625f : da, da * (float)s32);
                     }
                 } else if ((sub & 3) == 0) {
-                    s_side[m * (K >> 4) + c] = make_float2(da, -32.0f * da * (float)s16);
+                    s_side[m * (K >> 4) + q6_side_pos(c)] = make_float2(da, -32.0f * da * (float)s16);
                 }
                 if (out) {
                     *reinterpret_cast<uint32_t *>(a.codes_out + (size_t)m * K + 4 * k4) = packed;
@@ -225,40 +234,24 @@ __device__ __forceinline__ float warp_sum(float v)
 
 // ------------------------------------------------------------ work split
 // Rows are taken in groups of P consecutive rows; an item is (group, step s),
-// the step-s bytes of the group's rows.  Bulk: while every warp of the grid
-// can get one, groups are dealt round robin over all W warps (warp w takes
-// groups w, w+W, ...), so at any time the grid streams one contiguous window
-// of the weight.  Tail: the remaining NG mod W groups are split into
-// contiguous ranges per CTA, and each CTA's tail items into equal (+-1)
-// contiguous ranges per warp.  A group whose steps all fall in one warp is
-// written directly; a tail group cut between warps leaves a partial per warp
-// in shared memory, combined in warp order when the CTA is done.
+// the step-s bytes of the group's rows.  Groups are dealt round robin over
+// the W warps of the grid (warp w takes groups w, w+W, ...), so at any time
+// the grid streams one contiguous window of the weight; each group is
+// finished by one warp, so no partial sums cross warps.  (A split of the
+// last round into equal item ranges per CTA, combined in shared memory, was
+// measured slower: it breaks the window into per-CTA streams.)
 struct ItemSeq {
     int64_t g;                     // current item: group g, step s
     int s;
-    int64_t bulk_left;             // bulk items left, the current one included
-    int64_t tail_g;                // first tail item of this warp
-    int tail_s;
-    int64_t W;
+    int64_t sb;                    // index of the group's first superblock (g * P * B)
+    int64_t W, gsb;                // groups per round, superblocks per group
     __device__ __forceinline__ void next(int nsteps)
     {
-        if (bulk_left > 0) {
-            if (++s == nsteps) s = 0, g += W;
-            if (--bulk_left == 0) g = tail_g, s = tail_s;
-        } else if (++s == nsteps) {
-            s = 0, ++g;
-        }
+        if (++s == nsteps) s = 0, g += W, sb += W * gsb;
     }
 };
 
 constexpr int P = kRowsPerItem;
-constexpr int kMaxM = 8;
-
-struct Part {                                              // per warp: up to two partial groups
-    float v[2][P][kMaxM];
-    long long g[2];
-};
-
 // ------------------------------------------------------------------ Q4_K
 // slot: [P][1024] code bytes of the step, then [P][8] 16-byte metadata records
 
@@ -281,25 +274,25 @@ struct Q4Ops {
         for (int i = 0; i < 4; i++) c.aoff[i] = 16 * ((4 * lane + i) ^ (lane & 7));
         return c;
     }
-    // copy item (group starting at row n, step s) into a ring slot; no per-lane register payload
-    __device__ static uint32_t issue(uint8_t *slot, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n, int s,
-                                     int lane)
+    // copy item (group with first superblock sb, first row n, step s) into a ring slot; no register payload
+    __device__ static uint32_t issue(uint8_t *slot, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n,
+                                     int64_t sb, int s, int lane)
     {
         const int nsb = min(8, B - 8 * s), G = 4 * nsb;
-        const uint8_t *meta = w + N * (int64_t)B * 128;
+        const uint8_t *src = w + (sb << 7) + 1024 * s;                      // codes plane
+        const uint8_t *meta = w + N * (int64_t)B * 128 + ((sb + 8 * s) << 4); // metadata plane
 #pragma unroll
         for (int r = 0; r < P; r++) {
             if (n + r < N) {
-                const uint8_t *src = w + (n + r) * (int64_t)B * 128 + 1024 * s;
                 uint8_t *dst = slot + r * Q4_CODES;
                 if (lane < G) {
                     qk::cp_async16(dst + 16 * lane, src + 16 * lane);
                     qk::cp_async16(dst + 16 * G + 16 * lane, src + 16 * G + 16 * lane);
                 }
-                if (lane < nsb)
-                    qk::cp_async16(slot + P * Q4_CODES + r * Q4_META + 16 * lane,
-                                        meta + ((n + r) * B + 8 * s + lane) * 16);
+                if (lane < nsb) qk::cp_async16(slot + P * Q4_CODES + r * Q4_META + 16 * lane, meta + 16 * lane);
             }
+            src += (int64_t)B * 128;
+            meta += (int64_t)B * 16;
         }
         return 0;
     }
@@ -387,28 +380,32 @@ struct Q6Ops {
     }
     // copy an item into a ring slot; returns this lane's binary16 d register:
     // lane 8r+j (j < nsb) holds d of superblock 8s+j of row r (2-byte records)
-    __device__ static uint32_t issue(uint8_t *slot, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n, int s,
-                                     int lane)
+    __device__ static uint32_t issue(uint8_t *slot, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n,
+                                     int64_t sb, int s, int lane)
     {
         uint32_t dv = 0;
         const int nsb = min(8, B - 8 * s), L = 4 * nsb;
-        const int64_t NB = N * (int64_t)B;
+        const int64_t NB = N * (int64_t)B, sbs = sb + 8 * s;
+        const uint8_t *ql = w + (sb << 7) + 1024 * s;
+        const uint8_t *qh = w + (NB << 7) + (sbs << 6);
+        const uint8_t *sc = w + NB * 192 + (sbs << 4);
+        const uint8_t *dp = w + NB * 208 + (sbs << 1);
 #pragma unroll
         for (int r = 0; r < P; r++) {
             if (n + r < N) {
-                const int64_t sb0 = (n + r) * B + 8 * s;
-                const uint8_t *src = w + (n + r) * (int64_t)B * 128 + 1024 * s;
                 uint8_t *dst = slot + r * Q6_QL;
                 if (lane < L) {
-                    qk::cp_async16(dst + 16 * lane, src + 16 * lane);
-                    qk::cp_async16(dst + 16 * L + 16 * lane, src + 16 * L + 16 * lane);
-                    qk::cp_async16(slot + P * Q6_QL + r * Q6_QH + 16 * lane, w + NB * 128 + sb0 * 64 + 16 * lane);
+                    qk::cp_async16(dst + 16 * lane, ql + 16 * lane);
+                    qk::cp_async16(dst + 16 * L + 16 * lane, ql + 16 * L + 16 * lane);
+                    qk::cp_async16(slot + P * Q6_QL + r * Q6_QH + 16 * lane, qh + 16 * lane);
                 }
-                if (lane < nsb)
-                    qk::cp_async16(slot + P * (Q6_QL + Q6_QH) + r * Q6_SC + 16 * lane,
-                                        w + NB * 192 + (sb0 + lane) * 16);
-                if ((lane >> 3) == r && (lane & 7) < nsb) dv = qk::ldg_stream2(w + NB * 208 + (sb0 + (lane & 7)) * 2);
+                if (lane < nsb) qk::cp_async16(slot + P * (Q6_QL + Q6_QH) + r * Q6_SC + 16 * lane, sc + 16 * lane);
+                if ((lane >> 3) == r && (lane & 7) < nsb) dv = qk::ldg_stream2(dp + 2 * (lane & 7));
             }
+            ql += (int64_t)B * 128;
+            qh += (int64_t)B * 64;
+            sc += (int64_t)B * 16;
+            dp += (int64_t)B * 2;
         }
         return dv;
     }
@@ -422,44 +419,94 @@ struct Q6Ops {
         for (int r = 0; r < P; r++)
             d[r] = __half2float(__ushort_as_half((unsigned short)__shfl_sync(0xffffffffu, dreg, 8 * r + (lane >> 2))));
         if (lane >= L) return;
-        // 6-bit codes u = low4 | high2 << 4 in [0, 63]; the -32 offset comes with the staged block sums
-        uint32_t u[P][4][4];
+        uint4 qa[P], qb[P], qhh[P];
         float dsc[P][4];
 #pragma unroll
         for (int r = 0; r < P; r++) {
-            const uint4 a = lds16(sl + r * Q6_QL + 16 * lane), b = lds16(sl + r * Q6_QL + 16 * L + 16 * lane);
-            const uint4 h = lds16(sl + P * Q6_QL + r * Q6_QH + 16 * lane);
+            qa[r] = lds16(sl + r * Q6_QL + 16 * lane);
+            qb[r] = lds16(sl + r * Q6_QL + 16 * L + 16 * lane);
+            qhh[r] = lds16(sl + P * Q6_QL + r * Q6_QH + 16 * lane);
             const uint32_t scw =
                 *reinterpret_cast<const uint32_t *>(sl + P * (Q6_QL + Q6_QH) + r * Q6_SC + 4 * lane);
 #pragma unroll
             for (int t = 0; t < 4; t++) dsc[r][t] = d[r] * (float)(int)(int8_t)(scw >> (8 * t));
-            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w}, hw[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-            for (int j = 0; j < 4; j++) {
-                u[r][0][j] = (aw[j] & 0x0F0F0F0Fu) | ((hw[j] << 4) & 0x30303030u);
-                u[r][1][j] = (bw[j] & 0x0F0F0F0Fu) | ((hw[j] << 2) & 0x30303030u);
-                u[r][2][j] = ((aw[j] >> 4) & 0x0F0F0F0Fu) | (hw[j] & 0x30303030u);
-                u[r][3][j] = ((bw[j] >> 4) & 0x0F0F0F0Fu) | ((hw[j] >> 2) & 0x30303030u);
-            }
         }
         const uint8_t *abase = s_codes + 2048 * s;
-        const float2 *cbase = s_c16 + 128 * s;
+        const float4 *cbase = reinterpret_cast<const float4 *>(s_c16 + 128 * s + 4 * lane);
         const int nc = K >> 4;
+        if (M <= 2) {
+            // u = low4 + 16*high2: each part is dotted with its bits masked in place and the power-of-two
+            // factor restored on the integer sums (2 logic ops + 2 dp4a per word, no shifts)
 #pragma unroll
-        for (int m = 0; m < M; m++) {
-            const uint8_t *ar = abase + (size_t)m * K;
-            const float2 *cr = cbase + (size_t)m * nc;
+            for (int m = 0; m < M; m++) {
+                const uint8_t *ar = abase + (size_t)m * K;
+                const float4 c01 = cbase[(size_t)m * nc / 2], c23 = cbase[(size_t)m * nc / 2 + 1];
+                const float2 dc[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w),
+                                      make_float2(c23.x, c23.y), make_float2(c23.z, c23.w)};
+                uint4 av[4];
 #pragma unroll
-            for (int t = 0; t < 4; t++) {
-                const uint4 av = lds16(ar + lc.qoff[t]);
-                const float2 dc = cr[lc.coff[t]];                    // d_a * (dot - 32 * sum q_a)
+                for (int t = 0; t < 4; t++) av[t] = lds16(ar + lc.qoff[t]);
 #pragma unroll
                 for (int r = 0; r < P; r++) {
-                    int dot = qk::dp4a_ss(u[r][t][0], av.x, 0);
-                    dot = qk::dp4a_ss(u[r][t][1], av.y, dot);
-                    dot = qk::dp4a_ss(u[r][t][2], av.z, dot);
-                    dot = qk::dp4a_ss(u[r][t][3], av.w, dot);
-                    acc[r][m] = fmaf(dsc[r][t], fmaf(dc.x, (float)dot, dc.y), acc[r][m]);
+                    const uint32_t aw[4] = {qa[r].x, qa[r].y, qa[r].z, qa[r].w};
+                    const uint32_t bw[4] = {qb[r].x, qb[r].y, qb[r].z, qb[r].w};
+                    const uint32_t hw[4] = {qhh[r].x, qhh[r].y, qhh[r].z, qhh[r].w};
+                    int n0 = 0, h0 = 0, n1 = 0, h1 = 0, n2 = 0, h2 = 0, n3 = 0, h3 = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint32_t x0 = (&av[0].x)[j], x1 = (&av[1].x)[j], x2 = (&av[2].x)[j], x3 = (&av[3].x)[j];
+                        n0 = qk::dp4a_ss(aw[j] & 0x0F0F0F0Fu, x0, n0);   // low4 of quarter 0
+                        h0 = qk::dp4a_ss(hw[j] & 0x03030303u, x0, h0);   // high2 of quarter 0
+                        n1 = qk::dp4a_ss(bw[j] & 0x0F0F0F0Fu, x1, n1);
+                        h1 = qk::dp4a_ss(hw[j] & 0x0C0C0C0Cu, x1, h1);   // = 4 * high2
+                        n2 = qk::dp4a_us(aw[j] & 0xF0F0F0F0u, x2, n2);   // = 16 * low4
+                        h2 = qk::dp4a_ss(hw[j] & 0x30303030u, x2, h2);   // = 16 * high2
+                        n3 = qk::dp4a_us(bw[j] & 0xF0F0F0F0u, x3, n3);   // = 16 * low4
+                        h3 = qk::dp4a_us(hw[j] & 0xC0C0C0C0u, x3, h3);   // = 64 * high2
+                    }
+                    const int u0 = n0 + 16 * h0, u1 = n1 + 4 * h1;     // sum of u * q_a
+                    const int u2 = n2 + 16 * h2, u3 = n3 + 4 * h3;     // 16 * sum of u * q_a
+                    float t = acc[r][m];
+                    t = fmaf(dsc[r][0], fmaf(dc[0].x, (float)u0, dc[0].y), t);
+                    t = fmaf(dsc[r][1], fmaf(dc[1].x, (float)u1, dc[1].y), t);
+                    t = fmaf(dsc[r][2], fmaf(dc[2].x * 0.0625f, (float)u2, dc[2].y), t);
+                    t = fmaf(dsc[r][3], fmaf(dc[3].x * 0.0625f, (float)u3, dc[3].y), t);
+                    acc[r][m] = t;
+                }
+            }
+        } else {
+            // 6-bit codes u = low4 | high2 << 4 in [0, 63] built once and reused for every row m
+            uint32_t u[P][4][4];
+#pragma unroll
+            for (int r = 0; r < P; r++) {
+                const uint32_t aw[4] = {qa[r].x, qa[r].y, qa[r].z, qa[r].w};
+                const uint32_t bw[4] = {qb[r].x, qb[r].y, qb[r].z, qb[r].w};
+                const uint32_t hw[4] = {qhh[r].x, qhh[r].y, qhh[r].z, qhh[r].w};
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    u[r][0][j] = (aw[j] & 0x0F0F0F0Fu) | ((hw[j] << 4) & 0x30303030u);
+                    u[r][1][j] = (bw[j] & 0x0F0F0F0Fu) | ((hw[j] << 2) & 0x30303030u);
+                    u[r][2][j] = ((aw[j] >> 4) & 0x0F0F0F0Fu) | (hw[j] & 0x30303030u);
+                    u[r][3][j] = ((bw[j] >> 4) & 0x0F0F0F0Fu) | ((hw[j] >> 2) & 0x30303030u);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < M; m++) {
+                const uint8_t *ar = abase + (size_t)m * K;
+                const float4 c01 = cbase[(size_t)m * nc / 2], c23 = cbase[(size_t)m * nc / 2 + 1];
+                const float2 dc[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w),
+                                      make_float2(c23.x, c23.y), make_float2(c23.z, c23.w)};
+#pragma unroll
+                for (int t = 0; t < 4; t++) {
+                    const uint4 av = lds16(ar + lc.qoff[t]);
+#pragma unroll
+                    for (int r = 0; r < P; r++) {
+                        int dot = qk::dp4a_ss(u[r][t][0], av.x, 0);
+                        dot = qk::dp4a_ss(u[r][t][1], av.y, dot);
+                        dot = qk::dp4a_ss(u[r][t][2], av.z, dot);
+                        dot = qk::dp4a_ss(u[r][t][3], av.w, dot);
+                        acc[r][m] = fmaf(dsc[r][t], fmaf(dc[t].x, (float)dot, dc[t].y), acc[r][m]);
+                    }
                 }
             }
         }
@@ -486,28 +533,19 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
     uint8_t *ring = smem + warp * (R * Ops::SLOT);
     uint8_t *s_codes = smem + kWarps * R * Ops::SLOT;
     float2 *s_side = reinterpret_cast<float2 *>(s_codes + (size_t)M * K);
-    Part *part = reinterpret_cast<Part *>(s_codes + (size_t)M * K + (size_t)M * (K >> 5) * Ops::SIDE_PER_32);
     const typename Ops::LaneConst lc = Ops::lane_const(lane);
 
-    // bulk rounds of groups over all W warps, then this CTA's tail groups [ga, gb)
-    // and this warp's tail items [ia, ib) (tail item = group*nsteps + step)
+    // this warp's items: groups wg0, wg0+W, ... below NG, each with steps 0..nsteps-1
     const int64_t NG = (N + P - 1) / P;
     const int64_t W = (int64_t)gridDim.x * kWarps, wg0 = (int64_t)blockIdx.x * kWarps + warp;
-    const int64_t rounds = NG / W, tail0 = rounds * W, NT = NG - tail0;
-    const int64_t ga = tail0 + (int64_t)blockIdx.x * NT / gridDim.x;
-    const int64_t gb = tail0 + ((int64_t)blockIdx.x + 1) * NT / gridDim.x;
-    const int64_t T = (gb - ga) * nsteps;
-    const int64_t ia = (int64_t)warp * T / kWarps, ib = ((int64_t)warp + 1) * T / kWarps;
-    const int64_t total = rounds * nsteps + (ib - ia);
+    const int64_t total = wg0 < NG ? ((NG - 1 - wg0) / W + 1) * nsteps : 0;
     ItemSeq rd;
     rd.W = W;
-    rd.tail_g = ga + ia / nsteps;
-    rd.tail_s = (int)(ia % nsteps);
-    rd.bulk_left = rounds * nsteps;
-    rd.g = rounds > 0 ? wg0 : rd.tail_g;
-    rd.s = rounds > 0 ? 0 : rd.tail_s;
+    rd.gsb = (int64_t)P * B;
+    rd.g = wg0;
+    rd.s = 0;
+    rd.sb = wg0 * rd.gsb;
     ItemSeq wr = rd;
-    if (lane == 0) part[warp].g[0] = part[warp].g[1] = -1;
 
     // weights never depend on the previous kernel: the first R-1 items are
     // requested before waiting for it
@@ -516,7 +554,7 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
 #pragma unroll
     for (int j = 0; j < R - 1; j++) {
         reg[j] = 0;
-        if (wi < total) reg[j] = Ops::issue(ring + j * Ops::SLOT, w, N, B, P * wr.g, wr.s, lane);
+        if (wi < total) reg[j] = Ops::issue(ring + j * Ops::SLOT, w, N, B, P * wr.g, wr.sb, wr.s, lane);
         qk::cp_async_commit();
         wr.next(nsteps);
         ++wi;
@@ -532,12 +570,10 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
 #pragma unroll
         for (int m = 0; m < M; m++) acc[r][m] = 0.0f;
 
-    bool whole = rd.s == 0;             // this warp saw the current group's first step
-    int np = 0;                         // partial groups stored so far
     int slot = 0, wslot = R - 1;
     for (int64_t k = 0; k < total; k++) {
         uint32_t rnew = 0;
-        if (wi < total) rnew = Ops::issue(ring + wslot * Ops::SLOT, w, N, B, P * wr.g, wr.s, lane);
+        if (wi < total) rnew = Ops::issue(ring + wslot * Ops::SLOT, w, N, B, P * wr.g, wr.sb, wr.s, lane);
         qk::cp_async_commit();
         wr.next(nsteps);
         ++wi;
@@ -545,8 +581,8 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
         __syncwarp();
         Ops::template compute<M>(ring + slot * Ops::SLOT, rd.s, B, lane, reg[0], lc, s_codes, s_side, K, acc);
         __syncwarp();
-        const bool last_step = rd.s == nsteps - 1;
-        if (last_step || k == total - 1) {
+        if (rd.s == nsteps - 1) {
+            // fixed xor tree over the lanes, then lane m writes output m of each row of the group
 #pragma unroll
             for (int r = 0; r < P; r++)
 #pragma unroll
@@ -554,22 +590,13 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
                     const float v = warp_sum(acc[r][m]);
                     acc[r][m] = 0.0f;
                     const int64_t n = P * rd.g + r;
-                    if (whole && last_step) {
-                        if (lane == m && n < N) {
-                            const size_t o = (size_t)m * N + n;
-                            a.y[o] = a.residual ? __fadd_rn(v, a.residual[o]) : v;
-                        }
-                    } else if (lane == 0) {
-                        part[warp].v[np][r][m] = v;
+                    if (lane == m && n < N) {
+                        const size_t o = (size_t)m * N + n;
+                        a.y[o] = a.residual ? __fadd_rn(v, a.residual[o]) : v;
                     }
                 }
-            if (!(whole && last_step)) {
-                if (lane == 0) part[warp].g[np] = rd.g;
-                ++np;
-            }
         }
         rd.next(nsteps);
-        if (last_step || k == total - 1) whole = rd.s == 0;
 #pragma unroll
         for (int j = 0; j < R - 2; j++) reg[j] = reg[j + 1];
         reg[R - 2] = rnew;
@@ -577,31 +604,6 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
         slot = slot + 1 == R ? 0 : slot + 1;
     }
     qk::cp_async_wait<0>();
-    __syncthreads();
-    // groups cut between warps: sum their partials in warp order
-    if (warp == 0 && lane < M * P) {
-        const int m = lane / P, r = lane % P;
-        long long cur = -1;
-        float sum = 0.0f;
-        for (int ww = 0; ww < kWarps; ww++)
-            for (int k = 0; k < 2; k++) {
-                const long long gg = part[ww].g[k];
-                if (gg < 0) continue;
-                if (gg != cur) {
-                    if (cur >= 0 && P * cur + r < N) {
-                        const size_t o = (size_t)m * N + (size_t)(P * cur + r);
-                        a.y[o] = a.residual ? __fadd_rn(sum, a.residual[o]) : sum;
-                    }
-                    cur = gg;
-                    sum = 0.0f;
-                }
-                sum += part[ww].v[k][r][m];
-            }
-        if (cur >= 0 && P * cur + r < N) {
-            const size_t o = (size_t)m * N + (size_t)(P * cur + r);
-            a.y[o] = a.residual ? __fadd_rn(sum, a.residual[o]) : sum;
-        }
-    }
     if (QK_GEMV_TRIGGER == 2) qk::pdl_launch_dependents();
 }
 
@@ -688,17 +690,17 @@ int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, uns
                          qk::overlaps(a.scales_out, sbytes, a.residual, ybytes)))))
         return QK_E_ALIAS;
     const int warps = warps_for((int)M, fused);
-    // ring | activation codes | side data | per-warp partials
+    // ring | activation codes | side data
     const size_t smem = (size_t)warps * (qtype == QK_TYPE_Q4_K ? Q4_R * Q4_SLOT : Q6_R * Q6_SLOT) +
-                        (size_t)M * K + (size_t)M * (K / 32) * (qtype == QK_TYPE_Q4_K ? 8 : 16) +
-                        (size_t)warps * sizeof(Part);
+                        (size_t)M * K + (size_t)M * (K / 32) * (qtype == QK_TYPE_Q4_K ? 8 : 16);
     if (smem > qk::max_smem_optin()) return QK_E_SHAPE;
     gemv_fn kern = fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M);
     int st = prepare(kern, g_smem_set[qtype == QK_TYPE_Q4_K ? 0 : 1][fused ? 1 : 0][M - 1], smem);
     if (st != QK_OK) return st;
     int64_t grid = (int64_t)kCtasPerSm * qk::sm_count();
     const int64_t groups = (N + kRowsPerItem - 1) / kRowsPerItem;
-    if (grid > groups) grid = groups;                               // every CTA gets a group at least
+    const int64_t need = (groups + warps - 1) / warps;              // CTAs that get a group in the first round
+    if (grid > need) grid = need;
     a.N = N;
     a.K = (int)K;
     return qk::launch(kern, dim3((unsigned)grid), dim3(warps * 32), smem, (cudaStream_t)stream,
