@@ -219,6 +219,19 @@ int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales,
                void *workspace, size_t workspace_bytes,
                unsigned flags, void *stream);
 
+/* ========================================================== error flags
+ * Kernels that hand work between warps with mbarriers (qk_mmq_q4k) bound
+ * every wait.  A wait that gives up -- which only happens if the hardware or
+ * the kernel misbehaves -- sets bit QK_ERR_TIMEOUT of a device-wide flag
+ * word; the kernel then skips its remaining waits and returns, and its output
+ * is undefined.  qk_error_flags copies that word to *flags (synchronously,
+ * on the current device) and, when `clear` is non-zero, resets it to 0.
+ * Not part of the method: library bookkeeping only.
+ * Returns QK_E_NULL if flags is NULL, QK_E_CUDA if the copy fails.
+ */
+#define QK_ERR_TIMEOUT 1u
+int qk_error_flags(unsigned *flags, int clear);
+
 #ifdef __cplusplus
 }
 #endif

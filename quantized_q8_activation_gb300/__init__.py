@@ -34,7 +34,7 @@ STATUS = {0: "QK_OK", -1: "QK_E_NULL", -2: "QK_E_SHAPE", -3: "QK_E_ALIGN", -4: "
 # every symbol include/qk.h declares
 EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1", "qk_repacked_bytes",
            "qk_repack", "qk_gemv_q4k", "qk_gemv_q6k", "qk_gemv_q4k_f32", "qk_gemv_q6k_f32",
-           "qk_mmq_workspace_bytes", "qk_mmq_q4k"]
+           "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_error_flags"]
 
 _lib = None
 _lock = threading.Lock()
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             L.qk_gemv_q6k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
             L.qk_mmq_workspace_bytes.argtypes = [i64, i64, i64, szp]
             L.qk_mmq_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
+            L.qk_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
             for name in EXPORTS:
                 getattr(L, name).restype = ctypes.c_int if name != "qk_status_string" else ctypes.c_char_p
             _lib = L
@@ -129,6 +130,13 @@ def mmq_workspace_bytes(M: int, N: int, K: int) -> int:
     b = ctypes.c_size_t()
     _check(lib().qk_mmq_workspace_bytes(M, N, K, ctypes.byref(b)), "qk_mmq_workspace_bytes")
     return b.value
+
+
+def error_flags(clear: bool = True) -> int:
+    """Device error word (bit 0: a bounded in-kernel wait gave up); cleared when `clear`."""
+    f = ctypes.c_uint()
+    _check(lib().qk_error_flags(ctypes.byref(f), int(clear)), "qk_error_flags")
+    return f.value
 
 
 # --------------------------------------------------------------- operations

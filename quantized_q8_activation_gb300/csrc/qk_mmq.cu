@@ -1,215 +1,378 @@
-// qk_mmq.cu -- prefill contraction Y[M][N] = X_q8 . W_q4k^T (+ R).
+// qk_mmq.cu -- prefill contraction Y[M][N] = Xq8 . W_q4k^T (+ R) on the
+// sm_103a tensor cores (tcgen05, accumulators in tensor memory).
 //
-// Integer-exact tensor-core MMQ: the raw 4-bit Q4_K codes and the int8 q8_1
-// codes are the MMA operands; each 32-value sub-block's int32 products are
-// scaled by d_a * d * sc and the min term d_a * sum(q_a) * dmin * m is
-// subtracted, in binary32, outside the integer accumulation (minfer
-// "15 . The CUDA backend" sec. 2.3: weights stay quantized, raw block bytes
-// are staged to shared memory and decoded in registers next to the
-// mma.m16n8k32 int8 instruction, float scales folded outside the integer
-// loop).
+// Method (minfer "15 . The CUDA backend" sec. 2.3 / 3.2.6: quantized weight
+// bytes go straight to the tensor cores, float scales are folded outside the
+// integer accumulation).  This part runs integer MMA far below its f16 rate,
+// so the contraction uses kind::f16 with operands that are exact:
+//   B[n][k] = sc_j * q_w        an integer <= 945, exact in f16;
+//   A[m][k] = d_a * q_a = A_hi + A_lo, two f16 values whose sum is exact
+//             (d_a has 11 significant bits and q_a 7, so the product needs
+//             18 <= 2 x 11 bits);
+// the products and their binary32 sums over one 256-value superblock are
+// accumulated by the tensor core into T (tensor memory), then folded with the
+// superblock scale:  Y += d_b[n] * T.  The min term
+//   - sum_b,j dmin_b m_j d_a sum(q_a)  = - S . Mw^T,
+//   S[m][b,j] = d_a sum(q_a) / 16,   Mw[n][b,j] = 16 dmin_b m_j
+// (the power-of-two factors keep both in f16 range) is a second contraction
+// with K/32 terms on the tensor core too: each superblock adds K = 16 MMAs
+// (8 values + 8 zeros) of S (hi/lo) against Mw (hi/lo) into U.  The result is
+// Y - U (+ R).
 //
-// Tile: 64 activation rows x 128 weight rows per CTA (8 warps, 2 x 4, each
-// 32 x 32), one 256-value superblock per pipeline stage, two stages of
-// cp.async staging.  The weight tile is staged straight from the repacked
-// planes (two 64-byte runs of codes and the 16-byte scale record per row).
+// One CTA (16 warps) per 128 x 128 output tile and per SM (all 512 TMEM
+// columns: Y | T0 | T1 | U):
+//   warp 0      TMEM allocation; lane 0 issues every MMA and commit
+//   warps 4-7   fold T into Y per superblock, then the epilogue (TMEM lane
+//               quadrant = warp % 4)
+//   warps 8-15  operand converters: q8_1 codes + d_a -> A_hi / A_lo and Q4_K
+//               codes + scales -> B per 64-value K stage, written straight
+//               into the UMMA K-major SWIZZLE_128B layout; S and Mw into
+//               SWIZZLE_32B tiles once per superblock
+// Stages are handed over with mbarriers (full: converters -> MMA; empty: MMA
+// commit -> converters; T buffers: MMA commit -> fold, fold -> MMA).  Every
+// wait is bounded; a wait that gives up sets a device error flag
+// (qk_error_flags) and the kernel runs to its end without further waiting.
 #include "qk_common.cuh"
+#include "qk_tc.cuh"
 
 #include <atomic>
 
+__device__ unsigned g_qk_errors;
+
 namespace {
 
-constexpr int BM = 64, BN = 128, kThreads = 256;
-constexpr int A_STRIDE = 272;                 // 256 codes + 16 pad: conflict-free fragment reads
-constexpr int W_STRIDE = 144;                 // 128 codes + 16 meta
-constexpr int A_BYTES = BM * A_STRIDE;        // 17408
-constexpr int W_BYTES = BN * W_STRIDE;        // 18432
-constexpr int STAGE = A_BYTES + W_BYTES;      // 35840
-constexpr int SIDE_W = BN * 8 * 8;            // float2 {d*sc, dmin*m} per (row, sub-block)
-constexpr int SIDE_A = BM * 8 * 8;            // float2 {d_a, d_a*sum q_a} per (row, sub-block)
-constexpr int SMEM = 2 * STAGE + SIDE_W + SIDE_A;
+using namespace qk::tc;
 
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void *g, int bytes)
+constexpr int BM = 128, BN = 128, BK = 64;      // BK: one Q4_K group = two 32-value sub-blocks
+constexpr int NST = 3;                          // operand stages in flight
+constexpr int kThreads = 512;
+constexpr int kFoldWarp0 = 4, kConvWarp0 = 8;
+constexpr int kConv = 256, kFold = 128;
+
+constexpr int TILE = BM * BK * 2;               // 16 KB: 128 rows x 64 f16, SWIZZLE_128B K-major
+constexpr int STAGE = 3 * TILE;                 // A_hi | A_lo | B
+constexpr int MTILE = 128 * 16 * 2;             // 4 KB: 128 rows x 16 f16, SWIZZLE_32B K-major
+constexpr int MSET = 4 * MTILE;                 // S_hi | S_lo | Mw_hi | Mw_lo
+constexpr int OFF_MIN = NST * STAGE;
+constexpr int OFF_DB = OFF_MIN + 2 * MSET;      // fold: d_b of the tile's columns, 2 x 128 floats
+constexpr int OFF_BAR = OFF_DB + 2 * 128 * 4;
+enum { B_FULL = 0, B_EMPTY = NST, B_MINEMPTY = 2 * NST, B_TFULL = 2 * NST + 2, B_TEMPTY = 2 * NST + 4,
+       NBAR = 2 * NST + 6 };
+constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+constexpr int SMEM = OFF_TMEM + 16 + 1024;      // + slack to align the base to 1024
+constexpr uint32_t COL_Y = 0, COL_T0 = 128, COL_U = 384, TMEM_COLS = 512;
+constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
+
+// byte offset of 16-byte chunk c of row r in a SWIZZLE_128B K-major tile (rows of 128 bytes)
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4); }
+// byte offset of element j (< 8, first 16-byte chunk) of row r in a SWIZZLE_32B K-major tile (rows of 32 bytes)
+__device__ __forceinline__ uint32_t sw32(int r, int j) { return (r >> 3) * 256 + (r & 7) * 32 + (((r >> 2) & 1) << 4) + 2 * j; }
+
+__device__ __forceinline__ bool give_up() { return (*(volatile unsigned *)&g_qk_errors & kErrTimeout) != 0; }
+
+__device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity)
 {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "r"(bytes) : "memory");
+    if (!give_up()) mbar_wait(bar, parity, &g_qk_errors);
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-__device__ __forceinline__ void mma_s8(int (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                       uint32_t b0, uint32_t b1)
-{
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
+__device__ __forceinline__ void bar_fold() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// issue the cp.async copies of superblock sb into stage buffer `st`
-__device__ __forceinline__ void load_stage(uint8_t *smem, int st, const uint8_t *__restrict__ w,
-                                           const int8_t *__restrict__ codes, int64_t M, int64_t N, int64_t K,
-                                           int64_t m0, int64_t n0, int sb)
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+struct MmqArgs {
+    const uint8_t *w;
+    const int8_t *codes;
+    const __half2 *scales;
+    int64_t M, N, K;
+    const float *residual;
+    float *y;
+};
+
+// one converter thread's raw inputs of one K stage (stage it = superblock it/4, group it%4)
+struct Raw {
+    uint4 a0, a1;          // 32 activation codes: row m, k = 64g + 32h .. +31 of the superblock
+    uint32_t da;           // q8_1 scale pair (d, s) of that 32-value block, binary16 bits
+    uint4 b;               // 16 Q4_K code bytes: row n, half h of group g
+    uint4 mt;              // 16-byte metadata record of (row n, superblock)
+};
+
+__device__ __forceinline__ void load_raw(Raw &r, const MmqArgs &a, int64_t m, int64_t n, int it, int h)
 {
-    const int B = (int)(K >> 8);
-    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem + st * STAGE);
-    // activation: 64 rows x 256 bytes = 1024 chunks
-    for (int i = threadIdx.x; i < BM * 16; i += kThreads) {
-        const int r = i >> 4, c = i & 15;
-        const int64_t m = m0 + r;
-        const bool ok = m < M;
-        const int8_t *src = codes + (ok ? m : 0) * K + (int64_t)sb * 256 + 16 * c;
-        cp_async16(sbase + r * A_STRIDE + 16 * c, src, ok ? 16 : 0);
+    const int B = (int)(a.K >> 8);
+    const int sb = it >> 2, g = it & 3;
+    if (m < a.M) {
+        const int8_t *src = a.codes + m * a.K + sb * 256 + g * 64 + 32 * h;
+        r.a0 = *reinterpret_cast<const uint4 *>(src);
+        r.a1 = *reinterpret_cast<const uint4 *>(src + 16);
+        r.da = *reinterpret_cast<const uint32_t *>(a.scales + m * (a.K >> 5) + sb * 8 + 2 * g + h);
+    } else {
+        r.a0 = r.a1 = make_uint4(0, 0, 0, 0);
+        r.da = 0;
     }
-    // weights: 128 rows x (4 half-0 chunks, 4 half-1 chunks, 1 meta chunk)
-    const int s = sb >> 3, nsb = min(8, B - 8 * s), G = 4 * nsb, loc = sb - 8 * s;
-    for (int i = threadIdx.x; i < BN * 9; i += kThreads) {
-        const int r = i / 9, c = i - 9 * r;
-        const int64_t n = n0 + r;
-        const bool ok = n < N;
-        const int64_t nn = ok ? n : 0;
-        const uint8_t *src;
-        if (c < 4)
-            src = w + nn * B * 128 + 1024 * s + 16 * (4 * loc + c);
-        else if (c < 8)
-            src = w + nn * B * 128 + 1024 * s + 16 * G + 16 * (4 * loc + c - 4);
-        else
-            src = w + N * (int64_t)B * 128 + (nn * B + sb) * 16;
-        cp_async16(sbase + A_BYTES + r * W_STRIDE + 16 * c, src, ok ? 16 : 0);
+    if (n < a.N) {
+        const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s) + g;
+        const uint8_t *row = a.w + n * (int64_t)B * 128 + 1024 * s;
+        r.b = qk::ldg_stream16(row + (h ? 16 * G + 16 * u : 16 * u));
+        r.mt = qk::ldg_stream16(a.w + a.N * (int64_t)B * 128 + (n * B + sb) * 16);
+    } else {
+        r.b = r.mt = make_uint4(0, 0, 0, 0);
     }
 }
 
-__global__ void __launch_bounds__(kThreads) mmq_q4k_kernel(const uint8_t *__restrict__ w,
-                                                           const int8_t *__restrict__ codes,
-                                                           const __half2 *__restrict__ scales, int64_t M,
-                                                           int64_t N, int64_t K, const float *residual, float *y)
+// 4 int8 codes -> (A_hi, A_lo) f16 pairs with A_hi + A_lo = d * q exactly
+__device__ __forceinline__ void conv_a(uint32_t w4, __half2 d2, uint32_t &hi01, uint32_t &lo01, uint32_t &hi23,
+                                       uint32_t &lo23)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
-    float2 *side_w = reinterpret_cast<float2 *>(smem + 2 * STAGE);
-    float2 *side_a = reinterpret_cast<float2 *>(smem + 2 * STAGE + SIDE_W);
-    const int B = (int)(K >> 8);
-    const int64_t n0 = (int64_t)blockIdx.x * BN, m0 = (int64_t)blockIdx.y * BM;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int wm = warp >> 2, wn = warp & 3;     // warp tile origin: rows 32*wm, cols 32*wn
-    const int g = lane >> 2, t = lane & 3;
+    // each byte to 1024 + (q + 128) in an f16 lane, then subtract 1152
+    const uint32_t x = w4 ^ 0x80808080u;
+    const __half2 k1152 = u2h(0x64806480u);
+    const __half2 q01 = __hsub2(u2h(__byte_perm(x, 0x64646464u, 0x5140)), k1152);
+    const __half2 q23 = __hsub2(u2h(__byte_perm(x, 0x64646464u, 0x7362)), k1152);
+    const __half2 h01 = __hmul2(q01, d2), h23 = __hmul2(q23, d2);
+    hi01 = h2u(h01);
+    hi23 = h2u(h23);
+    lo01 = h2u(__hfma2(q01, d2, __hneg2(h01)));    // exact remainder d*q - hi
+    lo23 = h2u(__hfma2(q23, d2, __hneg2(h23)));
+}
 
-    qk::pdl_wait();
+// 4 code bytes -> (low nibble * sc_lo) and (high nibble * sc_hi) as f16 pairs (exact integers)
+__device__ __forceinline__ void conv_b(uint32_t w4, __half2 sl, __half2 sl1024, __half2 sh, __half2 sh64,
+                                       uint32_t &l01, uint32_t &l23, uint32_t &h01, uint32_t &h23)
+{
+    const uint32_t p01 = __byte_perm(w4, 0, 0x4140), p23 = __byte_perm(w4, 0, 0x4342);
+    // 1024 + q (low nibble) and 64 + q (high nibble, which sits 16x in its byte)
+    l01 = h2u(__hfma2(u2h((p01 & 0x000F000Fu) | 0x64006400u), sl, sl1024));
+    l23 = h2u(__hfma2(u2h((p23 & 0x000F000Fu) | 0x64006400u), sl, sl1024));
+    h01 = h2u(__hfma2(u2h((p01 & 0x00F000F0u) | 0x54005400u), sh, sh64));
+    h23 = h2u(__hfma2(u2h((p23 & 0x00F000F0u) | 0x54005400u), sh, sh64));
+}
+
+__device__ __forceinline__ void sts128(uint8_t *base, uint32_t off, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
+{
+    *reinterpret_cast<uint4 *>(base + off) = make_uint4(x, y, z, w);
+}
+
+__device__ __forceinline__ void split_f16(float v, __half &hi, __half &lo)
+{
+    hi = __float2half_rn(v);
+    lo = __float2half_rn(v - __half2float(hi));
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
+    float *dB = reinterpret_cast<float *>(smem + OFF_DB);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m0 = (int64_t)blockIdx.x * BM, n0 = (int64_t)blockIdx.y * BN;
+    const int B = (int)(a.K >> 8), nit = 4 * B;
+
     qk::pdl_launch_dependents();
-
-    float facc[2][4][4];
-#pragma unroll
-    for (int i = 0; i < 2; i++)
-#pragma unroll
-        for (int j = 0; j < 4; j++)
-#pragma unroll
-            for (int e = 0; e < 4; e++) facc[i][j][e] = 0.0f;
-
-    load_stage(smem, 0, w, codes, M, N, K, m0, n0, 0);
-    cp_commit();
-    for (int sb = 0; sb < B; sb++) {
-        const int st = sb & 1;
-        if (sb + 1 < B) load_stage(smem, st ^ 1, w, codes, M, N, K, m0, n0, sb + 1);
-        cp_commit();
-        cp_wait<1>();
-        __syncthreads();
-        const uint8_t *sa = smem + st * STAGE;
-        const uint8_t *sw = sa + A_BYTES;
-        // side data of this superblock
-        for (int i = threadIdx.x; i < BN * 8; i += kThreads) {
-            const int r = i >> 3, j = i & 7;
-            const uint32_t *mt = reinterpret_cast<const uint32_t *>(sw + r * W_STRIDE + 128);
-            const float d = __half2float(__ushort_as_half((unsigned short)(mt[0] & 0xffffu)));
-            const float dmin = __half2float(__ushort_as_half((unsigned short)(mt[0] >> 16)));
-            const uint8_t *rb = sw + r * W_STRIDE + 128 + 4 + 3 * (j >> 1);
-            const uint32_t rec = (uint32_t)rb[0] | ((uint32_t)rb[1] << 8) | ((uint32_t)rb[2] << 16);
-            const uint32_t sc = (j & 1) ? (rec >> 6) & 63u : rec & 63u;
-            const uint32_t mn = (j & 1) ? (rec >> 18) & 63u : (rec >> 12) & 63u;
-            side_w[i] = make_float2(d * (float)sc, dmin * (float)mn);
+    // setup: barriers, zero padding of the min-term tiles, TMEM allocation
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; i++) mbar_init(&bar[B_FULL + i], kConv), mbar_init(&bar[B_EMPTY + i], 1);
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&bar[B_MINEMPTY + i], 1);
+            mbar_init(&bar[B_TFULL + i], 1);
+            mbar_init(&bar[B_TEMPTY + i], kFold);
         }
-        for (int i = threadIdx.x; i < BM * 8; i += kThreads) {
-            const int r = i >> 3, j = i & 7;
-            const int64_t m = m0 + r;
-            float d = 0.0f, S = 0.0f;
-            if (m < M) {
-                const uint32_t *q = reinterpret_cast<const uint32_t *>(sa + r * A_STRIDE + 32 * j);
-                int s = 0;
-#pragma unroll
-                for (int k = 0; k < 8; k++) s = qk::dp4a_ss(q[k], 0x01010101u, s);
-                d = __low2float(scales[m * (K >> 5) + (int64_t)sb * 8 + j]);
-                S = d * (float)s;
-            }
-            side_a[i] = make_float2(d, S);
-        }
-        __syncthreads();
+        mbar_init_fence();
+    }
+    for (int i = threadIdx.x; i < 2 * MSET / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + OFF_MIN)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async();                         // the zero padding is read by the tensor core
+    if (warp == 0) {
+        tmem_alloc(tmem_ptr, TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_ptr;
+    qk::pdl_wait();
 
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t sbase = smem_u32(smem);
+            for (int sb = 0; sb < B; sb++) {
+                const int tb = sb & 1;
+                if (sb >= 2) wait_bar(&bar[B_TEMPTY + tb], ((sb - 2) >> 1) & 1);
+                fence_after_sync();
+                const uint32_t dT = tmem + COL_T0 + 128 * tb;
+                for (int g = 0; g < 4; g++) {
+                    const int it = 4 * sb + g, st = it % NST;
+                    wait_bar(&bar[B_FULL + st], (it / NST) & 1);
+                    fence_after_sync();
+                    const uint32_t s0 = sbase + st * STAGE;
 #pragma unroll
-        for (int gq = 0; gq < 4; gq++) {
-            // weight fragments for both sub-blocks of group gq: column g of each n8 tile
-            uint32_t blo[4][2], bhi[4][2];
-#pragma unroll
-            for (int nt = 0; nt < 4; nt++) {
-                const uint8_t *row = sw + (32 * wn + 8 * nt + g) * W_STRIDE;
-                const uint32_t h0 = *reinterpret_cast<const uint32_t *>(row + 16 * gq + 4 * t);
-                const uint32_t h1 = *reinterpret_cast<const uint32_t *>(row + 64 + 16 * gq + 4 * t);
-                blo[nt][0] = h0 & 0x0F0F0F0Fu, blo[nt][1] = h1 & 0x0F0F0F0Fu;
-                bhi[nt][0] = (h0 >> 4) & 0x0F0F0F0Fu, bhi[nt][1] = (h1 >> 4) & 0x0F0F0F0Fu;
+                    for (int kk = 0; kk < BK / 16; kk++) {
+                        const uint64_t ahi = smem_desc(s0 + 32 * kk, 16, 1024, kLayoutSw128);
+                        const uint64_t alo = smem_desc(s0 + TILE + 32 * kk, 16, 1024, kLayoutSw128);
+                        const uint64_t bd = smem_desc(s0 + 2 * TILE + 32 * kk, 16, 1024, kLayoutSw128);
+                        mma_f16(dT, ahi, bd, IDESC, (g | kk) != 0);
+                        mma_f16(dT, alo, bd, IDESC, 1);
+                    }
+                    mma_commit(&bar[B_EMPTY + st]);
+                }
+                const uint32_t ms = sbase + OFF_MIN + tb * MSET;
+                const uint64_t shi = smem_desc(ms, 16, 256, kLayoutSw32);
+                const uint64_t slo = smem_desc(ms + MTILE, 16, 256, kLayoutSw32);
+                const uint64_t whi = smem_desc(ms + 2 * MTILE, 16, 256, kLayoutSw32);
+                const uint64_t wlo = smem_desc(ms + 3 * MTILE, 16, 256, kLayoutSw32);
+                mma_f16(tmem + COL_U, shi, whi, IDESC, sb != 0);
+                mma_f16(tmem + COL_U, shi, wlo, IDESC, 1);
+                mma_f16(tmem + COL_U, slo, whi, IDESC, 1);
+                mma_commit(&bar[B_MINEMPTY + tb]);
+                mma_commit(&bar[B_TFULL + tb]);
             }
+        }
+        __syncwarp();
+    } else if (warp >= kFoldWarp0 && warp < kConvWarp0) {
+        // -------------------------------------------------------------- fold
+        const int ft = threadIdx.x - kFoldWarp0 * 32;            // 0..127: the column whose d_b it loads
+        const uint32_t lq = (uint32_t)((warp & 3) * 32) << 16;   // TMEM lane quadrant of this warp
+        const int row = (warp & 3) * 32 + lane;                  // output row within the tile
+        const int64_t nd = n0 + ft;
+        const uint8_t *dsrc = a.w + a.N * (int64_t)B * 128 + nd * B * 16;
+        float dnext = nd < a.N ? __half2float(__ushort_as_half(qk::ldg_stream2(dsrc))) : 0.0f;
+        for (int sb = 0; sb < B; sb++) {
+            const int tb = sb & 1;
+            dB[tb * 128 + ft] = dnext;
+            bar_fold();
+            if (sb + 1 < B && nd < a.N) dnext = __half2float(__ushort_as_half(qk::ldg_stream2(dsrc + 16 * (sb + 1))));
+            wait_bar(&bar[B_TFULL + tb], (sb >> 1) & 1);
+            fence_after_sync();
+            const float *d = dB + tb * 128;
+#pragma unroll 1
+            for (int c = 0; c < 4; c++) {
+                float t[32], yv[32];
+                tmem_ld32(tmem + lq + COL_T0 + 128 * tb + 32 * c, t);
+                if (sb > 0) tmem_ld32(tmem + lq + COL_Y + 32 * c, yv);
+                tmem_wait_ld();
+                if (sb > 0) {
 #pragma unroll
-            for (int hs = 0; hs < 2; hs++) {
-                const int j = 2 * gq + hs;
+                    for (int j = 0; j < 32; j++) yv[j] = fmaf(d[32 * c + j], t[j], yv[j]);
+                } else {
 #pragma unroll
-                for (int mt = 0; mt < 2; mt++) {
-                    const uint8_t *ar = sa + (32 * wm + 16 * mt + g) * A_STRIDE + 32 * j + 4 * t;
-                    const uint32_t a0 = *reinterpret_cast<const uint32_t *>(ar);
-                    const uint32_t a1 = *reinterpret_cast<const uint32_t *>(ar + 8 * A_STRIDE);
-                    const uint32_t a2 = *reinterpret_cast<const uint32_t *>(ar + 16);
-                    const uint32_t a3 = *reinterpret_cast<const uint32_t *>(ar + 8 * A_STRIDE + 16);
-                    const float2 sa0 = side_a[(32 * wm + 16 * mt + g) * 8 + j];
-                    const float2 sa1 = side_a[(32 * wm + 16 * mt + g + 8) * 8 + j];
+                    for (int j = 0; j < 32; j++) yv[j] = d[32 * c + j] * t[j];
+                }
+                tmem_st32(tmem + lq + COL_Y + 32 * c, yv);
+            }
+            tmem_wait_st();
+            fence_before_sync();
+            mbar_arrive(&bar[B_TEMPTY + tb]);
+        }
+        // epilogue: Y - U (+ R)
+        const int64_t m = m0 + row;
+#pragma unroll 1
+        for (int c = 0; c < 4; c++) {
+            float yv[32], uv[32];
+            tmem_ld32(tmem + lq + COL_Y + 32 * c, yv);
+            tmem_ld32(tmem + lq + COL_U + 32 * c, uv);
+            tmem_wait_ld();
+            if (m < a.M) {
+                const int64_t nb = n0 + 32 * c;
+                float *yr = a.y + m * a.N;
+                const float *rr = a.residual ? a.residual + m * a.N : nullptr;
 #pragma unroll
-                    for (int nt = 0; nt < 4; nt++) {
-                        int c[4] = {0, 0, 0, 0};
-                        if (hs == 0)
-                            mma_s8(c, a0, a1, a2, a3, blo[nt][0], blo[nt][1]);
-                        else
-                            mma_s8(c, a0, a1, a2, a3, bhi[nt][0], bhi[nt][1]);
-                        const float2 w0 = side_w[(32 * wn + 8 * nt + 2 * t) * 8 + j];
-                        const float2 w1 = side_w[(32 * wn + 8 * nt + 2 * t + 1) * 8 + j];
-                        float *f = facc[mt][nt];
-                        f[0] = fmaf(sa0.x * w0.x, (float)c[0], f[0]);
-                        f[0] = fmaf(-sa0.y, w0.y, f[0]);
-                        f[1] = fmaf(sa0.x * w1.x, (float)c[1], f[1]);
-                        f[1] = fmaf(-sa0.y, w1.y, f[1]);
-                        f[2] = fmaf(sa1.x * w0.x, (float)c[2], f[2]);
-                        f[2] = fmaf(-sa1.y, w0.y, f[2]);
-                        f[3] = fmaf(sa1.x * w1.x, (float)c[3], f[3]);
-                        f[3] = fmaf(-sa1.y, w1.y, f[3]);
+                for (int j = 0; j < 32; j++) {
+                    const int64_t n = nb + j;
+                    if (n < a.N) {
+                        const float v = yv[j] - uv[j];
+                        yr[n] = rr ? __fadd_rn(v, rr[n]) : v;
                     }
                 }
             }
         }
-        __syncthreads();
-    }
-    cp_wait<0>();
-
+    } else if (warp >= kConvWarp0) {
+        // --------------------------------------------------------- converters
+        const int ct = threadIdx.x - kConvWarp0 * 32;             // 0..255
+        const int row = ct >> 1, h = ct & 1;
+        const int64_t m = m0 + row, n = n0 + row;
+        Raw r0, r1, r2;
+        if (0 < nit) load_raw(r0, a, m, n, 0, h);
+        if (1 < nit) load_raw(r1, a, m, n, 1, h);
+        if (2 < nit) load_raw(r2, a, m, n, 2, h);
+        for (int it = 0; it < nit; it++) {
+            Raw r3;
+            if (it + 3 < nit) load_raw(r3, a, m, n, it + 3, h);
+            const int sb = it >> 2, g = it & 3, st = it % NST, tb = sb & 1;
+            if (it >= NST) wait_bar(&bar[B_EMPTY + st], ((it / NST) + 1) & 1);
+            if (g == 0 && sb >= 2) wait_bar(&bar[B_MINEMPTY + tb], ((sb - 2) >> 1) & 1);
+            uint8_t *s0 = smem + st * STAGE;
+            // ---- A: d_a * q_a as hi/lo f16 at stage k = 32h .. 32h+31 (chunks 4h .. 4h+3)
+            const __half dah = __ushort_as_half((unsigned short)(r0.da & 0xffffu));
+            const __half2 d2 = __halves2half2(dah, dah);
+            const uint32_t aw[8] = {r0.a0.x, r0.a0.y, r0.a0.z, r0.a0.w, r0.a1.x, r0.a1.y, r0.a1.z, r0.a1.w};
+            int qsum = 0;
 #pragma unroll
-    for (int mt = 0; mt < 2; mt++)
-#pragma unroll
-        for (int nt = 0; nt < 4; nt++)
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int64_t m = m0 + 32 * wm + 16 * mt + g + (e >> 1) * 8;
-                const int64_t n = n0 + 32 * wn + 8 * nt + 2 * t + (e & 1);
-                if (m < M && n < N) {
-                    const size_t o = (size_t)m * N + n;
-                    const float v = facc[mt][nt][e];
-                    y[o] = residual ? __fadd_rn(v, residual[o]) : v;
-                }
+            for (int q = 0; q < 4; q++) {
+                uint32_t hi[4], lo[4];
+                conv_a(aw[2 * q], d2, hi[0], lo[0], hi[1], lo[1]);
+                conv_a(aw[2 * q + 1], d2, hi[2], lo[2], hi[3], lo[3]);
+                sts128(s0, sw128(row, 4 * h + q), hi[0], hi[1], hi[2], hi[3]);
+                sts128(s0 + TILE, sw128(row, 4 * h + q), lo[0], lo[1], lo[2], lo[3]);
+                qsum = qk::dp4a_ss(aw[2 * q], 0x01010101u, qsum);
+                qsum = qk::dp4a_ss(aw[2 * q + 1], 0x01010101u, qsum);
             }
+            // ---- B: this half of group g; low nibbles = sub-block 2g at stage k 16h .. 16h+15,
+            //      high nibbles = sub-block 2g+1 at stage k 32+16h .. 32+16h+15
+            const uint32_t rec =
+                __byte_perm(__byte_perm(r0.mt.y, r0.mt.z, g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u), r0.mt.w,
+                            g == 0 ? 0x3210u : g == 1 ? 0x3210u : g == 2 ? 0x3410u : 0x3765u);
+            const int sc0 = rec & 63u, sc1 = (rec >> 6) & 63u, mn0 = (rec >> 12) & 63u, mn1 = (rec >> 18) & 63u;
+            const __half2 sl = __half2half2(__int2half_rn(sc0)), sh = __half2half2(__int2half_rn(sc1));
+            const __half2 sl1024 = __half2half2(__int2half_rn(-1024 * sc0));
+            const __half2 sh64 = __half2half2(__int2half_rn(-64 * sc1));
+            const uint32_t bw[4] = {r0.b.x, r0.b.y, r0.b.z, r0.b.w};
+            uint32_t L[8], H[8];
+#pragma unroll
+            for (int q = 0; q < 4; q++) conv_b(bw[q], sl, sl1024, sh, sh64, L[2 * q], L[2 * q + 1], H[2 * q], H[2 * q + 1]);
+            sts128(s0 + 2 * TILE, sw128(row, 2 * h), L[0], L[1], L[2], L[3]);
+            sts128(s0 + 2 * TILE, sw128(row, 2 * h + 1), L[4], L[5], L[6], L[7]);
+            sts128(s0 + 2 * TILE, sw128(row, 4 + 2 * h), H[0], H[1], H[2], H[3]);
+            sts128(s0 + 2 * TILE, sw128(row, 4 + 2 * h + 1), H[4], H[5], H[6], H[7]);
+            // ---- min term entry j = 2g + h: S = d_a sum(q_a) / 16, Mw = 16 dmin m_j
+            uint8_t *ms = smem + OFF_MIN + tb * MSET;
+            const int j = 2 * g + h;
+            __half shi, slo, whi, wlo;
+            split_f16(__half2float(dah) * (float)qsum * 0.0625f, shi, slo);
+            const float dmin = __half2float(__ushort_as_half((unsigned short)(r0.mt.x >> 16)));
+            split_f16(dmin * (float)(h ? mn1 : mn0) * 16.0f, whi, wlo);
+            *reinterpret_cast<__half *>(ms + sw32(row, j)) = shi;
+            *reinterpret_cast<__half *>(ms + MTILE + sw32(row, j)) = slo;
+            *reinterpret_cast<__half *>(ms + 2 * MTILE + sw32(row, j)) = whi;
+            *reinterpret_cast<__half *>(ms + 3 * MTILE + sw32(row, j)) = wlo;
+            fence_proxy_async();
+            mbar_arrive(&bar[B_FULL + st]);
+            r0 = r1, r1 = r2, r2 = r3;
+        }
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
 }
 
 }  // namespace
+
+extern "C" int qk_error_flags(unsigned *flags, int clear)
+{
+    if (!flags) return QK_E_NULL;
+    if (cudaMemcpyFromSymbol(flags, g_qk_errors, sizeof(unsigned)) != cudaSuccess) return QK_E_CUDA;
+    if (clear) {
+        const unsigned z = 0;
+        if (cudaMemcpyToSymbol(g_qk_errors, &z, sizeof(unsigned)) != cudaSuccess) return QK_E_CUDA;
+    }
+    return QK_OK;
+}
 
 extern "C" int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes)
 {
@@ -237,16 +400,17 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
     if (qk::overlaps(y, ybytes, w, wbytes) || qk::overlaps(y, ybytes, codes, cbytes) ||
         qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)))
         return QK_E_ALIAS;
-    static std::atomic<int> smem_set{0};
-    if (!smem_set.load()) {
+    if ((size_t)SMEM > qk::max_smem_optin()) return QK_E_CUDA;
+    static std::atomic<int> attr_set{0};
+    if (!attr_set.load()) {
         if (cudaFuncSetAttribute(mmq_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess ||
             qk::max_carveout(mmq_q4k_kernel) != cudaSuccess)
             return QK_E_CUDA;
-        smem_set.store(1);
+        attr_set.store(1);
     }
-    const int64_t gx = (N + BN - 1) / BN, gy = (M + BM - 1) / BM;
-    if (gy > 65535) return QK_E_SHAPE;
+    const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
+    if (gx > 0x7fffffffLL || gy > 65535) return QK_E_SHAPE;
+    MmqArgs args{static_cast<const uint8_t *>(w), codes, static_cast<const __half2 *>(scales), M, N, K, residual, y};
     return qk::launch(mmq_q4k_kernel, dim3((unsigned)gx, (unsigned)gy), dim3(kThreads), SMEM, (cudaStream_t)stream,
-                      (flags & QK_LAUNCH_PDL) != 0, static_cast<const uint8_t *>(w), codes,
-                      static_cast<const __half2 *>(scales), M, N, K, residual, y);
+                      (flags & QK_LAUNCH_PDL) != 0, args);
 }

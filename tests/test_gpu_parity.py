@@ -285,3 +285,30 @@ def test_mmq_residual_inplace_deterministic():
     assert torch.equal(y, y2)
     y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d, residual=r)
     check(y.cpu().numpy(), y_ref, ab, r, what="mmq residual")
+
+
+@pytest.mark.parametrize("scale", [1e-3, 30.0, 1000.0])
+def test_mmq_activation_magnitudes(scale):
+    """Small and large activations (the min-term operands are rescaled by powers of two)."""
+    M, N, K = 40, 96, 1024
+    w, wr = weights("q4k", N, K, seed=61)
+    x = synth.activations(M, K, seed=62) * np.float32(scale)
+    codes, scales = q8(x)
+    c, d = q8_host(codes, scales)
+    y = qk.mmq_q4k(wr, codes, scales, N, K).cpu().numpy()
+    y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d)
+    check(y, y_ref, ab, what=f"mmq scale={scale}")
+
+
+def test_mmq_edges_and_error_flags():
+    """One row, one column, a ragged 129 x 257 tile grid; no bounded wait gives up."""
+    qk.error_flags(clear=True)
+    for M, N, K in [(1, 1, 256), (129, 257, 512), (128, 128, 256)]:
+        w, wr = weights("q4k", N, K, seed=M + N)
+        codes, scales = q8(synth.activations(M, K, seed=N))
+        c, d = q8_host(codes, scales)
+        y = qk.mmq_q4k(wr, codes, scales, N, K).cpu().numpy()
+        y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d)
+        check(y, y_ref, ab, what=f"mmq edge M={M} N={N} K={K}")
+    torch.cuda.synchronize()
+    assert qk.error_flags(clear=True) == 0
