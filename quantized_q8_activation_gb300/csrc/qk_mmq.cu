@@ -22,20 +22,39 @@
 // One CTA (16 warps) per 128 x 128 output tile and per SM (all 512 TMEM
 // columns: Y | T0 | T1 | U):
 //   warp 0      TMEM allocation; lane 0 issues every MMA and commit
+//   warp 1      lane 0 streams the raw inputs with 2D TMA tensor copies into a
+//               ring in shared memory: per 64-value K stage the activation
+//               codes (128 x 64 B) and the two 16-byte halves of the Q4_K code
+//               bytes (128 x 16 B each); per superblock the q8_1 scale pairs
+//               (128 x 32 B) and the Q4_K metadata records (128 x 16 B)
 //   warps 4-7   fold T into Y per superblock, then the epilogue (TMEM lane
 //               quadrant = warp % 4)
-//   warps 8-15  operand converters: q8_1 codes + d_a -> A_hi / A_lo and Q4_K
-//               codes + scales -> B per 64-value K stage, written straight
-//               into the UMMA K-major SWIZZLE_128B layout; S and Mw into
-//               SWIZZLE_32B tiles once per superblock
-// Stages are handed over with mbarriers (full: converters -> MMA; empty: MMA
+//   warps 8-15  operand converters: raw codes + d_a -> A_hi / A_lo and Q4_K
+//               codes + scales -> B per K stage, written straight into the
+//               UMMA K-major SWIZZLE_128B layout; S and Mw entries into
+//               SWIZZLE_32B tiles
+// Stages are handed over with mbarriers (raw full: TMA transaction bytes;
+// raw empty: converters -> producer; full: converters -> MMA; empty: MMA
 // commit -> converters; T buffers: MMA commit -> fold, fold -> MMA).  Every
 // wait is bounded; a wait that gives up sets a device error flag
-// (qk_error_flags) and the kernel runs to its end without further waiting.
+// (qk_error_flags), and once it is set the other waits return after a few
+// polls, so the kernel runs to its end.
 #include "qk_common.cuh"
 #include "qk_tc.cuh"
 
+#include <cuda.h>
+
 #include <atomic>
+
+#ifndef QK_MMQ_NST
+#define QK_MMQ_NST 2        // converted operand stages
+#endif
+#ifndef QK_MMQ_RAW
+#define QK_MMQ_RAW 5        // raw K stages in flight
+#endif
+#ifndef QK_MMQ_SBRAW
+#define QK_MMQ_SBRAW 2      // raw per-superblock slots in flight
+#endif
 
 __device__ unsigned g_qk_errors;
 
@@ -44,7 +63,7 @@ namespace {
 using namespace qk::tc;
 
 constexpr int BM = 128, BN = 128, BK = 64;      // BK: one Q4_K group = two 32-value sub-blocks
-constexpr int NST = 3;                          // operand stages in flight
+constexpr int NST = QK_MMQ_NST, NRAW = QK_MMQ_RAW, NSB = QK_MMQ_SBRAW;
 constexpr int kThreads = 512;
 constexpr int kFoldWarp0 = 4, kConvWarp0 = 8;
 constexpr int kConv = 256, kFold = 128;
@@ -53,13 +72,31 @@ constexpr int TILE = BM * BK * 2;               // 16 KB: 128 rows x 64 f16, SWI
 constexpr int STAGE = 3 * TILE;                 // A_hi | A_lo | B
 constexpr int MTILE = 128 * 16 * 2;             // 4 KB: 128 rows x 16 f16, SWIZZLE_32B K-major
 constexpr int MSET = 4 * MTILE;                 // S_hi | S_lo | Mw_hi | Mw_lo
+// raw K stage: activation codes 128 x 64 B | code bytes, first halves 128 x 16 B | second halves
+constexpr int RAW_A = 0, RAW_B0 = BM * 64, RAW_B1 = RAW_B0 + BN * 16, RAW = RAW_B1 + BN * 16;
+// raw superblock slot: q8_1 scale pairs 128 x 8 x 4 B | metadata records 128 x 16 B
+constexpr int SBR_S = 0, SBR_M = BM * 32, SBR = SBR_M + BN * 16;
 constexpr int OFF_MIN = NST * STAGE;
-constexpr int OFF_DB = OFF_MIN + 2 * MSET;      // fold: d_b of the tile's columns, 2 x 128 floats
+constexpr int OFF_RAW = OFF_MIN + 2 * MSET;
+constexpr int OFF_SBR = OFF_RAW + NRAW * RAW;
+constexpr int OFF_DB = OFF_SBR + NSB * SBR;     // fold: d_b of the tile's columns, 2 x 128 floats
 constexpr int OFF_BAR = OFF_DB + 2 * 128 * 4;
-enum { B_FULL = 0, B_EMPTY = NST, B_MINEMPTY = 2 * NST, B_TFULL = 2 * NST + 2, B_TEMPTY = 2 * NST + 4,
-       NBAR = 2 * NST + 6 };
+enum {
+    B_FULL = 0,
+    B_EMPTY = B_FULL + NST,
+    B_MINEMPTY = B_EMPTY + NST,
+    B_TFULL = B_MINEMPTY + 2,
+    B_TEMPTY = B_TFULL + 2,
+    B_RFULL = B_TEMPTY + 2,
+    B_REMPTY = B_RFULL + NRAW,
+    B_SFULL = B_REMPTY + NRAW,
+    B_SEMPTY = B_SFULL + NSB,
+    NBAR = B_SEMPTY + NSB
+};
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int SMEM = OFF_TMEM + 16 + 1024;      // + slack to align the base to 1024
+static_assert(SMEM <= 232448, "shared memory plan exceeds the per-block opt-in limit");
+static_assert(RAW % 1024 == 0 && SBR % 1024 == 0 && OFF_RAW % 1024 == 0, "TMA destinations stay aligned");
 constexpr uint32_t COL_Y = 0, COL_T0 = 128, COL_U = 384, TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 
@@ -68,12 +105,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) { return (r >> 3) * 1024
 // byte offset of element j (< 8, first 16-byte chunk) of row r in a SWIZZLE_32B K-major tile (rows of 32 bytes)
 __device__ __forceinline__ uint32_t sw32(int r, int j) { return (r >> 3) * 256 + (r & 7) * 32 + (((r >> 2) & 1) << 4) + 2 * j; }
 
-__device__ __forceinline__ bool give_up() { return (*(volatile unsigned *)&g_qk_errors & kErrTimeout) != 0; }
-
-__device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity)
-{
-    if (!give_up()) mbar_wait(bar, parity, &g_qk_errors);
-}
+__device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity) { mbar_wait(bar, parity, &g_qk_errors); }
 
 __device__ __forceinline__ void bar_fold() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -81,44 +113,18 @@ __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<ui
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
 struct MmqArgs {
-    const uint8_t *w;
-    const int8_t *codes;
-    const __half2 *scales;
+    const uint8_t *w;       // repacked Q4_K weight (the fold reads d_b from its metadata)
     int64_t M, N, K;
     const float *residual;
     float *y;
 };
 
-// one converter thread's raw inputs of one K stage (stage it = superblock it/4, group it%4)
-struct Raw {
-    uint4 a0, a1;          // 32 activation codes: row m, k = 64g + 32h .. +31 of the superblock
-    uint32_t da;           // q8_1 scale pair (d, s) of that 32-value block, binary16 bits
-    uint4 b;               // 16 Q4_K code bytes: row n, half h of group g
-    uint4 mt;              // 16-byte metadata record of (row n, superblock)
+struct MmqMaps {
+    CUtensorMap codes;      // uint8  [M][K]          box 64 x 128
+    CUtensorMap scales;     // uint32 [M][K/32]       box 8 x 128   (q8_1 (d, s) pairs)
+    CUtensorMap wcodes;     // uint8  [N][B*128]      box 16 x 128  (code plane of the repacked weight)
+    CUtensorMap meta;       // uint8  [N][B*16]       box 16 x 128  (metadata plane)
 };
-
-__device__ __forceinline__ void load_raw(Raw &r, const MmqArgs &a, int64_t m, int64_t n, int it, int h)
-{
-    const int B = (int)(a.K >> 8);
-    const int sb = it >> 2, g = it & 3;
-    if (m < a.M) {
-        const int8_t *src = a.codes + m * a.K + sb * 256 + g * 64 + 32 * h;
-        r.a0 = *reinterpret_cast<const uint4 *>(src);
-        r.a1 = *reinterpret_cast<const uint4 *>(src + 16);
-        r.da = *reinterpret_cast<const uint32_t *>(a.scales + m * (a.K >> 5) + sb * 8 + 2 * g + h);
-    } else {
-        r.a0 = r.a1 = make_uint4(0, 0, 0, 0);
-        r.da = 0;
-    }
-    if (n < a.N) {
-        const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s) + g;
-        const uint8_t *row = a.w + n * (int64_t)B * 128 + 1024 * s;
-        r.b = qk::ldg_stream16(row + (h ? 16 * G + 16 * u : 16 * u));
-        r.mt = qk::ldg_stream16(a.w + a.N * (int64_t)B * 128 + (n * B + sb) * 16);
-    } else {
-        r.b = r.mt = make_uint4(0, 0, 0, 0);
-    }
-}
 
 // 4 int8 codes -> (A_hi, A_lo) f16 pairs with A_hi + A_lo = d * q exactly
 __device__ __forceinline__ void conv_a(uint32_t w4, __half2 d2, uint32_t &hi01, uint32_t &lo01, uint32_t &hi23,
@@ -159,7 +165,79 @@ __device__ __forceinline__ void split_f16(float v, __half &hi, __half &lo)
     lo = __float2half_rn(v - __half2float(hi));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a)
+// one converter thread's share of K stage `it` (smem stage st = it % NST): reads its raw inputs
+// from the TMA ring, writes the A_hi / A_lo / B chunks of tile row `row`, half h, and min-term
+// entry j = 2g + h, releases the raw slots and signals the stage full
+__device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, int it, int row, int h, int st)
+{
+    const int sb = it >> 2, g = it & 3, tb = sb & 1;
+    const int rs = it % NRAW, ss = sb % NSB;
+    // ---- raw inputs
+    wait_bar(&bar[B_RFULL + rs], (it / NRAW) & 1);
+    if (g == 0) wait_bar(&bar[B_SFULL + ss], (sb / NSB) & 1);
+    const uint8_t *raw = smem + OFF_RAW + rs * RAW;
+    const uint8_t *sbr = smem + OFF_SBR + ss * SBR;
+    const uint4 a0 = *reinterpret_cast<const uint4 *>(raw + RAW_A + row * 64 + 32 * h);
+    const uint4 a1 = *reinterpret_cast<const uint4 *>(raw + RAW_A + row * 64 + 32 * h + 16);
+    const uint4 bq = *reinterpret_cast<const uint4 *>(raw + (h ? RAW_B1 : RAW_B0) + row * 16);
+    const uint32_t da = *reinterpret_cast<const uint32_t *>(sbr + SBR_S + row * 32 + (2 * g + h) * 4);
+    const uint4 mt = *reinterpret_cast<const uint4 *>(sbr + SBR_M + row * 16);
+
+    if (it >= NST) wait_bar(&bar[B_EMPTY + st], ((it / NST) + 1) & 1);
+    if (g == 0 && sb >= 2) wait_bar(&bar[B_MINEMPTY + tb], ((sb - 2) >> 1) & 1);
+    uint8_t *s0 = smem + st * STAGE;
+    // ---- A: d_a * q_a as hi/lo f16 at stage k = 32h .. 32h+31 (chunks 4h .. 4h+3)
+    const __half dah = __ushort_as_half((unsigned short)(da & 0xffffu));
+    const __half2 d2 = __halves2half2(dah, dah);
+    const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    int qsum = 0;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        uint32_t hi[4], lo[4];
+        conv_a(aw[2 * q], d2, hi[0], lo[0], hi[1], lo[1]);
+        conv_a(aw[2 * q + 1], d2, hi[2], lo[2], hi[3], lo[3]);
+        sts128(s0, sw128(row, 4 * h + q), hi[0], hi[1], hi[2], hi[3]);
+        sts128(s0 + TILE, sw128(row, 4 * h + q), lo[0], lo[1], lo[2], lo[3]);
+        qsum = qk::dp4a_ss(aw[2 * q], 0x01010101u, qsum);
+        qsum = qk::dp4a_ss(aw[2 * q + 1], 0x01010101u, qsum);
+    }
+    // ---- B: this half of group g; low nibbles = sub-block 2g at stage k 16h .. 16h+15,
+    //      high nibbles = sub-block 2g+1 at stage k 32+16h .. 32+16h+15
+    const uint32_t rec = __byte_perm(__byte_perm(mt.y, mt.z, g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u), mt.w,
+                                     g == 0 ? 0x3210u : g == 1 ? 0x3210u : g == 2 ? 0x3410u : 0x3765u);
+    const int sc0 = rec & 63u, sc1 = (rec >> 6) & 63u, mn0 = (rec >> 12) & 63u, mn1 = (rec >> 18) & 63u;
+    const __half2 sl = __half2half2(__int2half_rn(sc0)), sh = __half2half2(__int2half_rn(sc1));
+    const __half2 sl1024 = __half2half2(__int2half_rn(-1024 * sc0));
+    const __half2 sh64 = __half2half2(__int2half_rn(-64 * sc1));
+    const uint32_t bw[4] = {bq.x, bq.y, bq.z, bq.w};
+    uint32_t L[8], H[8];
+#pragma unroll
+    for (int q = 0; q < 4; q++) conv_b(bw[q], sl, sl1024, sh, sh64, L[2 * q], L[2 * q + 1], H[2 * q], H[2 * q + 1]);
+    sts128(s0 + 2 * TILE, sw128(row, 2 * h), L[0], L[1], L[2], L[3]);
+    sts128(s0 + 2 * TILE, sw128(row, 2 * h + 1), L[4], L[5], L[6], L[7]);
+    sts128(s0 + 2 * TILE, sw128(row, 4 + 2 * h), H[0], H[1], H[2], H[3]);
+    sts128(s0 + 2 * TILE, sw128(row, 4 + 2 * h + 1), H[4], H[5], H[6], H[7]);
+    // ---- min term entry j = 2g + h: S = d_a sum(q_a) / 16, Mw = 16 dmin m_j
+    uint8_t *ms = smem + OFF_MIN + tb * MSET;
+    const int j = 2 * g + h;
+    __half shi, slo, whi, wlo;
+    split_f16(__half2float(dah) * (float)qsum * 0.0625f, shi, slo);
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(mt.x >> 16)));
+    split_f16(dmin * (float)(h ? mn1 : mn0) * 16.0f, whi, wlo);
+    *reinterpret_cast<__half *>(ms + sw32(row, j)) = shi;
+    *reinterpret_cast<__half *>(ms + MTILE + sw32(row, j)) = slo;
+    *reinterpret_cast<__half *>(ms + 2 * MTILE + sw32(row, j)) = whi;
+    *reinterpret_cast<__half *>(ms + 3 * MTILE + sw32(row, j)) = wlo;
+    // Release the raw slots only now: every value read from them has been consumed by the
+    // arithmetic above, so no shared load of this thread can still be pending when the producer
+    // lets the next TMA copy (async proxy) overwrite the slot.
+    mbar_arrive(&bar[B_REMPTY + rs]);
+    if (g == 3) mbar_arrive(&bar[B_SEMPTY + ss]);
+    fence_proxy_async();
+    mbar_arrive(&bar[B_FULL + st]);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -167,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a)
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     float *dB = reinterpret_cast<float *>(smem + OFF_DB);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t m0 = (int64_t)blockIdx.x * BM, n0 = (int64_t)blockIdx.y * BN;
+    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
     const int B = (int)(a.K >> 8), nit = 4 * B;
 
     qk::pdl_launch_dependents();
@@ -179,6 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a)
             mbar_init(&bar[B_TFULL + i], 1);
             mbar_init(&bar[B_TEMPTY + i], kFold);
         }
+        for (int i = 0; i < NRAW; i++) mbar_init(&bar[B_RFULL + i], 1), mbar_init(&bar[B_REMPTY + i], kConv);
+        for (int i = 0; i < NSB; i++) mbar_init(&bar[B_SFULL + i], 1), mbar_init(&bar[B_SEMPTY + i], kConv);
         mbar_init_fence();
     }
     for (int i = threadIdx.x; i < 2 * MSET / 16; i += kThreads)
@@ -228,6 +308,34 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a)
                 mma_f16(tmem + COL_U, slo, whi, IDESC, 1);
                 mma_commit(&bar[B_MINEMPTY + tb]);
                 mma_commit(&bar[B_TFULL + tb]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&maps.codes);
+            prefetch_tmap(&maps.scales);
+            prefetch_tmap(&maps.wcodes);
+            prefetch_tmap(&maps.meta);
+            for (int it = 0; it < nit; it++) {
+                const int sb = it >> 2, g = it & 3;
+                if (g == 0) {
+                    const int ss = sb % NSB;
+                    if (sb >= NSB) wait_bar(&bar[B_SEMPTY + ss], ((sb / NSB) + 1) & 1);
+                    uint8_t *d = smem + OFF_SBR + ss * SBR;
+                    mbar_arrive_expect_tx(&bar[B_SFULL + ss], SBR);
+                    tma_load_2d(d + SBR_S, &maps.scales, 8 * sb, m0, &bar[B_SFULL + ss]);
+                    tma_load_2d(d + SBR_M, &maps.meta, 16 * sb, n0, &bar[B_SFULL + ss]);
+                }
+                const int rs = it % NRAW;
+                if (it >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((it / NRAW) + 1) & 1);
+                uint8_t *d = smem + OFF_RAW + rs * RAW;
+                const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s) + g;
+                mbar_arrive_expect_tx(&bar[B_RFULL + rs], RAW);
+                tma_load_2d(d + RAW_A, &maps.codes, 256 * sb + 64 * g, m0, &bar[B_RFULL + rs]);
+                tma_load_2d(d + RAW_B0, &maps.wcodes, 1024 * s + 16 * u, n0, &bar[B_RFULL + rs]);
+                tma_load_2d(d + RAW_B1, &maps.wcodes, 1024 * s + 16 * G + 16 * u, n0, &bar[B_RFULL + rs]);
             }
         }
         __syncwarp();
@@ -290,66 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a)
         }
     } else if (warp >= kConvWarp0) {
         // --------------------------------------------------------- converters
+        // Unrolled by the stage count, so the converted stage index is static.
         const int ct = threadIdx.x - kConvWarp0 * 32;             // 0..255
         const int row = ct >> 1, h = ct & 1;
-        const int64_t m = m0 + row, n = n0 + row;
-        Raw r0, r1, r2;
-        if (0 < nit) load_raw(r0, a, m, n, 0, h);
-        if (1 < nit) load_raw(r1, a, m, n, 1, h);
-        if (2 < nit) load_raw(r2, a, m, n, 2, h);
-        for (int it = 0; it < nit; it++) {
-            Raw r3;
-            if (it + 3 < nit) load_raw(r3, a, m, n, it + 3, h);
-            const int sb = it >> 2, g = it & 3, st = it % NST, tb = sb & 1;
-            if (it >= NST) wait_bar(&bar[B_EMPTY + st], ((it / NST) + 1) & 1);
-            if (g == 0 && sb >= 2) wait_bar(&bar[B_MINEMPTY + tb], ((sb - 2) >> 1) & 1);
-            uint8_t *s0 = smem + st * STAGE;
-            // ---- A: d_a * q_a as hi/lo f16 at stage k = 32h .. 32h+31 (chunks 4h .. 4h+3)
-            const __half dah = __ushort_as_half((unsigned short)(r0.da & 0xffffu));
-            const __half2 d2 = __halves2half2(dah, dah);
-            const uint32_t aw[8] = {r0.a0.x, r0.a0.y, r0.a0.z, r0.a0.w, r0.a1.x, r0.a1.y, r0.a1.z, r0.a1.w};
-            int qsum = 0;
+        for (int it = 0; it < nit; it += NST) {
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-                uint32_t hi[4], lo[4];
-                conv_a(aw[2 * q], d2, hi[0], lo[0], hi[1], lo[1]);
-                conv_a(aw[2 * q + 1], d2, hi[2], lo[2], hi[3], lo[3]);
-                sts128(s0, sw128(row, 4 * h + q), hi[0], hi[1], hi[2], hi[3]);
-                sts128(s0 + TILE, sw128(row, 4 * h + q), lo[0], lo[1], lo[2], lo[3]);
-                qsum = qk::dp4a_ss(aw[2 * q], 0x01010101u, qsum);
-                qsum = qk::dp4a_ss(aw[2 * q + 1], 0x01010101u, qsum);
-            }
-            // ---- B: this half of group g; low nibbles = sub-block 2g at stage k 16h .. 16h+15,
-            //      high nibbles = sub-block 2g+1 at stage k 32+16h .. 32+16h+15
-            const uint32_t rec =
-                __byte_perm(__byte_perm(r0.mt.y, r0.mt.z, g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u), r0.mt.w,
-                            g == 0 ? 0x3210u : g == 1 ? 0x3210u : g == 2 ? 0x3410u : 0x3765u);
-            const int sc0 = rec & 63u, sc1 = (rec >> 6) & 63u, mn0 = (rec >> 12) & 63u, mn1 = (rec >> 18) & 63u;
-            const __half2 sl = __half2half2(__int2half_rn(sc0)), sh = __half2half2(__int2half_rn(sc1));
-            const __half2 sl1024 = __half2half2(__int2half_rn(-1024 * sc0));
-            const __half2 sh64 = __half2half2(__int2half_rn(-64 * sc1));
-            const uint32_t bw[4] = {r0.b.x, r0.b.y, r0.b.z, r0.b.w};
-            uint32_t L[8], H[8];
-#pragma unroll
-            for (int q = 0; q < 4; q++) conv_b(bw[q], sl, sl1024, sh, sh64, L[2 * q], L[2 * q + 1], H[2 * q], H[2 * q + 1]);
-            sts128(s0 + 2 * TILE, sw128(row, 2 * h), L[0], L[1], L[2], L[3]);
-            sts128(s0 + 2 * TILE, sw128(row, 2 * h + 1), L[4], L[5], L[6], L[7]);
-            sts128(s0 + 2 * TILE, sw128(row, 4 + 2 * h), H[0], H[1], H[2], H[3]);
-            sts128(s0 + 2 * TILE, sw128(row, 4 + 2 * h + 1), H[4], H[5], H[6], H[7]);
-            // ---- min term entry j = 2g + h: S = d_a sum(q_a) / 16, Mw = 16 dmin m_j
-            uint8_t *ms = smem + OFF_MIN + tb * MSET;
-            const int j = 2 * g + h;
-            __half shi, slo, whi, wlo;
-            split_f16(__half2float(dah) * (float)qsum * 0.0625f, shi, slo);
-            const float dmin = __half2float(__ushort_as_half((unsigned short)(r0.mt.x >> 16)));
-            split_f16(dmin * (float)(h ? mn1 : mn0) * 16.0f, whi, wlo);
-            *reinterpret_cast<__half *>(ms + sw32(row, j)) = shi;
-            *reinterpret_cast<__half *>(ms + MTILE + sw32(row, j)) = slo;
-            *reinterpret_cast<__half *>(ms + 2 * MTILE + sw32(row, j)) = whi;
-            *reinterpret_cast<__half *>(ms + 3 * MTILE + sw32(row, j)) = wlo;
-            fence_proxy_async();
-            mbar_arrive(&bar[B_FULL + st]);
-            r0 = r1, r1 = r2, r2 = r3;
+            for (int k = 0; k < NST; k++)
+                if (it + k < nit) convert_stage(smem, bar, it + k, row, h, k);
         }
     }
 
@@ -359,6 +414,40 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a)
         fence_after_sync();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled()
+{
+    static std::atomic<void *> fn{nullptr};
+    void *p = fn.load();
+    if (!p) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return nullptr;
+        fn.store(p);
+    }
+    return reinterpret_cast<EncodeTiledFn>(p);
+}
+
+// 2D row-major tensor [rows][cols] of elements of the map's type, row pitch `pitch` bytes; box bx x by
+bool make_map(EncodeTiledFn enc, CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t cols,
+              uint64_t rows, uint64_t pitch, uint32_t bx, uint32_t by)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch};
+    const cuuint32_t box[2] = {bx, by};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -388,7 +477,9 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
 {
     (void)workspace;
     (void)workspace_bytes;
-    if (M < 0 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || M > 0x7fffffffLL) return QK_E_SHAPE;
+    // TMA coordinates are signed 32-bit: rows and bytes of a row stay below 2^31
+    if (M < 0 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || M > 0x7fffffffLL || K > 0x7fffffffLL)
+        return QK_E_SHAPE;
     if (M == 0) return QK_OK;
     if (!w || !codes || !scales || !y) return QK_E_NULL;
     if (!qk::aligned(w, 16) || !qk::aligned(codes, 16) || !qk::aligned(scales, 16) || !qk::aligned(y, 4) ||
@@ -400,7 +491,19 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
     if (qk::overlaps(y, ybytes, w, wbytes) || qk::overlaps(y, ybytes, codes, cbytes) ||
         qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)))
         return QK_E_ALIAS;
+    const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
+    if (gx > 0x7fffffffLL || gy > 65535) return QK_E_SHAPE;
     if ((size_t)SMEM > qk::max_smem_optin()) return QK_E_CUDA;
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return QK_E_CUDA;
+    const int64_t B = K / 256;
+    const uint8_t *wb = static_cast<const uint8_t *>(w);
+    MmqMaps maps;
+    if (!make_map(enc, &maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, M, K, 64, BM) ||
+        !make_map(enc, &maps.scales, CU_TENSOR_MAP_DATA_TYPE_UINT32, scales, K / 32, M, K / 8, 8, BM) ||
+        !make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 16, BN) ||
+        !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 16, N, B * 16, 16, BN))
+        return QK_E_CUDA;
     static std::atomic<int> attr_set{0};
     if (!attr_set.load()) {
         if (cudaFuncSetAttribute(mmq_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess ||
@@ -408,9 +511,7 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
             return QK_E_CUDA;
         attr_set.store(1);
     }
-    const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
-    if (gx > 0x7fffffffLL || gy > 65535) return QK_E_SHAPE;
-    MmqArgs args{static_cast<const uint8_t *>(w), codes, static_cast<const __half2 *>(scales), M, N, K, residual, y};
+    MmqArgs args{wb, M, N, K, residual, y};
     return qk::launch(mmq_q4k_kernel, dim3((unsigned)gx, (unsigned)gy), dim3(kThreads), SMEM, (cudaStream_t)stream,
-                      (flags & QK_LAUNCH_PDL) != 0, args);
+                      (flags & QK_LAUNCH_PDL) != 0, args, maps);
 }

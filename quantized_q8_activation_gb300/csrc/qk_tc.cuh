@@ -38,15 +38,44 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; gives up after a
+// Wait for the phase with the given parity to complete.  Gives up after a
 // bounded number of polls (each poll may suspend the thread for a while),
-// sets `flags` and returns false.
+// sets kErrTimeout in `flags` and returns false.  Every 64 unsuccessful polls
+// it also reads `flags` and returns false at once if another thread has
+// already given up, so that a failed kernel drains quickly.  The global flag
+// word is never read on the fast path.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *flags)
 {
-    for (uint32_t i = 0; i < (1u << 22); i++)
+    for (uint32_t i = 1; i <= (1u << 22); i++) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && (*(volatile unsigned *)flags & kErrTimeout)) return false;
+    }
     atomicOr(flags, kErrTimeout);
     return false;
+}
+
+// arrive once and add `bytes` to the transaction count the phase waits for
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------------- TMA
+
+// 2D tiled bulk tensor copy global -> shared; completion is signalled as
+// transaction bytes on `bar`.  x is the innermost coordinate (elements).
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
 // make this thread's generic-proxy shared-memory writes visible to the async
