@@ -66,6 +66,49 @@ def int_ops(cfg) -> int:
     return sum(2 * cfg["M"] * N * K for (_, _, N, K, _, _) in cfg["gemms"])
 
 
+def front_end_fused(args, cfg) -> bool:
+    """Decode activation path: quantize inside the GEMV for one activation row (saves a
+    launch and a dependency), a separate quantize kernel for several rows (the in-GEMV
+    front end repeats the rows' quantization in every CTA)."""
+    if cfg["kind"] != "gemv":
+        return False
+    if args.front_end == "auto":
+        return cfg["M"] == 1
+    return args.front_end == "fused"
+
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, averaged over the
+# kernel's launches in one step) from one ncu capture of the command in the named profile.
+# Valid only while the kernel sources are the ones the counters were taken on.
+TRAFFIC: dict = {
+    (1, "gemv_q4k_f32"): {"bytes_per_launch": 30765504, "digest": "e2defd20d66373e5",
+                          "profile": "profiles/dram_traffic_per_launch.md"},
+    (2, "gemv_q6k_f32"): {"bytes_per_launch": 437122048, "digest": "e2defd20d66373e5",
+                          "profile": "profiles/gemv_q6k_f32_head_128256x4096.md"},
+    (4, "mmq_q4k"): {"bytes_per_launch": 145475584, "digest": "e2defd20d66373e5",
+                     "profile": "profiles/dram_traffic_per_launch.md"},
+}
+
+
+def kernel_sources_digest() -> str:
+    import hashlib
+    d = hashlib.sha1()
+    src = os.path.join(ROOT, "quantized_q8_activation_gb300", "csrc")
+    for f in sorted(os.listdir(src)):
+        if f.endswith((".cu", ".cuh")):
+            d.update(f.encode())
+            with open(os.path.join(src, f), "rb") as fh:
+                d.update(fh.read())
+    return d.hexdigest()[:16]
+
+
+def recorded_traffic(cfg_id: int, kernel: str, fused: bool):
+    t = TRAFFIC.get((cfg_id, kernel))
+    if t is None or t["digest"] != kernel_sources_digest():
+        return None
+    return t["bytes_per_launch"]
+
+
 def slots(cfg):
     """activation slots in step order with their K"""
     out = []
@@ -108,36 +151,50 @@ class Workload:
                 self.host_r[name] = synth.residual(M, N, seed=seed, tag=name)
                 self.r[name] = torch.from_numpy(self.host_r[name]).to(device)
             self.y[name] = torch.empty((M, N), dtype=torch.float32, device=device)
+        self.ws = None
+        if cfg["kind"] == "mmq":
+            need = max(qk.mmq_workspace_bytes(M, N, K) for (_, _, N, K, _, _) in cfg["gemms"])
+            self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device) if need else None
         torch.cuda.synchronize()
 
-    def step(self, copy: int, pdl: bool = True, stream=None, events=None, fused: bool = True):
+    def launch(self, gemm, copy: int, pdl: bool = True, stream=None, fused: bool = True):
+        """Enqueue the contraction kernel of one GEMM of the step (its q8_1 input, if it
+        has one, must already be in self.q8)."""
+        qk, cfg = self.qk, self.cfg
+        name, q, N, K, res, s = gemm
+        if fused and cfg["kind"] == "gemv":
+            fn = qk.gemv_q4k_f32 if q == "q4k" else qk.gemv_q6k_f32
+            fn(self.w[copy][name], self.x[s], N, K, residual=self.r.get(name), y=self.y[name],
+               pdl=pdl, stream=stream)
+        else:
+            codes, scales = self.q8[s]
+            kw = dict(residual=self.r.get(name), y=self.y[name], pdl=pdl, stream=stream)
+            if cfg["kind"] == "mmq":
+                qk.mmq_q4k(self.w[copy][name], codes, scales, N, K, workspace=self.ws, **kw)
+            else:
+                fn = qk.gemv_q4k if q == "q4k" else qk.gemv_q6k
+                fn(self.w[copy][name], codes, scales, N, K, **kw)
+
+    def step(self, copy: int, pdl: bool = True, stream=None, fused: bool = True):
         """Enqueue one step on `stream`.  Decode steps with `fused` quantize each
         activation inside its GEMV (qk_gemv_*_f32); otherwise a q8_1 quantize
-        kernel runs once per activation before its consumers.  With `events`
-        (a list), every GEMV/MMQ launch is bracketed by recorded CUDA events."""
+        kernel runs once per activation before its consumers."""
         qk, cfg = self.qk, self.cfg
         fused = fused and cfg["kind"] == "gemv"
         done = set()
-        for (name, q, N, K, res, s) in cfg["gemms"]:
+        for gemm in cfg["gemms"]:
+            s = gemm[5]
             if not fused and s not in done:
                 codes, scales = self.q8[s]
                 qk.quantize_q8_1(self.x[s], codes, scales, pdl=pdl, stream=stream)
                 done.add(s)
-            codes, scales = self.q8[s]
-            if events is not None:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-            if fused:
-                fn = qk.gemv_q4k_f32 if q == "q4k" else qk.gemv_q6k_f32
-                fn(self.w[copy][name], self.x[s], N, K, residual=self.r.get(name), y=self.y[name],
-                   pdl=pdl, stream=stream)
-            else:
-                fn = qk.mmq_q4k if cfg["kind"] == "mmq" else qk.gemv_q4k if q == "q4k" else qk.gemv_q6k
-                fn(self.w[copy][name], codes, scales, N, K, residual=self.r.get(name), y=self.y[name],
-                   pdl=pdl, stream=stream)
-            if events is not None:
-                e1.record(stream)
-                events.append((name, q, N, K, e0, e1))
+            self.launch(gemm, copy, pdl=pdl, stream=stream, fused=fused)
+
+    def kernel_key(self, gemm, fused: bool) -> str:
+        q = gemm[1]
+        if self.cfg["kind"] == "mmq":
+            return "mmq_q4k"
+        return ("gemv_q4k" if q == "q4k" else "gemv_q6k") + ("_f32" if fused else "")
 
     def launches_per_step(self, fused: bool = True) -> int:
         if fused and self.cfg["kind"] == "gemv":
@@ -241,22 +298,32 @@ def barrier(ws):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_step(cfg, host_w, host_x, host_r, threads: int, m_rows=None):
+def sample_rows(N: int, n_frac: float) -> int:
+    return max(1, min(N, int(round(N * n_frac))))
+
+
+def oracle_step(cfg, host_w, host_x, host_r, threads: int, m_rows=None, n_frac: float = 1.0):
     """One step of the workload on the CPU oracle (quantize + every contraction).
-    m_rows limits the activation rows (bounded sample for the prefill config)."""
+    m_rows limits the activation rows and n_frac the output rows of every contraction
+    (bounded samples); returns the units (weight bytes or int ops) the sample covers."""
     import oracle
     q8 = {}
     for s, x in host_x.items():
         xx = x if m_rows is None else x[:m_rows]
         c, d, _ = oracle.quantize_q8_1(xx)
         q8[s] = (c, d)
+    wbytes = ops = 0
     for (name, q, N, K, res, s) in cfg["gemms"]:
         c, d = q8[s]
         r = host_r.get(name)
         if r is not None and m_rows is not None:
             r = r[:m_rows]
+        n1 = sample_rows(N, n_frac)
         oracle.gemm(oracle.Q4_K if q == "q4k" else oracle.Q6_K, host_w[name], N, K, c, d, residual=r,
-                    threads=threads)
+                    rows=(0, n1), threads=threads)
+        wbytes += n1 * (K // 256) * BYTES_PER_SB[q]
+        ops += 2 * c.shape[0] * n1 * K
+    return ops if cfg["kind"] == "mmq" else wbytes
 
 
 def cpu_baseline(wl_host, cfg, budget_s: float = 12.0):
@@ -265,30 +332,32 @@ def cpu_baseline(wl_host, cfg, budget_s: float = 12.0):
     host_w, host_x, host_r = wl_host
     if cfg["kind"] == "mmq":
         m_rows = 8                                      # 8 of the 2048 tokens per sample step
-        units = int_ops(cfg) * m_rows / cfg["M"]
         unit, scale = "TOPS", 1e12
         sample = f"{m_rows} of {cfg['M']} activation rows of every GEMM per step (quantize + contraction)"
     else:
         m_rows = None
-        units = weight_bytes(cfg)
         unit, scale = "GB/s", 1e9
         sample = "the full step (quantize + every contraction) per sample"
     t0 = time.perf_counter()
     n = 0
+    done = 0
     while True:
-        oracle_step(cfg, host_w, host_x, host_r, threads, m_rows)
+        done += oracle_step(cfg, host_w, host_x, host_r, threads, m_rows)
         n += 1
-        if time.perf_counter() - t0 >= budget_s or n >= 50:
+        if time.perf_counter() - t0 >= budget_s or n >= 100000:
             break
     dt = time.perf_counter() - t0
-    return {"value": units * n / dt / scale, "unit": unit, "cores": threads, "kind": "oracle",
+    return {"value": done / dt / scale, "unit": unit, "cores": threads, "kind": "oracle",
             "sample": f"{n} x {sample}; {dt:.1f} s"}
 
 
 # ----------------------------------------------------------------- main arms
 
 def run_reference(args, ws, rank):
-    """The oracle on the host cores, on our arm's config/metric/unit."""
+    """The oracle on the host cores, on our arm's config/metric/unit.  Each step is a
+    bounded sample of the workload (every contraction on a slice of its output rows, and
+    for the prefill config on 8 activation rows), sized so the whole run takes about
+    two minutes whatever --steps is."""
     if rank != 0:
         return
     cfg = CONFIGS[args.config]
@@ -297,24 +366,31 @@ def run_reference(args, ws, rank):
     host_r = {name: synth.residual(cfg["M"], N, seed=0, tag=name) for (name, _, N, _, res, _) in cfg["gemms"] if res}
     threads = os.cpu_count() or 1
     m_rows = 8 if cfg["kind"] == "mmq" else None
-    for _ in range(args.warmup):
-        oracle_step(cfg, host_w, host_x, host_r, threads, m_rows)
+    # calibrate on a 1/64 slice, then size the per-step slice to the time budget
     t0 = time.perf_counter()
+    oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac=1 / 64)
+    t_slice = max(time.perf_counter() - t0, 1e-4)
+    per_step = 120.0 / (args.steps + args.warmup)
+    n_frac = min(1.0, max(1e-6, per_step / (t_slice * 64)))
+    for _ in range(args.warmup):
+        oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac)
+    t0 = time.perf_counter()
+    units = 0
     for _ in range(args.steps):
-        oracle_step(cfg, host_w, host_x, host_r, threads, m_rows)
+        units += oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac)
     dt = time.perf_counter() - t0
     if cfg["kind"] == "mmq":
-        value = int_ops(cfg) * (m_rows / cfg["M"]) * args.steps / dt / 1e12
-        unit = "TOPS"
-        sample = f"{m_rows} of {cfg['M']} activation rows per step"
+        value, unit = units / dt / 1e12, "TOPS"
+        sample = f"{m_rows} of {cfg['M']} activation rows"
     else:
-        value = weight_bytes(cfg) * args.steps / dt / 1e9
-        unit = "GB/s"
-        sample = "full step"
+        value, unit = units / dt / 1e9, "GB/s"
+        sample = "all activation rows"
+    sample += f", {n_frac:.4g} of the output rows of every contraction, per step (quantize included)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": cfg["name"], "M": cfg["M"]},
+            "data": "synthetic (seeded; distributions of the benchmark definition)",
+            "config": {"workload": cfg["name"], "config_id": args.config, "M": cfg["M"]},
             "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -332,11 +408,11 @@ def run_ours(args, ws, rank, local):
     C = wl.copies
     S = C * max(1, -(-args.graph_steps // C))        # steps per graph, a multiple of the copy count
 
-    fused = not args.unfused
+    fused = front_end_fused(args, cfg)
 
-    def steps(n, start=0, events=None, pdl=True, fused=fused):
+    def steps(n, start=0, pdl=True, fused=fused):
         for i in range(n):
-            wl.step((start + i) % C, pdl=pdl, stream=stream, events=events, fused=fused)
+            wl.step((start + i) % C, pdl=pdl, stream=stream, fused=fused)
 
     # warm-up (also settles per-kernel attributes before any capture)
     with torch.cuda.stream(stream):
@@ -366,7 +442,7 @@ def run_ours(args, ws, rank, local):
     ms = barrier_max(ms, ws, device)
     ms_step = ms / args.steps
 
-    # the other front end, for reference: same step with q8_1 quantize kernels (or fused, if --unfused)
+    # the other front end, for reference: the same step with the other activation path
     alt_ms_step = None
     if cfg["kind"] == "gemv":
         g_alt = capture(lambda: steps(S, fused=not fused), stream)
@@ -383,28 +459,37 @@ def run_ours(args, ws, rank, local):
         alt_ms_step = a0.elapsed_time(a1) / (reps * S)
         del g_alt
 
-    # per-launch durations of the contraction kernels (events around each launch)
-    # (eager launches queued behind a GPU-side sleep, so the GPU runs them back to back)
-    evs = []
-    n_ev = min(S, 4 * C * max(1, 10 // C))
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(200_000_000)
-        steps(n_ev, events=evs, pdl=False)
-    torch.cuda.synchronize()
+    # Per-kernel durations: each kernel type's launches of one step, S steps of them back to back
+    # in a graph of their own (same launch configuration as the step: PDL, rotating weight copies),
+    # timed with CUDA events on the launching stream.
+    groups = {}
+    for gemm in cfg["gemms"]:
+        groups.setdefault(wl.kernel_key(gemm, fused), []).append(gemm)
     per_kernel = {}
-    for (name, q, N, K, a, b) in evs:
-        key = "mmq_q4k" if cfg["kind"] == "mmq" else ("gemv_q4k" if q == "q4k" else "gemv_q6k")
-        if cfg["kind"] == "gemv" and fused:
-            key += "_f32"
-        d = per_kernel.setdefault(key, {"ms": 0.0, "n": 0, "bytes": 0, "ops": 0})
-        d["ms"] += a.elapsed_time(b)
-        d["n"] += 1
-        d["bytes"] += N * (K // 256) * BYTES_PER_SB[q]
-        d["ops"] += 2 * cfg["M"] * N * K
+    for key, gl in groups.items():
+        gk = capture(lambda: [wl.launch(g, i % C, pdl=True, stream=stream, fused=fused)
+                              for i in range(S) for g in gl], stream)
+        gk.replay()
+        torch.cuda.synchronize()
+        reps = max(1, min(nrep, 20))
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            k0.record(stream)
+            for _ in range(reps):
+                gk.replay()
+            k1.record(stream)
+        torch.cuda.synchronize()
+        del gk
+        n_launch = reps * S * len(gl)
+        per_kernel[key] = {"ms": k0.elapsed_time(k1) / (reps * S),          # per step
+                           "n": len(gl),                                     # launches per step
+                           "avg_us": k0.elapsed_time(k1) / n_launch * 1e3,
+                           "bytes": sum(N * (K // 256) * BYTES_PER_SB[q] for (_, q, N, K, _, _) in gl),
+                           "ops": sum(2 * cfg["M"] * N * K for (_, _, N, K, _, _) in gl)}
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
     dk = per_kernel[dom]
     hbm, bf16, peak_src = peaks()
+    traffic = recorded_traffic(args.config, dom, fused)
 
     if cfg["kind"] == "mmq":
         units = int_ops(cfg)
@@ -412,17 +497,21 @@ def run_ours(args, ws, rank, local):
         unit = "TOPS"
         achieved = dk["ops"] / (dk["ms"] * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                "frac": achieved / bf16, "traffic": None, "kernel": dom,
-                "peak_note": f"bf16 dense ({peak_src}); no int8 peak is measured on this part",
-                "avg_launch_us": dk["ms"] / dk["n"] * 1e3}
+                "frac": achieved / bf16, "traffic": traffic, "kernel": dom,
+                "algorithmic_ops_per_launch": dk["ops"] / dk["n"],
+                "peak_note": f"f16 tensor path: bf16 dense {peak_src} x nominal f16/bf16 ratio 1; "
+                             "achieved counts the algorithmic 2*M*N*K integer ops (the kernel issues "
+                             "two f16 MMAs per product for the exact hi/lo split)",
+                "avg_launch_us": dk["avg_us"]}
     else:
         units = weight_bytes(cfg)
         value = units * ws / (ms_step * 1e-3) / 1e9
         unit = "GB/s"
         achieved = dk["bytes"] / (dk["ms"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": None, "kernel": dom, "peak_note": f"hbm_gbs ({peak_src}, burst copy)",
-                "avg_launch_us": dk["ms"] / dk["n"] * 1e3}
+                "traffic": traffic, "kernel": dom, "peak_note": f"hbm_gbs ({peak_src}, burst copy)",
+                "algorithmic_bytes_per_launch": dk["bytes"] / dk["n"],
+                "avg_launch_us": dk["avg_us"]}
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     h2d = {s: torch.from_numpy(v).pin_memory() for s, v in wl.host_x.items()}
@@ -467,10 +556,12 @@ def run_ours(args, ws, rank, local):
                        "graph_steps": S, "pdl": True, "parallelism": f"replicas x{ws}",
                        "front_end": ("q8_1 quantization inside each GEMV (qk_gemv_*_f32)" if fused and
                                      cfg["kind"] == "gemv" else "qk_quantize_q8_1 kernel per activation")},
+            "alt_front_end": ("qk_quantize_q8_1 kernel per activation" if fused else
+                              "q8_1 quantization inside each GEMV") if cfg["kind"] == "gemv" else None,
             "alt_front_end_ms_per_step": alt_ms_step,
             "hbm_frac": (value / ws) / hbm if unit == "GB/s" else None,
             "roofline": roof,
-            "per_kernel": {k: {"launches": v["n"], "avg_us": v["ms"] / v["n"] * 1e3,
+            "per_kernel": {k: {"launches_per_step": v["n"], "avg_us": v["avg_us"],
                                "share": v["ms"] / sum(x["ms"] for x in per_kernel.values())}
                            for k, v in per_kernel.items()},
             "clocks": clk.summary(),
@@ -495,8 +586,10 @@ def main():
     ap.add_argument("--graph-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--unfused", action="store_true",
-                    help="decode: run the q8_1 quantize kernel before each GEMV instead of quantizing in the GEMV")
+    ap.add_argument("--front-end", choices=["auto", "fused", "unfused"], default="auto",
+                    help="decode activation path: q8_1 quantization inside each GEMV (fused) or a "
+                         "quantize kernel before its consumers (unfused); auto = fused for one "
+                         "activation row, unfused for several")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100}[args.config]
