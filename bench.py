@@ -66,15 +66,17 @@ def int_ops(cfg) -> int:
     return sum(2 * cfg["M"] * N * K for (_, _, N, K, _, _) in cfg["gemms"])
 
 
-def front_end_fused(args, cfg) -> bool:
-    """Decode activation path: quantize inside the GEMV for one activation row (saves a
-    launch and a dependency), a separate quantize kernel for several rows (the in-GEMV
-    front end repeats the rows' quantization in every CTA)."""
+def gemm_fused(policy: str, cfg, gemm) -> bool:
+    """Decode activation path of one GEMM: q8_1 quantization inside the GEMV ("fused")
+    or a quantize kernel before its consumers.  "auto" quantizes inside the GEMV when the
+    activation is small (M*K <= 4096: one float4 or two per thread), where saving the
+    extra kernel and dependency wins; larger activations use the quantize kernel, since
+    the in-GEMV front end repeats the quantization in every CTA."""
     if cfg["kind"] != "gemv":
         return False
-    if args.front_end == "auto":
-        return cfg["M"] == 1
-    return args.front_end == "fused"
+    if policy == "auto":
+        return cfg["M"] * gemm[3] <= 4096
+    return policy == "fused"
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, averaged over the
@@ -90,6 +92,16 @@ TRAFFIC: dict = {
 }
 
 
+def front_end_desc(front_end: str, cfg) -> str:
+    if cfg["kind"] != "gemv":
+        return "qk_quantize_q8_1 kernel per activation"
+    parts = []
+    for g in cfg["gemms"]:
+        parts.append(f"{g[0]}: " + ("q8_1 quantization inside the GEMV" if gemm_fused(front_end, cfg, g)
+                                     else "qk_quantize_q8_1 kernel"))
+    return f"{front_end}: " + "; ".join(parts)
+
+
 def kernel_sources_digest() -> str:
     import hashlib
     d = hashlib.sha1()
@@ -102,7 +114,7 @@ def kernel_sources_digest() -> str:
     return d.hexdigest()[:16]
 
 
-def recorded_traffic(cfg_id: int, kernel: str, fused: bool):
+def recorded_traffic(cfg_id: int, kernel: str):
     t = TRAFFIC.get((cfg_id, kernel))
     if t is None or t["digest"] != kernel_sources_digest():
         return None
@@ -175,15 +187,15 @@ class Workload:
                 fn = qk.gemv_q4k if q == "q4k" else qk.gemv_q6k
                 fn(self.w[copy][name], codes, scales, N, K, **kw)
 
-    def step(self, copy: int, pdl: bool = True, stream=None, fused: bool = True):
-        """Enqueue one step on `stream`.  Decode steps with `fused` quantize each
-        activation inside its GEMV (qk_gemv_*_f32); otherwise a q8_1 quantize
-        kernel runs once per activation before its consumers."""
+    def step(self, copy: int, pdl: bool = True, stream=None, front_end: str = "auto"):
+        """Enqueue one step on `stream`.  Each decode GEMM either quantizes its activation
+        inside the GEMV (qk_gemv_*_f32) or reads the q8_1 codes of a quantize kernel that
+        runs once per activation before its first consumer (see gemm_fused)."""
         qk, cfg = self.qk, self.cfg
-        fused = fused and cfg["kind"] == "gemv"
         done = set()
         for gemm in cfg["gemms"]:
             s = gemm[5]
+            fused = gemm_fused(front_end, cfg, gemm)
             if not fused and s not in done:
                 codes, scales = self.q8[s]
                 qk.quantize_q8_1(self.x[s], codes, scales, pdl=pdl, stream=stream)
@@ -196,10 +208,9 @@ class Workload:
             return "mmq_q4k"
         return ("gemv_q4k" if q == "q4k" else "gemv_q6k") + ("_f32" if fused else "")
 
-    def launches_per_step(self, fused: bool = True) -> int:
-        if fused and self.cfg["kind"] == "gemv":
-            return len(self.cfg["gemms"])
-        return len(slots(self.cfg)) + len(self.cfg["gemms"])
+    def launches_per_step(self, front_end: str = "auto") -> int:
+        slots_q = {g[5] for g in self.cfg["gemms"] if not gemm_fused(front_end, self.cfg, g)}
+        return len(slots_q) + len(self.cfg["gemms"])
 
 
 # -------------------------------------------------------------------- clocks
@@ -408,11 +419,11 @@ def run_ours(args, ws, rank, local):
     C = wl.copies
     S = C * max(1, -(-args.graph_steps // C))        # steps per graph, a multiple of the copy count
 
-    fused = front_end_fused(args, cfg)
+    front_end = args.front_end
 
-    def steps(n, start=0, pdl=True, fused=fused):
+    def steps(n, start=0, pdl=True, front_end=front_end):
         for i in range(n):
-            wl.step((start + i) % C, pdl=pdl, stream=stream, fused=fused)
+            wl.step((start + i) % C, pdl=pdl, stream=stream, front_end=front_end)
 
     # warm-up (also settles per-kernel attributes before any capture)
     with torch.cuda.stream(stream):
@@ -442,33 +453,39 @@ def run_ours(args, ws, rank, local):
     ms = barrier_max(ms, ws, device)
     ms_step = ms / args.steps
 
-    # the other front end, for reference: the same step with the other activation path
-    alt_ms_step = None
+    # the same step with the other activation paths, for reference
+    front_end_ms = {}
     if cfg["kind"] == "gemv":
-        g_alt = capture(lambda: steps(S, fused=not fused), stream)
-        g_alt.replay()
-        torch.cuda.synchronize()
-        reps = max(1, min(nrep, 50))
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            a0.record(stream)
-            for _ in range(reps):
-                g_alt.replay()
-            a1.record(stream)
-        torch.cuda.synchronize()
-        alt_ms_step = a0.elapsed_time(a1) / (reps * S)
-        del g_alt
+        for fe in ("fused", "unfused"):
+            if fe == front_end:
+                continue
+            g_alt = capture(lambda: steps(S, front_end=fe), stream)
+            g_alt.replay()
+            torch.cuda.synchronize()
+            reps = max(1, min(nrep, 50))
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a0.record(stream)
+                for _ in range(reps):
+                    g_alt.replay()
+                a1.record(stream)
+            torch.cuda.synchronize()
+            front_end_ms[fe] = a0.elapsed_time(a1) / (reps * S)
+            del g_alt
+        front_end_ms[front_end] = ms_step
 
     # Per-kernel durations: each kernel type's launches of one step, S steps of them back to back
     # in a graph of their own (same launch configuration as the step: PDL, rotating weight copies),
     # timed with CUDA events on the launching stream.
     groups = {}
     for gemm in cfg["gemms"]:
-        groups.setdefault(wl.kernel_key(gemm, fused), []).append(gemm)
+        f = gemm_fused(front_end, cfg, gemm)
+        groups.setdefault(wl.kernel_key(gemm, f), []).append((gemm, f))
     per_kernel = {}
-    for key, gl in groups.items():
-        gk = capture(lambda: [wl.launch(g, i % C, pdl=True, stream=stream, fused=fused)
-                              for i in range(S) for g in gl], stream)
+    for key, gf in groups.items():
+        gl = [g for g, _ in gf]
+        gk = capture(lambda: [wl.launch(g, i % C, pdl=True, stream=stream, fused=f)
+                              for i in range(S) for g, f in gf], stream)
         gk.replay()
         torch.cuda.synchronize()
         reps = max(1, min(nrep, 20))
@@ -489,7 +506,7 @@ def run_ours(args, ws, rank, local):
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
     dk = per_kernel[dom]
     hbm, bf16, peak_src = peaks()
-    traffic = recorded_traffic(args.config, dom, fused)
+    traffic = recorded_traffic(args.config, dom)
 
     if cfg["kind"] == "mmq":
         units = int_ops(cfg)
@@ -525,7 +542,7 @@ def run_ours(args, ws, rank, local):
             wl.x[s].copy_(t, non_blocking=True)
         for n, t in h2r.items():
             wl.r[n].copy_(t, non_blocking=True)
-        wl.step(i % C, pdl=True, stream=stream)
+        wl.step(i % C, pdl=True, stream=stream, front_end=front_end)
         for n, t in d2h.items():
             t.copy_(wl.y[n], non_blocking=True)
 
@@ -554,11 +571,8 @@ def run_ours(args, ws, rank, local):
                        "l2": f"inputs larger than L2: {C} rotating weight copies, "
                              f"{C * weight_bytes(cfg) / 1e6:.0f} MB working set",
                        "graph_steps": S, "pdl": True, "parallelism": f"replicas x{ws}",
-                       "front_end": ("q8_1 quantization inside each GEMV (qk_gemv_*_f32)" if fused and
-                                     cfg["kind"] == "gemv" else "qk_quantize_q8_1 kernel per activation")},
-            "alt_front_end": ("qk_quantize_q8_1 kernel per activation" if fused else
-                              "q8_1 quantization inside each GEMV") if cfg["kind"] == "gemv" else None,
-            "alt_front_end_ms_per_step": alt_ms_step,
+                       "front_end": front_end_desc(front_end, cfg)},
+            "front_end_ms_per_step": front_end_ms or None,
             "hbm_frac": (value / ws) / hbm if unit == "GB/s" else None,
             "roofline": roof,
             "per_kernel": {k: {"launches_per_step": v["n"], "avg_us": v["avg_us"],
@@ -567,7 +581,7 @@ def run_ours(args, ws, rank, local):
             "clocks": clk.summary(),
             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d_bytes,
                     "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_s * 1e3},
-            "gpu_launches": wl.launches_per_step(fused) * args.steps}
+            "gpu_launches": wl.launches_per_step(front_end) * args.steps}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline((wl.host_w, wl.host_x, wl.host_r), cfg, budget_s=args.cpu_seconds)
     if rank == 0:
@@ -588,8 +602,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--front-end", choices=["auto", "fused", "unfused"], default="auto",
                     help="decode activation path: q8_1 quantization inside each GEMV (fused) or a "
-                         "quantize kernel before its consumers (unfused); auto = fused for one "
-                         "activation row, unfused for several")
+                         "quantize kernel before its consumers (unfused); auto = fused for activations "
+                         "of at most 4096 values, unfused for larger ones")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100}[args.config]

@@ -125,21 +125,6 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // binary32 -> binary16, round to nearest even, saturating at +-65504
 __device__ __forceinline__ __half f16_sat(float v) { return __float2half_rn(fminf(fmaxf(v, -65504.0f), 65504.0f)); }
 
-// roundf(x / d) for the q8_1 code of x, exactly as the IEEE quotient would
-// give it.  Fast path: t = x * r with r = RN(1/d) differs from x/d by at most
-// 2^-23 |x/d| <= 1.6e-5, and RN(x/d) from x/d by at most 7.7e-6 (|x/d| <= 127.5),
-// so unless t lies within 2^-15 of a half-integer both round to the same
-// integer; near a tie (or if 1/d overflowed) the quotient is computed with an
-// IEEE division.
-__device__ __forceinline__ int q81_code(float x, float d, float r)
-{
-    const float t = x * r;
-    const float a = fabsf(t);
-    const float fr = a - truncf(a);
-    if (fabsf(fr - 0.5f) > 3.0517578125e-05f && a < 128.0f) return (int)roundf(t);
-    return (int)roundf(__fdiv_rn(x, d));
-}
-
 // q8_1 quantization of one 32-value block held by 8 consecutive lanes (lane
 // group 8j..8j+7 of the warp, 4 values each, all 32 lanes participating):
 // d = amax/127 (binary32 division), q = roundf(x/d) (0 when d == 0).  Returns
@@ -147,6 +132,13 @@ __device__ __forceinline__ int q81_code(float x, float d, float r)
 // s4 the sum of this lane's 4 codes.  Used by the standalone quantizer and by
 // the GEMV kernels that quantize their activation themselves, so both produce
 // the same codes bit for bit.
+//
+// roundf(x/d) is taken from t = x * r with r = RN(1/d): t differs from x/d by
+// at most 2^-23 |x/d| <= 1.6e-5 and RN(x/d) from x/d by at most 7.7e-6
+// (|x/d| <= 127.5), so unless t lies within 2^-15 of a half-integer both round
+// to the same integer.  Near a tie (or if 1/d overflowed) the code is taken
+// from the IEEE quotient instead; that path is entered warp-uniformly and only
+// when some lane needs it, so the common case has no branches.
 __device__ __forceinline__ uint32_t q81_quant8(float4 v, float &d, int &s4)
 {
     float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
@@ -154,17 +146,30 @@ __device__ __forceinline__ uint32_t q81_quant8(float4 v, float &d, int &s4)
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     d = __fdiv_rn(amax, 127.0f);
-    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-    if (d > 0.0f) {
-        const float r = __frcp_rn(d);
-        q0 = q81_code(v.x, d, r);
-        q1 = q81_code(v.y, d, r);
-        q2 = q81_code(v.z, d, r);
-        q3 = q81_code(v.w, d, r);
+    const bool live = d > 0.0f;
+    const float r = live ? __frcp_rn(d) : 0.0f;
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    int q[4];
+    bool near = false;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const float t = x[j] * r;
+        const float a = fabsf(t);
+        const float fr = a - truncf(a);
+        near |= !(fabsf(fr - 0.5f) > 3.0517578125e-05f && a < 128.0f);
+        q[j] = (int)roundf(t);
     }
-    s4 = q0 + q1 + q2 + q3;
-    return (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) | ((uint32_t)(q2 & 0xff) << 16) |
-           ((uint32_t)(q3 & 0xff) << 24);
+    near = near && live;
+    if (__any_sync(0xffffffffu, near)) {
+        if (near) {
+#pragma unroll
+            for (int j = 0; j < 4; j++) q[j] = (int)roundf(__fdiv_rn(x[j], d));
+        }
+    }
+    if (!live) q[0] = q[1] = q[2] = q[3] = 0;
+    s4 = q[0] + q[1] + q[2] + q[3];
+    return (uint32_t)(q[0] & 0xff) | ((uint32_t)(q[1] & 0xff) << 8) | ((uint32_t)(q[2] & 0xff) << 16) |
+           ((uint32_t)(q[3] & 0xff) << 24);
 }
 
 // stored binary16 s of a q8_1 block: s = d * sum(q) in binary32, then binary16

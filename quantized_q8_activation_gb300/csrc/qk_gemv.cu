@@ -167,40 +167,45 @@ __device__ void stage_act_q6k(const int8_t *__restrict__ codes, const __half2 *_
 // f32 front end: quantize the activation into the same shared-memory image
 // (Q6 selects the Q6_K side data).  8 lanes per 32-value block, 4 values per
 // lane; CTA 0 also writes the codes and scales out when asked to.
-template <int M, int NT, bool Q6>
-__device__ void stage_quant(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
+// U float4 per thread per batch, all of them loaded before any is quantized; the
+// batch loop has no early exit, so the U blocks' shuffle and division chains
+// interleave (lanes past the end quantize zeros and store nothing)
+template <int M, int NT, bool Q6, int U>
+__device__ void stage_quant_u(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
 {
-    constexpr int U = 8;                                   // loads in flight per thread
     const int K = a.K, k4n = K >> 2, total = M * k4n;      // total is a multiple of 8
     const int nb = K >> 5;
     const bool out = a.codes_out != nullptr && blockIdx.x == 0;
     for (int base = 0; base < total; base += NT * U) {
         float4 v[U];
+        int idx[U];
 #pragma unroll
         for (int u = 0; u < U; u++) {
             const int i = base + u * NT + threadIdx.x;
+            idx[u] = -1;
             v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (i < total) {
+                idx[u] = i;
                 const int m = i / k4n, k4 = i - m * k4n;
                 v[u] = *reinterpret_cast<const float4 *>(a.x + m * a.ldx + 4 * k4);
             }
         }
+        float d[U];
+        int s4[U];
+        uint32_t packed[U];
+#pragma unroll
+        for (int u = 0; u < U; u++) packed[u] = qk::q81_quant8(v[u], d[u], s4[u]);
 #pragma unroll
         for (int u = 0; u < U; u++) {
-            const int i = base + u * NT + threadIdx.x;
-            if (base + u * NT >= total) break;             // uniform: the whole batch row is past the end
-            const bool ok = i < total;
-            const int m = ok ? i / k4n : 0, k4 = ok ? i - m * k4n : 0;
-            float d;
-            int s4;
-            const uint32_t packed = qk::q81_quant8(v[u], d, s4);
-            int s16 = s4 + __shfl_xor_sync(0xffffffffu, s4, 1);
+            int s16 = s4[u] + __shfl_xor_sync(0xffffffffu, s4[u], 1);
             s16 += __shfl_xor_sync(0xffffffffu, s16, 2);                  // 16 values (4 lanes)
             const int s32 = s16 + __shfl_xor_sync(0xffffffffu, s16, 4);   // the 32-value block
-            if (ok) {
+            const int i = idx[u];
+            if (i >= 0) {
+                const int m = i / k4n, k4 = i - m * k4n;
                 const int c = k4 >> 2, sub = k4 & 7;
-                *reinterpret_cast<uint32_t *>(s_codes + (size_t)m * K + 16 * swz(c) + 4 * (k4 & 3)) = packed;
-                const __half dh = qk::f16_sat(d);
+                *reinterpret_cast<uint32_t *>(s_codes + (size_t)m * K + 16 * swz(c) + 4 * (k4 & 3)) = packed[u];
+                const __half dh = qk::f16_sat(d[u]);
                 const float da = __half2float(dh);                         // the stored scale is what the dot uses
                 if (!Q6) {
                     if (sub == 0) {
@@ -211,13 +216,25 @@ __device__ void stage_quant(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
                     s_side[m * (K >> 4) + q6_side_pos(c)] = make_float2(da, -32.0f * da * (float)s16);
                 }
                 if (out) {
-                    *reinterpret_cast<uint32_t *>(a.codes_out + (size_t)m * K + 4 * k4) = packed;
+                    *reinterpret_cast<uint32_t *>(a.codes_out + (size_t)m * K + 4 * k4) = packed[u];
                     if (sub == 0)
-                        a.scales_out[(size_t)m * nb + (k4 >> 3)] = __halves2half2(dh, qk::q81_sum_f16(d, s32));
+                        a.scales_out[(size_t)m * nb + (k4 >> 3)] = __halves2half2(dh, qk::q81_sum_f16(d[u], s32));
                 }
             }
         }
     }
+}
+
+// quantize the M x K f32 activation into the CTA's shared-memory q8_1 copy, with the
+// batch size matched to the float4 count per thread
+template <int M, int NT, bool Q6>
+__device__ void stage_quant(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
+{
+    const int per = (M * (a.K >> 2) + NT - 1) / NT;
+    if (per <= 1) stage_quant_u<M, NT, Q6, 1>(a, s_codes, s_side);
+    else if (per <= 2) stage_quant_u<M, NT, Q6, 2>(a, s_codes, s_side);
+    else if (per <= 4) stage_quant_u<M, NT, Q6, 4>(a, s_codes, s_side);
+    else stage_quant_u<M, NT, Q6, 8>(a, s_codes, s_side);
 }
 
 // ------------------------------------------------------------ row reduce
@@ -692,7 +709,7 @@ int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, uns
     const int warps = warps_for((int)M, fused);
     // ring | activation codes | side data
     const size_t smem = (size_t)warps * (qtype == QK_TYPE_Q4_K ? Q4_R * Q4_SLOT : Q6_R * Q6_SLOT) +
-                        (size_t)M * K + (size_t)M * (K / 32) * (qtype == QK_TYPE_Q4_K ? 8 : 16);
+                  (size_t)M * K + (size_t)M * (K / 32) * (qtype == QK_TYPE_Q4_K ? 8 : 16);
     if (smem > qk::max_smem_optin()) return QK_E_SHAPE;
     gemv_fn kern = fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M);
     int st = prepare(kern, g_smem_set[qtype == QK_TYPE_Q4_K ? 0 : 1][fused ? 1 : 0][M - 1], smem);

@@ -24,21 +24,22 @@ def sample_rows(N, n=24, seed=0):
     return sorted(r for r in rows if 0 <= r < N)
 
 
-@pytest.mark.parametrize("cfg_id,fused", [(0, True), (1, True), (2, True), (3, True), (1, False), (3, False),
-                                         (4, False)])
-def test_config_full_size(cfg_id, fused):
+@pytest.mark.parametrize("cfg_id,front_end", [(0, "fused"), (1, "fused"), (2, "fused"), (3, "fused"), (1, "unfused"),
+                                              (3, "unfused"), (1, "auto"), (4, "auto")])
+def test_config_full_size(cfg_id, front_end):
     import bench
     wl = bench.Workload(cfg_id, seed=0, copies=1)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        wl.step(0, pdl=True, stream=stream, fused=fused)
-        wl.step(0, pdl=True, stream=stream, fused=fused)          # twice: PDL chaining across steps
+        wl.step(0, pdl=True, stream=stream, front_end=front_end)
+        wl.step(0, pdl=True, stream=stream, front_end=front_end)  # twice: PDL chaining across steps
     torch.cuda.synchronize()
     cfg = wl.cfg
     q8 = {}
+    quantized = {g[5] for g in cfg["gemms"] if not bench.gemm_fused(front_end, cfg, g)}
     for s, x in wl.host_x.items():
         c, d, sref = oracle.quantize_q8_1(x)
-        if not fused:
+        if s in quantized:
             codes, scales = wl.q8[s]
             sc = scales.cpu().numpy().view(np.uint16)
             assert np.array_equal(codes.cpu().numpy(), c), s
