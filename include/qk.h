@@ -207,9 +207,20 @@ int qk_gemv_q6k_f32(const void *w, const float *x, int64_t ldx,
  * "15 . The CUDA backend" sec. 2.3 and 3.2.6).
  *
  * w, codes, scales, residual, y: as for qk_gemv_q4k.
- * Ranges: M >= 1, N >= 1, K % 256 == 0, K >= 256.  (M == 0 is a no-op.)
- * workspace: device scratch of qk_mmq_workspace_bytes() bytes, 256-byte
- *   aligned, or NULL when that size is 0.  Not read before written.
+ * Ranges: M >= 1, N >= 1, K % 256 == 0, K >= 256, ceil(M/128) <= 65535 and
+ * ceil(N/128) <= 65535.  (M == 0 is a no-op.)
+ * Activations must satisfy max |x| < 32000 per 32-value block (the exact
+ * f16 operand split of d * q and of d * sum(q) / 16 must not overflow).
+ * workspace: device scratch of at least qk_mmq_workspace_bytes(M, N, K)
+ *   bytes, 256-byte aligned, not overlapping any other argument.  The call
+ *   writes it (the q8_1 activation expanded once per 128-row tile into the
+ *   tensor-core operand layout) before reading it; nothing needs to be
+ *   initialised.  Its contents are consumed by kernels of this call that run
+ *   after the call returns, so the workspace must not be reused by work that
+ *   is not ordered after this call on `stream`.  Size:
+ *   ceil(M/128) * (K * 512 + (K/256) * 8192) bytes
+ *   (M = 2048, K = 18944: 164,888,576 bytes).
+ * Returns QK_E_WORKSPACE if workspace_bytes is too small.
  */
 int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
 

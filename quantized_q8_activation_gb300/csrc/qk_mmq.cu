@@ -19,26 +19,35 @@
 // (8 values + 8 zeros) of S (hi/lo) against Mw (hi/lo) into U.  The result is
 // Y - U (+ R).
 //
-// One CTA (16 warps) per 128 x 128 output tile and per SM (all 512 TMEM
-// columns: Y | T0 | T1 | U):
-//   warp 0      TMEM allocation; lane 0 issues every MMA and commit
-//   warp 1      lane 0 streams the raw inputs with 2D TMA tensor copies into a
-//               ring in shared memory: per 64-value K stage the activation
-//               codes (128 x 64 B) and the two 16-byte halves of the Q4_K code
-//               bytes (128 x 16 B each); per superblock the q8_1 scale pairs
-//               (128 x 32 B) and the Q4_K metadata records (128 x 16 B)
-//   warps 4-7   fold T into Y per superblock, then the epilogue (TMEM lane
-//               quadrant = warp % 4)
-//   warps 8-15  operand converters: raw codes + d_a -> A_hi / A_lo and Q4_K
-//               codes + scales -> B per K stage, written straight into the
-//               UMMA K-major SWIZZLE_128B layout; S and Mw entries into
-//               SWIZZLE_32B tiles
-// Stages are handed over with mbarriers (raw full: TMA transaction bytes;
-// raw empty: converters -> producer; full: converters -> MMA; empty: MMA
-// commit -> converters; T buffers: MMA commit -> fold, fold -> MMA).  Every
-// wait is bounded; a wait that gives up sets a device error flag
-// (qk_error_flags), and once it is set the other waits return after a few
-// polls, so the kernel runs to its end.
+// Two kernels per call:
+//  1. mmq_prep_kernel expands the q8_1 activation once per 128-row M-tile into
+//     the caller's workspace, already in the tensor core's shared-memory
+//     layout: per 64-value K stage a 32 KB block (A_hi and A_lo tiles, K-major
+//     SWIZZLE_128B), per superblock an 8 KB block (S_hi and S_lo tiles,
+//     K-major SWIZZLE_32B, zero padded).  Every N-tile then copies these
+//     blocks instead of converting the activation again.
+//  2. mmq_q4k_kernel, one CTA (16 warps) per 128 x 128 output tile and per SM
+//     (all 512 TMEM columns: Y | T0 | T1 | U):
+//       warp 0      TMEM allocation; lane 0 issues every MMA and commit
+//       warp 1      lane 0 copies the A stage blocks (and the S block of each
+//                   superblock) from the workspace straight into the operand
+//                   stages with cp.async.bulk
+//       warp 2      lane 0 streams the raw Q4_K bytes with 2D TMA tensor
+//                   copies into a ring: per K stage the two 16-byte halves of
+//                   the code bytes (128 x 16 B each), per superblock the
+//                   metadata records (128 x 16 B)
+//       warps 4-7   fold T into Y per superblock, then the epilogue (TMEM lane
+//                   quadrant = warp % 4)
+//       warps 8-15  weight converters: Q4_K codes + scales -> B per K stage in
+//                   the SWIZZLE_128B layout, and the Mw entries
+// Stages are handed over with mbarriers (full: converters + copy bytes -> MMA;
+// empty: MMA commit -> copy and converters; raw: TMA bytes -> converters ->
+// producer; T buffers: MMA commit -> fold, fold -> MMA).  Every wait is
+// bounded; a wait that gives up sets a device error flag (qk_error_flags), and
+// once it is set the other waits return after a few polls, so the kernel runs
+// to its end.  Before the CTA releases its tensor memory and exits, the MMA
+// thread waits for its last MMAs and the producers wait for their last copies
+// (bounded too), so nothing is left in flight.
 #include "qk_common.cuh"
 #include "qk_tc.cuh"
 
@@ -47,13 +56,13 @@
 #include <atomic>
 
 #ifndef QK_MMQ_NST
-#define QK_MMQ_NST 2        // converted operand stages
+#define QK_MMQ_NST 3        // operand stages
 #endif
 #ifndef QK_MMQ_RAW
-#define QK_MMQ_RAW 5        // raw K stages in flight
+#define QK_MMQ_RAW 8        // raw weight K stages in flight
 #endif
 #ifndef QK_MMQ_SBRAW
-#define QK_MMQ_SBRAW 2      // raw per-superblock slots in flight
+#define QK_MMQ_SBRAW 4      // raw metadata superblocks in flight
 #endif
 
 __device__ unsigned g_qk_errors;
@@ -67,15 +76,17 @@ constexpr int NST = QK_MMQ_NST, NRAW = QK_MMQ_RAW, NSB = QK_MMQ_SBRAW;
 constexpr int kThreads = 512;
 constexpr int kFoldWarp0 = 4, kConvWarp0 = 8;
 constexpr int kConv = 256, kFold = 128;
+constexpr int kConvWarps = kConv / 32, kFoldWarps = kFold / 32;   // barrier arrivals: one per warp
 
 constexpr int TILE = BM * BK * 2;               // 16 KB: 128 rows x 64 f16, SWIZZLE_128B K-major
 constexpr int STAGE = 3 * TILE;                 // A_hi | A_lo | B
+constexpr int ABLOCK = 2 * TILE;                // workspace block of one M-tile and K stage: A_hi | A_lo
 constexpr int MTILE = 128 * 16 * 2;             // 4 KB: 128 rows x 16 f16, SWIZZLE_32B K-major
 constexpr int MSET = 4 * MTILE;                 // S_hi | S_lo | Mw_hi | Mw_lo
-// raw K stage: activation codes 128 x 64 B | code bytes, first halves 128 x 16 B | second halves
-constexpr int RAW_A = 0, RAW_B0 = BM * 64, RAW_B1 = RAW_B0 + BN * 16, RAW = RAW_B1 + BN * 16;
-// raw superblock slot: q8_1 scale pairs 128 x 8 x 4 B | metadata records 128 x 16 B
-constexpr int SBR_S = 0, SBR_M = BM * 32, SBR = SBR_M + BN * 16;
+constexpr int SBLOCK = 2 * MTILE;               // workspace block of one M-tile and superblock: S_hi | S_lo
+// raw weight K stage: code bytes, first halves 128 x 16 B | second halves 128 x 16 B
+constexpr int RAW_B0 = 0, RAW_B1 = BN * 16, RAW = 2 * BN * 16;
+constexpr int SBR = BN * 16;                    // raw metadata records of one superblock
 constexpr int OFF_MIN = NST * STAGE;
 constexpr int OFF_RAW = OFF_MIN + 2 * MSET;
 constexpr int OFF_SBR = OFF_RAW + NRAW * RAW;
@@ -91,19 +102,22 @@ enum {
     B_REMPTY = B_RFULL + NRAW,
     B_SFULL = B_REMPTY + NRAW,
     B_SEMPTY = B_SFULL + NSB,
-    NBAR = B_SEMPTY + NSB
+    B_DONE = B_SEMPTY + NSB,       // every MMA of the CTA has completed
+    NBAR = B_DONE + 1
 };
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
 constexpr int SMEM = OFF_TMEM + 16 + 1024;      // + slack to align the base to 1024
 static_assert(SMEM <= 232448, "shared memory plan exceeds the per-block opt-in limit");
-static_assert(RAW % 1024 == 0 && SBR % 1024 == 0 && OFF_RAW % 1024 == 0, "TMA destinations stay aligned");
+static_assert(OFF_RAW % 1024 == 0 && OFF_SBR % 1024 == 0 && RAW % 1024 == 0, "copy destinations stay aligned");
 constexpr uint32_t COL_Y = 0, COL_T0 = 128, COL_U = 384, TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 
 // byte offset of 16-byte chunk c of row r in a SWIZZLE_128B K-major tile (rows of 128 bytes)
-__device__ __forceinline__ uint32_t sw128(int r, int c) { return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4); }
+__host__ __device__ constexpr uint32_t sw128(int r, int c) { return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4); }
 // byte offset of element j (< 8, first 16-byte chunk) of row r in a SWIZZLE_32B K-major tile (rows of 32 bytes)
-__device__ __forceinline__ uint32_t sw32(int r, int j) { return (r >> 3) * 256 + (r & 7) * 32 + (((r >> 2) & 1) << 4) + 2 * j; }
+__host__ __device__ constexpr uint32_t sw32(int r, int j) { return (r >> 3) * 256 + (r & 7) * 32 + (((r >> 2) & 1) << 4) + 2 * j; }
+// byte offset of the second (always zero) 16-byte chunk of row r in a SWIZZLE_32B K-major tile
+__host__ __device__ constexpr uint32_t sw32_pad(int r) { return (r >> 3) * 256 + (r & 7) * 32 + ((((r >> 2) & 1) ^ 1) << 4); }
 
 __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity) { mbar_wait(bar, parity, &g_qk_errors); }
 
@@ -114,14 +128,14 @@ __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__
 
 struct MmqArgs {
     const uint8_t *w;       // repacked Q4_K weight (the fold reads d_b from its metadata)
+    const uint8_t *wsA;     // workspace: [M-tiles][K/64] A blocks
+    const uint8_t *wsS;     //            [M-tiles][K/256] S blocks
     int64_t M, N, K;
     const float *residual;
     float *y;
 };
 
 struct MmqMaps {
-    CUtensorMap codes;      // uint8  [M][K]          box 64 x 128
-    CUtensorMap scales;     // uint32 [M][K/32]       box 8 x 128   (q8_1 (d, s) pairs)
     CUtensorMap wcodes;     // uint8  [N][B*128]      box 16 x 128  (code plane of the repacked weight)
     CUtensorMap meta;       // uint8  [N][B*16]       box 16 x 128  (metadata plane)
 };
@@ -165,42 +179,74 @@ __device__ __forceinline__ void split_f16(float v, __half &hi, __half &lo)
     lo = __float2half_rn(v - __half2float(hi));
 }
 
-// one converter thread's share of K stage `it` (smem stage st = it % NST): reads its raw inputs
-// from the TMA ring, writes the A_hi / A_lo / B chunks of tile row `row`, half h, and min-term
+// ------------------------------------------------------------- prep kernel
+// CTA (superblock sb, M-tile mt), 256 threads, 4 items each: item (row, j) is
+// the 32-value q8_1 block j of superblock sb of activation row 128 mt + row.
+// It writes the block's 32 (A_hi, A_lo) pairs into the stage block of K stage
+// 4 sb + j/2 (chunks 4 (j&1) .. +3) and the S entry j of its row; rows past M
+// are written as zeros.
+__global__ void __launch_bounds__(256) mmq_prep_kernel(const int8_t *__restrict__ codes,
+                                                       const __half2 *__restrict__ scales, int64_t M, int64_t K,
+                                                       uint8_t *__restrict__ wsA, uint8_t *__restrict__ wsS)
+{
+    qk::pdl_launch_dependents();
+    qk::pdl_wait();                              // codes may come from the previous kernel
+    const int sb = blockIdx.x, mt = blockIdx.y;
+    const int B = (int)(K >> 8), nstage = (int)(K >> 6);
+#pragma unroll 1
+    for (int i = 0; i < 4; i++) {
+        const int q = threadIdx.x + 256 * i;
+        const int row = q >> 3, j = q & 7, h = j & 1;
+        const int64_t m = (int64_t)mt * BM + row;
+        uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
+        uint32_t dbits = 0;
+        if (m < M) {
+            const int8_t *src = codes + m * K + sb * 256 + 32 * j;
+            a0 = *reinterpret_cast<const uint4 *>(src);
+            a1 = *reinterpret_cast<const uint4 *>(src + 16);
+            dbits = *reinterpret_cast<const uint32_t *>(scales + m * (K >> 5) + 8 * sb + j) & 0xffffu;
+        }
+        const __half dah = __ushort_as_half((unsigned short)dbits);
+        const __half2 d2 = __halves2half2(dah, dah);
+        const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        uint8_t *tA = wsA + ((size_t)mt * nstage + 4 * sb + (j >> 1)) * ABLOCK;
+        int qsum = 0;
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            uint32_t hi[4], lo[4];
+            conv_a(aw[2 * c], d2, hi[0], lo[0], hi[1], lo[1]);
+            conv_a(aw[2 * c + 1], d2, hi[2], lo[2], hi[3], lo[3]);
+            sts128(tA, sw128(row, 4 * h + c), hi[0], hi[1], hi[2], hi[3]);
+            sts128(tA + TILE, sw128(row, 4 * h + c), lo[0], lo[1], lo[2], lo[3]);
+            qsum = qk::dp4a_ss(aw[2 * c], 0x01010101u, qsum);
+            qsum = qk::dp4a_ss(aw[2 * c + 1], 0x01010101u, qsum);
+        }
+        uint8_t *tS = wsS + ((size_t)mt * B + sb) * SBLOCK;
+        __half shi, slo;
+        split_f16(__half2float(dah) * (float)qsum * 0.0625f, shi, slo);
+        *reinterpret_cast<__half *>(tS + sw32(row, j)) = shi;
+        *reinterpret_cast<__half *>(tS + MTILE + sw32(row, j)) = slo;
+        if (j < 2) *reinterpret_cast<uint4 *>(tS + j * MTILE + sw32_pad(row)) = make_uint4(0, 0, 0, 0);
+    }
+}
+
+// ------------------------------------------------------------- main kernel
+
+// one converter thread's share of K stage `it` (operand stage st = it % NST): reads its raw weight
+// bytes from the TMA ring, writes four B chunks of tile row `row` (half h of group g) and the Mw
 // entry j = 2g + h, releases the raw slots and signals the stage full
 __device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, int it, int row, int h, int st)
 {
     const int sb = it >> 2, g = it & 3, tb = sb & 1;
     const int rs = it % NRAW, ss = sb % NSB;
-    // ---- raw inputs
     wait_bar(&bar[B_RFULL + rs], (it / NRAW) & 1);
     if (g == 0) wait_bar(&bar[B_SFULL + ss], (sb / NSB) & 1);
-    const uint8_t *raw = smem + OFF_RAW + rs * RAW;
-    const uint8_t *sbr = smem + OFF_SBR + ss * SBR;
-    const uint4 a0 = *reinterpret_cast<const uint4 *>(raw + RAW_A + row * 64 + 32 * h);
-    const uint4 a1 = *reinterpret_cast<const uint4 *>(raw + RAW_A + row * 64 + 32 * h + 16);
-    const uint4 bq = *reinterpret_cast<const uint4 *>(raw + (h ? RAW_B1 : RAW_B0) + row * 16);
-    const uint32_t da = *reinterpret_cast<const uint32_t *>(sbr + SBR_S + row * 32 + (2 * g + h) * 4);
-    const uint4 mt = *reinterpret_cast<const uint4 *>(sbr + SBR_M + row * 16);
+    const uint4 bq = *reinterpret_cast<const uint4 *>(smem + OFF_RAW + rs * RAW + (h ? RAW_B1 : RAW_B0) + row * 16);
+    const uint4 mt = *reinterpret_cast<const uint4 *>(smem + OFF_SBR + ss * SBR + row * 16);
 
     if (it >= NST) wait_bar(&bar[B_EMPTY + st], ((it / NST) + 1) & 1);
     if (g == 0 && sb >= 2) wait_bar(&bar[B_MINEMPTY + tb], ((sb - 2) >> 1) & 1);
     uint8_t *s0 = smem + st * STAGE;
-    // ---- A: d_a * q_a as hi/lo f16 at stage k = 32h .. 32h+31 (chunks 4h .. 4h+3)
-    const __half dah = __ushort_as_half((unsigned short)(da & 0xffffu));
-    const __half2 d2 = __halves2half2(dah, dah);
-    const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    int qsum = 0;
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-        uint32_t hi[4], lo[4];
-        conv_a(aw[2 * q], d2, hi[0], lo[0], hi[1], lo[1]);
-        conv_a(aw[2 * q + 1], d2, hi[2], lo[2], hi[3], lo[3]);
-        sts128(s0, sw128(row, 4 * h + q), hi[0], hi[1], hi[2], hi[3]);
-        sts128(s0 + TILE, sw128(row, 4 * h + q), lo[0], lo[1], lo[2], lo[3]);
-        qsum = qk::dp4a_ss(aw[2 * q], 0x01010101u, qsum);
-        qsum = qk::dp4a_ss(aw[2 * q + 1], 0x01010101u, qsum);
-    }
     // ---- B: this half of group g; low nibbles = sub-block 2g at stage k 16h .. 16h+15,
     //      high nibbles = sub-block 2g+1 at stage k 32+16h .. 32+16h+15
     const uint32_t rec = __byte_perm(__byte_perm(mt.y, mt.z, g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u), mt.w,
@@ -217,24 +263,25 @@ __device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, int 
     sts128(s0 + 2 * TILE, sw128(row, 2 * h + 1), L[4], L[5], L[6], L[7]);
     sts128(s0 + 2 * TILE, sw128(row, 4 + 2 * h), H[0], H[1], H[2], H[3]);
     sts128(s0 + 2 * TILE, sw128(row, 4 + 2 * h + 1), H[4], H[5], H[6], H[7]);
-    // ---- min term entry j = 2g + h: S = d_a sum(q_a) / 16, Mw = 16 dmin m_j
+    // ---- min term entry j = 2g + h: Mw = 16 dmin m_j
     uint8_t *ms = smem + OFF_MIN + tb * MSET;
     const int j = 2 * g + h;
-    __half shi, slo, whi, wlo;
-    split_f16(__half2float(dah) * (float)qsum * 0.0625f, shi, slo);
+    __half whi, wlo;
     const float dmin = __half2float(__ushort_as_half((unsigned short)(mt.x >> 16)));
     split_f16(dmin * (float)(h ? mn1 : mn0) * 16.0f, whi, wlo);
-    *reinterpret_cast<__half *>(ms + sw32(row, j)) = shi;
-    *reinterpret_cast<__half *>(ms + MTILE + sw32(row, j)) = slo;
     *reinterpret_cast<__half *>(ms + 2 * MTILE + sw32(row, j)) = whi;
     *reinterpret_cast<__half *>(ms + 3 * MTILE + sw32(row, j)) = wlo;
-    // Release the raw slots only now: every value read from them has been consumed by the
-    // arithmetic above, so no shared load of this thread can still be pending when the producer
-    // lets the next TMA copy (async proxy) overwrite the slot.
-    mbar_arrive(&bar[B_REMPTY + rs]);
-    if (g == 3) mbar_arrive(&bar[B_SEMPTY + ss]);
+    // Each lane makes its own stores visible to the tensor core (async proxy); after the warp
+    // has synchronised, one lane arrives for the whole warp.  The raw slots are released only
+    // now: every value read from them has been consumed by the arithmetic above, so no shared
+    // load can still be pending when the producer lets the next TMA copy overwrite the slot.
     fence_proxy_async();
-    mbar_arrive(&bar[B_FULL + st]);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        mbar_arrive(&bar[B_REMPTY + rs]);
+        if (g == 3) mbar_arrive(&bar[B_SEMPTY + ss]);
+        mbar_arrive(&bar[B_FULL + st]);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
@@ -245,24 +292,28 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     float *dB = reinterpret_cast<float *>(smem + OFF_DB);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+    const int mtile = blockIdx.x;
+    const int m0 = mtile * BM, n0 = blockIdx.y * BN;
     const int B = (int)(a.K >> 8), nit = 4 * B;
 
     qk::pdl_launch_dependents();
-    // setup: barriers, zero padding of the min-term tiles, TMEM allocation
+    // setup: barriers, zero padding of the Mw tiles, TMEM allocation
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; i++) mbar_init(&bar[B_FULL + i], kConv), mbar_init(&bar[B_EMPTY + i], 1);
+        for (int i = 0; i < NST; i++) mbar_init(&bar[B_FULL + i], kConvWarps + 1), mbar_init(&bar[B_EMPTY + i], 1);
         for (int i = 0; i < 2; i++) {
             mbar_init(&bar[B_MINEMPTY + i], 1);
             mbar_init(&bar[B_TFULL + i], 1);
-            mbar_init(&bar[B_TEMPTY + i], kFold);
+            mbar_init(&bar[B_TEMPTY + i], kFoldWarps);
         }
-        for (int i = 0; i < NRAW; i++) mbar_init(&bar[B_RFULL + i], 1), mbar_init(&bar[B_REMPTY + i], kConv);
-        for (int i = 0; i < NSB; i++) mbar_init(&bar[B_SFULL + i], 1), mbar_init(&bar[B_SEMPTY + i], kConv);
+        for (int i = 0; i < NRAW; i++) mbar_init(&bar[B_RFULL + i], 1), mbar_init(&bar[B_REMPTY + i], kConvWarps);
+        for (int i = 0; i < NSB; i++) mbar_init(&bar[B_SFULL + i], 1), mbar_init(&bar[B_SEMPTY + i], kConvWarps);
+        mbar_init(&bar[B_DONE], 1);
         mbar_init_fence();
     }
-    for (int i = threadIdx.x; i < 2 * MSET / 16; i += kThreads)
-        reinterpret_cast<uint4 *>(smem + OFF_MIN)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < 2 * (SBLOCK / 16); i += kThreads) {
+        const int set = i / (SBLOCK / 16), k = i % (SBLOCK / 16);
+        reinterpret_cast<uint4 *>(smem + OFF_MIN + set * MSET + SBLOCK)[k] = make_uint4(0, 0, 0, 0);
+    }
     fence_proxy_async();                         // the zero padding is read by the tensor core
     if (warp == 0) {
         tmem_alloc(tmem_ptr, TMEM_COLS);
@@ -309,13 +360,34 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
                 mma_commit(&bar[B_MINEMPTY + tb]);
                 mma_commit(&bar[B_TFULL + tb]);
             }
+            // teardown: no MMA may still be running when the TMEM is released
+            mma_commit(&bar[B_DONE]);
+            wait_bar(&bar[B_DONE], 0);
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------ activation stage copies
         if (lane == 0) {
-            prefetch_tmap(&maps.codes);
-            prefetch_tmap(&maps.scales);
+            const int nstage = nit;
+            const uint8_t *srcA = a.wsA + (size_t)mtile * nstage * ABLOCK;
+            const uint8_t *srcS = a.wsS + (size_t)mtile * B * SBLOCK;
+            for (int it = 0; it < nit; it++) {
+                const int sb = it >> 2, g = it & 3, st = it % NST, tb = sb & 1;
+                if (it >= NST) wait_bar(&bar[B_EMPTY + st], ((it / NST) + 1) & 1);
+                if (g == 0 && sb >= 2) wait_bar(&bar[B_MINEMPTY + tb], ((sb - 2) >> 1) & 1);
+                mbar_arrive_expect_tx(&bar[B_FULL + st], ABLOCK + (g == 0 ? SBLOCK : 0));
+                bulk_copy_g2s(smem + st * STAGE, srcA + (size_t)it * ABLOCK, ABLOCK, &bar[B_FULL + st]);
+                if (g == 0)
+                    bulk_copy_g2s(smem + OFF_MIN + tb * MSET, srcS + (size_t)sb * SBLOCK, SBLOCK, &bar[B_FULL + st]);
+            }
+            // teardown: every copy this thread issued has landed (normally long since consumed)
+            for (int it = nit - NST < 0 ? 0 : nit - NST; it < nit; it++)
+                wait_bar(&bar[B_FULL + it % NST], (it / NST) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------ raw weight TMA producer
+        if (lane == 0) {
             prefetch_tmap(&maps.wcodes);
             prefetch_tmap(&maps.meta);
             for (int it = 0; it < nit; it++) {
@@ -323,27 +395,27 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
                 if (g == 0) {
                     const int ss = sb % NSB;
                     if (sb >= NSB) wait_bar(&bar[B_SEMPTY + ss], ((sb / NSB) + 1) & 1);
-                    uint8_t *d = smem + OFF_SBR + ss * SBR;
                     mbar_arrive_expect_tx(&bar[B_SFULL + ss], SBR);
-                    tma_load_2d(d + SBR_S, &maps.scales, 8 * sb, m0, &bar[B_SFULL + ss]);
-                    tma_load_2d(d + SBR_M, &maps.meta, 16 * sb, n0, &bar[B_SFULL + ss]);
+                    tma_load_2d(smem + OFF_SBR + ss * SBR, &maps.meta, 16 * sb, n0, &bar[B_SFULL + ss]);
                 }
                 const int rs = it % NRAW;
                 if (it >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((it / NRAW) + 1) & 1);
                 uint8_t *d = smem + OFF_RAW + rs * RAW;
                 const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s) + g;
                 mbar_arrive_expect_tx(&bar[B_RFULL + rs], RAW);
-                tma_load_2d(d + RAW_A, &maps.codes, 256 * sb + 64 * g, m0, &bar[B_RFULL + rs]);
                 tma_load_2d(d + RAW_B0, &maps.wcodes, 1024 * s + 16 * u, n0, &bar[B_RFULL + rs]);
                 tma_load_2d(d + RAW_B1, &maps.wcodes, 1024 * s + 16 * G + 16 * u, n0, &bar[B_RFULL + rs]);
             }
+            // teardown: every copy this thread issued has landed (normally long since consumed)
+            for (int it = nit - NRAW < 0 ? 0 : nit - NRAW; it < nit; it++)
+                wait_bar(&bar[B_RFULL + it % NRAW], (it / NRAW) & 1);
+            for (int sb = B - NSB < 0 ? 0 : B - NSB; sb < B; sb++) wait_bar(&bar[B_SFULL + sb % NSB], (sb / NSB) & 1);
         }
         __syncwarp();
     } else if (warp >= kFoldWarp0 && warp < kConvWarp0) {
         // -------------------------------------------------------------- fold
         const int ft = threadIdx.x - kFoldWarp0 * 32;            // 0..127: the column whose d_b it loads
         const uint32_t lq = (uint32_t)((warp & 3) * 32) << 16;   // TMEM lane quadrant of this warp
-        const int row = (warp & 3) * 32 + lane;                  // output row within the tile
         const int64_t nd = n0 + ft;
         const uint8_t *dsrc = a.w + a.N * (int64_t)B * 128 + nd * B * 16;
         float dnext = nd < a.N ? __half2float(__ushort_as_half(qk::ldg_stream2(dsrc))) : 0.0f;
@@ -372,35 +444,44 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
             }
             tmem_wait_st();
             fence_before_sync();
-            mbar_arrive(&bar[B_TEMPTY + tb]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_TEMPTY + tb]);
         }
-        // epilogue: Y - U (+ R)
-        const int64_t m = m0 + row;
+        // epilogue: Y - U (+ R), one 32 x 32 block per pass: a thread holds row (32q + lane) of the
+        // block; the block is transposed through shared memory (operand stage 0, idle once the last
+        // TFULL has been observed) so that each store writes 32 consecutive columns of one row
+        float *tb_s = reinterpret_cast<float *>(smem) + (warp - kFoldWarp0) * (32 * 33);
+        const int q0 = (warp & 3) * 32;
 #pragma unroll 1
         for (int c = 0; c < 4; c++) {
             float yv[32], uv[32];
             tmem_ld32(tmem + lq + COL_Y + 32 * c, yv);
             tmem_ld32(tmem + lq + COL_U + 32 * c, uv);
             tmem_wait_ld();
-            if (m < a.M) {
-                const int64_t nb = n0 + 32 * c;
-                float *yr = a.y + m * a.N;
-                const float *rr = a.residual ? a.residual + m * a.N : nullptr;
 #pragma unroll
-                for (int j = 0; j < 32; j++) {
-                    const int64_t n = nb + j;
-                    if (n < a.N) {
-                        const float v = yv[j] - uv[j];
-                        yr[n] = rr ? __fadd_rn(v, rr[n]) : v;
+            for (int j = 0; j < 32; j++) tb_s[lane * 33 + j] = yv[j] - uv[j];
+            __syncwarp();
+            const int64_t n = n0 + 32 * c + lane;
+            if (n < a.N) {
+#pragma unroll 4
+                for (int r = 0; r < 32; r++) {
+                    const int64_t m = m0 + q0 + r;
+                    if (m < a.M) {
+                        const float v = tb_s[r * 33 + lane];
+                        const size_t o = (size_t)m * a.N + n;
+                        a.y[o] = a.residual ? __fadd_rn(v, a.residual[o]) : v;
                     }
                 }
             }
+            __syncwarp();
         }
     } else if (warp >= kConvWarp0) {
         // --------------------------------------------------------- converters
-        // Unrolled by the stage count, so the converted stage index is static.
+        // Lanes 0-15 of a warp take 16 consecutive rows of half 0, lanes 16-31 the same rows of
+        // half 1, so every quarter warp stores to 8 distinct 16-byte bank groups.  Unrolled by the
+        // stage count, so the operand stage index is static.
         const int ct = threadIdx.x - kConvWarp0 * 32;             // 0..255
-        const int row = ct >> 1, h = ct & 1;
+        const int row = (ct & 15) + 16 * (ct >> 5), h = (ct >> 4) & 1;
         for (int it = 0; it < nit; it += NST) {
 #pragma unroll
             for (int k = 0; k < NST; k++)
@@ -450,6 +531,13 @@ bool make_map(EncodeTiledFn enc, CUtensorMap *map, CUtensorMapDataType dt, const
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// workspace bytes for an M x K activation: A blocks, then S blocks
+size_t ws_bytes(int64_t M, int64_t K)
+{
+    const size_t mt = (size_t)((M + BM - 1) / BM);
+    return mt * (size_t)(K / 64) * ABLOCK + mt * (size_t)(K / 256) * SBLOCK;
+}
+
 }  // namespace
 
 extern "C" int qk_error_flags(unsigned *flags, int clear)
@@ -467,7 +555,7 @@ extern "C" int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *b
 {
     if (!bytes) return QK_E_NULL;
     if (M < 0 || N < 1 || K < 256 || K % 256 != 0) return QK_E_SHAPE;
-    *bytes = 0;
+    *bytes = ws_bytes(M, K);
     return QK_OK;
 }
 
@@ -475,33 +563,34 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
                           const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,
                           void *stream)
 {
-    (void)workspace;
-    (void)workspace_bytes;
     // TMA coordinates are signed 32-bit: rows and bytes of a row stay below 2^31
     if (M < 0 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || M > 0x7fffffffLL || K > 0x7fffffffLL)
         return QK_E_SHAPE;
     if (M == 0) return QK_OK;
-    if (!w || !codes || !scales || !y) return QK_E_NULL;
+    if (!w || !codes || !scales || !y || !workspace) return QK_E_NULL;
     if (!qk::aligned(w, 16) || !qk::aligned(codes, 16) || !qk::aligned(scales, 16) || !qk::aligned(y, 4) ||
-        (residual && !qk::aligned(residual, 4)))
+        (residual && !qk::aligned(residual, 4)) || !qk::aligned(workspace, 256))
         return QK_E_ALIGN;
+    const size_t need = ws_bytes(M, K);
+    if (workspace_bytes < need) return QK_E_WORKSPACE;
     size_t wbytes = 0;
     qk_repacked_bytes(QK_TYPE_Q4_K, N, K, &wbytes);
     const size_t ybytes = (size_t)M * N * 4, cbytes = (size_t)M * K, sbytes = (size_t)M * (K / 32) * 4;
     if (qk::overlaps(y, ybytes, w, wbytes) || qk::overlaps(y, ybytes, codes, cbytes) ||
-        qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)))
+        qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)) ||
+        qk::overlaps(workspace, need, w, wbytes) || qk::overlaps(workspace, need, codes, cbytes) ||
+        qk::overlaps(workspace, need, scales, sbytes) || qk::overlaps(workspace, need, y, ybytes) ||
+        (residual && qk::overlaps(workspace, need, residual, ybytes)))
         return QK_E_ALIAS;
     const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
-    if (gx > 0x7fffffffLL || gy > 65535) return QK_E_SHAPE;
+    if (gx > 65535 || gy > 65535) return QK_E_SHAPE;
     if ((size_t)SMEM > qk::max_smem_optin()) return QK_E_CUDA;
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return QK_E_CUDA;
     const int64_t B = K / 256;
     const uint8_t *wb = static_cast<const uint8_t *>(w);
     MmqMaps maps;
-    if (!make_map(enc, &maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, K, M, K, 64, BM) ||
-        !make_map(enc, &maps.scales, CU_TENSOR_MAP_DATA_TYPE_UINT32, scales, K / 32, M, K / 8, 8, BM) ||
-        !make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 16, BN) ||
+    if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 16, BN) ||
         !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 16, N, B * 16, 16, BN))
         return QK_E_CUDA;
     static std::atomic<int> attr_set{0};
@@ -511,7 +600,12 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
             return QK_E_CUDA;
         attr_set.store(1);
     }
-    MmqArgs args{wb, M, N, K, residual, y};
+    uint8_t *wsA = static_cast<uint8_t *>(workspace);
+    uint8_t *wsS = wsA + (size_t)gx * (size_t)(K / 64) * ABLOCK;
+    int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, (cudaStream_t)stream,
+                        (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA, wsS);
+    if (st != QK_OK) return st;
+    MmqArgs args{wb, wsA, wsS, M, N, K, residual, y};
     return qk::launch(mmq_q4k_kernel, dim3((unsigned)gx, (unsigned)gy), dim3(kThreads), SMEM, (cudaStream_t)stream,
-                      (flags & QK_LAUNCH_PDL) != 0, args, maps);
+                      true, args, maps);
 }

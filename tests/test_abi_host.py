@@ -56,7 +56,6 @@ def test_sizes(L):
         qk.repacked_bytes(qk.Q4_K, 10, 100)
     with pytest.raises(qk.QKError):
         qk.repacked_bytes(7, 10, 256)
-    assert qk.mmq_workspace_bytes(2048, 4608, 3584) >= 0
 
 
 def call_gemv(L, fn, w=P, codes=P + 0x10000000, scales=P + 0x20000000, M=1, N=64, K=256, r=None,
@@ -118,14 +117,27 @@ def test_repack_rejects(L):
     assert f(qk.Q4_K, P, 4, 256, P + 144, None) == E_ALIAS
 
 
+def test_mmq_workspace_size():
+    # ceil(M/128) * (K*512 + (K/256)*8192)
+    assert qk.mmq_workspace_bytes(2048, 3584, 18944) == 16 * (18944 * 512 + 74 * 8192) == 164888576
+    assert qk.mmq_workspace_bytes(1, 64, 256) == 256 * 512 + 8192
+    assert qk.mmq_workspace_bytes(129, 64, 512) == 2 * (512 * 512 + 2 * 8192)
+    assert qk.mmq_workspace_bytes(0, 64, 256) == 0
+
+
 def test_mmq_rejects(L):
     f = L.qk_mmq_q4k
-    w, c, s, y = P, P + 0x10000000, P + 0x20000000, P + 0x30000000
+    w, c, s, y, ws = P, P + 0x10000000, P + 0x20000000, P + 0x30000000, P + 0x40000000
+    need = qk.mmq_workspace_bytes(16, 64, 256)
     assert f(w, c, s, 0, 64, 256, None, y, None, 0, 0, None) == 0   # M = 0: nothing to do
-    assert f(w, c, s, 16, 64, 320, None, y, None, 0, 0, None) == E_SHAPE
-    assert f(None, c, s, 16, 64, 256, None, y, None, 0, 0, None) == E_NULL
-    assert f(w, c + 1, s, 16, 64, 256, None, y, None, 0, 0, None) == E_ALIGN
-    assert f(w, c, s, 16, 64, 256, None, c, None, 0, 0, None) == E_ALIAS
+    assert f(w, c, s, 16, 64, 320, None, y, ws, need, 0, None) == E_SHAPE
+    assert f(None, c, s, 16, 64, 256, None, y, ws, need, 0, None) == E_NULL
+    assert f(w, c, s, 16, 64, 256, None, y, None, need, 0, None) == E_NULL        # no workspace
+    assert f(w, c + 1, s, 16, 64, 256, None, y, ws, need, 0, None) == E_ALIGN
+    assert f(w, c, s, 16, 64, 256, None, y, ws + 16, need, 0, None) == E_ALIGN    # workspace not 256-aligned
+    assert f(w, c, s, 16, 64, 256, None, y, ws, need - 16, 0, None) == -6         # QK_E_WORKSPACE
+    assert f(w, c, s, 16, 64, 256, None, c, ws, need, 0, None) == E_ALIAS
+    assert f(w, c, s, 16, 64, 256, None, y, y, need, 0, None) == E_ALIAS           # workspace over y
 
 
 def test_binding_refuses_cpu_tensors():
