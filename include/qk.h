@@ -230,6 +230,29 @@ int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales,
                void *workspace, size_t workspace_bytes,
                unsigned flags, void *stream);
 
+/* ================================================ MMQ without a workspace
+ * The pages have no counterpart of this entry point: it is a convenience of
+ * this library for callers that cannot supply a device workspace (a host
+ * without its own device allocator, or a steady-state loop that must not
+ * call cudaMalloc).  Same arguments and results as qk_mmq_q4k, but the
+ * workspace is a statically allocated device array of
+ * QK_MMQ_STATIC_WS_BYTES bytes inside the library; the call allocates and
+ * frees nothing.
+ *  - Problems with qk_mmq_workspace_bytes(M, N, K) > QK_MMQ_STATIC_WS_BYTES
+ *    return QK_E_WORKSPACE (nothing launched).  Example: M = 2048, K = 3584
+ *    needs 31,195,136 bytes and fits; K = 18944 does not.
+ *  - The array needs no initialisation (each call writes what it reads).
+ *  - All calls on a device share the array: calls that may run concurrently
+ *    (other streams, unordered host threads) race on it.
+ *  - The first call on each device looks the array's address up with
+ *    cudaGetSymbolAddress; make that first call outside stream capture.
+ */
+#define QK_MMQ_STATIC_WS_BYTES (32u << 20)
+int qk_mmq_q4k_noalloc(const void *w, const int8_t *codes, const void *scales,
+                       int64_t M, int64_t N, int64_t K,
+                       const float *residual, float *y,
+                       unsigned flags, void *stream);
+
 /* ========================================================== error flags
  * Kernels that hand work between warps with mbarriers (qk_mmq_q4k) bound
  * every wait.  A wait that gives up -- which only happens if the hardware or

@@ -34,7 +34,7 @@ STATUS = {0: "QK_OK", -1: "QK_E_NULL", -2: "QK_E_SHAPE", -3: "QK_E_ALIGN", -4: "
 # every symbol include/qk.h declares
 EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1", "qk_repacked_bytes",
            "qk_repack", "qk_gemv_q4k", "qk_gemv_q6k", "qk_gemv_q4k_f32", "qk_gemv_q6k_f32",
-           "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_error_flags"]
+           "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_mmq_q4k_noalloc", "qk_error_flags"]
 
 _lib = None
 _lock = threading.Lock()
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             L.qk_gemv_q6k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
             L.qk_mmq_workspace_bytes.argtypes = [i64, i64, i64, szp]
             L.qk_mmq_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
+            L.qk_mmq_q4k_noalloc.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
             L.qk_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
             for name in EXPORTS:
                 getattr(L, name).restype = ctypes.c_int if name != "qk_status_string" else ctypes.c_char_p
@@ -245,4 +246,20 @@ def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=F
     st = lib().qk_mmq_q4k(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
                           _p(workspace), wsb, LAUNCH_PDL if pdl else 0, _stream(stream))
     _check(st, "qk_mmq_q4k")
+    return y
+
+
+STATIC_WS_BYTES = 32 << 20          # QK_MMQ_STATIC_WS_BYTES
+
+
+def mmq_q4k_noalloc(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
+    """qk_mmq_q4k with the library's static workspace (no workspace argument; see qk.h)."""
+    M = codes.shape[0]
+    for t, n in ((w, "w"), (codes, "codes"), (scales, "scales")):
+        _cuda(t, n)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=codes.device)
+    st = lib().qk_mmq_q4k_noalloc(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual),
+                                  y.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
+    _check(st, "qk_mmq_q4k_noalloc")
     return y

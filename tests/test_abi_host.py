@@ -144,3 +144,13 @@ def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
         qk.quantize_q8_1(torch.zeros(1, 256))
+
+
+def test_mmq_noalloc_rejects_oversize(L):
+    f = L.qk_mmq_q4k_noalloc
+    w, c, s, y = P, P + 0x10000000, P + 0x20000000, P + 0x30000000
+    assert f(w, c, s, 0, 64, 256, None, y, 0, None) == 0                 # M = 0: nothing to do
+    assert f(w, c, s, 16, 64, 320, None, y, 0, None) == E_SHAPE
+    assert qk.mmq_workspace_bytes(2048, 3584, 18944) > qk.STATIC_WS_BYTES
+    assert f(w, c, s, 2048, 3584, 18944, None, y, 0, None) == -6       # QK_E_WORKSPACE, before any CUDA call
+    assert qk.mmq_workspace_bytes(2048, 4608, 3584) <= qk.STATIC_WS_BYTES
