@@ -276,7 +276,6 @@ constexpr int Q4_CODES = 1024, Q4_META = 128;
 
 struct Q4Ops {
     static constexpr int R = Q4_R, SLOT = Q4_SLOT;
-    static constexpr int SIDE_PER_32 = 8;                 // one float2 per 32-value block
     struct LaneConst {
         uint32_t selA, selB;
         int aoff[4];
@@ -378,7 +377,6 @@ constexpr int Q6_QL = 1024, Q6_QH = 512, Q6_SC = 128;
 
 struct Q6Ops {
     static constexpr int R = Q6_R, SLOT = Q6_SLOT;
-    static constexpr int SIDE_PER_32 = 16;                // one float2 per 16-value chunk
     struct LaneConst {
         int qoff[4], coff[4];
     };
