@@ -201,25 +201,29 @@ int qk_gemv_q6k_f32(const void *w, const float *x, int64_t ldx,
                     int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
 
 /* ===================================================================== MMQ
- * Prefill contraction of many activation rows with a Q4_K weight: quantized
- * weight bytes go straight to tensor-core MMA with integer-exact operands,
- * and the float scales are folded outside the integer accumulation (minfer
- * "15 . The CUDA backend" sec. 2.3 and 3.2.6).
+ * Prefill contraction of many activation rows with a Q4_K weight: the
+ * quantized weight bytes are streamed to the SMs in their Q4_K form and
+ * expanded tile by tile right before the tensor-core MMAs (minfer "15 . The
+ * CUDA backend" sec. 2.3 and 3.2.6).  Both operands enter f16 MMAs as pairs:
+ * the activation d_a * q_a exactly (A_hi + A_lo), the weight
+ * d*sc*q - dmin*m to about 2^-22 relative (W_hi + W_lo); the binary32 result
+ * is within 1e-4 * sum_k |w * xhat| of the exact contraction (in practice
+ * ~1e-7).
  *
  * w, codes, scales, residual, y: as for qk_gemv_q4k.
  * Ranges: M >= 1, N >= 1, K % 256 == 0, K >= 256, ceil(M/128) <= 65535 and
- * ceil(N/128) <= 65535.  (M == 0 is a no-op.)
- * Activations must satisfy max |x| < 32000 per 32-value block (the exact
- * f16 operand split of d * q and of d * sum(q) / 16 must not overflow).
+ * ceil(N/256) <= 65535.  (M == 0 is a no-op.)
+ * Value limits: max |x| <= 65000 per 32-value block (the f16 operand
+ * d_a * q_a must not overflow) and |w| < 255 for every dequantized weight
+ * (the weight operand is scaled by 256); LLM layers are far inside both.
  * workspace: device scratch of at least qk_mmq_workspace_bytes(M, N, K)
  *   bytes, 256-byte aligned, not overlapping any other argument.  The call
  *   writes it (the q8_1 activation expanded once per 128-row tile into the
  *   tensor-core operand layout) before reading it; nothing needs to be
  *   initialised.  Its contents are consumed by kernels of this call that run
  *   after the call returns, so the workspace must not be reused by work that
- *   is not ordered after this call on `stream`.  Size:
- *   ceil(M/128) * (K * 512 + (K/256) * 8192) bytes
- *   (M = 2048, K = 18944: 164,888,576 bytes).
+ *   is not ordered after this call on `stream`.  Size: ceil(M/128) * K * 512
+ *   bytes (M = 2048, K = 18944: 155,189,248 bytes).
  * Returns QK_E_WORKSPACE if workspace_bytes is too small.
  */
 int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
@@ -240,7 +244,7 @@ int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales,
  * frees nothing.
  *  - Problems with qk_mmq_workspace_bytes(M, N, K) > QK_MMQ_STATIC_WS_BYTES
  *    return QK_E_WORKSPACE (nothing launched).  Example: M = 2048, K = 3584
- *    needs 31,195,136 bytes and fits; K = 18944 does not.
+ *    needs 29,360,128 bytes and fits; K = 18944 does not.
  *  - The array needs no initialisation (each call writes what it reads).
  *  - All calls on a device share the array: calls that may run concurrently
  *    (other streams, unordered host threads) race on it.

@@ -94,6 +94,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
                  : "memory");
 }
 
+// bulk prefetch of [src, src + bytes) into L2 (16-byte aligned start, size a multiple of 16)
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -180,7 +186,7 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // UMMA shared-memory matrix descriptor, K-major operand:
 //   bits  0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   bits 32-45 stride byte offset >> 4, 46-47 version (1), 61-63 layout.
-constexpr uint64_t kLayoutSw128 = 2, kLayoutSw32 = 6;
+constexpr uint64_t kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint64_t layout)
 {

@@ -118,10 +118,10 @@ def test_repack_rejects(L):
 
 
 def test_mmq_workspace_size():
-    # ceil(M/128) * (K*512 + (K/256)*8192)
-    assert qk.mmq_workspace_bytes(2048, 3584, 18944) == 16 * (18944 * 512 + 74 * 8192) == 164888576
-    assert qk.mmq_workspace_bytes(1, 64, 256) == 256 * 512 + 8192
-    assert qk.mmq_workspace_bytes(129, 64, 512) == 2 * (512 * 512 + 2 * 8192)
+    # ceil(M/128) * K * 512
+    assert qk.mmq_workspace_bytes(2048, 3584, 18944) == 16 * 18944 * 512 == 155189248
+    assert qk.mmq_workspace_bytes(1, 64, 256) == 256 * 512
+    assert qk.mmq_workspace_bytes(129, 64, 512) == 2 * 512 * 512
     assert qk.mmq_workspace_bytes(0, 64, 256) == 0
 
 
