@@ -22,21 +22,25 @@
 //     layout: per 32-value K stage a 16 KB block (A_hi and A_lo tiles, K-major
 //     SWIZZLE_64B).  Every N-tile then copies these blocks instead of
 //     converting the activation again.
-//  2. mmq_q4k_kernel, one CTA (20 warps) per 128 x 256 output tile and per SM
-//     (256 TMEM columns hold the accumulator):
+//  2. mmq_q4k_kernel: a persistent grid, one CTA (24 warps) per SM, each CTA
+//     taking 128 x 256 output tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
+//     (M-tile fastest).  512 TMEM columns hold two accumulators, so one tile
+//     accumulates while the previous one is written out:
 //       warp 0      TMEM allocation; lane 0 issues every MMA and commit
 //       warp 2      lane 0 streams the raw Q4_K bytes with 2D TMA tensor copies
 //                   into a ring, per superblock: the two 64-byte runs of code
 //                   bytes (256 x 64 B each: first and second 16-byte halves of
 //                   its four groups) and the metadata records (256 x 16 B)
-//       warps 4-19  converters: per K stage they copy the stage's A block from
+//       warps 4-7   the epilogue of the previous tile (TMEM lane quadrant =
+//                   warp % 4) while the next one accumulates
+//       warps 8-23  converters: per K stage they copy the stage's A block from
 //                   the workspace (cp.async, 32 bytes per thread) and, two
 //                   threads per weight row, expand the Q4_K codes, scales and
-//                   mins into (W_hi, W_lo) in the SWIZZLE_64B layout.  Warps
-//                   4-7 then run the epilogue (TMEM lane quadrant = warp % 4)
+//                   mins into (W_hi, W_lo) in the SWIZZLE_64B layout
 // Stages are handed over with mbarriers (full: converters -> MMA; empty: MMA
-// commit -> converters; raw: TMA bytes -> converters ->
-// producer; done: last MMA commit -> epilogue).  Every wait is bounded; a wait
+// commit -> converters; raw: TMA bytes -> converters -> producer; accumulator
+// full / empty: MMA commit -> epilogue -> MMA; done: last MMA commit ->
+// teardown).  Every wait is bounded; a wait
 // that gives up sets a device error flag (qk_error_flags), and once it is set
 // the other waits return after a few polls, so the kernel runs to its end.
 // Before the CTA releases its tensor memory and exits, the MMA thread waits
@@ -58,9 +62,6 @@
 #ifndef QK_MMQ_SBRAW
 #define QK_MMQ_SBRAW 2      // raw metadata superblocks in flight
 #endif
-#ifndef QK_MMQ_STCS
-#define QK_MMQ_STCS 0       // 1: outputs stored with the streaming (evict-first) cache operator
-#endif
 
 __device__ unsigned g_qk_errors;
 
@@ -70,8 +71,8 @@ using namespace qk::tc;
 
 constexpr int BM = 128, BN = 256, BK = 32;      // BK: one Q4_K sub-block
 constexpr int NST = QK_MMQ_NST, NRAW = QK_MMQ_RAW, NSB = QK_MMQ_SBRAW;
-constexpr int kThreads = 640;
-constexpr int kEpiWarp0 = 4, kConvWarp0 = 4;                 // warps 4-7 convert, then run the epilogue
+constexpr int kThreads = 768;
+constexpr int kEpiWarp0 = 4, kEpiWarps = 4, kConvWarp0 = 8;  // epilogue warps 4-7, converters 8-23
 constexpr int kConv = 512, kConvWarps = kConv / 32;   // two converter threads per weight row
 static_assert(kConv == 2 * BN && kConvWarp0 * 32 + kConv == kThreads, "two converter threads per weight row");
 constexpr float kWScale = 256.0f, kWUnscale = 1.0f / 256.0f;
@@ -85,7 +86,9 @@ constexpr int RAW_H0 = 0, RAW_H1 = BN * 64, RAW = 2 * BN * 64;
 constexpr int SBR = BN * 16;                    // raw metadata records of one superblock
 constexpr int OFF_RAW = NST * STAGE;
 constexpr int OFF_SBR = OFF_RAW + NRAW * RAW;
-constexpr int OFF_BAR = OFF_SBR + NSB * SBR;
+constexpr int EPI_LD = 17;                      // epilogue transpose buffer: 32 rows x 16 columns, padded
+constexpr int OFF_EPI = OFF_SBR + NSB * SBR;
+constexpr int OFF_BAR = OFF_EPI + kEpiWarps * 32 * EPI_LD * 4;
 enum {
     B_FULL = 0,
     B_EMPTY = B_FULL + NST,
@@ -93,7 +96,9 @@ enum {
     B_REMPTY = B_RFULL + NRAW,
     B_SFULL = B_REMPTY + NRAW,
     B_SEMPTY = B_SFULL + NSB,
-    B_DONE = B_SEMPTY + NSB,       // every MMA of the CTA has completed
+    B_ACCFULL = B_SEMPTY + NSB,    // accumulator buffer holds a finished tile
+    B_ACCEMPTY = B_ACCFULL + 2,    // the epilogue has read the accumulator buffer
+    B_DONE = B_ACCEMPTY + 2,       // every MMA of the CTA has completed
     NBAR = B_DONE + 1
 };
 constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
@@ -101,7 +106,7 @@ constexpr int SMEM = OFF_TMEM + 16 + 1024;      // + slack to align the base to 
 static_assert(SMEM <= 232448, "shared memory plan exceeds the per-block opt-in limit");
 static_assert(STAGE % 1024 == 0 && OFF_RAW % 1024 == 0 && RAW % 1024 == 0 && SBR % 1024 == 0,
               "copy destinations and swizzle atoms stay aligned");
-constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_COLS = 2 * BN;           // two accumulators: tile k+1 accumulates while tile k drains
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 
 // byte offset of 16-byte chunk c (< 4) of row r in a SWIZZLE_64B K-major tile (rows of 64 bytes)
@@ -117,6 +122,7 @@ struct MmqArgs {
     int64_t M, N, K;
     const float *residual;
     float *y;
+    int mtiles, ntiles;     // tile t covers M-tile t % mtiles, N-tile t / mtiles
 };
 
 struct MmqMaps {
@@ -224,19 +230,21 @@ struct ConvState {
 // one converter thread's share of K stage `it` (operand stage st = it % NST): the 16 weights of
 // half h of sub-block j = it % 8 of row `row` as (W_hi, W_lo) chunks 2h and 2h+1, then the
 // stage is signalled full
+// it: K stage within the tile; gs / gsb: the stage and superblock counted over all tiles of
+// this CTA (ring slots and barrier phases)
 __device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, ConvState &cs, const uint8_t *srcA,
-                                              int it, int row, int h, int st)
+                                              int it, int gs, int gsb, int row, int h, int st)
 {
-    const int j = it & 7, sb = it >> 3, g = j >> 1, nib = j & 1;
-    const int rs = sb % NRAW, ss = sb % NSB;
+    const int j = it & 7, g = j >> 1, nib = j & 1;
+    const int rs = gsb % NRAW, ss = gsb % NSB;
     if (j == 0) {
-        wait_bar(&bar[B_SFULL + ss], (sb / NSB) & 1);
+        wait_bar(&bar[B_SFULL + ss], (gsb / NSB) & 1);
         cs.mt = *reinterpret_cast<const uint4 *>(smem + OFF_SBR + ss * SBR + row * 16);
-        wait_bar(&bar[B_RFULL + rs], (sb / NRAW) & 1);
+        wait_bar(&bar[B_RFULL + rs], (gsb / NRAW) & 1);
     }
     if (nib == 0)
         cs.c = *reinterpret_cast<const uint4 *>(smem + OFF_RAW + rs * RAW + (h ? RAW_H1 : RAW_H0) + row * 64 + 16 * g);
-    if (it >= NST) wait_bar(&bar[B_EMPTY + st], ((it / NST) + 1) & 1);
+    if (gs >= NST) wait_bar(&bar[B_EMPTY + st], ((gs / NST) + 1) & 1);
     uint8_t *s0 = smem + st * STAGE;
     // the stage's activation block (A_hi | A_lo, 16 KB): 32 bytes per converter thread, in flight
     // while the weights are converted
@@ -290,15 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mtile = blockIdx.x;
-    const int m0 = mtile * BM, n0 = blockIdx.y * BN;
     const int B = (int)(a.K >> 8), nit = 8 * B;
+    const int ntiles = a.mtiles * a.ntiles;
+    // this CTA's tiles: blockIdx.x, blockIdx.x + gridDim.x, ... (M-tile fastest, so the CTAs running
+    // at the same time share their activation and weight tiles in L2)
 
     qk::pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; i++) mbar_init(&bar[B_FULL + i], kConvWarps), mbar_init(&bar[B_EMPTY + i], 1);
         for (int i = 0; i < NRAW; i++) mbar_init(&bar[B_RFULL + i], 1), mbar_init(&bar[B_REMPTY + i], kConvWarps);
         for (int i = 0; i < NSB; i++) mbar_init(&bar[B_SFULL + i], 1), mbar_init(&bar[B_SEMPTY + i], kConvWarps);
+        for (int i = 0; i < 2; i++) mbar_init(&bar[B_ACCFULL + i], 1), mbar_init(&bar[B_ACCEMPTY + i], kEpiWarps);
         mbar_init(&bar[B_DONE], 1);
         mbar_init_fence();
     }
@@ -316,24 +326,32 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t sbase = smem_u32(smem);
-            for (int it = 0; it < nit; it++) {
-                const int st = it % NST;
-                wait_bar(&bar[B_FULL + st], (it / NST) & 1);
+            int kt = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
+                const int acc = kt & 1;
+                if (kt >= 2) wait_bar(&bar[B_ACCEMPTY + acc], ((kt >> 1) + 1) & 1);
                 fence_after_sync();
-                const uint32_t s0 = sbase + st * STAGE;
+                const uint32_t dacc = tmem + acc * BN;
+                for (int it = 0; it < nit; it++) {
+                    const int gs = kt * nit + it, st = gs % NST;
+                    wait_bar(&bar[B_FULL + st], (gs / NST) & 1);
+                    fence_after_sync();
+                    const uint32_t s0 = sbase + st * STAGE;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; kk++) {
-                    const uint64_t ahi = smem_desc(s0 + 32 * kk, 16, 512, kLayoutSw64);
-                    const uint64_t alo = smem_desc(s0 + ATILE + 32 * kk, 16, 512, kLayoutSw64);
-                    const uint64_t whi = smem_desc(s0 + 2 * ATILE + 32 * kk, 16, 512, kLayoutSw64);
-                    const uint64_t wlo = smem_desc(s0 + 2 * ATILE + WTILE + 32 * kk, 16, 512, kLayoutSw64);
-                    mma_f16(tmem, ahi, whi, IDESC, (it | kk) != 0);
-                    mma_f16(tmem, ahi, wlo, IDESC, 1);
-                    mma_f16(tmem, alo, whi, IDESC, 1);
+                    for (int kk = 0; kk < BK / 16; kk++) {
+                        const uint64_t ahi = smem_desc(s0 + 32 * kk, 16, 512, kLayoutSw64);
+                        const uint64_t alo = smem_desc(s0 + ATILE + 32 * kk, 16, 512, kLayoutSw64);
+                        const uint64_t whi = smem_desc(s0 + 2 * ATILE + 32 * kk, 16, 512, kLayoutSw64);
+                        const uint64_t wlo = smem_desc(s0 + 2 * ATILE + WTILE + 32 * kk, 16, 512, kLayoutSw64);
+                        mma_f16(dacc, ahi, whi, IDESC, (it | kk) != 0);
+                        mma_f16(dacc, ahi, wlo, IDESC, 1);
+                        mma_f16(dacc, alo, whi, IDESC, 1);
+                    }
+                    mma_commit(&bar[B_EMPTY + st]);
                 }
-                mma_commit(&bar[B_EMPTY + st]);
+                mma_commit(&bar[B_ACCFULL + acc]);
             }
-            // the epilogue starts once every MMA has completed; the CTA's TMEM is released after it
+            // teardown: no MMA may still be running when the TMEM is released
             mma_commit(&bar[B_DONE]);
             wait_bar(&bar[B_DONE], 0);
         }
@@ -343,73 +361,98 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
         if (lane == 0) {
             prefetch_tmap(&maps.wcodes);
             prefetch_tmap(&maps.meta);
-            for (int sb = 0; sb < B; sb++) {
-                const int ss = sb % NSB;
-                if (sb >= NSB) wait_bar(&bar[B_SEMPTY + ss], ((sb / NSB) + 1) & 1);
-                mbar_arrive_expect_tx(&bar[B_SFULL + ss], SBR);
-                tma_load_2d(smem + OFF_SBR + ss * SBR, &maps.meta, 16 * sb, n0, &bar[B_SFULL + ss]);
-                const int rs = sb % NRAW;
-                if (sb >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((sb / NRAW) + 1) & 1);
-                uint8_t *d = smem + OFF_RAW + rs * RAW;
-                // the superblock's 4 groups: first halves at 16u (u = 4 (sb - 8 s) .. +3), second at 16 G + 16u
-                const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s);
-                mbar_arrive_expect_tx(&bar[B_RFULL + rs], RAW);
-                tma_load_2d(d + RAW_H0, &maps.wcodes, 1024 * s + 16 * u, n0, &bar[B_RFULL + rs]);
-                tma_load_2d(d + RAW_H1, &maps.wcodes, 1024 * s + 16 * G + 16 * u, n0, &bar[B_RFULL + rs]);
+            int gsb = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                const int n0 = (t / a.mtiles) * BN;
+                for (int sb = 0; sb < B; sb++, gsb++) {
+                    const int ss = gsb % NSB;
+                    if (gsb >= NSB) wait_bar(&bar[B_SEMPTY + ss], ((gsb / NSB) + 1) & 1);
+                    mbar_arrive_expect_tx(&bar[B_SFULL + ss], SBR);
+                    tma_load_2d(smem + OFF_SBR + ss * SBR, &maps.meta, 16 * sb, n0, &bar[B_SFULL + ss]);
+                    const int rs = gsb % NRAW;
+                    if (gsb >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((gsb / NRAW) + 1) & 1);
+                    uint8_t *d = smem + OFF_RAW + rs * RAW;
+                    // the superblock's 4 groups: first halves at 16u (u = 4 (sb - 8 s) .. +3), second at 16 G + 16u
+                    const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s);
+                    mbar_arrive_expect_tx(&bar[B_RFULL + rs], RAW);
+                    tma_load_2d(d + RAW_H0, &maps.wcodes, 1024 * s + 16 * u, n0, &bar[B_RFULL + rs]);
+                    tma_load_2d(d + RAW_H1, &maps.wcodes, 1024 * s + 16 * G + 16 * u, n0, &bar[B_RFULL + rs]);
+                }
             }
             // teardown: every copy this thread issued has landed (normally long since consumed)
-            for (int sb = B - NRAW < 0 ? 0 : B - NRAW; sb < B; sb++) wait_bar(&bar[B_RFULL + sb % NRAW], (sb / NRAW) & 1);
-            for (int sb = B - NSB < 0 ? 0 : B - NSB; sb < B; sb++) wait_bar(&bar[B_SFULL + sb % NSB], (sb / NSB) & 1);
+            for (int g = gsb - NRAW < 0 ? 0 : gsb - NRAW; g < gsb; g++) wait_bar(&bar[B_RFULL + g % NRAW], (g / NRAW) & 1);
+            for (int g = gsb - NSB < 0 ? 0 : gsb - NSB; g < gsb; g++) wait_bar(&bar[B_SFULL + g % NSB], (g / NSB) & 1);
         }
         __syncwarp();
-    } else if (warp >= kConvWarp0) {
-        // --------------------------------------------------------- converters
-        // Lanes 0-15 of a warp take 16 consecutive rows of half 0, lanes 16-31 the same rows of
-        // half 1; a quarter warp stores 8 consecutive rows, which the 64-byte swizzle spreads over
-        // all 32 banks.  Unrolled by the stage count, so the operand stage index is static.
-        const int cwarp = warp - kConvWarp0;                      // 0..15
-        const int row = 16 * cwarp + (lane & 15), h = lane >> 4;
-        const uint8_t *srcA = a.wsA + (size_t)mtile * nit * ABLOCK;
-        ConvState cs;
-        cs.c = cs.mt = make_uint4(0, 0, 0, 0);
-        for (int it = 0; it < nit; it += NST) {
-#pragma unroll
-            for (int k = 0; k < NST; k++)
-                if (it + k < nit) convert_stage(smem, bar, cs, srcA, it + k, row, h, k);
-        }
-        if (warp < kEpiWarp0 + 4) {
-            // ---------------------------------------------------------- epilogue
-            // y = Y / 256 (+ R), one 32 x 32 block per pass: a thread holds row (32q + lane) of the
-            // block; the block is transposed through shared memory (operand stage 0, idle once
-            // every MMA has completed) so that each store writes 32 consecutive columns of one row
-            wait_bar(&bar[B_DONE], 0);
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+        // -------------------------------------------------------------- epilogue
+        // y = Y / 256 (+ R) per finished tile, 16 columns per pass: a thread holds row (32q + lane)
+        // of the block; the block is transposed through shared memory so that each store covers 16
+        // consecutive columns of two rows
+        const uint32_t lq = (uint32_t)((warp & 3) * 32) << 16;   // TMEM lane quadrant of this warp
+        float *tb_s = reinterpret_cast<float *>(smem + OFF_EPI) + (warp - kEpiWarp0) * (32 * EPI_LD);
+        const int q0 = (warp & 3) * 32;
+        int kt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
+            const int acc = kt & 1;
+            const int64_t m0 = (int64_t)(t % a.mtiles) * BM, n0 = (int64_t)(t / a.mtiles) * BN;
+            wait_bar(&bar[B_ACCFULL + acc], (kt >> 1) & 1);
             fence_after_sync();
-            const uint32_t lq = (uint32_t)((warp & 3) * 32) << 16;   // TMEM lane quadrant of this warp
-            float *tb_s = reinterpret_cast<float *>(smem) + (warp - kEpiWarp0) * (32 * 33);
-            const int q0 = (warp & 3) * 32;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; c++) {
-                float v[32];
-                tmem_ld32(tmem + lq + 32 * c, v);
+            for (int c = 0; c < BN / 16; c++) {
+                float v[16];
+                tmem_ld16(tmem + lq + acc * BN + 16 * c, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 32; jj++) tb_s[lane * 33 + jj] = v[jj] * kWUnscale;
+                for (int jj = 0; jj < 16; jj++) tb_s[lane * EPI_LD + jj] = v[jj] * kWUnscale;
                 __syncwarp();
-                const int64_t n = n0 + 32 * c + lane;
+                const int64_t n = n0 + 16 * c + (lane & 15);
                 if (n < a.N) {
 #pragma unroll 4
-                    for (int r = 0; r < 32; r++) {
+                    for (int rr = 0; rr < 16; rr++) {
+                        const int r = 2 * rr + (lane >> 4);
                         const int64_t m = m0 + q0 + r;
                         if (m < a.M) {
-                            const float val = tb_s[r * 33 + lane];
+                            const float val = tb_s[r * EPI_LD + (lane & 15)];
                             const size_t o = (size_t)m * a.N + n;
-                            const float out = a.residual ? __fadd_rn(val, a.residual[o]) : val;
-                            if (QK_MMQ_STCS) __stcs(a.y + o, out);
-                            else a.y[o] = out;
+                            a.y[o] = a.residual ? __fadd_rn(val, a.residual[o]) : val;
                         }
                     }
                 }
                 __syncwarp();
+            }
+            // the accumulator buffer may be overwritten once every lane's loads have completed
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[B_ACCEMPTY + acc]);
+        }
+    } else if (warp >= kConvWarp0) {
+        // --------------------------------------------------------- converters
+        // Lanes 0-15 of a warp take 16 consecutive rows of half 0, lanes 16-31 the same rows of
+        // half 1; a quarter warp stores 8 consecutive rows, which the 64-byte swizzle spreads over
+        // all 32 banks.
+        const int cwarp = warp - kConvWarp0;                      // 0..15
+        const int row = 16 * cwarp + (lane & 15), h = lane >> 4;
+        ConvState cs;
+        cs.c = cs.mt = make_uint4(0, 0, 0, 0);
+        int kt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
+            const uint8_t *srcA = a.wsA + (size_t)(t % a.mtiles) * nit * ABLOCK;
+            const int gs0 = kt * nit;
+            // the stage slot of K stage it is (gs0 + it) % NST: unroll so that it is static
+            static_assert(NST == 3, "the slot prologue below handles three stages");
+            int it = 0;
+            while (it < nit && (gs0 + it) % NST != 0) {
+                const int gs = gs0 + it;
+                if (gs % NST == 1) convert_stage(smem, bar, cs, srcA, it, gs, kt * B + (it >> 3), row, h, 1);
+                else convert_stage(smem, bar, cs, srcA, it, gs, kt * B + (it >> 3), row, h, 2);
+                it++;
+            }
+            for (; it < nit; it += NST) {
+#pragma unroll
+                for (int k = 0; k < NST; k++)
+                    if (it + k < nit)
+                        convert_stage(smem, bar, cs, srcA, it + k, gs0 + it + k, kt * B + ((it + k) >> 3), row, h, k);
             }
         }
     }
@@ -508,7 +551,7 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
         (residual && qk::overlaps(workspace, need, residual, ybytes)))
         return QK_E_ALIAS;
     const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
-    if (gx > 65535 || gy > 65535) return QK_E_SHAPE;
+    if (gx > 65535 || gy > 65535 || gx * gy > 0x7fffffffLL) return QK_E_SHAPE;
     if ((size_t)SMEM > qk::max_smem_optin()) return QK_E_CUDA;
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return QK_E_CUDA;
@@ -529,7 +572,8 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
     int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, (cudaStream_t)stream,
                         (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA);
     if (st != QK_OK) return st;
-    MmqArgs args{wsA, M, N, K, residual, y};
-    return qk::launch(mmq_q4k_kernel, dim3((unsigned)gx, (unsigned)gy), dim3(kThreads), SMEM, (cudaStream_t)stream,
-                      true, args, maps);
+    MmqArgs args{wsA, M, N, K, residual, y, (int)gx, (int)gy};
+    const int64_t tiles = gx * gy, grid = tiles < qk::sm_count() ? tiles : qk::sm_count();
+    return qk::launch(mmq_q4k_kernel, dim3((unsigned)grid), dim3(kThreads), SMEM, (cudaStream_t)stream, true, args,
+                      maps);
 }
