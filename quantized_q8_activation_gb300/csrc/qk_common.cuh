@@ -125,6 +125,33 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // binary32 -> binary16, round to nearest even, saturating at +-65504
 __device__ __forceinline__ __half f16_sat(float v) { return __float2half_rn(fminf(fmaxf(v, -65504.0f), 65504.0f)); }
 
+// request the 128-byte line holding p into L2 (no L1 allocation, no register result)
+__device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+// RN(a / 127) for every binary32 a >= 0 (zero, subnormal and normal): the
+// quotient q0 = RN(a * y) with y = RN(1/127) is corrected once with the exact
+// remainder r = a - 127 q0 (one fma), q = RN(q0 + r y) -- division by a
+// divisor known in advance (Markstein; Brisebarre, Muller and Raina,
+// "Accelerating correctly rounded floating-point division when the divisor
+// is known in advance", IEEE TC 2004).  For this divisor the sequence was
+// checked against IEEE division on all 2^31 non-negative finite inputs.
+__device__ __forceinline__ float div127_rn(float a)
+{
+    const float y = 0x1.020408p-7f;                         // RN(1/127)
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(-q0, 127.0f, a);
+    return __fmaf_rn(r, y, q0);
+}
+
+// approximate reciprocal (PTX rcp.approx.f32: at most 1 ulp of error over the
+// whole range, subnormal inputs included)
+__device__ __forceinline__ float rcp_approx(float v)
+{
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // q8_1 quantization of one 32-value block held by 8 consecutive lanes (lane
 // group 8j..8j+7 of the warp, 4 values each, all 32 lanes participating):
 // d = amax/127 (binary32 division), q = roundf(x/d) (0 when d == 0).  Returns
@@ -133,31 +160,32 @@ __device__ __forceinline__ __half f16_sat(float v) { return __float2half_rn(fmin
 // the GEMV kernels that quantize their activation themselves, so both produce
 // the same codes bit for bit.
 //
-// roundf(x/d) is taken from t = x * r with r = RN(1/d): t differs from x/d by
-// at most 2^-23 |x/d| <= 1.6e-5 and RN(x/d) from x/d by at most 7.7e-6
-// (|x/d| <= 127.5), so unless t lies within 2^-15 of a half-integer both round
-// to the same integer.  Near a tie (or if 1/d overflowed) the code is taken
-// from the IEEE quotient instead; that path is entered warp-uniformly and only
-// when some lane needs it, so the common case has no branches.
+// roundf(x/d) is taken from t = x * r with r = 1/d to within 1 ulp: |x/d| is at
+// most 127 (1 + 2^-24), so t differs from x/d by at most 1.5 * 2^-23 * 127.01
+// < 2.28e-5, and RN(x/d) from x/d by at most 7.6e-6.  Unless t lies within
+// 2^-15 = 3.05e-5 of a half-integer, x/d and RN(x/d) are on t's side of it, and
+// round-to-nearest-even of t (no tie there) equals roundf(RN(x/d)).  Near a
+// half-integer, or when 1/d is not finite, the code is taken from the IEEE
+// quotient instead; that path is entered warp-uniformly and only when some
+// lane needs it, so the common case has no branches.
 __device__ __forceinline__ uint32_t q81_quant8(float4 v, float &d, int &s4)
 {
     float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    d = __fdiv_rn(amax, 127.0f);
+    d = div127_rn(amax);
     const bool live = d > 0.0f;
-    const float r = live ? __frcp_rn(d) : 0.0f;
+    const float r = rcp_approx(d);
     const float x[4] = {v.x, v.y, v.z, v.w};
     int q[4];
     bool near = false;
 #pragma unroll
     for (int j = 0; j < 4; j++) {
-        const float t = x[j] * r;
-        const float a = fabsf(t);
-        const float fr = a - truncf(a);
-        near |= !(fabsf(fr - 0.5f) > 3.0517578125e-05f && a < 128.0f);
-        q[j] = (int)roundf(t);
+        const float t = __fmul_rn(x[j], r);
+        const float tr = rintf(t);
+        near |= !(fabsf(t - tr) < 0.5f - 3.0517578125e-05f);     // also true for a non-finite t
+        q[j] = __float2int_rz(tr);                                 // tr is an integer (or not finite)
     }
     near = near && live;
     if (__any_sync(0xffffffffu, near)) {

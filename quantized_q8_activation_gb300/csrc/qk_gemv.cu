@@ -125,15 +125,16 @@ __device__ void stage_act_q4k(const int8_t *__restrict__ codes, const __half2 *_
         const bool ok = i < total;
         const int m = ok ? i / nchunk : 0, c = ok ? i - m * nchunk : 0;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (ok) {
+        float d = 0.0f;
+        if (ok) {                                          // both loads in flight together
             v = *reinterpret_cast<const uint4 *>(codes + (size_t)m * K + 16 * c);
+            d = __low2float(scales[(size_t)m * (K >> 5) + (c >> 1)]);
             *reinterpret_cast<uint4 *>(s_codes + (size_t)m * K + 16 * swz(c)) = v;
         }
         int s = sum16(v);
         s += __shfl_xor_sync(0xffffffffu, s, 1);           // the other half of the 32-value block
         if (ok && (c & 1) == 0) {
             const int b = c >> 1;
-            const float d = __low2float(scales[(size_t)m * (K >> 5) + b]);
             s_sc[m * (K >> 5) + b] = make_float2((b & 1) ? d * 0.0625f : d, d * (float)s);
         }
     }
@@ -536,6 +537,27 @@ struct Q6Ops {
 
 // ---------------------------------------------------------------- driver
 
+// L2 prefetch of the rows this CTA is about to stage: the f32 activation, or the
+// q8_1 codes and scales (one prefetch per 128-byte line)
+template <int M, int NT, bool FUSED>
+__device__ __forceinline__ void prefetch_activation(const GemvArgs &a)
+{
+    const int K = a.K;
+    if (FUSED) {
+        const int per_row = K >> 5;                        // 128-byte lines of K floats
+        for (int i = threadIdx.x; i < M * per_row; i += NT) {
+            const int m = i / per_row, j = i - m * per_row;
+            qk::prefetch_l2(a.x + m * a.ldx + 32 * j);
+        }
+    } else {
+        const int code_lines = (M * K) >> 7, scale_lines = (M * K) >> 10;   // K is a multiple of 256
+        for (int i = threadIdx.x; i < code_lines + scale_lines; i += NT) {
+            if (i < code_lines) qk::prefetch_l2(a.codes + 128 * i);
+            else qk::prefetch_l2(reinterpret_cast<const uint8_t *>(a.scales) + 128 * (i - code_lines));
+        }
+    }
+}
+
 template <class Ops, int M, bool FUSED>
 __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
 {
@@ -574,6 +596,12 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
         wr.next(nsteps);
         ++wi;
     }
+    // The activation may be written by the previous kernel, so it is read only after the
+    // wait; its lines are requested into L2 now.  L2 is where the producer's stores land,
+    // so a line fetched early is updated in place and the reads after the wait see the
+    // producer's values; the prefetch only saves the DRAM latency when the activation is
+    // not in L2 already.
+    prefetch_activation<M, Cfg<M, FUSED>::threads, FUSED>(a);
     qk::pdl_wait();
     Ops::template stage<M, Cfg<M, FUSED>::threads, FUSED>(a, s_codes, s_side);
     __syncthreads();

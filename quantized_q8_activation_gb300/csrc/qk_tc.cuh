@@ -94,12 +94,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
                  : "memory");
 }
 
-// bulk prefetch of [src, src + bytes) into L2 (16-byte aligned start, size a multiple of 16)
-__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
