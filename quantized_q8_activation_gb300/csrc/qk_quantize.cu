@@ -20,15 +20,20 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_1_kernel(const float *__
                                                                  __half2 *__restrict__ scales, int64_t K)
 {
     qk::pdl_launch_dependents();            // let the consumer start its weight prefetch
-    qk::pdl_wait();                         // x may come from the previous kernel
     const int lane = threadIdx.x & 31;
     const int64_t blk = (int64_t)blockIdx.x * (kThreads / 8) + (threadIdx.x >> 3);   // q8_1 block id
     const bool live = blk < nblocks;
     const int64_t m = live ? blk / nb_row : 0;
     const int b = live ? (int)(blk - m * nb_row) : 0;
     const int sub = lane & 7;               // lane within the block's 8-lane group
+    const float *src = x + m * ldx + 32 * b + 4 * sub;
+    // x may come from the previous kernel: read it only after the wait, but request its
+    // lines into L2 now (the first and last lane of a block cover the block's 128 bytes);
+    // L2 is where the producer's stores land, so the reads after the wait are current
+    if (live && (sub == 0 || sub == 7)) qk::prefetch_l2(src);
+    qk::pdl_wait();
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live) v = *reinterpret_cast<const float4 *>(x + m * ldx + 32 * b + 4 * sub);
+    if (live) v = *reinterpret_cast<const float4 *>(src);
     float d;
     int sum;
     const uint32_t packed = qk::q81_quant8(v, d, sum);
