@@ -27,22 +27,25 @@
 //     (M-tile fastest).  512 TMEM columns hold two accumulators, so one tile
 //     accumulates while the previous one is written out:
 //       warp 0      TMEM allocation; lane 0 issues every MMA and commit
+//       warp 1      lane 0 copies each K stage's 16 KB activation block from the
+//                   workspace into the stage slot with one bulk copy, as soon as
+//                   the MMAs have released the slot
 //       warp 2      lane 0 streams the raw Q4_K bytes with 2D TMA tensor copies
 //                   into a ring, per superblock: the two 64-byte runs of code
 //                   bytes (256 x 64 B each: first and second 16-byte halves of
 //                   its four groups) and the metadata records (256 x 16 B)
 //       warps 4-7   the epilogue of the previous tile (TMEM lane quadrant =
 //                   warp % 4) while the next one accumulates
-//       warps 8-23  converters: per K stage they copy the stage's A block from
-//                   the workspace (cp.async, 32 bytes per thread) and, two
-//                   threads per weight row, expand the Q4_K codes, scales and
-//                   mins into (W_hi, W_lo) in the SWIZZLE_64B layout
-// Stages are handed over with mbarriers (full: converters -> MMA; empty: MMA
-// commit -> converters; raw: TMA bytes -> converters -> producer; accumulator
-// full / empty: MMA commit -> epilogue -> MMA; done: last MMA commit ->
-// teardown).  Every wait is bounded; a wait
-// that gives up sets a device error flag (qk_error_flags), and once it is set
-// the other waits return after a few polls, so the kernel runs to its end.
+//       warps 8-23  converters: two threads per weight row expand the Q4_K
+//                   codes, scales and mins of each K stage into (W_hi, W_lo) in
+//                   the SWIZZLE_64B layout
+// Stages are handed over with mbarriers (full: converters and the activation
+// copy's bytes -> MMA; empty: MMA commit -> converters and activation copier;
+// raw: TMA bytes -> converters -> producer; accumulator full / empty: MMA
+// commit -> epilogue -> MMA; done: last MMA commit -> teardown).  Every wait is
+// bounded; a wait that gives up sets a device error flag (qk_error_flags), and
+// once it is set the other waits return after a few polls, so the kernel runs
+// to its end.
 // Before the CTA releases its tensor memory and exits, the MMA thread waits
 // for its last MMAs and the producers for their last copies (bounded too), so
 // nothing is left in flight.
@@ -62,6 +65,7 @@
 #ifndef QK_MMQ_SBRAW
 #define QK_MMQ_SBRAW 2      // raw metadata superblocks in flight
 #endif
+
 
 __device__ unsigned g_qk_errors;
 
@@ -232,7 +236,7 @@ struct ConvState {
 // stage is signalled full
 // it: K stage within the tile; gs / gsb: the stage and superblock counted over all tiles of
 // this CTA (ring slots and barrier phases)
-__device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, ConvState &cs, const uint8_t *srcA,
+__device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, ConvState &cs,
                                               int it, int gs, int gsb, int row, int h, int st)
 {
     const int j = it & 7, g = j >> 1, nib = j & 1;
@@ -246,15 +250,6 @@ __device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, Conv
         cs.c = *reinterpret_cast<const uint4 *>(smem + OFF_RAW + rs * RAW + (h ? RAW_H1 : RAW_H0) + row * 64 + 16 * g);
     if (gs >= NST) wait_bar(&bar[B_EMPTY + st], ((gs / NST) + 1) & 1);
     uint8_t *s0 = smem + st * STAGE;
-    // the stage's activation block (A_hi | A_lo, 16 KB): 32 bytes per converter thread, in flight
-    // while the weights are converted
-    {
-        const int ct = threadIdx.x - kConvWarp0 * 32;
-        const uint8_t *src = srcA + (size_t)it * ABLOCK + 32 * ct;
-        qk::cp_async16(s0 + 32 * ct, src);
-        qk::cp_async16(s0 + 32 * ct + 16, src + 16);
-        qk::cp_async_commit();
-    }
     // this group's record: sc0 | sc1<<6 | m0<<12 | m1<<18 (sub-blocks 2g and 2g+1)
     const uint4 mt = cs.mt;
     const uint32_t rec = __byte_perm(__byte_perm(mt.y, mt.z, g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u), mt.w,
@@ -276,12 +271,11 @@ __device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, Conv
         sts128(s0 + 2 * ATILE, sw64(row, 2 * h + cc), hi[0], hi[1], hi[2], hi[3]);
         sts128(s0 + 2 * ATILE + WTILE, sw64(row, 2 * h + cc), lo[0], lo[1], lo[2], lo[3]);
     }
-    // Each lane waits for its activation copy and makes its own stores visible to the tensor
-    // core (async proxy); after the warp has synchronised, one lane arrives for the whole warp.
+    // Each lane makes its own stores visible to the tensor core (async proxy); after the warp
+    // has synchronised, one lane arrives for the whole warp.
     // A raw slot is released only after the values read from it have been consumed by the
     // arithmetic above, so no shared load can still be pending when the producer lets the next
     // TMA copy overwrite it.
-    qk::cp_async_wait<0>();
     fence_proxy_async();
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
@@ -305,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
 
     qk::pdl_launch_dependents();
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; i++) mbar_init(&bar[B_FULL + i], kConvWarps), mbar_init(&bar[B_EMPTY + i], 1);
+        for (int i = 0; i < NST; i++)
+            mbar_init(&bar[B_FULL + i], kConvWarps + 1), mbar_init(&bar[B_EMPTY + i], 1);
         for (int i = 0; i < NRAW; i++) mbar_init(&bar[B_RFULL + i], 1), mbar_init(&bar[B_REMPTY + i], kConvWarps);
         for (int i = 0; i < NSB; i++) mbar_init(&bar[B_SFULL + i], 1), mbar_init(&bar[B_SEMPTY + i], kConvWarps);
         for (int i = 0; i < 2; i++) mbar_init(&bar[B_ACCFULL + i], 1), mbar_init(&bar[B_ACCEMPTY + i], kEpiWarps);
@@ -354,6 +349,23 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
             // teardown: no MMA may still be running when the TMEM is released
             mma_commit(&bar[B_DONE]);
             wait_bar(&bar[B_DONE], 0);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ activation block copier
+        // one bulk copy per K stage of the stage's 16 KB activation block, issued as soon as the
+        // MMAs have released the stage slot; it completes on the stage's full barrier
+        if (lane == 0) {
+            int kt = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
+                const uint8_t *srcA = a.wsA + (size_t)(t % a.mtiles) * nit * ABLOCK;
+                for (int it = 0; it < nit; it++) {
+                    const int gs = kt * nit + it, st = gs % NST;
+                    if (gs >= NST) wait_bar(&bar[B_EMPTY + st], ((gs / NST) + 1) & 1);
+                    mbar_arrive_expect_tx(&bar[B_FULL + st], ABLOCK);
+                    bulk_copy_g2s(smem + st * STAGE, srcA + (size_t)it * ABLOCK, ABLOCK, &bar[B_FULL + st]);
+                }
+            }
         }
         __syncwarp();
     } else if (warp == 2) {
@@ -437,22 +449,21 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
         cs.c = cs.mt = make_uint4(0, 0, 0, 0);
         int kt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
-            const uint8_t *srcA = a.wsA + (size_t)(t % a.mtiles) * nit * ABLOCK;
             const int gs0 = kt * nit;
             // the stage slot of K stage it is (gs0 + it) % NST: unroll so that it is static
             static_assert(NST == 3, "the slot prologue below handles three stages");
             int it = 0;
             while (it < nit && (gs0 + it) % NST != 0) {
                 const int gs = gs0 + it;
-                if (gs % NST == 1) convert_stage(smem, bar, cs, srcA, it, gs, kt * B + (it >> 3), row, h, 1);
-                else convert_stage(smem, bar, cs, srcA, it, gs, kt * B + (it >> 3), row, h, 2);
+                if (gs % NST == 1) convert_stage(smem, bar, cs, it, gs, kt * B + (it >> 3), row, h, 1);
+                else convert_stage(smem, bar, cs, it, gs, kt * B + (it >> 3), row, h, 2);
                 it++;
             }
             for (; it < nit; it += NST) {
 #pragma unroll
                 for (int k = 0; k < NST; k++)
                     if (it + k < nit)
-                        convert_stage(smem, bar, cs, srcA, it + k, gs0 + it + k, kt * B + ((it + k) >> 3), row, h, k);
+                        convert_stage(smem, bar, cs, it + k, gs0 + it + k, kt * B + ((it + k) >> 3), row, h, k);
             }
         }
     }

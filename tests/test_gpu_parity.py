@@ -134,6 +134,30 @@ def test_gemv_parity(qt, M, N, K):
     check(y, y_ref, ab, what=f"{qt} M={M} N={N} K={K}")
 
 
+# Row counts that leave a partial last round of row pairs on the persistent grid
+# (152 SMs x 16 warps: a pair per warp per round), with 2 to 16 superblock steps
+# per pair and a ragged last pair.  Every output row is checked.
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+@pytest.mark.parametrize("K,frac", [(4096, 8), (8192, 8), (32768, 10), (32768, 20)])
+@pytest.mark.parametrize("front", ["q8", "f32"])
+def test_gemv_partial_last_round(qt, K, frac, front):
+    W = torch.cuda.get_device_properties(0).multi_processor_count * 16
+    N = 2 * (W + W // frac) - 1
+    M = 1 if K > 8192 else 3
+    w, wr = weights(qt, N, K, seed=N + K)
+    x = synth.activations(M, K, seed=K + 7)
+    if front == "q8":
+        codes, scales = q8(x)
+        c, d = q8_host(codes, scales)
+        y = gemv(qt, wr, codes, scales, N, K).cpu().numpy()
+    else:
+        codes, scales = qk.empty_q8_1(M, K)
+        y = gemv_f32(qt, wr, dev(x), N, K, codes_out=codes, scales_out=scales).cpu().numpy()
+        c, d = q8_host(codes, scales)
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+    check(y, y_ref, ab, what=f"{qt} {front} M={M} N={N} K={K}")
+
+
 @pytest.mark.parametrize("qt", ["q4k", "q6k"])
 @pytest.mark.parametrize("mode", ["separate", "inplace", "pdl"])
 def test_gemv_residual(qt, mode):
