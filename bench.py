@@ -14,6 +14,8 @@ data of the stated distributions):
   3  config 1 + config 2 at M = 4
   4  Qwen2-7B prefill MMQ at M = 2048: QKV 4608x3584, attn-out 3584x3584 (+res),
      gate||up 37888x3584, down 3584x18944 (+res)
+  5  config 4 as a Q4_K_M layer that keeps its down projection in Q6_K (the
+     Q4_K_M recipe routes some down and value projections to Q6_K)
 
 Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
 graphs (programmatic dependent launch between the kernels), bracketed by a
@@ -55,6 +57,8 @@ CONFIGS = {
             + [("head", "q6k", 128256, 4096, False, "x_head")]),
     4: dict(name="Qwen2-7B prefill MMQ, 2048 tokens (Q4_K)", M=2048, kind="mmq",
             gemms=[(n, "q4k", N, K, r, s) for (n, N, K, r, s) in synth.QWEN2_7B_PREFILL]),
+    5: dict(name="Qwen2-7B prefill MMQ, 2048 tokens (Q4_K, down projection in Q6_K)", M=2048, kind="mmq",
+            gemms=[(n, "q6k" if n == "down" else "q4k", N, K, r, s) for (n, N, K, r, s) in synth.QWEN2_7B_PREFILL]),
 }
 
 
@@ -184,7 +188,8 @@ class Workload:
             codes, scales = self.q8[s]
             kw = dict(residual=self.r.get(name), y=self.y[name], pdl=pdl, stream=stream)
             if cfg["kind"] == "mmq":
-                qk.mmq_q4k(self.w[copy][name], codes, scales, N, K, workspace=self.ws, **kw)
+                fn = qk.mmq_q4k if q == "q4k" else qk.mmq_q6k
+                fn(self.w[copy][name], codes, scales, N, K, workspace=self.ws, **kw)
             else:
                 fn = qk.gemv_q4k if q == "q4k" else qk.gemv_q6k
                 fn(self.w[copy][name], codes, scales, N, K, **kw)
@@ -207,7 +212,7 @@ class Workload:
     def kernel_key(self, gemm, fused: bool) -> str:
         q = gemm[1]
         if self.cfg["kind"] == "mmq":
-            return "mmq_q4k"
+            return "mmq_q4k" if q == "q4k" else "mmq_q6k"
         return ("gemv_q4k" if q == "q4k" else "gemv_q6k") + ("_f32" if fused else "")
 
     def launches_per_step(self, front_end: str = "auto") -> int:
@@ -608,7 +613,7 @@ def main():
                          "of at most 4096 values, unfused for larger ones")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100}[args.config]
+        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100, 5: 100}[args.config]
     args.graph_steps = max(1, min(args.graph_steps, args.steps))
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

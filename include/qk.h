@@ -234,6 +234,24 @@ int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales,
                void *workspace, size_t workspace_bytes,
                unsigned flags, void *stream);
 
+/*
+ * The same prefill contraction with a Q6_K weight (qk_repack output for
+ * QK_TYPE_Q6_K).  Q4_K_M models keep some tensors in Q6_K: minfer "15 .
+ * The CUDA backend" sec. 2.2 sends Q4_K, Q5_K and Q6_K weights to the same
+ * MMQ, and in cajeta.dev "xpu walkthrough" step 3 (prefill) the Q6_K value
+ * and down projections of 16 layers run on their own tiles.  Each weight
+ * enters the tensor cores as
+ * 256 * d * sc * (q - 32) = W_hi + W_lo, the same split as for Q4_K; the
+ * bound, the value limits (|x| <= 65000 per block, |w| < 255), the
+ * workspace (same size, qk_mmq_workspace_bytes) and every other argument
+ * rule are those of qk_mmq_q4k.
+ */
+int qk_mmq_q6k(const void *w, const int8_t *codes, const void *scales,
+               int64_t M, int64_t N, int64_t K,
+               const float *residual, float *y,
+               void *workspace, size_t workspace_bytes,
+               unsigned flags, void *stream);
+
 /* ================================================ MMQ without a workspace
  * The pages have no counterpart of this entry point: it is a convenience of
  * this library for callers that cannot supply a device workspace (a host

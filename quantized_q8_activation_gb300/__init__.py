@@ -34,7 +34,7 @@ STATUS = {0: "QK_OK", -1: "QK_E_NULL", -2: "QK_E_SHAPE", -3: "QK_E_ALIGN", -4: "
 # every symbol include/qk.h declares
 EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1", "qk_repacked_bytes",
            "qk_repack", "qk_gemv_q4k", "qk_gemv_q6k", "qk_gemv_q4k_f32", "qk_gemv_q6k_f32",
-           "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_mmq_q4k_noalloc", "qk_error_flags"]
+           "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_mmq_q6k", "qk_mmq_q4k_noalloc", "qk_error_flags"]
 
 _lib = None
 _lock = threading.Lock()
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
             L.qk_gemv_q6k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
             L.qk_mmq_workspace_bytes.argtypes = [i64, i64, i64, szp]
             L.qk_mmq_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
+            L.qk_mmq_q6k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
             L.qk_mmq_q4k_noalloc.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
             L.qk_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
             for name in EXPORTS:
@@ -234,6 +235,15 @@ def gemv_q6k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=N
 
 def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None):
     """Prefill contraction over a repacked Q4_K weight, any M."""
+    return _mmq("qk_mmq_q4k", w, codes, scales, N, K, residual, y, workspace, pdl, stream)
+
+
+def mmq_q6k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None):
+    """Prefill contraction over a repacked Q6_K weight, any M."""
+    return _mmq("qk_mmq_q6k", w, codes, scales, N, K, residual, y, workspace, pdl, stream)
+
+
+def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream):
     M = codes.shape[0]
     for t, n in ((w, "w"), (codes, "codes"), (scales, "scales")):
         _cuda(t, n)
@@ -243,9 +253,9 @@ def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=F
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=codes.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().qk_mmq_q4k(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
-                          _p(workspace), wsb, LAUNCH_PDL if pdl else 0, _stream(stream))
-    _check(st, "qk_mmq_q4k")
+    st = getattr(lib(), fn)(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
+                            _p(workspace), wsb, LAUNCH_PDL if pdl else 0, _stream(stream))
+    _check(st, fn)
     return y
 
 

@@ -1,5 +1,6 @@
-// qk_mmq.cu -- prefill contraction Y[M][N] = Xq8 . W_q4k^T (+ R) on the
-// sm_103a tensor cores (tcgen05, accumulator in tensor memory).
+// qk_mmq.cu -- prefill contraction Y[M][N] = Xq8 . W^T (+ R), W a Q4_K or a
+// Q6_K weight, on the sm_103a tensor cores (tcgen05, accumulator in tensor
+// memory).
 //
 // Method (minfer "15 . The CUDA backend" sec. 2.3 / 3.2.6: quantized weight
 // bytes go straight to the tensor cores; the activation is quantized to q8_1
@@ -8,12 +9,14 @@
 //   A[m][k] = d_a * q_a = A_hi + A_lo   exactly (d_a has 11 significant bits
 //             and q_a 7, so the product needs 18 <= 2 x 11 bits);
 //   W[n][k] = 256 * (d_b sc_j q_w - dmin_b m_j) = W_hi + W_lo, the Q4_K weight
-//             scaled by 2^8 (so that W_lo stays in the normal f16 range for
-//             the weights of LLM layers), split to 2^-21 relative;
+//             (Q6_K: 256 * d_b sc_j (q_w - 32), the same form with the min
+//             term 32 d_b sc_j) scaled by 2^8 (so that W_lo stays in the
+//             normal f16 range for the weights of LLM layers), split to
+//             2^-21 relative;
 //   Y = A_hi W_hi + A_hi W_lo + A_lo W_hi   (A_lo W_lo is below 2^-21 of each
 //             product and dropped), accumulated in binary32 over all of K in
 //             tensor memory;  y = Y / 256 (+ R).
-// The Q4_K bytes are dequantized tile by tile in shared memory right before
+// The k-quant bytes are dequantized tile by tile in shared memory right before
 // the MMAs that use them; they are read from memory in their quantized form.
 //
 // Two kernels per call:
@@ -22,7 +25,7 @@
 //     layout: per 32-value K stage a 16 KB block (A_hi and A_lo tiles, K-major
 //     SWIZZLE_64B).  Every N-tile then copies these blocks instead of
 //     converting the activation again.
-//  2. mmq_q4k_kernel: a persistent grid, one CTA (24 warps) per SM, each CTA
+//  2. mmq_kernel<QT>: a persistent grid, one CTA (24 warps) per SM, each CTA
 //     taking 128 x 256 output tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
 //     (M-tile fastest).  512 TMEM columns hold two accumulators, so one tile
 //     accumulates while the previous one is written out:
@@ -30,15 +33,20 @@
 //       warp 1      lane 0 copies each K stage's 16 KB activation block from the
 //                   workspace into the stage slot with one bulk copy, as soon as
 //                   the MMAs have released the slot
-//       warp 2      lane 0 streams the raw Q4_K bytes with 2D TMA tensor copies
-//                   into a ring, per superblock: the two 64-byte runs of code
-//                   bytes (256 x 64 B each: first and second 16-byte halves of
-//                   its four groups) and the metadata records (256 x 16 B)
+//       warp 2      lane 0 streams the raw weight bytes with 2D TMA tensor
+//                   copies into a ring.  Q4_K, per superblock: the two 64-byte
+//                   runs of code bytes (256 x 64 B each: first and second
+//                   16-byte halves of its four groups) and the metadata records
+//                   (256 x 16 B).  Q6_K, per half superblock (128 values): its
+//                   32-byte runs of the two ql chunks and of qh (256 x 32 B
+//                   each); per superblock the scale records (256 x 16 B).  The
+//                   Q6_K d plane (2 bytes per superblock) is read by the
+//                   converters themselves, one superblock ahead.
 //       warps 4-7   the epilogue of the previous tile (TMEM lane quadrant =
 //                   warp % 4) while the next one accumulates
-//       warps 8-23  converters: two threads per weight row expand the Q4_K
-//                   codes, scales and mins of each K stage into (W_hi, W_lo) in
-//                   the SWIZZLE_64B layout
+//       warps 8-23  converters: two threads per weight row expand the codes,
+//                   scales (and Q4_K mins) of each K stage into (W_hi, W_lo)
+//                   in the SWIZZLE_64B layout
 // Stages are handed over with mbarriers (full: converters and the activation
 // copy's bytes -> MMA; empty: MMA commit -> converters and activation copier;
 // raw: TMA bytes -> converters -> producer; accumulator full / empty: MMA
@@ -55,6 +63,7 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <cstring>
 
 #ifndef QK_MMQ_NST
 #define QK_MMQ_NST 3        // operand stages
@@ -73,7 +82,7 @@ namespace {
 
 using namespace qk::tc;
 
-constexpr int BM = 128, BN = 256, BK = 32;      // BK: one Q4_K sub-block
+constexpr int BM = 128, BN = 256, BK = 32;      // BK: one Q4_K / Q6_K 32-value sub-block
 constexpr int NST = QK_MMQ_NST, NRAW = QK_MMQ_RAW, NSB = QK_MMQ_SBRAW;
 constexpr int kThreads = 768;
 constexpr int kEpiWarp0 = 4, kEpiWarps = 4, kConvWarp0 = 8;  // epilogue warps 4-7, converters 8-23
@@ -85,14 +94,14 @@ constexpr int ATILE = BM * BK * 2;              // 8 KB: 128 rows x 32 f16 (64 B
 constexpr int WTILE = BN * BK * 2;              // 16 KB: 256 rows x 32 f16
 constexpr int STAGE = 2 * ATILE + 2 * WTILE;    // A_hi | A_lo | W_hi | W_lo
 constexpr int ABLOCK = 2 * ATILE;               // workspace block of one M-tile and K stage: A_hi | A_lo
-// raw weight superblock: code bytes, first halves of its 4 groups 256 x 64 B | second halves 256 x 64 B
-constexpr int RAW_H0 = 0, RAW_H1 = BN * 64, RAW = 2 * BN * 64;
-constexpr int SBR = BN * 16;                    // raw metadata records of one superblock
-constexpr int OFF_RAW = NST * STAGE;
-constexpr int OFF_SBR = OFF_RAW + NRAW * RAW;
+// raw unit of the Q4_K ring, one superblock's code bytes: first halves of its 4 groups 256 x 64 B |
+// second halves 256 x 64 B
+constexpr int RAW_H0 = 0, RAW_H1 = BN * 64, RAW_Q4 = 2 * BN * 64;
+// raw unit of the Q6_K ring, half a superblock: ql first-chunk run 256 x 32 B | ql second-chunk run
+// 256 x 32 B | qh 256 x 32 B
+constexpr int RAW_QL0 = 0, RAW_QL1 = BN * 32, RAW_QH = 2 * BN * 32, RAW_Q6 = 3 * BN * 32;
+constexpr int SBR = BN * 16;                    // per-superblock records (Q4_K metadata, Q6_K scales)
 constexpr int EPI_LD = 17;                      // epilogue transpose buffer: 32 rows x 16 columns, padded
-constexpr int OFF_EPI = OFF_SBR + NSB * SBR;
-constexpr int OFF_BAR = OFF_EPI + kEpiWarps * 32 * EPI_LD * 4;
 enum {
     B_FULL = 0,
     B_EMPTY = B_FULL + NST,
@@ -105,11 +114,21 @@ enum {
     B_DONE = B_ACCEMPTY + 2,       // every MMA of the CTA has completed
     NBAR = B_DONE + 1
 };
-constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
-constexpr int SMEM = OFF_TMEM + 16 + 1024;      // + slack to align the base to 1024
-static_assert(SMEM <= 232448, "shared memory plan exceeds the per-block opt-in limit");
-static_assert(STAGE % 1024 == 0 && OFF_RAW % 1024 == 0 && RAW % 1024 == 0 && SBR % 1024 == 0,
-              "copy destinations and swizzle atoms stay aligned");
+// shared-memory plan of mmq_kernel<QT>
+template <int QT>
+struct Plan {
+    static constexpr bool Q6 = QT == QK_TYPE_Q6_K;
+    static constexpr int RAW = Q6 ? RAW_Q6 : RAW_Q4;
+    static constexpr int OFF_RAW = NST * STAGE;
+    static constexpr int OFF_SBR = OFF_RAW + NRAW * RAW;
+    static constexpr int OFF_EPI = OFF_SBR + NSB * SBR;
+    static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * 32 * EPI_LD * 4;
+    static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_TMEM + 16 + 1024;   // + slack to align the base to 1024
+    static_assert(SMEM <= 232448, "shared memory plan exceeds the per-block opt-in limit");
+    static_assert(STAGE % 1024 == 0 && OFF_RAW % 1024 == 0 && RAW % 1024 == 0 && SBR % 1024 == 0,
+                  "copy destinations and swizzle atoms stay aligned");
+};
 constexpr uint32_t TMEM_COLS = 2 * BN;           // two accumulators: tile k+1 accumulates while tile k drains
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 
@@ -123,6 +142,7 @@ __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__
 
 struct MmqArgs {
     const uint8_t *wsA;     // workspace: [M-tiles][K/32] A blocks
+    const uint16_t *dq;     // Q6_K: the d plane of the repacked weight, binary16 [N][K/256]
     int64_t M, N, K;
     const float *residual;
     float *y;
@@ -130,8 +150,9 @@ struct MmqArgs {
 };
 
 struct MmqMaps {
-    CUtensorMap wcodes;     // uint8  [N][B*128]      box 64 x 256  (code plane of the repacked weight)
-    CUtensorMap meta;       // uint8  [N][B*16]       box 16 x 256  (metadata plane)
+    CUtensorMap wcodes;     // uint8  [N][B*128]  Q4_K code plane, box 64 x 256; Q6_K ql plane, box 32 x 256
+    CUtensorMap meta;       // uint8  [N][B*16]   Q4_K metadata plane / Q6_K scale plane, box 16 x 256
+    CUtensorMap qh;         // uint8  [N][B*64]   Q6_K qh plane, box 32 x 256 (unused for Q4_K)
 };
 
 // 4 int8 codes -> (A_hi, A_lo) f16 pairs with A_hi + A_lo = d * q exactly
@@ -225,10 +246,14 @@ __global__ void __launch_bounds__(256) mmq_prep_kernel(const int8_t *__restrict_
 
 // ------------------------------------------------------------- main kernel
 
-// Converter state of one half row across K stages: its 16 code bytes of the current
-// 64-value group and the row's metadata record of the current superblock.
+// Converter state of one half row across K stages.  Q4_K: its 16 code bytes of the current
+// 64-value group (c) and the row's metadata record of the current superblock (mt).  Q6_K: its 16
+// bytes of each ql chunk (c, c2) and of qh (qh) of the current half superblock, the row's scale
+// record of the current superblock (mt), and the superblock's d (binary16 bits) with the next
+// superblock's d already requested (dn).
 struct ConvState {
-    uint4 c, mt;
+    uint4 c, mt, c2, qh;
+    uint32_t d, dn;
 };
 
 // one converter thread's share of K stage `it` (operand stage st = it % NST): the 16 weights of
@@ -236,18 +261,19 @@ struct ConvState {
 // stage is signalled full
 // it: K stage within the tile; gs / gsb: the stage and superblock counted over all tiles of
 // this CTA (ring slots and barrier phases)
-__device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, ConvState &cs,
-                                              int it, int gs, int gsb, int row, int h, int st)
+__device__ __forceinline__ void convert_stage_q4(uint8_t *smem, uint64_t *bar, ConvState &cs,
+                                                 int it, int gs, int gsb, int row, int h, int st)
 {
+    using L = Plan<QK_TYPE_Q4_K>;
     const int j = it & 7, g = j >> 1, nib = j & 1;
     const int rs = gsb % NRAW, ss = gsb % NSB;
     if (j == 0) {
         wait_bar(&bar[B_SFULL + ss], (gsb / NSB) & 1);
-        cs.mt = *reinterpret_cast<const uint4 *>(smem + OFF_SBR + ss * SBR + row * 16);
+        cs.mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * SBR + row * 16);
         wait_bar(&bar[B_RFULL + rs], (gsb / NRAW) & 1);
     }
     if (nib == 0)
-        cs.c = *reinterpret_cast<const uint4 *>(smem + OFF_RAW + rs * RAW + (h ? RAW_H1 : RAW_H0) + row * 64 + 16 * g);
+        cs.c = *reinterpret_cast<const uint4 *>(smem + L::OFF_RAW + rs * L::RAW + (h ? RAW_H1 : RAW_H0) + row * 64 + 16 * g);
     if (gs >= NST) wait_bar(&bar[B_EMPTY + st], ((gs / NST) + 1) & 1);
     uint8_t *s0 = smem + st * STAGE;
     // this group's record: sc0 | sc1<<6 | m0<<12 | m1<<18 (sub-blocks 2g and 2g+1)
@@ -285,12 +311,86 @@ __device__ __forceinline__ void convert_stage(uint8_t *smem, uint64_t *bar, Conv
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
+// Q6_K: the d of superblock sb of tile t for this converter's weight row (0 past the last row)
+__device__ __forceinline__ uint32_t q6_d(const MmqArgs &a, int t, int sb, int row)
 {
+    const int64_t n = (int64_t)(t / a.mtiles) * BN + row;
+    return n < a.N ? (uint32_t)__ldg(a.dq + n * (a.K >> 8) + sb) : 0u;
+}
+
+// Q6_K share of one converter thread in K stage `it` (sub-block j = it % 8 of superblock it / 8:
+// half hs = j / 4 of the superblock, quarter q = j % 4): the 16 weights l = 16h .. 16h+15 of the
+// sub-block,
+//   w = 256 d sc (u - 32),  u = ql nibble | qh bit pair << 4,
+// with the ql byte from the first chunk run (q even) or the second (q odd), its low (q < 2) or high
+// nibble, the qh bits 2q, 2q+1, and scale byte 4 (2 hs + h) + q of the record.  Stored as
+// (W_hi, W_lo) chunks 2h and 2h+1, then the stage is signalled full.
+// gsb: superblock counted over all tiles of this CTA; t: the tile (for the d prefetch)
+__device__ __forceinline__ void convert_stage_q6(uint8_t *smem, uint64_t *bar, ConvState &cs, const MmqArgs &a,
+                                                 int t, int it, int gs, int gsb, int row, int h, int st)
+{
+    using L = Plan<QK_TYPE_Q6_K>;
+    const int j = it & 7, hs = j >> 2, q = j & 3;
+    const int gu = 2 * gsb + hs;                              // raw unit: half superblock
+    const int rs = gu % NRAW, ss = gsb % NSB;
+    if (j == 0) {
+        wait_bar(&bar[B_SFULL + ss], (gsb / NSB) & 1);
+        cs.mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * SBR + row * 16);
+        // this superblock's d was requested one superblock ago; request the next one's
+        const int B = (int)(a.K >> 8), sb = it >> 3;
+        cs.d = cs.dn;
+        if (sb + 1 < B) cs.dn = q6_d(a, t, sb + 1, row);
+        else if (t + (int)gridDim.x < a.mtiles * a.ntiles) cs.dn = q6_d(a, t + gridDim.x, 0, row);
+    }
+    if (q == 0) {
+        wait_bar(&bar[B_RFULL + rs], (gu / NRAW) & 1);
+        const uint8_t *r0 = smem + L::OFF_RAW + rs * L::RAW + row * 32 + 16 * h;
+        cs.c = *reinterpret_cast<const uint4 *>(r0 + RAW_QL0);
+        cs.c2 = *reinterpret_cast<const uint4 *>(r0 + RAW_QL1);
+        cs.qh = *reinterpret_cast<const uint4 *>(r0 + RAW_QH);
+    }
+    if (gs >= NST) wait_bar(&bar[B_EMPTY + st], ((gs / NST) + 1) & 1);
+    uint8_t *s0 = smem + st * STAGE;
+    const int p = 2 * hs + h;                                 // record bytes 4p .. 4p+3: quarters 0..3
+    const uint32_t scw = p == 0 ? cs.mt.x : p == 1 ? cs.mt.y : p == 2 ? cs.mt.z : cs.mt.w;
+    const int sc = (int)(int8_t)(scw >> (8 * q));
+    const float d = __half2float(__ushort_as_half((unsigned short)cs.d));
+    const float dsc = d * (float)sc * kWScale;               // exact: 11 + 8 significant bits, times 2^8
+    const float2 dsc2 = make_float2(dsc, dsc), ndmm2 = make_float2(-32.0f * dsc, -32.0f * dsc);
+    const uint4 lq = (q & 1) ? cs.c2 : cs.c;
+    const uint32_t lw[4] = {lq.x, lq.y, lq.z, lq.w};
+    const uint32_t hw[4] = {cs.qh.x, cs.qh.y, cs.qh.z, cs.qh.w};
+    const int ls = (q >> 1) * 4, hsft = 2 * q;
+#pragma unroll
+    for (int cc = 0; cc < 2; cc++) {
+        uint32_t hi[4], lo[4];
+        const uint32_t x0 = ((lw[2 * cc] >> ls) & 0x0F0F0F0Fu) | (((hw[2 * cc] >> hsft) & 0x03030303u) << 4);
+        const uint32_t x1 = ((lw[2 * cc + 1] >> ls) & 0x0F0F0F0Fu) | (((hw[2 * cc + 1] >> hsft) & 0x03030303u) << 4);
+        conv_w(x0, dsc2, ndmm2, hi[0], hi[1], lo[0], lo[1]);
+        conv_w(x1, dsc2, ndmm2, hi[2], hi[3], lo[2], lo[3]);
+        sts128(s0 + 2 * ATILE, sw64(row, 2 * h + cc), hi[0], hi[1], hi[2], hi[3]);
+        sts128(s0 + 2 * ATILE + WTILE, sw64(row, 2 * h + cc), lo[0], lo[1], lo[2], lo[3]);
+    }
+    // as for Q4_K: the stores are made visible to the async proxy, and a ring slot is released only
+    // after every value loaded from it has been used by the arithmetic (the second ql chunk is
+    // first used in quarter 1)
+    fence_proxy_async();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        if (q == 1) mbar_arrive(&bar[B_REMPTY + rs]);
+        if (j == 0) mbar_arrive(&bar[B_SEMPTY + ss]);
+        mbar_arrive(&bar[B_FULL + st]);
+    }
+}
+
+template <int QT>
+__global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
+{
+    using L = Plan<QT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + OFF_TMEM);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + L::OFF_TMEM);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = (int)(a.K >> 8), nit = 8 * B;
     const int ntiles = a.mtiles * a.ntiles;
@@ -373,26 +473,44 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
         if (lane == 0) {
             prefetch_tmap(&maps.wcodes);
             prefetch_tmap(&maps.meta);
-            int gsb = 0;
+            if (L::Q6) prefetch_tmap(&maps.qh);
+            int gsb = 0, gu = 0;                                  // superblocks and raw units issued
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
                 const int n0 = (t / a.mtiles) * BN;
                 for (int sb = 0; sb < B; sb++, gsb++) {
                     const int ss = gsb % NSB;
                     if (gsb >= NSB) wait_bar(&bar[B_SEMPTY + ss], ((gsb / NSB) + 1) & 1);
                     mbar_arrive_expect_tx(&bar[B_SFULL + ss], SBR);
-                    tma_load_2d(smem + OFF_SBR + ss * SBR, &maps.meta, 16 * sb, n0, &bar[B_SFULL + ss]);
-                    const int rs = gsb % NRAW;
-                    if (gsb >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((gsb / NRAW) + 1) & 1);
-                    uint8_t *d = smem + OFF_RAW + rs * RAW;
-                    // the superblock's 4 groups: first halves at 16u (u = 4 (sb - 8 s) .. +3), second at 16 G + 16u
+                    tma_load_2d(smem + L::OFF_SBR + ss * SBR, &maps.meta, 16 * sb, n0, &bar[B_SFULL + ss]);
+                    // the superblock's lanes u = 4 (sb - 8 s) .. +3 of its step s: first 16-byte chunks at 16u,
+                    // second chunks at 16 G + 16u
                     const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s);
-                    mbar_arrive_expect_tx(&bar[B_RFULL + rs], RAW);
-                    tma_load_2d(d + RAW_H0, &maps.wcodes, 1024 * s + 16 * u, n0, &bar[B_RFULL + rs]);
-                    tma_load_2d(d + RAW_H1, &maps.wcodes, 1024 * s + 16 * G + 16 * u, n0, &bar[B_RFULL + rs]);
+                    if constexpr (!L::Q6) {
+                        const int rs = gu % NRAW;
+                        if (gu >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((gu / NRAW) + 1) & 1);
+                        uint8_t *d = smem + L::OFF_RAW + rs * L::RAW;
+                        mbar_arrive_expect_tx(&bar[B_RFULL + rs], L::RAW);
+                        tma_load_2d(d + RAW_H0, &maps.wcodes, 1024 * s + 16 * u, n0, &bar[B_RFULL + rs]);
+                        tma_load_2d(d + RAW_H1, &maps.wcodes, 1024 * s + 16 * G + 16 * u, n0, &bar[B_RFULL + rs]);
+                        gu++;
+                    } else {
+                        // two raw units: superblock half hs holds lanes u + 2hs, u + 2hs + 1 of each ql run
+                        // and qh bytes 32hs .. 32hs+31
+                        for (int hs = 0; hs < 2; hs++, gu++) {
+                            const int rs = gu % NRAW;
+                            if (gu >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((gu / NRAW) + 1) & 1);
+                            uint8_t *d = smem + L::OFF_RAW + rs * L::RAW;
+                            mbar_arrive_expect_tx(&bar[B_RFULL + rs], L::RAW);
+                            tma_load_2d(d + RAW_QL0, &maps.wcodes, 1024 * s + 16 * u + 32 * hs, n0, &bar[B_RFULL + rs]);
+                            tma_load_2d(d + RAW_QL1, &maps.wcodes, 1024 * s + 16 * G + 16 * u + 32 * hs, n0,
+                                        &bar[B_RFULL + rs]);
+                            tma_load_2d(d + RAW_QH, &maps.qh, 64 * sb + 32 * hs, n0, &bar[B_RFULL + rs]);
+                        }
+                    }
                 }
             }
             // teardown: every copy this thread issued has landed (normally long since consumed)
-            for (int g = gsb - NRAW < 0 ? 0 : gsb - NRAW; g < gsb; g++) wait_bar(&bar[B_RFULL + g % NRAW], (g / NRAW) & 1);
+            for (int g = gu - NRAW < 0 ? 0 : gu - NRAW; g < gu; g++) wait_bar(&bar[B_RFULL + g % NRAW], (g / NRAW) & 1);
             for (int g = gsb - NSB < 0 ? 0 : gsb - NSB; g < gsb; g++) wait_bar(&bar[B_SFULL + g % NSB], (g / NSB) & 1);
         }
         __syncwarp();
@@ -402,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
         // of the block; the block is transposed through shared memory so that each store covers 16
         // consecutive columns of two rows
         const uint32_t lq = (uint32_t)((warp & 3) * 32) << 16;   // TMEM lane quadrant of this warp
-        float *tb_s = reinterpret_cast<float *>(smem + OFF_EPI) + (warp - kEpiWarp0) * (32 * EPI_LD);
+        float *tb_s = reinterpret_cast<float *>(smem + L::OFF_EPI) + (warp - kEpiWarp0) * (32 * EPI_LD);
         const int q0 = (warp & 3) * 32;
         int kt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
@@ -446,24 +564,29 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_q4k_kernel(const MmqArgs a, c
         const int cwarp = warp - kConvWarp0;                      // 0..15
         const int row = 16 * cwarp + (lane & 15), h = lane >> 4;
         ConvState cs;
-        cs.c = cs.mt = make_uint4(0, 0, 0, 0);
+        cs.c = cs.mt = cs.c2 = cs.qh = make_uint4(0, 0, 0, 0);
+        cs.d = 0;
+        cs.dn = L::Q6 ? q6_d(a, blockIdx.x, 0, row) : 0u;
         int kt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
             const int gs0 = kt * nit;
             // the stage slot of K stage it is (gs0 + it) % NST: unroll so that it is static
             static_assert(NST == 3, "the slot prologue below handles three stages");
             int it = 0;
+            auto conv = [&](int itk, int gs, int st) {
+                if constexpr (L::Q6) convert_stage_q6(smem, bar, cs, a, t, itk, gs, kt * B + (itk >> 3), row, h, st);
+                else convert_stage_q4(smem, bar, cs, itk, gs, kt * B + (itk >> 3), row, h, st);
+            };
             while (it < nit && (gs0 + it) % NST != 0) {
                 const int gs = gs0 + it;
-                if (gs % NST == 1) convert_stage(smem, bar, cs, it, gs, kt * B + (it >> 3), row, h, 1);
-                else convert_stage(smem, bar, cs, it, gs, kt * B + (it >> 3), row, h, 2);
+                if (gs % NST == 1) conv(it, gs, 1);
+                else conv(it, gs, 2);
                 it++;
             }
             for (; it < nit; it += NST) {
 #pragma unroll
                 for (int k = 0; k < NST; k++)
-                    if (it + k < nit)
-                        convert_stage(smem, bar, cs, it + k, gs0 + it + k, kt * B + ((it + k) >> 3), row, h, k);
+                    if (it + k < nit) conv(it + k, gs0 + it + k, k);
             }
         }
     }
@@ -517,6 +640,77 @@ size_t ws_bytes(int64_t M, int64_t K)
     return mt * (size_t)(K / BK) * ABLOCK;
 }
 
+template <int QT>
+int set_attrs()
+{
+    static std::atomic<int> done{0};
+    if (done.load()) return QK_OK;
+    if (cudaFuncSetAttribute(mmq_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan<QT>::SMEM) !=
+            cudaSuccess ||
+        qk::max_carveout(mmq_kernel<QT>) != cudaSuccess)
+        return QK_E_CUDA;
+    done.store(1);
+    return QK_OK;
+}
+
+int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N, int64_t K,
+        const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags, void *stream)
+{
+    // TMA coordinates are signed 32-bit: rows and bytes of a row stay below 2^31
+    if (M < 0 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || M > 0x7fffffffLL || K > 0x7fffffffLL)
+        return QK_E_SHAPE;
+    if (M == 0) return QK_OK;
+    if (!w || !codes || !scales || !y || !workspace) return QK_E_NULL;
+    if (!qk::aligned(w, 16) || !qk::aligned(codes, 16) || !qk::aligned(scales, 16) || !qk::aligned(y, 4) ||
+        (residual && !qk::aligned(residual, 4)) || !qk::aligned(workspace, 256))
+        return QK_E_ALIGN;
+    const size_t need = ws_bytes(M, K);
+    if (workspace_bytes < need) return QK_E_WORKSPACE;
+    size_t wbytes = 0;
+    qk_repacked_bytes(qt, N, K, &wbytes);
+    const size_t ybytes = (size_t)M * N * 4, cbytes = (size_t)M * K, sbytes = (size_t)M * (K / 32) * 4;
+    if (qk::overlaps(y, ybytes, w, wbytes) || qk::overlaps(y, ybytes, codes, cbytes) ||
+        qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)) ||
+        qk::overlaps(workspace, need, w, wbytes) || qk::overlaps(workspace, need, codes, cbytes) ||
+        qk::overlaps(workspace, need, scales, sbytes) || qk::overlaps(workspace, need, y, ybytes) ||
+        (residual && qk::overlaps(workspace, need, residual, ybytes)))
+        return QK_E_ALIAS;
+    const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
+    if (gx > 65535 || gy > 65535 || gx * gy > 0x7fffffffLL) return QK_E_SHAPE;
+    const bool q6 = qt == QK_TYPE_Q6_K;
+    const size_t smem = q6 ? (size_t)Plan<QK_TYPE_Q6_K>::SMEM : (size_t)Plan<QK_TYPE_Q4_K>::SMEM;
+    if (smem > qk::max_smem_optin()) return QK_E_CUDA;
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return QK_E_CUDA;
+    const int64_t B = K / 256;
+    const uint8_t *wb = static_cast<const uint8_t *>(w);
+    MmqMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (!q6) {
+        if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 64, BN) ||
+            !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 16, N, B * 16, 16, BN))
+            return QK_E_CUDA;
+    } else {
+        if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 32, BN) ||
+            !make_map(enc, &maps.qh, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 64, N, B * 64, 32, BN) ||
+            !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 192, B * 16, N, B * 16, 16, BN))
+            return QK_E_CUDA;
+    }
+    const int st0 = q6 ? set_attrs<QK_TYPE_Q6_K>() : set_attrs<QK_TYPE_Q4_K>();
+    if (st0 != QK_OK) return st0;
+    uint8_t *wsA = static_cast<uint8_t *>(workspace);
+    int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, (cudaStream_t)stream,
+                        (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA);
+    if (st != QK_OK) return st;
+    MmqArgs args{wsA, q6 ? reinterpret_cast<const uint16_t *>(wb + N * B * 208) : nullptr, M, N, K, residual, y,
+                 (int)gx, (int)gy};
+    const int64_t tiles = gx * gy, grid = tiles < qk::sm_count() ? tiles : qk::sm_count();
+    return q6 ? qk::launch(mmq_kernel<QK_TYPE_Q6_K>, dim3((unsigned)grid), dim3(kThreads), smem, (cudaStream_t)stream,
+                           true, args, maps)
+              : qk::launch(mmq_kernel<QK_TYPE_Q4_K>, dim3((unsigned)grid), dim3(kThreads), smem, (cudaStream_t)stream,
+                           true, args, maps);
+}
+
 }  // namespace
 
 extern "C" int qk_error_flags(unsigned *flags, int clear)
@@ -542,49 +736,12 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
                           const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,
                           void *stream)
 {
-    // TMA coordinates are signed 32-bit: rows and bytes of a row stay below 2^31
-    if (M < 0 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || M > 0x7fffffffLL || K > 0x7fffffffLL)
-        return QK_E_SHAPE;
-    if (M == 0) return QK_OK;
-    if (!w || !codes || !scales || !y || !workspace) return QK_E_NULL;
-    if (!qk::aligned(w, 16) || !qk::aligned(codes, 16) || !qk::aligned(scales, 16) || !qk::aligned(y, 4) ||
-        (residual && !qk::aligned(residual, 4)) || !qk::aligned(workspace, 256))
-        return QK_E_ALIGN;
-    const size_t need = ws_bytes(M, K);
-    if (workspace_bytes < need) return QK_E_WORKSPACE;
-    size_t wbytes = 0;
-    qk_repacked_bytes(QK_TYPE_Q4_K, N, K, &wbytes);
-    const size_t ybytes = (size_t)M * N * 4, cbytes = (size_t)M * K, sbytes = (size_t)M * (K / 32) * 4;
-    if (qk::overlaps(y, ybytes, w, wbytes) || qk::overlaps(y, ybytes, codes, cbytes) ||
-        qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)) ||
-        qk::overlaps(workspace, need, w, wbytes) || qk::overlaps(workspace, need, codes, cbytes) ||
-        qk::overlaps(workspace, need, scales, sbytes) || qk::overlaps(workspace, need, y, ybytes) ||
-        (residual && qk::overlaps(workspace, need, residual, ybytes)))
-        return QK_E_ALIAS;
-    const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
-    if (gx > 65535 || gy > 65535 || gx * gy > 0x7fffffffLL) return QK_E_SHAPE;
-    if ((size_t)SMEM > qk::max_smem_optin()) return QK_E_CUDA;
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return QK_E_CUDA;
-    const int64_t B = K / 256;
-    const uint8_t *wb = static_cast<const uint8_t *>(w);
-    MmqMaps maps;
-    if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 64, BN) ||
-        !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 16, N, B * 16, 16, BN))
-        return QK_E_CUDA;
-    static std::atomic<int> attr_set{0};
-    if (!attr_set.load()) {
-        if (cudaFuncSetAttribute(mmq_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess ||
-            qk::max_carveout(mmq_q4k_kernel) != cudaSuccess)
-            return QK_E_CUDA;
-        attr_set.store(1);
-    }
-    uint8_t *wsA = static_cast<uint8_t *>(workspace);
-    int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, (cudaStream_t)stream,
-                        (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA);
-    if (st != QK_OK) return st;
-    MmqArgs args{wsA, M, N, K, residual, y, (int)gx, (int)gy};
-    const int64_t tiles = gx * gy, grid = tiles < qk::sm_count() ? tiles : qk::sm_count();
-    return qk::launch(mmq_q4k_kernel, dim3((unsigned)grid), dim3(kThreads), SMEM, (cudaStream_t)stream, true, args,
-                      maps);
+    return mmq(QK_TYPE_Q4_K, w, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags, stream);
+}
+
+extern "C" int qk_mmq_q6k(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N, int64_t K,
+                          const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,
+                          void *stream)
+{
+    return mmq(QK_TYPE_Q6_K, w, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags, stream);
 }

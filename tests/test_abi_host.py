@@ -125,8 +125,9 @@ def test_mmq_workspace_size():
     assert qk.mmq_workspace_bytes(0, 64, 256) == 0
 
 
-def test_mmq_rejects(L):
-    f = L.qk_mmq_q4k
+@pytest.mark.parametrize("fn", ["qk_mmq_q4k", "qk_mmq_q6k"])
+def test_mmq_rejects(L, fn):
+    f = getattr(L, fn)
     w, c, s, y, ws = P, P + 0x10000000, P + 0x20000000, P + 0x30000000, P + 0x40000000
     need = qk.mmq_workspace_bytes(16, 64, 256)
     assert f(w, c, s, 0, 64, 256, None, y, None, 0, 0, None) == 0   # M = 0: nothing to do

@@ -25,7 +25,7 @@ def sample_rows(N, n=24, seed=0):
 
 
 @pytest.mark.parametrize("cfg_id,front_end", [(0, "fused"), (1, "fused"), (2, "fused"), (3, "fused"), (1, "unfused"),
-                                              (3, "unfused"), (1, "auto"), (4, "auto")])
+                                              (3, "unfused"), (1, "auto"), (4, "auto"), (5, "auto")])
 def test_config_full_size(cfg_id, front_end):
     import bench
     wl = bench.Workload(cfg_id, seed=0, copies=1)

@@ -284,55 +284,63 @@ def test_gemv_f32_matches_q8_path_bitwise(qt):
 
 # ----------------------------------------------------------------------- MMQ
 
+def mmq_fn(qt):
+    return qk.mmq_q4k if qt == "q4k" else qk.mmq_q6k
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
 @pytest.mark.parametrize("M,N,K", [(1, 64, 256), (17, 130, 512), (64, 128, 2304), (130, 300, 4096),
                                    (200, 77, 768), (65, 129, 256 * 9)])
-def test_mmq_parity(M, N, K):
-    w, wr = weights("q4k", N, K, seed=M * 3 + N + K)
+def test_mmq_parity(qt, M, N, K):
+    w, wr = weights(qt, N, K, seed=M * 3 + N + K)
     x = synth.activations(M, K, seed=M)
     codes, scales = q8(x)
     c, d = q8_host(codes, scales)
-    y = qk.mmq_q4k(wr, codes, scales, N, K).cpu().numpy()
-    y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d)
-    check(y, y_ref, ab, what=f"mmq M={M} N={N} K={K}")
+    y = mmq_fn(qt)(wr, codes, scales, N, K).cpu().numpy()
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+    check(y, y_ref, ab, what=f"mmq {qt} M={M} N={N} K={K}")
 
 
-def test_mmq_residual_inplace_deterministic():
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+def test_mmq_residual_inplace_deterministic(qt):
     M, N, K = 96, 200, 1024
-    w, wr = weights("q4k", N, K, seed=51)
+    w, wr = weights(qt, N, K, seed=51)
     codes, scales = q8(synth.activations(M, K, seed=52))
     c, d = q8_host(codes, scales)
     r = synth.residual(M, N, seed=53)
     rt = dev(r)
-    y = qk.mmq_q4k(wr, codes, scales, N, K, residual=rt, y=rt)
-    y2 = qk.mmq_q4k(wr, codes, scales, N, K, residual=dev(r), pdl=True)
+    y = mmq_fn(qt)(wr, codes, scales, N, K, residual=rt, y=rt)
+    y2 = mmq_fn(qt)(wr, codes, scales, N, K, residual=dev(r), pdl=True)
     torch.cuda.synchronize()
     assert torch.equal(y, y2)
-    y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d, residual=r)
-    check(y.cpu().numpy(), y_ref, ab, r, what="mmq residual")
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d, residual=r)
+    check(y.cpu().numpy(), y_ref, ab, r, what=f"mmq {qt} residual")
 
 
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
 @pytest.mark.parametrize("scale", [1e-3, 30.0, 1000.0])
-def test_mmq_activation_magnitudes(scale):
+def test_mmq_activation_magnitudes(qt, scale):
     """Small and large activations (the min-term operands are rescaled by powers of two)."""
     M, N, K = 40, 96, 1024
-    w, wr = weights("q4k", N, K, seed=61)
+    w, wr = weights(qt, N, K, seed=61)
     x = synth.activations(M, K, seed=62) * np.float32(scale)
     codes, scales = q8(x)
     c, d = q8_host(codes, scales)
-    y = qk.mmq_q4k(wr, codes, scales, N, K).cpu().numpy()
-    y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d)
-    check(y, y_ref, ab, what=f"mmq scale={scale}")
+    y = mmq_fn(qt)(wr, codes, scales, N, K).cpu().numpy()
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+    check(y, y_ref, ab, what=f"mmq {qt} scale={scale}")
 
 
-def test_mmq_edges_and_error_flags():
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+def test_mmq_edges_and_error_flags(qt):
     """One row, one column, a ragged 129 x 257 tile grid; no bounded wait gives up."""
     qk.error_flags(clear=True)
     for M, N, K in [(1, 1, 256), (129, 257, 512), (128, 128, 256)]:
-        w, wr = weights("q4k", N, K, seed=M + N)
+        w, wr = weights(qt, N, K, seed=M + N)
         codes, scales = q8(synth.activations(M, K, seed=N))
         c, d = q8_host(codes, scales)
-        y = qk.mmq_q4k(wr, codes, scales, N, K).cpu().numpy()
-        y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d)
-        check(y, y_ref, ab, what=f"mmq edge M={M} N={N} K={K}")
+        y = mmq_fn(qt)(wr, codes, scales, N, K).cpu().numpy()
+        y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+        check(y, y_ref, ab, what=f"mmq {qt} edge M={M} N={N} K={K}")
     torch.cuda.synchronize()
     assert qk.error_flags(clear=True) == 0
