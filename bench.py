@@ -16,6 +16,10 @@ data of the stated distributions):
      gate||up 37888x3584, down 3584x18944 (+res)
   5  config 4 as a Q4_K_M layer that keeps its down projection in Q6_K (the
      Q4_K_M recipe routes some down and value projections to Q6_K)
+  6  config 1 as a chain with the fused producers: RMSNorm -> q8_1 feeds QKV,
+     attn-out adds the residual stream h, RMSNorm(h) -> q8_1 feeds gate||up,
+     SwiGLU -> q8_1 of its output feeds down, which adds h (attention itself is
+     not part of the path: its output is a synthetic input)
 
 Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
 graphs (programmatic dependent launch between the kernels), bracketed by a
@@ -59,7 +63,11 @@ CONFIGS = {
             gemms=[(n, "q4k", N, K, r, s) for (n, N, K, r, s) in synth.QWEN2_7B_PREFILL]),
     5: dict(name="Qwen2-7B prefill MMQ, 2048 tokens (Q4_K, down projection in Q6_K)", M=2048, kind="mmq",
             gemms=[(n, "q6k" if n == "down" else "q4k", N, K, r, s) for (n, N, K, r, s) in synth.QWEN2_7B_PREFILL]),
+    6: dict(name="Llama-3-8B decode layer with fused RMSNorm/SwiGLU -> q8_1 producers, batch 1 (Q4_K)", M=1,
+            kind="chain", gemms=[(n, "q4k", N, K, r, s) for (n, N, K, r, s) in synth.LLAMA3_8B_LAYER],
+            inputs=["x_attn_in", "x_attn_out"]),
 }
+NORM_EPS = 1e-5                                       # Llama-3 RMSNorm epsilon
 
 
 def weight_bytes(cfg) -> int:
@@ -71,6 +79,8 @@ def int_ops(cfg) -> int:
 
 
 def gemm_fused(policy: str, cfg, gemm) -> bool:
+    if cfg["kind"] == "chain":                      # only attn-out reads an f32 activation the chain does not make
+        return gemm[0] == "attn_out"
     """Decode activation path of one GEMM: q8_1 quantization inside the GEMV ("fused")
     or a quantize kernel before its consumers.  "auto" quantizes inside the GEMV when the
     activation is small (M*K <= 4096: one float4 or two per thread), where saving the
@@ -99,6 +109,9 @@ TRAFFIC: dict = {
 
 
 def front_end_desc(front_end: str, cfg) -> str:
+    if cfg["kind"] == "chain":
+        return ("producers: qk_rmsnorm_q8_1 -> qkv; attn_out quantizes its f32 input inside the GEMV; "
+                "qk_rmsnorm_q8_1 -> gate_up; qk_swiglu_q8_1 -> down")
     if cfg["kind"] != "gemv":
         return "qk_quantize_q8_1 kernel per activation"
     parts = []
@@ -160,7 +173,8 @@ class Workload:
             for c in range(copies):
                 self.w[c][name] = qk.repack(qk.Q4_K if q == "q4k" else qk.Q6_K, g, N, K)
             del g
-        self.host_x = {s: synth.activations(M, K, seed=seed, tag=s) for s, K in slots(cfg)}
+        self.host_x = {s: synth.activations(M, K, seed=seed, tag=s) for s, K in slots(cfg)
+                       if s in cfg.get("inputs", [s])}
         self.x = {s: torch.from_numpy(v).to(device) for s, v in self.host_x.items()}
         self.q8 = {s: qk.empty_q8_1(M, K, device) for s, K in slots(cfg)}
         self.host_r, self.r, self.y = {}, {}, {}
@@ -169,6 +183,12 @@ class Workload:
                 self.host_r[name] = synth.residual(M, N, seed=seed, tag=name)
                 self.r[name] = torch.from_numpy(self.host_r[name]).to(device)
             self.y[name] = torch.empty((M, N), dtype=torch.float32, device=device)
+        self.host_g = {}
+        if cfg["kind"] == "chain":
+            self.host_g = chain_norm_weights(cfg, seed)
+            self.g = {t: torch.from_numpy(v).to(device) for t, v in self.host_g.items()}
+            self.r["down"] = self.y["attn_out"]       # down adds the residual stream h = attn-out's output
+            del self.host_r["down"]
         self.ws = None
         if cfg["kind"] == "mmq":
             need = max(qk.mmq_workspace_bytes(M, N, K) for (_, _, N, K, _, _) in cfg["gemms"])
@@ -180,7 +200,7 @@ class Workload:
         has one, must already be in self.q8)."""
         qk, cfg = self.qk, self.cfg
         name, q, N, K, res, s = gemm
-        if fused and cfg["kind"] == "gemv":
+        if fused and cfg["kind"] in ("gemv", "chain"):
             fn = qk.gemv_q4k_f32 if q == "q4k" else qk.gemv_q6k_f32
             fn(self.w[copy][name], self.x[s], N, K, residual=self.r.get(name), y=self.y[name],
                pdl=pdl, stream=stream)
@@ -199,6 +219,8 @@ class Workload:
         inside the GEMV (qk_gemv_*_f32) or reads the q8_1 codes of a quantize kernel that
         runs once per activation before its first consumer (see gemm_fused)."""
         qk, cfg = self.qk, self.cfg
+        if cfg["kind"] == "chain":
+            return self.chain_step(copy, pdl, stream)
         done = set()
         for gemm in cfg["gemms"]:
             s = gemm[5]
@@ -209,6 +231,22 @@ class Workload:
                 done.add(s)
             self.launch(gemm, copy, pdl=pdl, stream=stream, fused=fused)
 
+    def chain_step(self, copy: int, pdl: bool, stream):
+        """The decode layer with its producers: RMSNorm -> q8_1 -> QKV; attn-out (+ residual
+        stream) -> h; RMSNorm(h) -> q8_1 -> gate||up; SwiGLU -> q8_1 -> down (+ h)."""
+        qk, g = self.qk, {gm[0]: gm for gm in self.cfg["gemms"]}
+        kw = dict(pdl=pdl, stream=stream)
+        c, s = self.q8["x_attn_in"]
+        qk.rmsnorm_q8_1(self.x["x_attn_in"], self.g["attn"], NORM_EPS, codes=c, scales=s, **kw)
+        self.launch(g["qkv"], copy, fused=False, **kw)
+        self.launch(g["attn_out"], copy, fused=True, **kw)
+        c, s = self.q8["x_ffn_in"]
+        qk.rmsnorm_q8_1(self.y["attn_out"], self.g["ffn"], NORM_EPS, codes=c, scales=s, **kw)
+        self.launch(g["gate_up"], copy, fused=False, **kw)
+        c, s = self.q8["x_ffn_mid"]
+        qk.swiglu_q8_1(self.y["gate_up"], g["gate_up"][2] // 2, codes=c, scales=s, **kw)
+        self.launch(g["down"], copy, fused=False, **kw)
+
     def kernel_key(self, gemm, fused: bool) -> str:
         q = gemm[1]
         if self.cfg["kind"] == "mmq":
@@ -216,6 +254,8 @@ class Workload:
         return ("gemv_q4k" if q == "q4k" else "gemv_q6k") + ("_f32" if fused else "")
 
     def launches_per_step(self, front_end: str = "auto") -> int:
+        if self.cfg["kind"] == "chain":
+            return 3 + len(self.cfg["gemms"])         # two RMSNorm and one SwiGLU producer
         slots_q = {g[5] for g in self.cfg["gemms"] if not gemm_fused(front_end, self.cfg, g)}
         return len(slots_q) + len(self.cfg["gemms"])
 
@@ -320,10 +360,47 @@ def sample_rows(N: int, n_frac: float) -> int:
     return max(1, min(N, int(round(N * n_frac))))
 
 
-def oracle_step(cfg, host_w, host_x, host_r, threads: int, m_rows=None, n_frac: float = 1.0):
+def chain_norm_weights(cfg, seed: int = 0):
+    K = cfg["gemms"][0][3]
+    return {t: synth.norm_weight(K, seed=seed, tag=t) for t in ("attn", "ffn")}
+
+
+def oracle_chain_step(cfg, host_w, host_x, host_r, host_g, threads: int, n_frac: float = 1.0):
+    """The decode chain with its producers on the CPU oracle (RMSNorm, q8_1, contraction, SwiGLU),
+    each contraction on its first n_frac of output rows (the rest of its output left zero)."""
+    import oracle
+    gm = {g[0]: g for g in cfg["gemms"]}
+    M = cfg["M"]
+    units = 0
+
+    def gemm(name, x32, residual):
+        nonlocal units
+        _, q, N, K, _, _ = gm[name]
+        c, d, _ = oracle.quantize_q8_1(x32)
+        n1 = sample_rows(N, n_frac)
+        y, _ = oracle.gemm(oracle.Q4_K if q == "q4k" else oracle.Q6_K, host_w[name], N, K, c, d,
+                           residual=residual, rows=(0, n1), threads=threads)
+        out = np.zeros((M, N), np.float32)
+        out[:, :n1] = y
+        units += n1 * (K // 256) * BYTES_PER_SB[q]
+        return out
+
+    y1, _ = oracle.rmsnorm(host_x["x_attn_in"], host_g["attn"], NORM_EPS)
+    gemm("qkv", y1.astype(np.float32), None)
+    h = gemm("attn_out", host_x["x_attn_out"], host_r["attn_out"])
+    y2, _ = oracle.rmsnorm(h, host_g["ffn"], NORM_EPS)
+    gu = gemm("gate_up", y2.astype(np.float32), None)
+    mid = oracle.swiglu(gu, gm["gate_up"][2] // 2).astype(np.float32)
+    gemm("down", mid, h)
+    return units
+
+
+def oracle_step(cfg, host_w, host_x, host_r, threads: int, m_rows=None, n_frac: float = 1.0, host_g=None):
     """One step of the workload on the CPU oracle (quantize + every contraction).
     m_rows limits the activation rows and n_frac the output rows of every contraction
     (bounded samples); returns the units (weight bytes or int ops) the sample covers."""
+    if cfg["kind"] == "chain":
+        return oracle_chain_step(cfg, host_w, host_x, host_r, host_g, threads, n_frac)
     import oracle
     q8 = {}
     for s, x in host_x.items():
@@ -344,7 +421,7 @@ def oracle_step(cfg, host_w, host_x, host_r, threads: int, m_rows=None, n_frac: 
     return ops if cfg["kind"] == "mmq" else wbytes
 
 
-def cpu_baseline(wl_host, cfg, budget_s: float = 12.0):
+def cpu_baseline(wl_host, cfg, budget_s: float = 12.0, host_g=None):
     """Time the oracle as it stands on the host cores; bounded sample."""
     threads = os.cpu_count() or 1
     host_w, host_x, host_r = wl_host
@@ -355,12 +432,13 @@ def cpu_baseline(wl_host, cfg, budget_s: float = 12.0):
     else:
         m_rows = None
         unit, scale = "GB/s", 1e9
-        sample = "the full step (quantize + every contraction) per sample"
+        sample = ("the full step (quantize + every contraction" +
+                  (", RMSNorm and SwiGLU" if cfg["kind"] == "chain" else "") + ") per sample")
     t0 = time.perf_counter()
     n = 0
     done = 0
     while True:
-        done += oracle_step(cfg, host_w, host_x, host_r, threads, m_rows)
+        done += oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, host_g=host_g)
         n += 1
         if time.perf_counter() - t0 >= budget_s or n >= 100000:
             break
@@ -380,22 +458,23 @@ def run_reference(args, ws, rank):
         return
     cfg = CONFIGS[args.config]
     host_w = {name: synth.weights(q, N, K, seed=0, tag=name) for (name, q, N, K, _, _) in cfg["gemms"]}
-    host_x = {s: synth.activations(cfg["M"], K, seed=0, tag=s) for s, K in slots(cfg)}
+    host_x = {s: synth.activations(cfg["M"], K, seed=0, tag=s) for s, K in slots(cfg) if s in cfg.get("inputs", [s])}
     host_r = {name: synth.residual(cfg["M"], N, seed=0, tag=name) for (name, _, N, _, res, _) in cfg["gemms"] if res}
+    host_g = chain_norm_weights(cfg) if cfg["kind"] == "chain" else None
     threads = os.cpu_count() or 1
     m_rows = 8 if cfg["kind"] == "mmq" else None
     # calibrate on a 1/64 slice, then size the per-step slice to the time budget
     t0 = time.perf_counter()
-    oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac=1 / 64)
+    oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac=1 / 64, host_g=host_g)
     t_slice = max(time.perf_counter() - t0, 1e-4)
     per_step = 120.0 / (args.steps + args.warmup)
     n_frac = min(1.0, max(1e-6, per_step / (t_slice * 64)))
     for _ in range(args.warmup):
-        oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac)
+        oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac, host_g=host_g)
     t0 = time.perf_counter()
     units = 0
     for _ in range(args.steps):
-        units += oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac)
+        units += oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac, host_g=host_g)
     dt = time.perf_counter() - t0
     if cfg["kind"] == "mmq":
         value, unit = units / dt / 1e12, "TOPS"
@@ -590,7 +669,8 @@ def run_ours(args, ws, rank, local):
                     "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_s * 1e3},
             "gpu_launches": wl.launches_per_step(front_end) * args.steps}
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline((wl.host_w, wl.host_x, wl.host_r), cfg, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline((wl.host_w, wl.host_x, wl.host_r), cfg, budget_s=args.cpu_seconds,
+                                            host_g=wl.host_g)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -613,7 +693,7 @@ def main():
                          "of at most 4096 values, unfused for larger ones")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100, 5: 100}[args.config]
+        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100, 5: 100, 6: 40000}[args.config]
     args.graph_steps = max(1, min(args.graph_steps, args.steps))
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

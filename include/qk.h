@@ -101,6 +101,52 @@ int qk_q8_1_bytes(int64_t M, int64_t K, size_t *codes_bytes, size_t *scales_byte
 int qk_quantize_q8_1(const float *x, int64_t ldx, int64_t M, int64_t K,
                      int8_t *codes, void *scales, unsigned flags, void *stream);
 
+/* =============================================================== producers
+ * The producers of GEMV / MMQ inputs with the q8_1 pack fused into their
+ * write-out, so that no standalone quantization runs before the next
+ * contraction (leone-cuda "CUDA kernel design": RMSNorm and SwiGLU write
+ * their dense output and its q8_1 blocks in one kernel; minfer "15 . The
+ * CUDA backend" sec. 3.2.5: decode producers fuse an int8 quantize epilogue
+ * so the following MMVQ skips its quantize launch).  The codes and scales
+ * are exactly those qk_quantize_q8_1 gives for the binary32 output the kernel
+ * computes, whether or not that output is also written.
+ *
+ * qk_rmsnorm_q8_1: per row m, s = x[m] (+ r[m], binary32 add),
+ *   y = (s * inv) * g with inv = 1 / sqrtf(sum(s^2) / K + eps), all IEEE
+ *   binary32; the square sum is taken in a fixed order (reruns give the same
+ *   bits), sqrtf is the IEEE square root (leone-cuda: not the approximate
+ *   reciprocal square root).
+ *   x:      device float [M][ldx], 16-byte aligned, ldx % 4 == 0, ldx >= K.
+ *   r:      device float [M][K] or NULL (the residual-stream variant: left +
+ *           right is normalized), 16-byte aligned.
+ *   g:      device float [K], the norm weight, 16-byte aligned.
+ *   eps:    >= 0 and finite.
+ *   h_out:  device float [M][K] or NULL; receives s (with r: the updated
+ *           residual stream x + r).
+ *   y:      device float [M][K] or NULL; receives the normalized row.
+ *   codes, scales: q8_1 of y, laid out as qk_quantize_q8_1's outputs.
+ *   M >= 0 (0 launches nothing), K % 32 == 0.  Outputs are 16-byte aligned
+ *   and overlap neither the inputs nor each other.
+ */
+int qk_rmsnorm_q8_1(const float *x, int64_t ldx, const float *r, const float *g, float eps,
+                    int64_t M, int64_t K, float *h_out, float *y,
+                    int8_t *codes, void *scales, unsigned flags, void *stream);
+
+/*
+ * qk_swiglu_q8_1: per row m, h = silu(gate) * up = (g / (1 + expf(-g))) * u
+ *   in binary32 (expf: the CUDA math library's accurate exponential, IEEE
+ *   division and multiply), gate = gu[m][0 .. F), up = gu[m][F .. 2F): the
+ *   output row of the concatenated gate||up GEMV.
+ *   gu:     device float [M][ldgu], 16-byte aligned, ldgu % 4 == 0,
+ *           ldgu >= 2F.
+ *   h:      device float [M][F] or NULL; receives silu(gate) * up.
+ *   codes, scales: q8_1 of h ([M][F] and [M][F/32]).
+ *   0 <= M <= 65535, F % 32 == 0.  Outputs are 16-byte aligned and overlap
+ *   neither gu nor each other.
+ */
+int qk_swiglu_q8_1(const float *gu, int64_t ldgu, int64_t M, int64_t F, float *h,
+                   int8_t *codes, void *scales, unsigned flags, void *stream);
+
 /* ================================================================== repack
  * Load-time lossless repack of GGUF k-quant weights into the device layout
  * that the GEMV and MMQ kernels stream with aligned 16-byte loads (leone-cuda

@@ -65,6 +65,8 @@ def _load():
             lib.orc_gemm_rows.argtypes = [ctypes.c_int, p, i64, i64, i64, i64, p, p, i64, p, p, p]
             lib.orc_repack_q4k.argtypes = [p, i64, i64, p]
             lib.orc_repack_q6k.argtypes = [p, i64, i64, p]
+            lib.orc_rmsnorm.argtypes = [p, i64, p, p, ctypes.c_double, i64, i64, p, p]
+            lib.orc_swiglu.argtypes = [p, i64, i64, i64, p]
             _lib = lib
     return _lib
 
@@ -174,3 +176,32 @@ def repack(qtype: int, w: np.ndarray, N: int, K: int) -> np.ndarray:
     if fn(_ptr(w), N, K, _ptr(out)) != 0:
         raise ValueError("orc_repack failed")
     return out
+
+
+def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float, r: np.ndarray | None = None):
+    """RMSNorm of x (+ r): returns (y float64 [M][K], s float32 [M][K]) with s = x (+ r) in binary32."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    M, K = x.shape
+    g = np.ascontiguousarray(g, dtype=np.float32).reshape(K)
+    rr = None if r is None else np.ascontiguousarray(r, dtype=np.float32).reshape(M, K)
+    y = np.zeros((M, K), np.float64)
+    s = np.zeros((M, K), np.float32)
+    rc = _load().orc_rmsnorm(_ptr(x), K, None if rr is None else _ptr(rr), _ptr(g), float(eps), M, K, _ptr(s), _ptr(y))
+    if rc != 0:
+        raise ValueError(f"orc_rmsnorm failed ({rc})")
+    return y, s
+
+
+def swiglu(gu: np.ndarray, F: int) -> np.ndarray:
+    """silu(gate) * up of gate||up rows gu [M][>= 2F] -> float64 [M][F]."""
+    gu = np.ascontiguousarray(gu, dtype=np.float32)
+    if gu.ndim == 1:
+        gu = gu[None, :]
+    M, ld = gu.shape
+    h = np.zeros((M, F), np.float64)
+    rc = _load().orc_swiglu(_ptr(gu), ld, M, F, _ptr(h))
+    if rc != 0:
+        raise ValueError(f"orc_swiglu failed ({rc})")
+    return h

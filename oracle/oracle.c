@@ -39,6 +39,14 @@
  *  - orc_gemm_rows:  y[m][n] = sum_k w[n][k] * (d_a * q_a[m][k]) (+ r[m][n]),
  *                    the dequantize-then-dot definition, in binary64, plus
  *                    the per-output tolerance scale sum_k |w * xhat|.
+ *  - orc_rmsnorm:    RMSNorm of a row, s = x (+ r), y = s / sqrt(mean(s^2) +
+ *                    eps) * g (leone-cuda "CUDA kernel design", RMSNorm
+ *                    paragraphs: the residual variant normalizes left +
+ *                    right).  s is the binary32 sum the residual stream holds;
+ *                    the rest is binary64.
+ *  - orc_swiglu:     h = silu(gate) * up = gate / (1 + exp(-gate)) * up, in
+ *                    binary64, gate and up being the two halves of a gate||up
+ *                    row (leone-cuda "CUDA kernel design", SwiGLU paragraph).
  *  - orc_repack_*:   the device weight layout this project defines for its
  *                    GPU kernels (a lossless byte permutation; leone-cuda
  *                    "CUDA kernel design" repacks Q4_K into a code part and a
@@ -358,5 +366,44 @@ int orc_repack_q6k(const uint8_t *gguf, int64_t N, int64_t K, uint8_t *out)
             memcpy(dp + (n * B + b) * 2, blk + 208, 2);
         }
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------ producers */
+
+/* RMSNorm of M rows of K values: s = x (+ r) (binary32 add, as stored in the
+   residual stream), y = s / sqrt(sum(s^2) / K + eps) * g in binary64.  s_out
+   (nullable) receives s. */
+int orc_rmsnorm(const float *x, int64_t ldx, const float *r, const float *g, double eps, int64_t M,
+                int64_t K, float *s_out, double *y)
+{
+    if (M < 0 || K <= 0 || ldx < K || !(eps >= 0.0)) return -1;
+    for (int64_t m = 0; m < M; m++) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; k++) {
+            float sk = x[m * ldx + k];
+            if (r) sk = sk + r[m * K + k];          /* float + float: one binary32 rounding */
+            if (s_out) s_out[m * K + k] = sk;
+            ss += (double)sk * (double)sk;
+        }
+        const double inv = 1.0 / sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; k++) {
+            float sk = x[m * ldx + k];
+            if (r) sk = sk + r[m * K + k];
+            y[m * K + k] = (double)sk * inv * (double)g[k];
+        }
+    }
+    return 0;
+}
+
+/* h[m][f] = silu(gate) * up with gate = gu[m][f], up = gu[m][F + f], binary64 */
+int orc_swiglu(const float *gu, int64_t ld, int64_t M, int64_t F, double *h)
+{
+    if (M < 0 || F <= 0 || ld < 2 * F) return -1;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t f = 0; f < F; f++) {
+            const double gv = gu[m * ld + f], uv = gu[m * ld + F + f];
+            h[m * F + f] = gv / (1.0 + exp(-gv)) * uv;
+        }
     return 0;
 }

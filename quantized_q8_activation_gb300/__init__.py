@@ -10,6 +10,7 @@ Typical use::
     import quantized_q8_activation_gb300 as qk
     w = qk.repack(qk.Q4_K, gguf_bytes_on_device, N, K)      # once, at load
     codes, scales = qk.quantize_q8_1(x)                      # x: float32 [M][K] on cuda
+    codes, scales = qk.rmsnorm_q8_1(x, g, 1e-5)              # or fused into the producer
     y = qk.gemv_q4k(w, codes, scales, N, K, residual=r)      # M <= 8
     y = qk.mmq_q4k(w, codes, scales, N, K)                   # any M
 """
@@ -34,7 +35,8 @@ STATUS = {0: "QK_OK", -1: "QK_E_NULL", -2: "QK_E_SHAPE", -3: "QK_E_ALIGN", -4: "
 # every symbol include/qk.h declares
 EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1", "qk_repacked_bytes",
            "qk_repack", "qk_gemv_q4k", "qk_gemv_q6k", "qk_gemv_q4k_f32", "qk_gemv_q6k_f32",
-           "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_mmq_q6k", "qk_mmq_q4k_noalloc", "qk_error_flags"]
+           "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_mmq_q6k", "qk_mmq_q4k_noalloc", "qk_error_flags",
+           "qk_rmsnorm_q8_1", "qk_swiglu_q8_1"]
 
 _lib = None
 _lock = threading.Lock()
@@ -80,6 +82,8 @@ def lib() -> ctypes.CDLL:
             L.qk_mmq_workspace_bytes.argtypes = [i64, i64, i64, szp]
             L.qk_mmq_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
             L.qk_mmq_q6k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
+            L.qk_rmsnorm_q8_1.argtypes = [p, i64, p, p, ctypes.c_float, i64, i64, p, p, p, p, u, p]
+            L.qk_swiglu_q8_1.argtypes = [p, i64, i64, i64, p, p, p, u, p]
             L.qk_mmq_q4k_noalloc.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
             L.qk_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
             for name in EXPORTS:
@@ -162,6 +166,48 @@ def quantize_q8_1(x: torch.Tensor, codes=None, scales=None, pdl: bool = False, s
     st = lib().qk_quantize_q8_1(x.data_ptr(), x.stride(0) if M > 1 else K, M, K, codes.data_ptr(),
                                 scales.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
     _check(st, "qk_quantize_q8_1")
+    return codes, scales
+
+
+def rmsnorm_q8_1(x: torch.Tensor, g: torch.Tensor, eps: float, r=None, h_out=None, y=None, codes=None,
+                 scales=None, pdl: bool = False, stream=None):
+    """RMSNorm of x (+ r) with weight g, written as q8_1 (and, when y / h_out are given, as f32).
+    Returns (codes, scales)."""
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    if x.dtype != torch.float32 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("x must be a float32 CUDA tensor with unit stride along K")
+    M, K = x.shape
+    _cuda(g, "g")
+    for t, n in ((r, "r"), (h_out, "h_out"), (y, "y")):
+        if t is not None:
+            _cuda(t, n)
+    if codes is None or scales is None:
+        codes, scales = empty_q8_1(M, K, x.device)
+    _cuda(codes, "codes"), _cuda(scales, "scales")
+    st = lib().qk_rmsnorm_q8_1(x.data_ptr(), x.stride(0) if M > 1 else K, _p(r), g.data_ptr(), float(eps), M, K,
+                               _p(h_out), _p(y), codes.data_ptr(), scales.data_ptr(), LAUNCH_PDL if pdl else 0,
+                               _stream(stream))
+    _check(st, "qk_rmsnorm_q8_1")
+    return codes, scales
+
+
+def swiglu_q8_1(gu: torch.Tensor, F: int, h=None, codes=None, scales=None, pdl: bool = False, stream=None):
+    """silu(gate) * up of a gate||up row block gu [M][>= 2F] (gate first), written as q8_1 (and as
+    f32 into h when given).  Returns (codes, scales)."""
+    if gu.dim() == 1:
+        gu = gu.view(1, -1)
+    if gu.dtype != torch.float32 or not gu.is_cuda or gu.stride(1) != 1:
+        raise ValueError("gu must be a float32 CUDA tensor with unit stride along its rows")
+    M = gu.shape[0]
+    if h is not None:
+        _cuda(h, "h")
+    if codes is None or scales is None:
+        codes, scales = empty_q8_1(M, F, gu.device)
+    _cuda(codes, "codes"), _cuda(scales, "scales")
+    st = lib().qk_swiglu_q8_1(gu.data_ptr(), gu.stride(0) if M > 1 else gu.shape[1], M, F, _p(h), codes.data_ptr(),
+                              scales.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
+    _check(st, "qk_swiglu_q8_1")
     return codes, scales
 
 

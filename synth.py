@@ -13,7 +13,7 @@ Distributions (the benchmark definition of the workload):
   Q6_K superblock (210 B): 128 B of low-4-bit codes and 64 B of high-2-bit
       codes (uniform random bits), 16 int8 scales ~ U[-32, 31], f16 d ~
       U(1e-3, 1e-2).
-  activations and residuals: float32 ~ N(0, 1).
+  activations and residuals: float32 ~ N(0, 1); RMSNorm weights 1 + 0.1 N(0, 1).
 Every tensor has its own stream: numpy PCG64 seeded with (seed, tag).
 """
 from __future__ import annotations
@@ -75,6 +75,11 @@ def activations(M: int, K: int, seed: int = 0, tag: str = "x") -> np.ndarray:
 
 def residual(M: int, N: int, seed: int = 0, tag: str = "r") -> np.ndarray:
     return _rng(seed, "res:" + tag).standard_normal((M, N), dtype=np.float32)
+
+
+def norm_weight(K: int, seed: int = 0, tag: str = "g") -> np.ndarray:
+    """RMSNorm weight: float32 1 + 0.1 * N(0, 1) per channel (trained norm weights sit near 1)."""
+    return (1.0 + 0.1 * _rng(seed, "norm:" + tag).standard_normal(K)).astype(np.float32)
 
 
 # ---------------------------------------------------------------- workloads

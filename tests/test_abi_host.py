@@ -155,3 +155,36 @@ def test_mmq_noalloc_rejects_oversize(L):
     assert qk.mmq_workspace_bytes(2048, 3584, 18944) > qk.STATIC_WS_BYTES
     assert f(w, c, s, 2048, 3584, 18944, None, y, 0, None) == -6       # QK_E_WORKSPACE, before any CUDA call
     assert qk.mmq_workspace_bytes(2048, 4608, 3584) <= qk.STATIC_WS_BYTES
+
+
+def test_rmsnorm_q8_1_rejects(L):
+    f = L.qk_rmsnorm_q8_1
+    x, r, g, h, y, c, s = (P + i * 0x10000000 for i in range(7))
+    assert f(x, 256, None, g, 1e-5, 0, 256, None, None, c, s, 0, None) == 0          # M = 0: nothing to do
+    assert f(x, 256, None, g, 1e-5, 1, 100, None, None, c, s, 0, None) == E_SHAPE    # K % 32
+    assert f(x, 128, None, g, 1e-5, 1, 256, None, None, c, s, 0, None) == E_SHAPE    # ldx < K
+    assert f(x, 256, None, g, -1.0, 1, 256, None, None, c, s, 0, None) == E_SHAPE    # eps < 0
+    assert f(x, 256, None, g, float("nan"), 1, 256, None, None, c, s, 0, None) == E_SHAPE
+    assert f(x, 256, None, None, 1e-5, 1, 256, None, None, c, s, 0, None) == E_NULL
+    assert f(x, 256, None, g, 1e-5, 1, 256, None, None, None, s, 0, None) == E_NULL
+    assert f(x + 4, 256, None, g, 1e-5, 1, 256, None, None, c, s, 0, None) == E_ALIGN
+    assert f(x, 256, r + 8, g, 1e-5, 1, 256, None, None, c, s, 0, None) == E_ALIGN
+    assert f(x, 258, None, g, 1e-5, 2, 256, None, None, c, s, 0, None) == E_ALIGN   # ldx % 4
+    assert f(x, 256, None, g, 1e-5, 1, 256, None, x, c, s, 0, None) == E_ALIAS       # y over x
+    assert f(x, 256, r, g, 1e-5, 1, 256, r, None, c, s, 0, None) == E_ALIAS         # h_out over r
+    assert f(x, 256, None, g, 1e-5, 1, 256, None, y, y + 512, s, 0, None) == E_ALIAS  # codes over y
+
+
+def test_swiglu_q8_1_rejects(L):
+    f = L.qk_swiglu_q8_1
+    gu, h, c, s = (P + i * 0x10000000 for i in range(4))
+    assert f(gu, 512, 0, 256, h, c, s, 0, None) == 0                   # M = 0: nothing to do
+    assert f(gu, 512, 1, 100, h, c, s, 0, None) == E_SHAPE             # F % 32
+    assert f(gu, 256, 1, 256, h, c, s, 0, None) == E_SHAPE             # ldgu < 2F
+    assert f(gu, 512, 65536, 256, h, c, s, 0, None) == E_SHAPE         # M beyond the grid's y extent
+    assert f(None, 512, 1, 256, h, c, s, 0, None) == E_NULL
+    assert f(gu, 512, 1, 256, h, None, s, 0, None) == E_NULL
+    assert f(gu + 4, 512, 1, 256, h, c, s, 0, None) == E_ALIGN
+    assert f(gu, 514, 2, 256, h, c, s, 0, None) == E_ALIGN
+    assert f(gu, 512, 1, 256, gu + 1024, c, s, 0, None) == E_ALIAS     # h inside gu
+    assert f(gu, 512, 1, 256, h, h + 512, s, 0, None) == E_ALIAS       # codes inside h
