@@ -63,7 +63,16 @@ extern "C" {
  * (e.g. qk_repack must have completed, or have been followed by another
  * launch, before the first PDL launch that reads its output).  Without the
  * flag every call is ordinary stream-ordered work.
+ *
+ * QK_MMQ_TILE_256 / QK_MMQ_TILE_128 (MMQ only): force output tiles 256 or
+ * 128 weight rows wide.  By default the MMQ picks per call the width whose
+ * waves of tiles over the SMs should finish first, counting a 128-wide tile
+ * as 0.7 of a 256-wide one (in practice: 128 for problems that fit in one
+ * wave, 256 otherwise).  Results are the same within the stated bound either
+ * way; the flags exist for tests and tuning.  Setting both is QK_E_SHAPE.
  */
+#define QK_MMQ_TILE_256 2u
+#define QK_MMQ_TILE_128 4u
 
 /* Library version (major*10000 + minor*100 + patch). */
 int qk_version(void);

@@ -27,6 +27,8 @@ from . import build as _build
 Q4_K = 1
 Q6_K = 2
 LAUNCH_PDL = 1
+MMQ_TILE_256 = 2
+MMQ_TILE_128 = 4
 
 QK_OK = 0
 STATUS = {0: "QK_OK", -1: "QK_E_NULL", -2: "QK_E_SHAPE", -3: "QK_E_ALIGN", -4: "QK_E_ALIAS",
@@ -279,17 +281,18 @@ def gemv_q6k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=N
                      pdl, stream)
 
 
-def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None):
-    """Prefill contraction over a repacked Q4_K weight, any M."""
-    return _mmq("qk_mmq_q4k", w, codes, scales, N, K, residual, y, workspace, pdl, stream)
+def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None, tile=None):
+    """Prefill contraction over a repacked Q4_K weight, any M.  tile: None (the library picks
+    the tile width), 256 or 128."""
+    return _mmq("qk_mmq_q4k", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile)
 
 
-def mmq_q6k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None):
+def mmq_q6k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None, tile=None):
     """Prefill contraction over a repacked Q6_K weight, any M."""
-    return _mmq("qk_mmq_q6k", w, codes, scales, N, K, residual, y, workspace, pdl, stream)
+    return _mmq("qk_mmq_q6k", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile)
 
 
-def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream):
+def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile=None):
     M = codes.shape[0]
     for t, n in ((w, "w"), (codes, "codes"), (scales, "scales")):
         _cuda(t, n)
@@ -299,8 +302,9 @@ def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream):
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=codes.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    flags = (LAUNCH_PDL if pdl else 0) | {None: 0, 256: MMQ_TILE_256, 128: MMQ_TILE_128}[tile]
     st = getattr(lib(), fn)(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
-                            _p(workspace), wsb, LAUNCH_PDL if pdl else 0, _stream(stream))
+                            _p(workspace), wsb, flags, _stream(stream))
     _check(st, fn)
     return y
 

@@ -82,25 +82,13 @@ namespace {
 
 using namespace qk::tc;
 
-constexpr int BM = 128, BN = 256, BK = 32;      // BK: one Q4_K / Q6_K 32-value sub-block
+constexpr int BM = 128, BK = 32;                // BK: one Q4_K / Q6_K 32-value sub-block
 constexpr int NST = QK_MMQ_NST, NRAW = QK_MMQ_RAW, NSB = QK_MMQ_SBRAW;
-constexpr int kThreads = 768;
-constexpr int kEpiWarp0 = 4, kEpiWarps = 4, kConvWarp0 = 8;  // epilogue warps 4-7, converters 8-23
-constexpr int kConv = 512, kConvWarps = kConv / 32;   // two converter threads per weight row
-static_assert(kConv == 2 * BN && kConvWarp0 * 32 + kConv == kThreads, "two converter threads per weight row");
+constexpr int kEpiWarp0 = 4, kEpiWarps = 4, kConvWarp0 = 8;  // epilogue warps 4-7, converters from warp 8
 constexpr float kWScale = 256.0f, kWUnscale = 1.0f / 256.0f;
 
 constexpr int ATILE = BM * BK * 2;              // 8 KB: 128 rows x 32 f16 (64 B rows), SWIZZLE_64B K-major
-constexpr int WTILE = BN * BK * 2;              // 16 KB: 256 rows x 32 f16
-constexpr int STAGE = 2 * ATILE + 2 * WTILE;    // A_hi | A_lo | W_hi | W_lo
 constexpr int ABLOCK = 2 * ATILE;               // workspace block of one M-tile and K stage: A_hi | A_lo
-// raw unit of the Q4_K ring, one superblock's code bytes: first halves of its 4 groups 256 x 64 B |
-// second halves 256 x 64 B
-constexpr int RAW_H0 = 0, RAW_H1 = BN * 64, RAW_Q4 = 2 * BN * 64;
-// raw unit of the Q6_K ring, half a superblock: ql first-chunk run 256 x 32 B | ql second-chunk run
-// 256 x 32 B | qh 256 x 32 B
-constexpr int RAW_QL0 = 0, RAW_QL1 = BN * 32, RAW_QH = 2 * BN * 32, RAW_Q6 = 3 * BN * 32;
-constexpr int SBR = BN * 16;                    // per-superblock records (Q4_K metadata, Q6_K scales)
 constexpr int EPI_LD = 17;                      // epilogue transpose buffer: 32 rows x 16 columns, padded
 enum {
     B_FULL = 0,
@@ -114,10 +102,25 @@ enum {
     B_DONE = B_ACCEMPTY + 2,       // every MMA of the CTA has completed
     NBAR = B_DONE + 1
 };
-// shared-memory plan of mmq_kernel<QT>
-template <int QT>
+// Tile width and shared-memory plan of mmq_kernel<QT, BN>: output tiles of 128 x BN (BN = 256, or
+// 128 where 256-wide tiles leave a costly partial last wave on the SMs), two converter threads per
+// weight row.
+template <int QT, int BN_>
 struct Plan {
+    static constexpr int BN = BN_;
     static constexpr bool Q6 = QT == QK_TYPE_Q6_K;
+    static constexpr int kConv = 2 * BN, kConvWarps = kConv / 32, kThreads = kConvWarp0 * 32 + kConv;
+    static constexpr int WTILE = BN * BK * 2;              // BN rows x 32 f16
+    static constexpr int STAGE = 2 * ATILE + 2 * WTILE;    // A_hi | A_lo | W_hi | W_lo
+    // raw unit of the Q4_K ring, one superblock's code bytes: first halves of its 4 groups BN x 64 B |
+    // second halves BN x 64 B
+    static constexpr int RAW_H0 = 0, RAW_H1 = BN * 64, RAW_Q4 = 2 * BN * 64;
+    // raw unit of the Q6_K ring, half a superblock: ql first-chunk run BN x 32 B | ql second-chunk run
+    // BN x 32 B | qh BN x 32 B
+    static constexpr int RAW_QL0 = 0, RAW_QL1 = BN * 32, RAW_QH = 2 * BN * 32, RAW_Q6 = 3 * BN * 32;
+    static constexpr int SBR = BN * 16;                    // per-superblock records (Q4_K metadata, Q6_K scales)
+    static constexpr uint32_t TMEM_COLS = 2 * BN;          // two accumulators: one accumulates while one drains
+    static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
     static constexpr int RAW = Q6 ? RAW_Q6 : RAW_Q4;
     static constexpr int OFF_RAW = NST * STAGE;
     static constexpr int OFF_SBR = OFF_RAW + NRAW * RAW;
@@ -129,8 +132,6 @@ struct Plan {
     static_assert(STAGE % 1024 == 0 && OFF_RAW % 1024 == 0 && RAW % 1024 == 0 && SBR % 1024 == 0,
                   "copy destinations and swizzle atoms stay aligned");
 };
-constexpr uint32_t TMEM_COLS = 2 * BN;           // two accumulators: tile k+1 accumulates while tile k drains
-constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 
 // byte offset of 16-byte chunk c (< 4) of row r in a SWIZZLE_64B K-major tile (rows of 64 bytes)
 __host__ __device__ constexpr uint32_t sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
@@ -261,21 +262,22 @@ struct ConvState {
 // stage is signalled full
 // it: K stage within the tile; gs / gsb: the stage and superblock counted over all tiles of
 // this CTA (ring slots and barrier phases)
+template <class L>
 __device__ __forceinline__ void convert_stage_q4(uint8_t *smem, uint64_t *bar, ConvState &cs,
                                                  int it, int gs, int gsb, int row, int h, int st)
 {
-    using L = Plan<QK_TYPE_Q4_K>;
     const int j = it & 7, g = j >> 1, nib = j & 1;
     const int rs = gsb % NRAW, ss = gsb % NSB;
     if (j == 0) {
         wait_bar(&bar[B_SFULL + ss], (gsb / NSB) & 1);
-        cs.mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * SBR + row * 16);
+        cs.mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * L::SBR + row * 16);
         wait_bar(&bar[B_RFULL + rs], (gsb / NRAW) & 1);
     }
     if (nib == 0)
-        cs.c = *reinterpret_cast<const uint4 *>(smem + L::OFF_RAW + rs * L::RAW + (h ? RAW_H1 : RAW_H0) + row * 64 + 16 * g);
+        cs.c = *reinterpret_cast<const uint4 *>(smem + L::OFF_RAW + rs * L::RAW + (h ? L::RAW_H1 : L::RAW_H0) + row * 64 +
+                                                16 * g);
     if (gs >= NST) wait_bar(&bar[B_EMPTY + st], ((gs / NST) + 1) & 1);
-    uint8_t *s0 = smem + st * STAGE;
+    uint8_t *s0 = smem + st * L::STAGE;
     // this group's record: sc0 | sc1<<6 | m0<<12 | m1<<18 (sub-blocks 2g and 2g+1)
     const uint4 mt = cs.mt;
     const uint32_t rec = __byte_perm(__byte_perm(mt.y, mt.z, g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u), mt.w,
@@ -295,7 +297,7 @@ __device__ __forceinline__ void convert_stage_q4(uint8_t *smem, uint64_t *bar, C
         conv_w(x0, dsc2, ndmm2, hi[0], hi[1], lo[0], lo[1]);
         conv_w(x1, dsc2, ndmm2, hi[2], hi[3], lo[2], lo[3]);
         sts128(s0 + 2 * ATILE, sw64(row, 2 * h + cc), hi[0], hi[1], hi[2], hi[3]);
-        sts128(s0 + 2 * ATILE + WTILE, sw64(row, 2 * h + cc), lo[0], lo[1], lo[2], lo[3]);
+        sts128(s0 + 2 * ATILE + L::WTILE, sw64(row, 2 * h + cc), lo[0], lo[1], lo[2], lo[3]);
     }
     // Each lane makes its own stores visible to the tensor core (async proxy); after the warp
     // has synchronised, one lane arrives for the whole warp.
@@ -312,6 +314,7 @@ __device__ __forceinline__ void convert_stage_q4(uint8_t *smem, uint64_t *bar, C
 }
 
 // Q6_K: the d of superblock sb of tile t for this converter's weight row (0 past the last row)
+template <int BN>
 __device__ __forceinline__ uint32_t q6_d(const MmqArgs &a, int t, int sb, int row)
 {
     const int64_t n = (int64_t)(t / a.mtiles) * BN + row;
@@ -326,31 +329,31 @@ __device__ __forceinline__ uint32_t q6_d(const MmqArgs &a, int t, int sb, int ro
 // nibble, the qh bits 2q, 2q+1, and scale byte 4 (2 hs + h) + q of the record.  Stored as
 // (W_hi, W_lo) chunks 2h and 2h+1, then the stage is signalled full.
 // gsb: superblock counted over all tiles of this CTA; t: the tile (for the d prefetch)
+template <class L>
 __device__ __forceinline__ void convert_stage_q6(uint8_t *smem, uint64_t *bar, ConvState &cs, const MmqArgs &a,
                                                  int t, int it, int gs, int gsb, int row, int h, int st)
 {
-    using L = Plan<QK_TYPE_Q6_K>;
     const int j = it & 7, hs = j >> 2, q = j & 3;
     const int gu = 2 * gsb + hs;                              // raw unit: half superblock
     const int rs = gu % NRAW, ss = gsb % NSB;
     if (j == 0) {
         wait_bar(&bar[B_SFULL + ss], (gsb / NSB) & 1);
-        cs.mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * SBR + row * 16);
+        cs.mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * L::SBR + row * 16);
         // this superblock's d was requested one superblock ago; request the next one's
         const int B = (int)(a.K >> 8), sb = it >> 3;
         cs.d = cs.dn;
-        if (sb + 1 < B) cs.dn = q6_d(a, t, sb + 1, row);
-        else if (t + (int)gridDim.x < a.mtiles * a.ntiles) cs.dn = q6_d(a, t + gridDim.x, 0, row);
+        if (sb + 1 < B) cs.dn = q6_d<L::BN>(a, t, sb + 1, row);
+        else if (t + (int)gridDim.x < a.mtiles * a.ntiles) cs.dn = q6_d<L::BN>(a, t + gridDim.x, 0, row);
     }
     if (q == 0) {
         wait_bar(&bar[B_RFULL + rs], (gu / NRAW) & 1);
         const uint8_t *r0 = smem + L::OFF_RAW + rs * L::RAW + row * 32 + 16 * h;
-        cs.c = *reinterpret_cast<const uint4 *>(r0 + RAW_QL0);
-        cs.c2 = *reinterpret_cast<const uint4 *>(r0 + RAW_QL1);
-        cs.qh = *reinterpret_cast<const uint4 *>(r0 + RAW_QH);
+        cs.c = *reinterpret_cast<const uint4 *>(r0 + L::RAW_QL0);
+        cs.c2 = *reinterpret_cast<const uint4 *>(r0 + L::RAW_QL1);
+        cs.qh = *reinterpret_cast<const uint4 *>(r0 + L::RAW_QH);
     }
     if (gs >= NST) wait_bar(&bar[B_EMPTY + st], ((gs / NST) + 1) & 1);
-    uint8_t *s0 = smem + st * STAGE;
+    uint8_t *s0 = smem + st * L::STAGE;
     const int p = 2 * hs + h;                                 // record bytes 4p .. 4p+3: quarters 0..3
     const uint32_t scw = p == 0 ? cs.mt.x : p == 1 ? cs.mt.y : p == 2 ? cs.mt.z : cs.mt.w;
     const int sc = (int)(int8_t)(scw >> (8 * q));
@@ -369,7 +372,7 @@ __device__ __forceinline__ void convert_stage_q6(uint8_t *smem, uint64_t *bar, C
         conv_w(x0, dsc2, ndmm2, hi[0], hi[1], lo[0], lo[1]);
         conv_w(x1, dsc2, ndmm2, hi[2], hi[3], lo[2], lo[3]);
         sts128(s0 + 2 * ATILE, sw64(row, 2 * h + cc), hi[0], hi[1], hi[2], hi[3]);
-        sts128(s0 + 2 * ATILE + WTILE, sw64(row, 2 * h + cc), lo[0], lo[1], lo[2], lo[3]);
+        sts128(s0 + 2 * ATILE + L::WTILE, sw64(row, 2 * h + cc), lo[0], lo[1], lo[2], lo[3]);
     }
     // as for Q4_K: the stores are made visible to the async proxy, and a ring slot is released only
     // after every value loaded from it has been used by the arithmetic (the second ql chunk is
@@ -383,10 +386,12 @@ __device__ __forceinline__ void convert_stage_q6(uint8_t *smem, uint64_t *bar, C
     }
 }
 
-template <int QT>
-__global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
+template <int QT, int BN_>
+__global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
+    mmq_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
 {
-    using L = Plan<QT>;
+    using L = Plan<QT, BN_>;
+    constexpr int BN = L::BN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
@@ -400,15 +405,15 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const
     qk::pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; i++)
-            mbar_init(&bar[B_FULL + i], kConvWarps + 1), mbar_init(&bar[B_EMPTY + i], 1);
-        for (int i = 0; i < NRAW; i++) mbar_init(&bar[B_RFULL + i], 1), mbar_init(&bar[B_REMPTY + i], kConvWarps);
-        for (int i = 0; i < NSB; i++) mbar_init(&bar[B_SFULL + i], 1), mbar_init(&bar[B_SEMPTY + i], kConvWarps);
+            mbar_init(&bar[B_FULL + i], L::kConvWarps + 1), mbar_init(&bar[B_EMPTY + i], 1);
+        for (int i = 0; i < NRAW; i++) mbar_init(&bar[B_RFULL + i], 1), mbar_init(&bar[B_REMPTY + i], L::kConvWarps);
+        for (int i = 0; i < NSB; i++) mbar_init(&bar[B_SFULL + i], 1), mbar_init(&bar[B_SEMPTY + i], L::kConvWarps);
         for (int i = 0; i < 2; i++) mbar_init(&bar[B_ACCFULL + i], 1), mbar_init(&bar[B_ACCEMPTY + i], kEpiWarps);
         mbar_init(&bar[B_DONE], 1);
         mbar_init_fence();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_ptr, TMEM_COLS);
+        tmem_alloc(tmem_ptr, L::TMEM_COLS);
         tmem_relinquish();
     }
     fence_before_sync();
@@ -431,16 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const
                     const int gs = kt * nit + it, st = gs % NST;
                     wait_bar(&bar[B_FULL + st], (gs / NST) & 1);
                     fence_after_sync();
-                    const uint32_t s0 = sbase + st * STAGE;
+                    const uint32_t s0 = sbase + st * L::STAGE;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; kk++) {
                         const uint64_t ahi = smem_desc(s0 + 32 * kk, 16, 512, kLayoutSw64);
                         const uint64_t alo = smem_desc(s0 + ATILE + 32 * kk, 16, 512, kLayoutSw64);
                         const uint64_t whi = smem_desc(s0 + 2 * ATILE + 32 * kk, 16, 512, kLayoutSw64);
-                        const uint64_t wlo = smem_desc(s0 + 2 * ATILE + WTILE + 32 * kk, 16, 512, kLayoutSw64);
-                        mma_f16(dacc, ahi, whi, IDESC, (it | kk) != 0);
-                        mma_f16(dacc, ahi, wlo, IDESC, 1);
-                        mma_f16(dacc, alo, whi, IDESC, 1);
+                        const uint64_t wlo = smem_desc(s0 + 2 * ATILE + L::WTILE + 32 * kk, 16, 512, kLayoutSw64);
+                        mma_f16(dacc, ahi, whi, L::IDESC, (it | kk) != 0);
+                        mma_f16(dacc, ahi, wlo, L::IDESC, 1);
+                        mma_f16(dacc, alo, whi, L::IDESC, 1);
                     }
                     mma_commit(&bar[B_EMPTY + st]);
                 }
@@ -463,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const
                     const int gs = kt * nit + it, st = gs % NST;
                     if (gs >= NST) wait_bar(&bar[B_EMPTY + st], ((gs / NST) + 1) & 1);
                     mbar_arrive_expect_tx(&bar[B_FULL + st], ABLOCK);
-                    bulk_copy_g2s(smem + st * STAGE, srcA + (size_t)it * ABLOCK, ABLOCK, &bar[B_FULL + st]);
+                    bulk_copy_g2s(smem + st * L::STAGE, srcA + (size_t)it * ABLOCK, ABLOCK, &bar[B_FULL + st]);
                 }
             }
         }
@@ -480,8 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const
                 for (int sb = 0; sb < B; sb++, gsb++) {
                     const int ss = gsb % NSB;
                     if (gsb >= NSB) wait_bar(&bar[B_SEMPTY + ss], ((gsb / NSB) + 1) & 1);
-                    mbar_arrive_expect_tx(&bar[B_SFULL + ss], SBR);
-                    tma_load_2d(smem + L::OFF_SBR + ss * SBR, &maps.meta, 16 * sb, n0, &bar[B_SFULL + ss]);
+                    mbar_arrive_expect_tx(&bar[B_SFULL + ss], L::SBR);
+                    tma_load_2d(smem + L::OFF_SBR + ss * L::SBR, &maps.meta, 16 * sb, n0, &bar[B_SFULL + ss]);
                     // the superblock's lanes u = 4 (sb - 8 s) .. +3 of its step s: first 16-byte chunks at 16u,
                     // second chunks at 16 G + 16u
                     const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s);
@@ -490,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const
                         if (gu >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((gu / NRAW) + 1) & 1);
                         uint8_t *d = smem + L::OFF_RAW + rs * L::RAW;
                         mbar_arrive_expect_tx(&bar[B_RFULL + rs], L::RAW);
-                        tma_load_2d(d + RAW_H0, &maps.wcodes, 1024 * s + 16 * u, n0, &bar[B_RFULL + rs]);
-                        tma_load_2d(d + RAW_H1, &maps.wcodes, 1024 * s + 16 * G + 16 * u, n0, &bar[B_RFULL + rs]);
+                        tma_load_2d(d + L::RAW_H0, &maps.wcodes, 1024 * s + 16 * u, n0, &bar[B_RFULL + rs]);
+                        tma_load_2d(d + L::RAW_H1, &maps.wcodes, 1024 * s + 16 * G + 16 * u, n0, &bar[B_RFULL + rs]);
                         gu++;
                     } else {
                         // two raw units: superblock half hs holds lanes u + 2hs, u + 2hs + 1 of each ql run
@@ -501,10 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const
                             if (gu >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((gu / NRAW) + 1) & 1);
                             uint8_t *d = smem + L::OFF_RAW + rs * L::RAW;
                             mbar_arrive_expect_tx(&bar[B_RFULL + rs], L::RAW);
-                            tma_load_2d(d + RAW_QL0, &maps.wcodes, 1024 * s + 16 * u + 32 * hs, n0, &bar[B_RFULL + rs]);
-                            tma_load_2d(d + RAW_QL1, &maps.wcodes, 1024 * s + 16 * G + 16 * u + 32 * hs, n0,
+                            tma_load_2d(d + L::RAW_QL0, &maps.wcodes, 1024 * s + 16 * u + 32 * hs, n0, &bar[B_RFULL + rs]);
+                            tma_load_2d(d + L::RAW_QL1, &maps.wcodes, 1024 * s + 16 * G + 16 * u + 32 * hs, n0,
                                         &bar[B_RFULL + rs]);
-                            tma_load_2d(d + RAW_QH, &maps.qh, 64 * sb + 32 * hs, n0, &bar[B_RFULL + rs]);
+                            tma_load_2d(d + L::RAW_QH, &maps.qh, 64 * sb + 32 * hs, n0, &bar[B_RFULL + rs]);
                         }
                     }
                 }
@@ -566,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const
         ConvState cs;
         cs.c = cs.mt = cs.c2 = cs.qh = make_uint4(0, 0, 0, 0);
         cs.d = 0;
-        cs.dn = L::Q6 ? q6_d(a, blockIdx.x, 0, row) : 0u;
+        cs.dn = L::Q6 ? q6_d<BN>(a, blockIdx.x, 0, row) : 0u;
         int kt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
             const int gs0 = kt * nit;
@@ -574,8 +579,8 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const
             static_assert(NST == 3, "the slot prologue below handles three stages");
             int it = 0;
             auto conv = [&](int itk, int gs, int st) {
-                if constexpr (L::Q6) convert_stage_q6(smem, bar, cs, a, t, itk, gs, kt * B + (itk >> 3), row, h, st);
-                else convert_stage_q4(smem, bar, cs, itk, gs, kt * B + (itk >> 3), row, h, st);
+                if constexpr (L::Q6) convert_stage_q6<L>(smem, bar, cs, a, t, itk, gs, kt * B + (itk >> 3), row, h, st);
+                else convert_stage_q4<L>(smem, bar, cs, itk, gs, kt * B + (itk >> 3), row, h, st);
             };
             while (it < nit && (gs0 + it) % NST != 0) {
                 const int gs = gs0 + it;
@@ -595,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) mmq_kernel(const MmqArgs a, const
     __syncthreads();
     if (warp == 0) {
         fence_after_sync();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc(tmem, L::TMEM_COLS);
     }
 }
 
@@ -640,17 +645,38 @@ size_t ws_bytes(int64_t M, int64_t K)
     return mt * (size_t)(K / BK) * ABLOCK;
 }
 
-template <int QT>
+template <int QT, int BN>
 int set_attrs()
 {
     static std::atomic<int> done{0};
     if (done.load()) return QK_OK;
-    if (cudaFuncSetAttribute(mmq_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan<QT>::SMEM) !=
-            cudaSuccess ||
-        qk::max_carveout(mmq_kernel<QT>) != cudaSuccess)
+    if (cudaFuncSetAttribute(mmq_kernel<QT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Plan<QT, BN>::SMEM) != cudaSuccess ||
+        qk::max_carveout(mmq_kernel<QT, BN>) != cudaSuccess)
         return QK_E_CUDA;
     done.store(1);
     return QK_OK;
+}
+
+// Tile width for an M x N problem on `sms` SMs.  A CTA takes ceil(tiles / sms) tiles one after the
+// other.  A 128-wide tile takes about 0.7 of a 256-wide one (measured on the prefill shapes: the
+// activation operand, the MMA issue and the epilogue do not halve with the tile), so 128 is taken
+// only where ceil(tiles_128 / sms) * 0.7 < ceil(tiles_256 / sms): in practice single-wave problems.
+int pick_bn(int64_t M, int64_t N, int sms)
+{
+    const int64_t gx = (M + BM - 1) / BM;
+    const int64_t w256 = (gx * ((N + 255) / 256) + sms - 1) / sms, w128 = (gx * ((N + 127) / 128) + sms - 1) / sms;
+    return w128 * 7 < w256 * 10 ? 128 : 256;
+}
+
+template <int QT, int BN>
+int launch_mmq(const MmqArgs &args, const MmqMaps &maps, int64_t tiles, cudaStream_t stream)
+{
+    const int st = set_attrs<QT, BN>();
+    if (st != QK_OK) return st;
+    const int64_t grid = tiles < qk::sm_count() ? tiles : qk::sm_count();
+    return qk::launch(mmq_kernel<QT, BN>, dim3((unsigned)grid), dim3(Plan<QT, BN>::kThreads), Plan<QT, BN>::SMEM,
+                      stream, true, args, maps);
 }
 
 int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N, int64_t K,
@@ -675,11 +701,13 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
         qk::overlaps(workspace, need, scales, sbytes) || qk::overlaps(workspace, need, y, ybytes) ||
         (residual && qk::overlaps(workspace, need, residual, ybytes)))
         return QK_E_ALIAS;
+    if ((flags & QK_MMQ_TILE_256) && (flags & QK_MMQ_TILE_128)) return QK_E_SHAPE;
+    const int BN = (flags & QK_MMQ_TILE_256) ? 256 : (flags & QK_MMQ_TILE_128) ? 128 : pick_bn(M, N, qk::sm_count());
     const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
     if (gx > 65535 || gy > 65535 || gx * gy > 0x7fffffffLL) return QK_E_SHAPE;
     const bool q6 = qt == QK_TYPE_Q6_K;
-    const size_t smem = q6 ? (size_t)Plan<QK_TYPE_Q6_K>::SMEM : (size_t)Plan<QK_TYPE_Q4_K>::SMEM;
-    if (smem > qk::max_smem_optin()) return QK_E_CUDA;
+    const size_t smem = q6 ? (size_t)Plan<QK_TYPE_Q6_K, 256>::SMEM : (size_t)Plan<QK_TYPE_Q4_K, 256>::SMEM;
+    if (smem > qk::max_smem_optin()) return QK_E_CUDA;     // the larger plan of each weight type
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return QK_E_CUDA;
     const int64_t B = K / 256;
@@ -687,28 +715,29 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
     MmqMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (!q6) {
-        if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 64, BN) ||
-            !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 16, N, B * 16, 16, BN))
+        if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 64, (uint32_t)BN) ||
+            !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 16, N, B * 16, 16,
+                      (uint32_t)BN))
             return QK_E_CUDA;
     } else {
-        if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 32, BN) ||
-            !make_map(enc, &maps.qh, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 64, N, B * 64, 32, BN) ||
-            !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 192, B * 16, N, B * 16, 16, BN))
+        if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 32, (uint32_t)BN) ||
+            !make_map(enc, &maps.qh, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 64, N, B * 64, 32,
+                      (uint32_t)BN) ||
+            !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 192, B * 16, N, B * 16, 16,
+                      (uint32_t)BN))
             return QK_E_CUDA;
     }
-    const int st0 = q6 ? set_attrs<QK_TYPE_Q6_K>() : set_attrs<QK_TYPE_Q4_K>();
-    if (st0 != QK_OK) return st0;
     uint8_t *wsA = static_cast<uint8_t *>(workspace);
     int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, (cudaStream_t)stream,
                         (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA);
     if (st != QK_OK) return st;
     MmqArgs args{wsA, q6 ? reinterpret_cast<const uint16_t *>(wb + N * B * 208) : nullptr, M, N, K, residual, y,
                  (int)gx, (int)gy};
-    const int64_t tiles = gx * gy, grid = tiles < qk::sm_count() ? tiles : qk::sm_count();
-    return q6 ? qk::launch(mmq_kernel<QK_TYPE_Q6_K>, dim3((unsigned)grid), dim3(kThreads), smem, (cudaStream_t)stream,
-                           true, args, maps)
-              : qk::launch(mmq_kernel<QK_TYPE_Q4_K>, dim3((unsigned)grid), dim3(kThreads), smem, (cudaStream_t)stream,
-                           true, args, maps);
+    const int64_t tiles = gx * gy;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (q6) return BN == 128 ? launch_mmq<QK_TYPE_Q6_K, 128>(args, maps, tiles, cs)
+                             : launch_mmq<QK_TYPE_Q6_K, 256>(args, maps, tiles, cs);
+    return BN == 128 ? launch_mmq<QK_TYPE_Q4_K, 128>(args, maps, tiles, cs) : launch_mmq<QK_TYPE_Q4_K, 256>(args, maps, tiles, cs);
 }
 
 }  // namespace

@@ -139,6 +139,7 @@ def test_mmq_rejects(L, fn):
     assert f(w, c, s, 16, 64, 256, None, y, ws, need - 16, 0, None) == -6         # QK_E_WORKSPACE
     assert f(w, c, s, 16, 64, 256, None, c, ws, need, 0, None) == E_ALIAS
     assert f(w, c, s, 16, 64, 256, None, y, y, need, 0, None) == E_ALIAS           # workspace over y
+    assert f(w, c, s, 16, 64, 256, None, y, ws, need, 6, None) == E_SHAPE          # both tile widths forced
 
 
 def test_binding_refuses_cpu_tensors():

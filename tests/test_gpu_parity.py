@@ -288,17 +288,34 @@ def mmq_fn(qt):
     return qk.mmq_q4k if qt == "q4k" else qk.mmq_q6k
 
 
+@pytest.mark.parametrize("tile", [None, 256, 128])
 @pytest.mark.parametrize("qt", ["q4k", "q6k"])
 @pytest.mark.parametrize("M,N,K", [(1, 64, 256), (17, 130, 512), (64, 128, 2304), (130, 300, 4096),
                                    (200, 77, 768), (65, 129, 256 * 9)])
-def test_mmq_parity(qt, M, N, K):
+def test_mmq_parity(qt, M, N, K, tile):
     w, wr = weights(qt, N, K, seed=M * 3 + N + K)
     x = synth.activations(M, K, seed=M)
     codes, scales = q8(x)
     c, d = q8_host(codes, scales)
-    y = mmq_fn(qt)(wr, codes, scales, N, K).cpu().numpy()
+    y = mmq_fn(qt)(wr, codes, scales, N, K, tile=tile).cpu().numpy()
     y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
-    check(y, y_ref, ab, what=f"mmq {qt} M={M} N={N} K={K}")
+    check(y, y_ref, ab, what=f"mmq {qt} M={M} N={N} K={K} tile={tile}")
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+def test_mmq_tile_widths_agree_and_many_tiles_per_cta(qt):
+    """More tiles than SMs at both widths (each CTA walks several tiles and both accumulators);
+    the two widths agree to the bound."""
+    M, N, K = 300, 128 * 160, 256
+    w, wr = weights(qt, N, K, seed=77)
+    x = synth.activations(M, K, seed=78)
+    codes, scales = q8(x)
+    c, d = q8_host(codes, scales)
+    rows = (N - 700, N)
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d, rows=rows)
+    for tile in (256, 128):
+        y = mmq_fn(qt)(wr, codes, scales, N, K, tile=tile).cpu().numpy()
+        check(y[:, rows[0]:rows[1]], y_ref, ab, what=f"mmq {qt} tile={tile}")
 
 
 @pytest.mark.parametrize("qt", ["q4k", "q6k"])
