@@ -20,6 +20,7 @@ data of the stated distributions):
      attn-out adds the residual stream h, RMSNorm(h) -> q8_1 feeds gate||up,
      SwiGLU -> q8_1 of its output feeds down, which adds h (attention itself is
      not part of the path: its output is a synthetic input)
+  7  config 1 with every weight in Q5_K (a Q5_K_M-style layer)
 
 Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
 graphs (programmatic dependent launch between the kernels), bracketed by a
@@ -47,7 +48,8 @@ import synth  # noqa: E402
 
 METRIC = "Q4_K/Q6_K GEMV weight GB/s (% of HBM peak); prefill MMQ int8 TOPS"
 L2_BYTES = 129 * 2 ** 20
-BYTES_PER_SB = {"q4k": 144, "q6k": 210}
+BYTES_PER_SB = {"q4k": 144, "q6k": 210, "q5k": 176}
+OTYPE = {"q4k": 1, "q6k": 2, "q5k": 3}                # oracle type ids
 
 CONFIGS = {
     0: dict(name="single Q4_K GEMV 4096x4096, batch 1", M=1, kind="gemv",
@@ -66,6 +68,8 @@ CONFIGS = {
     6: dict(name="Llama-3-8B decode layer with fused RMSNorm/SwiGLU -> q8_1 producers, batch 1 (Q4_K)", M=1,
             kind="chain", gemms=[(n, "q4k", N, K, r, s) for (n, N, K, r, s) in synth.LLAMA3_8B_LAYER],
             inputs=["x_attn_in", "x_attn_out"]),
+    7: dict(name="Llama-3-8B decode layer, batch 1 (Q5_K)", M=1, kind="gemv",
+            gemms=[(n, "q5k", N, K, r, s) for (n, N, K, r, s) in synth.LLAMA3_8B_LAYER]),
 }
 NORM_EPS = 1e-5                                       # Llama-3 RMSNorm epsilon
 
@@ -171,7 +175,7 @@ class Workload:
             self.host_w[name] = hw
             g = torch.from_numpy(hw).to(device)
             for c in range(copies):
-                self.w[c][name] = qk.repack(qk.Q4_K if q == "q4k" else qk.Q6_K, g, N, K)
+                self.w[c][name] = qk.repack(OTYPE[q], g, N, K)
             del g
         self.host_x = {s: synth.activations(M, K, seed=seed, tag=s) for s, K in slots(cfg)
                        if s in cfg.get("inputs", [s])}
@@ -201,7 +205,7 @@ class Workload:
         qk, cfg = self.qk, self.cfg
         name, q, N, K, res, s = gemm
         if fused and cfg["kind"] in ("gemv", "chain"):
-            fn = qk.gemv_q4k_f32 if q == "q4k" else qk.gemv_q6k_f32
+            fn = {"q4k": qk.gemv_q4k_f32, "q5k": qk.gemv_q5k_f32, "q6k": qk.gemv_q6k_f32}[q]
             fn(self.w[copy][name], self.x[s], N, K, residual=self.r.get(name), y=self.y[name],
                pdl=pdl, stream=stream)
         else:
@@ -211,7 +215,7 @@ class Workload:
                 fn = qk.mmq_q4k if q == "q4k" else qk.mmq_q6k
                 fn(self.w[copy][name], codes, scales, N, K, workspace=self.ws, **kw)
             else:
-                fn = qk.gemv_q4k if q == "q4k" else qk.gemv_q6k
+                fn = {"q4k": qk.gemv_q4k, "q5k": qk.gemv_q5k, "q6k": qk.gemv_q6k}[q]
                 fn(self.w[copy][name], codes, scales, N, K, **kw)
 
     def step(self, copy: int, pdl: bool = True, stream=None, front_end: str = "auto"):
@@ -251,7 +255,7 @@ class Workload:
         q = gemm[1]
         if self.cfg["kind"] == "mmq":
             return "mmq_q4k" if q == "q4k" else "mmq_q6k"
-        return ("gemv_q4k" if q == "q4k" else "gemv_q6k") + ("_f32" if fused else "")
+        return "gemv_" + q + ("_f32" if fused else "")
 
     def launches_per_step(self, front_end: str = "auto") -> int:
         if self.cfg["kind"] == "chain":
@@ -378,7 +382,7 @@ def oracle_chain_step(cfg, host_w, host_x, host_r, host_g, threads: int, n_frac:
         _, q, N, K, _, _ = gm[name]
         c, d, _ = oracle.quantize_q8_1(x32)
         n1 = sample_rows(N, n_frac)
-        y, _ = oracle.gemm(oracle.Q4_K if q == "q4k" else oracle.Q6_K, host_w[name], N, K, c, d,
+        y, _ = oracle.gemm(OTYPE[q], host_w[name], N, K, c, d,
                            residual=residual, rows=(0, n1), threads=threads)
         out = np.zeros((M, N), np.float32)
         out[:, :n1] = y
@@ -414,7 +418,7 @@ def oracle_step(cfg, host_w, host_x, host_r, threads: int, m_rows=None, n_frac: 
         if r is not None and m_rows is not None:
             r = r[:m_rows]
         n1 = sample_rows(N, n_frac)
-        oracle.gemm(oracle.Q4_K if q == "q4k" else oracle.Q6_K, host_w[name], N, K, c, d, residual=r,
+        oracle.gemm(OTYPE[q], host_w[name], N, K, c, d, residual=r,
                     rows=(0, n1), threads=threads)
         wbytes += n1 * (K // 256) * BYTES_PER_SB[q]
         ops += 2 * c.shape[0] * n1 * K
@@ -693,7 +697,7 @@ def main():
                          "of at most 4096 values, unfused for larger ones")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100, 5: 100, 6: 40000}[args.config]
+        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100, 5: 100, 6: 40000, 7: 40000}[args.config]
     args.graph_steps = max(1, min(args.graph_steps, args.steps))
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

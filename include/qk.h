@@ -50,6 +50,7 @@ extern "C" {
 /* quantization types for qk_repacked_bytes / qk_repack */
 #define QK_TYPE_Q4_K 1
 #define QK_TYPE_Q6_K 2
+#define QK_TYPE_Q5_K 3
 
 /* flags for the compute calls */
 #define QK_LAUNCH_PDL 1u
@@ -166,6 +167,9 @@ int qk_swiglu_q8_1(const float *gu, int64_t ldgu, int64_t M, int64_t F, float *h
  * GGUF input: row-major [N][K/256] superblocks;
  *   Q4_K 144 B: f16 d, f16 dmin, 12 B packed 6-bit scales/mins, 128 B codes;
  *   Q6_K 210 B: 128 B low 4 bits, 64 B high 2 bits, 16 int8 scales, f16 d.
+ *   Q5_K 176 B: f16 d, f16 dmin, 12 B 6-bit scales/mins packed as for Q4_K,
+ *     32 B qh (value 64g+l takes bit 2g of qh[l] as its fifth bit, value
+ *     64g+32+l bit 2g+1), 128 B qs (low / high nibbles as for Q4_K).
  * Output (B = K/256 superblocks per row, same total byte count):
  *   Q4_K: codes plane [0, N*B*128): row n at n*B*128, cut into steps of up
  *           to 8 superblocks at 1024*s; step s holds G = 4*nsb groups
@@ -183,9 +187,16 @@ int qk_swiglu_q8_1(const float *gu, int64_t ldgu, int64_t M, int64_t F, float *h
  *         scale plane [N*B*192, N*B*208): 16 B per superblock, byte 4p+t =
  *           GGUF sc[8h + e + 2t] (p = 2h+e).
  *         d plane [N*B*208, N*B*210): binary16 d per superblock.
+ *   Q5_K: codes plane [0, N*B*128): the qs bytes, ordered exactly as the
+ *           Q4_K codes plane.
+ *         fifth-bit plane [N*B*128, N*B*160): 32 B per superblock, 8 B per
+ *           group g: little-endian words R_lo then R_hi; bit 8b+w of R_lo is
+ *           bit 2g of GGUF qh[4w+b] (the low nibble of code byte 4w+b of the
+ *           group), bit 8b+w of R_hi is bit 2g+1 (its high nibble).
+ *         meta plane [N*B*160, N*B*176): as for Q4_K.
  */
 
-/* Bytes of the repacked weight (== GGUF bytes: N*K/256*144 or *210). */
+/* Bytes of the repacked weight (== GGUF bytes: N*K/256 * 144, 176 or 210). */
 int qk_repacked_bytes(int qtype, int64_t N, int64_t K, size_t *bytes);
 
 /*
@@ -230,6 +241,18 @@ int qk_gemv_q6k(const void *w, const int8_t *codes, const void *scales,
                 const float *residual, float *y, unsigned flags, void *stream);
 
 /*
+ * The same GEMV over a Q5_K weight (qk_repack output for QK_TYPE_Q5_K):
+ * minfer "15 . The CUDA backend" sec. 2.2 and cajeta.dev "xpu walkthrough"
+ * sec. 4.2 serve Q5_K beside Q4_K and Q6_K.  The fold is that of Q4_K with
+ * 5-bit codes (q = nibble + 16 * fifth bit): d*sc and dmin*m per 32 values,
+ * the min term from the exact integer code sum of the activation block.
+ * Arguments as for qk_gemv_q4k; M*K <= 65536.
+ */
+int qk_gemv_q5k(const void *w, const int8_t *codes, const void *scales,
+                int64_t M, int64_t N, int64_t K,
+                const float *residual, float *y, unsigned flags, void *stream);
+
+/*
  * Same GEMVs with the q8_1 quantization of the activation done inside the
  * kernel (every CTA quantizes x into shared memory with the same arithmetic
  * as qk_quantize_q8_1, so the codes are bit-identical).  For decode, where an
@@ -251,6 +274,11 @@ int qk_gemv_q4k_f32(const void *w, const float *x, int64_t ldx,
                     int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
 
 int qk_gemv_q6k_f32(const void *w, const float *x, int64_t ldx,
+                    int64_t M, int64_t N, int64_t K,
+                    const float *residual, float *y,
+                    int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
+
+int qk_gemv_q5k_f32(const void *w, const float *x, int64_t ldx,
                     int64_t M, int64_t N, int64_t K,
                     const float *residual, float *y,
                     int8_t *codes_out, void *scales_out, unsigned flags, void *stream);

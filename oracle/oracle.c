@@ -32,6 +32,15 @@
  *                    "15 . The CUDA backend", sec. 2.3, block_q4_K nibbles,
  *                    sub-scales and mins).  The bit layout is the public GGUF
  *                    one; the pages name the fields but do not print it.
+ *  - orc_q5k_*:      GGUF Q5_K superblock (256 values, 176 bytes: f16 d, f16
+ *                    dmin, 12 bytes of 6-bit scales and mins packed as for
+ *                    Q4_K, 32 bytes qh of fifth bits, 128 bytes qs of low
+ *                    nibbles); value = d*sc*q - dmin*m with q = nibble + 16 *
+ *                    fifth bit (minfer "15 . The CUDA backend" sec. 2.2 and
+ *                    cajeta.dev "xpu walkthrough" sec. 4.2 name Q5_K among
+ *                    the k-quants they serve).  The layout is the public GGUF
+ *                    one (group g: low nibbles of qs[32g..] with qh bit 2g,
+ *                    high nibbles with qh bit 2g+1); the pages do not print it.
  *  - orc_q6k_*:      GGUF Q6_K superblock (256 values, 210 bytes: 128 bytes
  *                    of low 4 bits, 64 bytes of high 2 bits, 16 int8 scales,
  *                    f16 d); value = d*sc*(q - 32) (minfer sec. 3.2.2, "raw
@@ -63,13 +72,15 @@
 #define ORC_Q81 32          /* values per q8_1 block */
 #define ORC_Q4K_BYTES 144
 #define ORC_Q6K_BYTES 210
+#define ORC_Q5K_BYTES 176
 
-enum { ORC_Q4_K = 1, ORC_Q6_K = 2 };
+enum { ORC_Q4_K = 1, ORC_Q6_K = 2, ORC_Q5_K = 3 };
 
 int orc_block_bytes(int qtype)
 {
     if (qtype == ORC_Q4_K) return ORC_Q4K_BYTES;
     if (qtype == ORC_Q6_K) return ORC_Q6K_BYTES;
+    if (qtype == ORC_Q5_K) return ORC_Q5K_BYTES;
     return -1;
 }
 
@@ -195,6 +206,29 @@ void orc_q4k_dequant(const uint8_t *blk, double *out)
     }
 }
 
+/* ------------------------------------------------------------------- Q5_K */
+
+/* one 176-byte superblock -> 256 binary64 weights */
+void orc_q5k_dequant(const uint8_t *blk, double *out)
+{
+    double d = orc_f16_to_f64(rd16(blk));
+    double dmin = orc_f16_to_f64(rd16(blk + 2));
+    const uint8_t *q12 = blk + 4;
+    const uint8_t *qh = blk + 16;
+    const uint8_t *qs = blk + 48;
+    for (int g = 0; g < 4; g++) {
+        int sc0, m0, sc1, m1;
+        orc_q4k_scale_min(q12, 2 * g, &sc0, &m0);
+        orc_q4k_scale_min(q12, 2 * g + 1, &sc1, &m1);
+        for (int l = 0; l < 32; l++) {
+            int lo = (qs[32 * g + l] & 0x0f) | (((qh[l] >> (2 * g)) & 1) << 4);
+            int hi = (qs[32 * g + l] >> 4) | (((qh[l] >> (2 * g + 1)) & 1) << 4);
+            out[64 * g + l] = d * sc0 * lo - dmin * m0;
+            out[64 * g + 32 + l] = d * sc1 * hi - dmin * m1;
+        }
+    }
+}
+
 /* ------------------------------------------------------------------- Q6_K */
 
 void orc_q6k_dequant(const uint8_t *blk, double *out)
@@ -226,6 +260,7 @@ int orc_dequant_row(int qtype, const uint8_t *row, int64_t K, double *out)
     if (bs < 0 || K % ORC_QK != 0) return -1;
     for (int64_t b = 0; b < K / ORC_QK; b++) {
         if (qtype == ORC_Q4_K) orc_q4k_dequant(row + b * bs, out + b * ORC_QK);
+        else if (qtype == ORC_Q5_K) orc_q5k_dequant(row + b * bs, out + b * ORC_QK);
         else orc_q6k_dequant(row + b * bs, out + b * ORC_QK);
     }
     return 0;
@@ -308,6 +343,66 @@ int orc_repack_q4k(const uint8_t *gguf, int64_t N, int64_t K, uint8_t *out)
                 int64_t u = 4 * (b - 8 * s) + g;
                 memcpy(step + 16 * u, blk + 16 + 32 * g, 16);
                 memcpy(step + 16 * G + 16 * u, blk + 16 + 32 * g + 16, 16);
+            }
+            uint8_t *mt = meta + (n * B + b) * 16;
+            memcpy(mt, blk, 4);
+            for (int g = 0; g < 4; g++) {
+                int sc0, m0, sc1, m1;
+                orc_q4k_scale_min(blk + 4, 2 * g, &sc0, &m0);
+                orc_q4k_scale_min(blk + 4, 2 * g + 1, &sc1, &m1);
+                uint32_t rec = (uint32_t)sc0 | ((uint32_t)sc1 << 6) |
+                               ((uint32_t)m0 << 12) | ((uint32_t)m1 << 18);
+                mt[4 + 3 * g + 0] = (uint8_t)(rec & 0xff);
+                mt[4 + 3 * g + 1] = (uint8_t)((rec >> 8) & 0xff);
+                mt[4 + 3 * g + 2] = (uint8_t)((rec >> 16) & 0xff);
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Q5_K device layout for an N x K weight (B = K/256), N*B*176 bytes in three
+ * planes:
+ *   codes plane at 0, N*B*128 bytes: the GGUF qs bytes in the Q4_K codes
+ *     plane order (steps of up to 8 superblocks, group u of a step at 16*u
+ *     and 16*G + 16*u).
+ *   fifth-bit plane at N*B*128, 32 bytes per superblock, 8 per group g:
+ *     two little-endian 32-bit words R_lo (bytes 8g..8g+3) and R_hi
+ *     (8g+4..8g+7).  Bit 8b + w of R_lo is the fifth bit of the low-nibble
+ *     value of code byte l = 4w + b (w = 0..7, b = 0..3), i.e. GGUF qh[l]
+ *     bit 2g; R_hi holds qh[l] bit 2g+1 for the high nibbles the same way.
+ *   meta plane at N*B*160, 16 bytes per superblock exactly as for Q4_K.
+ */
+int orc_repack_q5k(const uint8_t *gguf, int64_t N, int64_t K, uint8_t *out)
+{
+    if (K % ORC_QK != 0 || N < 0) return -1;
+    int64_t B = K / ORC_QK;
+    uint8_t *codes = out;
+    uint8_t *hb = out + N * B * 128;
+    uint8_t *meta = out + N * B * 160;
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t b = 0; b < B; b++) {
+            const uint8_t *blk = gguf + (n * B + b) * ORC_Q5K_BYTES;
+            int64_t s = b / 8;
+            int64_t nsb = (B - 8 * s) < 8 ? (B - 8 * s) : 8;
+            int64_t G = 4 * nsb;
+            uint8_t *step = codes + n * B * 128 + 1024 * s;
+            for (int g = 0; g < 4; g++) {
+                int64_t u = 4 * (b - 8 * s) + g;
+                memcpy(step + 16 * u, blk + 48 + 32 * g, 16);
+                memcpy(step + 16 * G + 16 * u, blk + 48 + 32 * g + 16, 16);
+                uint32_t rlo = 0, rhi = 0;
+                for (int l = 0; l < 32; l++) {
+                    int w = l / 4, byte = l % 4;
+                    rlo |= (uint32_t)((blk[16 + l] >> (2 * g)) & 1) << (8 * byte + w);
+                    rhi |= (uint32_t)((blk[16 + l] >> (2 * g + 1)) & 1) << (8 * byte + w);
+                }
+                uint8_t *r = hb + (n * B + b) * 32 + 8 * g;
+                for (int k = 0; k < 4; k++) {
+                    r[k] = (uint8_t)(rlo >> (8 * k));
+                    r[4 + k] = (uint8_t)(rhi >> (8 * k));
+                }
             }
             uint8_t *mt = meta + (n * B + b) * 16;
             memcpy(mt, blk, 4);

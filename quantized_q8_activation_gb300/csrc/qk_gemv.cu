@@ -1,5 +1,5 @@
 // qk_gemv.cu -- decode GEMV y = x_q8 . W^T (+ r) for M = 1..8 activation rows
-// over a repacked Q4_K or Q6_K weight.
+// over a repacked Q4_K, Q5_K or Q6_K weight.
 //
 // Design (GB300, HBM-bound):
 //  - Persistent grid, one CTA of 16 warps per SM.  Warp w of the grid owns
@@ -74,6 +74,7 @@ constexpr int kCtasPerSm = QK_GEMV_CTAS_PER_SM;
 constexpr int kRowsPerItem = 2;                                     // rows a lane works on at once
 constexpr int Q4_R = QK_GEMV_Q4_RING, Q4_SLOT = kRowsPerItem * (1024 + 128);       // codes + 8 metadata records
 constexpr int Q6_R = QK_GEMV_Q6_RING, Q6_SLOT = kRowsPerItem * (1024 + 512 + 128); // ql + qh + scales
+constexpr int Q5_R = QK_GEMV_Q4_RING, Q5_SLOT = kRowsPerItem * (1024 + 256 + 128);  // codes + fifth bits + metadata
 static_assert(Q4_R >= 2 && Q6_R >= 2, "ring needs two slots at least");
 
 // kernel arguments (one struct: the q8_1 and the f32 front ends share the kernels)
@@ -371,6 +372,114 @@ struct Q4Ops {
     }
 };
 
+// ------------------------------------------------------------------ Q5_K
+// slot: [P][1024] code bytes of the step, [P][256] fifth-bit words, [P][8] 16-byte metadata records.
+// The codes and metadata are those of Q4_K; each lane adds its group's two fifth-bit words
+// (R_lo, R_hi: bit 8b + w is the fifth bit of code byte 4w + b's low / high nibble).
+
+constexpr int Q5_HB = 256;
+
+struct Q5Ops {
+    static constexpr int R = Q5_R, SLOT = Q5_SLOT;
+    using LaneConst = Q4Ops::LaneConst;
+    __device__ static LaneConst lane_const(int lane) { return Q4Ops::lane_const(lane); }
+    __device__ static uint32_t issue(uint8_t *slot, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n,
+                                     int64_t sb, int s, int lane)
+    {
+        const int nsb = min(8, B - 8 * s), G = 4 * nsb;
+        const int64_t NB = N * (int64_t)B;
+        const uint8_t *src = w + (sb << 7) + 1024 * s;                      // codes plane
+        const uint8_t *hb = w + (NB << 7) + ((sb + 8 * s) << 5);            // fifth-bit plane
+        const uint8_t *meta = w + NB * 160 + ((sb + 8 * s) << 4);           // metadata plane
+#pragma unroll
+        for (int r = 0; r < P; r++) {
+            if (n + r < N) {
+                uint8_t *dst = slot + r * Q4_CODES;
+                if (lane < G) {
+                    qk::cp_async16(dst + 16 * lane, src + 16 * lane);
+                    qk::cp_async16(dst + 16 * G + 16 * lane, src + 16 * G + 16 * lane);
+                }
+                if (lane < 2 * nsb) qk::cp_async16(slot + P * Q4_CODES + r * Q5_HB + 16 * lane, hb + 16 * lane);
+                if (lane < nsb)
+                    qk::cp_async16(slot + P * (Q4_CODES + Q5_HB) + r * Q4_META + 16 * lane, meta + 16 * lane);
+            }
+            src += (int64_t)B * 128;
+            hb += (int64_t)B * 32;
+            meta += (int64_t)B * 16;
+        }
+        return 0;
+    }
+    // fifth bits of code word w (bytes 4w .. 4w+3) moved to bit 4 of each byte
+    __device__ __forceinline__ static uint32_t fifth(uint32_t R, int w)
+    {
+        return (w <= 4 ? R << (4 - w) : R >> (w - 4)) & 0x10101010u;
+    }
+    template <int M>
+    __device__ static void compute(const uint8_t *sl, int s, int B, int lane, uint32_t, const LaneConst &lc,
+                                   const uint8_t *s_codes, const float2 *s_sc, int K, float (&acc)[P][M])
+    {
+        const int G = 4 * min(8, B - 8 * s);
+        if (lane >= G) return;
+        uint32_t lo5[P][8];                        // low-nibble codes with their fifth bits (0 .. 31)
+        uint32_t hn[P][8], hb[P][8];               // high nibbles in place (16 q) and their fifth bits (0 / 1)
+        float d[P], dmin[P], m0[P], m1[P];
+        int sc0[P], sc1[P];
+#pragma unroll
+        for (int r = 0; r < P; r++) {
+            const uint4 c0 = lds16(sl + r * Q4_CODES + 16 * lane);
+            const uint4 c1 = lds16(sl + r * Q4_CODES + 16 * G + 16 * lane);
+            const uint2 fb = *reinterpret_cast<const uint2 *>(sl + P * Q4_CODES + r * Q5_HB + 8 * lane);
+            const uint4 mt = lds16(sl + P * (Q4_CODES + Q5_HB) + r * Q4_META + 16 * (lane >> 2));
+            const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                lo5[r][i] = (cw[i] & 0x0F0F0F0Fu) | fifth(fb.x, i);
+                hn[r][i] = cw[i] & 0xF0F0F0F0u;
+                hb[r][i] = (fb.y >> i) & 0x01010101u;
+            }
+            d[r] = f16lo(mt.x);
+            dmin[r] = f16hi(mt.x);
+            const uint32_t rec = __byte_perm(__byte_perm(mt.y, mt.z, lc.selA), mt.w, lc.selB);
+            sc0[r] = rec & 63u;
+            sc1[r] = (rec >> 6) & 63u;
+            m0[r] = (float)((rec >> 12) & 63u);
+            m1[r] = (float)((rec >> 18) & 63u);
+        }
+        const uint8_t *abase = s_codes + 2048 * s;
+        const float2 *sbase = s_sc + 64 * s + 2 * lane;
+        const int nb = K >> 5;
+#pragma unroll
+        for (int m = 0; m < M; m++) {
+            const uint8_t *ar = abase + (size_t)m * K;
+            const uint4 a0 = lds16(ar + lc.aoff[0]), a1 = lds16(ar + lc.aoff[1]);   // sub-block 2g
+            const uint4 a2 = lds16(ar + lc.aoff[2]), a3 = lds16(ar + lc.aoff[3]);   // sub-block 2g+1
+            const uint32_t al[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t ah[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+            const float4 sa = *reinterpret_cast<const float4 *>(sbase + (size_t)m * nb);   // d0 S0 d1/16 S1
+#pragma unroll
+            for (int r = 0; r < P; r++) {
+                int il = 0, ih = 0, ib = 0;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    il = qk::dp4a_ss(lo5[r][i], al[i], il);
+                    ih = qk::dp4a_us(hn[r][i], ah[i], ih);
+                    ib = qk::dp4a_ss(hb[r][i], ah[i], ib);
+                }
+                ih += ib << 8;                     // 16 * (high nibble + 16 * fifth bit)
+                float t = sa.x * (float)(il * sc0[r]);
+                t = fmaf(sa.z, (float)(ih * sc1[r]), t);
+                const float v = fmaf(m1[r], sa.w, m0[r] * sa.y);
+                acc[r][m] = fmaf(d[r], t, fmaf(-dmin[r], v, acc[r][m]));
+            }
+        }
+    }
+    template <int M, int NT, bool FUSED>
+    __device__ static void stage(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
+    {
+        Q4Ops::stage<M, NT, FUSED>(a, s_codes, s_side);
+    }
+};
+
 // ------------------------------------------------------------------ Q6_K
 // slot: [P][1024] ql bytes of the step, [P][512] qh bytes, [P][8] 16-byte scale records
 
@@ -664,12 +773,19 @@ __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) g
     gemv_body<Q6Ops, M, FUSED>(a, smem);
 }
 
+template <int M, bool FUSED>
+__global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q5k_kernel(const GemvArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    gemv_body<Q5Ops, M, FUSED>(a, smem);
+}
+
 // ------------------------------------------------------------------ host
 
 typedef void (*gemv_fn)(const GemvArgs);
 
 // per kernel: largest dynamic shared memory opted in so far (per process)
-std::atomic<int> g_smem_set[2][2][8];
+std::atomic<int> g_smem_set[3][2][8];
 
 int prepare(gemv_fn kern, std::atomic<int> &done, size_t smem)
 {
@@ -693,7 +809,10 @@ gemv_fn pick(int qtype, int M)
     static const gemv_fn q6[8] = {gemv_q6k_kernel<1, FUSED>, gemv_q6k_kernel<2, FUSED>, gemv_q6k_kernel<3, FUSED>,
                                   gemv_q6k_kernel<4, FUSED>, gemv_q6k_kernel<5, FUSED>, gemv_q6k_kernel<6, FUSED>,
                                   gemv_q6k_kernel<7, FUSED>, gemv_q6k_kernel<8, FUSED>};
-    return qtype == QK_TYPE_Q4_K ? q4[M - 1] : q6[M - 1];
+    static const gemv_fn q5[8] = {gemv_q5k_kernel<1, FUSED>, gemv_q5k_kernel<2, FUSED>, gemv_q5k_kernel<3, FUSED>,
+                                  gemv_q5k_kernel<4, FUSED>, gemv_q5k_kernel<5, FUSED>, gemv_q5k_kernel<6, FUSED>,
+                                  gemv_q5k_kernel<7, FUSED>, gemv_q5k_kernel<8, FUSED>};
+    return qtype == QK_TYPE_Q4_K ? q4[M - 1] : qtype == QK_TYPE_Q5_K ? q5[M - 1] : q6[M - 1];
 }
 
 int warps_for(int M, bool fused)
@@ -704,7 +823,7 @@ int warps_for(int M, bool fused)
 int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, unsigned flags, void *stream)
 {
     if (M < 1 || M > 8 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 ||
-        M * K > (qtype == QK_TYPE_Q4_K ? 81920 : 40960))
+        M * K > (qtype == QK_TYPE_Q4_K ? 81920 : qtype == QK_TYPE_Q5_K ? 65536 : 40960))
         return QK_E_SHAPE;
     if (!a.w || !a.y) return QK_E_NULL;
     if (fused ? !a.x : (!a.codes || !a.scales)) return QK_E_NULL;
@@ -734,11 +853,13 @@ int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, uns
         return QK_E_ALIAS;
     const int warps = warps_for((int)M, fused);
     // ring | activation codes | side data
-    const size_t smem = (size_t)warps * (qtype == QK_TYPE_Q4_K ? Q4_R * Q4_SLOT : Q6_R * Q6_SLOT) +
-                  (size_t)M * K + (size_t)M * (K / 32) * (qtype == QK_TYPE_Q4_K ? 8 : 16);
+    const size_t smem = (size_t)warps * (qtype == QK_TYPE_Q4_K   ? Q4_R * Q4_SLOT
+                                         : qtype == QK_TYPE_Q5_K ? Q5_R * Q5_SLOT
+                                                                 : Q6_R * Q6_SLOT) +
+                        (size_t)M * K + (size_t)M * (K / 32) * (qtype == QK_TYPE_Q6_K ? 16 : 8);
     if (smem > qk::max_smem_optin()) return QK_E_SHAPE;
     gemv_fn kern = fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M);
-    int st = prepare(kern, g_smem_set[qtype == QK_TYPE_Q4_K ? 0 : 1][fused ? 1 : 0][M - 1], smem);
+    int st = prepare(kern, g_smem_set[qtype - 1][fused ? 1 : 0][M - 1], smem);
     if (st != QK_OK) return st;
     int64_t grid = (int64_t)kCtasPerSm * qk::sm_count();
     const int64_t groups = (N + kRowsPerItem - 1) / kRowsPerItem;
@@ -787,6 +908,20 @@ extern "C" int qk_gemv_q6k(const void *w, const int8_t *codes, const void *scale
                            int64_t K, const float *residual, float *y, unsigned flags, void *stream)
 {
     return gemv(QK_TYPE_Q6_K, false, q8_args(w, codes, scales, residual, y), M, N, K, flags, stream);
+}
+
+extern "C" int qk_gemv_q5k(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N,
+                           int64_t K, const float *residual, float *y, unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q5_K, false, q8_args(w, codes, scales, residual, y), M, N, K, flags, stream);
+}
+
+extern "C" int qk_gemv_q5k_f32(const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                               const float *residual, float *y, int8_t *codes_out, void *scales_out,
+                               unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q5_K, true, f32_args(w, x, ldx, residual, y, codes_out, scales_out), M, N, K, flags,
+                stream);
 }
 
 extern "C" int qk_gemv_q4k_f32(const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,

@@ -1,4 +1,4 @@
-// qk_repack.cu -- load-time lossless repack of GGUF Q4_K / Q6_K superblocks
+// qk_repack.cu -- load-time lossless repack of GGUF Q4_K / Q5_K / Q6_K superblocks
 // into the device layout documented in qk.h.
 //
 // Why: the GEMV and MMQ kernels stream weights with aligned 16-byte loads in
@@ -66,6 +66,54 @@ __global__ void __launch_bounds__(kThreads) repack_q4k_kernel(const uint8_t *__r
     *reinterpret_cast<uint4 *>(dst + N * (int64_t)B * 128 + i * 16) = *reinterpret_cast<const uint4 *>(meta);
 }
 
+// Q5_K: the Q4_K planes (codes, metadata) plus the fifth-bit plane (two words per group)
+__global__ void __launch_bounds__(kThreads) repack_q5k_kernel(const uint8_t *__restrict__ src, int64_t N, int B,
+                                                              uint8_t *__restrict__ dst)
+{
+    const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;   // superblock id
+    if (i >= N * B) return;
+    const int64_t n = i / B;
+    const int b = (int)(i - n * B);
+    const uint8_t *blk = src + i * 176;                              // 176 = 11 x 16: aligned
+    uint8_t hdr[16];
+    *reinterpret_cast<uint4 *>(hdr) = *reinterpret_cast<const uint4 *>(blk);
+    __align__(16) uint8_t qh[32];
+    *reinterpret_cast<uint4 *>(qh) = *reinterpret_cast<const uint4 *>(blk + 16);
+    *reinterpret_cast<uint4 *>(qh + 16) = *reinterpret_cast<const uint4 *>(blk + 32);
+    const int64_t NB = N * (int64_t)B;
+
+    const int s = b >> 3, nsb = min(8, B - 8 * s), G = 4 * nsb;
+    uint8_t *step = dst + n * (int64_t)B * 128 + 1024 * s;
+    __align__(16) uint32_t fb[8];
+    for (int g = 0; g < 4; g++) {
+        const int u = 4 * (b - 8 * s) + g;
+        copy16(step + 16 * u, blk + 48 + 32 * g);
+        copy16(step + 16 * G + 16 * u, blk + 48 + 32 * g + 16);
+        uint32_t rlo = 0, rhi = 0;
+        for (int l = 0; l < 32; l++) {
+            const int sh = 8 * (l & 3) + (l >> 2);
+            rlo |= (uint32_t)((qh[l] >> (2 * g)) & 1) << sh;
+            rhi |= (uint32_t)((qh[l] >> (2 * g + 1)) & 1) << sh;
+        }
+        fb[2 * g] = rlo;
+        fb[2 * g + 1] = rhi;
+    }
+    copy16(dst + NB * 128 + i * 32, reinterpret_cast<const uint8_t *>(fb));
+    copy16(dst + NB * 128 + i * 32 + 16, reinterpret_cast<const uint8_t *>(fb + 4));
+    uint8_t meta[16];
+    meta[0] = hdr[0], meta[1] = hdr[1], meta[2] = hdr[2], meta[3] = hdr[3];
+    for (int g = 0; g < 4; g++) {
+        uint32_t sc0, m0, sc1, m1;
+        q4k_unpack_scale(hdr + 4, 2 * g, sc0, m0);
+        q4k_unpack_scale(hdr + 4, 2 * g + 1, sc1, m1);
+        const uint32_t rec = sc0 | (sc1 << 6) | (m0 << 12) | (m1 << 18);
+        meta[4 + 3 * g] = (uint8_t)rec;
+        meta[5 + 3 * g] = (uint8_t)(rec >> 8);
+        meta[6 + 3 * g] = (uint8_t)(rec >> 16);
+    }
+    *reinterpret_cast<uint4 *>(dst + NB * 160 + i * 16) = *reinterpret_cast<const uint4 *>(meta);
+}
+
 __global__ void __launch_bounds__(kThreads) repack_q6k_kernel(const uint8_t *__restrict__ src, int64_t N, int B,
                                                               uint8_t *__restrict__ dst)
 {
@@ -98,15 +146,15 @@ __global__ void __launch_bounds__(kThreads) repack_q6k_kernel(const uint8_t *__r
 extern "C" int qk_repacked_bytes(int qtype, int64_t N, int64_t K, size_t *bytes)
 {
     if (!bytes) return QK_E_NULL;
-    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K) return QK_E_TYPE;
+    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K && qtype != QK_TYPE_Q5_K) return QK_E_TYPE;
     if (N < 1 || K < 256 || K % 256 != 0) return QK_E_SHAPE;
-    *bytes = (size_t)N * (size_t)(K / 256) * (qtype == QK_TYPE_Q4_K ? 144 : 210);
+    *bytes = (size_t)N * (size_t)(K / 256) * (qtype == QK_TYPE_Q4_K ? 144 : qtype == QK_TYPE_Q5_K ? 176 : 210);
     return QK_OK;
 }
 
 extern "C" int qk_repack(int qtype, const void *gguf, int64_t N, int64_t K, void *dst, void *stream)
 {
-    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K) return QK_E_TYPE;
+    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K && qtype != QK_TYPE_Q5_K) return QK_E_TYPE;
     if (N < 1 || K < 256 || K % 256 != 0 || K / 256 > (1 << 24)) return QK_E_SHAPE;
     if (!gguf || !dst) return QK_E_NULL;
     if (!qk::aligned(gguf, 16) || !qk::aligned(dst, 16)) return QK_E_ALIGN;
@@ -117,7 +165,7 @@ extern "C" int qk_repack(int qtype, const void *gguf, int64_t N, int64_t K, void
     const int64_t nsb = N * B;
     const int64_t grid = (nsb + kThreads - 1) / kThreads;
     if (grid > 0x7fffffffLL) return QK_E_SHAPE;
-    auto kern = qtype == QK_TYPE_Q4_K ? repack_q4k_kernel : repack_q6k_kernel;
+    auto kern = qtype == QK_TYPE_Q4_K ? repack_q4k_kernel : qtype == QK_TYPE_Q5_K ? repack_q5k_kernel : repack_q6k_kernel;
     return qk::launch(kern, dim3((unsigned)grid), dim3(kThreads), 0, (cudaStream_t)stream, false,
                       static_cast<const uint8_t *>(gguf), N, B, static_cast<uint8_t *>(dst));
 }

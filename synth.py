@@ -10,6 +10,8 @@ Distributions (the benchmark definition of the workload):
       12 bytes of packed 6-bit scales and mins, 128 bytes of 4-bit codes.
       The 12-byte packing maps 16 six-bit fields onto 96 bits one to one, so
       uniform random bytes are exactly uniform random scales and mins.
+  Q5_K superblock (176 B): d and dmin as for Q4_K, then uniform random bytes
+      for the packed scales and mins, the 32 bytes of fifth bits and the codes.
   Q6_K superblock (210 B): 128 B of low-4-bit codes and 64 B of high-2-bit
       codes (uniform random bits), 16 int8 scales ~ U[-32, 31], f16 d ~
       U(1e-3, 1e-2).
@@ -25,6 +27,7 @@ import numpy as np
 QK = 256
 Q4K_BYTES = 144
 Q6K_BYTES = 210
+Q5K_BYTES = 176
 
 
 def _rng(seed: int, tag: str) -> np.random.Generator:
@@ -61,9 +64,23 @@ def q6k_weights(N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
     return blk.reshape(-1)
 
 
+def q5k_weights(N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
+    """GGUF Q5_K bytes for an N x K weight, row-major [N][K/256][176]: f16 d ~ U(1e-3, 1e-2),
+    f16 dmin ~ U(0, 5e-3), then uniform random bytes (6-bit scales and mins, fifth bits, codes)."""
+    assert K % QK == 0
+    nb = N * (K // QK)
+    rng = _rng(seed, "q5k:" + tag)
+    blk = rng.integers(0, 256, size=(nb, Q5K_BYTES), dtype=np.uint8)
+    blk[:, 0:2] = _f16_bytes(rng.uniform(1e-3, 1e-2, size=nb))
+    blk[:, 2:4] = _f16_bytes(rng.uniform(0.0, 5e-3, size=nb))
+    return blk.reshape(-1)
+
+
 def weights(qtype: str, N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
     if qtype == "q4k":
         return q4k_weights(N, K, seed, tag)
+    if qtype == "q5k":
+        return q5k_weights(N, K, seed, tag)
     if qtype == "q6k":
         return q6k_weights(N, K, seed, tag)
     raise ValueError(qtype)
