@@ -51,6 +51,7 @@ extern "C" {
 #define QK_TYPE_Q4_K 1
 #define QK_TYPE_Q6_K 2
 #define QK_TYPE_Q5_K 3
+#define QK_TYPE_Q8_0 4
 
 /* flags for the compute calls */
 #define QK_LAUNCH_PDL 1u
@@ -170,6 +171,7 @@ int qk_swiglu_q8_1(const float *gu, int64_t ldgu, int64_t M, int64_t F, float *h
  *   Q5_K 176 B: f16 d, f16 dmin, 12 B 6-bit scales/mins packed as for Q4_K,
  *     32 B qh (value 64g+l takes bit 2g of qh[l] as its fifth bit, value
  *     64g+32+l bit 2g+1), 128 B qs (low / high nibbles as for Q4_K).
+ *   Q8_0 34 B per 32 values: f16 d, 32 int8 codes (w = d * q).
  * Output (B = K/256 superblocks per row, same total byte count):
  *   Q4_K: codes plane [0, N*B*128): row n at n*B*128, cut into steps of up
  *           to 8 superblocks at 1024*s; step s holds G = 4*nsb groups
@@ -194,9 +196,13 @@ int qk_swiglu_q8_1(const float *gu, int64_t ldgu, int64_t M, int64_t F, float *h
  *           bit 2g of GGUF qh[4w+b] (the low nibble of code byte 4w+b of the
  *           group), bit 8b+w of R_hi is bit 2g+1 (its high nibble).
  *         meta plane [N*B*160, N*B*176): as for Q4_K.
+ *   Q8_0: codes plane [0, N*K): int8 codes row-major [N][K]; d plane
+ *           [N*K, N*K*34/32): binary16 d per block, row-major [N][K/32].
+ *           (K % 256 == 0 here too.)
  */
 
-/* Bytes of the repacked weight (== GGUF bytes: N*K/256 * 144, 176 or 210). */
+/* Bytes of the repacked weight (== GGUF bytes: N*K/256 * 144, 176 or 210;
+ * N*K/32 * 34 for Q8_0). */
 int qk_repacked_bytes(int qtype, int64_t N, int64_t K, size_t *bytes);
 
 /*
@@ -253,6 +259,17 @@ int qk_gemv_q5k(const void *w, const int8_t *codes, const void *scales,
                 const float *residual, float *y, unsigned flags, void *stream);
 
 /*
+ * The same GEMV over a Q8_0 weight (qk_repack output for QK_TYPE_Q8_0):
+ * cajeta.dev "xpu walkthrough" sec. 4.2 serves Q8_0 in its batched decode.
+ * Per 32-value block the int8 x int8 dot is exact and is folded with
+ * d_w * d_a in binary32.  Arguments as for qk_gemv_q4k; K % 256 == 0 and
+ * M*K <= 65536.
+ */
+int qk_gemv_q8_0(const void *w, const int8_t *codes, const void *scales,
+                 int64_t M, int64_t N, int64_t K,
+                 const float *residual, float *y, unsigned flags, void *stream);
+
+/*
  * Same GEMVs with the q8_1 quantization of the activation done inside the
  * kernel (every CTA quantizes x into shared memory with the same arithmetic
  * as qk_quantize_q8_1, so the codes are bit-identical).  For decode, where an
@@ -282,6 +299,11 @@ int qk_gemv_q5k_f32(const void *w, const float *x, int64_t ldx,
                     int64_t M, int64_t N, int64_t K,
                     const float *residual, float *y,
                     int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
+
+int qk_gemv_q8_0_f32(const void *w, const float *x, int64_t ldx,
+                     int64_t M, int64_t N, int64_t K,
+                     const float *residual, float *y,
+                     int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
 
 /* ===================================================================== MMQ
  * Prefill contraction of many activation rows with a Q4_K weight: the

@@ -27,8 +27,9 @@ _LIB = os.path.join(_BUILD, "liboracle.so")
 Q4_K = 1
 Q6_K = 2
 Q5_K = 3
+Q8_0 = 4
 QK = 256
-BLOCK_BYTES = {Q4_K: 144, Q6_K: 210, Q5_K: 176}
+BLOCK_BYTES = {Q4_K: 144, Q6_K: 210, Q5_K: 176, Q8_0: 272}   # per 256 values (Q8_0: eight 34-byte blocks)
 
 _lib = None
 _lock = threading.Lock()
@@ -68,6 +69,8 @@ def _load():
             lib.orc_repack_q6k.argtypes = [p, i64, i64, p]
             lib.orc_repack_q5k.argtypes = [p, i64, i64, p]
             lib.orc_q5k_dequant.argtypes = [p, p]
+            lib.orc_q80_dequant.argtypes = [p, p]
+            lib.orc_repack_q80.argtypes = [p, i64, i64, p]
             lib.orc_rmsnorm.argtypes = [p, i64, p, p, ctypes.c_double, i64, i64, p, p]
             lib.orc_swiglu.argtypes = [p, i64, i64, i64, p]
             _lib = lib
@@ -116,6 +119,8 @@ def dequant_block(qtype: int, blk) -> np.ndarray:
         _load().orc_q4k_dequant(_ptr(b), _ptr(out))
     elif qtype == Q5_K:
         _load().orc_q5k_dequant(_ptr(b), _ptr(out))
+    elif qtype == Q8_0:
+        _load().orc_q80_dequant(_ptr(b), _ptr(out))
     else:
         _load().orc_q6k_dequant(_ptr(b), _ptr(out))
     return out
@@ -177,7 +182,8 @@ def repack(qtype: int, w: np.ndarray, N: int, K: int) -> np.ndarray:
     """Expected device layout (uint8, same byte count) for GGUF bytes w."""
     w = np.ascontiguousarray(w, dtype=np.uint8).reshape(-1)
     out = np.zeros(N * (K // QK) * BLOCK_BYTES[qtype], np.uint8)
-    fn = {Q4_K: _load().orc_repack_q4k, Q6_K: _load().orc_repack_q6k, Q5_K: _load().orc_repack_q5k}[qtype]
+    fn = {Q4_K: _load().orc_repack_q4k, Q6_K: _load().orc_repack_q6k, Q5_K: _load().orc_repack_q5k,
+          Q8_0: _load().orc_repack_q80}[qtype]
     if fn(_ptr(w), N, K, _ptr(out)) != 0:
         raise ValueError("orc_repack failed")
     return out

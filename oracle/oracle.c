@@ -41,6 +41,11 @@
  *                    the k-quants they serve).  The layout is the public GGUF
  *                    one (group g: low nibbles of qs[32g..] with qh bit 2g,
  *                    high nibbles with qh bit 2g+1); the pages do not print it.
+ *  - orc_q80_*:      GGUF Q8_0 blocks (32 values, 34 bytes: f16 d, 32 int8
+ *                    codes); value = d*q (cajeta.dev "xpu walkthrough" sec.
+ *                    4.2 serves Q8_0 beside the k-quants).  Handled in runs of
+ *                    8 blocks (256 values, 272 bytes) so that rows walk the
+ *                    same 256-value units as the k-quants.
  *  - orc_q6k_*:      GGUF Q6_K superblock (256 values, 210 bytes: 128 bytes
  *                    of low 4 bits, 64 bytes of high 2 bits, 16 int8 scales,
  *                    f16 d); value = d*sc*(q - 32) (minfer sec. 3.2.2, "raw
@@ -73,14 +78,16 @@
 #define ORC_Q4K_BYTES 144
 #define ORC_Q6K_BYTES 210
 #define ORC_Q5K_BYTES 176
+#define ORC_Q80_BYTES 272       /* 8 Q8_0 blocks of 34 bytes: one 256-value unit */
 
-enum { ORC_Q4_K = 1, ORC_Q6_K = 2, ORC_Q5_K = 3 };
+enum { ORC_Q4_K = 1, ORC_Q6_K = 2, ORC_Q5_K = 3, ORC_Q8_0 = 4 };
 
 int orc_block_bytes(int qtype)
 {
     if (qtype == ORC_Q4_K) return ORC_Q4K_BYTES;
     if (qtype == ORC_Q6_K) return ORC_Q6K_BYTES;
     if (qtype == ORC_Q5_K) return ORC_Q5K_BYTES;
+    if (qtype == ORC_Q8_0) return ORC_Q80_BYTES;
     return -1;
 }
 
@@ -229,6 +236,18 @@ void orc_q5k_dequant(const uint8_t *blk, double *out)
     }
 }
 
+/* ------------------------------------------------------------------- Q8_0 */
+
+/* eight consecutive 34-byte blocks -> 256 binary64 weights */
+void orc_q80_dequant(const uint8_t *blk, double *out)
+{
+    for (int b = 0; b < 8; b++) {
+        const uint8_t *p = blk + 34 * b;
+        double d = orc_f16_to_f64(rd16(p));
+        for (int l = 0; l < 32; l++) out[32 * b + l] = d * (double)(int8_t)p[2 + l];
+    }
+}
+
 /* ------------------------------------------------------------------- Q6_K */
 
 void orc_q6k_dequant(const uint8_t *blk, double *out)
@@ -261,6 +280,7 @@ int orc_dequant_row(int qtype, const uint8_t *row, int64_t K, double *out)
     for (int64_t b = 0; b < K / ORC_QK; b++) {
         if (qtype == ORC_Q4_K) orc_q4k_dequant(row + b * bs, out + b * ORC_QK);
         else if (qtype == ORC_Q5_K) orc_q5k_dequant(row + b * bs, out + b * ORC_QK);
+        else if (qtype == ORC_Q8_0) orc_q80_dequant(row + b * bs, out + b * ORC_QK);
         else orc_q6k_dequant(row + b * bs, out + b * ORC_QK);
     }
     return 0;
@@ -418,6 +438,27 @@ int orc_repack_q5k(const uint8_t *gguf, int64_t N, int64_t K, uint8_t *out)
             }
         }
     }
+    return 0;
+}
+
+/*
+ * Q8_0 device layout for an N x K weight, N*K*34/32 bytes in two planes:
+ *   codes plane at 0, N*K bytes: the int8 codes, row-major [N][K].
+ *   d plane at N*K, the binary16 d of each 32-value block, row-major
+ *     [N][K/32].
+ */
+int orc_repack_q80(const uint8_t *gguf, int64_t N, int64_t K, uint8_t *out)
+{
+    if (K % ORC_QK != 0 || N < 0) return -1;
+    int64_t nb = K / 32;
+    uint8_t *codes = out;
+    uint8_t *dp = out + N * K;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < nb; b++) {
+            const uint8_t *p = gguf + (n * nb + b) * 34;
+            memcpy(codes + n * K + 32 * b, p + 2, 32);
+            memcpy(dp + (n * nb + b) * 2, p, 2);
+        }
     return 0;
 }
 

@@ -1,5 +1,5 @@
 // qk_gemv.cu -- decode GEMV y = x_q8 . W^T (+ r) for M = 1..8 activation rows
-// over a repacked Q4_K, Q5_K or Q6_K weight.
+// over a repacked Q4_K, Q5_K, Q6_K or Q8_0 weight.
 //
 // Design (GB300, HBM-bound):
 //  - Persistent grid, one CTA of 16 warps per SM.  Warp w of the grid owns
@@ -75,6 +75,7 @@ constexpr int kRowsPerItem = 2;                                     // rows a la
 constexpr int Q4_R = QK_GEMV_Q4_RING, Q4_SLOT = kRowsPerItem * (1024 + 128);       // codes + 8 metadata records
 constexpr int Q6_R = QK_GEMV_Q6_RING, Q6_SLOT = kRowsPerItem * (1024 + 512 + 128); // ql + qh + scales
 constexpr int Q5_R = QK_GEMV_Q4_RING, Q5_SLOT = kRowsPerItem * (1024 + 256 + 128);  // codes + fifth bits + metadata
+constexpr int Q80_R = 2, Q80_SLOT = kRowsPerItem * (2048 + 128);                       // int8 codes + block scales
 static_assert(Q4_R >= 2 && Q6_R >= 2, "ring needs two slots at least");
 
 // kernel arguments (one struct: the q8_1 and the f32 front ends share the kernels)
@@ -480,6 +481,98 @@ struct Q5Ops {
     }
 };
 
+// ------------------------------------------------------------------ Q8_0
+// slot: [P][2048] int8 codes of the step (2048 values), then [P][128] binary16 block scales.
+// Lane l takes the 16-value chunks l, l + 32, l + 64, l + 96 of the step; its dot with the
+// activation chunk (same 32-value block) is folded with d_w * d_a per chunk.
+
+constexpr int Q80_CODES = 2048, Q80_D = 128;
+
+struct Q80Ops {
+    static constexpr int R = Q80_R, SLOT = Q80_SLOT;
+    struct LaneConst {
+        int aoff[4];
+    };
+    __device__ static LaneConst lane_const(int lane)
+    {
+        LaneConst c;
+#pragma unroll
+        for (int i = 0; i < 4; i++) c.aoff[i] = 16 * swz(lane + 32 * i);
+        return c;
+    }
+    __device__ static uint32_t issue(uint8_t *slot, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n,
+                                     int64_t sb, int s, int lane)
+    {
+        const int nsb = min(8, B - 8 * s), nch = 16 * nsb;
+        const uint8_t *src = w + (sb << 8) + 2048 * s;                               // codes plane, row n
+        const uint8_t *dsrc = w + ((N * (int64_t)B) << 8) + (sb << 4) + 128 * s;    // d plane, row n
+#pragma unroll
+        for (int r = 0; r < P; r++) {
+            if (n + r < N) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int c = lane + 32 * i;
+                    if (c < nch) qk::cp_async16(slot + r * Q80_CODES + 16 * c, src + 16 * c);
+                }
+                if (lane < nsb) qk::cp_async16(slot + P * Q80_CODES + r * Q80_D + 16 * lane, dsrc + 16 * lane);
+            }
+            src += (int64_t)B << 8;
+            dsrc += (int64_t)B << 4;
+        }
+        return 0;
+    }
+    template <int M>
+    __device__ static void compute(const uint8_t *sl, int s, int B, int lane, uint32_t, const LaneConst &lc,
+                                   const uint8_t *s_codes, const float2 *s_sc, int K, float (&acc)[P][M])
+    {
+        const int nch = 16 * min(8, B - 8 * s);
+        if (lane >= nch) return;
+        uint4 wc[P][4];
+        float dw[P][4];
+#pragma unroll
+        for (int r = 0; r < P; r++)
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int c = lane + 32 * i;
+                wc[r][i] = make_uint4(0, 0, 0, 0);
+                dw[r][i] = 0.0f;
+                if (c < nch) {
+                    wc[r][i] = lds16(sl + r * Q80_CODES + 16 * c);
+                    dw[r][i] = __half2float(*reinterpret_cast<const __half *>(sl + P * Q80_CODES + r * Q80_D +
+                                                                              2 * (c >> 1)));
+                }
+            }
+        const uint8_t *abase = s_codes + 2048 * s;
+        const int nb = K >> 5;
+#pragma unroll
+        for (int m = 0; m < M; m++) {
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int c = lane + 32 * i;
+                if (c < nch) {
+                    const uint4 a = lds16(abase + (size_t)m * K + lc.aoff[i]);
+                    // the Q4_K side data holds d_a / 16 for odd 32-value blocks: undo it (exact)
+                    const float2 sa = s_sc[(size_t)m * nb + 64 * s + (c >> 1)];
+                    const float da = (c & 2) ? sa.x * 16.0f : sa.x;
+#pragma unroll
+                    for (int r = 0; r < P; r++) {
+                        int dot = qk::dp4a_ss(wc[r][i].x, a.x, 0);
+                        dot = qk::dp4a_ss(wc[r][i].y, a.y, dot);
+                        dot = qk::dp4a_ss(wc[r][i].z, a.z, dot);
+                        dot = qk::dp4a_ss(wc[r][i].w, a.w, dot);
+                        acc[r][m] = fmaf(dw[r][i] * da, (float)dot, acc[r][m]);
+                    }
+                }
+            }
+        }
+    }
+    template <int M, int NT, bool FUSED>
+    __device__ static void stage(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
+    {
+        Q4Ops::stage<M, NT, FUSED>(a, s_codes, s_side);
+    }
+};
+
 // ------------------------------------------------------------------ Q6_K
 // slot: [P][1024] ql bytes of the step, [P][512] qh bytes, [P][8] 16-byte scale records
 
@@ -780,12 +873,19 @@ __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) g
     gemv_body<Q5Ops, M, FUSED>(a, smem);
 }
 
+template <int M, bool FUSED>
+__global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q80_kernel(const GemvArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    gemv_body<Q80Ops, M, FUSED>(a, smem);
+}
+
 // ------------------------------------------------------------------ host
 
 typedef void (*gemv_fn)(const GemvArgs);
 
 // per kernel: largest dynamic shared memory opted in so far (per process)
-std::atomic<int> g_smem_set[3][2][8];
+std::atomic<int> g_smem_set[4][2][8];
 
 int prepare(gemv_fn kern, std::atomic<int> &done, size_t smem)
 {
@@ -812,7 +912,13 @@ gemv_fn pick(int qtype, int M)
     static const gemv_fn q5[8] = {gemv_q5k_kernel<1, FUSED>, gemv_q5k_kernel<2, FUSED>, gemv_q5k_kernel<3, FUSED>,
                                   gemv_q5k_kernel<4, FUSED>, gemv_q5k_kernel<5, FUSED>, gemv_q5k_kernel<6, FUSED>,
                                   gemv_q5k_kernel<7, FUSED>, gemv_q5k_kernel<8, FUSED>};
-    return qtype == QK_TYPE_Q4_K ? q4[M - 1] : qtype == QK_TYPE_Q5_K ? q5[M - 1] : q6[M - 1];
+    static const gemv_fn q80[8] = {gemv_q80_kernel<1, FUSED>, gemv_q80_kernel<2, FUSED>, gemv_q80_kernel<3, FUSED>,
+                                   gemv_q80_kernel<4, FUSED>, gemv_q80_kernel<5, FUSED>, gemv_q80_kernel<6, FUSED>,
+                                   gemv_q80_kernel<7, FUSED>, gemv_q80_kernel<8, FUSED>};
+    return qtype == QK_TYPE_Q4_K   ? q4[M - 1]
+           : qtype == QK_TYPE_Q5_K ? q5[M - 1]
+           : qtype == QK_TYPE_Q8_0 ? q80[M - 1]
+                                   : q6[M - 1];
 }
 
 int warps_for(int M, bool fused)
@@ -823,7 +929,7 @@ int warps_for(int M, bool fused)
 int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, unsigned flags, void *stream)
 {
     if (M < 1 || M > 8 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 ||
-        M * K > (qtype == QK_TYPE_Q4_K ? 81920 : qtype == QK_TYPE_Q5_K ? 65536 : 40960))
+        M * K > (qtype == QK_TYPE_Q4_K ? 81920 : qtype == QK_TYPE_Q6_K ? 40960 : 65536))
         return QK_E_SHAPE;
     if (!a.w || !a.y) return QK_E_NULL;
     if (fused ? !a.x : (!a.codes || !a.scales)) return QK_E_NULL;
@@ -855,6 +961,7 @@ int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, uns
     // ring | activation codes | side data
     const size_t smem = (size_t)warps * (qtype == QK_TYPE_Q4_K   ? Q4_R * Q4_SLOT
                                          : qtype == QK_TYPE_Q5_K ? Q5_R * Q5_SLOT
+                                         : qtype == QK_TYPE_Q8_0 ? Q80_R * Q80_SLOT
                                                                  : Q6_R * Q6_SLOT) +
                         (size_t)M * K + (size_t)M * (K / 32) * (qtype == QK_TYPE_Q6_K ? 16 : 8);
     if (smem > qk::max_smem_optin()) return QK_E_SHAPE;
@@ -921,6 +1028,20 @@ extern "C" int qk_gemv_q5k_f32(const void *w, const float *x, int64_t ldx, int64
                                unsigned flags, void *stream)
 {
     return gemv(QK_TYPE_Q5_K, true, f32_args(w, x, ldx, residual, y, codes_out, scales_out), M, N, K, flags,
+                stream);
+}
+
+extern "C" int qk_gemv_q8_0(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N,
+                            int64_t K, const float *residual, float *y, unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q8_0, false, q8_args(w, codes, scales, residual, y), M, N, K, flags, stream);
+}
+
+extern "C" int qk_gemv_q8_0_f32(const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                                const float *residual, float *y, int8_t *codes_out, void *scales_out,
+                                unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q8_0, true, f32_args(w, x, ldx, residual, y, codes_out, scales_out), M, N, K, flags,
                 stream);
 }
 

@@ -1,4 +1,4 @@
-// qk_repack.cu -- load-time lossless repack of GGUF Q4_K / Q5_K / Q6_K superblocks
+// qk_repack.cu -- load-time lossless repack of GGUF Q4_K / Q5_K / Q6_K superblocks and Q8_0 blocks
 // into the device layout documented in qk.h.
 //
 // Why: the GEMV and MMQ kernels stream weights with aligned 16-byte loads in
@@ -114,6 +114,23 @@ __global__ void __launch_bounds__(kThreads) repack_q5k_kernel(const uint8_t *__r
     *reinterpret_cast<uint4 *>(dst + NB * 160 + i * 16) = *reinterpret_cast<const uint4 *>(meta);
 }
 
+// Q8_0: one thread per 34-byte block (2-byte aligned): codes to the codes plane, d to the d plane.
+// B here counts 32-value blocks per row.
+__global__ void __launch_bounds__(kThreads) repack_q80_kernel(const uint8_t *__restrict__ src, int64_t N, int B,
+                                                              uint8_t *__restrict__ dst)
+{
+    const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;   // block id
+    if (i >= N * B) return;
+    __align__(16) uint16_t blk[17];
+    const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src + i * 34);
+    for (int k = 0; k < 17; k++) blk[k] = s16[k];
+    __align__(16) uint8_t codes[32];
+    for (int k = 0; k < 32; k++) codes[k] = reinterpret_cast<const uint8_t *>(blk)[2 + k];
+    copy16(dst + i * 32, codes);
+    copy16(dst + i * 32 + 16, codes + 16);
+    *reinterpret_cast<uint16_t *>(dst + N * (int64_t)B * 32 + i * 2) = blk[0];
+}
+
 __global__ void __launch_bounds__(kThreads) repack_q6k_kernel(const uint8_t *__restrict__ src, int64_t N, int B,
                                                               uint8_t *__restrict__ dst)
 {
@@ -146,26 +163,32 @@ __global__ void __launch_bounds__(kThreads) repack_q6k_kernel(const uint8_t *__r
 extern "C" int qk_repacked_bytes(int qtype, int64_t N, int64_t K, size_t *bytes)
 {
     if (!bytes) return QK_E_NULL;
-    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K && qtype != QK_TYPE_Q5_K) return QK_E_TYPE;
+    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K && qtype != QK_TYPE_Q5_K && qtype != QK_TYPE_Q8_0)
+        return QK_E_TYPE;
     if (N < 1 || K < 256 || K % 256 != 0) return QK_E_SHAPE;
-    *bytes = (size_t)N * (size_t)(K / 256) * (qtype == QK_TYPE_Q4_K ? 144 : qtype == QK_TYPE_Q5_K ? 176 : 210);
+    const size_t per256 = qtype == QK_TYPE_Q4_K ? 144 : qtype == QK_TYPE_Q5_K ? 176 : qtype == QK_TYPE_Q8_0 ? 272 : 210;
+    *bytes = (size_t)N * (size_t)(K / 256) * per256;
     return QK_OK;
 }
 
 extern "C" int qk_repack(int qtype, const void *gguf, int64_t N, int64_t K, void *dst, void *stream)
 {
-    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K && qtype != QK_TYPE_Q5_K) return QK_E_TYPE;
+    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K && qtype != QK_TYPE_Q5_K && qtype != QK_TYPE_Q8_0)
+        return QK_E_TYPE;
     if (N < 1 || K < 256 || K % 256 != 0 || K / 256 > (1 << 24)) return QK_E_SHAPE;
     if (!gguf || !dst) return QK_E_NULL;
     if (!qk::aligned(gguf, 16) || !qk::aligned(dst, 16)) return QK_E_ALIGN;
     size_t bytes = 0;
     qk_repacked_bytes(qtype, N, K, &bytes);
     if (qk::overlaps(gguf, bytes, dst, bytes)) return QK_E_ALIAS;
-    const int B = (int)(K / 256);
+    const int B = (int)(K / (qtype == QK_TYPE_Q8_0 ? 32 : 256));     // repack units per row
     const int64_t nsb = N * B;
     const int64_t grid = (nsb + kThreads - 1) / kThreads;
     if (grid > 0x7fffffffLL) return QK_E_SHAPE;
-    auto kern = qtype == QK_TYPE_Q4_K ? repack_q4k_kernel : qtype == QK_TYPE_Q5_K ? repack_q5k_kernel : repack_q6k_kernel;
+    auto kern = qtype == QK_TYPE_Q4_K   ? repack_q4k_kernel
+                : qtype == QK_TYPE_Q5_K ? repack_q5k_kernel
+                : qtype == QK_TYPE_Q8_0 ? repack_q80_kernel
+                                        : repack_q6k_kernel;
     return qk::launch(kern, dim3((unsigned)grid), dim3(kThreads), 0, (cudaStream_t)stream, false,
                       static_cast<const uint8_t *>(gguf), N, B, static_cast<uint8_t *>(dst));
 }

@@ -12,6 +12,7 @@ Distributions (the benchmark definition of the workload):
       uniform random bytes are exactly uniform random scales and mins.
   Q5_K superblock (176 B): d and dmin as for Q4_K, then uniform random bytes
       for the packed scales and mins, the 32 bytes of fifth bits and the codes.
+  Q8_0 block (34 B): f16 d ~ U(1e-3, 1e-2), 32 int8 codes uniform on [-127, 127].
   Q6_K superblock (210 B): 128 B of low-4-bit codes and 64 B of high-2-bit
       codes (uniform random bits), 16 int8 scales ~ U[-32, 31], f16 d ~
       U(1e-3, 1e-2).
@@ -76,7 +77,21 @@ def q5k_weights(N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
     return blk.reshape(-1)
 
 
+def q80_weights(N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
+    """GGUF Q8_0 bytes for an N x K weight, row-major [N][K/32][34]: f16 d ~ U(1e-3, 1e-2) (the
+    k-quant scale range), int8 codes uniform on [-127, 127]."""
+    assert K % 32 == 0
+    nb = N * (K // 32)
+    rng = _rng(seed, "q80:" + tag)
+    blk = np.empty((nb, 34), np.uint8)
+    blk[:, 0:2] = _f16_bytes(rng.uniform(1e-3, 1e-2, size=nb))
+    blk[:, 2:34] = rng.integers(-127, 128, size=(nb, 32), dtype=np.int8).view(np.uint8)
+    return blk.reshape(-1)
+
+
 def weights(qtype: str, N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
+    if qtype == "q80":
+        return q80_weights(N, K, seed, tag)
     if qtype == "q4k":
         return q4k_weights(N, K, seed, tag)
     if qtype == "q5k":
