@@ -22,6 +22,8 @@ data of the stated distributions):
      not part of the path: its output is a synthetic input)
   7  config 1 with every weight in Q5_K (a Q5_K_M-style layer)
   8  config 1 with every weight in Q8_0
+  9  config 1 with every weight in Q3_K
+ 10  config 1 with every weight in Q2_K
 
 Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
 graphs (programmatic dependent launch between the kernels), bracketed by a
@@ -49,8 +51,9 @@ import synth  # noqa: E402
 
 METRIC = "Q4_K/Q6_K GEMV weight GB/s (% of HBM peak); prefill MMQ int8 TOPS"
 L2_BYTES = 129 * 2 ** 20
-BYTES_PER_SB = {"q4k": 144, "q6k": 210, "q5k": 176, "q80": 272}   # bytes per 256 weights
-OTYPE = {"q4k": 1, "q6k": 2, "q5k": 3, "q80": 4}                   # type ids (library and oracle)
+# device bytes per 256 weights (GGUF bytes, except Q3_K whose scales the repack unpacks: 114 for 110)
+BYTES_PER_SB = {"q4k": 144, "q6k": 210, "q5k": 176, "q80": 272, "q2k": 84, "q3k": 114}
+OTYPE = {"q4k": 1, "q6k": 2, "q5k": 3, "q80": 4, "q2k": 5, "q3k": 6}   # type ids (library and oracle)
 
 CONFIGS = {
     0: dict(name="single Q4_K GEMV 4096x4096, batch 1", M=1, kind="gemv",
@@ -73,6 +76,10 @@ CONFIGS = {
             gemms=[(n, "q5k", N, K, r, s) for (n, N, K, r, s) in synth.LLAMA3_8B_LAYER]),
     8: dict(name="Llama-3-8B decode layer, batch 1 (Q8_0)", M=1, kind="gemv",
             gemms=[(n, "q80", N, K, r, s) for (n, N, K, r, s) in synth.LLAMA3_8B_LAYER]),
+    9: dict(name="Llama-3-8B decode layer, batch 1 (Q3_K)", M=1, kind="gemv",
+            gemms=[(n, "q3k", N, K, r, s) for (n, N, K, r, s) in synth.LLAMA3_8B_LAYER]),
+    10: dict(name="Llama-3-8B decode layer, batch 1 (Q2_K)", M=1, kind="gemv",
+             gemms=[(n, "q2k", N, K, r, s) for (n, N, K, r, s) in synth.LLAMA3_8B_LAYER]),
 }
 NORM_EPS = 1e-5                                       # Llama-3 RMSNorm epsilon
 
@@ -208,7 +215,8 @@ class Workload:
         qk, cfg = self.qk, self.cfg
         name, q, N, K, res, s = gemm
         if fused and cfg["kind"] in ("gemv", "chain"):
-            fn = {"q4k": qk.gemv_q4k_f32, "q5k": qk.gemv_q5k_f32, "q6k": qk.gemv_q6k_f32, "q80": qk.gemv_q8_0_f32}[q]
+            fn = {"q4k": qk.gemv_q4k_f32, "q5k": qk.gemv_q5k_f32, "q6k": qk.gemv_q6k_f32, "q80": qk.gemv_q8_0_f32,
+                  "q2k": qk.gemv_q2k_f32, "q3k": qk.gemv_q3k_f32}[q]
             fn(self.w[copy][name], self.x[s], N, K, residual=self.r.get(name), y=self.y[name],
                pdl=pdl, stream=stream)
         else:
@@ -218,7 +226,8 @@ class Workload:
                 fn = qk.mmq_q4k if q == "q4k" else qk.mmq_q6k
                 fn(self.w[copy][name], codes, scales, N, K, workspace=self.ws, **kw)
             else:
-                fn = {"q4k": qk.gemv_q4k, "q5k": qk.gemv_q5k, "q6k": qk.gemv_q6k, "q80": qk.gemv_q8_0}[q]
+                fn = {"q4k": qk.gemv_q4k, "q5k": qk.gemv_q5k, "q6k": qk.gemv_q6k, "q80": qk.gemv_q8_0,
+                      "q2k": qk.gemv_q2k, "q3k": qk.gemv_q3k}[q]
                 fn(self.w[copy][name], codes, scales, N, K, **kw)
 
     def step(self, copy: int, pdl: bool = True, stream=None, front_end: str = "auto"):
@@ -700,7 +709,8 @@ def main():
                          "of at most 4096 values, unfused for larger ones")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100, 5: 100, 6: 40000, 7: 40000, 8: 30000}[args.config]
+        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100, 5: 100, 6: 40000, 7: 40000, 8: 30000,
+                      9: 40000, 10: 40000}[args.config]
     args.graph_steps = max(1, min(args.graph_steps, args.steps))
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -52,6 +52,8 @@ extern "C" {
 #define QK_TYPE_Q6_K 2
 #define QK_TYPE_Q5_K 3
 #define QK_TYPE_Q8_0 4
+#define QK_TYPE_Q2_K 5
+#define QK_TYPE_Q3_K 6
 
 /* flags for the compute calls */
 #define QK_LAUNCH_PDL 1u
@@ -172,6 +174,14 @@ int qk_swiglu_q8_1(const float *gu, int64_t ldgu, int64_t M, int64_t F, float *h
  *     32 B qh (value 64g+l takes bit 2g of qh[l] as its fifth bit, value
  *     64g+32+l bit 2g+1), 128 B qs (low / high nibbles as for Q4_K).
  *   Q8_0 34 B per 32 values: f16 d, 32 int8 codes (w = d * q).
+ *   Q2_K 84 B: scales[16] (low nibble scale, high nibble min of each 16
+ *     values), qs[64] (2-bit codes), f16 d, f16 dmin; value 128n+32j+l takes
+ *     bits 2j of qs[32n+l] and the scale byte of sub-block 8n+2j+(l>=16):
+ *     w = d*sc*q - dmin*m.
+ *   Q3_K 110 B: hmask[32], qs[64], 12 B of sixteen 6-bit scales, f16 d;
+ *     w = d*(S-32)*(q - 4 + 4h), h = bit 4n+j of hmask[l] (q, S as for Q2_K;
+ *     scale s: low nibble in byte s (s < 8) or the high nibble of byte s-8,
+ *     high two bits at bits 2*(s/4) of byte 8 + s%4).
  * Output (B = K/256 superblocks per row, same total byte count):
  *   Q4_K: codes plane [0, N*B*128): row n at n*B*128, cut into steps of up
  *           to 8 superblocks at 1024*s; step s holds G = 4*nsb groups
@@ -199,10 +209,21 @@ int qk_swiglu_q8_1(const float *gu, int64_t ldgu, int64_t M, int64_t F, float *h
  *   Q8_0: codes plane [0, N*K): int8 codes row-major [N][K]; d plane
  *           [N*K, N*K*34/32): binary16 d per block, row-major [N][K/32].
  *           (K % 256 == 0 here too.)
+ *   Q2_K: codes plane [0, N*B*64): row n at n*B*64, steps of up to 8
+ *           superblocks at 512*s; lane u of a step is superblock 8s+u/4 with
+ *           p = u%4 = 2n'+e and holds GGUF qs[32n'+16e ..+16] at 16u.
+ *         scale plane [N*B*64, N*B*80): 16 B per superblock, byte 4p+t = GGUF
+ *           scales[8n'+2t+e].
+ *         d plane [N*B*80, N*B*84): d, dmin (binary16) per superblock.
+ *   Q3_K (114 B per superblock: 4 B more than GGUF, the scales unpacked):
+ *         codes plane as for Q2_K; hmask plane [N*B*64, N*B*96): GGUF hmask;
+ *         scale plane [N*B*96, N*B*112): int8 S-32 in Q2_K's lane order;
+ *         d plane [N*B*112, N*B*114).
  */
 
-/* Bytes of the repacked weight (== GGUF bytes: N*K/256 * 144, 176 or 210;
- * N*K/32 * 34 for Q8_0). */
+/* Bytes of the repacked weight (== GGUF bytes: N*K/256 * 144, 176, 210 or 84;
+ * N*K/32 * 34 for Q8_0; N*K/256 * 114 for Q3_K, 4 B per superblock more than
+ * its 110-byte GGUF block). */
 int qk_repacked_bytes(int qtype, int64_t N, int64_t K, size_t *bytes);
 
 /*
@@ -270,6 +291,22 @@ int qk_gemv_q8_0(const void *w, const int8_t *codes, const void *scales,
                  const float *residual, float *y, unsigned flags, void *stream);
 
 /*
+ * The same GEMV over Q2_K and Q3_K weights (qk_repack output for
+ * QK_TYPE_Q2_K / QK_TYPE_Q3_K; cajeta.dev "xpu walkthrough" sec. 4.2 serves
+ * both).  Per 16 values the integer dot of the codes with the q8_1 codes is
+ * exact; it is folded with d*sc (Q2_K, the min term from the exact integer
+ * code sum of the activation) or d*(S-32) (Q3_K, its -4 offset likewise).
+ * Arguments as for qk_gemv_q4k; M*K <= 81920.
+ */
+int qk_gemv_q2k(const void *w, const int8_t *codes, const void *scales,
+                int64_t M, int64_t N, int64_t K,
+                const float *residual, float *y, unsigned flags, void *stream);
+
+int qk_gemv_q3k(const void *w, const int8_t *codes, const void *scales,
+                int64_t M, int64_t N, int64_t K,
+                const float *residual, float *y, unsigned flags, void *stream);
+
+/*
  * Same GEMVs with the q8_1 quantization of the activation done inside the
  * kernel (every CTA quantizes x into shared memory with the same arithmetic
  * as qk_quantize_q8_1, so the codes are bit-identical).  For decode, where an
@@ -304,6 +341,16 @@ int qk_gemv_q8_0_f32(const void *w, const float *x, int64_t ldx,
                      int64_t M, int64_t N, int64_t K,
                      const float *residual, float *y,
                      int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
+
+int qk_gemv_q2k_f32(const void *w, const float *x, int64_t ldx,
+                    int64_t M, int64_t N, int64_t K,
+                    const float *residual, float *y,
+                    int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
+
+int qk_gemv_q3k_f32(const void *w, const float *x, int64_t ldx,
+                    int64_t M, int64_t N, int64_t K,
+                    const float *residual, float *y,
+                    int8_t *codes_out, void *scales_out, unsigned flags, void *stream);
 
 /* ===================================================================== MMQ
  * Prefill contraction of many activation rows with a Q4_K weight: the

@@ -28,8 +28,11 @@ Q4_K = 1
 Q6_K = 2
 Q5_K = 3
 Q8_0 = 4
+Q2_K = 5
+Q3_K = 6
 QK = 256
-BLOCK_BYTES = {Q4_K: 144, Q6_K: 210, Q5_K: 176, Q8_0: 272}   # per 256 values (Q8_0: eight 34-byte blocks)
+BLOCK_BYTES = {Q4_K: 144, Q6_K: 210, Q5_K: 176, Q8_0: 272, Q2_K: 84, Q3_K: 110}   # GGUF bytes per 256 values
+DEVICE_BYTES = {**BLOCK_BYTES, Q3_K: 114}          # repacked bytes per 256 values (Q3_K scales unpacked)
 
 _lib = None
 _lock = threading.Lock()
@@ -71,6 +74,11 @@ def _load():
             lib.orc_q5k_dequant.argtypes = [p, p]
             lib.orc_q80_dequant.argtypes = [p, p]
             lib.orc_repack_q80.argtypes = [p, i64, i64, p]
+            lib.orc_q2k_dequant.argtypes = [p, p]
+            lib.orc_q3k_dequant.argtypes = [p, p]
+            lib.orc_q3k_scale.argtypes = [p, ctypes.c_int]
+            lib.orc_repack_q2k.argtypes = [p, i64, i64, p]
+            lib.orc_repack_q3k.argtypes = [p, i64, i64, p]
             lib.orc_rmsnorm.argtypes = [p, i64, p, p, ctypes.c_double, i64, i64, p, p]
             lib.orc_swiglu.argtypes = [p, i64, i64, i64, p]
             _lib = lib
@@ -121,6 +129,10 @@ def dequant_block(qtype: int, blk) -> np.ndarray:
         _load().orc_q5k_dequant(_ptr(b), _ptr(out))
     elif qtype == Q8_0:
         _load().orc_q80_dequant(_ptr(b), _ptr(out))
+    elif qtype == Q2_K:
+        _load().orc_q2k_dequant(_ptr(b), _ptr(out))
+    elif qtype == Q3_K:
+        _load().orc_q3k_dequant(_ptr(b), _ptr(out))
     else:
         _load().orc_q6k_dequant(_ptr(b), _ptr(out))
     return out
@@ -181,9 +193,9 @@ def gemm(qtype: int, w: np.ndarray, N: int, K: int, codes: np.ndarray, d_a: np.n
 def repack(qtype: int, w: np.ndarray, N: int, K: int) -> np.ndarray:
     """Expected device layout (uint8, same byte count) for GGUF bytes w."""
     w = np.ascontiguousarray(w, dtype=np.uint8).reshape(-1)
-    out = np.zeros(N * (K // QK) * BLOCK_BYTES[qtype], np.uint8)
+    out = np.zeros(N * (K // QK) * DEVICE_BYTES[qtype], np.uint8)
     fn = {Q4_K: _load().orc_repack_q4k, Q6_K: _load().orc_repack_q6k, Q5_K: _load().orc_repack_q5k,
-          Q8_0: _load().orc_repack_q80}[qtype]
+          Q8_0: _load().orc_repack_q80, Q2_K: _load().orc_repack_q2k, Q3_K: _load().orc_repack_q3k}[qtype]
     if fn(_ptr(w), N, K, _ptr(out)) != 0:
         raise ValueError("orc_repack failed")
     return out
@@ -216,3 +228,9 @@ def swiglu(gu: np.ndarray, F: int) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"orc_swiglu failed ({rc})")
     return h
+
+
+def q3k_scale(sc12, s: int) -> int:
+    """Signed sub-block scale s (0..15) of a Q3_K superblock's 12 packed scale bytes."""
+    b = np.frombuffer(bytes(sc12), np.uint8).copy()
+    return int(_load().orc_q3k_scale(_ptr(b), s))

@@ -46,6 +46,22 @@
  *                    4.2 serves Q8_0 beside the k-quants).  Handled in runs of
  *                    8 blocks (256 values, 272 bytes) so that rows walk the
  *                    same 256-value units as the k-quants.
+ *  - orc_q2k_*:      GGUF Q2_K superblock (256 values, 84 bytes: 16 scale bytes
+ *                    (low nibble the scale, high nibble the min of each
+ *                    16-value sub-block), 64 bytes of 2-bit codes, f16 d, f16
+ *                    dmin); value = d*sc*q - dmin*m.
+ *  - orc_q3k_*:      GGUF Q3_K superblock (256 values, 110 bytes: 32 bytes
+ *                    hmask, 64 bytes of 2-bit codes, 12 bytes of sixteen 6-bit
+ *                    scales, f16 d); value = d*(S - 32)*(q - 4*(1 - h)) with h
+ *                    the hmask bit.  For both: value 128n + 32j + l takes code
+ *                    bits 2j of qs[32n + l] and the scale of sub-block
+ *                    8n + 2j + (l >= 16); Q3_K's h is bit 4n + j of hmask[l].
+ *                    The 12 Q3_K scale bytes hold the low nibbles of scales
+ *                    0-7 and 8-15 in bytes 0-7 (low, high nibble) and the high
+ *                    two bits of scale s in byte 8 + s%4, bits 2*(s/4).  (The
+ *                    pages name Q2_K and Q3_K among the served formats --
+ *                    cajeta.dev "xpu walkthrough" sec. 4.2 -- but print no
+ *                    layout; this is the public GGUF one.)
  *  - orc_q6k_*:      GGUF Q6_K superblock (256 values, 210 bytes: 128 bytes
  *                    of low 4 bits, 64 bytes of high 2 bits, 16 int8 scales,
  *                    f16 d); value = d*sc*(q - 32) (minfer sec. 3.2.2, "raw
@@ -79,8 +95,10 @@
 #define ORC_Q6K_BYTES 210
 #define ORC_Q5K_BYTES 176
 #define ORC_Q80_BYTES 272       /* 8 Q8_0 blocks of 34 bytes: one 256-value unit */
+#define ORC_Q2K_BYTES 84
+#define ORC_Q3K_BYTES 110
 
-enum { ORC_Q4_K = 1, ORC_Q6_K = 2, ORC_Q5_K = 3, ORC_Q8_0 = 4 };
+enum { ORC_Q4_K = 1, ORC_Q6_K = 2, ORC_Q5_K = 3, ORC_Q8_0 = 4, ORC_Q2_K = 5, ORC_Q3_K = 6 };
 
 int orc_block_bytes(int qtype)
 {
@@ -88,6 +106,8 @@ int orc_block_bytes(int qtype)
     if (qtype == ORC_Q6_K) return ORC_Q6K_BYTES;
     if (qtype == ORC_Q5_K) return ORC_Q5K_BYTES;
     if (qtype == ORC_Q8_0) return ORC_Q80_BYTES;
+    if (qtype == ORC_Q2_K) return ORC_Q2K_BYTES;
+    if (qtype == ORC_Q3_K) return ORC_Q3K_BYTES;
     return -1;
 }
 
@@ -248,6 +268,42 @@ void orc_q80_dequant(const uint8_t *blk, double *out)
     }
 }
 
+/* ------------------------------------------------------------- Q2_K, Q3_K */
+
+void orc_q2k_dequant(const uint8_t *blk, double *out)
+{
+    const uint8_t *sc = blk, *qs = blk + 16;
+    double d = orc_f16_to_f64(rd16(blk + 80));
+    double dmin = orc_f16_to_f64(rd16(blk + 82));
+    for (int n = 0; n < 2; n++)
+        for (int j = 0; j < 4; j++)
+            for (int l = 0; l < 32; l++) {
+                int q = (qs[32 * n + l] >> (2 * j)) & 3;
+                int s = sc[8 * n + 2 * j + (l >= 16)];
+                out[128 * n + 32 * j + l] = d * (s & 15) * q - dmin * (s >> 4);
+            }
+}
+
+/* signed 6-bit scale s (0..15) of a Q3_K superblock, minus 32 */
+int orc_q3k_scale(const uint8_t *sc12, int s)
+{
+    int lo = s < 8 ? (sc12[s] & 15) : (sc12[s - 8] >> 4);
+    int hi = (sc12[8 + (s & 3)] >> (2 * (s >> 2))) & 3;
+    return (lo | (hi << 4)) - 32;
+}
+
+void orc_q3k_dequant(const uint8_t *blk, double *out)
+{
+    const uint8_t *hm = blk, *qs = blk + 32, *sc12 = blk + 96;
+    double d = orc_f16_to_f64(rd16(blk + 108));
+    for (int n = 0; n < 2; n++)
+        for (int j = 0; j < 4; j++)
+            for (int l = 0; l < 32; l++) {
+                int q = ((qs[32 * n + l] >> (2 * j)) & 3) - (((hm[l] >> (4 * n + j)) & 1) ? 0 : 4);
+                out[128 * n + 32 * j + l] = d * orc_q3k_scale(sc12, 8 * n + 2 * j + (l >= 16)) * q;
+            }
+}
+
 /* ------------------------------------------------------------------- Q6_K */
 
 void orc_q6k_dequant(const uint8_t *blk, double *out)
@@ -281,6 +337,8 @@ int orc_dequant_row(int qtype, const uint8_t *row, int64_t K, double *out)
         if (qtype == ORC_Q4_K) orc_q4k_dequant(row + b * bs, out + b * ORC_QK);
         else if (qtype == ORC_Q5_K) orc_q5k_dequant(row + b * bs, out + b * ORC_QK);
         else if (qtype == ORC_Q8_0) orc_q80_dequant(row + b * bs, out + b * ORC_QK);
+        else if (qtype == ORC_Q2_K) orc_q2k_dequant(row + b * bs, out + b * ORC_QK);
+        else if (qtype == ORC_Q3_K) orc_q3k_dequant(row + b * bs, out + b * ORC_QK);
         else orc_q6k_dequant(row + b * bs, out + b * ORC_QK);
     }
     return 0;
@@ -458,6 +516,65 @@ int orc_repack_q80(const uint8_t *gguf, int64_t N, int64_t K, uint8_t *out)
             const uint8_t *p = gguf + (n * nb + b) * 34;
             memcpy(codes + n * K + 32 * b, p + 2, 32);
             memcpy(dp + (n * nb + b) * 2, p, 2);
+        }
+    return 0;
+}
+
+/*
+ * Q2_K / Q3_K device layouts (B = K/256).  Both start with a codes plane of
+ * N*B*64 bytes, row n at n*B*64, cut into steps of up to 8 superblocks at
+ * 512*s; lane u of a step is superblock 8s + u/4 with p = u%4 = 2n' + e and
+ * holds GGUF qs[32n' + 16e .. +16] at 16*u.  Scale records are 16 bytes per
+ * superblock in lane order: byte 4p + t is the scale of sub-block 8n' + 2t + e.
+ *   Q2_K (84 bytes per superblock): codes | scale plane (the GGUF scale bytes,
+ *     scale in the low nibble, min in the high) at N*B*64 | d, dmin (binary16)
+ *     at N*B*80, 4 bytes per superblock.
+ *   Q3_K (114 bytes per superblock, 4 more than GGUF: the sixteen 6-bit scales
+ *     are stored unpacked): codes | hmask plane (GGUF hmask, 32 bytes per
+ *     superblock) at N*B*64 | scale plane (int8 scale - 32) at N*B*96 | d
+ *     (binary16) at N*B*112.
+ */
+static void q23_codes_and_order(const uint8_t *qs, int64_t n, int64_t b, int64_t B, uint8_t *codes)
+{
+    int64_t s = b / 8;
+    uint8_t *step = codes + n * B * 64 + 512 * s;
+    for (int p = 0; p < 4; p++) {
+        int hn = p / 2, e = p % 2;
+        int64_t u = 4 * (b - 8 * s) + p;
+        memcpy(step + 16 * u, qs + 32 * hn + 16 * e, 16);
+    }
+}
+
+int orc_repack_q2k(const uint8_t *gguf, int64_t N, int64_t K, uint8_t *out)
+{
+    if (K % ORC_QK != 0 || N < 0) return -1;
+    int64_t B = K / ORC_QK, NB = N * B;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < B; b++) {
+            const uint8_t *blk = gguf + (n * B + b) * ORC_Q2K_BYTES;
+            q23_codes_and_order(blk + 16, n, b, B, out);
+            for (int p = 0; p < 4; p++)
+                for (int t = 0; t < 4; t++)
+                    out[NB * 64 + (n * B + b) * 16 + 4 * p + t] = blk[8 * (p / 2) + 2 * t + (p % 2)];
+            memcpy(out + NB * 80 + (n * B + b) * 4, blk + 80, 4);
+        }
+    return 0;
+}
+
+int orc_repack_q3k(const uint8_t *gguf, int64_t N, int64_t K, uint8_t *out)
+{
+    if (K % ORC_QK != 0 || N < 0) return -1;
+    int64_t B = K / ORC_QK, NB = N * B;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t b = 0; b < B; b++) {
+            const uint8_t *blk = gguf + (n * B + b) * ORC_Q3K_BYTES;
+            q23_codes_and_order(blk + 32, n, b, B, out);
+            memcpy(out + NB * 64 + (n * B + b) * 32, blk, 32);
+            for (int p = 0; p < 4; p++)
+                for (int t = 0; t < 4; t++)
+                    out[NB * 96 + (n * B + b) * 16 + 4 * p + t] =
+                        (uint8_t)(int8_t)orc_q3k_scale(blk + 96, 8 * (p / 2) + 2 * t + (p % 2));
+            memcpy(out + NB * 112 + (n * B + b) * 2, blk + 108, 2);
         }
     return 0;
 }

@@ -28,6 +28,8 @@ Q4_K = 1
 Q6_K = 2
 Q5_K = 3
 Q8_0 = 4
+Q2_K = 5
+Q3_K = 6
 LAUNCH_PDL = 1
 MMQ_TILE_256 = 2
 MMQ_TILE_128 = 4
@@ -39,7 +41,8 @@ STATUS = {0: "QK_OK", -1: "QK_E_NULL", -2: "QK_E_SHAPE", -3: "QK_E_ALIGN", -4: "
 # every symbol include/qk.h declares
 EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1", "qk_repacked_bytes",
            "qk_repack", "qk_gemv_q4k", "qk_gemv_q6k", "qk_gemv_q5k", "qk_gemv_q4k_f32", "qk_gemv_q6k_f32",
-           "qk_gemv_q5k_f32", "qk_gemv_q8_0", "qk_gemv_q8_0_f32",
+           "qk_gemv_q5k_f32", "qk_gemv_q8_0", "qk_gemv_q8_0_f32", "qk_gemv_q2k", "qk_gemv_q3k",
+           "qk_gemv_q2k_f32", "qk_gemv_q3k_f32",
            "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_mmq_q6k", "qk_mmq_q4k_noalloc", "qk_error_flags",
            "qk_rmsnorm_q8_1", "qk_swiglu_q8_1"]
 
@@ -84,10 +87,14 @@ def lib() -> ctypes.CDLL:
             L.qk_gemv_q6k.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
             L.qk_gemv_q5k.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
             L.qk_gemv_q8_0.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
+            L.qk_gemv_q2k.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
+            L.qk_gemv_q3k.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
             L.qk_gemv_q4k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
             L.qk_gemv_q6k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
             L.qk_gemv_q5k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
             L.qk_gemv_q8_0_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
+            L.qk_gemv_q2k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
+            L.qk_gemv_q3k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, p, u, p]
             L.qk_mmq_workspace_bytes.argtypes = [i64, i64, i64, szp]
             L.qk_mmq_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
             L.qk_mmq_q6k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
@@ -224,7 +231,8 @@ def repack(qtype: int, gguf: torch.Tensor, N: int, K: int, out=None, stream=None
     """GGUF superblocks (uint8 CUDA tensor) -> repacked device weight (uint8)."""
     _cuda(gguf, "gguf")
     nbytes = repacked_bytes(qtype, N, K)
-    if gguf.numel() * gguf.element_size() < nbytes:
+    gguf_bytes = N * (K // 256) * 110 if qtype == Q3_K else nbytes
+    if gguf.numel() * gguf.element_size() < gguf_bytes:
         raise ValueError("gguf buffer smaller than N*K/256 superblocks")
     if out is None:
         out = torch.empty(nbytes, dtype=torch.uint8, device=gguf.device)
@@ -268,6 +276,16 @@ def gemv_q8_0(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=N
     return _gemv(lib().qk_gemv_q8_0, "qk_gemv_q8_0", w, codes, scales, N, K, residual, y, pdl, stream)
 
 
+def gemv_q2k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
+    """GEMV over a repacked Q2_K weight, 1 <= M <= 8 activation rows."""
+    return _gemv(lib().qk_gemv_q2k, "qk_gemv_q2k", w, codes, scales, N, K, residual, y, pdl, stream)
+
+
+def gemv_q3k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
+    """GEMV over a repacked Q3_K weight, 1 <= M <= 8 activation rows."""
+    return _gemv(lib().qk_gemv_q3k, "qk_gemv_q3k", w, codes, scales, N, K, residual, y, pdl, stream)
+
+
 def _gemv_f32(fn, name, w, x, N, K, residual, y, codes_out, scales_out, pdl, stream):
     if x.dim() == 1:
         x = x.view(1, -1)
@@ -307,6 +325,18 @@ def gemv_q5k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=N
 def gemv_q8_0_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
     """GEMV over a repacked Q8_0 weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
     return _gemv_f32(lib().qk_gemv_q8_0_f32, "qk_gemv_q8_0_f32", w, x, N, K, residual, y, codes_out, scales_out,
+                     pdl, stream)
+
+
+def gemv_q2k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+    """GEMV over a repacked Q2_K weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
+    return _gemv_f32(lib().qk_gemv_q2k_f32, "qk_gemv_q2k_f32", w, x, N, K, residual, y, codes_out, scales_out,
+                     pdl, stream)
+
+
+def gemv_q3k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+    """GEMV over a repacked Q3_K weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
+    return _gemv_f32(lib().qk_gemv_q3k_f32, "qk_gemv_q3k_f32", w, x, N, K, residual, y, codes_out, scales_out,
                      pdl, stream)
 
 

@@ -1,5 +1,5 @@
 // qk_gemv.cu -- decode GEMV y = x_q8 . W^T (+ r) for M = 1..8 activation rows
-// over a repacked Q4_K, Q5_K, Q6_K or Q8_0 weight.
+// over a repacked k-quant (Q2_K, Q3_K, Q4_K, Q5_K, Q6_K) or Q8_0 weight.
 //
 // Design (GB300, HBM-bound):
 //  - Persistent grid, one CTA of 16 warps per SM.  Warp w of the grid owns
@@ -76,6 +76,7 @@ constexpr int Q4_R = QK_GEMV_Q4_RING, Q4_SLOT = kRowsPerItem * (1024 + 128);    
 constexpr int Q6_R = QK_GEMV_Q6_RING, Q6_SLOT = kRowsPerItem * (1024 + 512 + 128); // ql + qh + scales
 constexpr int Q5_R = QK_GEMV_Q4_RING, Q5_SLOT = kRowsPerItem * (1024 + 256 + 128);  // codes + fifth bits + metadata
 constexpr int Q80_R = 2, Q80_SLOT = kRowsPerItem * (2048 + 128);                       // int8 codes + block scales
+constexpr int Q2_SLOT = kRowsPerItem * (512 + 128), Q3_SLOT = kRowsPerItem * (512 + 256 + 128);  // codes (+ hmask) + scales
 static_assert(Q4_R >= 2 && Q6_R >= 2, "ring needs two slots at least");
 
 // kernel arguments (one struct: the q8_1 and the f32 front ends share the kernels)
@@ -737,6 +738,112 @@ struct Q6Ops {
     }
 };
 
+// ------------------------------------------------------------- Q2_K / Q3_K
+// slot: [P][512] 2-bit codes of the step, Q3_K only [P][256] hmask bytes, then [P][128] scale records.
+// The lane of superblock j of the step with p = lane % 4 = 2n + e holds code bytes 32n + 16e .. +16
+// (four codes each: quarters t = 0..3 at bits 2t) and meets the same activation chunks as the Q6_K
+// lanes, so the Q6_K activation staging (d_a and -32 d_a sum(q_a) per 16 values) serves both:
+//   Q2_K  w = d sc q - dmin m:       acc += d sc (d_a dot) + dmin m (-32 d_a sum(q_a)) / 32
+//   Q3_K  w = d S (q3 - 4), q3 = q + 4 h:  acc += d S (d_a dot(q3) + (-32 d_a sum(q_a)) / 8)
+
+template <int QT>
+struct Q23Ops {
+    static constexpr bool Q3 = QT == QK_TYPE_Q3_K;
+    static constexpr int CODES = 512, HM = Q3 ? 256 : 0, SCR = 128;
+    static constexpr int R = Q4_R, SLOT = Q3 ? Q3_SLOT : Q2_SLOT;
+    using LaneConst = Q6Ops::LaneConst;
+    __device__ static LaneConst lane_const(int lane) { return Q6Ops::lane_const(lane); }
+    // copy an item into a ring slot; returns this lane's d record: lane 8r + j (j < nsb) holds the
+    // binary16 d (Q3_K) or d | dmin << 16 (Q2_K) of superblock 8s + j of row r
+    __device__ static uint32_t issue(uint8_t *slot, const uint8_t *__restrict__ w, int64_t N, int B, int64_t n,
+                                     int64_t sb, int s, int lane)
+    {
+        uint32_t dv = 0;
+        const int nsb = min(8, B - 8 * s), L = 4 * nsb;
+        const int64_t NB = N * (int64_t)B, sbs = sb + 8 * s;
+        const uint8_t *codes = w + (sb << 6) + 512 * s;
+        const uint8_t *hm = w + (NB << 6) + (sbs << 5);
+        const uint8_t *sc = w + NB * (Q3 ? 96 : 64) + (sbs << 4);
+        const uint8_t *dd = w + NB * (Q3 ? 112 : 80) + sbs * (Q3 ? 2 : 4);
+#pragma unroll
+        for (int r = 0; r < P; r++) {
+            if (n + r < N) {
+                if (lane < L) qk::cp_async16(slot + r * CODES + 16 * lane, codes + 16 * lane);
+                if (Q3 && lane < 2 * nsb) qk::cp_async16(slot + P * CODES + r * HM + 16 * lane, hm + 16 * lane);
+                if (lane < nsb) qk::cp_async16(slot + P * (CODES + HM) + r * SCR + 16 * lane, sc + 16 * lane);
+                if ((lane >> 3) == r && (lane & 7) < nsb)
+                    dv = Q3 ? qk::ldg_stream2(dd + 2 * (lane & 7)) : qk::ldg_stream4(dd + 4 * (lane & 7));
+            }
+            codes += (int64_t)B * 64;
+            hm += (int64_t)B * 32;
+            sc += (int64_t)B * 16;
+            dd += (int64_t)B * (Q3 ? 2 : 4);
+        }
+        return dv;
+    }
+    template <int M>
+    __device__ static void compute(const uint8_t *sl, int s, int B, int lane, uint32_t dreg, const LaneConst &lc,
+                                   const uint8_t *s_codes, const float2 *s_c16, int K, float (&acc)[P][M])
+    {
+        const int L = 4 * min(8, B - 8 * s);
+        uint32_t dr[P];
+#pragma unroll
+        for (int r = 0; r < P; r++) dr[r] = __shfl_sync(0xffffffffu, dreg, 8 * r + (lane >> 2));
+        if (lane >= L) return;
+        const int hsh = 4 * ((lane >> 1) & 1);                // hmask bit 4n + t of this lane's half n
+        uint4 cq[P], hq[P];
+        float dsl[P][4], dml[P][4];
+#pragma unroll
+        for (int r = 0; r < P; r++) {
+            cq[r] = lds16(sl + r * CODES + 16 * lane);
+            hq[r] = Q3 ? lds16(sl + P * CODES + r * HM + 32 * (lane >> 2) + 16 * (lane & 1)) : make_uint4(0, 0, 0, 0);
+            const uint32_t scw = *reinterpret_cast<const uint32_t *>(sl + P * (CODES + HM) + r * SCR + 4 * lane);
+            const float d = f16lo(dr[r]);
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+                if (Q3) {
+                    dsl[r][t] = d * (float)(int)(int8_t)(scw >> (8 * t));
+                    dml[r][t] = 0.0f;
+                } else {
+                    dsl[r][t] = d * (float)((scw >> (8 * t)) & 15u);
+                    dml[r][t] = f16hi(dr[r]) * (float)((scw >> (8 * t + 4)) & 15u) * 0.03125f;   // / 32, exact
+                }
+            }
+        }
+        const uint8_t *abase = s_codes + 2048 * s;
+        const float2 *cb = s_c16 + 128 * s + 4 * lane;
+        const int nc = K >> 4;
+#pragma unroll
+        for (int m = 0; m < M; m++) {
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+                const uint4 av = lds16(abase + (size_t)m * K + lc.qoff[t]);
+                const float2 dc = cb[(size_t)m * nc + t];
+#pragma unroll
+                for (int r = 0; r < P; r++) {
+                    const uint32_t xw[4] = {cq[r].x, cq[r].y, cq[r].z, cq[r].w};
+                    const uint32_t hw[4] = {hq[r].x, hq[r].y, hq[r].z, hq[r].w};
+                    const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+                    int dot = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        uint32_t c = (xw[k] >> (2 * t)) & 0x03030303u;
+                        if (Q3) c |= ((hw[k] >> (hsh + t)) & 0x01010101u) << 2;
+                        dot = qk::dp4a_ss(c, aw[k], dot);
+                    }
+                    if (Q3) acc[r][m] = fmaf(dsl[r][t], fmaf(dc.x, (float)dot, dc.y * 0.125f), acc[r][m]);
+                    else acc[r][m] = fmaf(dsl[r][t], dc.x * (float)dot, fmaf(dml[r][t], dc.y, acc[r][m]));
+                }
+            }
+        }
+    }
+    template <int M, int NT, bool FUSED>
+    __device__ static void stage(const GemvArgs &a, uint8_t *s_codes, float2 *s_side)
+    {
+        Q6Ops::stage<M, NT, FUSED>(a, s_codes, s_side);
+    }
+};
+
 // ---------------------------------------------------------------- driver
 
 // L2 prefetch of the rows this CTA is about to stage: the f32 activation, or the
@@ -880,12 +987,26 @@ __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) g
     gemv_body<Q80Ops, M, FUSED>(a, smem);
 }
 
+template <int M, bool FUSED>
+__global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q2k_kernel(const GemvArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    gemv_body<Q23Ops<QK_TYPE_Q2_K>, M, FUSED>(a, smem);
+}
+
+template <int M, bool FUSED>
+__global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q3k_kernel(const GemvArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    gemv_body<Q23Ops<QK_TYPE_Q3_K>, M, FUSED>(a, smem);
+}
+
 // ------------------------------------------------------------------ host
 
 typedef void (*gemv_fn)(const GemvArgs);
 
 // per kernel: largest dynamic shared memory opted in so far (per process)
-std::atomic<int> g_smem_set[4][2][8];
+std::atomic<int> g_smem_set[6][2][8];
 
 int prepare(gemv_fn kern, std::atomic<int> &done, size_t smem)
 {
@@ -915,9 +1036,17 @@ gemv_fn pick(int qtype, int M)
     static const gemv_fn q80[8] = {gemv_q80_kernel<1, FUSED>, gemv_q80_kernel<2, FUSED>, gemv_q80_kernel<3, FUSED>,
                                    gemv_q80_kernel<4, FUSED>, gemv_q80_kernel<5, FUSED>, gemv_q80_kernel<6, FUSED>,
                                    gemv_q80_kernel<7, FUSED>, gemv_q80_kernel<8, FUSED>};
+    static const gemv_fn q2[8] = {gemv_q2k_kernel<1, FUSED>, gemv_q2k_kernel<2, FUSED>, gemv_q2k_kernel<3, FUSED>,
+                                  gemv_q2k_kernel<4, FUSED>, gemv_q2k_kernel<5, FUSED>, gemv_q2k_kernel<6, FUSED>,
+                                  gemv_q2k_kernel<7, FUSED>, gemv_q2k_kernel<8, FUSED>};
+    static const gemv_fn q3[8] = {gemv_q3k_kernel<1, FUSED>, gemv_q3k_kernel<2, FUSED>, gemv_q3k_kernel<3, FUSED>,
+                                  gemv_q3k_kernel<4, FUSED>, gemv_q3k_kernel<5, FUSED>, gemv_q3k_kernel<6, FUSED>,
+                                  gemv_q3k_kernel<7, FUSED>, gemv_q3k_kernel<8, FUSED>};
     return qtype == QK_TYPE_Q4_K   ? q4[M - 1]
            : qtype == QK_TYPE_Q5_K ? q5[M - 1]
            : qtype == QK_TYPE_Q8_0 ? q80[M - 1]
+           : qtype == QK_TYPE_Q2_K ? q2[M - 1]
+           : qtype == QK_TYPE_Q3_K ? q3[M - 1]
                                    : q6[M - 1];
 }
 
@@ -929,7 +1058,9 @@ int warps_for(int M, bool fused)
 int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, unsigned flags, void *stream)
 {
     if (M < 1 || M > 8 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 ||
-        M * K > (qtype == QK_TYPE_Q4_K ? 81920 : qtype == QK_TYPE_Q6_K ? 40960 : 65536))
+        M * K > (qtype == QK_TYPE_Q4_K || qtype == QK_TYPE_Q2_K || qtype == QK_TYPE_Q3_K ? 81920
+                 : qtype == QK_TYPE_Q6_K                                                ? 40960
+                                                                                        : 65536))
         return QK_E_SHAPE;
     if (!a.w || !a.y) return QK_E_NULL;
     if (fused ? !a.x : (!a.codes || !a.scales)) return QK_E_NULL;
@@ -959,11 +1090,14 @@ int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, uns
         return QK_E_ALIAS;
     const int warps = warps_for((int)M, fused);
     // ring | activation codes | side data
+    const bool q6side = qtype == QK_TYPE_Q6_K || qtype == QK_TYPE_Q2_K || qtype == QK_TYPE_Q3_K;
     const size_t smem = (size_t)warps * (qtype == QK_TYPE_Q4_K   ? Q4_R * Q4_SLOT
                                          : qtype == QK_TYPE_Q5_K ? Q5_R * Q5_SLOT
                                          : qtype == QK_TYPE_Q8_0 ? Q80_R * Q80_SLOT
+                                         : qtype == QK_TYPE_Q2_K ? Q4_R * Q2_SLOT
+                                         : qtype == QK_TYPE_Q3_K ? Q4_R * Q3_SLOT
                                                                  : Q6_R * Q6_SLOT) +
-                        (size_t)M * K + (size_t)M * (K / 32) * (qtype == QK_TYPE_Q6_K ? 16 : 8);
+                        (size_t)M * K + (size_t)M * (K / 32) * (q6side ? 16 : 8);
     if (smem > qk::max_smem_optin()) return QK_E_SHAPE;
     gemv_fn kern = fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M);
     int st = prepare(kern, g_smem_set[qtype - 1][fused ? 1 : 0][M - 1], smem);
@@ -1042,6 +1176,34 @@ extern "C" int qk_gemv_q8_0_f32(const void *w, const float *x, int64_t ldx, int6
                                 unsigned flags, void *stream)
 {
     return gemv(QK_TYPE_Q8_0, true, f32_args(w, x, ldx, residual, y, codes_out, scales_out), M, N, K, flags,
+                stream);
+}
+
+extern "C" int qk_gemv_q2k(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N,
+                           int64_t K, const float *residual, float *y, unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q2_K, false, q8_args(w, codes, scales, residual, y), M, N, K, flags, stream);
+}
+
+extern "C" int qk_gemv_q3k(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N,
+                           int64_t K, const float *residual, float *y, unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q3_K, false, q8_args(w, codes, scales, residual, y), M, N, K, flags, stream);
+}
+
+extern "C" int qk_gemv_q2k_f32(const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                               const float *residual, float *y, int8_t *codes_out, void *scales_out,
+                               unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q2_K, true, f32_args(w, x, ldx, residual, y, codes_out, scales_out), M, N, K, flags,
+                stream);
+}
+
+extern "C" int qk_gemv_q3k_f32(const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                               const float *residual, float *y, int8_t *codes_out, void *scales_out,
+                               unsigned flags, void *stream)
+{
+    return gemv(QK_TYPE_Q3_K, true, f32_args(w, x, ldx, residual, y, codes_out, scales_out), M, N, K, flags,
                 stream);
 }
 

@@ -131,6 +131,70 @@ __global__ void __launch_bounds__(kThreads) repack_q80_kernel(const uint8_t *__r
     *reinterpret_cast<uint16_t *>(dst + N * (int64_t)B * 32 + i * 2) = blk[0];
 }
 
+// Q2_K (84-byte blocks, 4-byte aligned) and Q3_K (110-byte blocks, 2-byte aligned): one thread per
+// superblock, staged through registers; codes in the lane order of the step, scale records in lane
+// order (Q3_K: the 6-bit scales unpacked to int8 minus 32), then the per-type planes
+__device__ __forceinline__ void q23_codes(const uint8_t *qs, int64_t n, int b, int B, uint8_t *dst)
+{
+    const int s = b >> 3;
+    uint8_t *step = dst + n * (int64_t)B * 64 + 512 * s;
+    for (int p = 0; p < 4; p++) {
+        const int hn = p >> 1, e = p & 1, u = 4 * (b - 8 * s) + p;
+        __align__(16) uint8_t c[16];
+        for (int k = 0; k < 16; k++) c[k] = qs[32 * hn + 16 * e + k];
+        copy16(step + 16 * u, c);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) repack_q2k_kernel(const uint8_t *__restrict__ src, int64_t N, int B,
+                                                              uint8_t *__restrict__ dst)
+{
+    const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (i >= N * B) return;
+    const int64_t n = i / B;
+    const int b = (int)(i - n * B);
+    __align__(16) uint32_t blk[21];
+    const uint32_t *s32 = reinterpret_cast<const uint32_t *>(src + i * 84);
+    for (int k = 0; k < 21; k++) blk[k] = s32[k];
+    const uint8_t *bb = reinterpret_cast<const uint8_t *>(blk);
+    const int64_t NB = N * (int64_t)B;
+    q23_codes(bb + 16, n, b, B, dst);
+    __align__(16) uint8_t sc[16];
+    for (int p = 0; p < 4; p++)
+        for (int t = 0; t < 4; t++) sc[4 * p + t] = bb[8 * (p >> 1) + 2 * t + (p & 1)];
+    copy16(dst + NB * 64 + i * 16, sc);
+    *reinterpret_cast<uint32_t *>(dst + NB * 80 + i * 4) = blk[20];
+}
+
+__device__ __forceinline__ int q3k_scale(const uint8_t *sc12, int s)
+{
+    const int lo = s < 8 ? (sc12[s] & 15) : (sc12[s - 8] >> 4);
+    const int hi = (sc12[8 + (s & 3)] >> (2 * (s >> 2))) & 3;
+    return (lo | (hi << 4)) - 32;
+}
+
+__global__ void __launch_bounds__(kThreads) repack_q3k_kernel(const uint8_t *__restrict__ src, int64_t N, int B,
+                                                              uint8_t *__restrict__ dst)
+{
+    const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (i >= N * B) return;
+    const int64_t n = i / B;
+    const int b = (int)(i - n * B);
+    __align__(16) uint16_t blk[56];
+    const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src + i * 110);
+    for (int k = 0; k < 55; k++) blk[k] = s16[k];
+    const uint8_t *bb = reinterpret_cast<const uint8_t *>(blk);
+    const int64_t NB = N * (int64_t)B;
+    q23_codes(bb + 32, n, b, B, dst);
+    copy16(dst + NB * 64 + i * 32, bb);
+    copy16(dst + NB * 64 + i * 32 + 16, bb + 16);
+    __align__(16) uint8_t sc[16];
+    for (int p = 0; p < 4; p++)
+        for (int t = 0; t < 4; t++) sc[4 * p + t] = (uint8_t)(int8_t)q3k_scale(bb + 96, 8 * (p >> 1) + 2 * t + (p & 1));
+    copy16(dst + NB * 96 + i * 16, sc);
+    *reinterpret_cast<uint16_t *>(dst + NB * 112 + i * 2) = blk[54];
+}
+
 __global__ void __launch_bounds__(kThreads) repack_q6k_kernel(const uint8_t *__restrict__ src, int64_t N, int B,
                                                               uint8_t *__restrict__ dst)
 {
@@ -163,24 +227,24 @@ __global__ void __launch_bounds__(kThreads) repack_q6k_kernel(const uint8_t *__r
 extern "C" int qk_repacked_bytes(int qtype, int64_t N, int64_t K, size_t *bytes)
 {
     if (!bytes) return QK_E_NULL;
-    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K && qtype != QK_TYPE_Q5_K && qtype != QK_TYPE_Q8_0)
-        return QK_E_TYPE;
+    if (qtype < QK_TYPE_Q4_K || qtype > QK_TYPE_Q3_K) return QK_E_TYPE;
     if (N < 1 || K < 256 || K % 256 != 0) return QK_E_SHAPE;
-    const size_t per256 = qtype == QK_TYPE_Q4_K ? 144 : qtype == QK_TYPE_Q5_K ? 176 : qtype == QK_TYPE_Q8_0 ? 272 : 210;
+    static const size_t per[7] = {0, 144, 210, 176, 272, 84, 114};     // device bytes per 256 weights
+    const size_t per256 = per[qtype];
     *bytes = (size_t)N * (size_t)(K / 256) * per256;
     return QK_OK;
 }
 
 extern "C" int qk_repack(int qtype, const void *gguf, int64_t N, int64_t K, void *dst, void *stream)
 {
-    if (qtype != QK_TYPE_Q4_K && qtype != QK_TYPE_Q6_K && qtype != QK_TYPE_Q5_K && qtype != QK_TYPE_Q8_0)
-        return QK_E_TYPE;
+    if (qtype < QK_TYPE_Q4_K || qtype > QK_TYPE_Q3_K) return QK_E_TYPE;
     if (N < 1 || K < 256 || K % 256 != 0 || K / 256 > (1 << 24)) return QK_E_SHAPE;
     if (!gguf || !dst) return QK_E_NULL;
     if (!qk::aligned(gguf, 16) || !qk::aligned(dst, 16)) return QK_E_ALIGN;
     size_t bytes = 0;
     qk_repacked_bytes(qtype, N, K, &bytes);
-    if (qk::overlaps(gguf, bytes, dst, bytes)) return QK_E_ALIAS;
+    const size_t gguf_bytes = qtype == QK_TYPE_Q3_K ? (size_t)N * (size_t)(K / 256) * 110 : bytes;
+    if (qk::overlaps(gguf, gguf_bytes, dst, bytes)) return QK_E_ALIAS;
     const int B = (int)(K / (qtype == QK_TYPE_Q8_0 ? 32 : 256));     // repack units per row
     const int64_t nsb = N * B;
     const int64_t grid = (nsb + kThreads - 1) / kThreads;
@@ -188,6 +252,8 @@ extern "C" int qk_repack(int qtype, const void *gguf, int64_t N, int64_t K, void
     auto kern = qtype == QK_TYPE_Q4_K   ? repack_q4k_kernel
                 : qtype == QK_TYPE_Q5_K ? repack_q5k_kernel
                 : qtype == QK_TYPE_Q8_0 ? repack_q80_kernel
+                : qtype == QK_TYPE_Q2_K ? repack_q2k_kernel
+                : qtype == QK_TYPE_Q3_K ? repack_q3k_kernel
                                         : repack_q6k_kernel;
     return qk::launch(kern, dim3((unsigned)grid), dim3(kThreads), 0, (cudaStream_t)stream, false,
                       static_cast<const uint8_t *>(gguf), N, B, static_cast<uint8_t *>(dst));

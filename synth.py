@@ -12,6 +12,8 @@ Distributions (the benchmark definition of the workload):
       uniform random bytes are exactly uniform random scales and mins.
   Q5_K superblock (176 B): d and dmin as for Q4_K, then uniform random bytes
       for the packed scales and mins, the 32 bytes of fifth bits and the codes.
+  Q2_K superblock (84 B) and Q3_K superblock (110 B): uniform random bytes
+      except f16 d ~ U(1e-3, 1e-2) (and Q2_K dmin ~ U(0, 5e-3)).
   Q8_0 block (34 B): f16 d ~ U(1e-3, 1e-2), 32 int8 codes uniform on [-127, 127].
   Q6_K superblock (210 B): 128 B of low-4-bit codes and 64 B of high-2-bit
       codes (uniform random bits), 16 int8 scales ~ U[-32, 31], f16 d ~
@@ -89,7 +91,34 @@ def q80_weights(N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
     return blk.reshape(-1)
 
 
+def q2k_weights(N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
+    """GGUF Q2_K bytes [N][K/256][84]: uniform random scale/min nibbles and codes, f16 d ~ U(1e-3, 1e-2),
+    f16 dmin ~ U(0, 5e-3)."""
+    assert K % QK == 0
+    nb = N * (K // QK)
+    rng = _rng(seed, "q2k:" + tag)
+    blk = rng.integers(0, 256, size=(nb, 84), dtype=np.uint8)
+    blk[:, 80:82] = _f16_bytes(rng.uniform(1e-3, 1e-2, size=nb))
+    blk[:, 82:84] = _f16_bytes(rng.uniform(0.0, 5e-3, size=nb))
+    return blk.reshape(-1)
+
+
+def q3k_weights(N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
+    """GGUF Q3_K bytes [N][K/256][110]: uniform random hmask, codes and packed 6-bit scales,
+    f16 d ~ U(1e-3, 1e-2)."""
+    assert K % QK == 0
+    nb = N * (K // QK)
+    rng = _rng(seed, "q3k:" + tag)
+    blk = rng.integers(0, 256, size=(nb, 110), dtype=np.uint8)
+    blk[:, 108:110] = _f16_bytes(rng.uniform(1e-3, 1e-2, size=nb))
+    return blk.reshape(-1)
+
+
 def weights(qtype: str, N: int, K: int, seed: int = 0, tag: str = "w") -> np.ndarray:
+    if qtype == "q2k":
+        return q2k_weights(N, K, seed, tag)
+    if qtype == "q3k":
+        return q3k_weights(N, K, seed, tag)
     if qtype == "q80":
         return q80_weights(N, K, seed, tag)
     if qtype == "q4k":

@@ -54,6 +54,8 @@ def test_sizes(L):
     assert qk.repacked_bytes(qk.Q6_K, 128256, 4096) == 430940160
     assert qk.repacked_bytes(qk.Q5_K, 4096, 4096) == 4096 * 16 * 176
     assert qk.repacked_bytes(qk.Q8_0, 4096, 4096) == 4096 * 128 * 34
+    assert qk.repacked_bytes(qk.Q2_K, 4096, 4096) == 4096 * 16 * 84
+    assert qk.repacked_bytes(qk.Q3_K, 4096, 4096) == 4096 * 16 * 114
     with pytest.raises(qk.QKError):
         qk.repacked_bytes(qk.Q4_K, 10, 100)
     with pytest.raises(qk.QKError):
@@ -65,7 +67,8 @@ def call_gemv(L, fn, w=P, codes=P + 0x10000000, scales=P + 0x20000000, M=1, N=64
     return getattr(L, fn)(w, codes, scales, M, N, K, r, y, 0, None)
 
 
-@pytest.mark.parametrize("fn", ["qk_gemv_q4k", "qk_gemv_q5k", "qk_gemv_q6k", "qk_gemv_q8_0"])
+@pytest.mark.parametrize("fn", ["qk_gemv_q4k", "qk_gemv_q5k", "qk_gemv_q6k", "qk_gemv_q8_0", "qk_gemv_q2k",
+                                "qk_gemv_q3k"])
 def test_gemv_rejects(L, fn):
     assert call_gemv(L, fn, w=None) == E_NULL
     assert call_gemv(L, fn, y=None) == E_NULL
@@ -74,7 +77,8 @@ def test_gemv_rejects(L, fn):
     assert call_gemv(L, fn, M=0) == E_SHAPE
     assert call_gemv(L, fn, M=9) == E_SHAPE
     assert call_gemv(L, fn, N=0) == E_SHAPE
-    kmax = {"qk_gemv_q4k": 40, "qk_gemv_q5k": 32, "qk_gemv_q6k": 20, "qk_gemv_q8_0": 32}[fn]   # 256s at M = 8
+    kmax = {"qk_gemv_q4k": 40, "qk_gemv_q5k": 32, "qk_gemv_q6k": 20, "qk_gemv_q8_0": 32, "qk_gemv_q2k": 40,
+            "qk_gemv_q3k": 40}[fn]                                  # 256-value units at M = 8
     assert call_gemv(L, fn, M=8, K=256 * (kmax + 1)) == E_SHAPE     # activation too large
     assert call_gemv(L, fn, M=8, K=256 * kmax, y=None) == E_NULL     # at the limit
     assert call_gemv(L, fn, w=P + 8) == E_ALIGN
@@ -84,7 +88,8 @@ def test_gemv_rejects(L, fn):
     assert call_gemv(L, fn, r=P + 0x30000000 + 4) == E_ALIAS       # residual partially overlaps y
 
 
-@pytest.mark.parametrize("fn", ["qk_gemv_q4k_f32", "qk_gemv_q5k_f32", "qk_gemv_q6k_f32", "qk_gemv_q8_0_f32"])
+@pytest.mark.parametrize("fn", ["qk_gemv_q4k_f32", "qk_gemv_q5k_f32", "qk_gemv_q6k_f32", "qk_gemv_q8_0_f32",
+                                "qk_gemv_q2k_f32", "qk_gemv_q3k_f32"])
 def test_gemv_f32_rejects(L, fn):
     f = getattr(L, fn)
     w, x, y, c, s = P, P + 0x10000000, P + 0x30000000, P + 0x40000000, P + 0x50000000
@@ -113,7 +118,8 @@ def test_quantize_rejects(L):
 
 def test_repack_rejects(L):
     f = L.qk_repack
-    assert f(5, P, 4, 256, P + 0x10000000, None) == E_TYPE
+    assert f(7, P, 4, 256, P + 0x10000000, None) == E_TYPE
+    assert f(0, P, 4, 256, P + 0x10000000, None) == E_TYPE
     assert f(qk.Q4_K, P, 4, 300, P + 0x10000000, None) == E_SHAPE
     assert f(qk.Q4_K, None, 4, 256, P + 0x10000000, None) == E_NULL
     assert f(qk.Q6_K, P + 2, 4, 256, P + 0x10000000, None) == E_ALIGN

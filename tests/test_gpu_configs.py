@@ -26,7 +26,7 @@ def sample_rows(N, n=24, seed=0):
 
 @pytest.mark.parametrize("cfg_id,front_end", [(0, "fused"), (1, "fused"), (2, "fused"), (3, "fused"), (1, "unfused"),
                                               (3, "unfused"), (1, "auto"), (4, "auto"), (5, "auto"), (7, "auto"),
-                                              (8, "auto")])
+                                              (8, "auto"), (9, "auto"), (10, "auto")])
 def test_config_full_size(cfg_id, front_end):
     import bench
     wl = bench.Workload(cfg_id, seed=0, copies=1)
@@ -50,7 +50,8 @@ def test_config_full_size(cfg_id, front_end):
         y = wl.y[name].cpu().numpy()
         c, d = q8[s]
         r = wl.host_r.get(name)
-        qt = {"q4k": oracle.Q4_K, "q5k": oracle.Q5_K, "q6k": oracle.Q6_K, "q80": oracle.Q8_0}[q]
+        qt = {"q4k": oracle.Q4_K, "q5k": oracle.Q5_K, "q6k": oracle.Q6_K, "q80": oracle.Q8_0,
+              "q2k": oracle.Q2_K, "q3k": oracle.Q3_K}[q]
         for n in sample_rows(N, seed=N):
             y_ref, ab = oracle.gemm(qt, wl.host_w[name], N, K, c, d, residual=r, rows=(n, n + 1))
             tol = 1e-4 * ab[:, 0] + (0 if r is None else 2.0 ** -22 * np.abs(r[:, n]))

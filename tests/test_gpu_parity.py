@@ -17,7 +17,8 @@ import synth
 pytestmark = pytest.mark.gpu
 
 qk = None
-QT = {"q4k": (1, oracle.Q4_K), "q6k": (2, oracle.Q6_K), "q5k": (3, oracle.Q5_K), "q80": (4, oracle.Q8_0)}
+QT = {"q4k": (1, oracle.Q4_K), "q6k": (2, oracle.Q6_K), "q5k": (3, oracle.Q5_K), "q80": (4, oracle.Q8_0),
+      "q2k": (5, oracle.Q2_K), "q3k": (6, oracle.Q3_K)}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -108,7 +109,7 @@ def test_quantize_saturates_large_blocks():
 
 # -------------------------------------------------------------------- repack
 
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 @pytest.mark.parametrize("N,K", [(1, 256), (3, 2304), (5, 4096), (2, 256 * 17), (9, 256 * 8)])
 def test_repack_bitexact(qt, N, K):
     w, wr = weights(qt, N, K, seed=N * 7 + K)
@@ -118,10 +119,11 @@ def test_repack_bitexact(qt, N, K):
 # ---------------------------------------------------------------------- GEMV
 
 def gemv(qt, *a, **kw):
-    return {"q4k": qk.gemv_q4k, "q5k": qk.gemv_q5k, "q6k": qk.gemv_q6k, "q80": qk.gemv_q8_0}[qt](*a, **kw)
+    return {"q4k": qk.gemv_q4k, "q5k": qk.gemv_q5k, "q6k": qk.gemv_q6k, "q80": qk.gemv_q8_0,
+            "q2k": qk.gemv_q2k, "q3k": qk.gemv_q3k}[qt](*a, **kw)
 
 
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("N,K", [(1, 256), (37, 2304), (300, 4096), (130, 256 * 11)])
 def test_gemv_parity(qt, M, N, K):
@@ -137,7 +139,7 @@ def test_gemv_parity(qt, M, N, K):
 # Row counts that leave a partial last round of row pairs on the persistent grid
 # (152 SMs x 16 warps: a pair per warp per round), with 2 to 16 superblock steps
 # per pair and a ragged last pair.  Every output row is checked.
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 @pytest.mark.parametrize("K,frac", [(4096, 8), (8192, 8), (32768, 10), (32768, 20)])
 @pytest.mark.parametrize("front", ["q8", "f32"])
 def test_gemv_partial_last_round(qt, K, frac, front):
@@ -158,7 +160,7 @@ def test_gemv_partial_last_round(qt, K, frac, front):
     check(y, y_ref, ab, what=f"{qt} {front} M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 @pytest.mark.parametrize("mode", ["separate", "inplace", "pdl"])
 def test_gemv_residual(qt, mode):
     M, N, K = 4, 515, 4096
@@ -177,7 +179,7 @@ def test_gemv_residual(qt, mode):
     check(y.cpu().numpy(), y_ref, ab, r, what=f"{qt} residual {mode}")
 
 
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 def test_gemv_edges(qt):
     # zero activation gives the residual exactly; one-hot activation gives a scaled column
     N, K = 33, 512
@@ -195,10 +197,10 @@ def test_gemv_edges(qt):
     check(y, y_ref, ab, what="one-hot")
 
 
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 def test_gemv_max_activation(qt):
     M, N = 8, 40
-    K = {"q4k": 10240, "q5k": 8192, "q6k": 5120, "q80": 8192}[qt]   # M*K at the documented limit
+    K = {"q4k": 10240, "q5k": 8192, "q6k": 5120, "q80": 8192, "q2k": 10240, "q3k": 10240}[qt]   # at the limit
     w, wr = weights(qt, N, K, seed=31)
     x = synth.activations(M, K, seed=32)
     codes, scales = q8(x)
@@ -208,7 +210,7 @@ def test_gemv_max_activation(qt):
     check(y, y_ref, ab, what="max M*K")
 
 
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 def test_gemv_deterministic_and_guard_band(qt):
     M, N, K = 3, 1000, 4096
     w, wr = weights(qt, N, K, seed=41)
@@ -226,10 +228,10 @@ def test_gemv_deterministic_and_guard_band(qt):
 
 def gemv_f32(qt, *a, **kw):
     return {"q4k": qk.gemv_q4k_f32, "q5k": qk.gemv_q5k_f32, "q6k": qk.gemv_q6k_f32,
-            "q80": qk.gemv_q8_0_f32}[qt](*a, **kw)
+            "q80": qk.gemv_q8_0_f32, "q2k": qk.gemv_q2k_f32, "q3k": qk.gemv_q3k_f32}[qt](*a, **kw)
 
 
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("N,K", [(1, 256), (37, 2304), (300, 4096), (130, 256 * 11)])
 def test_gemv_f32_parity_and_codes(qt, M, N, K):
@@ -246,7 +248,7 @@ def test_gemv_f32_parity_and_codes(qt, M, N, K):
     check(y, y_ref, ab, what=f"{qt} f32 M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 @pytest.mark.parametrize("mode", ["separate", "inplace", "pdl", "strided"])
 def test_gemv_f32_residual(qt, mode):
     M, N, K = 2, 515, 4096
@@ -270,7 +272,7 @@ def test_gemv_f32_residual(qt, mode):
     check(y.cpu().numpy(), y_ref, ab, r, what=f"{qt} f32 residual {mode}")
 
 
-@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80"])
+@pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 def test_gemv_f32_matches_q8_path_bitwise(qt):
     # same codes, same kernel body: the two front ends give identical outputs
     M, N, K = 2, 700, 4096
