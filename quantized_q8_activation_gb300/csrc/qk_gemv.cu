@@ -744,7 +744,10 @@ struct Q6Ops {
 // (four codes each: quarters t = 0..3 at bits 2t) and meets the same activation chunks as the Q6_K
 // lanes, so the Q6_K activation staging (d_a and -32 d_a sum(q_a) per 16 values) serves both:
 //   Q2_K  w = d sc q - dmin m:       acc += d sc (d_a dot) + dmin m (-32 d_a sum(q_a)) / 32
-//   Q3_K  w = d S (q3 - 4), q3 = q + 4 h:  acc += d S (d_a dot(q3) + (-32 d_a sum(q_a)) / 8)
+//   Q3_K  w = d S (q + 4 h - 4):     acc += d S (d_a (dot(q) + 4 dot(h)) + (-32 d_a sum(q_a)) / 8)
+// The codes of quarter t are dotted in place (bits 2t, 2t+1 of each byte: 4^t q, at most 192, an
+// unsigned byte) and the hmask bits likewise (2^(4n+t) h); the powers of two are undone in the
+// binary32 factors, exactly.
 
 template <int QT>
 struct Q23Ops {
@@ -801,11 +804,12 @@ struct Q23Ops {
             const float d = f16lo(dr[r]);
 #pragma unroll
             for (int t = 0; t < 4; t++) {
+                const float inv4t = 1.0f / (float)(1 << (2 * t));                 // 4^-t, exact
                 if (Q3) {
                     dsl[r][t] = d * (float)(int)(int8_t)(scw >> (8 * t));
                     dml[r][t] = 0.0f;
                 } else {
-                    dsl[r][t] = d * (float)((scw >> (8 * t)) & 15u);
+                    dsl[r][t] = d * (float)((scw >> (8 * t)) & 15u) * inv4t;
                     dml[r][t] = f16hi(dr[r]) * (float)((scw >> (8 * t + 4)) & 15u) * 0.03125f;   // / 32, exact
                 }
             }
@@ -824,15 +828,21 @@ struct Q23Ops {
                     const uint32_t xw[4] = {cq[r].x, cq[r].y, cq[r].z, cq[r].w};
                     const uint32_t hw[4] = {hq[r].x, hq[r].y, hq[r].z, hq[r].w};
                     const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-                    int dot = 0;
+                    const uint32_t cmask = 0x03030303u << (2 * t), hmask = 0x01010101u << (hsh + t);
+                    int dot = 0, doth = 0;
 #pragma unroll
                     for (int k = 0; k < 4; k++) {
-                        uint32_t c = (xw[k] >> (2 * t)) & 0x03030303u;
-                        if (Q3) c |= ((hw[k] >> (hsh + t)) & 0x01010101u) << 2;
-                        dot = qk::dp4a_ss(c, aw[k], dot);
+                        dot = qk::dp4a_us(xw[k] & cmask, aw[k], dot);                 // 4^t q
+                        if (Q3) doth = qk::dp4a_us(hw[k] & hmask, aw[k], doth);       // 2^(4n+t) h
                     }
-                    if (Q3) acc[r][m] = fmaf(dsl[r][t], fmaf(dc.x, (float)dot, dc.y * 0.125f), acc[r][m]);
-                    else acc[r][m] = fmaf(dsl[r][t], dc.x * (float)dot, fmaf(dml[r][t], dc.y, acc[r][m]));
+                    if (Q3) {
+                        // d_a (q . a + 4 h . a) with q . a = dot / 4^t and h . a = doth / 2^(4n+t)
+                        const float qa = fmaf((float)doth, __uint_as_float((uint32_t)(129 - hsh - t) << 23),
+                                              (float)dot * (1.0f / (float)(1 << (2 * t))));
+                        acc[r][m] = fmaf(dsl[r][t], fmaf(dc.x, qa, dc.y * 0.125f), acc[r][m]);
+                    } else {
+                        acc[r][m] = fmaf(dsl[r][t], dc.x * (float)dot, fmaf(dml[r][t], dc.y, acc[r][m]));
+                    }
                 }
             }
         }
