@@ -143,11 +143,13 @@ __device__ void stage_act_q4k(const int8_t *__restrict__ codes, const __half2 *_
     }
 }
 
-// Q6_K side data per (m, 16-value chunk): {d_a, -32 * d_a * sum(q_a)}, the
-// activation scale and the offset term of the weight codes' -32 bias (exact).
+// Q6_K side data per (m, 16-value chunk): d_a and -32 * d_a * sum(q_a), the
+// activation scale and the offset term of the weight codes' -32 bias (exact),
+// kept as two float planes D [M][K/16] and Bias [M][K/16] (Bias after D).
 // Within each 128-chunk step the entries are stored in the order the lanes
 // read them: chunk 16j + 8h + e + 2t (lane 4j+2h+e, quarter t) at 4*lane + t,
-// so a lane fetches its four entries with two conflict-free 16-byte loads.
+// so a lane fetches its four scales and its four biases with one 16-byte load
+// each, 8 lanes covering 128 consecutive bytes (no bank conflict).
 __device__ __forceinline__ int q6_side_pos(int c)
 {
     const int lo = c & 127;
@@ -159,13 +161,26 @@ __device__ void stage_act_q6k(const int8_t *__restrict__ codes, const __half2 *_
                               uint8_t *s_codes, float2 *s_c16)
 {
     const int nchunk = K >> 4;
+    float *sd = reinterpret_cast<float *>(s_c16), *sb = sd + M * nchunk;
     for (int i = threadIdx.x; i < M * nchunk; i += NT) {
         const int m = i / nchunk, c = i - m * nchunk;
         const uint4 v = *reinterpret_cast<const uint4 *>(codes + (size_t)m * K + 16 * c);
         *reinterpret_cast<uint4 *>(s_codes + (size_t)m * K + 16 * swz(c)) = v;
         const float d = __low2float(scales[(size_t)m * (K >> 5) + (c >> 1)]);
-        s_c16[m * nchunk + q6_side_pos(c)] = make_float2(d, -32.0f * d * (float)sum16(v));
+        const int pos = m * nchunk + q6_side_pos(c);
+        sd[pos] = d;
+        sb[pos] = -32.0f * d * (float)sum16(v);
     }
+}
+
+// a lane's four Q6_K side entries of activation row m at step s: d_a and bias of quarters 0..3
+template <int M>
+__device__ __forceinline__ void q6_side4(const float2 *s_c16, int K, int m, int s, int lane, float4 &dq, float4 &bq)
+{
+    const int nc = K >> 4;
+    const float *sd = reinterpret_cast<const float *>(s_c16) + (size_t)m * nc + 128 * s + 4 * lane;
+    dq = *reinterpret_cast<const float4 *>(sd);
+    bq = *reinterpret_cast<const float4 *>(sd + (size_t)M * nc);
 }
 
 // f32 front end: quantize the activation into the same shared-memory image
@@ -217,7 +232,10 @@ __device__ void stage_quant_u(const GemvArgs &a, uint8_t *s_codes, float2 *s_sid
                         s_side[m * nb + b] = make_float2((b & 1) ? da * 0.0625f : da, da * (float)s32);
                     }
                 } else if ((sub & 3) == 0) {
-                    s_side[m * (K >> 4) + q6_side_pos(c)] = make_float2(da, -32.0f * da * (float)s16);
+                    float *sd = reinterpret_cast<float *>(s_side);
+                    const int pos = m * (K >> 4) + q6_side_pos(c);
+                    sd[pos] = da;
+                    sd[M * (K >> 4) + pos] = -32.0f * da * (float)s16;
                 }
                 if (out) {
                     *reinterpret_cast<uint32_t *>(a.codes_out + (size_t)m * K + 4 * k4) = packed[u];
@@ -651,17 +669,16 @@ struct Q6Ops {
             for (int t = 0; t < 4; t++) dsc[r][t] = d[r] * (float)(int)(int8_t)(scw >> (8 * t));
         }
         const uint8_t *abase = s_codes + 2048 * s;
-        const float4 *cbase = reinterpret_cast<const float4 *>(s_c16 + 128 * s + 4 * lane);
-        const int nc = K >> 4;
         if (M <= 2) {
             // u = low4 + 16*high2: each part is dotted with its bits masked in place and the power-of-two
             // factor restored on the integer sums (2 logic ops + 2 dp4a per word, no shifts)
 #pragma unroll
             for (int m = 0; m < M; m++) {
                 const uint8_t *ar = abase + (size_t)m * K;
-                const float4 c01 = cbase[(size_t)m * nc / 2], c23 = cbase[(size_t)m * nc / 2 + 1];
-                const float2 dc[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w),
-                                      make_float2(c23.x, c23.y), make_float2(c23.z, c23.w)};
+                float4 dq, bq;
+                q6_side4<M>(s_c16, K, m, s, lane, dq, bq);
+                const float2 dc[4] = {make_float2(dq.x, bq.x), make_float2(dq.y, bq.y), make_float2(dq.z, bq.z),
+                                      make_float2(dq.w, bq.w)};
                 uint4 av[4];
 #pragma unroll
                 for (int t = 0; t < 4; t++) av[t] = lds16(ar + lc.qoff[t]);
@@ -712,9 +729,10 @@ struct Q6Ops {
 #pragma unroll
             for (int m = 0; m < M; m++) {
                 const uint8_t *ar = abase + (size_t)m * K;
-                const float4 c01 = cbase[(size_t)m * nc / 2], c23 = cbase[(size_t)m * nc / 2 + 1];
-                const float2 dc[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w),
-                                      make_float2(c23.x, c23.y), make_float2(c23.z, c23.w)};
+                float4 dq, bq;
+                q6_side4<M>(s_c16, K, m, s, lane, dq, bq);
+                const float2 dc[4] = {make_float2(dq.x, bq.x), make_float2(dq.y, bq.y), make_float2(dq.z, bq.z),
+                                      make_float2(dq.w, bq.w)};
 #pragma unroll
                 for (int t = 0; t < 4; t++) {
                     const uint4 av = lds16(ar + lc.qoff[t]);
@@ -815,14 +833,16 @@ struct Q23Ops {
             }
         }
         const uint8_t *abase = s_codes + 2048 * s;
-        const float2 *cb = s_c16 + 128 * s + 4 * lane;
-        const int nc = K >> 4;
 #pragma unroll
         for (int m = 0; m < M; m++) {
+            float4 dq, bq;
+            q6_side4<M>(s_c16, K, m, s, lane, dq, bq);
+            const float2 dcs[4] = {make_float2(dq.x, bq.x), make_float2(dq.y, bq.y), make_float2(dq.z, bq.z),
+                                   make_float2(dq.w, bq.w)};
 #pragma unroll
             for (int t = 0; t < 4; t++) {
                 const uint4 av = lds16(abase + (size_t)m * K + lc.qoff[t]);
-                const float2 dc = cb[(size_t)m * nc + t];
+                const float2 dc = dcs[t];
 #pragma unroll
                 for (int r = 0; r < P; r++) {
                     const uint32_t xw[4] = {cq[r].x, cq[r].y, cq[r].z, cq[r].w};
