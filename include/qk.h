@@ -356,26 +356,32 @@ int qk_gemv_q3k_f32(const void *w, const float *x, int64_t ldx,
  * Prefill contraction of many activation rows with a Q4_K weight: the
  * quantized weight bytes are streamed to the SMs in their Q4_K form and
  * expanded tile by tile right before the tensor-core MMAs (minfer "15 . The
- * CUDA backend" sec. 2.3 and 3.2.6).  Both operands enter f16 MMAs as pairs:
- * the activation d_a * q_a exactly (A_hi + A_lo), the weight
- * d*sc*q - dmin*m to about 2^-22 relative (W_hi + W_lo); the binary32 result
- * is within 1e-4 * sum_k |w * xhat| of the exact contraction (in practice
- * ~1e-7).
+ * CUDA backend" sec. 2.3 and 3.2.6).  The contraction is regrouped as
+ *   y = sum_b d_b * (sum_{k in b} (d_a q_a) * (sc q)) - sum_j dmin m_j * S_j
+ * (b: superblocks, j: 32-value sub-blocks, S_j = d_a * sum q_a): the
+ * activation enters f16 MMAs exactly as A_hi + A_lo, the integer sc*q (< 1024)
+ * exactly as one f16, each superblock accumulates on its own and is scaled by
+ * d_b in binary32, and the min term is a contraction over the K/32
+ * sub-blocks of S (split to 2^-22) with dmin*m (split exactly).  The binary32
+ * result is within 1e-4 * sum_k |w * xhat| of the exact contraction (in
+ * practice ~1e-7).
  *
  * w, codes, scales, residual, y: as for qk_gemv_q4k.
  * Ranges: M >= 1, N >= 1, K % 256 == 0, K >= 256, ceil(M/128) <= 65535 and
  * ceil(N/256) <= 65535.  (M == 0 is a no-op.)
- * Value limits: max |x| <= 65000 per 32-value block (the f16 operand
- * d_a * q_a must not overflow) and |w| < 255 for every dequantized weight
- * (the weight operand is scaled by 256); LLM layers are far inside both.
+ * Value limits: max |x| <= 32000 per 32-value block (the f16 operands
+ * d_a * q_a and S_j / 16 must not overflow) and dmin * m < 63 for every
+ * sub-block (the operand 1024 * dmin * m is an f16); LLM layers are far
+ * inside both.
  * workspace: device scratch of at least qk_mmq_workspace_bytes(M, N, K)
  *   bytes, 256-byte aligned, not overlapping any other argument.  The call
  *   writes it (the q8_1 activation expanded once per 128-row tile into the
- *   tensor-core operand layout) before reading it; nothing needs to be
- *   initialised.  Its contents are consumed by kernels of this call that run
- *   after the call returns, so the workspace must not be reused by work that
- *   is not ordered after this call on `stream`.  Size: ceil(M/128) * K * 512
- *   bytes (M = 2048, K = 18944: 155,189,248 bytes).
+ *   tensor-core operand layout, then its sub-block sums S) before reading it;
+ *   nothing needs to be initialised.  Its contents are consumed by kernels of
+ *   this call that run after the call returns, so the workspace must not be
+ *   reused by work that is not ordered after this call on `stream`.  Size:
+ *   ceil(M/128) * (K * 512 + ceil(K/512) * 8192) bytes (M = 2048,
+ *   K = 18944: 160,038,912 bytes).
  * Returns QK_E_WORKSPACE if workspace_bytes is too small.
  */
 int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
@@ -393,10 +399,12 @@ int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales,
  * MMQ, and in cajeta.dev "xpu walkthrough" step 3 (prefill) the Q6_K value
  * and down projections of 16 layers run on their own tiles.  Each weight
  * enters the tensor cores as
- * 256 * d * sc * (q - 32) = W_hi + W_lo, the same split as for Q4_K; the
- * bound, the value limits (|x| <= 65000 per block, |w| < 255), the
- * workspace (same size, qk_mmq_workspace_bytes) and every other argument
- * rule are those of qk_mmq_q4k.
+ * 256 * d * sc * (q - 32) = W_hi + W_lo (to about 2^-22 relative; sc * (q - 32)
+ * reaches 4096 and is not exact in one f16), against A_hi + A_lo; the bound,
+ * the workspace (same size, qk_mmq_workspace_bytes; the sums S are not
+ * used) and every other argument rule are those of qk_mmq_q4k.  Value
+ * limits: max |x| <= 65000 per 32-value block and |w| < 255 for every
+ * dequantized weight (the weight operand is scaled by 256).
  */
 int qk_mmq_q6k(const void *w, const int8_t *codes, const void *scales,
                int64_t M, int64_t N, int64_t K,
@@ -414,7 +422,7 @@ int qk_mmq_q6k(const void *w, const int8_t *codes, const void *scales,
  * frees nothing.
  *  - Problems with qk_mmq_workspace_bytes(M, N, K) > QK_MMQ_STATIC_WS_BYTES
  *    return QK_E_WORKSPACE (nothing launched).  Example: M = 2048, K = 3584
- *    needs 29,360,128 bytes and fits; K = 18944 does not.
+ *    needs 30,277,632 bytes and fits; K = 18944 does not.
  *  - The array needs no initialisation (each call writes what it reads).
  *  - All calls on a device share the array: calls that may run concurrently
  *    (other streams, unordered host threads) race on it.

@@ -5,17 +5,24 @@
 // Method (minfer "15 . The CUDA backend" sec. 2.3 / 3.2.6: quantized weight
 // bytes go straight to the tensor cores; the activation is quantized to q8_1
 // once per matmul input).  This part runs integer MMA far below its f16 rate,
-// so both operands enter kind::f16 MMAs as pairs of f16 values:
+// so the operands enter kind::f16 MMAs as f16 values, split where one f16 is
+// not exact:
 //   A[m][k] = d_a * q_a = A_hi + A_lo   exactly (d_a has 11 significant bits
-//             and q_a 7, so the product needs 18 <= 2 x 11 bits);
-//   W[n][k] = 256 * (d_b sc_j q_w - dmin_b m_j) = W_hi + W_lo, the Q4_K weight
-//             (Q6_K: 256 * d_b sc_j (q_w - 32), the same form with the min
-//             term 32 d_b sc_j) scaled by 2^8 (so that W_lo stays in the
-//             normal f16 range for the weights of LLM layers), split to
-//             2^-21 relative;
-//   Y = A_hi W_hi + A_hi W_lo + A_lo W_hi   (A_lo W_lo is below 2^-21 of each
-//             product and dropped), accumulated in binary32 over all of K in
-//             tensor memory;  y = Y / 256 (+ R).
+//             and q_a 7, so the product needs 18 <= 2 x 11 bits).
+//   Q4_K (mmq_q4k_kernel): the contraction is regrouped by superblock b and
+//             sub-block j as  y = sum_b d_b (A . sc q)_b - sum_j dmin m_j S_j
+//             (S_j = d_a sum q_a of the sub-block): sc q < 1024 is one exact
+//             f16, so a K stage takes two MMAs (A_hi, A_lo) against one weight
+//             tile; each superblock accumulates on its own and the epilogue
+//             folds it into a register tile with d_b; the min term is a short
+//             contraction of the sums S (split to 2^-22) with dmin m (split
+//             exactly).
+//   Q6_K (mmq_kernel): W[n][k] = 256 * d_b sc_j (q_w - 32) = W_hi + W_lo to
+//             2^-21 relative (sc (q - 32) reaches 4096, not exact in one f16;
+//             scaled by 2^8 so that W_lo stays a normal f16 for the weights of
+//             LLM layers); Y = A_hi W_hi + A_hi W_lo + A_lo W_hi (A_lo W_lo is
+//             below 2^-21 of each product and dropped), accumulated in binary32
+//             over all of K in tensor memory; y = Y / 256 (+ R).
 // The k-quant bytes are dequantized tile by tile in shared memory right before
 // the MMAs that use them; they are read from memory in their quantized form.
 //
@@ -23,30 +30,18 @@
 //  1. mmq_prep_kernel expands the q8_1 activation once per 128-row M-tile into
 //     the caller's workspace, already in the tensor core's shared-memory
 //     layout: per 32-value K stage a 16 KB block (A_hi and A_lo tiles, K-major
-//     SWIZZLE_64B).  Every N-tile then copies these blocks instead of
-//     converting the activation again.
-//  2. mmq_kernel<QT>: a persistent grid, one CTA (24 warps) per SM, each CTA
-//     taking 128 x 256 output tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
-//     (M-tile fastest).  512 TMEM columns hold two accumulators, so one tile
-//     accumulates while the previous one is written out:
-//       warp 0      TMEM allocation; lane 0 issues every MMA and commit
-//       warp 1      lane 0 copies each K stage's 16 KB activation block from the
-//                   workspace into the stage slot with one bulk copy, as soon as
-//                   the MMAs have released the slot
-//       warp 2      lane 0 streams the raw weight bytes with 2D TMA tensor
-//                   copies into a ring.  Q4_K, per superblock: the two 64-byte
-//                   runs of code bytes (256 x 64 B each: first and second
-//                   16-byte halves of its four groups) and the metadata records
-//                   (256 x 16 B).  Q6_K, per half superblock (128 values): its
-//                   32-byte runs of the two ql chunks and of qh (256 x 32 B
-//                   each); per superblock the scale records (256 x 16 B).  The
-//                   Q6_K d plane (2 bytes per superblock) is read by the
-//                   converters themselves, one superblock ahead.
-//       warps 4-7   the epilogue of the previous tile (TMEM lane quadrant =
-//                   warp % 4) while the next one accumulates
-//       warps 8-23  converters: two threads per weight row expand the codes,
-//                   scales (and Q4_K mins) of each K stage into (W_hi, W_lo)
-//                   in the SWIZZLE_64B layout
+//     SWIZZLE_64B), and for Q4_K per pair of superblocks an 8 KB tile of the
+//     sub-block sums (S_hi | S_lo).  Every N-tile then copies these blocks
+//     instead of converting the activation again.
+//  2. the main kernel: a persistent grid, one CTA per SM, each CTA taking
+//     128 x BN output tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
+//     (M-tile fastest).  Warp 0 lane 0 issues every MMA and commit, warp 1
+//     lane 0 copies each stage's activation block from the workspace with one
+//     bulk copy, warp 2 lane 0 streams the raw weight bytes with 2D TMA tensor
+//     copies into a ring (the code runs of a superblock and its per-row
+//     records), epilogue warps read the accumulators, and converter warps
+//     expand each K stage's codes and scales into f16 tiles in the
+//     SWIZZLE_64B layout.  The roles of each kernel are listed above it.
 // Stages are handed over with mbarriers (full: converters and the activation
 // copy's bytes -> MMA; empty: MMA commit -> converters and activation copier;
 // raw: TMA bytes -> converters -> producer; accumulator full / empty: MMA
@@ -90,6 +85,11 @@ constexpr float kWScale = 256.0f, kWUnscale = 1.0f / 256.0f;
 constexpr int ATILE = BM * BK * 2;              // 8 KB: 128 rows x 32 f16 (64 B rows), SWIZZLE_64B K-major
 constexpr int ABLOCK = 2 * ATILE;               // workspace block of one M-tile and K stage: A_hi | A_lo
 constexpr int EPI_LD = 17;                      // epilogue transpose buffer: 32 rows x 16 columns, padded
+// Q4_K split-scale kernel: the sums tile of one min stage, 128 rows x (S_hi 16 | S_lo 16) f16, SWIZZLE_64B
+constexpr int SBLK = BM * 64;
+constexpr float kSScale = 0.0625f;              // S' = S / 16
+constexpr float kMScale = 1024.0f;              // Mw' = 1024 dmin m
+constexpr float kMinUndo = -1.0f / 64.0f;       // -sum S Mw = -(sum S' Mw') / 64
 enum {
     B_FULL = 0,
     B_EMPTY = B_FULL + NST,
@@ -102,26 +102,22 @@ enum {
     B_DONE = B_ACCEMPTY + 2,       // every MMA of the CTA has completed
     NBAR = B_DONE + 1
 };
-// Tile width and shared-memory plan of mmq_kernel<QT, BN>: output tiles of 128 x BN (BN = 256, or
-// 128 where 256-wide tiles leave a costly partial last wave on the SMs), two converter threads per
-// weight row.
+// Tile width and shared-memory plan of mmq_kernel<QT, BN> (QT = Q6_K): output tiles of 128 x BN
+// (BN = 256, or 128 where 256-wide tiles leave a costly partial last wave on the SMs), two converter
+// threads per weight row.
 template <int QT, int BN_>
 struct Plan {
+    static_assert(QT == QK_TYPE_Q6_K, "Q4_K runs on mmq_q4k_kernel");
     static constexpr int BN = BN_;
-    static constexpr bool Q6 = QT == QK_TYPE_Q6_K;
     static constexpr int kConv = 2 * BN, kConvWarps = kConv / 32, kThreads = kConvWarp0 * 32 + kConv;
     static constexpr int WTILE = BN * BK * 2;              // BN rows x 32 f16
     static constexpr int STAGE = 2 * ATILE + 2 * WTILE;    // A_hi | A_lo | W_hi | W_lo
-    // raw unit of the Q4_K ring, one superblock's code bytes: first halves of its 4 groups BN x 64 B |
-    // second halves BN x 64 B
-    static constexpr int RAW_H0 = 0, RAW_H1 = BN * 64, RAW_Q4 = 2 * BN * 64;
-    // raw unit of the Q6_K ring, half a superblock: ql first-chunk run BN x 32 B | ql second-chunk run
-    // BN x 32 B | qh BN x 32 B
-    static constexpr int RAW_QL0 = 0, RAW_QL1 = BN * 32, RAW_QH = 2 * BN * 32, RAW_Q6 = 3 * BN * 32;
-    static constexpr int SBR = BN * 16;                    // per-superblock records (Q4_K metadata, Q6_K scales)
+    // raw unit, half a superblock: ql first-chunk run BN x 32 B | ql second-chunk run BN x 32 B | qh
+    // BN x 32 B
+    static constexpr int RAW_QL0 = 0, RAW_QL1 = BN * 32, RAW_QH = 2 * BN * 32, RAW = 3 * BN * 32;
+    static constexpr int SBR = BN * 16;                    // per-superblock scale records
     static constexpr uint32_t TMEM_COLS = 2 * BN;          // two accumulators: one accumulates while one drains
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
-    static constexpr int RAW = Q6 ? RAW_Q6 : RAW_Q4;
     static constexpr int OFF_RAW = NST * STAGE;
     static constexpr int OFF_SBR = OFF_RAW + NRAW * RAW;
     static constexpr int OFF_EPI = OFF_SBR + NSB * SBR;
@@ -135,6 +131,8 @@ struct Plan {
 
 // byte offset of 16-byte chunk c (< 4) of row r in a SWIZZLE_64B K-major tile (rows of 64 bytes)
 __host__ __device__ constexpr uint32_t sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
+// byte offset of 16-byte chunk c (< 2) of row r in a SWIZZLE_32B tile (rows of 32 bytes)
+__host__ __device__ constexpr uint32_t sw32(int r, int c) { return r * 32 + ((c ^ ((r >> 2) & 1)) << 4); }
 
 __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity) { mbar_wait(bar, parity, &g_qk_errors); }
 
@@ -143,6 +141,7 @@ __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__
 
 struct MmqArgs {
     const uint8_t *wsA;     // workspace: [M-tiles][K/32] A blocks
+    const uint8_t *wsS;     // Q4_K: [M-tiles][ceil(K/512)] sums tiles (after all A blocks)
     const uint16_t *dq;     // Q6_K: the d plane of the repacked weight, binary16 [N][K/256]
     int64_t M, N, K;
     const float *residual;
@@ -211,12 +210,12 @@ __device__ __forceinline__ void sts128(uint8_t *base, uint32_t off, uint32_t x, 
 // block of K stage 8 sb + j; rows past M are written as zeros.
 __global__ void __launch_bounds__(256) mmq_prep_kernel(const int8_t *__restrict__ codes,
                                                        const __half2 *__restrict__ scales, int64_t M, int64_t K,
-                                                       uint8_t *__restrict__ wsA)
+                                                       uint8_t *__restrict__ wsA, uint8_t *__restrict__ wsS)
 {
     qk::pdl_launch_dependents();
     qk::pdl_wait();                              // codes may come from the previous kernel
     const int sb = blockIdx.x, mt = blockIdx.y;
-    const int nit = (int)(K >> 5);
+    const int nit = (int)(K >> 5), B = (int)(K >> 8), nmin = (B + 1) >> 1;
 #pragma unroll 1
     for (int i = 0; i < 4; i++) {
         const int q = threadIdx.x + 256 * i;
@@ -242,6 +241,26 @@ __global__ void __launch_bounds__(256) mmq_prep_kernel(const int8_t *__restrict_
             sts128(tA, sw64(row, c), hi[0], hi[1], hi[2], hi[3]);
             sts128(tA + ATILE, sw64(row, c), lo[0], lo[1], lo[2], lo[3]);
         }
+        if (wsS) {
+            // the block's source sum S = d_a * sum(q_a), exact in binary32 (11 x 13 significant bits),
+            // scaled by 2^-4 and split into f16 S_hi + S_lo (to 2^-22 of S): sub-block j of superblock
+            // sb is column 8 (sb % 2) + j (S_hi) and 16 + 8 (sb % 2) + j (S_lo) of row `row` of the
+            // sums tile sb / 2
+            int sum = 0;
+#pragma unroll
+            for (int w = 0; w < 8; w++) sum = __dp4a((int)aw[w], 0x01010101, sum);
+            const float S = __half2float(dah) * (float)sum * kSScale;
+            const __half sh = __float2half_rn(S);
+            const __half sl = __float2half_rn(S - __half2float(sh));
+            uint8_t *tS = wsS + ((size_t)mt * nmin + (sb >> 1)) * SBLK;
+            const int e = sb & 1;
+            *reinterpret_cast<__half *>(tS + sw64(row, e) + 2 * j) = sh;
+            *reinterpret_cast<__half *>(tS + sw64(row, 2 + e) + 2 * j) = sl;
+            if (e == 0 && sb + 1 == B) {         // odd B: the last tile's second superblock does not exist
+                *reinterpret_cast<__half *>(tS + sw64(row, 1) + 2 * j) = __ushort_as_half(0);
+                *reinterpret_cast<__half *>(tS + sw64(row, 3) + 2 * j) = __ushort_as_half(0);
+            }
+        }
     }
 }
 
@@ -256,62 +275,6 @@ struct ConvState {
     uint4 c, mt, c2, qh;
     uint32_t d, dn;
 };
-
-// one converter thread's share of K stage `it` (operand stage st = it % NST): the 16 weights of
-// half h of sub-block j = it % 8 of row `row` as (W_hi, W_lo) chunks 2h and 2h+1, then the
-// stage is signalled full
-// it: K stage within the tile; gs / gsb: the stage and superblock counted over all tiles of
-// this CTA (ring slots and barrier phases)
-template <class L>
-__device__ __forceinline__ void convert_stage_q4(uint8_t *smem, uint64_t *bar, ConvState &cs,
-                                                 int it, int gs, int gsb, int row, int h, int st)
-{
-    const int j = it & 7, g = j >> 1, nib = j & 1;
-    const int rs = gsb % NRAW, ss = gsb % NSB;
-    if (j == 0) {
-        wait_bar(&bar[B_SFULL + ss], (gsb / NSB) & 1);
-        cs.mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * L::SBR + row * 16);
-        wait_bar(&bar[B_RFULL + rs], (gsb / NRAW) & 1);
-    }
-    if (nib == 0)
-        cs.c = *reinterpret_cast<const uint4 *>(smem + L::OFF_RAW + rs * L::RAW + (h ? L::RAW_H1 : L::RAW_H0) + row * 64 +
-                                                16 * g);
-    if (gs >= NST) wait_bar(&bar[B_EMPTY + st], ((gs / NST) + 1) & 1);
-    uint8_t *s0 = smem + st * L::STAGE;
-    // this group's record: sc0 | sc1<<6 | m0<<12 | m1<<18 (sub-blocks 2g and 2g+1)
-    const uint4 mt = cs.mt;
-    const uint32_t rec = __byte_perm(__byte_perm(mt.y, mt.z, g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u), mt.w,
-                                     g == 0 ? 0x3210u : g == 1 ? 0x3210u : g == 2 ? 0x3410u : 0x3765u);
-    const int sc = nib ? (int)((rec >> 6) & 63u) : (int)(rec & 63u);
-    const int mm = nib ? (int)((rec >> 18) & 63u) : (int)((rec >> 12) & 63u);
-    const float d = __half2float(__ushort_as_half((unsigned short)(mt.x & 0xffffu)));
-    const float dmin = __half2float(__ushort_as_half((unsigned short)(mt.x >> 16)));
-    const float dsc = d * (float)sc * kWScale, dmm = dmin * (float)mm * kWScale;   // exact products
-    const float2 dsc2 = make_float2(dsc, dsc), ndmm2 = make_float2(-dmm, -dmm);
-    const uint32_t cw[4] = {cs.c.x, cs.c.y, cs.c.z, cs.c.w};
-#pragma unroll
-    for (int cc = 0; cc < 2; cc++) {
-        uint32_t hi[4], lo[4];
-        const uint32_t x0 = nib ? (cw[2 * cc] >> 4) & 0x0F0F0F0Fu : cw[2 * cc] & 0x0F0F0F0Fu;
-        const uint32_t x1 = nib ? (cw[2 * cc + 1] >> 4) & 0x0F0F0F0Fu : cw[2 * cc + 1] & 0x0F0F0F0Fu;
-        conv_w(x0, dsc2, ndmm2, hi[0], hi[1], lo[0], lo[1]);
-        conv_w(x1, dsc2, ndmm2, hi[2], hi[3], lo[2], lo[3]);
-        sts128(s0 + 2 * ATILE, sw64(row, 2 * h + cc), hi[0], hi[1], hi[2], hi[3]);
-        sts128(s0 + 2 * ATILE + L::WTILE, sw64(row, 2 * h + cc), lo[0], lo[1], lo[2], lo[3]);
-    }
-    // Each lane makes its own stores visible to the tensor core (async proxy); after the warp
-    // has synchronised, one lane arrives for the whole warp.
-    // A raw slot is released only after the values read from it have been consumed by the
-    // arithmetic above, so no shared load can still be pending when the producer lets the next
-    // TMA copy overwrite it.
-    fence_proxy_async();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) {
-        if (j == 6) mbar_arrive(&bar[B_REMPTY + rs]);           // last read of this superblock's codes
-        if (j == 0) mbar_arrive(&bar[B_SEMPTY + ss]);
-        mbar_arrive(&bar[B_FULL + st]);
-    }
-}
 
 // Q6_K: the d of superblock sb of tile t for this converter's weight row (0 past the last row)
 template <int BN>
@@ -386,6 +349,15 @@ __device__ __forceinline__ void convert_stage_q6(uint8_t *smem, uint64_t *bar, C
     }
 }
 
+// Q6_K main kernel, one CTA (8 + 2 BN / 32 warps) per SM:
+//   warp 0      TMEM allocation (two BN-column accumulators: one tile accumulates while the previous
+//               one is written out); lane 0 issues every MMA and commit
+//   warp 1      lane 0: one bulk copy per K stage of its 16 KB activation block
+//   warp 2      lane 0: per half superblock the 32-byte runs of the two ql chunks and of qh (BN x 32 B
+//               each), per superblock the scale records (BN x 16 B); the d plane (2 bytes per
+//               superblock) is read by the converters themselves, one superblock ahead
+//   warps 4-7   the epilogue of the previous tile (TMEM lane quadrant = warp % 4)
+//   warps 8..   converters: two threads per weight row expand each K stage into (W_hi, W_lo)
 template <int QT, int BN_>
 __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
     mmq_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
@@ -478,7 +450,7 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&maps.wcodes);
             prefetch_tmap(&maps.meta);
-            if (L::Q6) prefetch_tmap(&maps.qh);
+            prefetch_tmap(&maps.qh);
             int gsb = 0, gu = 0;                                  // superblocks and raw units issued
             for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
                 const int n0 = (t / a.mtiles) * BN;
@@ -490,27 +462,17 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
                     // the superblock's lanes u = 4 (sb - 8 s) .. +3 of its step s: first 16-byte chunks at 16u,
                     // second chunks at 16 G + 16u
                     const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s);
-                    if constexpr (!L::Q6) {
+                    // two raw units: superblock half hs holds lanes u + 2hs, u + 2hs + 1 of each ql run and qh
+                    // bytes 32hs .. 32hs+31
+                    for (int hs = 0; hs < 2; hs++, gu++) {
                         const int rs = gu % NRAW;
                         if (gu >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((gu / NRAW) + 1) & 1);
                         uint8_t *d = smem + L::OFF_RAW + rs * L::RAW;
                         mbar_arrive_expect_tx(&bar[B_RFULL + rs], L::RAW);
-                        tma_load_2d(d + L::RAW_H0, &maps.wcodes, 1024 * s + 16 * u, n0, &bar[B_RFULL + rs]);
-                        tma_load_2d(d + L::RAW_H1, &maps.wcodes, 1024 * s + 16 * G + 16 * u, n0, &bar[B_RFULL + rs]);
-                        gu++;
-                    } else {
-                        // two raw units: superblock half hs holds lanes u + 2hs, u + 2hs + 1 of each ql run
-                        // and qh bytes 32hs .. 32hs+31
-                        for (int hs = 0; hs < 2; hs++, gu++) {
-                            const int rs = gu % NRAW;
-                            if (gu >= NRAW) wait_bar(&bar[B_REMPTY + rs], ((gu / NRAW) + 1) & 1);
-                            uint8_t *d = smem + L::OFF_RAW + rs * L::RAW;
-                            mbar_arrive_expect_tx(&bar[B_RFULL + rs], L::RAW);
-                            tma_load_2d(d + L::RAW_QL0, &maps.wcodes, 1024 * s + 16 * u + 32 * hs, n0, &bar[B_RFULL + rs]);
-                            tma_load_2d(d + L::RAW_QL1, &maps.wcodes, 1024 * s + 16 * G + 16 * u + 32 * hs, n0,
-                                        &bar[B_RFULL + rs]);
-                            tma_load_2d(d + L::RAW_QH, &maps.qh, 64 * sb + 32 * hs, n0, &bar[B_RFULL + rs]);
-                        }
+                        tma_load_2d(d + L::RAW_QL0, &maps.wcodes, 1024 * s + 16 * u + 32 * hs, n0, &bar[B_RFULL + rs]);
+                        tma_load_2d(d + L::RAW_QL1, &maps.wcodes, 1024 * s + 16 * G + 16 * u + 32 * hs, n0,
+                                    &bar[B_RFULL + rs]);
+                        tma_load_2d(d + L::RAW_QH, &maps.qh, 64 * sb + 32 * hs, n0, &bar[B_RFULL + rs]);
                     }
                 }
             }
@@ -571,7 +533,7 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
         ConvState cs;
         cs.c = cs.mt = cs.c2 = cs.qh = make_uint4(0, 0, 0, 0);
         cs.d = 0;
-        cs.dn = L::Q6 ? q6_d<BN>(a, blockIdx.x, 0, row) : 0u;
+        cs.dn = q6_d<BN>(a, blockIdx.x, 0, row);
         int kt = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
             const int gs0 = kt * nit;
@@ -579,8 +541,7 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
             static_assert(NST == 3, "the slot prologue below handles three stages");
             int it = 0;
             auto conv = [&](int itk, int gs, int st) {
-                if constexpr (L::Q6) convert_stage_q6<L>(smem, bar, cs, a, t, itk, gs, kt * B + (itk >> 3), row, h, st);
-                else convert_stage_q4<L>(smem, bar, cs, itk, gs, kt * B + (itk >> 3), row, h, st);
+                convert_stage_q6<L>(smem, bar, cs, a, t, itk, gs, kt * B + (itk >> 3), row, h, st);
             };
             while (it < nit && (gs0 + it) % NST != 0) {
                 const int gs = gs0 + it;
@@ -592,6 +553,450 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < NST; k++)
                     if (it + k < nit) conv(it + k, gs0 + it + k, k);
+            }
+        }
+    }
+
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------ Q4_K split-scale kernel
+// For Q4_K the tile's contraction is regrouped so that every weight operand is
+// exact in one f16 (Q4_K / q8_1 decomposition of minfer "15 . The CUDA
+// backend" sec. 3.2.6: the sub-block scale times the code dot, the min times
+// the source sum):
+//   y[m][n] = sum_b d_b[n] * (sum_{k in b} A[m][k] sc[n][k/32] q[n][k])
+//             - sum_j (dmin m)[n][j] S[m][j]
+// with A = d_a q_a = A_hi + A_lo (exact), S[m][j] = d_a sum(q_a) of sub-block
+// j.  W'[n][k] = sc q is an integer below 1024, so a K stage needs two MMAs
+// (A_hi W', A_lo W') and one f16 weight tile; each superblock b accumulates in
+// a tensor-memory buffer of its own, and the epilogue warps fold it into a
+// register copy of the output tile with the superblock scale d_b (an f16, so
+// the product is one binary32 rounding).  The min term is its own short
+// contraction over the K/32 sub-blocks, issued first for each tile: sums
+// tiles (S_hi | S_lo, built by the prep kernel) against (Mw_hi | Mw_lo),
+// Mw = 1024 dmin m (17 significant bits, split exactly), three MMAs per 16
+// sub-blocks; its accumulator seeds the register tile.
+// Warps: 0 MMA, 1 activation copier, 2 TMA producer, 3 idle, 4-11 epilogue
+// (TMEM lane quadrant warp % 4, column half (warp - 4) / 4), 12.. converters
+// (one thread per weight row).  With 256-wide tiles the epilogue warps hold
+// 128 accumulator columns each and take registers from the other warps
+// (setmaxnreg); the split adds up to the launch's 640 x 96.
+template <int BN_>
+struct Plan4 {
+    static constexpr int BN = BN_;
+    static constexpr int kEpiW0 = 4, kEpiW = 8, kConvW0 = 12, kConvW = BN / 32;
+    static constexpr int kThreads = (kConvW0 + kConvW) * 32;
+    static constexpr int CPT = BN / 2;                     // output columns per epilogue thread
+    static constexpr int WTILE = BN * 64;                  // BN rows x 32 f16
+    static constexpr int STAGE = 2 * ATILE + WTILE;        // A_hi | A_lo (or the sums tile) | W' (or Mw)
+    // raw unit: half a superblock's code bytes, first 16-byte halves of its 2 groups | second halves
+    static constexpr int RAW_H1 = BN * 32, RAW = 2 * BN * 32;
+    static constexpr int SBR = BN * 16;
+    static constexpr int NST = BN == 256 ? 4 : 6, NRAW = 3, NSB = 4, ND = 4;
+    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
+    static constexpr int OFF_RAW = NST * STAGE;
+    static constexpr int OFF_SBR = OFF_RAW + NRAW * RAW;
+    static constexpr int OFF_D = OFF_SBR + NSB * SBR;          // superblock scales d_b, binary32 [ND][BN]
+    static constexpr int OFF_EPI = OFF_D + ND * BN * 4;
+    static constexpr int OFF_BAR = OFF_EPI + kEpiW * 32 * EPI_LD * 4;
+    enum {
+        FULL = 0,
+        EMPTY = FULL + NST,
+        RFULL = EMPTY + NST,
+        REMPTY = RFULL + NRAW,
+        SFULL = REMPTY + NRAW,
+        SEMPTY = SFULL + NSB,
+        DFULL = SEMPTY + NSB,
+        DEMPTY = DFULL + ND,
+        ACCFULL = DEMPTY + ND,
+        ACCEMPTY = ACCFULL + 2,
+        DONE = ACCEMPTY + 2,
+        NBAR = DONE + 1
+    };
+    static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_TMEM + 16 + 1024;
+    static constexpr bool kSplitRegs = BN == 256;
+#ifndef QK_MMQ4_RMISC
+#define QK_MMQ4_RMISC 48
+#endif
+#ifndef QK_MMQ4_REPI
+#define QK_MMQ4_REPI 168
+#endif
+#ifndef QK_MMQ4_RCONV
+#define QK_MMQ4_RCONV 48
+#endif
+    // registers per thread: at launch, then warps 0-3, epilogue warps, converters
+    static constexpr int kRegLaunch = 96, kRegMisc = QK_MMQ4_RMISC, kRegEpi = QK_MMQ4_REPI, kRegConv = QK_MMQ4_RCONV;
+    static_assert(SMEM <= 232448, "shared memory plan exceeds the per-block opt-in limit");
+    static_assert(STAGE % 1024 == 0 && OFF_RAW % 1024 == 0 && RAW % 1024 == 0 && OFF_SBR % 1024 == 0,
+                  "copy destinations and swizzle atoms stay aligned");
+    static_assert(!kSplitRegs || (4 * kRegMisc + kEpiW * kRegEpi + kConvW * kRegConv) * 32 <= kThreads * kRegLaunch,
+                  "the register split must fit in the launch's registers");
+};
+
+template <int N> __device__ __forceinline__ void reg_alloc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N> __device__ __forceinline__ void reg_dealloc() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+
+// the 24-bit record of group g (sub-blocks 2g, 2g+1) of a Q4_K metadata record:
+// sc[2g] | sc[2g+1] << 6 | m[2g] << 12 | m[2g+1] << 18
+__device__ __forceinline__ uint32_t q4_group(const uint4 &mt, int g)
+{
+    return __byte_perm(__byte_perm(mt.y, mt.z, g == 0 ? 0x3210u : g == 1 ? 0x6543u : 0x7676u), mt.w,
+                       g == 0 ? 0x3210u : g == 1 ? 0x3210u : g == 2 ? 0x3410u : 0x3765u);
+}
+
+// 4 nibbles (one per byte of x, masked to 0..15) times the sub-block scale sc (< 64) as two f16
+// pairs, exactly: each product (< 1024) sits in a 16-bit lane of 0x6400 + sc q, the f16 1024 + sc q,
+// and 1024 is subtracted
+__device__ __forceinline__ void w_sc(uint32_t x, uint32_t sc, uint32_t &p01, uint32_t &p23)
+{
+    const __half2 k1024 = u2h(0x64006400u);
+    p01 = h2u(__hsub2(u2h(__byte_perm(x, 0u, 0x4140u) * sc + 0x64006400u), k1024));
+    p23 = h2u(__hsub2(u2h(__byte_perm(x, 0u, 0x4342u) * sc + 0x64006400u), k1024));
+}
+
+// the 8 min products Mw' = 1024 dmin m_j of one superblock record, split exactly into f16 pairs
+// hi (11 significant bits: the binary32 value with its 13 low mantissa bits cleared) and lo (the
+// remaining at most 6 bits); word i holds sub-blocks 2i, 2i+1
+__device__ __forceinline__ void mins_hilo(const uint4 &mt, uint32_t (&hi)[4], uint32_t (&lo)[4])
+{
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(mt.x >> 16))) * kMScale;
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+        const uint32_t r = q4_group(mt, g);
+        const float w0 = dmin * (float)((r >> 12) & 63u), w1 = dmin * (float)((r >> 18) & 63u);   // exact
+        const float h0 = __uint_as_float(__float_as_uint(w0) & 0xFFFFE000u);
+        const float h1 = __uint_as_float(__float_as_uint(w1) & 0xFFFFE000u);
+        hi[g] = h2u(__floats2half2_rn(h0, h1));
+        lo[g] = h2u(__floats2half2_rn(w0 - h0, w1 - h1));
+    }
+}
+
+template <int BN_>
+__global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
+    mmq_q4k_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
+{
+    using L = Plan4<BN_>;
+    constexpr int BN = L::BN, NS = L::NST, NR = L::NRAW, NB = L::NSB, ND = L::ND;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + L::OFF_TMEM);
+    float *dring = reinterpret_cast<float *>(smem + L::OFF_D);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int B = (int)(a.K >> 8), nmin = (B + 1) >> 1;
+    const int ntiles = a.mtiles * a.ntiles;
+
+    qk::pdl_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; i++) mbar_init(&bar[L::FULL + i], L::kConvW + 1), mbar_init(&bar[L::EMPTY + i], 1);
+        for (int i = 0; i < NR; i++) mbar_init(&bar[L::RFULL + i], 1), mbar_init(&bar[L::REMPTY + i], L::kConvW);
+        for (int i = 0; i < NB; i++) mbar_init(&bar[L::SFULL + i], 1), mbar_init(&bar[L::SEMPTY + i], L::kConvW);
+        for (int i = 0; i < ND; i++) mbar_init(&bar[L::DFULL + i], L::kConvW), mbar_init(&bar[L::DEMPTY + i], L::kEpiW);
+        for (int i = 0; i < 2; i++) mbar_init(&bar[L::ACCFULL + i], 1), mbar_init(&bar[L::ACCEMPTY + i], L::kEpiW);
+        mbar_init(&bar[L::DONE], 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_ptr, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_ptr;
+    qk::pdl_wait();
+    const bool epi = warp >= L::kEpiW0 && warp < L::kEpiW0 + L::kEpiW;
+
+    // each warpgroup sets its register count first thing in its own branch
+    if (warp < L::kEpiW0) {
+    if constexpr (L::kSplitRegs) reg_dealloc<L::kRegMisc>();
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        // accumulator events in order: per tile the min term, then one per superblock
+        if (lane == 0) {
+            const uint32_t sbase = smem_u32(smem);
+            int gs = 0, ge = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                for (int ev = 0; ev <= B; ev++, ge++) {
+                    const int acc = ge & 1;
+                    if (ge >= 2) wait_bar(&bar[L::ACCEMPTY + acc], ((ge >> 1) + 1) & 1);
+                    fence_after_sync();
+                    const uint32_t dacc = tmem + acc * BN;
+                    const int nst = ev == 0 ? nmin : 8;
+                    for (int i = 0; i < nst; i++, gs++) {
+                        const int st = gs % NS;
+                        wait_bar(&bar[L::FULL + st], (gs / NS) & 1);
+                        fence_after_sync();
+                        const uint32_t s0 = sbase + st * L::STAGE, w0 = s0 + 2 * ATILE;
+                        if (ev == 0) {
+                            const uint64_t shi = smem_desc(s0, 16, 512, kLayoutSw64);
+                            const uint64_t slo = smem_desc(s0 + 32, 16, 512, kLayoutSw64);
+                            const uint64_t mhi = smem_desc(w0, 16, 512, kLayoutSw64);
+                            const uint64_t mlo = smem_desc(w0 + 32, 16, 512, kLayoutSw64);
+                            mma_f16(dacc, shi, mhi, L::IDESC, i != 0);
+                            mma_f16(dacc, shi, mlo, L::IDESC, 1);
+                            mma_f16(dacc, slo, mhi, L::IDESC, 1);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < BK / 16; kk++) {
+                                const uint64_t ahi = smem_desc(s0 + 32 * kk, 16, 512, kLayoutSw64);
+                                const uint64_t alo = smem_desc(s0 + ATILE + 32 * kk, 16, 512, kLayoutSw64);
+                                const uint64_t wd = smem_desc(w0 + 32 * kk, 16, 512, kLayoutSw64);
+                                mma_f16(dacc, ahi, wd, L::IDESC, (i | kk) != 0);
+                                mma_f16(dacc, alo, wd, L::IDESC, 1);
+                            }
+                        }
+                        mma_commit(&bar[L::EMPTY + st]);
+                    }
+                    mma_commit(&bar[L::ACCFULL + acc]);
+                }
+            }
+            // teardown: no MMA may still be running when the TMEM is released
+            mma_commit(&bar[L::DONE]);
+            wait_bar(&bar[L::DONE], 0);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ activation block copier
+        // per tile the sums tiles of its min stages (8 KB each), then the A blocks (16 KB)
+        if (lane == 0) {
+            int gs = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                const int mt = t % a.mtiles;
+                const uint8_t *srcS = a.wsS + (size_t)mt * nmin * SBLK;
+                const uint8_t *srcA = a.wsA + (size_t)mt * (8 * B) * ABLOCK;
+                for (int i = 0; i < nmin + 8 * B; i++, gs++) {
+                    const int st = gs % NS;
+                    if (gs >= NS) wait_bar(&bar[L::EMPTY + st], ((gs / NS) + 1) & 1);
+                    const bool mn = i < nmin;
+                    const uint32_t bytes = mn ? SBLK : ABLOCK;
+                    mbar_arrive_expect_tx(&bar[L::FULL + st], bytes);
+                    bulk_copy_g2s(smem + st * L::STAGE, mn ? srcS + (size_t)i * SBLK : srcA + (size_t)(i - nmin) * ABLOCK,
+                                  bytes, &bar[L::FULL + st]);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------ raw weight TMA producer
+        // per tile: the metadata records of every superblock (min stages), then per superblock its
+        // record again and its code bytes
+        if (lane == 0) {
+            prefetch_tmap(&maps.wcodes);
+            prefetch_tmap(&maps.meta);
+            int gsb = 0, gu = 0;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                const int n0 = (t / a.mtiles) * BN;
+                for (int pass = 0; pass < 2; pass++) {
+                    for (int sb = 0; sb < B; sb++, gsb++) {
+                        const int ss = gsb % NB;
+                        if (gsb >= NB) wait_bar(&bar[L::SEMPTY + ss], ((gsb / NB) + 1) & 1);
+                        mbar_arrive_expect_tx(&bar[L::SFULL + ss], L::SBR);
+                        tma_load_2d(smem + L::OFF_SBR + ss * L::SBR, &maps.meta, 16 * sb, n0, &bar[L::SFULL + ss]);
+                        if (pass == 0) continue;
+                        // the superblock's groups u = 4 (sb - 8 s) .. +3 of its step s: first 16-byte halves
+                        // at 16u, second halves at 16 G + 16u; one raw unit per pair of groups
+                        const int s = sb >> 3, G = 4 * min(8, B - 8 * s), u = 4 * (sb - 8 * s);
+                        for (int hs = 0; hs < 2; hs++, gu++) {
+                            const int rs = gu % NR;
+                            if (gu >= NR) wait_bar(&bar[L::REMPTY + rs], ((gu / NR) + 1) & 1);
+                            uint8_t *d = smem + L::OFF_RAW + rs * L::RAW;
+                            mbar_arrive_expect_tx(&bar[L::RFULL + rs], L::RAW);
+                            tma_load_2d(d, &maps.wcodes, 1024 * s + 16 * (u + 2 * hs), n0, &bar[L::RFULL + rs]);
+                            tma_load_2d(d + L::RAW_H1, &maps.wcodes, 1024 * s + 16 * G + 16 * (u + 2 * hs), n0,
+                                        &bar[L::RFULL + rs]);
+                        }
+                    }
+                }
+            }
+            // teardown: every copy this thread issued has landed (normally long since consumed)
+            for (int g = gu - NR < 0 ? 0 : gu - NR; g < gu; g++) wait_bar(&bar[L::RFULL + g % NR], (g / NR) & 1);
+            for (int g = gsb - NB < 0 ? 0 : gsb - NB; g < gsb; g++) wait_bar(&bar[L::SFULL + g % NB], (g / NB) & 1);
+        }
+        __syncwarp();
+    }
+    } else if (epi) {
+        if constexpr (L::kSplitRegs) reg_alloc<L::kRegEpi>();
+        // -------------------------------------------------------------- epilogue
+        // thread: row (32 quad + lane) of the tile, columns ch CPT .. +CPT, in registers across the
+        // tile's accumulator events; then y = R (+ residual), transposed through shared memory 16
+        // columns at a time so that each store covers 16 consecutive columns of two rows
+        const int ew = warp - L::kEpiW0, quad = warp & 3, ch = ew >> 2;
+        const uint32_t lq = (uint32_t)(quad * 32) << 16;
+        float *tb_s = reinterpret_cast<float *>(smem + L::OFF_EPI) + ew * (32 * EPI_LD);
+        float R[L::CPT];
+        int ge = 0, gd = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            const int64_t m0 = (int64_t)(t % a.mtiles) * BM, n0 = (int64_t)(t / a.mtiles) * BN;
+            {
+                const int acc = ge & 1;
+                wait_bar(&bar[L::ACCFULL + acc], (ge >> 1) & 1);
+                fence_after_sync();
+                const uint32_t tb = tmem + lq + acc * BN + ch * L::CPT;
+#pragma unroll
+                for (int c = 0; c < L::CPT / 16; c++) {
+                    float v[16];
+                    tmem_ld16(tb + 16 * c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; i++) R[16 * c + i] = v[i] * kMinUndo;
+                }
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[L::ACCEMPTY + acc]);
+                ge++;
+            }
+#pragma unroll 1
+            for (int sb = 0; sb < B; sb++, ge++, gd++) {
+                const int acc = ge & 1, ds = gd % ND;
+                wait_bar(&bar[L::DFULL + ds], (gd / ND) & 1);
+                wait_bar(&bar[L::ACCFULL + acc], (ge >> 1) & 1);
+                fence_after_sync();
+                const uint32_t tb = tmem + lq + acc * BN + ch * L::CPT;
+                const float4 *dv = reinterpret_cast<const float4 *>(dring + ds * BN + ch * L::CPT);
+#pragma unroll
+                for (int c = 0; c < L::CPT / 8; c++) {
+                    float v[8];
+                    tmem_ld8(tb + 8 * c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 2; q++) {
+                        const float4 d4 = dv[2 * c + q];
+                        R[8 * c + 4 * q + 0] = __fmaf_rn(d4.x, v[4 * q + 0], R[8 * c + 4 * q + 0]);
+                        R[8 * c + 4 * q + 1] = __fmaf_rn(d4.y, v[4 * q + 1], R[8 * c + 4 * q + 1]);
+                        R[8 * c + 4 * q + 2] = __fmaf_rn(d4.z, v[4 * q + 2], R[8 * c + 4 * q + 2]);
+                        R[8 * c + 4 * q + 3] = __fmaf_rn(d4.w, v[4 * q + 3], R[8 * c + 4 * q + 3]);
+                    }
+                }
+                // the buffer may be overwritten once every lane's loads have completed; the scales
+                // were consumed above
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bar[L::ACCEMPTY + acc]);
+                    mbar_arrive(&bar[L::DEMPTY + ds]);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < L::CPT / 16; c++) {
+#pragma unroll
+                for (int i = 0; i < 16; i++) tb_s[lane * EPI_LD + i] = R[16 * c + i];
+                __syncwarp();
+                const int64_t n = n0 + ch * L::CPT + 16 * c + (lane & 15);
+                if (n < a.N) {
+#pragma unroll 4
+                    for (int rr = 0; rr < 16; rr++) {
+                        const int r = 2 * rr + (lane >> 4);
+                        const int64_t m = m0 + quad * 32 + r;
+                        if (m < a.M) {
+                            const float val = tb_s[r * EPI_LD + (lane & 15)];
+                            const size_t o = (size_t)m * a.N + n;
+                            a.y[o] = a.residual ? __fadd_rn(val, a.residual[o]) : val;
+                        }
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    } else {
+        if constexpr (L::kSplitRegs) reg_dealloc<L::kRegConv>();
+        // --------------------------------------------------------- converters
+        // one thread per weight row; a quarter warp stores 8 consecutive rows, which the 64-byte
+        // swizzle spreads over all 32 banks
+        const int row = 32 * (warp - L::kConvW0) + lane;
+        int gs = 0, gsb = 0, gu = 0, gd = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            // min stages: sub-blocks of superblocks 2i and 2i+1 -> (Mw_hi | Mw_lo)
+#pragma unroll 1
+            for (int i = 0; i < nmin; i++, gs++) {
+                const int st = gs % NS;
+                const bool two = 2 * i + 1 < B;
+                const int ss0 = gsb % NB, ss1 = (gsb + 1) % NB;
+                wait_bar(&bar[L::SFULL + ss0], (gsb / NB) & 1);
+                const uint4 r0 = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss0 * L::SBR + row * 16);
+                uint4 r1 = make_uint4(0, 0, 0, 0);
+                if (two) {
+                    wait_bar(&bar[L::SFULL + ss1], ((gsb + 1) / NB) & 1);
+                    r1 = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss1 * L::SBR + row * 16);
+                }
+                uint32_t h0[4], l0[4], h1[4], l1[4];
+                mins_hilo(r0, h0, l0);
+                mins_hilo(r1, h1, l1);
+                if (gs >= NS) wait_bar(&bar[L::EMPTY + st], ((gs / NS) + 1) & 1);
+                uint8_t *w0 = smem + st * L::STAGE + 2 * ATILE;
+                sts128(w0, sw64(row, 0), h0[0], h0[1], h0[2], h0[3]);
+                sts128(w0, sw64(row, 1), h1[0], h1[1], h1[2], h1[3]);
+                sts128(w0, sw64(row, 2), l0[0], l0[1], l0[2], l0[3]);
+                sts128(w0, sw64(row, 3), l1[0], l1[1], l1[2], l1[3]);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bar[L::SEMPTY + ss0]);
+                    if (two) mbar_arrive(&bar[L::SEMPTY + ss1]);
+                    mbar_arrive(&bar[L::FULL + st]);
+                }
+                gsb += two ? 2 : 1;
+            }
+            // main stages: per superblock its scale d into the scale ring, then sub-block j -> W' = sc q
+#pragma unroll 1
+            for (int sb = 0; sb < B; sb++, gsb++, gd++) {
+                const int ss = gsb % NB, ds = gd % ND;
+                wait_bar(&bar[L::SFULL + ss], (gsb / NB) & 1);
+                const uint4 mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * L::SBR + row * 16);
+                if (gd >= ND) wait_bar(&bar[L::DEMPTY + ds], ((gd / ND) + 1) & 1);
+                dring[ds * BN + row] = __half2float(__ushort_as_half((unsigned short)(mt.x & 0xffffu)));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[L::DFULL + ds]);
+                // raw unit hs = j / 4 holds groups 2hs, 2hs+1; its tiles arrive 32-byte swizzled (16-byte
+                // chunk c of row r at sw32(r, c)), so that a quarter warp's 8 rows read distinct banks
+                uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+                int rs = 0;
+#pragma unroll
+                for (int j = 0; j < 8; j++, gs++) {
+                    const int g = j >> 1, nib = j & 1, st = gs % NS;
+                    if ((j & 3) == 0) {
+                        rs = gu % NR;
+                        wait_bar(&bar[L::RFULL + rs], (gu / NR) & 1);
+                    }
+                    if (nib == 0) {
+                        const uint8_t *raw = smem + L::OFF_RAW + rs * L::RAW;
+                        c0 = *reinterpret_cast<const uint4 *>(raw + sw32(row, g & 1));
+                        c1 = *reinterpret_cast<const uint4 *>(raw + L::RAW_H1 + sw32(row, g & 1));
+                    }
+                    const uint32_t rec = q4_group(mt, g);
+                    const uint32_t sc = nib ? (rec >> 6) & 63u : rec & 63u;
+                    if (gs >= NS) wait_bar(&bar[L::EMPTY + st], ((gs / NS) + 1) & 1);
+                    uint8_t *w0 = smem + st * L::STAGE + 2 * ATILE;
+                    const uint32_t x[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                    for (int cc = 0; cc < 4; cc++) {
+                        const uint32_t xa = (nib ? x[2 * cc] >> 4 : x[2 * cc]) & 0x0F0F0F0Fu;
+                        const uint32_t xb = (nib ? x[2 * cc + 1] >> 4 : x[2 * cc + 1]) & 0x0F0F0F0Fu;
+                        uint32_t p0, p1, p2, p3;
+                        w_sc(xa, sc, p0, p1);
+                        w_sc(xb, sc, p2, p3);
+                        sts128(w0, sw64(row, cc), p0, p1, p2, p3);
+                    }
+                    // each lane makes its stores visible to the tensor core (async proxy), then one lane
+                    // arrives for the warp; a raw slot is released only after the values read from it
+                    // have been consumed above
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if ((j & 3) == 2) mbar_arrive(&bar[L::REMPTY + rs]);   // last read of this raw unit
+                        if (j == 0) mbar_arrive(&bar[L::SEMPTY + ss]);
+                        mbar_arrive(&bar[L::FULL + st]);
+                    }
+                    if ((j & 3) == 3) gu++;
+                }
             }
         }
     }
@@ -627,22 +1032,60 @@ EncodeTiledFn encode_tiled()
 
 // 2D row-major tensor [rows][cols] of elements of the map's type, row pitch `pitch` bytes; box bx x by
 bool make_map(EncodeTiledFn enc, CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t cols,
-              uint64_t rows, uint64_t pitch, uint32_t bx, uint32_t by)
+              uint64_t rows, uint64_t pitch, uint32_t bx, uint32_t by,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE)
 {
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {pitch};
     const cuuint32_t box[2] = {bx, by};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// workspace bytes for an M x K activation: one A block per M-tile and 32-value K stage
-size_t ws_bytes(int64_t M, int64_t K)
+// workspace bytes for an M x K activation: one A block per M-tile and 32-value K stage, then one
+// sums tile per M-tile and pair of superblocks
+size_t ws_a_bytes(int64_t M, int64_t K)
 {
     const size_t mt = (size_t)((M + BM - 1) / BM);
     return mt * (size_t)(K / BK) * ABLOCK;
+}
+size_t ws_bytes(int64_t M, int64_t K)
+{
+    const size_t mt = (size_t)((M + BM - 1) / BM);
+    return ws_a_bytes(M, K) + mt * (size_t)((K / 256 + 1) / 2) * SBLK;
+}
+
+// The register-split kernel must be launched with exactly the registers its setmaxnreg split hands
+// out: with fewer, the epilogue warps' increase could never be granted.  Checked once per kernel,
+// before its first launch.
+template <int BN>
+int set_attrs_q4()
+{
+    static std::atomic<int> done{0};
+    if (done.load()) return QK_OK;
+    if (cudaFuncSetAttribute(mmq_q4k_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan4<BN>::SMEM) !=
+            cudaSuccess ||
+        qk::max_carveout(mmq_q4k_kernel<BN>) != cudaSuccess)
+        return QK_E_CUDA;
+    if (Plan4<BN>::kSplitRegs) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, mmq_q4k_kernel<BN>) != cudaSuccess || fa.numRegs != Plan4<BN>::kRegLaunch)
+            return QK_E_CUDA;
+    }
+    done.store(1);
+    return QK_OK;
+}
+
+template <int BN>
+int launch_mmq_q4(const MmqArgs &args, const MmqMaps &maps, int64_t tiles, cudaStream_t stream)
+{
+    const int st = set_attrs_q4<BN>();
+    if (st != QK_OK) return st;
+    const int64_t grid = tiles < qk::sm_count() ? tiles : qk::sm_count();
+    return qk::launch(mmq_q4k_kernel<BN>, dim3((unsigned)grid), dim3(Plan4<BN>::kThreads), Plan4<BN>::SMEM, stream,
+                      true, args, maps);
 }
 
 template <int QT, int BN>
@@ -706,7 +1149,7 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
     const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
     if (gx > 65535 || gy > 65535 || gx * gy > 0x7fffffffLL) return QK_E_SHAPE;
     const bool q6 = qt == QK_TYPE_Q6_K;
-    const size_t smem = q6 ? (size_t)Plan<QK_TYPE_Q6_K, 256>::SMEM : (size_t)Plan<QK_TYPE_Q4_K, 256>::SMEM;
+    const size_t smem = q6 ? (size_t)Plan<QK_TYPE_Q6_K, 256>::SMEM : (size_t)Plan4<256>::SMEM;
     if (smem > qk::max_smem_optin()) return QK_E_CUDA;     // the larger plan of each weight type
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return QK_E_CUDA;
@@ -715,7 +1158,8 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
     MmqMaps maps;
     memset(&maps, 0, sizeof(maps));
     if (!q6) {
-        if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 64, (uint32_t)BN) ||
+        if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 32, (uint32_t)BN,
+                      CU_TENSOR_MAP_SWIZZLE_32B) ||
             !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 16, N, B * 16, 16,
                       (uint32_t)BN))
             return QK_E_CUDA;
@@ -728,16 +1172,22 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
             return QK_E_CUDA;
     }
     uint8_t *wsA = static_cast<uint8_t *>(workspace);
-    int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, (cudaStream_t)stream,
-                        (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA);
-    if (st != QK_OK) return st;
-    MmqArgs args{wsA, q6 ? reinterpret_cast<const uint16_t *>(wb + N * B * 208) : nullptr, M, N, K, residual, y,
-                 (int)gx, (int)gy};
+    uint8_t *wsS = q6 ? nullptr : wsA + ws_a_bytes(M, K);
     const int64_t tiles = gx * gy;
     cudaStream_t cs = (cudaStream_t)stream;
+    if (!q6) {
+        // validate the main kernel's launch configuration before anything is launched
+        const int sa = BN == 128 ? set_attrs_q4<128>() : set_attrs_q4<256>();
+        if (sa != QK_OK) return sa;
+    }
+    int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, cs,
+                        (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA, wsS);
+    if (st != QK_OK) return st;
+    MmqArgs args{wsA, wsS, q6 ? reinterpret_cast<const uint16_t *>(wb + N * B * 208) : nullptr, M, N, K, residual, y,
+                 (int)gx, (int)gy};
     if (q6) return BN == 128 ? launch_mmq<QK_TYPE_Q6_K, 128>(args, maps, tiles, cs)
                              : launch_mmq<QK_TYPE_Q6_K, 256>(args, maps, tiles, cs);
-    return BN == 128 ? launch_mmq<QK_TYPE_Q4_K, 128>(args, maps, tiles, cs) : launch_mmq<QK_TYPE_Q4_K, 256>(args, maps, tiles, cs);
+    return BN == 128 ? launch_mmq_q4<128>(args, maps, tiles, cs) : launch_mmq_q4<256>(args, maps, tiles, cs);
 }
 
 }  // namespace

@@ -127,10 +127,11 @@ def test_repack_rejects(L):
 
 
 def test_mmq_workspace_size():
-    # ceil(M/128) * K * 512
-    assert qk.mmq_workspace_bytes(2048, 3584, 18944) == 16 * 18944 * 512 == 155189248
-    assert qk.mmq_workspace_bytes(1, 64, 256) == 256 * 512
-    assert qk.mmq_workspace_bytes(129, 64, 512) == 2 * 512 * 512
+    # ceil(M/128) * (K * 512 + ceil(K/512) * 8192)
+    assert qk.mmq_workspace_bytes(2048, 3584, 18944) == 16 * (18944 * 512 + 37 * 8192) == 160038912
+    assert qk.mmq_workspace_bytes(1, 64, 256) == 256 * 512 + 8192
+    assert qk.mmq_workspace_bytes(129, 64, 512) == 2 * (512 * 512 + 8192)
+    assert qk.mmq_workspace_bytes(128, 64, 1280) == 1280 * 512 + 3 * 8192     # 5 superblocks: 3 sums tiles
     assert qk.mmq_workspace_bytes(0, 64, 256) == 0
 
 
