@@ -364,3 +364,51 @@ def test_mmq_edges_and_error_flags(qt):
         check(y, y_ref, ab, what=f"mmq {qt} edge M={M} N={N} K={K}")
     torch.cuda.synchronize()
     assert qk.error_flags(clear=True) == 0
+
+
+def special_scale_weights(qt, N, K, seed):
+    """synth weights with per-row cases of the superblock scales edited in the GGUF bytes:
+    row n % 5 == 0: d = 0 in every other superblock (Q4_K: only the min term is left there);
+    1: dmin = 0 everywhere (Q4_K); 2: a large scale in superblock 1 (Q4_K: dmin = 0.98, so
+    dmin * m reaches 61.7, just inside the operand limit of 63; Q6_K: d = 0.2, |w| up to 205);
+    3: every scale zero (the row is exactly 0); 4: unchanged."""
+    w = synth.weights(qt, N, K, seed=seed).copy()
+    blocks = w.reshape(N, K // 256, oracle.BLOCK_BYTES[QT[qt][1]])
+    doff = 0 if qt == "q4k" else 208                   # GGUF offset of the f16 d
+
+    def f16(v):
+        return np.frombuffer(np.float16(v).tobytes(), np.uint8)
+
+    for n in range(N):
+        kind = n % 5
+        if kind == 0:
+            blocks[n, ::2, doff:doff + 2] = 0
+        elif kind == 1 and qt == "q4k":
+            blocks[n, :, 2:4] = 0
+        elif kind == 2:
+            if qt == "q4k":
+                blocks[n, 1, 2:4] = f16(0.98)
+            else:
+                blocks[n, 1, doff:doff + 2] = f16(0.2)
+        elif kind == 3:
+            blocks[n, :, doff:doff + 2] = 0
+            if qt == "q4k":
+                blocks[n, :, 2:4] = 0
+    return w
+
+
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+def test_mmq_superblock_scale_special_cases(qt):
+    """Zero superblock scales (the per-superblock fold multiplies by 0, the min term stands
+    alone), zero mins, scales at the operand limits, all-zero rows (exactly 0); an odd number
+    of superblocks (the last min stage's second half is empty) and ragged tiles."""
+    M, N, K = 130, 300, 256 * 7
+    w = special_scale_weights(qt, N, K, seed=91)
+    wr = qk.repack(QT[qt][0], dev(w), N, K)
+    codes, scales = q8(synth.activations(M, K, seed=93))
+    c, d = q8_host(codes, scales)
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+    for tile in (256, 128):
+        y = mmq_fn(qt)(wr, codes, scales, N, K, tile=tile).cpu().numpy()
+        check(y, y_ref, ab, what=f"mmq {qt} special scales tile={tile}")
+        assert np.all(y[:, 3::5] == 0)
