@@ -117,7 +117,7 @@ TRAFFIC: dict = {
                           "profile": "profiles/gemv_q6k_f32_head_128256x4096.md"},
     (3, "gemv_q6k"): {"bytes_per_launch": 435261696, "digest": "bc3a9e2fedd8c4ef",
                       "profile": "profiles/dram_traffic_per_launch.md"},
-    (4, "mmq_q4k"): {"bytes_per_launch": 233749376, "digest": "f626f1b055bbfd79",
+    (4, "mmq_q4k"): {"bytes_per_launch": 233749376, "digest": "b1c1938ee3b443a4",
                      "profile": "profiles/dram_traffic_per_launch.md"},
 }
 

@@ -362,7 +362,8 @@ int qk_gemv_q3k_f32(const void *w, const float *x, int64_t ldx,
  * activation enters f16 MMAs exactly as A_hi + A_lo, the integer sc*q (< 1024)
  * exactly as one f16, each superblock accumulates on its own and is scaled by
  * d_b in binary32, and the min term is a contraction over the K/32
- * sub-blocks of S (split to 2^-22) with dmin*m (split exactly).  The binary32
+ * sub-blocks of S (split to 2^-22) with dmin*m (split exactly down to
+ * 1024*dmin*m = 2^-8, to 2^-25 absolute below).  The binary32
  * result is within 1e-4 * sum_k |w * xhat| of the exact contraction (in
  * practice ~1e-7).
  *

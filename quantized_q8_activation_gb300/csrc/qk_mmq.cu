@@ -580,7 +580,7 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
 // the product is one binary32 rounding).  The min term is its own short
 // contraction over the K/32 sub-blocks, issued first for each tile: sums
 // tiles (S_hi | S_lo, built by the prep kernel) against (Mw_hi | Mw_lo),
-// Mw = 1024 dmin m (17 significant bits, split exactly), three MMAs per 16
+// Mw = 1024 dmin m (17 significant bits, split exactly down to 2^-8), three MMAs per 16
 // sub-blocks; its accumulator seeds the register tile.
 // Warps: 0 MMA, 1 activation copier, 2 TMA producer, 3 idle, 4-11 epilogue
 // (TMEM lane quadrant warp % 4, column half (warp - 4) / 4), 12.. converters
@@ -662,9 +662,10 @@ __device__ __forceinline__ void w_sc(uint32_t x, uint32_t sc, uint32_t &p01, uin
     p23 = h2u(__hsub2(u2h(__byte_perm(x, 0u, 0x4342u) * sc + 0x64006400u), k1024));
 }
 
-// the 8 min products Mw' = 1024 dmin m_j of one superblock record, split exactly into f16 pairs
-// hi (11 significant bits: the binary32 value with its 13 low mantissa bits cleared) and lo (the
-// remaining at most 6 bits); word i holds sub-blocks 2i, 2i+1
+// the 8 min products Mw' = 1024 dmin m_j of one superblock record as f16 pairs hi (11 significant
+// bits: the binary32 value with its 13 low mantissa bits cleared) and lo (the remaining at most 6
+// bits), exact down to Mw' = 2^-8 (below it lo's last bit falls under the f16 subnormal step);
+// word i holds sub-blocks 2i, 2i+1
 __device__ __forceinline__ void mins_hilo(const uint4 &mt, uint32_t (&hi)[4], uint32_t (&lo)[4])
 {
     const float dmin = __half2float(__ushort_as_half((unsigned short)(mt.x >> 16))) * kMScale;
