@@ -472,7 +472,7 @@ def run_reference(args, ws, rank):
     """The oracle on the host cores, on our arm's config/metric/unit.  Each step is a
     bounded sample of the workload (every contraction on a slice of its output rows, and
     for the prefill config on 8 activation rows), sized so the whole run takes about
-    two minutes whatever --steps is."""
+    --ref-seconds (two minutes by default) whatever --steps is."""
     if rank != 0:
         return
     cfg = CONFIGS[args.config]
@@ -486,7 +486,7 @@ def run_reference(args, ws, rank):
     t0 = time.perf_counter()
     oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac=1 / 64, host_g=host_g)
     t_slice = max(time.perf_counter() - t0, 1e-4)
-    per_step = 120.0 / (args.steps + args.warmup)
+    per_step = args.ref_seconds / (args.steps + args.warmup)
     n_frac = min(1.0, max(1e-6, per_step / (t_slice * 64)))
     for _ in range(args.warmup):
         oracle_step(cfg, host_w, host_x, host_r, threads, m_rows, n_frac, host_g=host_g)
@@ -707,6 +707,8 @@ def main():
     ap.add_argument("--copies", type=int, default=None, help="weight copies rotated between steps")
     ap.add_argument("--graph-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: total host time the warm-up and timed steps are sized to")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--front-end", choices=["auto", "fused", "unfused"], default="auto",
                     help="decode activation path: q8_1 quantization inside each GEMV (fused) or a "
