@@ -157,6 +157,17 @@ def recorded_traffic(cfg_id: int, kernel: str):
     return t["bytes_per_launch"]
 
 
+def launches_per_step(cfg, front_end: str = "auto") -> int:
+    """kernels of this library one step launches: the quantize kernels of unfused activations,
+    one GEMV per decode GEMM, two kernels (prep and main) per MMQ call, and the chain's
+    two RMSNorm and one SwiGLU producers"""
+    if cfg["kind"] == "chain":
+        return 3 + len(cfg["gemms"])
+    slots_q = {g[5] for g in cfg["gemms"] if not gemm_fused(front_end, cfg, g)}
+    per_gemm = 2 if cfg["kind"] == "mmq" else 1
+    return len(slots_q) + per_gemm * len(cfg["gemms"])
+
+
 def slots(cfg):
     """activation slots in step order with their K"""
     out = []
@@ -273,10 +284,7 @@ class Workload:
         return "gemv_" + q + ("_f32" if fused else "")
 
     def launches_per_step(self, front_end: str = "auto") -> int:
-        if self.cfg["kind"] == "chain":
-            return 3 + len(self.cfg["gemms"])         # two RMSNorm and one SwiGLU producer
-        slots_q = {g[5] for g in self.cfg["gemms"] if not gemm_fused(front_end, self.cfg, g)}
-        return len(slots_q) + len(self.cfg["gemms"])
+        return launches_per_step(self.cfg, front_end)
 
 
 # -------------------------------------------------------------------- clocks
@@ -682,7 +690,9 @@ def run_ours(args, ws, rank, local):
             "front_end_ms_per_step": front_end_ms or None,
             "hbm_frac": (value / ws) / hbm if unit == "GB/s" else None,
             "roofline": roof,
-            "per_kernel": {k: {"launches_per_step": v["n"], "avg_us": v["avg_us"],
+            # per entry point: its calls per step (an MMQ call is two kernels, prep and main), the
+            # average call time and its share of the entry points' time
+            "per_kernel": {k: {"calls_per_step": v["n"], "avg_us": v["avg_us"],
                                "share": v["ms"] / sum(x["ms"] for x in per_kernel.values())}
                            for k, v in per_kernel.items()},
             "clocks": clk.summary(),
