@@ -612,7 +612,7 @@ def run_ours(args, ws, rank, local):
         del gk
         n_launch = reps * S * len(gl)
         per_kernel[key] = {"ms": k0.elapsed_time(k1) / (reps * S),          # per step
-                           "n": len(gl),                                     # launches per step
+                           "n": len(gl),                                     # calls per step
                            "avg_us": k0.elapsed_time(k1) / n_launch * 1e3,
                            "bytes": sum(N * (K // 256) * BYTES_PER_SB[q] for (_, q, N, K, _, _) in gl),
                            "ops": sum(2 * cfg["M"] * N * K for (_, _, N, K, _, _) in gl)}
@@ -633,7 +633,8 @@ def run_ours(args, ws, rank, local):
                              "achieved counts the algorithmic 2*M*N*K integer ops (the kernel issues "
                              + ("two f16 MMAs per product (A_hi, A_lo against the exact sc*q) plus the "
                                 "K/32-deep min-term contraction" if dom == "mmq_q4k" else
-                                "three f16 MMAs per product for the hi/lo split") + ")",
+                                "three f16 MMAs per product for the hi/lo split") + "); a launch here is one "
+                             "qk_mmq call, its prep kernel and its main kernel",
                 "avg_launch_us": dk["avg_us"]}
     else:
         units = weight_bytes(cfg)
