@@ -253,6 +253,59 @@ def test_q6k_qh_and_scale_golden():
     assert np.all(w[mask] == 1.0)
 
 
+@pytest.mark.parametrize("direction", ["raise", "lower"])
+def test_q6k_qh_every_pair_golden(direction):
+    # every qh bit pair, in both halves and both 16-value scale groups: one pair moved off the neutral
+    # 0b10 must change exactly the value the hand-derived table names, by 16 (or -16) times d * sc of
+    # the named scale (distinct scales 1..16, so a wrong scale index shows too)
+    g = gold("q6k_layout.json")
+    sc = list(range(1, 17))
+    pairs = set()
+    for p in g["qh_pair_probes"]:
+        t = p["pair"]
+        qh = [0xAA] * 64
+        if direction == "raise":
+            qh[p["byte"]] = 0xAA | (1 << (2 * t))                           # 0b10 -> 0b11: code 48
+        else:
+            qh[p["byte"]] = (0xAA & ~(3 << (2 * t))) | (1 << (2 * t))       # 0b10 -> 0b01: code 16
+        w = oracle.dequant_block(oracle.Q6_K, q6k_block(sc=sc, qh=qh))
+        want = (16.0 if direction == "raise" else -16.0) * sc[p["scale_index"]]
+        assert np.nonzero(w)[0].tolist() == [p["index"]], p
+        assert w[p["index"]] == want, p
+        pairs.add((p["byte"] // 32, p["byte"] % 32 >= 16, t))
+    assert len(pairs) == 16                       # 2 halves x 2 scale groups x 4 bit pairs
+
+
+def _q6k_int_matrix_numpy(w, N, K):
+    """Integer weights q - 32 of unit-scale Q6_K rows, rebuilt with numpy from the GGUF planes:
+    value 128h + 32t + l takes ql[64h + 32(t % 2) + l] (low nibble for t < 2, high for t >= 2)
+    and bits 2t, 2t+1 of qh[32h + l]."""
+    blk = w.reshape(N, K // 256, 210).astype(np.int64)
+    ql, qh = blk[:, :, 0:128], blk[:, :, 128:192]
+    parts = []
+    for h in range(2):
+        for t in range(4):
+            lo = ql[:, :, 64 * h + 32 * (t % 2):64 * h + 32 * (t % 2) + 32]
+            nib = (lo >> 4) if t >= 2 else (lo & 15)
+            hb = (qh[:, :, 32 * h:32 * h + 32] >> (2 * t)) & 3
+            parts.append((nib | (hb << 4)) - 32)
+    return np.concatenate(parts, axis=2).reshape(N, K)
+
+
+def test_q6k_contraction_integer_case_vs_numpy():
+    # d = 1 and every sc = 1: w = q - 32 (integers), so y is an exact integer matmul
+    rng = np.random.default_rng(14)
+    N, K, M = 5, 768, 3
+    w = np.concatenate([q6k_block(sc=[1] * 16, ql=rng.integers(0, 256, 128), qh=rng.integers(0, 256, 64))
+                        for _ in range(N * K // 256)])
+    codes = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    d_a = np.full((M, K // 32), 0x3C00, np.uint16)
+    y, ab = oracle.gemm(oracle.Q6_K, w, N, K, codes, d_a)
+    Wi = _q6k_int_matrix_numpy(w, N, K)
+    assert np.array_equal(y, (codes.astype(np.int64) @ Wi.T).astype(np.float64))
+    assert np.array_equal(ab, (np.abs(codes.astype(np.int64)) @ np.abs(Wi).T).astype(np.float64))
+
+
 def test_q6k_code_range_and_sign():
     # all bits set -> code 63 -> 31; all clear -> -32; negative scale flips sign
     w = oracle.dequant_block(oracle.Q6_K, q6k_block(ql=[0xFF] * 128, qh=[0xFF] * 64, sc=[-2] * 16))
@@ -338,10 +391,53 @@ def test_contraction_linearity_and_brute_force(qt):
     y2, _ = oracle.gemm(qtype, w, N, K, c2, d_a)
     y12, _ = oracle.gemm(qtype, w, N, K, (c1.astype(np.int16) + c2).astype(np.int8), d_a)
     assert np.allclose(y12, y1 + y2, rtol=1e-12, atol=1e-12)
-    # dense binary64 product of the dequantized matrices (numpy matmul as the library step)
-    W = oracle.dequant_matrix(qtype, w, N, K)
+    # dense binary64 product with the weights dequantized by this test's own loops (not the oracle's
+    # dequantizer; numpy's float16 decode and matmul are the library steps)
+    W = _dense_dequant(qt, w, N, K)
     xhat = np.repeat(d_a.view(np.float16).astype(np.float64), 32, axis=1) * c1
     assert np.allclose(y1, xhat @ W.T, rtol=1e-12, atol=1e-12)
+
+
+def _f16(b0, b1):
+    return float(np.array([b0 | (b1 << 8)], np.uint16).view(np.float16)[0])
+
+
+def _dense_dequant(qt, w, N, K):
+    """A second dequantizer, written separately from the oracle's, straight from the GGUF field
+    layout: Q4_K d, dmin, 12 scale bytes (6-bit sc/m), 128 code bytes whose group g holds sub-block
+    2g in its low nibbles and 2g + 1 in its high nibbles; Q6_K ql[128], qh[64], int8 sc[16], d."""
+    out = np.zeros((N, K))
+    bs = 144 if qt == "q4k" else 210
+    for n in range(N):
+        for b in range(K // 256):
+            blk = [int(v) for v in w[(n * (K // 256) + b) * bs:(n * (K // 256) + b + 1) * bs]]
+            vals = [0.0] * 256
+            if qt == "q4k":
+                d, dmin, S = _f16(blk[0], blk[1]), _f16(blk[2], blk[3]), blk[4:16]
+                for j in range(8):
+                    if j < 4:
+                        sc, m = S[j] & 63, S[j + 4] & 63
+                    else:
+                        sc = (S[j + 4] & 15) | ((S[j - 4] >> 6) << 4)
+                        m = (S[j + 4] >> 4) | ((S[j] >> 6) << 4)
+                    g, hi = j // 2, j % 2
+                    for l in range(32):
+                        byte = blk[16 + 32 * g + l]
+                        q = (byte >> 4) if hi else (byte & 15)
+                        vals[32 * j + l] = d * sc * q - dmin * m
+            else:
+                ql, qh = blk[0:128], blk[128:192]
+                sc = [v - 256 if v > 127 else v for v in blk[192:208]]
+                d = _f16(blk[208], blk[209])
+                for v in range(256):
+                    h, r = divmod(v, 128)
+                    t, l = divmod(r, 32)
+                    lo = ql[64 * h + 32 * (t % 2) + l]
+                    nib = (lo >> 4) if t >= 2 else (lo & 15)
+                    q = (nib | (((qh[32 * h + l] >> (2 * t)) & 3) << 4)) - 32
+                    vals[v] = d * sc[8 * h + 2 * t + l // 16] * q
+            out[n, 256 * b:256 * b + 256] = vals
+    return out
 
 
 def test_contraction_row_slices_and_threads_agree():
