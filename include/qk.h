@@ -373,7 +373,7 @@ int qk_gemv_q3k_f32(const void *w, const float *x, int64_t ldx,
  * Value limits: max |x| <= 32000 per 32-value block (the f16 operands
  * d_a * q_a and S_j / 16 must not overflow) and dmin * m < 63 for every
  * sub-block (the operand 1024 * dmin * m is an f16); LLM layers are far
- * inside both.
+ * inside both.  A call outside them sets QK_ERR_RANGE (qk_error_flags).
  * workspace: device scratch of at least qk_mmq_workspace_bytes(M, N, K)
  *   bytes, 256-byte aligned, not overlapping any other argument.  The call
  *   writes it (the q8_1 activation expanded once per 128-row tile into the
@@ -405,7 +405,8 @@ int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales,
  * the workspace (same size, qk_mmq_workspace_bytes; the sums S are not
  * used) and every other argument rule are those of qk_mmq_q4k.  Value
  * limits: max |x| <= 65000 per 32-value block and |w| < 255 for every
- * dequantized weight (the weight operand is scaled by 256).
+ * dequantized weight (the weight operand is scaled by 256); a call outside
+ * them sets QK_ERR_RANGE (qk_error_flags).
  */
 int qk_mmq_q6k(const void *w, const int8_t *codes, const void *scales,
                int64_t M, int64_t N, int64_t K,
@@ -437,16 +438,27 @@ int qk_mmq_q4k_noalloc(const void *w, const int8_t *codes, const void *scales,
                        unsigned flags, void *stream);
 
 /* ========================================================== error flags
- * Kernels that hand work between warps with mbarriers (qk_mmq_q4k) bound
- * every wait.  A wait that gives up -- which only happens if the hardware or
- * the kernel misbehaves -- sets bit QK_ERR_TIMEOUT of a device-wide flag
- * word; the kernel then skips its remaining waits and returns, and its output
- * is undefined.  qk_error_flags copies that word to *flags (synchronously,
- * on the current device) and, when `clear` is non-zero, resets it to 0.
- * Not part of the method: library bookkeeping only.
+ * A device-wide flag word that the MMQ kernels set when something went wrong
+ * that the host could not see before the launch (invariant violations are
+ * reported, never passed over silently: minfer "15 . The CUDA backend"
+ * sec. 3.4).  Bits:
+ *  QK_ERR_TIMEOUT  a bounded mbarrier wait gave up -- which only happens if
+ *                  the hardware or the kernel misbehaves; the kernel then
+ *                  skips its remaining waits and returns.
+ *  QK_ERR_RANGE    an input is outside the MMQ's value limits, so an f16
+ *                  operand would overflow: a q8_1 block with d_a * 127 >
+ *                  32000 (qk_mmq_q4k) or > 65000 (qk_mmq_q6k), a Q4_K
+ *                  sub-block with dmin * m >= 63, or a Q6_K superblock whose
+ *                  largest |d * sc| * 32 is >= 255 (a weight can reach
+ *                  |w| >= 255).  The GEMVs have no such limits.
+ * With either bit set the output of the call is undefined.  qk_error_flags
+ * copies the word to *flags (synchronously, on the current device) and, when
+ * `clear` is non-zero, resets it to 0.  The word is not cleared by the
+ * kernels: it collects every call since the last clear.
  * Returns QK_E_NULL if flags is NULL, QK_E_CUDA if the copy fails.
  */
 #define QK_ERR_TIMEOUT 1u
+#define QK_ERR_RANGE 2u
 int qk_error_flags(unsigned *flags, int clear);
 
 #ifdef __cplusplus

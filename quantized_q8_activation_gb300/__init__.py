@@ -5,6 +5,13 @@ the C ABI declared in include/qk.h.  PyTorch provides device memory and
 streams.  There is no CPU fallback: if the shared library is missing or a
 call fails, an exception is raised.
 
+The C entry points allocate nothing.  These wrappers do, for convenience:
+an output (or q8_1 buffer) that is not passed in is allocated with torch, and
+mmq_q4k / mmq_q6k allocate their workspace with torch when none is given
+(pass `workspace=` to keep a steady-state loop free of allocations, or use
+mmq_q4k_noalloc).  Each call runs with the device of its tensors current, so
+the library's per-device set-up and launches go to that device.
+
 Typical use::
 
     import quantized_q8_activation_gb300 as qk
@@ -33,6 +40,9 @@ Q3_K = 6
 LAUNCH_PDL = 1
 MMQ_TILE_256 = 2
 MMQ_TILE_128 = 4
+
+ERR_TIMEOUT = 1     # error_flags(): a bounded in-kernel wait gave up
+ERR_RANGE = 2       # error_flags(): an MMQ input was outside the value limits (see include/qk.h)
 
 QK_OK = 0
 STATUS = {0: "QK_OK", -1: "QK_E_NULL", -2: "QK_E_SHAPE", -3: "QK_E_ALIGN", -4: "QK_E_ALIAS",
@@ -134,6 +144,11 @@ def _cuda(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _on(t: torch.Tensor):
+    """Make t's device the current CUDA device for the call (the C ABI works on the current device)."""
+    return torch.cuda.device(t.device)
+
+
 # ------------------------------------------------------------------- sizes
 
 def q8_1_bytes(M: int, K: int) -> tuple[int, int]:
@@ -155,7 +170,8 @@ def mmq_workspace_bytes(M: int, N: int, K: int) -> int:
 
 
 def error_flags(clear: bool = True) -> int:
-    """Device error word (bit 0: a bounded in-kernel wait gave up); cleared when `clear`."""
+    """Device error word (ERR_TIMEOUT: a bounded in-kernel wait gave up; ERR_RANGE: an MMQ input
+    outside the value limits); cleared when `clear`."""
     f = ctypes.c_uint()
     _check(lib().qk_error_flags(ctypes.byref(f), int(clear)), "qk_error_flags")
     return f.value
@@ -179,8 +195,9 @@ def quantize_q8_1(x: torch.Tensor, codes=None, scales=None, pdl: bool = False, s
     if codes is None or scales is None:
         codes, scales = empty_q8_1(M, K, x.device)
     _cuda(codes, "codes"), _cuda(scales, "scales")
-    st = lib().qk_quantize_q8_1(x.data_ptr(), x.stride(0) if M > 1 else K, M, K, codes.data_ptr(),
-                                scales.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
+    with _on(x):
+        st = lib().qk_quantize_q8_1(x.data_ptr(), x.stride(0) if M > 1 else K, M, K, codes.data_ptr(),
+                                    scales.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
     _check(st, "qk_quantize_q8_1")
     return codes, scales
 
@@ -201,9 +218,10 @@ def rmsnorm_q8_1(x: torch.Tensor, g: torch.Tensor, eps: float, r=None, h_out=Non
     if codes is None or scales is None:
         codes, scales = empty_q8_1(M, K, x.device)
     _cuda(codes, "codes"), _cuda(scales, "scales")
-    st = lib().qk_rmsnorm_q8_1(x.data_ptr(), x.stride(0) if M > 1 else K, _p(r), g.data_ptr(), float(eps), M, K,
-                               _p(h_out), _p(y), codes.data_ptr(), scales.data_ptr(), LAUNCH_PDL if pdl else 0,
-                               _stream(stream))
+    with _on(x):
+        st = lib().qk_rmsnorm_q8_1(x.data_ptr(), x.stride(0) if M > 1 else K, _p(r), g.data_ptr(), float(eps), M,
+                                   K, _p(h_out), _p(y), codes.data_ptr(), scales.data_ptr(),
+                                   LAUNCH_PDL if pdl else 0, _stream(stream))
     _check(st, "qk_rmsnorm_q8_1")
     return codes, scales
 
@@ -221,8 +239,9 @@ def swiglu_q8_1(gu: torch.Tensor, F: int, h=None, codes=None, scales=None, pdl: 
     if codes is None or scales is None:
         codes, scales = empty_q8_1(M, F, gu.device)
     _cuda(codes, "codes"), _cuda(scales, "scales")
-    st = lib().qk_swiglu_q8_1(gu.data_ptr(), gu.stride(0) if M > 1 else gu.shape[1], M, F, _p(h), codes.data_ptr(),
-                              scales.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
+    with _on(gu):
+        st = lib().qk_swiglu_q8_1(gu.data_ptr(), gu.stride(0) if M > 1 else gu.shape[1], M, F, _p(h),
+                                  codes.data_ptr(), scales.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
     _check(st, "qk_swiglu_q8_1")
     return codes, scales
 
@@ -237,7 +256,8 @@ def repack(qtype: int, gguf: torch.Tensor, N: int, K: int, out=None, stream=None
     if out is None:
         out = torch.empty(nbytes, dtype=torch.uint8, device=gguf.device)
     _cuda(out, "out")
-    _check(lib().qk_repack(qtype, gguf.data_ptr(), N, K, out.data_ptr(), _stream(stream)), "qk_repack")
+    with _on(gguf):
+        _check(lib().qk_repack(qtype, gguf.data_ptr(), N, K, out.data_ptr(), _stream(stream)), "qk_repack")
     return out
 
 
@@ -250,8 +270,9 @@ def _gemv(fn, name, w, codes, scales, N, K, residual, y, pdl, stream):
     _cuda(y, "y")
     if residual is not None:
         _cuda(residual, "residual")
-    st = fn(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
-            LAUNCH_PDL if pdl else 0, _stream(stream))
+    with _on(codes):
+        st = fn(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
+                LAUNCH_PDL if pdl else 0, _stream(stream))
     _check(st, name)
     return y
 
@@ -298,8 +319,9 @@ def _gemv_f32(fn, name, w, x, N, K, residual, y, codes_out, scales_out, pdl, str
     _cuda(y, "y")
     if residual is not None:
         _cuda(residual, "residual")
-    st = fn(w.data_ptr(), x.data_ptr(), x.stride(0) if M > 1 else K, M, N, K, _p(residual), y.data_ptr(),
-            _p(codes_out), _p(scales_out), LAUNCH_PDL if pdl else 0, _stream(stream))
+    with _on(x):
+        st = fn(w.data_ptr(), x.data_ptr(), x.stride(0) if M > 1 else K, M, N, K, _p(residual), y.data_ptr(),
+                _p(codes_out), _p(scales_out), LAUNCH_PDL if pdl else 0, _stream(stream))
     _check(st, name)
     return y
 
@@ -342,12 +364,13 @@ def gemv_q3k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=N
 
 def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None, tile=None):
     """Prefill contraction over a repacked Q4_K weight, any M.  tile: None (the library picks
-    the tile width), 256 or 128."""
+    the tile width), 256 or 128.  workspace: a uint8 CUDA tensor of at least
+    mmq_workspace_bytes(M, N, K) bytes; when None, this wrapper allocates one with torch."""
     return _mmq("qk_mmq_q4k", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile)
 
 
 def mmq_q6k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None, tile=None):
-    """Prefill contraction over a repacked Q6_K weight, any M."""
+    """Prefill contraction over a repacked Q6_K weight, any M (workspace as for mmq_q4k)."""
     return _mmq("qk_mmq_q6k", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile)
 
 
@@ -362,8 +385,9 @@ def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile=N
         workspace = torch.empty(need, dtype=torch.uint8, device=codes.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     flags = (LAUNCH_PDL if pdl else 0) | {None: 0, 256: MMQ_TILE_256, 128: MMQ_TILE_128}[tile]
-    st = getattr(lib(), fn)(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
-                            _p(workspace), wsb, flags, _stream(stream))
+    with _on(codes):
+        st = getattr(lib(), fn)(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual),
+                                y.data_ptr(), _p(workspace), wsb, flags, _stream(stream))
     _check(st, fn)
     return y
 
@@ -378,7 +402,8 @@ def mmq_q4k_noalloc(w, codes, scales, N, K, residual=None, y=None, pdl=False, st
         _cuda(t, n)
     if y is None:
         y = torch.empty((M, N), dtype=torch.float32, device=codes.device)
-    st = lib().qk_mmq_q4k_noalloc(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual),
-                                  y.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
+    with _on(codes):
+        st = lib().qk_mmq_q4k_noalloc(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual),
+                                      y.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
     _check(st, "qk_mmq_q4k_noalloc")
     return y

@@ -50,6 +50,19 @@ inline int launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
 // Number of SMs of the current device (queried once per device id).
 int sm_count();
 
+// Devices the per-device caches of the library cover (ids 0 .. kMaxDevices-1).
+constexpr int kMaxDevices = 64;
+
+// Id of the host thread's current CUDA device, or -1 if it cannot be read or is
+// past kMaxDevices.  Every one-time set-up (kernel attributes, symbol addresses)
+// is cached per device id, since each device holds its own copy of the module.
+inline int device_slot()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
 // Largest dynamic shared memory a CTA may opt in to on the current device.
 size_t max_smem_optin();
 

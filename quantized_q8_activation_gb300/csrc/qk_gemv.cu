@@ -1035,8 +1035,8 @@ __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) g
 
 typedef void (*gemv_fn)(const GemvArgs);
 
-// per kernel: largest dynamic shared memory opted in so far (per process)
-std::atomic<int> g_smem_set[6][2][8];
+// per device and kernel: largest dynamic shared memory opted in so far
+std::atomic<int> g_smem_set[qk::kMaxDevices][6][2][8];
 
 int prepare(gemv_fn kern, std::atomic<int> &done, size_t smem)
 {
@@ -1130,7 +1130,9 @@ int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, uns
                         (size_t)M * K + (size_t)M * (K / 32) * (q6side ? 16 : 8);
     if (smem > qk::max_smem_optin()) return QK_E_SHAPE;
     gemv_fn kern = fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M);
-    int st = prepare(kern, g_smem_set[qtype - 1][fused ? 1 : 0][M - 1], smem);
+    const int dev = qk::device_slot();
+    if (dev < 0) return QK_E_CUDA;
+    int st = prepare(kern, g_smem_set[dev][qtype - 1][fused ? 1 : 0][M - 1], smem);
     if (st != QK_OK) return st;
     int64_t grid = (int64_t)kCtasPerSm * qk::sm_count();
     const int64_t groups = (N + kRowsPerItem - 1) / kRowsPerItem;

@@ -73,6 +73,12 @@
 
 __device__ unsigned g_qk_errors;
 
+// an operand of the contraction would leave the binary16 range: flag it (one atomic per warp)
+__device__ __forceinline__ void flag_range(bool bad)
+{
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(&g_qk_errors, QK_ERR_RANGE);
+}
+
 namespace {
 
 using namespace qk::tc;
@@ -231,6 +237,9 @@ __global__ void __launch_bounds__(256) mmq_prep_kernel(const int8_t *__restrict_
         }
         const __half dah = __ushort_as_half((unsigned short)dbits);
         const __half2 d2 = __halves2half2(dah, dah);
+        // value limits of the f16 operands: d_a * 127 (the block's largest |x|) at most 32000 when the
+        // sums S / 16 are built (Q4_K), 65000 otherwise (Q6_K); beyond them the result is undefined
+        flag_range(__half2float(dah) * 127.0f > (wsS ? 32000.0f : 65000.0f));
         const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         uint8_t *tA = wsA + ((size_t)mt * nit + 8 * sb + j) * ABLOCK;
 #pragma unroll
@@ -307,6 +316,12 @@ __device__ __forceinline__ void convert_stage_q6(uint8_t *smem, uint64_t *bar, C
         cs.d = cs.dn;
         if (sb + 1 < B) cs.dn = q6_d<L::BN>(a, t, sb + 1, row);
         else if (t + (int)gridDim.x < a.mtiles * a.ntiles) cs.dn = q6_d<L::BN>(a, t + gridDim.x, 0, row);
+        // value limit |w| < 255: |w| <= 32 |d sc| over the codes of a sub-block; checked once per
+        // superblock with its largest |sc| (flags every sub-block that can reach 255)
+        const uint32_t am = __vmaxu4(__vmaxu4(__vabsss4(cs.mt.x), __vabsss4(cs.mt.y)),
+                                     __vmaxu4(__vabsss4(cs.mt.z), __vabsss4(cs.mt.w)));
+        const uint32_t am2 = __vmaxu4(am, am >> 16), amax = max(am2 & 0xffu, (am2 >> 8) & 0xffu);
+        flag_range(32.0f * fabsf(__half2float(__ushort_as_half((unsigned short)cs.d))) * (float)amax >= 255.0f);
     }
     if (q == 0) {
         wait_bar(&bar[B_RFULL + rs], (gu / NRAW) & 1);
@@ -666,13 +681,14 @@ __device__ __forceinline__ void w_sc(uint32_t x, uint32_t sc, uint32_t &p01, uin
 // bits: the binary32 value with its 13 low mantissa bits cleared) and lo (the remaining at most 6
 // bits), exact down to Mw' = 2^-8 (below it lo's last bit falls under the f16 subnormal step);
 // word i holds sub-blocks 2i, 2i+1
-__device__ __forceinline__ void mins_hilo(const uint4 &mt, uint32_t (&hi)[4], uint32_t (&lo)[4])
+__device__ __forceinline__ void mins_hilo(const uint4 &mt, uint32_t (&hi)[4], uint32_t (&lo)[4], bool &bad)
 {
     const float dmin = __half2float(__ushort_as_half((unsigned short)(mt.x >> 16))) * kMScale;
 #pragma unroll
     for (int g = 0; g < 4; g++) {
         const uint32_t r = q4_group(mt, g);
         const float w0 = dmin * (float)((r >> 12) & 63u), w1 = dmin * (float)((r >> 18) & 63u);   // exact
+        bad |= fmaxf(w0, w1) >= 63.0f * kMScale;                  // value limit dmin * m < 63
         const float h0 = __uint_as_float(__float_as_uint(w0) & 0xFFFFE000u);
         const float h1 = __uint_as_float(__float_as_uint(w1) & 0xFFFFE000u);
         hi[g] = h2u(__floats2half2_rn(h0, h1));
@@ -929,8 +945,10 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                     r1 = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss1 * L::SBR + row * 16);
                 }
                 uint32_t h0[4], l0[4], h1[4], l1[4];
-                mins_hilo(r0, h0, l0);
-                mins_hilo(r1, h1, l1);
+                bool bad = false;
+                mins_hilo(r0, h0, l0, bad);
+                mins_hilo(r1, h1, l1, bad);
+                flag_range(bad);
                 if (gs >= NS) wait_bar(&bar[L::EMPTY + st], ((gs / NS) + 1) & 1);
                 uint8_t *w0 = smem + st * L::STAGE + 2 * ATILE;
                 sts128(w0, sw64(row, 0), h0[0], h0[1], h0[2], h0[3]);
@@ -1064,7 +1082,10 @@ size_t ws_bytes(int64_t M, int64_t K)
 template <int BN>
 int set_attrs_q4()
 {
-    static std::atomic<int> done{0};
+    static std::atomic<int> done_dev[qk::kMaxDevices];
+    const int dev = qk::device_slot();
+    if (dev < 0) return QK_E_CUDA;
+    std::atomic<int> &done = done_dev[dev];
     if (done.load()) return QK_OK;
     if (cudaFuncSetAttribute(mmq_q4k_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan4<BN>::SMEM) !=
             cudaSuccess ||
@@ -1092,7 +1113,10 @@ int launch_mmq_q4(const MmqArgs &args, const MmqMaps &maps, int64_t tiles, cudaS
 template <int QT, int BN>
 int set_attrs()
 {
-    static std::atomic<int> done{0};
+    static std::atomic<int> done_dev[qk::kMaxDevices];
+    const int dev = qk::device_slot();
+    if (dev < 0) return QK_E_CUDA;
+    std::atomic<int> &done = done_dev[dev];
     if (done.load()) return QK_OK;
     if (cudaFuncSetAttribute(mmq_kernel<QT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Plan<QT, BN>::SMEM) != cudaSuccess ||

@@ -34,9 +34,9 @@ static __device__ __align__(256) uint8_t g_mmq_static_ws[kStaticWsBytes];
 // per-device cache of the array's address
 void *static_ws_address()
 {
-    static std::atomic<void *> cache[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    static std::atomic<void *> cache[qk::kMaxDevices];
+    const int dev = qk::device_slot();
+    if (dev < 0) return nullptr;
     void *p = cache[dev].load(std::memory_order_acquire);
     if (p) return p;
     if (cudaGetSymbolAddress(&p, g_mmq_static_ws) != cudaSuccess || !p) return nullptr;

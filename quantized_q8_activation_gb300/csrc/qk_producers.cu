@@ -176,7 +176,7 @@ int carveout_once(Kern kern, std::atomic<int> &flag)
     return QK_OK;
 }
 
-std::atomic<int> g_carve[6];
+std::atomic<int> g_carve[qk::kMaxDevices][6];     // per device and kernel
 
 }  // namespace
 
@@ -209,24 +209,26 @@ extern "C" int qk_rmsnorm_q8_1(const float *x, int64_t ldx, const float *r, cons
     const bool pdl = (flags & QK_LAUNCH_PDL) != 0;
     const dim3 grid((unsigned)M), block(kThreads);
     cudaStream_t st = (cudaStream_t)stream;
+    const int dev = qk::device_slot();
+    if (dev < 0) return QK_E_CUDA;
     int s;
     if (per <= 1) {
-        if ((s = carveout_once(rmsnorm_q8_1_kernel<1>, g_carve[0])) != QK_OK) return s;
+        if ((s = carveout_once(rmsnorm_q8_1_kernel<1>, g_carve[dev][0])) != QK_OK) return s;
         return qk::launch(rmsnorm_q8_1_kernel<1>, grid, block, 0, st, pdl, a);
     }
     if (per <= 2) {
-        if ((s = carveout_once(rmsnorm_q8_1_kernel<2>, g_carve[1])) != QK_OK) return s;
+        if ((s = carveout_once(rmsnorm_q8_1_kernel<2>, g_carve[dev][1])) != QK_OK) return s;
         return qk::launch(rmsnorm_q8_1_kernel<2>, grid, block, 0, st, pdl, a);
     }
     if (per <= 4) {
-        if ((s = carveout_once(rmsnorm_q8_1_kernel<4>, g_carve[2])) != QK_OK) return s;
+        if ((s = carveout_once(rmsnorm_q8_1_kernel<4>, g_carve[dev][2])) != QK_OK) return s;
         return qk::launch(rmsnorm_q8_1_kernel<4>, grid, block, 0, st, pdl, a);
     }
     if (per <= 8) {
-        if ((s = carveout_once(rmsnorm_q8_1_kernel<8>, g_carve[3])) != QK_OK) return s;
+        if ((s = carveout_once(rmsnorm_q8_1_kernel<8>, g_carve[dev][3])) != QK_OK) return s;
         return qk::launch(rmsnorm_q8_1_kernel<8>, grid, block, 0, st, pdl, a);
     }
-    if ((s = carveout_once(rmsnorm_q8_1_kernel<0>, g_carve[4])) != QK_OK) return s;
+    if ((s = carveout_once(rmsnorm_q8_1_kernel<0>, g_carve[dev][4])) != QK_OK) return s;
     return qk::launch(rmsnorm_q8_1_kernel<0>, grid, block, 0, st, pdl, a);
 }
 
@@ -244,8 +246,10 @@ extern "C" int qk_swiglu_q8_1(const float *gu, int64_t ldgu, int64_t M, int64_t 
     if (qk::overlaps(h, hb, gu, gb) || qk::overlaps(codes, cb, gu, gb) || qk::overlaps(scales, sb, gu, gb) ||
         qk::overlaps(h, hb, codes, cb) || qk::overlaps(h, hb, scales, sb) || qk::overlaps(codes, cb, scales, sb))
         return QK_E_ALIAS;
+    const int dev = qk::device_slot();
+    if (dev < 0) return QK_E_CUDA;
     int s;
-    if ((s = carveout_once(swiglu_q8_1_kernel, g_carve[5])) != QK_OK) return s;
+    if ((s = carveout_once(swiglu_q8_1_kernel, g_carve[dev][5])) != QK_OK) return s;
     const int64_t gx = (F / 4 + kThreads - 1) / kThreads;
     return qk::launch(swiglu_q8_1_kernel, dim3((unsigned)gx, (unsigned)M), dim3(kThreads), 0, (cudaStream_t)stream,
                       (flags & QK_LAUNCH_PDL) != 0, gu, ldgu, (int)F, h, codes,

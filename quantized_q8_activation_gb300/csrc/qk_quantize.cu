@@ -70,10 +70,12 @@ extern "C" int qk_quantize_q8_1(const float *x, int64_t ldx, int64_t M, int64_t 
     if (qk::overlaps(x, xbytes, codes, cbytes) || qk::overlaps(x, xbytes, scales, sbytes) ||
         qk::overlaps(codes, cbytes, scales, sbytes))
         return QK_E_ALIAS;
-    static std::atomic<int> carveout_set{0};
-    if (!carveout_set.load(std::memory_order_relaxed)) {
+    static std::atomic<int> carveout_set[qk::kMaxDevices];          // per device
+    const int dev = qk::device_slot();
+    if (dev < 0) return QK_E_CUDA;
+    if (!carveout_set[dev].load(std::memory_order_relaxed)) {
         if (qk::max_carveout(quantize_q8_1_kernel) != cudaSuccess) return QK_E_CUDA;
-        carveout_set.store(1, std::memory_order_relaxed);
+        carveout_set[dev].store(1, std::memory_order_relaxed);
     }
     const int nb_row = (int)(K / 32);
     const int64_t nblocks = M * nb_row;

@@ -408,7 +408,45 @@ def test_mmq_superblock_scale_special_cases(qt):
     codes, scales = q8(synth.activations(M, K, seed=93))
     c, d = q8_host(codes, scales)
     y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+    qk.error_flags(clear=True)
     for tile in (256, 128):
         y = mmq_fn(qt)(wr, codes, scales, N, K, tile=tile).cpu().numpy()
         check(y, y_ref, ab, what=f"mmq {qt} special scales tile={tile}")
         assert np.all(y[:, 3::5] == 0)
+    assert qk.error_flags(clear=True) == 0            # inside the value limits: no range flag
+
+
+def _f16_bytes(v):
+    return np.frombuffer(np.float16(v).tobytes(), np.uint8)
+
+
+@pytest.mark.parametrize("case", ["q4k_x", "q4k_min", "q6k_x", "q6k_w", "inside"])
+def test_mmq_value_limits_set_range_flag(case):
+    """An input outside the MMQ's value limits sets QK_ERR_RANGE (the f16 operands would overflow,
+    so the output is undefined); the same call inside them leaves the word clear."""
+    qt = "q6k" if case.startswith("q6k") else "q4k"
+    M, N, K = 24, 96, 512
+    w = synth.weights(qt, N, K, seed=31).copy()
+    blocks = w.reshape(N, K // 256, oracle.BLOCK_BYTES[QT[qt][1]])
+    x = synth.activations(M, K, seed=32)
+    if case == "q4k_x":
+        x[5, 64:96] *= np.float32(40000.0 / np.abs(x[5, 64:96]).max())          # d_a * 127 = 40000 > 32000
+    elif case == "q4k_min":
+        blocks[7, 1, 8] = (blocks[7, 1, 8] & 0xC0) | 63                        # m_0 = 63 (GGUF scale byte 4)
+        blocks[7, 1, 2:4] = _f16_bytes(70.0 / 63.0)                            # dmin * m_0 = 70 >= 63
+    elif case == "q6k_x":
+        x[3, 0:32] *= np.float32(70000.0 / np.abs(x[3, 0:32]).max())           # d_a * 127 = 70000 > 65000
+    elif case == "q6k_w":
+        blocks[11, 0, 192] = np.uint8(0xE0)                                    # sc[0] = -32
+        blocks[11, 0, 208:210] = _f16_bytes(0.25)                              # 32 * |d sc| = 256 >= 255
+    wr = qk.repack(QT[qt][0], dev(w), N, K)
+    codes, scales = q8(x)
+    qk.error_flags(clear=True)
+    mmq_fn(qt)(wr, codes, scales, N, K)
+    torch.cuda.synchronize()
+    flags = qk.error_flags(clear=True)
+    if case == "inside":
+        assert flags == 0
+    else:
+        assert flags & qk.ERR_RANGE, (case, flags)
+        assert not flags & qk.ERR_TIMEOUT
