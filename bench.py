@@ -9,7 +9,7 @@ Workloads (benchmark configurations; shapes of the named models, synthetic
 data of the stated distributions):
   0  single Q4_K GEMV 4096 x 4096, M = 1
   1  Llama-3-8B decode layer, M = 1: QKV 6144x4096, attn-out 4096x4096 (+res),
-     gate||up 28672x4096 (one q8_1 activation), down 4096x14336 (+res)   [default]
+     gate||up 28672x4096 (one q8_1 activation), down 4096x14336 (+res)   [headline]
   2  Q6_K output head 128256 x 4096, M = 1
   3  config 1 + config 2 at M = 4
   4  Qwen2-7B prefill MMQ at M = 2048: QKV 4608x3584, attn-out 3584x3584 (+res),
@@ -25,11 +25,19 @@ data of the stated distributions):
   9  config 1 with every weight in Q3_K
  10  config 1 with every weight in Q2_K
 
+Default run: config 1 is the headline line; configs 0, 2, 3 and 4 are timed
+with the same --steps / --warmup and reported under "configs" in the same
+JSON line, with the measured tensor-core peaks for the MMQ.  --config N times
+only workload N.
+
 Timing: W untimed warm-up steps, then exactly K steps replayed from CUDA
 graphs (programmatic dependent launch between the kernels), bracketed by a
-barrier and torch.cuda.synchronize(), timed with CUDA events on the launching
-stream.  Weight copies rotate between steps so the working set exceeds L2.
-`--impl reference` times the CPU oracle on the host cores instead.
+barrier and torch.cuda.synchronize().  The K steps are split into R >= 5
+graph replays of S steps, each timed with its own CUDA events on the
+launching stream; ms_per_step is the median replay per step, with the
+spread and the all-K total beside it.  Weight copies rotate between steps so
+the working set exceeds L2.  `--impl reference` times the CPU oracle on the
+host cores instead.
 """
 from __future__ import annotations
 
@@ -179,6 +187,17 @@ def slots(cfg):
 
 # ------------------------------------------------------------------ workload
 
+def packed(shapes, device, align: int = 64):
+    """One float32 buffer holding a tensor of each shape (offsets aligned to `align` elements);
+    returns the buffer and the views."""
+    offs, n = [], 0
+    for sh in shapes:
+        offs.append(n)
+        n += -(-int(np.prod(sh)) // align) * align
+    buf = torch.empty(max(n, align), dtype=torch.float32, device=device)
+    return buf, [buf[o:o + int(np.prod(sh))].view(*sh) for o, sh in zip(offs, shapes)]
+
+
 class Workload:
     """Device buffers for one configuration: repacked weights (several copies),
     f32 activations and residuals, q8_1 buffers and outputs."""
@@ -201,22 +220,29 @@ class Workload:
             for c in range(copies):
                 self.w[c][name] = qk.repack(OTYPE[q], g, N, K)
             del g
-        self.host_x = {s: synth.activations(M, K, seed=seed, tag=s) for s, K in slots(cfg)
-                       if s in cfg.get("inputs", [s])}
-        self.x = {s: torch.from_numpy(v).to(device) for s, v in self.host_x.items()}
+        # inputs (f32 activations and residuals) and outputs live in one packed device buffer
+        # each, so an end-to-end step moves them with one copy per direction
+        chain = cfg["kind"] == "chain"
+        x_specs = [(s, (M, K)) for s, K in slots(cfg) if s in cfg.get("inputs", [s])]
+        r_specs = [(name, (M, N)) for (name, _, N, _, res, _) in cfg["gemms"] if res and not (chain and name == "down")]
+        y_specs = [(name, (M, N)) for (name, _, N, _, _, _) in cfg["gemms"]]
+        self.inbuf, views = packed([sh for _, sh in x_specs + r_specs], device)
+        self.x = {s: v for (s, _), v in zip(x_specs, views[:len(x_specs)])}
+        self.r = {n: v for (n, _), v in zip(r_specs, views[len(x_specs):])}
+        self.outbuf, yv = packed([sh for _, sh in y_specs], device)
+        self.y = {n: v for (n, _), v in zip(y_specs, yv)}
+        self.host_x = {s: synth.activations(M, sh[1], seed=seed, tag=s) for s, sh in x_specs}
+        self.host_r = {n: synth.residual(M, sh[1], seed=seed, tag=n) for n, sh in r_specs}
+        for s, v in self.host_x.items():
+            self.x[s].copy_(torch.from_numpy(v))
+        for n, v in self.host_r.items():
+            self.r[n].copy_(torch.from_numpy(v))
         self.q8 = {s: qk.empty_q8_1(M, K, device) for s, K in slots(cfg)}
-        self.host_r, self.r, self.y = {}, {}, {}
-        for (name, _, N, _, res, _) in cfg["gemms"]:
-            if res:
-                self.host_r[name] = synth.residual(M, N, seed=seed, tag=name)
-                self.r[name] = torch.from_numpy(self.host_r[name]).to(device)
-            self.y[name] = torch.empty((M, N), dtype=torch.float32, device=device)
         self.host_g = {}
-        if cfg["kind"] == "chain":
+        if chain:
             self.host_g = chain_norm_weights(cfg, seed)
             self.g = {t: torch.from_numpy(v).to(device) for t, v in self.host_g.items()}
             self.r["down"] = self.y["attn_out"]       # down adds the residual stream h = attn-out's output
-            del self.host_r["down"]
         self.ws = None
         if cfg["kind"] == "mmq":
             need = max(qk.mmq_workspace_bytes(M, N, K) for (_, _, N, K, _, _) in cfg["gemms"])
@@ -448,9 +474,9 @@ def oracle_step(cfg, host_w, host_x, host_r, threads: int, m_rows=None, n_frac: 
     return ops if cfg["kind"] == "mmq" else wbytes
 
 
-def cpu_baseline(wl_host, cfg, budget_s: float = 12.0, host_g=None):
-    """Time the oracle as it stands on the host cores; bounded sample."""
-    threads = os.cpu_count() or 1
+def cpu_baseline(wl_host, cfg, budget_s: float = 12.0, host_g=None, threads=None):
+    """Time the oracle as it stands on the host cores (all of them, or `threads`); bounded sample."""
+    threads = threads or os.cpu_count() or 1
     host_w, host_x, host_r = wl_host
     if cfg["kind"] == "mmq":
         m_rows = 8                                      # 8 of the 2048 tokens per sample step
@@ -520,204 +546,342 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+class StepGraphs:
+    """The timed region of K steps, step i using weight copy i % C.
+    K <= S (one graph holds the region): the region is one CUDA graph of K steps, so programmatic
+    dependent launch links every step, and it is replayed `regions` times, each replay timed.
+    K > S: the region is R = K // S graphs of S steps (R >= 5 by the choice of S) plus a remainder
+    graph, each full replay timed.  Graphs with the same copy sequence are captured once."""
+
+    def __init__(self, step_fn, K: int, S: int, C: int, stream, regions: int = 5):
+        if K <= S:
+            S = K
+        self.S = S
+        self.R, self.rem = (regions, 0) if K == S else (K // S, K % S)
+        cache = {}
+
+        def graph(off, n):
+            key = (off, n)
+            if key not in cache:
+                cache[key] = capture(lambda: [step_fn((off + i) % C) for i in range(n)], stream)
+            return cache[key]
+
+        self.plan = [graph(0 if K == S else (r * S) % C, S) for r in range(self.R)]
+        self.tail = graph((self.R * S) % C, self.rem) if self.rem else None
+        self.graphs = list(cache.values())
+
+    def warm(self):
+        for g in self.graphs:
+            g.replay()
+        torch.cuda.synchronize()
+
+    def run_timed(self, stream):
+        """Replay the region (K steps, or `regions` times K steps when one graph holds it), each
+        full replay between its own pair of events; returns the per-step milliseconds of each
+        full replay and the total milliseconds."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(self.R + 2)]
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for r, g in enumerate(self.plan):
+                g.replay()
+                ev[r + 1].record(stream)
+            if self.tail is not None:
+                self.tail.replay()
+            ev[-1].record(stream)
+        torch.cuda.synchronize()
+        per = [ev[r].elapsed_time(ev[r + 1]) / self.S for r in range(self.R)]
+        return per, ev[0].elapsed_time(ev[-1])
+
+
+def steps_per_replay(K: int, graph_steps: int) -> int:
+    """Steps per graph: all K when one graph of at most graph_steps holds them (the region is then
+    replayed five times), else at most graph_steps and small enough for five replays or more."""
+    return K if K <= graph_steps else max(1, min(graph_steps, K // 5))
+
+
+def time_graphs(step_fn, K, S, C, stream):
+    sg = StepGraphs(step_fn, K, S, C, stream)
+    sg.warm()
+    per, total = sg.run_timed(stream)
+    del sg
+    return per, total
+
+
+def kernel_groups(wl, front_end):
+    """The step's launches grouped by kernel family (the quantize kernels as their own group), in
+    step order: {key: [(kind, gemm or slot, fused)]}."""
+    cfg, groups, done = wl.cfg, {}, set()
+    for gemm in cfg["gemms"]:
+        f = gemm_fused(front_end, cfg, gemm)
+        if not f and gemm[5] not in done and cfg["kind"] != "chain":     # the chain's producers quantize
+            groups.setdefault("quantize_q8_1", []).append(("quantize", gemm[5], False))
+            done.add(gemm[5])
+        groups.setdefault(wl.kernel_key(gemm, f), []).append(("gemm", gemm, f))
+    return groups
+
+
+def measure_config(cfg_id, args, stream, ws, device, peaks_meas=None, headline=False):
+    """Time one workload: the K-step region (median of replays), each kernel family on its own,
+    the end-to-end path with host buffers, and the roofline of the dominant kernel."""
+    import quantized_q8_activation_gb300 as qk
+    cfg = CONFIGS[cfg_id]
+    front_end = args.front_end
+    wl = Workload(cfg_id, seed=0, copies=args.copies)
+    C, K = wl.copies, args.steps
+    S = steps_per_replay(K, args.graph_steps)
+    units = int_ops(cfg) if cfg["kind"] == "mmq" else weight_bytes(cfg)
+    unit, scale = ("TOPS", 1e12) if cfg["kind"] == "mmq" else ("GB/s", 1e9)
+
+    def step(copy, fe=front_end):
+        wl.step(copy, pdl=True, stream=stream, front_end=fe)
+
+    # warm-up (also settles per-kernel attributes before any capture)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i % C)
+    torch.cuda.synchronize()
+
+    sg = StepGraphs(step, K, S, C, stream)
+    sg.warm()
+    barrier(ws)
+    torch.cuda.synchronize()
+    per, total_ms = sg.run_timed(stream)
+    barrier(ws)
+    del sg
+    med = statistics.median(per)
+    ms_step = barrier_max(med, ws, device)
+    total_ms = barrier_max(total_ms, ws, device)
+
+    out = {"workload": cfg["name"], "config_id": cfg_id, "M": cfg["M"],
+           "value": units * ws / (ms_step * 1e-3) / scale, "unit": unit, "ms_per_step": ms_step,
+           "timing": {"replays": len(per), "steps_per_replay": S,
+                      "how": (f"the {K}-step region as one graph, replayed {len(per)} times, each replay timed"
+                              if S == K else f"{K} steps as {len(per)} timed replays of {S}-step graphs"),
+                      "ms_per_step_median": med, "ms_per_step_min": min(per), "ms_per_step_max": max(per),
+                      "ms_per_step_all_replays": total_ms / (S * len(per) + (K % S if S < K else 0)),
+                      "weight_copies": C},
+           "tokens_per_s": cfg["M"] * ws / (ms_step * 1e-3),
+           "weight_bytes_per_step": weight_bytes(cfg), "int_ops_per_step": int_ops(cfg),
+           "front_end": front_end_desc(front_end, cfg),
+           "gpu_launches": wl.launches_per_step(front_end) * K}
+    if unit == "GB/s":
+        out["hbm_frac"] = (out["value"] / ws) / peaks()[0]
+
+    # the same step with the other decode activation paths, for reference
+    if headline and cfg["kind"] == "gemv":
+        fe_ms = {front_end: ms_step}
+        for fe in ("fused", "unfused"):
+            if fe != front_end:
+                p2, _ = time_graphs(lambda c, fe=fe: step(c, fe), K, S, C, stream)
+                fe_ms[fe] = statistics.median(p2)
+        out["front_end_ms_per_step"] = fe_ms
+
+    # Per kernel family: the step's launches of that family only, S steps of them back to back in
+    # graphs of their own (same launch configuration: PDL, rotating weight copies), timed with CUDA
+    # events on the launching stream; median over the replays.
+    per_kernel = {}
+    for key, items in kernel_groups(wl, front_end).items():
+        def launches(copy, items=items):
+            for kind, what, f in items:
+                if kind == "quantize":
+                    codes, scales = wl.q8[what]
+                    qk.quantize_q8_1(wl.x[what], codes, scales, pdl=True, stream=stream)
+                else:
+                    wl.launch(what, copy, pdl=True, stream=stream, fused=f)
+        p2, _ = time_graphs(launches, K, S, C, stream)
+        kms = statistics.median(p2)
+        gl = [w for kind, w, _ in items if kind == "gemm"]
+        nb = sum(N * (K_ // 256) * BYTES_PER_SB[q] for (_, q, N, K_, _, _) in gl)
+        nops = sum(2 * cfg["M"] * N * K_ for (_, _, N, K_, _, _) in gl)
+        act = sum(cfg["M"] * dict(slots(cfg))[w] * 4 for kind, w, _ in items if kind == "quantize")
+        per_kernel[key] = {"calls_per_step": len(items), "ms_per_step": kms, "avg_us": kms / len(items) * 1e3,
+                           "weight_bytes": nb, "ops": nops, "activation_bytes_in": act}
+    tot = sum(v["ms_per_step"] for v in per_kernel.values()) or 1.0
+    for v in per_kernel.values():
+        v["share"] = v["ms_per_step"] / tot
+        if v["weight_bytes"]:
+            v["weight_gbs"] = v["weight_bytes"] / (v["ms_per_step"] * 1e-3) / 1e9
+        if v["ops"] and cfg["kind"] == "mmq":
+            v["tops"] = v["ops"] / (v["ms_per_step"] * 1e-3) / 1e12
+        if v["activation_bytes_in"]:
+            v["activation_gbs"] = v["activation_bytes_in"] / (v["ms_per_step"] * 1e-3) / 1e9
+    out["per_kernel"] = per_kernel
+    # per GEMM: its contraction call alone, in the same launch configuration
+    per_gemm = {}
+    for gemm in cfg["gemms"]:
+        f = gemm_fused(front_end, cfg, gemm)
+        p2, _ = time_graphs(lambda copy, g=gemm, f=f: wl.launch(g, copy, pdl=True, stream=stream, fused=f),
+                            K, S, C, stream)
+        us = statistics.median(p2) * 1e3
+        name, q, N, K_, _, _ = gemm
+        e = {"us": us, "kernel": wl.kernel_key(gemm, f)}
+        if cfg["kind"] == "mmq":
+            e["tops"] = 2 * cfg["M"] * N * K_ / (us * 1e-6) / 1e12
+        else:
+            e["weight_gbs"] = N * (K_ // 256) * BYTES_PER_SB[q] / (us * 1e-6) / 1e9
+        per_gemm[name] = e
+    out["per_gemm"] = per_gemm
+    contraction = {k: v for k, v in per_kernel.items() if k != "quantize_q8_1"}
+    if contraction:
+        dom = max(contraction, key=lambda k: contraction[k]["ms_per_step"])
+        out["roofline"] = roofline(cfg, cfg_id, dom, contraction[dom], peaks_meas)
+
+    out["e2e"] = measure_e2e(wl, step, K, S, C, stream, ws, device, units, scale, unit)
+    res = (wl.host_w, wl.host_x, wl.host_r, wl.host_g)
+    del wl
+    torch.cuda.empty_cache()
+    return out, res
+
+
+def roofline(cfg, cfg_id, dom, dk, peaks_meas):
+    hbm, bf16, peak_src = peaks()
+    traffic = recorded_traffic(cfg_id, dom)
+    n = dk["calls_per_step"]
+    if cfg["kind"] == "mmq":
+        achieved = dk["ops"] / (dk["ms_per_step"] * 1e-3) / 1e12
+        # f16 tensor MMAs the kernel issues per algorithmic integer product: two (A_hi, A_lo against the exact
+        # sc*q) plus the min term's K/32-deep contraction (3 MMAs per 16 sub-blocks, ~4.7 % more) for Q4_K;
+        # three (hi/lo splits) for Q6_K
+        mma_per_product = (2.0 + 3.0 / 64.0) if dom == "mmq_q4k" else 3.0
+        r = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
+             "traffic": traffic, "kernel": dom, "algorithmic_ops_per_launch": dk["ops"] / n,
+             "avg_launch_us": dk["avg_us"],
+             "peak_note": f"bf16 dense {peak_src} (MEASURED_PEAKS.json) x nominal f16/bf16 ratio 1; achieved counts "
+                          "the algorithmic 2*M*N*K integer ops; a launch is one qk_mmq call (its prep and main kernel)",
+             "f16_mma_per_integer_product": mma_per_product}
+        if peaks_meas:
+            f16p, s8p = peaks_meas.get("tcgen05_f16_tflops"), peaks_meas.get("mma_sync_s8_tops")
+            if f16p:
+                r["f16_tcgen05_peak"] = f16p
+                r["frac_of_f16_tcgen05_peak"] = achieved / f16p
+                r["issued_mma_utilisation"] = achieved * mma_per_product / f16p
+            if s8p:
+                r["int8_mma_sync_peak"] = s8p
+                r["ratio_to_int8_mma_sync_peak"] = achieved / s8p
+        return r
+    achieved = dk["weight_bytes"] / (dk["ms_per_step"] * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": traffic, "kernel": dom, "peak_note": f"hbm_gbs ({peak_src}, burst copy)",
+            "algorithmic_bytes_per_launch": dk["weight_bytes"] / n, "avg_launch_us": dk["avg_us"]}
+
+
+def measure_e2e(wl, step, K, S, C, stream, ws, device, units, scale, unit):
+    """The same metric through the public API with host buffers: every step copies its f32
+    activations and residuals in from pinned host memory (one copy of the packed input block)
+    and its outputs back out (one copy of the packed output block), inside the timed region."""
+    host_in = torch.empty(wl.inbuf.numel(), dtype=torch.float32).pin_memory()
+    off = 0
+    flat = wl.inbuf
+    # the host block mirrors the device block's layout (same views, same offsets)
+    for t in list(wl.x.values()) + [v for n, v in wl.r.items() if n in wl.host_r]:
+        o = t.data_ptr() - flat.data_ptr()
+        host_in[o // 4:o // 4 + t.numel()].copy_(t.reshape(-1).cpu())
+    host_out = torch.empty(wl.outbuf.numel(), dtype=torch.float32).pin_memory()
+
+    def e2e_step(copy):
+        wl.inbuf.copy_(host_in, non_blocking=True)
+        step(copy)
+        host_out.copy_(wl.outbuf, non_blocking=True)
+
+    sg = StepGraphs(e2e_step, K, S, C, stream)
+    sg.warm()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    per, total_ms = sg.run_timed(stream)
+    wall = (time.perf_counter() - t0) * 1e3
+    del sg
+    ms = barrier_max(statistics.median(per), ws, device)
+    return {"value": units * ws / (ms * 1e-3) / scale, "unit": unit,
+            "h2d_bytes_per_step": wl.inbuf.numel() * 4, "d2h_bytes_per_step": wl.outbuf.numel() * 4,
+            "ms_per_step": ms, "ms_per_step_wall_all_k": wall / K, "copies_per_step": 2}
+
+
+def measure_peaks():
+    """The two tensor-core ceilings of the prefill MMQ, measured on this device (include/qk_peak.h)."""
+    import quantized_q8_activation_gb300 as qk
+    f16, _ = qk.peak_tcgen05_f16(iters=4096, reps=10)
+    s8, _ = qk.peak_mma_s8(iters=20000, reps=5)
+    return {"tcgen05_f16_tflops": f16, "mma_sync_s8_tops": s8,
+            "how": "own micro-benchmarks (include/qk_peak.h): tcgen05.mma kind::f16 128x256x16 back to back from one "
+                   "thread per SM, and mma.sync m16n8k32 s8 with 8 chains per warp, 16 warps per SM; CUDA events"}
+
+
 def run_ours(args, ws, rank, local):
     import quantized_q8_activation_gb300 as qk
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     qk.build()
     qk.lib()
-    cfg = CONFIGS[args.config]
-    wl = Workload(args.config, seed=0, copies=args.copies)
     stream = torch.cuda.Stream(device)
-    C = wl.copies
-    S = C * max(1, -(-args.graph_steps // C))        # steps per graph, a multiple of the copy count
-
-    front_end = args.front_end
-
-    def steps(n, start=0, pdl=True, front_end=front_end):
-        for i in range(n):
-            wl.step((start + i) % C, pdl=pdl, stream=stream, front_end=front_end)
-
-    # warm-up (also settles per-kernel attributes before any capture)
-    with torch.cuda.stream(stream):
-        steps(max(args.warmup, 1))
-    torch.cuda.synchronize()
-    g_main = capture(lambda: steps(S), stream)
-    rem = args.steps % S
-    g_rem = capture(lambda: steps(rem), stream) if rem else None
-    nrep = args.steps // S
-    g_main.replay()                                     # one untimed replay of the graph itself
-    torch.cuda.synchronize()
-
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(ws)
-    torch.cuda.synchronize()
+    head = args.config if args.config is not None else 1
+    extra = [] if args.config is not None else [0, 2, 3, 4]
+    ids = [head] + extra
+    need_peaks = any(CONFIGS[c]["kind"] == "mmq" for c in ids)
     with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(nrep):
-                g_main.replay()
-            if g_rem is not None:
-                g_rem.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-    barrier(ws)
-    ms = e0.elapsed_time(e1)
-    ms = barrier_max(ms, ws, device)
-    ms_step = ms / args.steps
-
-    # the same step with the other activation paths, for reference
-    front_end_ms = {}
-    if cfg["kind"] == "gemv":
-        for fe in ("fused", "unfused"):
-            if fe == front_end:
-                continue
-            g_alt = capture(lambda: steps(S, front_end=fe), stream)
-            g_alt.replay()
-            torch.cuda.synchronize()
-            reps = max(1, min(nrep, 50))
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a0.record(stream)
-                for _ in range(reps):
-                    g_alt.replay()
-                a1.record(stream)
-            torch.cuda.synchronize()
-            front_end_ms[fe] = a0.elapsed_time(a1) / (reps * S)
-            del g_alt
-        front_end_ms[front_end] = ms_step
-
-    # Per-kernel durations: each kernel type's launches of one step, S steps of them back to back
-    # in a graph of their own (same launch configuration as the step: PDL, rotating weight copies),
-    # timed with CUDA events on the launching stream.
-    groups = {}
-    for gemm in cfg["gemms"]:
-        f = gemm_fused(front_end, cfg, gemm)
-        groups.setdefault(wl.kernel_key(gemm, f), []).append((gemm, f))
-    per_kernel = {}
-    for key, gf in groups.items():
-        gl = [g for g, _ in gf]
-        gk = capture(lambda: [wl.launch(g, i % C, pdl=True, stream=stream, fused=f)
-                              for i in range(S) for g, f in gf], stream)
-        gk.replay()
-        torch.cuda.synchronize()
-        reps = max(1, min(nrep, 20))
-        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            k0.record(stream)
-            for _ in range(reps):
-                gk.replay()
-            k1.record(stream)
-        torch.cuda.synchronize()
-        del gk
-        n_launch = reps * S * len(gl)
-        per_kernel[key] = {"ms": k0.elapsed_time(k1) / (reps * S),          # per step
-                           "n": len(gl),                                     # calls per step
-                           "avg_us": k0.elapsed_time(k1) / n_launch * 1e3,
-                           "bytes": sum(N * (K // 256) * BYTES_PER_SB[q] for (_, q, N, K, _, _) in gl),
-                           "ops": sum(2 * cfg["M"] * N * K for (_, _, N, K, _, _) in gl)}
-    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
-    dk = per_kernel[dom]
-    hbm, bf16, peak_src = peaks()
-    traffic = recorded_traffic(args.config, dom)
-
-    if cfg["kind"] == "mmq":
-        units = int_ops(cfg)
-        value = units * ws / (ms_step * 1e-3) / 1e12
-        unit = "TOPS"
-        achieved = dk["ops"] / (dk["ms"] * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                "frac": achieved / bf16, "traffic": traffic, "kernel": dom,
-                "algorithmic_ops_per_launch": dk["ops"] / dk["n"],
-                "peak_note": f"f16 tensor path: bf16 dense {peak_src} x nominal f16/bf16 ratio 1; "
-                             "achieved counts the algorithmic 2*M*N*K integer ops (the kernel issues "
-                             + ("two f16 MMAs per product (A_hi, A_lo against the exact sc*q) plus the "
-                                "K/32-deep min-term contraction" if dom == "mmq_q4k" else
-                                "three f16 MMAs per product for the hi/lo split") + "); a launch here is one "
-                             "qk_mmq call, its prep kernel and its main kernel",
-                "avg_launch_us": dk["avg_us"]}
-    else:
-        units = weight_bytes(cfg)
-        value = units * ws / (ms_step * 1e-3) / 1e9
-        unit = "GB/s"
-        achieved = dk["bytes"] / (dk["ms"] * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": traffic, "kernel": dom, "peak_note": f"hbm_gbs ({peak_src}, burst copy)",
-                "algorithmic_bytes_per_launch": dk["bytes"] / dk["n"],
-                "avg_launch_us": dk["avg_us"]}
-
-    # end to end through the public API with host buffers (pinned), copies inside the timed region
-    h2d = {s: torch.from_numpy(v).pin_memory() for s, v in wl.host_x.items()}
-    h2r = {n: torch.from_numpy(v).pin_memory() for n, v in wl.host_r.items()}
-    d2h = {n: torch.empty(tuple(t.shape), dtype=torch.float32).pin_memory() for n, t in wl.y.items()}
-    h2d_bytes = sum(t.numel() * 4 for t in h2d.values()) + sum(t.numel() * 4 for t in h2r.values())
-    d2h_bytes = sum(t.numel() * 4 for t in d2h.values())
-
-    def e2e_step(i):
-        for s, t in h2d.items():
-            wl.x[s].copy_(t, non_blocking=True)
-        for n, t in h2r.items():
-            wl.r[n].copy_(t, non_blocking=True)
-        wl.step(i % C, pdl=True, stream=stream, front_end=front_end)
-        for n, t in d2h.items():
-            t.copy_(wl.y[n], non_blocking=True)
-
-    e2e_steps = min(args.steps, max(S, 200))
-    g_e2e = capture(lambda: [e2e_step(i) for i in range(S)], stream)
-    g_e2e.replay()
-    torch.cuda.synchronize()
-    reps = max(1, e2e_steps // S)
-    barrier(ws)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(reps):
-            g_e2e.replay()
-    torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / (reps * S)
-    e2e_s = barrier_max(e2e_s, ws, device)
-    e2e_value = (units * ws / e2e_s / (1e12 if unit == "TOPS" else 1e9))
-
-    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8",
-            "data": "synthetic (seeded; distributions of the benchmark definition)",
-            "config": {"workload": cfg["name"], "config_id": args.config, "M": cfg["M"],
+        peaks_meas = measure_peaks() if need_peaks else None
+        results, hosts = {}, {}
+        for c in ids:
+            steps0 = args.steps
+            if args.steps is None:
+                args.steps = DEFAULT_STEPS[c]
+            results[c], host = measure_config(c, args, stream, ws, device, peaks_meas, headline=(c == head))
+            if c == head or CONFIGS[c]["kind"] == "mmq":          # the workloads the oracle baseline times
+                hosts[c] = host
+            args.steps = steps0
+    h = results[head]
+    cfg = CONFIGS[head]
+    line = {"metric": METRIC, "value": h["value"], "unit": h["unit"], "n_gpus": ws,
+            "steps": args.steps if args.steps is not None else DEFAULT_STEPS[head], "warmup": args.warmup,
+            "ms_per_step": h["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8", "data": "synthetic (seeded; distributions of the benchmark definition)",
+            "config": {"workload": cfg["name"], "config_id": head, "M": cfg["M"],
                        "weight_bytes_per_step": weight_bytes(cfg), "int_ops_per_step": int_ops(cfg),
-                       "l2": f"inputs larger than L2: {C} rotating weight copies, "
-                             f"{C * weight_bytes(cfg) / 1e6:.0f} MB working set",
-                       "graph_steps": S, "pdl": True, "parallelism": f"replicas x{ws}",
-                       "front_end": front_end_desc(front_end, cfg)},
-            "front_end_ms_per_step": front_end_ms or None,
-            "hbm_frac": (value / ws) / hbm if unit == "GB/s" else None,
-            "roofline": roof,
-            # per entry point: its calls per step (an MMQ call is two kernels, prep and main), the
-            # average call time and its share of the entry points' time
-            "per_kernel": {k: {"calls_per_step": v["n"], "avg_us": v["avg_us"],
-                               "share": v["ms"] / sum(x["ms"] for x in per_kernel.values())}
-                           for k, v in per_kernel.items()},
-            "clocks": clk.summary(),
-            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d_bytes,
-                    "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_s * 1e3},
-            "gpu_launches": wl.launches_per_step(front_end) * args.steps}
+                       "l2": f"inputs larger than L2: {h['timing']['weight_copies']} rotating weight copies, "
+                             f"{h['timing']['weight_copies'] * weight_bytes(cfg) / 1e6:.0f} MB working set",
+                       "pdl": True, "parallelism": f"replicas x{ws}", "front_end": h["front_end"]},
+            "timing": h["timing"], "tokens_per_s": h["tokens_per_s"]}
+    for k in ("front_end_ms_per_step", "hbm_frac", "roofline", "per_kernel", "per_gemm"):
+        if k in h:
+            line[k] = h[k]
+    line["clocks"] = clk.summary()
+    line["e2e"] = h["e2e"]
+    line["gpu_launches"] = h["gpu_launches"]
+    if peaks_meas:
+        line["tensor_peaks"] = peaks_meas
+    if extra:
+        line["configs"] = {str(c): results[c] for c in extra}
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline((wl.host_w, wl.host_x, wl.host_r), cfg, budget_s=args.cpu_seconds,
-                                            host_g=wl.host_g)
+        hw, hx, hr, hg = hosts[head]
+        line["cpu_baseline"] = cpu_baseline((hw, hx, hr), cfg, budget_s=args.cpu_seconds, host_g=hg)
+        line["cpu_baseline_1thread"] = cpu_baseline((hw, hx, hr), cfg, budget_s=args.cpu_seconds, host_g=hg,
+                                                    threads=1)
+        for c in extra:
+            if CONFIGS[c]["kind"] == "mmq":
+                hw, hx, hr, hg = hosts[c]
+                line["configs"][str(c)]["cpu_baseline"] = cpu_baseline((hw, hx, hr), CONFIGS[c],
+                                                                       budget_s=args.cpu_seconds / 2, host_g=hg)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+DEFAULT_STEPS = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100, 5: 100, 6: 40000, 7: 40000, 8: 30000,
+                 9: 40000, 10: 40000}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default per config: about a second of GPU work)")
+                    help="timed steps of every workload (default per workload: about a second of GPU work)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, choices=sorted(CONFIGS))
+    ap.add_argument("--config", type=int, default=None, choices=sorted(CONFIGS),
+                    help="time only this workload (default: config 1 as the headline, with configs 0, 2, 3 "
+                         "and 4 under 'configs')")
     ap.add_argument("--copies", type=int, default=None, help="weight copies rotated between steps")
     ap.add_argument("--graph-steps", type=int, default=100)
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: total host time the warm-up and timed steps are sized to")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -726,12 +890,10 @@ def main():
                          "quantize kernel before its consumers (unfused); auto = fused for activations "
                          "of at most 4096 values, unfused for larger ones")
     args = ap.parse_args()
-    if args.steps is None:
-        args.steps = {0: 100000, 1: 40000, 2: 10000, 3: 8000, 4: 100, 5: 100, 6: 40000, 7: 40000, 8: 30000,
-                      9: 40000, 10: 40000}[args.config]
-    args.graph_steps = max(1, min(args.graph_steps, args.steps))
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps is not None and args.steps < 1:
+        ap.error("--steps must be >= 1")
     ws, rank, local = dist_env()
     if ws > 1:
         import torch.distributed as dist
@@ -740,6 +902,10 @@ def main():
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
     try:
         if args.impl == "reference":
+            if args.config is None:
+                args.config = 1
+            if args.steps is None:
+                args.steps = DEFAULT_STEPS[args.config]
             run_reference(args, ws, rank)
         else:
             run_ours(args, ws, rank, local)

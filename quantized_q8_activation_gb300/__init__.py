@@ -54,7 +54,9 @@ EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1"
            "qk_gemv_q5k_f32", "qk_gemv_q8_0", "qk_gemv_q8_0_f32", "qk_gemv_q2k", "qk_gemv_q3k",
            "qk_gemv_q2k_f32", "qk_gemv_q3k_f32",
            "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_mmq_q6k", "qk_mmq_q4k_noalloc", "qk_error_flags",
-           "qk_rmsnorm_q8_1", "qk_swiglu_q8_1"]
+           "qk_rmsnorm_q8_1", "qk_swiglu_q8_1",
+           # include/qk_peak.h (measurement)
+           "qk_peak_mma_s8", "qk_peak_tcgen05_f16"]
 
 _lib = None
 _lock = threading.Lock()
@@ -112,6 +114,9 @@ def lib() -> ctypes.CDLL:
             L.qk_swiglu_q8_1.argtypes = [p, i64, i64, i64, p, p, p, u, p]
             L.qk_mmq_q4k_noalloc.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
             L.qk_error_flags.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
+            dp = ctypes.POINTER(ctypes.c_double)
+            L.qk_peak_mma_s8.argtypes = [i64, ctypes.c_int, dp, dp, p]
+            L.qk_peak_tcgen05_f16.argtypes = [i64, ctypes.c_int, dp, dp, p]
             for name in EXPORTS:
                 getattr(L, name).restype = ctypes.c_int if name != "qk_status_string" else ctypes.c_char_p
             _lib = L
@@ -407,3 +412,21 @@ def mmq_q4k_noalloc(w, codes, scales, N, K, residual=None, y=None, pdl=False, st
                                       y.data_ptr(), LAUNCH_PDL if pdl else 0, _stream(stream))
     _check(st, "qk_mmq_q4k_noalloc")
     return y
+
+
+# ------------------------------------------------------------- measurement
+
+def _peak(fn, name, iters, reps, stream):
+    rate, ms = ctypes.c_double(), ctypes.c_double()
+    _check(fn(int(iters), int(reps), ctypes.byref(rate), ctypes.byref(ms), _stream(stream)), name)
+    return rate.value, ms.value
+
+
+def peak_mma_s8(iters: int = 20000, reps: int = 5, stream=None):
+    """Measured mma.sync m16n8k32 s8 rate of the current device: (TOPS, milliseconds timed)."""
+    return _peak(lib().qk_peak_mma_s8, "qk_peak_mma_s8", iters, reps, stream)
+
+
+def peak_tcgen05_f16(iters: int = 4096, reps: int = 5, stream=None):
+    """Measured tcgen05 kind::f16 (128 x 256 x 16) rate of the current device: (TFLOP/s, milliseconds)."""
+    return _peak(lib().qk_peak_tcgen05_f16, "qk_peak_tcgen05_f16", iters, reps, stream)

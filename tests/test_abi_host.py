@@ -14,7 +14,8 @@ import pytest
 import quantized_q8_activation_gb300 as qk
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "qk.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 P = 0x7F0000000000          # fake, 256-byte aligned device addresses
 E_NULL, E_SHAPE, E_ALIGN, E_ALIAS, E_TYPE = -1, -2, -3, -4, -5
@@ -27,9 +28,15 @@ def L():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(qk_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(qk_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_headers_found():
+    assert [os.path.basename(h) for h in HEADERS] == ["qk.h", "qk_peak.h"]
 
 
 def test_header_declares_the_binding_exports():
@@ -199,3 +206,13 @@ def test_swiglu_q8_1_rejects(L):
     assert f(gu, 514, 2, 256, h, c, s, 0, None) == E_ALIGN
     assert f(gu, 512, 1, 256, gu + 1024, c, s, 0, None) == E_ALIAS     # h inside gu
     assert f(gu, 512, 1, 256, h, h + 512, s, 0, None) == E_ALIAS       # codes inside h
+
+
+def test_peak_rejects(L):
+    r, ms = ctypes.c_double(), ctypes.c_double()
+    for fn in ("qk_peak_mma_s8", "qk_peak_tcgen05_f16"):
+        f = getattr(L, fn)
+        assert f(100, 1, None, ctypes.byref(ms), None) == E_NULL
+        assert f(0, 1, ctypes.byref(r), ctypes.byref(ms), None) == E_SHAPE
+        assert f(100, 0, ctypes.byref(r), ctypes.byref(ms), None) == E_SHAPE
+        assert f(100, 1001, ctypes.byref(r), ctypes.byref(ms), None) == E_SHAPE
