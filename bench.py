@@ -112,7 +112,7 @@ def gemm_fused(policy: str, cfg, gemm) -> bool:
         return False
     if policy == "auto":
         return cfg["M"] * gemm[3] <= 4096
-    return policy == "fused"
+    return policy == "fused"                        # "unfused" and "batched" read q8_1
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, averaged over the
@@ -136,6 +136,9 @@ def front_end_desc(front_end: str, cfg) -> str:
                 "qk_rmsnorm_q8_1 -> gate_up; qk_swiglu_q8_1 -> down")
     if cfg["kind"] != "gemv":
         return "qk_quantize_q8_1 kernel per activation"
+    if front_end == "batched":
+        return ("batched: one qk_quantize_q8_1 launch over all of the step's f32 activations (contiguous in "
+                "the input buffer), then every GEMV reads q8_1")
     parts = []
     for g in cfg["gemms"]:
         parts.append(f"{g[0]}: " + ("q8_1 quantization inside the GEMV" if gemm_fused(front_end, cfg, g)
@@ -171,6 +174,8 @@ def launches_per_step(cfg, front_end: str = "auto") -> int:
     two RMSNorm and one SwiGLU producers"""
     if cfg["kind"] == "chain":
         return 3 + len(cfg["gemms"])
+    if front_end == "batched" and cfg["kind"] == "gemv":
+        return 1 + len(cfg["gemms"])
     slots_q = {g[5] for g in cfg["gemms"] if not gemm_fused(front_end, cfg, g)}
     per_gemm = 2 if cfg["kind"] == "mmq" else 1
     return len(slots_q) + per_gemm * len(cfg["gemms"])
@@ -187,15 +192,15 @@ def slots(cfg):
 
 # ------------------------------------------------------------------ workload
 
-def packed(shapes, device, align: int = 64):
-    """One float32 buffer holding a tensor of each shape (offsets aligned to `align` elements);
-    returns the buffer and the views."""
+def packed(shapes, device, align: int = 128):
+    """One zero-filled float32 buffer holding a tensor of each shape (offsets aligned to `align`
+    elements); returns the buffer, the views and the offsets."""
     offs, n = [], 0
     for sh in shapes:
         offs.append(n)
         n += -(-int(np.prod(sh)) // align) * align
-    buf = torch.empty(max(n, align), dtype=torch.float32, device=device)
-    return buf, [buf[o:o + int(np.prod(sh))].view(*sh) for o, sh in zip(offs, shapes)]
+    buf = torch.zeros(max(n, align), dtype=torch.float32, device=device)
+    return buf, [buf[o:o + int(np.prod(sh))].view(*sh) for o, sh in zip(offs, shapes)], offs
 
 
 class Workload:
@@ -226,10 +231,17 @@ class Workload:
         x_specs = [(s, (M, K)) for s, K in slots(cfg) if s in cfg.get("inputs", [s])]
         r_specs = [(name, (M, N)) for (name, _, N, _, res, _) in cfg["gemms"] if res and not (chain and name == "down")]
         y_specs = [(name, (M, N)) for (name, _, N, _, _, _) in cfg["gemms"]]
-        self.inbuf, views = packed([sh for _, sh in x_specs + r_specs], device)
+        self.inbuf, views, offs = packed([sh for _, sh in x_specs + r_specs], device)
         self.x = {s: v for (s, _), v in zip(x_specs, views[:len(x_specs)])}
         self.r = {n: v for (n, _), v in zip(r_specs, views[len(x_specs):])}
-        self.outbuf, yv = packed([sh for _, sh in y_specs], device)
+        # the activations come first: their q8_1 codes and scales are packed the same way, so one
+        # quantize launch over the prefix quantizes every activation of the step (32-value blocks
+        # never cross an activation, whose sizes and offsets are multiples of 128 values)
+        self.x_prefix = offs[len(x_specs)] if r_specs else self.inbuf.numel()
+        self.q8_codes = torch.empty(self.x_prefix, dtype=torch.int8, device=device)
+        self.q8_scales = torch.empty((self.x_prefix // 32, 2), dtype=torch.float16, device=device)
+        x_off = {s: o for (s, _), o in zip(x_specs, offs)}
+        self.outbuf, yv, _ = packed([sh for _, sh in y_specs], device)
         self.y = {n: v for (n, _), v in zip(y_specs, yv)}
         self.host_x = {s: synth.activations(M, sh[1], seed=seed, tag=s) for s, sh in x_specs}
         self.host_r = {n: synth.residual(M, sh[1], seed=seed, tag=n) for n, sh in r_specs}
@@ -237,7 +249,14 @@ class Workload:
             self.x[s].copy_(torch.from_numpy(v))
         for n, v in self.host_r.items():
             self.r[n].copy_(torch.from_numpy(v))
-        self.q8 = {s: qk.empty_q8_1(M, K, device) for s, K in slots(cfg)}
+        self.q8 = {}
+        for s, K in slots(cfg):
+            if s in x_off:
+                o = x_off[s]
+                self.q8[s] = (self.q8_codes[o:o + M * K].view(M, K),
+                              self.q8_scales[o // 32:(o + M * K) // 32].view(M, K // 32, 2))
+            else:
+                self.q8[s] = qk.empty_q8_1(M, K, device)
         self.host_g = {}
         if chain:
             self.host_g = chain_norm_weights(cfg, seed)
@@ -270,13 +289,18 @@ class Workload:
                       "q2k": qk.gemv_q2k, "q3k": qk.gemv_q3k}[q]
                 fn(self.w[copy][name], codes, scales, N, K, **kw)
 
-    def step(self, copy: int, pdl: bool = True, stream=None, front_end: str = "auto"):
+    def step(self, copy: int, pdl: bool = True, stream=None, front_end: str = "batched"):
         """Enqueue one step on `stream`.  Each decode GEMM either quantizes its activation
         inside the GEMV (qk_gemv_*_f32) or reads the q8_1 codes of a quantize kernel that
         runs once per activation before its first consumer (see gemm_fused)."""
         qk, cfg = self.qk, self.cfg
         if cfg["kind"] == "chain":
             return self.chain_step(copy, pdl, stream)
+        if front_end == "batched" and cfg["kind"] == "gemv":
+            self.quantize_all(pdl, stream)
+            for gemm in cfg["gemms"]:
+                self.launch(gemm, copy, pdl=pdl, stream=stream, fused=False)
+            return
         done = set()
         for gemm in cfg["gemms"]:
             s = gemm[5]
@@ -286,6 +310,12 @@ class Workload:
                 qk.quantize_q8_1(self.x[s], codes, scales, pdl=pdl, stream=stream)
                 done.add(s)
             self.launch(gemm, copy, pdl=pdl, stream=stream, fused=fused)
+
+    def quantize_all(self, pdl: bool, stream):
+        """One qk_quantize_q8_1 launch over every f32 activation of the step (the packed prefix)."""
+        n = self.x_prefix
+        self.qk.quantize_q8_1(self.inbuf[:n].view(1, n), self.q8_codes.view(1, n),
+                              self.q8_scales.view(1, n // 32, 2), pdl=pdl, stream=stream)
 
     def chain_step(self, copy: int, pdl: bool, stream):
         """The decode layer with its producers: RMSNorm -> q8_1 -> QKV; attn-out (+ residual
@@ -611,6 +641,11 @@ def kernel_groups(wl, front_end):
     """The step's launches grouped by kernel family (the quantize kernels as their own group), in
     step order: {key: [(kind, gemm or slot, fused)]}."""
     cfg, groups, done = wl.cfg, {}, set()
+    if front_end == "batched" and cfg["kind"] == "gemv":
+        groups["quantize_q8_1"] = [("quantize_all", None, False)]
+        for gemm in cfg["gemms"]:
+            groups.setdefault(wl.kernel_key(gemm, False), []).append(("gemm", gemm, False))
+        return groups
     for gemm in cfg["gemms"]:
         f = gemm_fused(front_end, cfg, gemm)
         if not f and gemm[5] not in done and cfg["kind"] != "chain":     # the chain's producers quantize
@@ -670,7 +705,7 @@ def measure_config(cfg_id, args, stream, ws, device, peaks_meas=None, headline=F
     # the same step with the other decode activation paths, for reference
     if headline and cfg["kind"] == "gemv":
         fe_ms = {front_end: ms_step}
-        for fe in ("fused", "unfused"):
+        for fe in ("fused", "unfused", "auto", "batched"):
             if fe != front_end:
                 p2, _ = time_graphs(lambda c, fe=fe: step(c, fe), K, S, C, stream)
                 fe_ms[fe] = statistics.median(p2)
@@ -683,7 +718,9 @@ def measure_config(cfg_id, args, stream, ws, device, peaks_meas=None, headline=F
     for key, items in kernel_groups(wl, front_end).items():
         def launches(copy, items=items):
             for kind, what, f in items:
-                if kind == "quantize":
+                if kind == "quantize_all":
+                    wl.quantize_all(True, stream)
+                elif kind == "quantize":
                     codes, scales = wl.q8[what]
                     qk.quantize_q8_1(wl.x[what], codes, scales, pdl=True, stream=stream)
                 else:
@@ -694,6 +731,7 @@ def measure_config(cfg_id, args, stream, ws, device, peaks_meas=None, headline=F
         nb = sum(N * (K_ // 256) * BYTES_PER_SB[q] for (_, q, N, K_, _, _) in gl)
         nops = sum(2 * cfg["M"] * N * K_ for (_, _, N, K_, _, _) in gl)
         act = sum(cfg["M"] * dict(slots(cfg))[w] * 4 for kind, w, _ in items if kind == "quantize")
+        act += sum(wl.x_prefix * 4 for kind, _, _ in items if kind == "quantize_all")
         per_kernel[key] = {"calls_per_step": len(items), "ms_per_step": kms, "avg_us": kms / len(items) * 1e3,
                            "weight_bytes": nb, "ops": nops, "activation_bytes_in": act}
     tot = sum(v["ms_per_step"] for v in per_kernel.values()) or 1.0
@@ -885,10 +923,11 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: total host time the warm-up and timed steps are sized to")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--front-end", choices=["auto", "fused", "unfused"], default="auto",
-                    help="decode activation path: q8_1 quantization inside each GEMV (fused) or a "
-                         "quantize kernel before its consumers (unfused); auto = fused for activations "
-                         "of at most 4096 values, unfused for larger ones")
+    ap.add_argument("--front-end", choices=["batched", "auto", "fused", "unfused"], default="batched",
+                    help="decode activation path: one quantize kernel over all of the step's f32 "
+                         "activations, then q8_1 GEMVs (batched, default); q8_1 quantization inside each "
+                         "GEMV (fused); a quantize kernel per activation before its consumers (unfused); "
+                         "auto = fused for activations of at most 4096 values, unfused for larger ones")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

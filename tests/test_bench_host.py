@@ -14,6 +14,8 @@ def test_launches_per_step_match_the_ncu_launch_lists():
     assert bench.launches_per_step(bench.CONFIGS[6]) == 7
     assert bench.launches_per_step(bench.CONFIGS[1], "unfused") == 8     # 4 activations + 4 GEMVs
     assert bench.launches_per_step(bench.CONFIGS[1], "fused") == 4
+    assert bench.launches_per_step(bench.CONFIGS[1], "batched") == 5     # one quantize for all + 4 GEMVs
+    assert bench.launches_per_step(bench.CONFIGS[3], "batched") == 6
 
 
 def test_recorded_traffic_is_keyed_to_existing_kernel_families():

@@ -25,7 +25,8 @@ def sample_rows(N, n=24, seed=0):
 
 
 @pytest.mark.parametrize("cfg_id,front_end", [(0, "fused"), (1, "fused"), (2, "fused"), (3, "fused"), (1, "unfused"),
-                                              (3, "unfused"), (1, "auto"), (4, "auto"), (5, "auto"), (7, "auto"),
+                                              (3, "unfused"), (1, "auto"), (0, "batched"), (1, "batched"),
+                                              (2, "batched"), (3, "batched"), (4, "auto"), (5, "auto"), (7, "auto"),
                                               (8, "auto"), (9, "auto"), (10, "auto")])
 def test_config_full_size(cfg_id, front_end):
     import bench
