@@ -92,6 +92,12 @@ CONFIGS = {
 NORM_EPS = 1e-5                                       # Llama-3 RMSNorm epsilon
 
 
+def mmq_base_workspace(M: int, K: int) -> int:
+    """Bytes of an MMQ workspace without the split-K scratch (include/qk.h, qk_mmq_workspace_bytes):
+    per 128-row M-tile a 16 KB activation block per 32 values of K and an 8 KB sums tile per 512."""
+    return -(-M // 128) * (K * 512 + -(-K // 512) * 8192)
+
+
 def weight_bytes(cfg) -> int:
     return sum(N * (K // 256) * BYTES_PER_SB[q] for (_, q, N, K, _, _) in cfg["gemms"])
 
@@ -207,7 +213,7 @@ class Workload:
     """Device buffers for one configuration: repacked weights (several copies),
     f32 activations and residuals, q8_1 buffers and outputs."""
 
-    def __init__(self, cfg_id: int, seed: int = 0, copies: int | None = None, device="cuda"):
+    def __init__(self, cfg_id: int, seed: int = 0, copies: int | None = None, device="cuda", mmq_split: str = "auto"):
         import quantized_q8_activation_gb300 as qk
         self.qk = qk
         self.cfg_id = cfg_id
@@ -241,8 +247,14 @@ class Workload:
         self.banks = [self._make_bank(device)]
         self.use_bank(0)
         self.ws = None
+        self.mmq_split = mmq_split
         if cfg["kind"] == "mmq":
-            need = max(qk.mmq_workspace_bytes(M, N, K) for (_, _, N, K, _, _) in cfg["gemms"])
+            # qk_mmq_workspace_bytes includes the scratch of the split-K tail; a base-size workspace
+            # (mmq_split="off") runs every call unsplit
+            if mmq_split == "off":
+                need = max(mmq_base_workspace(M, K) for (_, _, _, K, _, _) in cfg["gemms"])
+            else:
+                need = max(qk.mmq_workspace_bytes(M, N, K) for (_, _, N, K, _, _) in cfg["gemms"])
             self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device) if need else None
         torch.cuda.synchronize()
 
@@ -304,7 +316,10 @@ class Workload:
             kw = dict(residual=self.r.get(name), y=self.y[name], pdl=pdl, stream=stream)
             if cfg["kind"] == "mmq":
                 fn = qk.mmq_q4k if q == "q4k" else qk.mmq_q6k
-                fn(self.w[copy][name], codes, scales, N, K, workspace=self.ws, **kw)
+                ws = self.ws
+                if self.mmq_split == "off":                    # this GEMM's base size: no split scratch
+                    ws = ws[:mmq_base_workspace(self.M, K)]
+                fn(self.w[copy][name], codes, scales, N, K, workspace=ws, **kw)
             else:
                 fn = {"q4k": qk.gemv_q4k, "q5k": qk.gemv_q5k, "q6k": qk.gemv_q6k, "q80": qk.gemv_q8_0,
                       "q2k": qk.gemv_q2k, "q3k": qk.gemv_q3k}[q]
@@ -682,7 +697,7 @@ def measure_config(cfg_id, args, stream, ws, device, peaks_meas=None, headline=F
     import quantized_q8_activation_gb300 as qk
     cfg = CONFIGS[cfg_id]
     front_end = args.front_end
-    wl = Workload(cfg_id, seed=0, copies=args.copies)
+    wl = Workload(cfg_id, seed=0, copies=args.copies, mmq_split=args.mmq_split)
     C, K = wl.copies, args.steps
     S = steps_per_replay(K, args.graph_steps)
     units = int_ops(cfg) if cfg["kind"] == "mmq" else weight_bytes(cfg)
@@ -987,6 +1002,9 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="--impl reference: total host time the warm-up and timed steps are sized to")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mmq-split", choices=["auto", "off"], default="auto",
+                    help="prefill MMQ workspace: with the split-K scratch (the library splits a tile's K range "
+                         "where its waves over the SMs are poorly filled) or the base size only (no split)")
     ap.add_argument("--front-end", choices=["batched", "auto", "fused", "unfused"], default="batched",
                     help="decode activation path: one quantize kernel over all of the step's f32 "
                          "activations, then q8_1 GEMVs (batched, default); q8_1 quantization inside each "

@@ -381,9 +381,17 @@ int qk_gemv_q3k_f32(const void *w, const float *x, int64_t ldx,
  *   nothing needs to be initialised.  Its contents are consumed by kernels of
  *   this call that run after the call returns, so the workspace must not be
  *   reused by work that is not ordered after this call on `stream`.  Size:
- *   ceil(M/128) * (K * 512 + ceil(K/512) * 8192) bytes (M = 2048,
- *   K = 18944: 160,038,912 bytes).
- * Returns QK_E_WORKSPACE if workspace_bytes is too small.
+ *   at least the base ceil(M/128) * (K * 512 + ceil(K/512) * 8192) bytes
+ *   (M = 2048, K = 18944: 160,038,912 bytes).  qk_mmq_workspace_bytes adds,
+ *   on the current device, the scratch of a split of each output tile's K
+ *   range over two work units, which the Q4_K MMQ takes when its tiles fill
+ *   the SMs' last wave poorly and K is long (at least 48 superblocks, so that
+ *   each unit has 24; Qwen2-7B down: 224 tiles on 152 SMs, K = 18944); the
+ *   two partial tiles are added in binary32 by the second unit to finish
+ *   (the same bits either way).  Where no split is taken it adds nothing.  A workspace of at least the base size
+ *   but below qk_mmq_workspace_bytes runs the call unsplit; the two forms
+ *   differ only in rounding, within the same bound, and each is reproducible.
+ * Returns QK_E_WORKSPACE if workspace_bytes is below the base size.
  */
 int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);
 
@@ -422,9 +430,11 @@ int qk_mmq_q6k(const void *w, const int8_t *codes, const void *scales,
  * workspace is a statically allocated device array of
  * QK_MMQ_STATIC_WS_BYTES bytes inside the library; the call allocates and
  * frees nothing.
- *  - Problems with qk_mmq_workspace_bytes(M, N, K) > QK_MMQ_STATIC_WS_BYTES
- *    return QK_E_WORKSPACE (nothing launched).  Example: M = 2048, K = 3584
- *    needs 30,277,632 bytes and fits; K = 18944 does not.
+ *  - Problems whose base workspace size (qk_mmq_q4k) exceeds
+ *    QK_MMQ_STATIC_WS_BYTES return QK_E_WORKSPACE (nothing launched).
+ *    Example: M = 2048, K = 3584 needs 30,277,632 bytes and fits; K = 18944
+ *    does not.  Where the array cannot also hold the split-K scratch, the
+ *    call runs unsplit.
  *  - The array needs no initialisation (each call writes what it reads).
  *  - All calls on a device share the array: calls that may run concurrently
  *    (other streams, unordered host threads) race on it.

@@ -66,6 +66,9 @@ inline int device_slot()
 // Largest dynamic shared memory a CTA may opt in to on the current device.
 size_t max_smem_optin();
 
+// MMQ workspace bytes without the split-K scratch (enough for an unsplit call).
+size_t mmq_base_workspace_bytes(int64_t M, int64_t K);
+
 // Every kernel of the library asks for the same (maximal) shared-memory
 // carveout, so consecutive kernels never force an L1/shared reconfiguration.
 template <typename Kern>

@@ -60,6 +60,9 @@
 #include <atomic>
 #include <cstring>
 
+#ifndef QK_MMQ_EPI_UNROLL
+#define QK_MMQ_EPI_UNROLL 8  // output rows whose residual values are loaded together
+#endif
 #ifndef QK_MMQ_NST
 #define QK_MMQ_NST 3        // operand stages
 #endif
@@ -83,6 +86,7 @@ namespace {
 
 using namespace qk::tc;
 
+constexpr int kEpiUnroll = QK_MMQ_EPI_UNROLL;
 constexpr int BM = 128, BK = 32;                // BK: one Q4_K / Q6_K 32-value sub-block
 constexpr int NST = QK_MMQ_NST, NRAW = QK_MMQ_RAW, NSB = QK_MMQ_SBRAW;
 constexpr int kEpiWarp0 = 4, kEpiWarps = 4, kConvWarp0 = 8;  // epilogue warps 4-7, converters from warp 8
@@ -145,6 +149,7 @@ __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity) { mbar_
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
+constexpr int kMaxSplit = 2;
 struct MmqArgs {
     const uint8_t *wsA;     // workspace: [M-tiles][K/32] A blocks
     const uint8_t *wsS;     // Q4_K: [M-tiles][ceil(K/512)] sums tiles (after all A blocks)
@@ -153,7 +158,48 @@ struct MmqArgs {
     const float *residual;
     float *y;
     int mtiles, ntiles;     // tile t covers M-tile t % mtiles, N-tile t / mtiles
+    // Q4_K split of the K range: work unit u is segment u % split of tile u / split; segment 0 covers
+    // superblocks [0, mid) and the min term, segment 1 [mid, K/256).  With split == 2 each unit
+    // leaves its partial tile in part[u] and the second unit of a tile to finish (cnt[tile]) adds the
+    // two partials and writes y.
+    int split;
+    int mid;                // split == 2: segment 0 covers superblocks [0, mid), segment 1 [mid, K/256)
+    float *part;            // [units][128][BN]
+    unsigned *cnt;          // [tiles], zeroed by the prep kernel
 };
+
+// One 32 x 16 chunk of an output tile, staged in a warp's transpose buffer (row r at r * EPI_LD),
+// to y: lane l stores column n (its own) of rows mb + 2 rr (rr < 16), mb = the chunk's first row
+// + l / 16, adding the residual where there is one.  The residual may be y itself, so each group
+// of kEpiUnroll rows has all its residual values loaded before any of its outputs is stored;
+// grouped, the loads of a group are in flight together.
+__device__ __forceinline__ void store_chunk(const MmqArgs &a, const float *tb_s, int64_t mb, int64_t n, int lane)
+{
+    const int tc = lane & 15, tr = lane >> 4;
+    if (!a.residual) {
+#pragma unroll
+        for (int rr = 0; rr < 16; rr++) {
+            const int64_t m = mb + 2 * rr;
+            if (m < a.M) a.y[(size_t)m * a.N + n] = tb_s[(2 * rr + tr) * EPI_LD + tc];
+        }
+        return;
+    }
+    const size_t ob = (size_t)mb * a.N + n, st2 = 2 * (size_t)a.N;
+#pragma unroll
+    for (int h = 0; h < 16 / kEpiUnroll; h++) {
+        float rv[kEpiUnroll];
+#pragma unroll
+        for (int i = 0; i < kEpiUnroll; i++) {
+            const int rr = kEpiUnroll * h + i;
+            rv[i] = mb + 2 * rr < a.M ? __ldcg(a.residual + ob + rr * st2) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < kEpiUnroll; i++) {
+            const int rr = kEpiUnroll * h + i;
+            if (mb + 2 * rr < a.M) a.y[ob + rr * st2] = __fadd_rn(tb_s[(2 * rr + tr) * EPI_LD + tc], rv[i]);
+        }
+    }
+}
 
 struct MmqMaps {
     CUtensorMap wcodes;     // uint8  [N][B*128]  Q4_K code plane, box 64 x 256; Q6_K ql plane, box 32 x 256
@@ -216,11 +262,14 @@ __device__ __forceinline__ void sts128(uint8_t *base, uint32_t off, uint32_t x, 
 // block of K stage 8 sb + j; rows past M are written as zeros.
 __global__ void __launch_bounds__(256) mmq_prep_kernel(const int8_t *__restrict__ codes,
                                                        const __half2 *__restrict__ scales, int64_t M, int64_t K,
-                                                       uint8_t *__restrict__ wsA, uint8_t *__restrict__ wsS)
+                                                       uint8_t *__restrict__ wsA, uint8_t *__restrict__ wsS,
+                                                       unsigned *__restrict__ cnt, int ncnt)
 {
     qk::pdl_launch_dependents();
     qk::pdl_wait();                              // codes may come from the previous kernel
     const int sb = blockIdx.x, mt = blockIdx.y;
+    if (sb == 0 && mt == 0)                      // the split-K tile counters of this call start at zero
+        for (int i = threadIdx.x; i < ncnt; i += 256) cnt[i] = 0;
     const int nit = (int)(K >> 5), B = (int)(K >> 8), nmin = (B + 1) >> 1;
 #pragma unroll 1
     for (int i = 0; i < 4; i++) {
@@ -520,16 +569,7 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
                 __syncwarp();
                 const int64_t n = n0 + 16 * c + (lane & 15);
                 if (n < a.N) {
-#pragma unroll 4
-                    for (int rr = 0; rr < 16; rr++) {
-                        const int r = 2 * rr + (lane >> 4);
-                        const int64_t m = m0 + q0 + r;
-                        if (m < a.M) {
-                            const float val = tb_s[r * EPI_LD + (lane & 15)];
-                            const size_t o = (size_t)m * a.N + n;
-                            a.y[o] = a.residual ? __fadd_rn(val, a.residual[o]) : val;
-                        }
-                    }
+                    store_chunk(a, tb_s, m0 + q0 + (lane >> 4), n, lane);
                 }
                 __syncwarp();
             }
@@ -696,6 +736,14 @@ __device__ __forceinline__ void mins_hilo(const uint4 &mt, uint32_t (&hi)[4], ui
     }
 }
 
+// superblock range [seg_lo, seg_hi) of segment seg of a tile
+__device__ __forceinline__ int seg_lo(const MmqArgs &a, int seg) { return seg == 0 ? 0 : a.mid; }
+__device__ __forceinline__ int seg_hi(const MmqArgs &a, int seg, int B) { return seg == 0 && a.split > 1 ? a.mid : B; }
+
+// named barrier 1 over the epilogue warps only
+template <int NW>
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory"); }
+
 template <int BN_>
 __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
     mmq_q4k_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
@@ -709,7 +757,7 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
     float *dring = reinterpret_cast<float *>(smem + L::OFF_D);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = (int)(a.K >> 8), nmin = (B + 1) >> 1;
-    const int ntiles = a.mtiles * a.ntiles;
+    const int S = a.split, nunits = a.mtiles * a.ntiles * S;
 
     qk::pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -741,8 +789,10 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         if (lane == 0) {
             const uint32_t sbase = smem_u32(smem);
             int gs = 0, ge = 0;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                for (int ev = 0; ev <= B; ev++, ge++) {
+            for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+                const int seg = u % S, nsb = seg_hi(a, seg, B) - seg_lo(a, seg);
+                // events: the min term (segment 0 only), then one per superblock of the segment
+                for (int ev = seg == 0 ? 0 : 1; ev <= nsb; ev++, ge++) {
                     const int acc = ge & 1;
                     if (ge >= 2) wait_bar(&bar[L::ACCEMPTY + acc], ((ge >> 1) + 1) & 1);
                     fence_after_sync();
@@ -786,11 +836,13 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         // per tile the sums tiles of its min stages (8 KB each), then the A blocks (16 KB)
         if (lane == 0) {
             int gs = 0;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                const int mt = t % a.mtiles;
+            for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+                const int t = u / S, seg = u % S, mt = t % a.mtiles;
                 const uint8_t *srcS = a.wsS + (size_t)mt * nmin * SBLK;
                 const uint8_t *srcA = a.wsA + (size_t)mt * (8 * B) * ABLOCK;
-                for (int i = 0; i < nmin + 8 * B; i++, gs++) {
+                // the sums tiles of the min stages (segment 0), then the A blocks of the segment's superblocks
+                const int i0 = seg == 0 ? 0 : nmin + 8 * seg_lo(a, seg), i1 = nmin + 8 * seg_hi(a, seg, B);
+                for (int i = i0; i < i1; i++, gs++) {
                     const int st = gs % NS;
                     if (gs >= NS) wait_bar(&bar[L::EMPTY + st], ((gs / NS) + 1) & 1);
                     const bool mn = i < nmin;
@@ -810,10 +862,13 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
             prefetch_tmap(&maps.wcodes);
             prefetch_tmap(&maps.meta);
             int gsb = 0, gu = 0;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+                const int t = u / S, seg = u % S;
                 const int n0 = (t / a.mtiles) * BN;
-                for (int pass = 0; pass < 2; pass++) {
-                    for (int sb = 0; sb < B; sb++, gsb++) {
+                // pass 0 (segment 0): every superblock's record for the min stages; pass 1: the segment's
+                // superblocks, record and code bytes
+                for (int pass = seg == 0 ? 0 : 1; pass < 2; pass++) {
+                    for (int sb = pass == 0 ? 0 : seg_lo(a, seg); sb < (pass == 0 ? B : seg_hi(a, seg, B)); sb++, gsb++) {
                         const int ss = gsb % NB;
                         if (gsb >= NB) wait_bar(&bar[L::SEMPTY + ss], ((gsb / NB) + 1) & 1);
                         mbar_arrive_expect_tx(&bar[L::SFULL + ss], L::SBR);
@@ -851,9 +906,13 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         float *tb_s = reinterpret_cast<float *>(smem + L::OFF_EPI) + ew * (32 * EPI_LD);
         float R[L::CPT];
         int ge = 0, gd = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+            const int t = u / S, seg = u % S;
             const int64_t m0 = (int64_t)(t % a.mtiles) * BM, n0 = (int64_t)(t / a.mtiles) * BN;
-            {
+            if (seg != 0) {
+#pragma unroll
+                for (int i = 0; i < L::CPT; i++) R[i] = 0.0f;
+            } else {
                 const int acc = ge & 1;
                 wait_bar(&bar[L::ACCFULL + acc], (ge >> 1) & 1);
                 fence_after_sync();
@@ -872,7 +931,7 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                 ge++;
             }
 #pragma unroll 1
-            for (int sb = 0; sb < B; sb++, ge++, gd++) {
+            for (int sb = seg_lo(a, seg); sb < seg_hi(a, seg, B); sb++, ge++, gd++) {
                 const int acc = ge & 1, ds = gd % ND;
                 wait_bar(&bar[L::DFULL + ds], (gd / ND) & 1);
                 wait_bar(&bar[L::ACCFULL + acc], (ge >> 1) & 1);
@@ -902,6 +961,41 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                     mbar_arrive(&bar[L::DEMPTY + ds]);
                 }
             }
+            if (S > 1) {
+                // this segment's partial tile: row (32 quad + lane), columns ch CPT .. +CPT, contiguous
+                const size_t poff = ((size_t)(quad * 32 + lane)) * BN + ch * L::CPT;
+                float4 *mine = reinterpret_cast<float4 *>(a.part + (size_t)u * BM * BN + poff);
+#pragma unroll
+                for (int c = 0; c < L::CPT / 4; c++) mine[c] = make_float4(R[4 * c], R[4 * c + 1], R[4 * c + 2], R[4 * c + 3]);
+                __threadfence();
+                epi_sync<L::kEpiW>();
+                unsigned *flag = reinterpret_cast<unsigned *>(smem + L::OFF_TMEM + 8);
+                if (ew == 0 && lane == 0) {
+                    const unsigned prev = atomicAdd(&a.cnt[t], 1u);
+                    const bool last = prev == (unsigned)(S - 1);
+                    if (last) {
+                        __threadfence();
+                        a.cnt[t] = 0;                      // ready for the next call on this workspace
+                    }
+                    *flag = last ? 1u : 0u;
+                }
+                epi_sync<L::kEpiW>();
+                const bool last = *flag != 0;
+                epi_sync<L::kEpiW>();                      // the flag is read before the next unit rewrites it
+                if (!last) continue;
+                // the last of the two segments to finish: y = P_0 + P_1, the same bits whichever it is
+                // (binary32 addition is commutative)
+                const float4 *other =
+                    reinterpret_cast<const float4 *>(a.part + (size_t)(u - seg + (1 - seg)) * BM * BN + poff);
+#pragma unroll
+                for (int c = 0; c < L::CPT / 4; c++) {
+                    const float4 w = __ldcg(other + c);
+                    R[4 * c] = __fadd_rn(R[4 * c], w.x);
+                    R[4 * c + 1] = __fadd_rn(R[4 * c + 1], w.y);
+                    R[4 * c + 2] = __fadd_rn(R[4 * c + 2], w.z);
+                    R[4 * c + 3] = __fadd_rn(R[4 * c + 3], w.w);
+                }
+            }
 #pragma unroll
             for (int c = 0; c < L::CPT / 16; c++) {
 #pragma unroll
@@ -909,16 +1003,7 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                 __syncwarp();
                 const int64_t n = n0 + ch * L::CPT + 16 * c + (lane & 15);
                 if (n < a.N) {
-#pragma unroll 4
-                    for (int rr = 0; rr < 16; rr++) {
-                        const int r = 2 * rr + (lane >> 4);
-                        const int64_t m = m0 + quad * 32 + r;
-                        if (m < a.M) {
-                            const float val = tb_s[r * EPI_LD + (lane & 15)];
-                            const size_t o = (size_t)m * a.N + n;
-                            a.y[o] = a.residual ? __fadd_rn(val, a.residual[o]) : val;
-                        }
-                    }
+                    store_chunk(a, tb_s, m0 + quad * 32 + (lane >> 4), n, lane);
                 }
                 __syncwarp();
             }
@@ -930,10 +1015,11 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         // swizzle spreads over all 32 banks
         const int row = 32 * (warp - L::kConvW0) + lane;
         int gs = 0, gsb = 0, gu = 0, gd = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-            // min stages: sub-blocks of superblocks 2i and 2i+1 -> (Mw_hi | Mw_lo)
+        for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+            const int seg = u % S;
+            // min stages (segment 0): sub-blocks of superblocks 2i and 2i+1 -> (Mw_hi | Mw_lo)
 #pragma unroll 1
-            for (int i = 0; i < nmin; i++, gs++) {
+            for (int i = 0; i < (seg == 0 ? nmin : 0); i++, gs++) {
                 const int st = gs % NS;
                 const bool two = 2 * i + 1 < B;
                 const int ss0 = gsb % NB, ss1 = (gsb + 1) % NB;
@@ -966,7 +1052,7 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
             }
             // main stages: per superblock its scale d into the scale ring, then sub-block j -> W' = sc q
 #pragma unroll 1
-            for (int sb = 0; sb < B; sb++, gsb++, gd++) {
+            for (int sb = seg_lo(a, seg); sb < seg_hi(a, seg, B); sb++, gsb++, gd++) {
                 const int ss = gsb % NB, ds = gd % ND;
                 wait_bar(&bar[L::SFULL + ss], (gsb / NB) & 1);
                 const uint4 mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * L::SBR + row * 16);
@@ -1076,6 +1162,58 @@ size_t ws_bytes(int64_t M, int64_t K)
     return ws_a_bytes(M, K) + mt * (size_t)((K / 256 + 1) / 2) * SBLK;
 }
 
+// Split of each tile's K range over `split` work units (Q4_K, at most two): taken when it shortens the
+// schedule of waves of units over the SMs by more than the partial-tile traffic costs (3 %), and only
+// for long segments (kMinSegSb superblocks or more each): every unit ends with an epilogue that
+// writes its partial tile and the second one reads it back, which on short segments costs more than
+// the shorter schedule saves (measured: K = 3584, 7 superblocks a segment, 224 tiles on 152 SMs ran
+// slower split; K = 18944, 35 and 39 superblocks, ran 7 % faster split).  Segment 0 covers superblocks
+// [0, mid) and the min term, segment 1 [mid, K/256).
+constexpr int kMinSegSb = 24;
+int pick_split(int64_t tiles, int B, int sms)
+{
+    double best = (double)((tiles + sms - 1) / sms);
+    int bs = 1;
+    for (int S = 2; S <= kMaxSplit; S++) {
+        if (B < kMinSegSb * S) break;
+        const double c = (double)((tiles * S + sms - 1) / sms) / S * (1.0 + 0.03 * (S - 1));
+        if (c < best - 1e-9) best = c, bs = S;
+    }
+    return bs;
+}
+
+// first superblock of segment 1: the two segments' MMA work balanced, segment 0 also carrying the min term
+int split_mid(int B)
+{
+    const double c = 3.0 * ((B + 1) / 2) / 32.0;                // the min term in superblock units
+    int b = (int)((B + c) / 2 - c + 0.5);
+    return b < 1 ? 1 : b > B - 1 ? B - 1 : b;
+}
+
+// tile width and split of a Q4_K call on `sms` SMs
+struct Q4Plan {
+    int BN, split;
+    int64_t tiles;
+};
+
+int pick_bn(int64_t M, int64_t N, int sms);
+
+Q4Plan q4_plan(int64_t M, int64_t N, int64_t K, unsigned flags, int sms)
+{
+    Q4Plan p;
+    p.BN = (flags & QK_MMQ_TILE_256) ? 256 : (flags & QK_MMQ_TILE_128) ? 128 : pick_bn(M, N, sms);
+    p.tiles = ((M + BM - 1) / BM) * ((N + p.BN - 1) / p.BN);
+    p.split = pick_split(p.tiles, (int)(K / 256), sms);
+    return p;
+}
+
+// scratch of a split call after the base workspace: the partial tiles, then the tile counters
+size_t split_bytes(const Q4Plan &p)
+{
+    if (p.split <= 1) return 0;
+    return (size_t)p.tiles * p.split * BM * p.BN * 4 + (size_t)p.tiles * 4;
+}
+
 // The register-split kernel must be launched with exactly the registers its setmaxnreg split hands
 // out: with fewer, the epilogue warps' increase could never be granted.  Checked once per kernel,
 // before its first launch.
@@ -1132,6 +1270,7 @@ int set_attrs()
 // only where ceil(tiles_128 / sms) * 0.7 < ceil(tiles_256 / sms): in practice single-wave problems.
 int pick_bn(int64_t M, int64_t N, int sms)
 {
+    if (sms < 1) sms = 1;
     const int64_t gx = (M + BM - 1) / BM;
     const int64_t w256 = (gx * ((N + 255) / 256) + sms - 1) / sms, w128 = (gx * ((N + 127) / 128) + sms - 1) / sms;
     return w128 * 7 < w256 * 10 ? 128 : 256;
@@ -1160,17 +1299,21 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
         return QK_E_ALIGN;
     const size_t need = ws_bytes(M, K);
     if (workspace_bytes < need) return QK_E_WORKSPACE;
+    if ((flags & QK_MMQ_TILE_256) && (flags & QK_MMQ_TILE_128)) return QK_E_SHAPE;
+    const int sms = qk::sm_count();
+    Q4Plan plan = q4_plan(M, N, K, flags, sms);
+    if (qt == QK_TYPE_Q6_K || workspace_bytes < need + split_bytes(plan)) plan.split = 1;   // no scratch: no split
+    const size_t used = need + split_bytes(plan);                     // the workspace bytes this call writes
     size_t wbytes = 0;
     qk_repacked_bytes(qt, N, K, &wbytes);
     const size_t ybytes = (size_t)M * N * 4, cbytes = (size_t)M * K, sbytes = (size_t)M * (K / 32) * 4;
     if (qk::overlaps(y, ybytes, w, wbytes) || qk::overlaps(y, ybytes, codes, cbytes) ||
         qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)) ||
-        qk::overlaps(workspace, need, w, wbytes) || qk::overlaps(workspace, need, codes, cbytes) ||
-        qk::overlaps(workspace, need, scales, sbytes) || qk::overlaps(workspace, need, y, ybytes) ||
-        (residual && qk::overlaps(workspace, need, residual, ybytes)))
+        qk::overlaps(workspace, used, w, wbytes) || qk::overlaps(workspace, used, codes, cbytes) ||
+        qk::overlaps(workspace, used, scales, sbytes) || qk::overlaps(workspace, used, y, ybytes) ||
+        (residual && qk::overlaps(workspace, used, residual, ybytes)))
         return QK_E_ALIAS;
-    if ((flags & QK_MMQ_TILE_256) && (flags & QK_MMQ_TILE_128)) return QK_E_SHAPE;
-    const int BN = (flags & QK_MMQ_TILE_256) ? 256 : (flags & QK_MMQ_TILE_128) ? 128 : pick_bn(M, N, qk::sm_count());
+    const int BN = plan.BN;
     const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
     if (gx > 65535 || gy > 65535 || gx * gy > 0x7fffffffLL) return QK_E_SHAPE;
     const bool q6 = qt == QK_TYPE_Q6_K;
@@ -1205,14 +1348,35 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
         const int sa = BN == 128 ? set_attrs_q4<128>() : set_attrs_q4<256>();
         if (sa != QK_OK) return sa;
     }
+    float *part = nullptr;
+    unsigned *cnt = nullptr;
+    if (plan.split > 1) {
+        part = reinterpret_cast<float *>(wsA + need);
+        cnt = reinterpret_cast<unsigned *>(wsA + need + (size_t)plan.tiles * plan.split * BM * BN * 4);
+    }
     int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, cs,
-                        (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA, wsS);
+                        (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA, wsS,
+                        cnt, plan.split > 1 ? (int)plan.tiles : 0);
     if (st != QK_OK) return st;
-    MmqArgs args{wsA, wsS, q6 ? reinterpret_cast<const uint16_t *>(wb + N * B * 208) : nullptr, M, N, K, residual, y,
-                 (int)gx, (int)gy};
+    MmqArgs args{};
+    args.wsA = wsA;
+    args.wsS = wsS;
+    args.dq = q6 ? reinterpret_cast<const uint16_t *>(wb + N * B * 208) : nullptr;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.residual = residual;
+    args.y = y;
+    args.mtiles = (int)gx;
+    args.ntiles = (int)gy;
+    args.split = plan.split;
+    args.mid = plan.split > 1 ? split_mid((int)B) : (int)B;
+    args.part = part;
+    args.cnt = cnt;
     if (q6) return BN == 128 ? launch_mmq<QK_TYPE_Q6_K, 128>(args, maps, tiles, cs)
                              : launch_mmq<QK_TYPE_Q6_K, 256>(args, maps, tiles, cs);
-    return BN == 128 ? launch_mmq_q4<128>(args, maps, tiles, cs) : launch_mmq_q4<256>(args, maps, tiles, cs);
+    return BN == 128 ? launch_mmq_q4<128>(args, maps, tiles * plan.split, cs)
+                     : launch_mmq_q4<256>(args, maps, tiles * plan.split, cs);
 }
 
 }  // namespace
@@ -1232,9 +1396,14 @@ extern "C" int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *b
 {
     if (!bytes) return QK_E_NULL;
     if (M < 0 || N < 1 || K < 256 || K % 256 != 0) return QK_E_SHAPE;
-    *bytes = ws_bytes(M, K);
+    *bytes = ws_bytes(M, K) + (M > 0 ? split_bytes(q4_plan(M, N, K, 0, qk::sm_count())) : 0);
     return QK_OK;
 }
+
+namespace qk {
+// the workspace a call needs without the split scratch (a workspace of this size runs unsplit)
+size_t mmq_base_workspace_bytes(int64_t M, int64_t K) { return ws_bytes(M, K); }
+}  // namespace qk
 
 extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N, int64_t K,
                           const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,

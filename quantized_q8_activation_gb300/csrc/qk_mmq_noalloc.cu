@@ -53,7 +53,8 @@ extern "C" int qk_mmq_q4k_noalloc(const void *w, const int8_t *codes, const void
     const int st = qk_mmq_workspace_bytes(M, N, K, &need);
     if (st != QK_OK) return st;
     if (M == 0) return QK_OK;
-    if (need > kStaticWsBytes) return QK_E_WORKSPACE;
+    // the static array runs the call unsplit when it cannot also hold the split-K scratch
+    if (qk::mmq_base_workspace_bytes(M, K) > kStaticWsBytes) return QK_E_WORKSPACE;
     void *ws = static_ws_address();
     if (!ws) return QK_E_CUDA;
     return qk_mmq_q4k(w, codes, scales, M, N, K, residual, y, ws, kStaticWsBytes, flags, stream);

@@ -416,6 +416,40 @@ def test_mmq_superblock_scale_special_cases(qt):
     assert qk.error_flags(clear=True) == 0            # inside the value limits: no range flag
 
 
+@pytest.mark.parametrize("M,N", [(256, 256 * 112), (200, 256 * 112 - 40)])
+def test_mmq_q4k_split_k_tail(M, N):
+    """224 tiles of 128 x 256 on 152 SMs with 48 superblocks of K: with the full workspace the Q4_K
+    MMQ splits each tile's K range over two work units (the second to finish adds the partial tiles).
+    Checked against the oracle on sampled rows, against the same call run unsplit (a base-size
+    workspace), for reproducibility, and for the tile counters being left at zero."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the split decision is sized for 152 SMs")
+    K = 48 * 256
+    w, wr = weights("q4k", N, K, seed=41)
+    codes, scales = q8(synth.activations(M, K, seed=42))
+    c, d = q8_host(codes, scales)
+    r = dev(synth.residual(M, N, seed=43))
+    full = qk.mmq_workspace_bytes(M, N, K)
+    base = 2 * (K * 512 + (K // 512) * 8192)              # two M-tiles: A blocks and sums tiles
+    assert full > base                                    # the split scratch is requested
+    ws = torch.empty(full, dtype=torch.uint8, device="cuda")
+    qk.error_flags(clear=True)
+    y1 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws)
+    y2 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws, pdl=True)
+    yu = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws[:base])
+    torch.cuda.synchronize()
+    assert qk.error_flags(clear=True) == 0
+    assert torch.equal(y1, y2)
+    counters = ws[full - 224 * 4:].view(torch.int32)
+    assert torch.count_nonzero(counters).item() == 0
+    r_np = r.cpu().numpy()
+    for lo in (0, N // 2 - 20, N - 40):                   # first, middle and last tiles
+        hi = lo + 40
+        y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d, residual=r_np, rows=(lo, hi))
+        check(y1.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"split rows {lo}")
+        check(yu.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"unsplit rows {lo}")
+
+
 def _f16_bytes(v):
     return np.frombuffer(np.float16(v).tobytes(), np.uint8)
 
