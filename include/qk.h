@@ -422,6 +422,41 @@ int qk_mmq_q6k(const void *w, const int8_t *codes, const void *scales,
                void *workspace, size_t workspace_bytes,
                unsigned flags, void *stream);
 
+/* ======================================= Q4_K MMQ with a min-operand plane
+ * The load-time scale plane of minfer "15 . The CUDA backend" sec. 3.2.6
+ * (the W_dsc plane: scale pairs computed once when the weights are loaded,
+ * so that the MMQ's hot loop does not decode the packed sub-block fields),
+ * restated for this library's Q4_K MMQ.  Its min term needs, per weight row
+ * and sub-block, the operand 1024 * dmin * m split exactly into two f16
+ * (hi: 11 significant bits, lo: the rest); without a plane every CTA builds
+ * them from the 6-bit fields for every tile.  The plane holds them ready:
+ *   qk_q4k_min_plane_bytes: N * ceil(K/512) * 64 bytes.
+ *   qk_q4k_min_plane: builds the plane of a repacked Q4_K weight w (N x K,
+ *     qk_repack output) into `plane` (device, 16-byte aligned, `bytes` >=
+ *     qk_q4k_min_plane_bytes, not overlapping w).  Layout: [N][ceil(K/512)]
+ *     records of 64 bytes, record (n, i) = the 8 hi f16 pairs of superblocks
+ *     2i and 2i+1 (sub-blocks 0-7 of each, two per 4-byte word) then their
+ *     8 lo pairs; an odd last superblock leaves its partner's words zero.
+ *     Asynchronous on `stream`; a weight with dmin * m >= 63 sets
+ *     QK_ERR_RANGE (qk_error_flags), as the MMQ would.
+ *   qk_mmq_q4k_plane: qk_mmq_q4k reading the min operands from the plane
+ *     (built from the same w; not checked) instead of building them.  Same
+ *     arguments otherwise, and the same result bit for bit: the operands are
+ *     the same words.
+ * Returns as qk_mmq_q4k; QK_E_NULL for a NULL plane, QK_E_ALIGN for a plane
+ * not 16-byte aligned, QK_E_ALIAS if it overlaps y or the workspace, and
+ * QK_E_WORKSPACE from qk_q4k_min_plane for too small a plane.
+ */
+int qk_q4k_min_plane_bytes(int64_t N, int64_t K, size_t *bytes);
+
+int qk_q4k_min_plane(const void *w, int64_t N, int64_t K, void *plane, size_t bytes, void *stream);
+
+int qk_mmq_q4k_plane(const void *w, const void *plane, const int8_t *codes, const void *scales,
+                     int64_t M, int64_t N, int64_t K,
+                     const float *residual, float *y,
+                     void *workspace, size_t workspace_bytes,
+                     unsigned flags, void *stream);
+
 /* ================================================ MMQ without a workspace
  * The pages have no counterpart of this entry point: it is a convenience of
  * this library for callers that cannot supply a device workspace (a host

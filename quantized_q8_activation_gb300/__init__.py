@@ -54,6 +54,7 @@ EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1"
            "qk_gemv_q5k_f32", "qk_gemv_q8_0", "qk_gemv_q8_0_f32", "qk_gemv_q2k", "qk_gemv_q3k",
            "qk_gemv_q2k_f32", "qk_gemv_q3k_f32",
            "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_mmq_q6k", "qk_mmq_q4k_noalloc", "qk_error_flags",
+           "qk_q4k_min_plane_bytes", "qk_q4k_min_plane", "qk_mmq_q4k_plane",
            "qk_rmsnorm_q8_1", "qk_swiglu_q8_1",
            # include/qk_peak.h (measurement)
            "qk_peak_mma_s8", "qk_peak_tcgen05_f16"]
@@ -110,6 +111,9 @@ def lib() -> ctypes.CDLL:
             L.qk_mmq_workspace_bytes.argtypes = [i64, i64, i64, szp]
             L.qk_mmq_q4k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
             L.qk_mmq_q6k.argtypes = [p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
+            L.qk_q4k_min_plane_bytes.argtypes = [i64, i64, szp]
+            L.qk_q4k_min_plane.argtypes = [p, i64, i64, p, ctypes.c_size_t, p]
+            L.qk_mmq_q4k_plane.argtypes = [p, p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
             L.qk_rmsnorm_q8_1.argtypes = [p, i64, p, p, ctypes.c_float, i64, i64, p, p, p, p, u, p]
             L.qk_swiglu_q8_1.argtypes = [p, i64, i64, i64, p, p, p, u, p]
             L.qk_mmq_q4k_noalloc.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
@@ -379,7 +383,37 @@ def mmq_q6k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=F
     return _mmq("qk_mmq_q6k", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile)
 
 
-def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile=None):
+def q4k_min_plane_bytes(N: int, K: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().qk_q4k_min_plane_bytes(N, K, ctypes.byref(b)), "qk_q4k_min_plane_bytes")
+    return b.value
+
+
+def q4k_min_plane(w, N, K, plane=None, stream=None):
+    """The load-time min-operand plane of a repacked Q4_K weight (qk_q4k_min_plane), for
+    mmq_q4k_plane.  plane: a uint8 CUDA tensor of q4k_min_plane_bytes(N, K) bytes; when None,
+    this wrapper allocates one with torch."""
+    _cuda(w, "w")
+    need = q4k_min_plane_bytes(N, K)
+    if plane is None:
+        plane = torch.empty(need, dtype=torch.uint8, device=w.device)
+    _cuda(plane, "plane")
+    with _on(w):
+        st = lib().qk_q4k_min_plane(w.data_ptr(), N, K, plane.data_ptr(), plane.numel() * plane.element_size(),
+                                    _stream(stream))
+    _check(st, "qk_q4k_min_plane")
+    return plane
+
+
+def mmq_q4k_plane(w, plane, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None,
+                  tile=None):
+    """mmq_q4k reading the min operands from a plane made by q4k_min_plane from the same weight
+    (same result bit for bit; workspace as for mmq_q4k)."""
+    _cuda(plane, "plane")
+    return _mmq("qk_mmq_q4k_plane", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile, plane)
+
+
+def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile=None, plane=None):
     M = codes.shape[0]
     for t, n in ((w, "w"), (codes, "codes"), (scales, "scales")):
         _cuda(t, n)
@@ -390,9 +424,13 @@ def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile=N
         workspace = torch.empty(need, dtype=torch.uint8, device=codes.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     flags = (LAUNCH_PDL if pdl else 0) | {None: 0, 256: MMQ_TILE_256, 128: MMQ_TILE_128}[tile]
+    args = (codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(), _p(workspace), wsb, flags,
+            _stream(stream))
     with _on(codes):
-        st = getattr(lib(), fn)(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual),
-                                y.data_ptr(), _p(workspace), wsb, flags, _stream(stream))
+        if plane is None:
+            st = getattr(lib(), fn)(w.data_ptr(), *args)
+        else:
+            st = getattr(lib(), fn)(w.data_ptr(), plane.data_ptr(), *args)
     _check(st, fn)
     return y
 

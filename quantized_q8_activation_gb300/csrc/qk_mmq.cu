@@ -202,9 +202,10 @@ __device__ __forceinline__ void store_chunk(const MmqArgs &a, const float *tb_s,
 }
 
 struct MmqMaps {
-    CUtensorMap wcodes;     // uint8  [N][B*128]  Q4_K code plane, box 64 x 256; Q6_K ql plane, box 32 x 256
-    CUtensorMap meta;       // uint8  [N][B*16]   Q4_K metadata plane / Q6_K scale plane, box 16 x 256
-    CUtensorMap qh;         // uint8  [N][B*64]   Q6_K qh plane, box 32 x 256 (unused for Q4_K)
+    CUtensorMap wcodes;     // uint8  [N][B*128]  Q4_K code plane, box 32 x BN (32-byte swizzle); Q6_K ql plane
+    CUtensorMap meta;       // uint8  [N][B*16]   Q4_K metadata plane / Q6_K scale plane, box 16 x BN
+    CUtensorMap qh;         // uint8  [N][B*64]   Q6_K qh plane, box 32 x BN (unused for Q4_K)
+    CUtensorMap plane;      // uint8  [N][nmin*64] Q4_K min-operand plane, box 64 x BN (64-byte swizzle; plane calls)
 };
 
 // 4 int8 codes -> (A_hi, A_lo) f16 pairs with A_hi + A_lo = d * q exactly
@@ -736,6 +737,34 @@ __device__ __forceinline__ void mins_hilo(const uint4 &mt, uint32_t (&hi)[4], ui
     }
 }
 
+// Load-time min-operand plane of a repacked Q4_K weight (qk_q4k_min_plane): for row n and pair i of
+// superblocks (2i, 2i+1), the 64 bytes a min stage's converter builds from their metadata records,
+// in the order it stores them: the Mw_hi words of superblock 2i, those of 2i+1, then the Mw_lo words
+// of each (a missing superblock 2i+1 gives zeros).  One thread per (n, i).
+__global__ void __launch_bounds__(256) q4k_min_plane_kernel(const uint4 *__restrict__ meta, int64_t N, int B,
+                                                            uint4 *__restrict__ plane)
+{
+    const int nmin = (B + 1) >> 1;
+    const int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    bool bad = false;
+    if (idx < N * nmin) {
+        const int64_t n = idx / nmin;
+        const int i = (int)(idx - n * nmin);
+        const uint4 *rec = meta + n * B + 2 * i;
+        const uint4 r0 = __ldg(rec);
+        const uint4 r1 = 2 * i + 1 < B ? __ldg(rec + 1) : make_uint4(0, 0, 0, 0);
+        uint32_t h0[4], l0[4], h1[4], l1[4];
+        mins_hilo(r0, h0, l0, bad);
+        mins_hilo(r1, h1, l1, bad);
+        uint4 *o = plane + 4 * idx;
+        o[0] = make_uint4(h0[0], h0[1], h0[2], h0[3]);
+        o[1] = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+        o[2] = make_uint4(l0[0], l0[1], l0[2], l0[3]);
+        o[3] = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+    }
+    flag_range(bad);
+}
+
 // superblock range [seg_lo, seg_hi) of segment seg of a tile
 __device__ __forceinline__ int seg_lo(const MmqArgs &a, int seg) { return seg == 0 ? 0 : a.mid; }
 __device__ __forceinline__ int seg_hi(const MmqArgs &a, int seg, int B) { return seg == 0 && a.split > 1 ? a.mid : B; }
@@ -744,7 +773,7 @@ __device__ __forceinline__ int seg_hi(const MmqArgs &a, int seg, int B) { return
 template <int NW>
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory"); }
 
-template <int BN_>
+template <int BN_, bool PL>
 __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
     mmq_q4k_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
 {
@@ -856,18 +885,26 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------ raw weight TMA producer
-        // per tile: the metadata records of every superblock (min stages), then per superblock its
-        // record again and its code bytes
+        // per tile: the metadata records of every superblock (min stages; with a min-operand plane, its
+        // tiles instead, through the raw ring), then per superblock its record again and its code bytes
         if (lane == 0) {
             prefetch_tmap(&maps.wcodes);
             prefetch_tmap(&maps.meta);
+            if (PL) prefetch_tmap(&maps.plane);
             int gsb = 0, gu = 0;
             for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
                 const int t = u / S, seg = u % S;
                 const int n0 = (t / a.mtiles) * BN;
-                // pass 0 (segment 0): every superblock's record for the min stages; pass 1: the segment's
-                // superblocks, record and code bytes
-                for (int pass = seg == 0 ? 0 : 1; pass < 2; pass++) {
+                if (PL && seg == 0)
+                    for (int i = 0; i < nmin; i++, gu++) {
+                        const int rs = gu % NR;
+                        if (gu >= NR) wait_bar(&bar[L::REMPTY + rs], ((gu / NR) + 1) & 1);
+                        mbar_arrive_expect_tx(&bar[L::RFULL + rs], L::RAW);
+                        tma_load_2d(smem + L::OFF_RAW + rs * L::RAW, &maps.plane, 64 * i, n0, &bar[L::RFULL + rs]);
+                    }
+                // pass 0 (segment 0, no plane): every superblock's record for the min stages; pass 1: the
+                // segment's superblocks, record and code bytes
+                for (int pass = seg == 0 && !PL ? 0 : 1; pass < 2; pass++) {
                     for (int sb = pass == 0 ? 0 : seg_lo(a, seg); sb < (pass == 0 ? B : seg_hi(a, seg, B)); sb++, gsb++) {
                         const int ss = gsb % NB;
                         if (gsb >= NB) wait_bar(&bar[L::SEMPTY + ss], ((gsb / NB) + 1) & 1);
@@ -1021,6 +1058,27 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
 #pragma unroll 1
             for (int i = 0; i < (seg == 0 ? nmin : 0); i++, gs++) {
                 const int st = gs % NS;
+                if constexpr (PL) {
+                    // the stage's operand row, built at load time: copied from the raw ring as it is
+                    const int rs = gu % NR;
+                    wait_bar(&bar[L::RFULL + rs], (gu / NR) & 1);
+                    const uint8_t *raw = smem + L::OFF_RAW + rs * L::RAW;
+                    uint4 q[4];
+#pragma unroll
+                    for (int c = 0; c < 4; c++) q[c] = *reinterpret_cast<const uint4 *>(raw + sw64(row, c));
+                    if (gs >= NS) wait_bar(&bar[L::EMPTY + st], ((gs / NS) + 1) & 1);
+                    uint8_t *w0 = smem + st * L::STAGE + 2 * ATILE;
+#pragma unroll
+                    for (int c = 0; c < 4; c++) sts128(w0, sw64(row, c), q[c].x, q[c].y, q[c].z, q[c].w);
+                    fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&bar[L::REMPTY + rs]);     // its values were stored above
+                        mbar_arrive(&bar[L::FULL + st]);
+                    }
+                    gu++;
+                    continue;
+                }
                 const bool two = 2 * i + 1 < B;
                 const int ss0 = gsb % NB, ss1 = (gsb + 1) % NB;
                 wait_bar(&bar[L::SFULL + ss0], (gsb / NB) & 1);
@@ -1217,7 +1275,7 @@ size_t split_bytes(const Q4Plan &p)
 // The register-split kernel must be launched with exactly the registers its setmaxnreg split hands
 // out: with fewer, the epilogue warps' increase could never be granted.  Checked once per kernel,
 // before its first launch.
-template <int BN>
+template <int BN, bool PL>
 int set_attrs_q4()
 {
     static std::atomic<int> done_dev[qk::kMaxDevices];
@@ -1225,27 +1283,27 @@ int set_attrs_q4()
     if (dev < 0) return QK_E_CUDA;
     std::atomic<int> &done = done_dev[dev];
     if (done.load()) return QK_OK;
-    if (cudaFuncSetAttribute(mmq_q4k_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Plan4<BN>::SMEM) !=
-            cudaSuccess ||
-        qk::max_carveout(mmq_q4k_kernel<BN>) != cudaSuccess)
+    if (cudaFuncSetAttribute(mmq_q4k_kernel<BN, PL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Plan4<BN>::SMEM) != cudaSuccess ||
+        qk::max_carveout(mmq_q4k_kernel<BN, PL>) != cudaSuccess)
         return QK_E_CUDA;
     if (Plan4<BN>::kSplitRegs) {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, mmq_q4k_kernel<BN>) != cudaSuccess || fa.numRegs != Plan4<BN>::kRegLaunch)
+        if (cudaFuncGetAttributes(&fa, mmq_q4k_kernel<BN, PL>) != cudaSuccess || fa.numRegs != Plan4<BN>::kRegLaunch)
             return QK_E_CUDA;
     }
     done.store(1);
     return QK_OK;
 }
 
-template <int BN>
+template <int BN, bool PL>
 int launch_mmq_q4(const MmqArgs &args, const MmqMaps &maps, int64_t tiles, cudaStream_t stream)
 {
-    const int st = set_attrs_q4<BN>();
+    const int st = set_attrs_q4<BN, PL>();
     if (st != QK_OK) return st;
     const int64_t grid = tiles < qk::sm_count() ? tiles : qk::sm_count();
-    return qk::launch(mmq_q4k_kernel<BN>, dim3((unsigned)grid), dim3(Plan4<BN>::kThreads), Plan4<BN>::SMEM, stream,
-                      true, args, maps);
+    return qk::launch(mmq_q4k_kernel<BN, PL>, dim3((unsigned)grid), dim3(Plan4<BN>::kThreads), Plan4<BN>::SMEM,
+                      stream, true, args, maps);
 }
 
 template <int QT, int BN>
@@ -1286,8 +1344,12 @@ int launch_mmq(const MmqArgs &args, const MmqMaps &maps, int64_t tiles, cudaStre
                       stream, true, args, maps);
 }
 
-int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N, int64_t K,
-        const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags, void *stream)
+// bytes of the Q4_K min-operand plane of an N x K weight: 64 per row and pair of superblocks
+size_t plane_bytes(int64_t N, int64_t K) { return (size_t)N * (size_t)((K / 256 + 1) / 2) * 64; }
+
+int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const void *scales, int64_t M, int64_t N,
+        int64_t K, const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,
+        void *stream)
 {
     // TMA coordinates are signed 32-bit: rows and bytes of a row stay below 2^31
     if (M < 0 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || M > 0x7fffffffLL || K > 0x7fffffffLL)
@@ -1295,7 +1357,7 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
     if (M == 0) return QK_OK;
     if (!w || !codes || !scales || !y || !workspace) return QK_E_NULL;
     if (!qk::aligned(w, 16) || !qk::aligned(codes, 16) || !qk::aligned(scales, 16) || !qk::aligned(y, 4) ||
-        (residual && !qk::aligned(residual, 4)) || !qk::aligned(workspace, 256))
+        (residual && !qk::aligned(residual, 4)) || !qk::aligned(workspace, 256) || !qk::aligned(plane, 16))
         return QK_E_ALIGN;
     const size_t need = ws_bytes(M, K);
     if (workspace_bytes < need) return QK_E_WORKSPACE;
@@ -1311,7 +1373,9 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
         qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)) ||
         qk::overlaps(workspace, used, w, wbytes) || qk::overlaps(workspace, used, codes, cbytes) ||
         qk::overlaps(workspace, used, scales, sbytes) || qk::overlaps(workspace, used, y, ybytes) ||
-        (residual && qk::overlaps(workspace, used, residual, ybytes)))
+        (residual && qk::overlaps(workspace, used, residual, ybytes)) ||
+        (plane && (qk::overlaps(y, ybytes, plane, plane_bytes(N, K)) ||
+                   qk::overlaps(workspace, used, plane, plane_bytes(N, K)))))
         return QK_E_ALIAS;
     const int BN = plan.BN;
     const int64_t gx = (M + BM - 1) / BM, gy = (N + BN - 1) / BN;
@@ -1331,6 +1395,10 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
             !make_map(enc, &maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 16, N, B * 16, 16,
                       (uint32_t)BN))
             return QK_E_CUDA;
+        const uint64_t prow = (uint64_t)((B + 1) / 2) * 64;
+        if (plane && !make_map(enc, &maps.plane, CU_TENSOR_MAP_DATA_TYPE_UINT8, plane, prow, N, prow, 64,
+                               (uint32_t)BN, CU_TENSOR_MAP_SWIZZLE_64B))
+            return QK_E_CUDA;
     } else {
         if (!make_map(enc, &maps.wcodes, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb, B * 128, N, B * 128, 32, (uint32_t)BN) ||
             !make_map(enc, &maps.qh, CU_TENSOR_MAP_DATA_TYPE_UINT8, wb + N * B * 128, B * 64, N, B * 64, 32,
@@ -1345,7 +1413,8 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
     cudaStream_t cs = (cudaStream_t)stream;
     if (!q6) {
         // validate the main kernel's launch configuration before anything is launched
-        const int sa = BN == 128 ? set_attrs_q4<128>() : set_attrs_q4<256>();
+        const int sa = plane ? (BN == 128 ? set_attrs_q4<128, true>() : set_attrs_q4<256, true>())
+                             : (BN == 128 ? set_attrs_q4<128, false>() : set_attrs_q4<256, false>());
         if (sa != QK_OK) return sa;
     }
     float *part = nullptr;
@@ -1375,8 +1444,10 @@ int mmq(int qt, const void *w, const int8_t *codes, const void *scales, int64_t 
     args.cnt = cnt;
     if (q6) return BN == 128 ? launch_mmq<QK_TYPE_Q6_K, 128>(args, maps, tiles, cs)
                              : launch_mmq<QK_TYPE_Q6_K, 256>(args, maps, tiles, cs);
-    return BN == 128 ? launch_mmq_q4<128>(args, maps, tiles * plan.split, cs)
-                     : launch_mmq_q4<256>(args, maps, tiles * plan.split, cs);
+    const int64_t units = tiles * plan.split;
+    if (plane)
+        return BN == 128 ? launch_mmq_q4<128, true>(args, maps, units, cs) : launch_mmq_q4<256, true>(args, maps, units, cs);
+    return BN == 128 ? launch_mmq_q4<128, false>(args, maps, units, cs) : launch_mmq_q4<256, false>(args, maps, units, cs);
 }
 
 }  // namespace
@@ -1409,12 +1480,49 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
                           const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,
                           void *stream)
 {
-    return mmq(QK_TYPE_Q4_K, w, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags, stream);
+    return mmq(QK_TYPE_Q4_K, w, nullptr, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags,
+               stream);
+}
+
+extern "C" int qk_q4k_min_plane_bytes(int64_t N, int64_t K, size_t *bytes)
+{
+    if (!bytes) return QK_E_NULL;
+    if (N < 1 || K < 256 || K % 256 != 0) return QK_E_SHAPE;
+    *bytes = plane_bytes(N, K);
+    return QK_OK;
+}
+
+extern "C" int qk_q4k_min_plane(const void *w, int64_t N, int64_t K, void *plane, size_t bytes, void *stream)
+{
+    if (N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || K > 0x7fffffffLL) return QK_E_SHAPE;
+    if (!w || !plane) return QK_E_NULL;
+    if (!qk::aligned(w, 16) || !qk::aligned(plane, 16)) return QK_E_ALIGN;
+    const size_t need = plane_bytes(N, K);
+    if (bytes < need) return QK_E_WORKSPACE;
+    size_t wbytes = 0;
+    qk_repacked_bytes(QK_TYPE_Q4_K, N, K, &wbytes);
+    if (qk::overlaps(plane, need, w, wbytes)) return QK_E_ALIAS;
+    const int B = (int)(K / 256);
+    const int64_t threads = N * ((B + 1) / 2), blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return QK_E_SHAPE;
+    const uint4 *meta = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(w) + (size_t)N * B * 128);
+    return qk::launch(q4k_min_plane_kernel, dim3((unsigned)blocks), dim3(256), 0, (cudaStream_t)stream, false, meta,
+                      N, B, static_cast<uint4 *>(plane));
+}
+
+extern "C" int qk_mmq_q4k_plane(const void *w, const void *plane, const int8_t *codes, const void *scales, int64_t M,
+                                int64_t N, int64_t K, const float *residual, float *y, void *workspace,
+                                size_t workspace_bytes, unsigned flags, void *stream)
+{
+    if (M > 0 && !plane) return QK_E_NULL;
+    return mmq(QK_TYPE_Q4_K, w, plane, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags,
+               stream);
 }
 
 extern "C" int qk_mmq_q6k(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N, int64_t K,
                           const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,
                           void *stream)
 {
-    return mmq(QK_TYPE_Q6_K, w, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags, stream);
+    return mmq(QK_TYPE_Q6_K, w, nullptr, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags,
+               stream);
 }

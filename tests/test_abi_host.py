@@ -159,6 +159,29 @@ def test_mmq_rejects(L, fn):
     assert f(w, c, s, 16, 64, 256, None, y, ws, need, 6, None) == E_SHAPE          # both tile widths forced
 
 
+def test_min_plane_size_and_rejects(L):
+    assert qk.q4k_min_plane_bytes(3584, 3584) == 3584 * 7 * 64
+    assert qk.q4k_min_plane_bytes(10, 256) == 10 * 64                   # one superblock: one record
+    assert qk.q4k_min_plane_bytes(10, 1280) == 10 * 3 * 64              # five: three records
+    w, pl, c, s, y, ws = (P + i * 0x10000000 for i in range(6))
+    need = qk.q4k_min_plane_bytes(64, 512)
+    f = L.qk_q4k_min_plane
+    assert f(w, 64, 320, pl, need, None) == E_SHAPE
+    assert f(w, 0, 512, pl, need, None) == E_SHAPE
+    assert f(None, 64, 512, pl, need, None) == E_NULL
+    assert f(w, 64, 512, None, need, None) == E_NULL
+    assert f(w, 64, 512, pl + 8, need, None) == E_ALIGN
+    assert f(w, 64, 512, pl, need - 1, None) == -6                     # QK_E_WORKSPACE
+    assert f(w, 64, 512, w, need, None) == E_ALIAS
+    g = L.qk_mmq_q4k_plane
+    wsn = qk.mmq_workspace_bytes(16, 64, 512)
+    assert g(w, pl, c, s, 0, 64, 512, None, y, None, 0, 0, None) == 0    # M = 0: nothing to do
+    assert g(w, None, c, s, 16, 64, 512, None, y, ws, wsn, 0, None) == E_NULL
+    assert g(w, pl + 4, c, s, 16, 64, 512, None, y, ws, wsn, 0, None) == E_ALIGN
+    assert g(w, y, c, s, 16, 64, 512, None, y, ws, wsn, 0, None) == E_ALIAS   # plane over y
+    assert g(w, ws, c, s, 16, 64, 512, None, y, ws, wsn, 0, None) == E_ALIAS  # plane over the workspace
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):
