@@ -92,12 +92,6 @@ CONFIGS = {
 NORM_EPS = 1e-5                                       # Llama-3 RMSNorm epsilon
 
 
-def mmq_base_workspace(M: int, K: int) -> int:
-    """Bytes of an MMQ workspace without the split-K scratch (include/qk.h, qk_mmq_workspace_bytes):
-    per 128-row M-tile a 16 KB activation block per 32 values of K and an 8 KB sums tile per 512."""
-    return -(-M // 128) * (K * 512 + -(-K // 512) * 8192)
-
-
 def weight_bytes(cfg) -> int:
     return sum(N * (K // 256) * BYTES_PER_SB[q] for (_, q, N, K, _, _) in cfg["gemms"])
 
@@ -213,8 +207,7 @@ class Workload:
     """Device buffers for one configuration: repacked weights (several copies),
     f32 activations and residuals, q8_1 buffers and outputs."""
 
-    def __init__(self, cfg_id: int, seed: int = 0, copies: int | None = None, device="cuda", mmq_split: str = "auto",
-                 mmq_plane: bool = False):
+    def __init__(self, cfg_id: int, seed: int = 0, copies: int | None = None, device="cuda", mmq_plane: bool = False):
         import quantized_q8_activation_gb300 as qk
         self.qk = qk
         self.cfg_id = cfg_id
@@ -248,7 +241,6 @@ class Workload:
         self.banks = [self._make_bank(device)]
         self.use_bank(0)
         self.ws = None
-        self.mmq_split = mmq_split
         # Q4_K MMQ with load-time min-operand planes (built here, with the weights, outside any timing)
         self.plane = [dict() for _ in range(copies)]
         if cfg["kind"] == "mmq" and mmq_plane:
@@ -257,12 +249,7 @@ class Workload:
                     for c in range(copies):
                         self.plane[c][name] = qk.q4k_min_plane(self.w[c][name], N, K)
         if cfg["kind"] == "mmq":
-            # qk_mmq_workspace_bytes includes the scratch of the split-K tail; a base-size workspace
-            # (mmq_split="off") runs every call unsplit
-            if mmq_split == "off":
-                need = max(mmq_base_workspace(M, K) for (_, _, _, K, _, _) in cfg["gemms"])
-            else:
-                need = max(qk.mmq_workspace_bytes(M, N, K) for (_, _, N, K, _, _) in cfg["gemms"])
+            need = max(qk.mmq_workspace_bytes(M, N, K) for (_, _, N, K, _, _) in cfg["gemms"])
             self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device) if need else None
         torch.cuda.synchronize()
 
@@ -324,8 +311,6 @@ class Workload:
             kw = dict(residual=self.r.get(name), y=self.y[name], pdl=pdl, stream=stream)
             if cfg["kind"] == "mmq":
                 ws = self.ws
-                if self.mmq_split == "off":                    # this GEMM's base size: no split scratch
-                    ws = ws[:mmq_base_workspace(self.M, K)]
                 plane = self.plane[copy].get(name)
                 if plane is not None:
                     qk.mmq_q4k_plane(self.w[copy][name], plane, codes, scales, N, K, workspace=ws, **kw)
@@ -709,8 +694,7 @@ def measure_config(cfg_id, args, stream, ws, device, peaks_meas=None, headline=F
     import quantized_q8_activation_gb300 as qk
     cfg = CONFIGS[cfg_id]
     front_end = args.front_end
-    wl = Workload(cfg_id, seed=0, copies=args.copies, mmq_split=args.mmq_split,
-                  mmq_plane=args.mmq_min_operands == "plane")
+    wl = Workload(cfg_id, seed=0, copies=args.copies, mmq_plane=args.mmq_min_operands == "plane")
     C, K = wl.copies, args.steps
     S = steps_per_replay(K, args.graph_steps)
     units = int_ops(cfg) if cfg["kind"] == "mmq" else weight_bytes(cfg)
@@ -751,7 +735,7 @@ def measure_config(cfg_id, args, stream, ws, device, peaks_meas=None, headline=F
     if unit == "GB/s":
         out["hbm_frac"] = (out["value"] / ws) / peaks()[0]
     if cfg["kind"] == "mmq":
-        out["mmq"] = {"split_k": args.mmq_split,
+        out["mmq"] = {"tile_width": "chosen per GEMM by the library (128, 192 or 256)", "split_k": "off",
                       "min_operands": "load-time plane (qk_q4k_min_plane)" if args.mmq_min_operands == "plane"
                       else "built in every tile from the 6-bit fields"}
 
@@ -1023,9 +1007,6 @@ def main():
                     help="prefill Q4_K MMQ: read the min-term operands from load-time planes built with the weights "
                          "(qk_q4k_min_plane, default; measured 1.8 %% faster per step) or build them from the 6-bit "
                          "fields in every tile")
-    ap.add_argument("--mmq-split", choices=["auto", "off"], default="auto",
-                    help="prefill MMQ workspace: with the split-K scratch (the library splits a tile's K range "
-                         "where its waves over the SMs are poorly filled) or the base size only (no split)")
     ap.add_argument("--front-end", choices=["batched", "auto", "fused", "unfused"], default="batched",
                     help="decode activation path: one quantize kernel over all of the step's f32 "
                          "activations, then q8_1 GEMVs (batched, default); q8_1 quantization inside each "

@@ -68,15 +68,26 @@ extern "C" {
  * launch, before the first PDL launch that reads its output).  Without the
  * flag every call is ordinary stream-ordered work.
  *
- * QK_MMQ_TILE_256 / QK_MMQ_TILE_128 (MMQ only): force output tiles 256 or
- * 128 weight rows wide.  By default the MMQ picks per call the width whose
- * waves of tiles over the SMs should finish first, counting a 128-wide tile
- * as 0.7 of a 256-wide one (in practice: 128 for problems that fit in one
- * wave, 256 otherwise).  Results are the same within the stated bound either
- * way; the flags exist for tests and tuning.  Setting both is QK_E_SHAPE.
+ * QK_MMQ_TILE_256 / QK_MMQ_TILE_192 / QK_MMQ_TILE_128 (MMQ only): force
+ * output tiles 256, 192 (Q4_K only) or 128 weight rows wide.  By default the
+ * MMQ picks per call the width whose waves of tiles over the SMs should
+ * finish first, from a per-width model of a tile's time (a fixed part and a
+ * part per 32-value K stage, measured on the prefill shapes): in practice
+ * 128 for problems that fit in one wave, 192 for short K where 256-wide tiles
+ * leave a second wave half empty, 256 otherwise.  Results are the same
+ * within the stated bound either way; the flags exist for tests and tuning.
+ * Setting more than one, or QK_MMQ_TILE_192 for Q6_K, is QK_E_SHAPE.
+ *
+ * QK_MMQ_SPLIT_K (Q4_K MMQ only): split each output tile's K range over two
+ * work units, the second to finish adding the two partial tiles (binary32,
+ * the same bits either way).  Taken only when K has at least 48 superblocks
+ * and the workspace also holds the split scratch (see qk_mmq_q4k); otherwise
+ * ignored.  Off by default: on the prefill shapes it measured slower.
  */
 #define QK_MMQ_TILE_256 2u
 #define QK_MMQ_TILE_128 4u
+#define QK_MMQ_TILE_192 8u
+#define QK_MMQ_SPLIT_K 16u
 
 /* Library version (major*10000 + minor*100 + patch). */
 int qk_version(void);
@@ -382,15 +393,13 @@ int qk_gemv_q3k_f32(const void *w, const float *x, int64_t ldx,
  *   this call that run after the call returns, so the workspace must not be
  *   reused by work that is not ordered after this call on `stream`.  Size:
  *   at least the base ceil(M/128) * (K * 512 + ceil(K/512) * 8192) bytes
- *   (M = 2048, K = 18944: 160,038,912 bytes).  qk_mmq_workspace_bytes adds,
- *   on the current device, the scratch of a split of each output tile's K
- *   range over two work units, which the Q4_K MMQ takes when its tiles fill
- *   the SMs' last wave poorly and K is long (at least 48 superblocks, so that
- *   each unit has 24; Qwen2-7B down: 224 tiles on 152 SMs, K = 18944); the
- *   two partial tiles are added in binary32 by the second unit to finish
- *   (the same bits either way).  Where no split is taken it adds nothing.  A workspace of at least the base size
- *   but below qk_mmq_workspace_bytes runs the call unsplit; the two forms
- *   differ only in rounding, within the same bound, and each is reproducible.
+ *   (M = 2048, K = 18944: 160,038,912 bytes); qk_mmq_workspace_bytes
+ *   returns it.  A call with QK_MMQ_SPLIT_K (Q4_K) splits only if the
+ *   workspace also holds the split scratch after the base size: 512 * BN
+ *   bytes of partial tile per work unit and 4 bytes per tile, BN the tile
+ *   width the call picks (M = 2048, N = 3584 at 256: 224 tiles, 58,721,152
+ *   bytes); with less it runs unsplit.  Split and unsplit results differ
+ *   only in rounding, within the same bound, and each is reproducible.
  * Returns QK_E_WORKSPACE if workspace_bytes is below the base size.
  */
 int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);

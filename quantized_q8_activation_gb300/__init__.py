@@ -40,6 +40,8 @@ Q3_K = 6
 LAUNCH_PDL = 1
 MMQ_TILE_256 = 2
 MMQ_TILE_128 = 4
+MMQ_TILE_192 = 8
+MMQ_SPLIT_K = 16
 
 ERR_TIMEOUT = 1     # error_flags(): a bounded in-kernel wait gave up
 ERR_RANGE = 2       # error_flags(): an MMQ input was outside the value limits (see include/qk.h)
@@ -371,11 +373,13 @@ def gemv_q3k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=N
                      pdl, stream)
 
 
-def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None, tile=None):
+def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None, tile=None,
+            split_k=False):
     """Prefill contraction over a repacked Q4_K weight, any M.  tile: None (the library picks
-    the tile width), 256 or 128.  workspace: a uint8 CUDA tensor of at least
+    the tile width), 256, 192 or 128.  split_k: QK_MMQ_SPLIT_K (taken only if the workspace also
+    holds the split scratch, include/qk.h).  workspace: a uint8 CUDA tensor of at least
     mmq_workspace_bytes(M, N, K) bytes; when None, this wrapper allocates one with torch."""
-    return _mmq("qk_mmq_q4k", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile)
+    return _mmq("qk_mmq_q4k", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile, split_k=split_k)
 
 
 def mmq_q6k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None, tile=None):
@@ -406,14 +410,15 @@ def q4k_min_plane(w, N, K, plane=None, stream=None):
 
 
 def mmq_q4k_plane(w, plane, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None,
-                  tile=None):
+                  tile=None, split_k=False):
     """mmq_q4k reading the min operands from a plane made by q4k_min_plane from the same weight
     (same result bit for bit; workspace as for mmq_q4k)."""
     _cuda(plane, "plane")
-    return _mmq("qk_mmq_q4k_plane", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile, plane)
+    return _mmq("qk_mmq_q4k_plane", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile, plane,
+                split_k)
 
 
-def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile=None, plane=None):
+def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile=None, plane=None, split_k=False):
     M = codes.shape[0]
     for t, n in ((w, "w"), (codes, "codes"), (scales, "scales")):
         _cuda(t, n)
@@ -423,7 +428,8 @@ def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile=N
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=codes.device)
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    flags = (LAUNCH_PDL if pdl else 0) | {None: 0, 256: MMQ_TILE_256, 128: MMQ_TILE_128}[tile]
+    flags = (LAUNCH_PDL if pdl else 0) | {None: 0, 256: MMQ_TILE_256, 192: MMQ_TILE_192, 128: MMQ_TILE_128}[tile]
+    flags |= MMQ_SPLIT_K if split_k else 0
     args = (codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(), _p(workspace), wsb, flags,
             _stream(stream))
     with _on(codes):

@@ -146,6 +146,11 @@ __host__ __device__ constexpr uint32_t sw32(int r, int c) { return r * 32 + ((c 
 
 __device__ __forceinline__ void wait_bar(uint64_t *bar, uint32_t parity) { mbar_wait(bar, parity, &g_qk_errors); }
 
+// named barriers kStageBar0 + stage slot, 64 threads: the sync warp (warp 3) arrives, the MMA warp syncs
+constexpr int kStageBar0 = 2;
+__device__ __forceinline__ void stage_arrive(int id) { asm volatile("bar.arrive %0, 64;" ::"r"(id) : "memory"); }
+__device__ __forceinline__ void stage_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
@@ -429,6 +434,7 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
 {
     using L = Plan<QT, BN_>;
     constexpr int BN = L::BN;
+    static_assert(kStageBar0 + NST <= 16, "a named barrier per stage slot");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
@@ -461,17 +467,16 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t sbase = smem_u32(smem);
-            int kt = 0;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
-                const int acc = kt & 1;
-                if (kt >= 2) wait_bar(&bar[B_ACCEMPTY + acc], ((kt >> 1) + 1) & 1);
-                fence_after_sync();
-                const uint32_t dacc = tmem + acc * BN;
-                for (int it = 0; it < nit; it++) {
-                    const int gs = kt * nit + it, st = gs % NST;
-                    wait_bar(&bar[B_FULL + st], (gs / NST) & 1);
+        // the warp takes each stage from the sync warp (warp 3) through a named barrier; lane 0 issues
+        const uint32_t sbase = smem_u32(smem);
+        int kt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
+            const int acc = kt & 1;
+            const uint32_t dacc = tmem + acc * BN;
+            for (int it = 0; it < nit; it++) {
+                const int gs = kt * nit + it, st = gs % NST;
+                stage_sync(kStageBar0 + st);
+                if (lane == 0) {
                     fence_after_sync();
                     const uint32_t s0 = sbase + st * L::STAGE;
 #pragma unroll
@@ -485,14 +490,31 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
                         mma_f16(dacc, alo, whi, L::IDESC, 1);
                     }
                     mma_commit(&bar[B_EMPTY + st]);
+                    if (it == nit - 1) mma_commit(&bar[B_ACCFULL + acc]);
                 }
-                mma_commit(&bar[B_ACCFULL + acc]);
+                __syncwarp();
             }
-            // teardown: no MMA may still be running when the TMEM is released
+        }
+        // teardown: no MMA may still be running when the TMEM is released
+        if (lane == 0) {
             mma_commit(&bar[B_DONE]);
             wait_bar(&bar[B_DONE], 0);
         }
         __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ sync warp
+        // per stage: wait (bounded) for its operands and, at a tile's first stage, for the accumulator
+        // buffer; then hand the stage to the MMA warp (it arrives even after a wait gave up)
+        int kt = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, kt++) {
+            const int acc = kt & 1;
+            if (kt >= 2) wait_bar(&bar[B_ACCEMPTY + acc], ((kt >> 1) + 1) & 1);
+            for (int it = 0; it < nit; it++) {
+                const int gs = kt * nit + it, st = gs % NST;
+                wait_bar(&bar[B_FULL + st], (gs / NST) & 1);
+                stage_arrive(kStageBar0 + st);
+            }
+        }
     } else if (warp == 1) {
         // ------------------------------------------------ activation block copier
         // one bulk copy per K stage of the stage's 16 KB activation block, issued as soon as the
@@ -640,22 +662,28 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
 // sub-blocks; its accumulator seeds the register tile.
 // Warps: 0 MMA, 1 activation copier, 2 TMA producer, 3 idle, 4-11 epilogue
 // (TMEM lane quadrant warp % 4, column half (warp - 4) / 4), 12.. converters
-// (one thread per weight row).  With 256-wide tiles the epilogue warps hold
-// 128 accumulator columns each and take registers from the other warps
-// (setmaxnreg); the split adds up to the launch's 640 x 96.
+// (one thread per weight row).  With 256- and 192-wide tiles the epilogue warps
+// hold 128 or 96 accumulator columns each and take registers from the other
+// warps (setmaxnreg); the split stays within the launch's registers (640 x 96
+// or 576 x 96).  BN = 192 keeps two 192-column accumulators in a
+// 512-column tensor-memory allocation.
 template <int BN_>
 struct Plan4 {
     static constexpr int BN = BN_;
     static constexpr int kEpiW0 = 4, kEpiW = 8, kConvW0 = 12, kConvW = BN / 32;
-    static constexpr int kThreads = (kConvW0 + kConvW) * 32;
+    // setmaxnreg acts on whole warpgroups (4 warps), so the launch rounds the converter warps up to a
+    // multiple of 4; the extra warps (BN = 192: two) only give their registers back and wait at the end
+    static constexpr int kConvWL = (kConvW + 3) / 4 * 4;
+    static constexpr int kThreads = (kConvW0 + kConvWL) * 32;
     static constexpr int CPT = BN / 2;                     // output columns per epilogue thread
     static constexpr int WTILE = BN * 64;                  // BN rows x 32 f16
     static constexpr int STAGE = 2 * ATILE + WTILE;        // A_hi | A_lo (or the sums tile) | W' (or Mw)
     // raw unit: half a superblock's code bytes, first 16-byte halves of its 2 groups | second halves
     static constexpr int RAW_H1 = BN * 32, RAW = 2 * BN * 32;
     static constexpr int SBR = BN * 16;
-    static constexpr int NST = BN == 256 ? 4 : 6, NRAW = 3, NSB = 4, ND = 4;
-    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static_assert(BN == 128 || BN == 192 || BN == 256, "tile widths 128, 192, 256");
+    static constexpr int NST = BN == 128 ? 6 : 4, NRAW = 3, NSB = 4, ND = 4;
+    static constexpr uint32_t TMEM_COLS = BN == 128 ? 256 : 512;   // a power of two holding both accumulators
     static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
     static constexpr int OFF_RAW = NST * STAGE;
     static constexpr int OFF_SBR = OFF_RAW + NRAW * RAW;
@@ -678,7 +706,7 @@ struct Plan4 {
     };
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_TMEM + 16 + 1024;
-    static constexpr bool kSplitRegs = BN == 256;
+    static constexpr bool kSplitRegs = BN >= 192;
 #ifndef QK_MMQ4_RMISC
 #define QK_MMQ4_RMISC 48
 #endif
@@ -688,13 +716,20 @@ struct Plan4 {
 #ifndef QK_MMQ4_RCONV
 #define QK_MMQ4_RCONV 48
 #endif
-    // registers per thread: at launch, then warps 0-3, epilogue warps, converters
-    static constexpr int kRegLaunch = 96, kRegMisc = QK_MMQ4_RMISC, kRegEpi = QK_MMQ4_REPI, kRegConv = QK_MMQ4_RCONV;
+    // registers per thread: the least a launch may have (the split's total over the threads, rounded up to
+    // the allocation unit of 8), then warps 0-3, epilogue warps, converters
+    static constexpr int kRegMisc = QK_MMQ4_RMISC, kRegConv = QK_MMQ4_RCONV;
+    static constexpr int kRegEpi = QK_MMQ4_REPI;
+    static constexpr int kRegLaunch =
+        ((4 * kRegMisc + kEpiW * kRegEpi + kConvWL * kRegConv) * 32 / kThreads + 7) / 8 * 8;
     static_assert(SMEM <= 232448, "shared memory plan exceeds the per-block opt-in limit");
     static_assert(STAGE % 1024 == 0 && OFF_RAW % 1024 == 0 && RAW % 1024 == 0 && OFF_SBR % 1024 == 0,
                   "copy destinations and swizzle atoms stay aligned");
-    static_assert(!kSplitRegs || (4 * kRegMisc + kEpiW * kRegEpi + kConvW * kRegConv) * 32 <= kThreads * kRegLaunch,
+    static_assert(!kSplitRegs || (4 * kRegMisc + kEpiW * kRegEpi + kConvWL * kRegConv) * 32 <= kThreads * kRegLaunch,
                   "the register split must fit in the launch's registers");
+    static_assert(kThreads % 128 == 0 && kEpiW0 % 4 == 0 && kEpiW % 4 == 0 && kConvW0 % 4 == 0,
+                  "every setmaxnreg warpgroup is whole");
+    static_assert(!kSplitRegs || kRegLaunch * kThreads <= 65536, "the launch's registers fit one SM");
 };
 
 template <int N> __device__ __forceinline__ void reg_alloc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
@@ -708,14 +743,23 @@ __device__ __forceinline__ uint32_t q4_group(const uint4 &mt, int g)
                        g == 0 ? 0x3210u : g == 1 ? 0x3210u : g == 2 ? 0x3410u : 0x3765u);
 }
 
-// 4 nibbles (one per byte of x, masked to 0..15) times the sub-block scale sc (< 64) as two f16
-// pairs, exactly: each product (< 1024) sits in a 16-bit lane of 0x6400 + sc q, the f16 1024 + sc q,
-// and 1024 is subtracted
-__device__ __forceinline__ void w_sc(uint32_t x, uint32_t sc, uint32_t &p01, uint32_t &p23)
+// the f16 pairs (sc, sc) and (-1024 sc, -1024 sc) of a sub-block scale sc < 64 (both exact)
+struct ScPair {
+    __half2 s, n;
+};
+__device__ __forceinline__ ScPair sc_pair(uint32_t sc)
 {
-    const __half2 k1024 = u2h(0x64006400u);
-    p01 = h2u(__hsub2(u2h(__byte_perm(x, 0u, 0x4140u) * sc + 0x64006400u), k1024));
-    p23 = h2u(__hsub2(u2h(__byte_perm(x, 0u, 0x4342u) * sc + 0x64006400u), k1024));
+    const __half2 s2 = __half2half2(__ushort2half_rn((unsigned short)sc));
+    return ScPair{s2, __hmul2(s2, u2h(0xE400E400u))};              // x (-1024), exact
+}
+
+// 4 nibbles (one per byte of x, masked to 0..15) times the sub-block scale sc as two f16 pairs,
+// exactly: each byte goes to a 16-bit lane under 0x64 (the f16 1024 + q), and one fused multiply-add
+// gives (1024 + q) sc - 1024 sc = sc q, an integer below 1024 that the single rounding leaves exact
+__device__ __forceinline__ void w_sc(uint32_t x, const ScPair &k, uint32_t &p01, uint32_t &p23)
+{
+    p01 = h2u(__hfma2(u2h(__byte_perm(x, 0x64646464u, 0x4140u)), k.s, k.n));
+    p23 = h2u(__hfma2(u2h(__byte_perm(x, 0x64646464u, 0x4342u)), k.s, k.n));
 }
 
 // the 8 min products Mw' = 1024 dmin m_j of one superblock record as f16 pairs hi (11 significant
@@ -773,12 +817,14 @@ __device__ __forceinline__ int seg_hi(const MmqArgs &a, int seg, int B) { return
 template <int NW>
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory"); }
 
+
 template <int BN_, bool PL>
 __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
     mmq_q4k_kernel(const MmqArgs a, const __grid_constant__ MmqMaps maps)
 {
     using L = Plan4<BN_>;
     constexpr int BN = L::BN, NS = L::NST, NR = L::NRAW, NB = L::NSB, ND = L::ND;
+    static_assert(kStageBar0 + NS <= 16, "a named barrier per stage slot");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
@@ -814,22 +860,23 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
     if constexpr (L::kSplitRegs) reg_dealloc<L::kRegMisc>();
     if (warp == 0) {
         // ------------------------------------------------------------ MMA issuer
-        // accumulator events in order: per tile the min term, then one per superblock
-        if (lane == 0) {
-            const uint32_t sbase = smem_u32(smem);
-            int gs = 0, ge = 0;
-            for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-                const int seg = u % S, nsb = seg_hi(a, seg, B) - seg_lo(a, seg);
-                // events: the min term (segment 0 only), then one per superblock of the segment
-                for (int ev = seg == 0 ? 0 : 1; ev <= nsb; ev++, ge++) {
-                    const int acc = ge & 1;
-                    if (ge >= 2) wait_bar(&bar[L::ACCEMPTY + acc], ((ge >> 1) + 1) & 1);
-                    fence_after_sync();
-                    const uint32_t dacc = tmem + acc * BN;
-                    const int nst = ev == 0 ? nmin : 8;
-                    for (int i = 0; i < nst; i++, gs++) {
-                        const int st = gs % NS;
-                        wait_bar(&bar[L::FULL + st], (gs / NS) & 1);
+        // accumulator events in order: per tile the min term, then one per superblock.  The warp takes
+        // each stage from the sync warp (warp 3) through a named barrier and lane 0 issues its MMAs: the
+        // issuing thread never polls shared memory between MMAs (a poll there leaves the tensor pipe
+        // idle for about 150 ns a stage)
+        const uint32_t sbase = smem_u32(smem);
+        int gs = 0, ge = 0;
+        for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+            const int seg = u % S, nsb = seg_hi(a, seg, B) - seg_lo(a, seg);
+            // events: the min term (segment 0 only), then one per superblock of the segment
+            for (int ev = seg == 0 ? 0 : 1; ev <= nsb; ev++, ge++) {
+                const int acc = ge & 1;
+                const uint32_t dacc = tmem + acc * BN;
+                const int nst = ev == 0 ? nmin : 8;
+                for (int i = 0; i < nst; i++, gs++) {
+                    const int st = gs % NS;
+                    stage_sync(kStageBar0 + st);
+                    if (lane == 0) {
                         fence_after_sync();
                         const uint32_t s0 = sbase + st * L::STAGE, w0 = s0 + 2 * ATILE;
                         if (ev == 0) {
@@ -851,15 +898,38 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                             }
                         }
                         mma_commit(&bar[L::EMPTY + st]);
+                        if (i == nst - 1) mma_commit(&bar[L::ACCFULL + acc]);
                     }
-                    mma_commit(&bar[L::ACCFULL + acc]);
+                    __syncwarp();
                 }
             }
-            // teardown: no MMA may still be running when the TMEM is released
+        }
+        // teardown: no MMA may still be running when the TMEM is released
+        if (lane == 0) {
             mma_commit(&bar[L::DONE]);
             wait_bar(&bar[L::DONE], 0);
         }
         __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ sync warp
+        // the issuer's loop again: per stage, wait (bounded) for its operands and, at the first stage of
+        // an event, for the accumulator buffer, then hand the stage to the MMA warp.  It arrives for every
+        // stage even after a wait gave up, so the issuer's barrier always completes.  A stage barrier is
+        // reused only after the issuer has passed it: the stage's next operands need its MMAs' commit.
+        int gs = 0, ge = 0;
+        for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+            const int seg = u % S, nsb = seg_hi(a, seg, B) - seg_lo(a, seg);
+            for (int ev = seg == 0 ? 0 : 1; ev <= nsb; ev++, ge++) {
+                const int acc = ge & 1;
+                if (ge >= 2) wait_bar(&bar[L::ACCEMPTY + acc], ((ge >> 1) + 1) & 1);
+                const int nst = ev == 0 ? nmin : 8;
+                for (int i = 0; i < nst; i++, gs++) {
+                    const int st = gs % NS;
+                    wait_bar(&bar[L::FULL + st], (gs / NS) & 1);
+                    stage_arrive(kStageBar0 + st);
+                }
+            }
+        }
     } else if (warp == 1) {
         // ------------------------------------------------ activation block copier
         // per tile the sums tiles of its min stages (8 KB each), then the A blocks (16 KB)
@@ -1046,7 +1116,9 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
             }
         }
     } else {
+        // one setmaxnreg for the whole warpgroup, the padding warps (no rows) included
         if constexpr (L::kSplitRegs) reg_dealloc<L::kRegConv>();
+        if (warp < L::kConvW0 + L::kConvW) {
         // --------------------------------------------------------- converters
         // one thread per weight row; a quarter warp stores 8 consecutive rows, which the 64-byte
         // swizzle spreads over all 32 banks
@@ -1118,49 +1190,48 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                 dring[ds * BN + row] = __half2float(__ushort_as_half((unsigned short)(mt.x & 0xffffu)));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[L::DFULL + ds]);
-                // raw unit hs = j / 4 holds groups 2hs, 2hs+1; its tiles arrive 32-byte swizzled (16-byte
-                // chunk c of row r at sw32(r, c)), so that a quarter warp's 8 rows read distinct banks
-                uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+                // sub-blocks 2g and 2g+1 (the low and high nibbles of group g's code bytes) are converted
+                // together: one proxy fence and one warp handoff for both stages
                 int rs = 0;
 #pragma unroll
-                for (int j = 0; j < 8; j++, gs++) {
-                    const int g = j >> 1, nib = j & 1, st = gs % NS;
-                    if ((j & 3) == 0) {
+                for (int g = 0; g < 4; g++, gs += 2) {
+                    const int st0 = gs % NS, st1 = (gs + 1) % NS;
+                    if ((g & 1) == 0) {
                         rs = gu % NR;
                         wait_bar(&bar[L::RFULL + rs], (gu / NR) & 1);
                     }
-                    if (nib == 0) {
-                        const uint8_t *raw = smem + L::OFF_RAW + rs * L::RAW;
-                        c0 = *reinterpret_cast<const uint4 *>(raw + sw32(row, g & 1));
-                        c1 = *reinterpret_cast<const uint4 *>(raw + L::RAW_H1 + sw32(row, g & 1));
-                    }
+                    const uint8_t *raw = smem + L::OFF_RAW + rs * L::RAW;
+                    const uint4 c0 = *reinterpret_cast<const uint4 *>(raw + sw32(row, g & 1));
+                    const uint4 c1 = *reinterpret_cast<const uint4 *>(raw + L::RAW_H1 + sw32(row, g & 1));
                     const uint32_t rec = q4_group(mt, g);
-                    const uint32_t sc = nib ? (rec >> 6) & 63u : rec & 63u;
-                    if (gs >= NS) wait_bar(&bar[L::EMPTY + st], ((gs / NS) + 1) & 1);
-                    uint8_t *w0 = smem + st * L::STAGE + 2 * ATILE;
+                    const ScPair k0 = sc_pair(rec & 63u), k1 = sc_pair((rec >> 6) & 63u);
+                    if (gs >= NS) wait_bar(&bar[L::EMPTY + st0], ((gs / NS) + 1) & 1);
+                    if (gs + 1 >= NS) wait_bar(&bar[L::EMPTY + st1], (((gs + 1) / NS) + 1) & 1);
+                    uint8_t *w0 = smem + st0 * L::STAGE + 2 * ATILE;
+                    uint8_t *w1 = smem + st1 * L::STAGE + 2 * ATILE;
                     const uint32_t x[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
                     for (int cc = 0; cc < 4; cc++) {
-                        const uint32_t xa = (nib ? x[2 * cc] >> 4 : x[2 * cc]) & 0x0F0F0F0Fu;
-                        const uint32_t xb = (nib ? x[2 * cc + 1] >> 4 : x[2 * cc + 1]) & 0x0F0F0F0Fu;
                         uint32_t p0, p1, p2, p3;
-                        w_sc(xa, sc, p0, p1);
-                        w_sc(xb, sc, p2, p3);
+                        w_sc(x[2 * cc] & 0x0F0F0F0Fu, k0, p0, p1);
+                        w_sc(x[2 * cc + 1] & 0x0F0F0F0Fu, k0, p2, p3);
                         sts128(w0, sw64(row, cc), p0, p1, p2, p3);
+                        w_sc((x[2 * cc] >> 4) & 0x0F0F0F0Fu, k1, p0, p1);
+                        w_sc((x[2 * cc + 1] >> 4) & 0x0F0F0F0Fu, k1, p2, p3);
+                        sts128(w1, sw64(row, cc), p0, p1, p2, p3);
                     }
-                    // each lane makes its stores visible to the tensor core (async proxy), then one lane
-                    // arrives for the warp; a raw slot is released only after the values read from it
-                    // have been consumed above
                     fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) {
-                        if ((j & 3) == 2) mbar_arrive(&bar[L::REMPTY + rs]);   // last read of this raw unit
-                        if (j == 0) mbar_arrive(&bar[L::SEMPTY + ss]);
-                        mbar_arrive(&bar[L::FULL + st]);
+                        if (g & 1) mbar_arrive(&bar[L::REMPTY + rs]);        // last read of this raw unit
+                        if (g == 0) mbar_arrive(&bar[L::SEMPTY + ss]);
+                        mbar_arrive(&bar[L::FULL + st0]);
+                        mbar_arrive(&bar[L::FULL + st1]);
                     }
-                    if ((j & 3) == 3) gu++;
+                    if (g & 1) gu++;
                 }
             }
+        }
         }
     }
 
@@ -1220,25 +1291,9 @@ size_t ws_bytes(int64_t M, int64_t K)
     return ws_a_bytes(M, K) + mt * (size_t)((K / 256 + 1) / 2) * SBLK;
 }
 
-// Split of each tile's K range over `split` work units (Q4_K, at most two): taken when it shortens the
-// schedule of waves of units over the SMs by more than the partial-tile traffic costs (3 %), and only
-// for long segments (kMinSegSb superblocks or more each): every unit ends with an epilogue that
-// writes its partial tile and the second one reads it back, which on short segments costs more than
-// the shorter schedule saves (measured: K = 3584, 7 superblocks a segment, 224 tiles on 152 SMs ran
-// slower split; K = 18944, 35 and 39 superblocks, ran 7 % faster split).  Segment 0 covers superblocks
-// [0, mid) and the min term, segment 1 [mid, K/256).
+// Split of each tile's K range over two work units (Q4_K, QK_MMQ_SPLIT_K): each unit needs kMinSegSb
+// superblocks or more.  Segment 0 covers superblocks [0, mid) and the min term, segment 1 [mid, K/256).
 constexpr int kMinSegSb = 24;
-int pick_split(int64_t tiles, int B, int sms)
-{
-    double best = (double)((tiles + sms - 1) / sms);
-    int bs = 1;
-    for (int S = 2; S <= kMaxSplit; S++) {
-        if (B < kMinSegSb * S) break;
-        const double c = (double)((tiles * S + sms - 1) / sms) / S * (1.0 + 0.03 * (S - 1));
-        if (c < best - 1e-9) best = c, bs = S;
-    }
-    return bs;
-}
 
 // first superblock of segment 1: the two segments' MMA work balanced, segment 0 also carrying the min term
 int split_mid(int B)
@@ -1254,15 +1309,38 @@ struct Q4Plan {
     int64_t tiles;
 };
 
-int pick_bn(int64_t M, int64_t N, int sms);
-
-Q4Plan q4_plan(int64_t M, int64_t N, int64_t K, unsigned flags, int sms)
+// Time of one work unit: a fixed part (the tile's pipeline start and its output) and a part per K
+// stage, measured per tile width on the Qwen2-7B prefill GEMMs (K = 3584 and 18944, split-scale kernel
+// with the sync warp and the min-operand plane): 256: 40 us + 0.43 us a stage, 192: 26 + 0.48,
+// 128: 14 + 0.424.  A split unit adds 39 us (its partial tile out and back, the second pipeline start).
+double unit_us(int BN, int64_t stages, int split)
 {
-    Q4Plan p;
-    p.BN = (flags & QK_MMQ_TILE_256) ? 256 : (flags & QK_MMQ_TILE_128) ? 128 : pick_bn(M, N, sms);
-    p.tiles = ((M + BM - 1) / BM) * ((N + p.BN - 1) / p.BN);
-    p.split = pick_split(p.tiles, (int)(K / 256), sms);
-    return p;
+    const double a = BN == 256 ? 40.0 : BN == 192 ? 26.0 : 14.0, b = BN == 256 ? 0.43 : BN == 192 ? 0.48 : 0.424;
+    return a + b * (double)stages + (split > 1 ? 39.0 : 0.0);
+}
+
+// The width whose waves of tiles over the SMs should finish first (a forced width, QK_MMQ_TILE_*,
+// is taken as it is).  The K range of each tile is split in two only on request (QK_MMQ_SPLIT_K) and
+// for K of at least 2 kMinSegSb superblocks: on the benchmark shapes the model above puts a split
+// behind the unsplit tile (measured: K = 18944, 224 tiles of 256: 642 us split, 620 unsplit).
+Q4Plan q4_plan(int64_t M, int64_t N, int64_t K, unsigned flags, int sms, int max_split = kMaxSplit)
+{
+    if (sms < 1) sms = 1;
+    const int forced = (flags & QK_MMQ_TILE_256) ? 256 : (flags & QK_MMQ_TILE_192) ? 192
+                     : (flags & QK_MMQ_TILE_128) ? 128 : 0;
+    const int widths[3] = {256, 192, 128};
+    const int64_t gx = (M + BM - 1) / BM, B = K / 256, stages = 8 * B + (B + 1) / 2;
+    Q4Plan best{256, 1, gx * ((N + 255) / 256)};
+    double bc = 1e300;
+    for (int wi = 0; wi < 3; wi++) {
+        const int BN = widths[wi];
+        if (forced && BN != forced) continue;
+        const int64_t tiles = gx * ((N + BN - 1) / BN);
+        const double c = (double)((tiles + sms - 1) / sms) * unit_us(BN, stages, 1);
+        if (c < bc * (1.0 - 1e-9)) bc = c, best = Q4Plan{BN, 1, tiles};
+    }
+    if ((flags & QK_MMQ_SPLIT_K) && max_split >= 2 && B >= 2 * kMinSegSb) best.split = 2;
+    return best;
 }
 
 // scratch of a split call after the base workspace: the partial tiles, then the tile counters
@@ -1272,7 +1350,7 @@ size_t split_bytes(const Q4Plan &p)
     return (size_t)p.tiles * p.split * BM * p.BN * 4 + (size_t)p.tiles * 4;
 }
 
-// The register-split kernel must be launched with exactly the registers its setmaxnreg split hands
+// The register-split kernel must be launched with at least the registers its setmaxnreg split hands
 // out: with fewer, the epilogue warps' increase could never be granted.  Checked once per kernel,
 // before its first launch.
 template <int BN, bool PL>
@@ -1289,7 +1367,7 @@ int set_attrs_q4()
         return QK_E_CUDA;
     if (Plan4<BN>::kSplitRegs) {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, mmq_q4k_kernel<BN, PL>) != cudaSuccess || fa.numRegs != Plan4<BN>::kRegLaunch)
+        if (cudaFuncGetAttributes(&fa, mmq_q4k_kernel<BN, PL>) != cudaSuccess || fa.numRegs < Plan4<BN>::kRegLaunch)
             return QK_E_CUDA;
     }
     done.store(1);
@@ -1361,10 +1439,19 @@ int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const voi
         return QK_E_ALIGN;
     const size_t need = ws_bytes(M, K);
     if (workspace_bytes < need) return QK_E_WORKSPACE;
-    if ((flags & QK_MMQ_TILE_256) && (flags & QK_MMQ_TILE_128)) return QK_E_SHAPE;
+    const unsigned tf = flags & (QK_MMQ_TILE_256 | QK_MMQ_TILE_192 | QK_MMQ_TILE_128);
+    if (tf & (tf - 1)) return QK_E_SHAPE;                               // more than one width forced
     const int sms = qk::sm_count();
-    Q4Plan plan = q4_plan(M, N, K, flags, sms);
-    if (qt == QK_TYPE_Q6_K || workspace_bytes < need + split_bytes(plan)) plan.split = 1;   // no scratch: no split
+    Q4Plan plan;
+    if (qt == QK_TYPE_Q6_K) {
+        if (tf == QK_MMQ_TILE_192) return QK_E_SHAPE;                   // Q6_K tiles are 128 or 256 wide
+        plan.BN = tf == QK_MMQ_TILE_256 ? 256 : tf == QK_MMQ_TILE_128 ? 128 : pick_bn(M, N, sms);
+        plan.split = 1;
+        plan.tiles = ((M + BM - 1) / BM) * ((N + plan.BN - 1) / plan.BN);
+    } else {
+        plan = q4_plan(M, N, K, flags, sms);
+        if (workspace_bytes < need + split_bytes(plan)) plan = q4_plan(M, N, K, flags, sms, 1);  // no scratch
+    }
     const size_t used = need + split_bytes(plan);                     // the workspace bytes this call writes
     size_t wbytes = 0;
     qk_repacked_bytes(qt, N, K, &wbytes);
@@ -1413,8 +1500,10 @@ int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const voi
     cudaStream_t cs = (cudaStream_t)stream;
     if (!q6) {
         // validate the main kernel's launch configuration before anything is launched
-        const int sa = plane ? (BN == 128 ? set_attrs_q4<128, true>() : set_attrs_q4<256, true>())
-                             : (BN == 128 ? set_attrs_q4<128, false>() : set_attrs_q4<256, false>());
+        const int sa = plane ? (BN == 128 ? set_attrs_q4<128, true>() : BN == 192 ? set_attrs_q4<192, true>()
+                                                                       : set_attrs_q4<256, true>())
+                             : (BN == 128 ? set_attrs_q4<128, false>() : BN == 192 ? set_attrs_q4<192, false>()
+                                                                       : set_attrs_q4<256, false>());
         if (sa != QK_OK) return sa;
     }
     float *part = nullptr;
@@ -1446,8 +1535,12 @@ int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const voi
                              : launch_mmq<QK_TYPE_Q6_K, 256>(args, maps, tiles, cs);
     const int64_t units = tiles * plan.split;
     if (plane)
-        return BN == 128 ? launch_mmq_q4<128, true>(args, maps, units, cs) : launch_mmq_q4<256, true>(args, maps, units, cs);
-    return BN == 128 ? launch_mmq_q4<128, false>(args, maps, units, cs) : launch_mmq_q4<256, false>(args, maps, units, cs);
+        return BN == 128   ? launch_mmq_q4<128, true>(args, maps, units, cs)
+               : BN == 192 ? launch_mmq_q4<192, true>(args, maps, units, cs)
+                           : launch_mmq_q4<256, true>(args, maps, units, cs);
+    return BN == 128   ? launch_mmq_q4<128, false>(args, maps, units, cs)
+           : BN == 192 ? launch_mmq_q4<192, false>(args, maps, units, cs)
+                       : launch_mmq_q4<256, false>(args, maps, units, cs);
 }
 
 }  // namespace
@@ -1467,7 +1560,7 @@ extern "C" int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *b
 {
     if (!bytes) return QK_E_NULL;
     if (M < 0 || N < 1 || K < 256 || K % 256 != 0) return QK_E_SHAPE;
-    *bytes = ws_bytes(M, K) + (M > 0 ? split_bytes(q4_plan(M, N, K, 0, qk::sm_count())) : 0);
+    *bytes = ws_bytes(M, K);                  // the split scratch of QK_MMQ_SPLIT_K is the caller's to add
     return QK_OK;
 }
 

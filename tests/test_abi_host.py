@@ -156,7 +156,10 @@ def test_mmq_rejects(L, fn):
     assert f(w, c, s, 16, 64, 256, None, y, ws, need - 16, 0, None) == -6         # QK_E_WORKSPACE
     assert f(w, c, s, 16, 64, 256, None, c, ws, need, 0, None) == E_ALIAS
     assert f(w, c, s, 16, 64, 256, None, y, y, need, 0, None) == E_ALIAS           # workspace over y
-    assert f(w, c, s, 16, 64, 256, None, y, ws, need, 6, None) == E_SHAPE          # both tile widths forced
+    assert f(w, c, s, 16, 64, 256, None, y, ws, need, 6, None) == E_SHAPE          # two tile widths forced
+    assert f(w, c, s, 16, 64, 256, None, y, ws, need, 10, None) == E_SHAPE         # 256 and 192 forced
+    if fn == "qk_mmq_q6k":
+        assert f(w, c, s, 16, 64, 256, None, y, ws, need, 8, None) == E_SHAPE      # Q6_K has no 192-wide tile
 
 
 def test_min_plane_size_and_rejects(L):

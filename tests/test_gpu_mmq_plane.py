@@ -69,7 +69,7 @@ def test_min_plane_bytes(N, K):
 
 
 @pytest.mark.parametrize("M,N,K,tile", [(200, 1000, 768, None), (256, 512, 1024, 128), (130, 2000, 2560, 256),
-                                        (1, 300, 256, None), (333, 4608, 3584, None)])
+                                        (1, 300, 256, None), (333, 4608, 3584, None), (150, 3584, 1280, 192)])
 def test_mmq_plane_bitexact(M, N, K, tile):
     w = synth.weights("q4k", N, K, seed=M + N)
     wr = qk.repack(1, dev(w), N, K)
@@ -92,17 +92,16 @@ def test_mmq_plane_bitexact(M, N, K, tile):
 
 
 def test_mmq_plane_split_k():
-    """The plane with the split-K tail (224 tiles on 152 SMs, 48 superblocks of K)."""
-    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
-        pytest.skip("the split decision is sized for 152 SMs")
+    """The plane with the K range of each tile split in two (QK_MMQ_SPLIT_K; 224 tiles, 48 superblocks)."""
     M, N, K = 256, 256 * 112, 48 * 256
     w = synth.weights("q4k", N, K, seed=7)
     wr = qk.repack(1, dev(w), N, K)
     codes, scales = qk.quantize_q8_1(dev(synth.activations(M, K, seed=8)))
     plane = qk.q4k_min_plane(wr, N, K)
-    ws = torch.empty(qk.mmq_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
-    y0 = qk.mmq_q4k(wr, codes, scales, N, K, workspace=ws)
-    y1 = qk.mmq_q4k_plane(wr, plane, codes, scales, N, K, workspace=ws)
+    ws = torch.empty(2 * (K * 512 + (K // 512) * 8192) + 224 * 2 * 128 * 256 * 4 + 224 * 4, dtype=torch.uint8,
+                     device="cuda")                       # with the scratch of a split of 224 256-wide tiles
+    y0 = qk.mmq_q4k(wr, codes, scales, N, K, workspace=ws, tile=256, split_k=True)
+    y1 = qk.mmq_q4k_plane(wr, plane, codes, scales, N, K, workspace=ws, tile=256, split_k=True)
     torch.cuda.synchronize()
     assert torch.equal(y0, y1)
 

@@ -291,11 +291,13 @@ def mmq_fn(qt):
     return qk.mmq_q4k if qt == "q4k" else qk.mmq_q6k
 
 
-@pytest.mark.parametrize("tile", [None, 256, 128])
+@pytest.mark.parametrize("tile", [None, 256, 192, 128])
 @pytest.mark.parametrize("qt", ["q4k", "q6k"])
 @pytest.mark.parametrize("M,N,K", [(1, 64, 256), (17, 130, 512), (64, 128, 2304), (130, 300, 4096),
-                                   (200, 77, 768), (65, 129, 256 * 9)])
+                                   (200, 77, 768), (65, 129, 256 * 9), (140, 450, 1024)])
 def test_mmq_parity(qt, M, N, K, tile):
+    if qt == "q6k" and tile == 192:
+        pytest.skip("Q6_K tiles are 128 or 256 wide")
     w, wr = weights(qt, N, K, seed=M * 3 + N + K)
     x = synth.activations(M, K, seed=M)
     codes, scales = q8(x)
@@ -316,7 +318,7 @@ def test_mmq_tile_widths_agree_and_many_tiles_per_cta(qt):
     c, d = q8_host(codes, scales)
     rows = (N - 700, N)
     y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d, rows=rows)
-    for tile in (256, 128):
+    for tile in (256, 192, 128) if qt == "q4k" else (256, 128):
         y = mmq_fn(qt)(wr, codes, scales, N, K, tile=tile).cpu().numpy()
         check(y[:, rows[0]:rows[1]], y_ref, ab, what=f"mmq {qt} tile={tile}")
 
@@ -418,25 +420,27 @@ def test_mmq_superblock_scale_special_cases(qt):
 
 @pytest.mark.parametrize("M,N", [(256, 256 * 112), (200, 256 * 112 - 40)])
 def test_mmq_q4k_split_k_tail(M, N):
-    """224 tiles of 128 x 256 on 152 SMs with 48 superblocks of K: with the full workspace the Q4_K
-    MMQ splits each tile's K range over two work units (the second to finish adds the partial tiles).
+    """224 tiles of 128 x 256 with 48 superblocks of K, QK_MMQ_SPLIT_K: with the split
+    scratch in the workspace the Q4_K MMQ splits each tile's K range over two work units (the second
+    to finish adds the partial tiles).
     Checked against the oracle on sampled rows, against the same call run unsplit (a base-size
     workspace), for reproducibility, and for the tile counters being left at zero."""
-    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
-        pytest.skip("the split decision is sized for 152 SMs")
     K = 48 * 256
     w, wr = weights("q4k", N, K, seed=41)
     codes, scales = q8(synth.activations(M, K, seed=42))
     c, d = q8_host(codes, scales)
     r = dev(synth.residual(M, N, seed=43))
-    full = qk.mmq_workspace_bytes(M, N, K)
     base = 2 * (K * 512 + (K // 512) * 8192)              # two M-tiles: A blocks and sums tiles
-    assert full > base                                    # the split scratch is requested
-    ws = torch.empty(full, dtype=torch.uint8, device="cuda")
+    full = base + 224 * 2 * 128 * 256 * 4 + 224 * 4       # with the scratch of a split of 224 256-wide tiles
+    assert qk.mmq_workspace_bytes(M, N, K) == base
+    ws = torch.full((full,), 0xAB, dtype=torch.uint8, device="cuda")
     qk.error_flags(clear=True)
-    y1 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws)
-    y2 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws, pdl=True)
-    yu = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws[:base])
+    y1 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws, tile=256, split_k=True)
+    torch.cuda.synchronize()
+    assert int((ws[base:base + 4096] != 0xAB).sum()) > 0          # the split wrote its partial tiles
+    y2 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws, pdl=True, tile=256, split_k=True)
+    yu = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws[:base], tile=256, split_k=True)
+    y9 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws, tile=192)
     torch.cuda.synchronize()
     assert qk.error_flags(clear=True) == 0
     assert torch.equal(y1, y2)
@@ -448,6 +452,7 @@ def test_mmq_q4k_split_k_tail(M, N):
         y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d, residual=r_np, rows=(lo, hi))
         check(y1.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"split rows {lo}")
         check(yu.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"unsplit rows {lo}")
+        check(y9.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"192-wide rows {lo}")
 
 
 def _f16_bytes(v):

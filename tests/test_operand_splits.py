@@ -3,8 +3,9 @@
 The MMQ kernels feed the tensor cores binary16 operands and rest their error bound on
 how those are formed (the header's MMQ contract):
   - the activation d_a * q_a as A_hi + A_lo, exactly;
-  - the Q4_K weight operand sc * q (6-bit scale, 4-bit code) as one f16, built in a
-    16-bit lane as the bits 0x6400 + sc * q (the f16 1024 + sc * q) minus 1024;
+  - the Q4_K weight operand sc * q (6-bit scale, 4-bit code) as one f16, built from the
+    16-bit lane 0x6400 + q (the f16 1024 + q) by one fused multiply-add with sc and
+    -1024 * sc;
   - the Q4_K min operand 1024 * dmin * m as Mw_hi (the binary32 value with its 13 low
     mantissa bits cleared) + Mw_lo (the rest), exactly wherever the rest's last bit is
     an f16 number;
@@ -51,6 +52,24 @@ def test_q4k_weight_operand_bit_construction():
     prod = word * sc[:, :, None] + 0x64006400
     assert np.all((prod >> 16) == 0x6400 + sc[:, :, None] * q[:, None, :])
     assert np.all((prod & 0xFFFF) == 0x6400 + sc[:, :, None] * q[:, :, None])
+
+
+def test_q4k_weight_operand_fma():
+    # every (sc, q): 0x6400 | q is the f16 1024 + q; sc and -1024 sc are f16 numbers; the exact
+    # (1024 + q) sc - 1024 sc = sc q (below 1024) is an f16 number, so the one rounding of a fused
+    # multiply-add in binary16 leaves it unchanged
+    sc = np.arange(64, dtype=np.int64)[:, None]
+    q = np.arange(16, dtype=np.int64)[None, :]
+    a = (0x6400 | q).astype(np.uint16).view(np.float16).astype(np.float64)
+    assert np.array_equal(a, 1024.0 + q)
+    s16 = sc.astype(np.float16)
+    n16 = (s16.astype(np.float64) * -1024.0).astype(np.float16)
+    assert np.array_equal(s16.astype(np.float64), sc.astype(np.float64))
+    assert np.array_equal(n16.astype(np.float64), -1024.0 * sc)
+    exact = a * s16.astype(np.float64) + n16.astype(np.float64)            # exact in binary64
+    assert np.array_equal(exact, (sc * q).astype(np.float64))
+    assert np.array_equal(exact.astype(np.float16).astype(np.float64), exact)
+    assert np.abs(a * s16.astype(np.float64)).max() < 65504.0            # no overflow on the way
 
 
 def split_hi_lo_f32(w32):
