@@ -35,20 +35,26 @@
 //     instead of converting the activation again.
 //  2. the main kernel: a persistent grid, one CTA per SM, each CTA taking
 //     128 x BN output tiles t = blockIdx.x, blockIdx.x + gridDim.x, ...
-//     (M-tile fastest).  Warp 0 lane 0 issues every MMA and commit, warp 1
-//     lane 0 copies each stage's activation block from the workspace with one
-//     bulk copy, warp 2 lane 0 streams the raw weight bytes with 2D TMA tensor
+//     (M-tile fastest).  Warp 0 lane 0 issues every MMA and commit, warp 3
+//     (the sync warp) waits for each stage's operands and accumulator buffer
+//     and hands the stage to warp 0 through a named barrier, warp 1 lane 0
+//     copies each stage's activation block from the workspace with one bulk
+//     copy, warp 2 lane 0 streams the raw weight bytes with 2D TMA tensor
 //     copies into a ring (the code runs of a superblock and its per-row
 //     records), epilogue warps read the accumulators, and converter warps
 //     expand each K stage's codes and scales into f16 tiles in the
 //     SWIZZLE_64B layout.  The roles of each kernel are listed above it.
 // Stages are handed over with mbarriers (full: converters and the activation
-// copy's bytes -> MMA; empty: MMA commit -> converters and activation copier;
-// raw: TMA bytes -> converters -> producer; accumulator full / empty: MMA
-// commit -> epilogue -> MMA; done: last MMA commit -> teardown).  Every wait is
-// bounded; a wait that gives up sets a device error flag (qk_error_flags), and
-// once it is set the other waits return after a few polls, so the kernel runs
-// to its end.
+// copy's bytes -> sync warp -> MMA; empty: MMA commit -> converters and
+// activation copier; raw: TMA bytes -> converters -> producer; accumulator
+// full / empty: MMA commit -> epilogue -> sync warp -> MMA; done: last MMA
+// commit -> teardown).  The MMA thread itself never polls an mbarrier between
+// MMAs: a shared-memory poll there idles the tensor pipe (about 150 ns a
+// stage, measured), while a named barrier (bar.sync) does not.  Every
+// mbarrier wait is bounded; a wait that gives up sets a device error flag
+// (qk_error_flags), and once it is set the other waits return after a few
+// polls, so the kernel runs to its end (the sync warp still releases every
+// stage, so the MMA warp's named barriers always complete).
 // Before the CTA releases its tensor memory and exits, the MMA thread waits
 // for its last MMAs and the producers for their last copies (bounded too), so
 // nothing is left in flight.
@@ -660,7 +666,7 @@ __global__ void __launch_bounds__(Plan<QT, BN_>::kThreads, 1)
 // tiles (S_hi | S_lo, built by the prep kernel) against (Mw_hi | Mw_lo),
 // Mw = 1024 dmin m (17 significant bits, split exactly down to 2^-8), three MMAs per 16
 // sub-blocks; its accumulator seeds the register tile.
-// Warps: 0 MMA, 1 activation copier, 2 TMA producer, 3 idle, 4-11 epilogue
+// Warps: 0 MMA, 1 activation copier, 2 TMA producer, 3 sync warp, 4-11 epilogue
 // (TMEM lane quadrant warp % 4, column half (warp - 4) / 4), 12.. converters
 // (one thread per weight row).  With 256- and 192-wide tiles the epilogue warps
 // hold 128 or 96 accumulator columns each and take registers from the other
