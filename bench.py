@@ -119,14 +119,16 @@ def gemm_fused(policy: str, cfg, gemm) -> bool:
 # kernel's launches in one step) from one ncu capture of the command in the named profile.
 # Valid only while the kernel sources are the ones the counters were taken on.
 TRAFFIC: dict = {
-    (1, "gemv_q4k_f32"): {"bytes_per_launch": 29981181, "digest": "bc3a9e2fedd8c4ef",
-                          "profile": "profiles/dram_traffic_per_launch.md"},
-    (2, "gemv_q6k_f32"): {"bytes_per_launch": 437107968, "digest": "bc3a9e2fedd8c4ef",
-                          "profile": "profiles/gemv_q6k_f32_head_128256x4096.md"},
-    (3, "gemv_q6k"): {"bytes_per_launch": 435261696, "digest": "bc3a9e2fedd8c4ef",
+    (0, "gemv_q4k"): {"bytes_per_launch": 9464527, "digest": "ab63c82967201baa",
                       "profile": "profiles/dram_traffic_per_launch.md"},
-    (4, "mmq_q4k"): {"bytes_per_launch": 233749376, "digest": "b1c1938ee3b443a4",
-                     "profile": "profiles/dram_traffic_per_launch.md"},
+    (1, "gemv_q4k"): {"bytes_per_launch": 30709818, "digest": "ab63c82967201baa",
+                      "profile": "profiles/launches_llama3_8b_decode_layer.md"},
+    (2, "gemv_q6k"): {"bytes_per_launch": 434216499, "digest": "ab63c82967201baa",
+                      "profile": "profiles/gemv_q6k_head_128256x4096.md"},
+    (3, "gemv_q6k"): {"bytes_per_launch": 435280896, "digest": "ab63c82967201baa",
+                      "profile": "profiles/gemv_q6k_head_m4_128256x4096.md"},
+    (4, "mmq_q4k"): {"bytes_per_launch": 289731232, "digest": "4fad9d23e5b83fae",
+                     "profile": "profiles/launches_qwen2_7b_prefill_mmq.md"},
 }
 
 
