@@ -78,11 +78,12 @@ extern "C" {
  * within the stated bound either way; the flags exist for tests and tuning.
  * Setting more than one, or QK_MMQ_TILE_192 for Q6_K, is QK_E_SHAPE.
  *
- * QK_MMQ_SPLIT_K (Q4_K MMQ only): split each output tile's K range over two
+ * QK_MMQ_SPLIT_K (Q4_K MMQ only): split every output tile's K range over two
  * work units, the second to finish adding the two partial tiles (binary32,
  * the same bits either way).  Taken only when K has at least 48 superblocks
  * and the workspace also holds the split scratch (see qk_mmq_q4k); otherwise
- * ignored.  Off by default: on the prefill shapes it measured slower.
+ * ignored.  By default only the tiles of a poorly filled last wave are
+ * split (qk_mmq_q4k); splitting every tile measured slower.
  */
 #define QK_MMQ_TILE_256 2u
 #define QK_MMQ_TILE_128 4u
@@ -393,13 +394,18 @@ int qk_gemv_q3k_f32(const void *w, const float *x, int64_t ldx,
  *   this call that run after the call returns, so the workspace must not be
  *   reused by work that is not ordered after this call on `stream`.  Size:
  *   at least the base ceil(M/128) * (K * 512 + ceil(K/512) * 8192) bytes
- *   (M = 2048, K = 18944: 160,038,912 bytes); qk_mmq_workspace_bytes
- *   returns it.  A call with QK_MMQ_SPLIT_K (Q4_K) splits only if the
- *   workspace also holds the split scratch after the base size: 512 * BN
- *   bytes of partial tile per work unit and 4 bytes per tile, BN the tile
- *   width the call picks (M = 2048, N = 3584 at 256: 224 tiles, 58,721,152
- *   bytes); with less it runs unsplit.  Split and unsplit results differ
- *   only in rounding, within the same bound, and each is reproducible.
+ *   (M = 2048, K = 18944: 160,038,912 bytes).  After it, a Q4_K call whose
+ *   tiles are split in two along K keeps scratch: 1024 * BN bytes of partial
+ *   tiles and 4 bytes of counter per split tile, BN the tile width it picks.
+ *   By default the Q4_K MMQ splits the tiles of a poorly filled last wave
+ *   when K has at least 48 superblocks (Qwen2-7B down, M = 2048: 72 of 224
+ *   tiles of 256 on 152 SMs, 18,874,656 bytes); QK_MMQ_SPLIT_K splits every
+ *   tile.  qk_mmq_workspace_bytes returns the base size plus the default
+ *   plan's scratch on the current device (QK_MMQ_SPLIT_K's is the caller's
+ *   to add: 224 tiles, 58,721,152 bytes).  A workspace without room for the
+ *   scratch runs the call unsplit.  Split and unsplit results differ only
+ *   in rounding, within the same bound, and each is reproducible (the two
+ *   partial tiles are added in binary32 by the second unit to finish).
  * Returns QK_E_WORKSPACE if workspace_bytes is below the base size.
  */
 int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes);

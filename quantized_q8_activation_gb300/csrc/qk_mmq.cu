@@ -169,14 +169,15 @@ struct MmqArgs {
     const float *residual;
     float *y;
     int mtiles, ntiles;     // tile t covers M-tile t % mtiles, N-tile t / mtiles
-    // Q4_K split of the K range: work unit u is segment u % split of tile u / split; segment 0 covers
-    // superblocks [0, mid) and the min term, segment 1 [mid, K/256).  With split == 2 each unit
-    // leaves its partial tile in part[u] and the second unit of a tile to finish (cnt[tile]) adds the
-    // two partials and writes y.
-    int split;
-    int mid;                // split == 2: segment 0 covers superblocks [0, mid), segment 1 [mid, K/256)
-    float *part;            // [units][128][BN]
-    unsigned *cnt;          // [tiles], zeroed by the prep kernel
+    // Q4_K split of the K range: tiles [0, nfull) are work units of their own; each tile from nfull on
+    // is split over two units (segment 0: superblocks [0, mid) and the min term; segment 1: [mid,
+    // K/256)), each leaving its partial tile in part[], the second of the two to finish (cnt[]) adding
+    // the partials and writing y.
+    int split;              // 1: no split tiles (nfull = all tiles); 2: tiles from nfull on are split
+    int nfull;
+    int mid;
+    float *part;            // [2 (tiles - nfull)][128][BN]
+    unsigned *cnt;          // [tiles - nfull], zeroed by the prep kernel
 };
 
 // One 32 x 16 chunk of an output tile, staged in a warp's transpose buffer (row r at r * EPI_LD),
@@ -815,9 +816,19 @@ __global__ void __launch_bounds__(256) q4k_min_plane_kernel(const uint4 *__restr
     flag_range(bad);
 }
 
-// superblock range [seg_lo, seg_hi) of segment seg of a tile
-__device__ __forceinline__ int seg_lo(const MmqArgs &a, int seg) { return seg == 0 ? 0 : a.mid; }
-__device__ __forceinline__ int seg_hi(const MmqArgs &a, int seg, int B) { return seg == 0 && a.split > 1 ? a.mid : B; }
+// work unit u: its tile, its segment of the tile's K range and the number of segments of that tile
+struct Unit {
+    int t, seg, ns;
+};
+__device__ __forceinline__ Unit unit_of(const MmqArgs &a, int u)
+{
+    if (u < a.nfull) return Unit{u, 0, 1};
+    const int v = u - a.nfull;
+    return Unit{a.nfull + (v >> 1), v & 1, 2};
+}
+// superblock range [seg_lo, seg_hi) of a unit
+__device__ __forceinline__ int seg_lo(const MmqArgs &a, const Unit &un) { return un.seg == 0 ? 0 : a.mid; }
+__device__ __forceinline__ int seg_hi(const MmqArgs &a, const Unit &un, int B) { return un.seg == 0 && un.ns > 1 ? a.mid : B; }
 
 // named barrier 1 over the epilogue warps only
 template <int NW>
@@ -838,7 +849,7 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
     float *dring = reinterpret_cast<float *>(smem + L::OFF_D);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = (int)(a.K >> 8), nmin = (B + 1) >> 1;
-    const int S = a.split, nunits = a.mtiles * a.ntiles * S;
+    const int ntiles = a.mtiles * a.ntiles, nunits = ntiles + (a.split > 1 ? ntiles - a.nfull : 0);
 
     qk::pdl_launch_dependents();
     if (threadIdx.x == 0) {
@@ -873,9 +884,10 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         const uint32_t sbase = smem_u32(smem);
         int gs = 0, ge = 0;
         for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-            const int seg = u % S, nsb = seg_hi(a, seg, B) - seg_lo(a, seg);
+            const Unit un = unit_of(a, u);
+            const int nsb = seg_hi(a, un, B) - seg_lo(a, un);
             // events: the min term (segment 0 only), then one per superblock of the segment
-            for (int ev = seg == 0 ? 0 : 1; ev <= nsb; ev++, ge++) {
+            for (int ev = un.seg == 0 ? 0 : 1; ev <= nsb; ev++, ge++) {
                 const int acc = ge & 1;
                 const uint32_t dacc = tmem + acc * BN;
                 const int nst = ev == 0 ? nmin : 8;
@@ -924,8 +936,9 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         // reused only after the issuer has passed it: the stage's next operands need its MMAs' commit.
         int gs = 0, ge = 0;
         for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-            const int seg = u % S, nsb = seg_hi(a, seg, B) - seg_lo(a, seg);
-            for (int ev = seg == 0 ? 0 : 1; ev <= nsb; ev++, ge++) {
+            const Unit un = unit_of(a, u);
+            const int nsb = seg_hi(a, un, B) - seg_lo(a, un);
+            for (int ev = un.seg == 0 ? 0 : 1; ev <= nsb; ev++, ge++) {
                 const int acc = ge & 1;
                 if (ge >= 2) wait_bar(&bar[L::ACCEMPTY + acc], ((ge >> 1) + 1) & 1);
                 const int nst = ev == 0 ? nmin : 8;
@@ -942,11 +955,12 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         if (lane == 0) {
             int gs = 0;
             for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-                const int t = u / S, seg = u % S, mt = t % a.mtiles;
+                const Unit un = unit_of(a, u);
+                const int t = un.t, seg = un.seg, mt = t % a.mtiles;
                 const uint8_t *srcS = a.wsS + (size_t)mt * nmin * SBLK;
                 const uint8_t *srcA = a.wsA + (size_t)mt * (8 * B) * ABLOCK;
                 // the sums tiles of the min stages (segment 0), then the A blocks of the segment's superblocks
-                const int i0 = seg == 0 ? 0 : nmin + 8 * seg_lo(a, seg), i1 = nmin + 8 * seg_hi(a, seg, B);
+                const int i0 = seg == 0 ? 0 : nmin + 8 * seg_lo(a, un), i1 = nmin + 8 * seg_hi(a, un, B);
                 for (int i = i0; i < i1; i++, gs++) {
                     const int st = gs % NS;
                     if (gs >= NS) wait_bar(&bar[L::EMPTY + st], ((gs / NS) + 1) & 1);
@@ -969,7 +983,8 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
             if (PL) prefetch_tmap(&maps.plane);
             int gsb = 0, gu = 0;
             for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-                const int t = u / S, seg = u % S;
+                const Unit un = unit_of(a, u);
+                const int t = un.t, seg = un.seg;
                 const int n0 = (t / a.mtiles) * BN;
                 if (PL && seg == 0)
                     for (int i = 0; i < nmin; i++, gu++) {
@@ -981,7 +996,7 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                 // pass 0 (segment 0, no plane): every superblock's record for the min stages; pass 1: the
                 // segment's superblocks, record and code bytes
                 for (int pass = seg == 0 && !PL ? 0 : 1; pass < 2; pass++) {
-                    for (int sb = pass == 0 ? 0 : seg_lo(a, seg); sb < (pass == 0 ? B : seg_hi(a, seg, B)); sb++, gsb++) {
+                    for (int sb = pass == 0 ? 0 : seg_lo(a, un); sb < (pass == 0 ? B : seg_hi(a, un, B)); sb++, gsb++) {
                         const int ss = gsb % NB;
                         if (gsb >= NB) wait_bar(&bar[L::SEMPTY + ss], ((gsb / NB) + 1) & 1);
                         mbar_arrive_expect_tx(&bar[L::SFULL + ss], L::SBR);
@@ -1020,7 +1035,8 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         float R[L::CPT];
         int ge = 0, gd = 0;
         for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-            const int t = u / S, seg = u % S;
+            const Unit un = unit_of(a, u);
+            const int t = un.t, seg = un.seg;
             const int64_t m0 = (int64_t)(t % a.mtiles) * BM, n0 = (int64_t)(t / a.mtiles) * BN;
             if (seg != 0) {
 #pragma unroll
@@ -1044,7 +1060,7 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                 ge++;
             }
 #pragma unroll 1
-            for (int sb = seg_lo(a, seg); sb < seg_hi(a, seg, B); sb++, ge++, gd++) {
+            for (int sb = seg_lo(a, un); sb < seg_hi(a, un, B); sb++, ge++, gd++) {
                 const int acc = ge & 1, ds = gd % ND;
                 wait_bar(&bar[L::DFULL + ds], (gd / ND) & 1);
                 wait_bar(&bar[L::ACCFULL + acc], (ge >> 1) & 1);
@@ -1074,21 +1090,22 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                     mbar_arrive(&bar[L::DEMPTY + ds]);
                 }
             }
-            if (S > 1) {
+            if (un.ns > 1) {
+                const int v = u - a.nfull;                 // this split unit's partial-tile slot
                 // this segment's partial tile: row (32 quad + lane), columns ch CPT .. +CPT, contiguous
                 const size_t poff = ((size_t)(quad * 32 + lane)) * BN + ch * L::CPT;
-                float4 *mine = reinterpret_cast<float4 *>(a.part + (size_t)u * BM * BN + poff);
+                float4 *mine = reinterpret_cast<float4 *>(a.part + (size_t)v * BM * BN + poff);
 #pragma unroll
                 for (int c = 0; c < L::CPT / 4; c++) mine[c] = make_float4(R[4 * c], R[4 * c + 1], R[4 * c + 2], R[4 * c + 3]);
                 __threadfence();
                 epi_sync<L::kEpiW>();
                 unsigned *flag = reinterpret_cast<unsigned *>(smem + L::OFF_TMEM + 8);
                 if (ew == 0 && lane == 0) {
-                    const unsigned prev = atomicAdd(&a.cnt[t], 1u);
-                    const bool last = prev == (unsigned)(S - 1);
+                    const unsigned prev = atomicAdd(&a.cnt[t - a.nfull], 1u);
+                    const bool last = prev == 1u;
                     if (last) {
                         __threadfence();
-                        a.cnt[t] = 0;                      // ready for the next call on this workspace
+                        a.cnt[t - a.nfull] = 0;            // ready for the next call on this workspace
                     }
                     *flag = last ? 1u : 0u;
                 }
@@ -1099,7 +1116,7 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
                 // the last of the two segments to finish: y = P_0 + P_1, the same bits whichever it is
                 // (binary32 addition is commutative)
                 const float4 *other =
-                    reinterpret_cast<const float4 *>(a.part + (size_t)(u - seg + (1 - seg)) * BM * BN + poff);
+                    reinterpret_cast<const float4 *>(a.part + (size_t)(v ^ 1) * BM * BN + poff);
 #pragma unroll
                 for (int c = 0; c < L::CPT / 4; c++) {
                     const float4 w = __ldcg(other + c);
@@ -1131,7 +1148,8 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
         const int row = 32 * (warp - L::kConvW0) + lane;
         int gs = 0, gsb = 0, gu = 0, gd = 0;
         for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-            const int seg = u % S;
+            const Unit un = unit_of(a, u);
+            const int seg = un.seg;
             // min stages (segment 0): sub-blocks of superblocks 2i and 2i+1 -> (Mw_hi | Mw_lo)
 #pragma unroll 1
             for (int i = 0; i < (seg == 0 ? nmin : 0); i++, gs++) {
@@ -1188,7 +1206,7 @@ __global__ void __launch_bounds__(Plan4<BN_>::kThreads, 1)
             }
             // main stages: per superblock its scale d into the scale ring, then sub-block j -> W' = sc q
 #pragma unroll 1
-            for (int sb = seg_lo(a, seg); sb < seg_hi(a, seg, B); sb++, gsb++, gd++) {
+            for (int sb = seg_lo(a, un); sb < seg_hi(a, un, B); sb++, gsb++, gd++) {
                 const int ss = gsb % NB, ds = gd % ND;
                 wait_bar(&bar[L::SFULL + ss], (gsb / NB) & 1);
                 const uint4 mt = *reinterpret_cast<const uint4 *>(smem + L::OFF_SBR + ss * L::SBR + row * 16);
@@ -1313,22 +1331,25 @@ int split_mid(int B)
 struct Q4Plan {
     int BN, split;
     int64_t tiles;
+    int64_t tail;           // split == 2: the tiles split in two (the last `tail` ones)
 };
 
 // Time of one work unit: a fixed part (the tile's pipeline start and its output) and a part per K
 // stage, measured per tile width on the Qwen2-7B prefill GEMMs (K = 3584 and 18944, split-scale kernel
 // with the sync warp and the min-operand plane): 256: 40 us + 0.43 us a stage, 192: 26 + 0.48,
-// 128: 14 + 0.424.  A split unit adds 39 us (its partial tile out and back, the second pipeline start).
+// 128: 14 + 0.424.  A unit of a split tile adds 40 us (its partial tile out and back, its own
+// pipeline start; measured with every down tile split: 648 us for three waves of half tiles).
 double unit_us(int BN, int64_t stages, int split)
 {
     const double a = BN == 256 ? 40.0 : BN == 192 ? 26.0 : 14.0, b = BN == 256 ? 0.43 : BN == 192 ? 0.48 : 0.424;
-    return a + b * (double)stages + (split > 1 ? 39.0 : 0.0);
+    return a + b * (double)stages + (split > 1 ? 40.0 : 0.0);
 }
 
-// The width whose waves of tiles over the SMs should finish first (a forced width, QK_MMQ_TILE_*,
-// is taken as it is).  The K range of each tile is split in two only on request (QK_MMQ_SPLIT_K) and
-// for K of at least 2 kMinSegSb superblocks: on the benchmark shapes the model above puts a split
-// behind the unsplit tile (measured: K = 18944, 224 tiles of 256: 642 us split, 620 unsplit).
+// The width, and whether to split the tiles of a poorly filled last wave, whose waves of work units
+// over the SMs should finish first.  A forced width (QK_MMQ_TILE_*) is taken as it is; QK_MMQ_SPLIT_K
+// splits every tile.  A split needs K of at least 2 kMinSegSb superblocks; the tail split takes the
+// last wave's tiles (fewer than half the SMs) as two units each, so that the tail runs as one wave
+// of half tiles: Qwen2-7B down, 224 tiles of 256 on 152 SMs, 152 whole tiles then 144 half tiles.
 Q4Plan q4_plan(int64_t M, int64_t N, int64_t K, unsigned flags, int sms, int max_split = kMaxSplit)
 {
     if (sms < 1) sms = 1;
@@ -1336,24 +1357,35 @@ Q4Plan q4_plan(int64_t M, int64_t N, int64_t K, unsigned flags, int sms, int max
                      : (flags & QK_MMQ_TILE_128) ? 128 : 0;
     const int widths[3] = {256, 192, 128};
     const int64_t gx = (M + BM - 1) / BM, B = K / 256, stages = 8 * B + (B + 1) / 2;
-    Q4Plan best{256, 1, gx * ((N + 255) / 256)};
+    const bool can_split = max_split >= 2 && B >= 2 * kMinSegSb;
+    Q4Plan best{256, 1, gx * ((N + 255) / 256), 0};
     double bc = 1e300;
     for (int wi = 0; wi < 3; wi++) {
         const int BN = widths[wi];
         if (forced && BN != forced) continue;
         const int64_t tiles = gx * ((N + BN - 1) / BN);
+        if (can_split && (flags & QK_MMQ_SPLIT_K)) {                   // every tile split
+            best = Q4Plan{BN, 2, tiles, tiles};
+            bc = 0.0;
+            continue;
+        }
         const double c = (double)((tiles + sms - 1) / sms) * unit_us(BN, stages, 1);
-        if (c < bc * (1.0 - 1e-9)) bc = c, best = Q4Plan{BN, 1, tiles};
+        if (c < bc * (1.0 - 1e-9)) bc = c, best = Q4Plan{BN, 1, tiles, 0};
+        const int64_t tail = tiles % sms;
+        if (can_split && tail > 0 && 2 * tail <= sms) {
+            const double ct = (double)(tiles / sms) * unit_us(BN, stages, 1) + unit_us(BN, stages / 2, 2);
+            if (ct < bc * (1.0 - 1e-9)) bc = ct, best = Q4Plan{BN, 2, tiles, tail};
+        }
     }
-    if ((flags & QK_MMQ_SPLIT_K) && max_split >= 2 && B >= 2 * kMinSegSb) best.split = 2;
     return best;
 }
 
-// scratch of a split call after the base workspace: the partial tiles, then the tile counters
+// scratch of a split call after the base workspace: two partial tiles per split tile, then one
+// counter per split tile
 size_t split_bytes(const Q4Plan &p)
 {
     if (p.split <= 1) return 0;
-    return (size_t)p.tiles * p.split * BM * p.BN * 4 + (size_t)p.tiles * 4;
+    return (size_t)p.tail * 2 * BM * p.BN * 4 + (size_t)p.tail * 4;
 }
 
 // The register-split kernel must be launched with at least the registers its setmaxnreg split hands
@@ -1454,6 +1486,7 @@ int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const voi
         plan.BN = tf == QK_MMQ_TILE_256 ? 256 : tf == QK_MMQ_TILE_128 ? 128 : pick_bn(M, N, sms);
         plan.split = 1;
         plan.tiles = ((M + BM - 1) / BM) * ((N + plan.BN - 1) / plan.BN);
+        plan.tail = 0;
     } else {
         plan = q4_plan(M, N, K, flags, sms);
         if (workspace_bytes < need + split_bytes(plan)) plan = q4_plan(M, N, K, flags, sms, 1);  // no scratch
@@ -1516,11 +1549,11 @@ int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const voi
     unsigned *cnt = nullptr;
     if (plan.split > 1) {
         part = reinterpret_cast<float *>(wsA + need);
-        cnt = reinterpret_cast<unsigned *>(wsA + need + (size_t)plan.tiles * plan.split * BM * BN * 4);
+        cnt = reinterpret_cast<unsigned *>(wsA + need + (size_t)plan.tail * 2 * BM * BN * 4);
     }
     int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, cs,
                         (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA, wsS,
-                        cnt, plan.split > 1 ? (int)plan.tiles : 0);
+                        cnt, plan.split > 1 ? (int)plan.tail : 0);
     if (st != QK_OK) return st;
     MmqArgs args{};
     args.wsA = wsA;
@@ -1534,12 +1567,13 @@ int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const voi
     args.mtiles = (int)gx;
     args.ntiles = (int)gy;
     args.split = plan.split;
+    args.nfull = (int)(plan.split > 1 ? tiles - plan.tail : tiles);
     args.mid = plan.split > 1 ? split_mid((int)B) : (int)B;
     args.part = part;
     args.cnt = cnt;
     if (q6) return BN == 128 ? launch_mmq<QK_TYPE_Q6_K, 128>(args, maps, tiles, cs)
                              : launch_mmq<QK_TYPE_Q6_K, 256>(args, maps, tiles, cs);
-    const int64_t units = tiles * plan.split;
+    const int64_t units = tiles + (plan.split > 1 ? plan.tail : 0);
     if (plane)
         return BN == 128   ? launch_mmq_q4<128, true>(args, maps, units, cs)
                : BN == 192 ? launch_mmq_q4<192, true>(args, maps, units, cs)
@@ -1566,7 +1600,9 @@ extern "C" int qk_mmq_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *b
 {
     if (!bytes) return QK_E_NULL;
     if (M < 0 || N < 1 || K < 256 || K % 256 != 0) return QK_E_SHAPE;
-    *bytes = ws_bytes(M, K);                  // the split scratch of QK_MMQ_SPLIT_K is the caller's to add
+    // the scratch of the tail split the call would take on this device (QK_MMQ_SPLIT_K's is the
+    // caller's to add)
+    *bytes = ws_bytes(M, K) + (M > 0 ? split_bytes(q4_plan(M, N, K, 0, qk::sm_count())) : 0);
     return QK_OK;
 }
 

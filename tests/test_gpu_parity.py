@@ -432,7 +432,7 @@ def test_mmq_q4k_split_k_tail(M, N):
     r = dev(synth.residual(M, N, seed=43))
     base = 2 * (K * 512 + (K // 512) * 8192)              # two M-tiles: A blocks and sums tiles
     full = base + 224 * 2 * 128 * 256 * 4 + 224 * 4       # with the scratch of a split of 224 256-wide tiles
-    assert qk.mmq_workspace_bytes(M, N, K) == base
+    assert qk.mmq_workspace_bytes(M, N, K) >= base
     ws = torch.full((full,), 0xAB, dtype=torch.uint8, device="cuda")
     qk.error_flags(clear=True)
     y1 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws, tile=256, split_k=True)
@@ -453,6 +453,42 @@ def test_mmq_q4k_split_k_tail(M, N):
         check(y1.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"split rows {lo}")
         check(yu.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"unsplit rows {lo}")
         check(y9.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"192-wide rows {lo}")
+
+
+@pytest.mark.parametrize("M,N", [(256, 256 * 112), (200, 256 * 112 - 40)])
+def test_mmq_q4k_tail_split(M, N):
+    """The default plan on 152 SMs: 224 tiles of 256 with 48 superblocks of K run as 152 whole
+    tiles, then the last wave's 72 tiles split in two (144 half tiles).  Checked against the
+    oracle on the first and last tiles (a whole tile and a split one), against the same call run
+    unsplit, for reproducibility, and for the split scratch being written and its counters left
+    at zero."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("the tail split is sized for 152 SMs")
+    K = 48 * 256
+    w, wr = weights("q4k", N, K, seed=44)
+    codes, scales = q8(synth.activations(M, K, seed=45))
+    c, d = q8_host(codes, scales)
+    r = dev(synth.residual(M, N, seed=46))
+    base = 2 * (K * 512 + (K // 512) * 8192)
+    full = qk.mmq_workspace_bytes(M, N, K)
+    assert full == base + 72 * 2 * 128 * 256 * 4 + 72 * 4           # the plan's tail scratch
+    ws = torch.full((full,), 0xAB, dtype=torch.uint8, device="cuda")
+    qk.error_flags(clear=True)
+    y1 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws, tile=256)
+    torch.cuda.synchronize()
+    assert int((ws[base:base + 4096] != 0xAB).sum()) > 0              # partial tiles written
+    y2 = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws, tile=256, pdl=True)
+    yu = qk.mmq_q4k(wr, codes, scales, N, K, residual=r, workspace=ws[:base], tile=256)
+    torch.cuda.synchronize()
+    assert qk.error_flags(clear=True) == 0
+    assert torch.equal(y1, y2)
+    assert torch.count_nonzero(ws[full - 72 * 4:]).item() == 0
+    r_np = r.cpu().numpy()
+    for lo in (0, N - 40):
+        hi = lo + 40
+        y_ref, ab = oracle.gemm(oracle.Q4_K, w, N, K, c, d, residual=r_np, rows=(lo, hi))
+        check(y1.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"tail-split rows {lo}")
+        check(yu.cpu().numpy()[:, lo:hi], y_ref, ab, r_np[:, lo:hi], what=f"unsplit rows {lo}")
 
 
 def _f16_bytes(v):
