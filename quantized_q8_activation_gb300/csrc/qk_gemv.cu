@@ -64,11 +64,14 @@ namespace {
 #ifndef QK_GEMV_MINB_FUSED
 #define QK_GEMV_MINB_FUSED 1
 #endif
+#ifndef QK_GEMV_MINB_SMALL_M
+#define QK_GEMV_MINB_SMALL_M 1         // CTAs per SM the q8_1-input kernels for M <= 2 are compiled for
+#endif
 template <int M, bool FUSED>
 struct Cfg {
     static constexpr int warps = M > 2 ? QK_GEMV_WARPS : FUSED ? QK_GEMV_WARPS_FUSED : QK_GEMV_WARPS_SMALL_M;
     static constexpr int threads = warps * 32;
-    static constexpr int minb = (M <= 2 && FUSED) ? QK_GEMV_MINB_FUSED : 1;
+    static constexpr int minb = M <= 2 ? (FUSED ? QK_GEMV_MINB_FUSED : QK_GEMV_MINB_SMALL_M) : 1;
 };
 constexpr int kCtasPerSm = QK_GEMV_CTAS_PER_SM;
 constexpr int kRowsPerItem = 2;                                     // rows a lane works on at once
