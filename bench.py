@@ -119,15 +119,15 @@ def gemm_fused(policy: str, cfg, gemm) -> bool:
 # kernel's launches in one step) from one ncu capture of the command in the named profile.
 # Valid only while the kernel sources are the ones the counters were taken on.
 TRAFFIC: dict = {
-    (0, "gemv_q4k"): {"bytes_per_launch": 9464527, "digest": "ab63c82967201baa",
+    (0, "gemv_q4k"): {"bytes_per_launch": 9464478, "digest": "deacd4a9d539f614",
                       "profile": "profiles/dram_traffic_per_launch.md"},
-    (1, "gemv_q4k"): {"bytes_per_launch": 30709818, "digest": "ab63c82967201baa",
+    (1, "gemv_q4k"): {"bytes_per_launch": 30709798, "digest": "deacd4a9d539f614",
                       "profile": "profiles/launches_llama3_8b_decode_layer.md"},
-    (2, "gemv_q6k"): {"bytes_per_launch": 434216499, "digest": "ab63c82967201baa",
+    (2, "gemv_q6k"): {"bytes_per_launch": 434187136, "digest": "deacd4a9d539f614",
                       "profile": "profiles/gemv_q6k_head_128256x4096.md"},
-    (3, "gemv_q6k"): {"bytes_per_launch": 435280896, "digest": "ab63c82967201baa",
+    (3, "gemv_q6k"): {"bytes_per_launch": 435365376, "digest": "deacd4a9d539f614",
                       "profile": "profiles/gemv_q6k_head_m4_128256x4096.md"},
-    (4, "mmq_q4k"): {"bytes_per_launch": 289731232, "digest": "4fad9d23e5b83fae",
+    (4, "mmq_q4k"): {"bytes_per_launch": 291980608, "digest": "98dd40edc013c482",
                      "profile": "profiles/launches_qwen2_7b_prefill_mmq.md"},
 }
 
