@@ -284,19 +284,29 @@ __global__ void __launch_bounds__(256) mmq_prep_kernel(const int8_t *__restrict_
     if (sb == 0 && mt == 0)                      // the split-K tile counters of this call start at zero
         for (int i = threadIdx.x; i < ncnt; i += 256) cnt[i] = 0;
     const int nit = (int)(K >> 5), B = (int)(K >> 8), nmin = (B + 1) >> 1;
-#pragma unroll 1
+    // every load of the thread's four blocks is issued before any of them is used (the loads of one
+    // block at a time left the kernel waiting on DRAM four times over)
+    uint4 ra0[4], ra1[4];
+    uint32_t rd[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int q = threadIdx.x + 256 * i;
+        const int64_t m = (int64_t)mt * BM + (q >> 3);
+        ra0[i] = ra1[i] = make_uint4(0, 0, 0, 0);
+        rd[i] = 0;
+        if (m < M) {
+            const int8_t *src = codes + m * K + sb * 256 + 32 * (q & 7);
+            ra0[i] = *reinterpret_cast<const uint4 *>(src);
+            ra1[i] = *reinterpret_cast<const uint4 *>(src + 16);
+            rd[i] = *reinterpret_cast<const uint32_t *>(scales + m * (K >> 5) + 8 * sb + (q & 7)) & 0xffffu;
+        }
+    }
+#pragma unroll
     for (int i = 0; i < 4; i++) {
         const int q = threadIdx.x + 256 * i;
         const int row = q >> 3, j = q & 7;
-        const int64_t m = (int64_t)mt * BM + row;
-        uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
-        uint32_t dbits = 0;
-        if (m < M) {
-            const int8_t *src = codes + m * K + sb * 256 + 32 * j;
-            a0 = *reinterpret_cast<const uint4 *>(src);
-            a1 = *reinterpret_cast<const uint4 *>(src + 16);
-            dbits = *reinterpret_cast<const uint32_t *>(scales + m * (K >> 5) + 8 * sb + j) & 0xffffu;
-        }
+        const uint4 a0 = ra0[i], a1 = ra1[i];
+        const uint32_t dbits = rd[i];
         const __half dah = __ushort_as_half((unsigned short)dbits);
         const __half2 d2 = __halves2half2(dah, dah);
         // value limits of the f16 operands: d_a * 127 (the block's largest |x|) at most 32000 when the
