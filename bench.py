@@ -103,6 +103,8 @@ def int_ops(cfg) -> int:
 def gemm_fused(policy: str, cfg, gemm) -> bool:
     if cfg["kind"] == "chain":                      # only attn-out reads an f32 activation the chain does not make
         return gemm[0] == "attn_out"
+    if cfg["kind"] == "mmq":                        # prefill: the q8_1 quantization inside the MMQ call
+        return policy != "unfused"
     """Decode activation path of one GEMM: q8_1 quantization inside the GEMV ("fused")
     or a quantize kernel before its consumers.  "auto" quantizes inside the GEMV when the
     activation is small (M*K <= 4096: one float4 or two per thread), where saving the
@@ -136,6 +138,9 @@ def front_end_desc(front_end: str, cfg) -> str:
     if cfg["kind"] == "chain":
         return ("producers: qk_rmsnorm_q8_1 -> qkv; attn_out quantizes its f32 input inside the GEMV; "
                 "qk_rmsnorm_q8_1 -> gate_up; qk_swiglu_q8_1 -> down")
+    if cfg["kind"] == "mmq":
+        return ("q8_1 quantization inside each MMQ call (qk_mmq_*_f32)" if front_end != "unfused"
+                else "qk_quantize_q8_1 kernel per activation, then the q8_1 MMQ entry points")
     if cfg["kind"] != "gemv":
         return "qk_quantize_q8_1 kernel per activation"
     if front_end == "batched":
@@ -311,7 +316,14 @@ class Workload:
         else:
             codes, scales = self.q8[s]
             kw = dict(residual=self.r.get(name), y=self.y[name], pdl=pdl, stream=stream)
-            if cfg["kind"] == "mmq":
+            if cfg["kind"] == "mmq" and fused:
+                # the f32 activation quantized inside the call (the q8_1 buffers are not touched)
+                plane = self.plane[copy].get(name)
+                if q == "q4k":
+                    qk.mmq_q4k_f32(self.w[copy][name], self.x[s], N, K, workspace=self.ws, plane=plane, **kw)
+                else:
+                    qk.mmq_q6k_f32(self.w[copy][name], self.x[s], N, K, workspace=self.ws, **kw)
+            elif cfg["kind"] == "mmq":
                 ws = self.ws
                 plane = self.plane[copy].get(name)
                 if plane is not None:
@@ -371,7 +383,7 @@ class Workload:
     def kernel_key(self, gemm, fused: bool) -> str:
         q = gemm[1]
         if self.cfg["kind"] == "mmq":
-            return "mmq_q4k" if q == "q4k" else "mmq_q6k"
+            return ("mmq_q4k" if q == "q4k" else "mmq_q6k") + ("_f32" if fused else "")
         return "gemv_" + q + ("_f32" if fused else "")
 
     def launches_per_step(self, front_end: str = "auto") -> int:

@@ -472,6 +472,35 @@ int qk_mmq_q4k_plane(const void *w, const void *plane, const int8_t *codes, cons
                      void *workspace, size_t workspace_bytes,
                      unsigned flags, void *stream);
 
+/* ============================================== MMQ from f32 activations
+ * The prefill contraction with the q8_1 quantization of the activation done
+ * inside the call (the GEMV's _f32 entry points do the same for decode): the
+ * activation is quantized once per call, as minfer "15 . The CUDA backend"
+ * sec. 2.3 prescribes, by the kernel that expands it into the workspace, so
+ * the separate quantize launch and the q8_1 round trip through memory go.
+ * The codes and binary16 scales are those of qk_quantize_q8_1, bit for bit
+ * (the same block quantizer); they are not stored.  The results are
+ * therefore bit-identical to qk_quantize_q8_1 followed by qk_mmq_q4k /
+ * qk_mmq_q4k_plane / qk_mmq_q6k on the same arguments.
+ *   x: device f32 activation rows, row i at x + i * ldx, ldx >= K, 16-byte
+ *      aligned with ldx % 4 == 0; must not overlap y or the workspace.
+ *   plane (qk_mmq_q4k_f32 only): a min-operand plane (qk_q4k_min_plane) or
+ *      NULL for none.
+ * Everything else (shapes, value limits, workspace, flags, errors) as for
+ * qk_mmq_q4k / qk_mmq_q6k; QK_E_NULL for a NULL x.
+ */
+int qk_mmq_q4k_f32(const void *w, const void *plane, const float *x, int64_t ldx,
+                   int64_t M, int64_t N, int64_t K,
+                   const float *residual, float *y,
+                   void *workspace, size_t workspace_bytes,
+                   unsigned flags, void *stream);
+
+int qk_mmq_q6k_f32(const void *w, const float *x, int64_t ldx,
+                   int64_t M, int64_t N, int64_t K,
+                   const float *residual, float *y,
+                   void *workspace, size_t workspace_bytes,
+                   unsigned flags, void *stream);
+
 /* ================================================ MMQ without a workspace
  * The pages have no counterpart of this entry point: it is a convenience of
  * this library for callers that cannot supply a device workspace (a host

@@ -56,7 +56,7 @@ EXPORTS = ["qk_version", "qk_status_string", "qk_q8_1_bytes", "qk_quantize_q8_1"
            "qk_gemv_q5k_f32", "qk_gemv_q8_0", "qk_gemv_q8_0_f32", "qk_gemv_q2k", "qk_gemv_q3k",
            "qk_gemv_q2k_f32", "qk_gemv_q3k_f32",
            "qk_mmq_workspace_bytes", "qk_mmq_q4k", "qk_mmq_q6k", "qk_mmq_q4k_noalloc", "qk_error_flags",
-           "qk_q4k_min_plane_bytes", "qk_q4k_min_plane", "qk_mmq_q4k_plane",
+           "qk_q4k_min_plane_bytes", "qk_q4k_min_plane", "qk_mmq_q4k_plane", "qk_mmq_q4k_f32", "qk_mmq_q6k_f32",
            "qk_rmsnorm_q8_1", "qk_swiglu_q8_1",
            # include/qk_peak.h (measurement)
            "qk_peak_mma_s8", "qk_peak_tcgen05_f16"]
@@ -116,6 +116,8 @@ def lib() -> ctypes.CDLL:
             L.qk_q4k_min_plane_bytes.argtypes = [i64, i64, szp]
             L.qk_q4k_min_plane.argtypes = [p, i64, i64, p, ctypes.c_size_t, p]
             L.qk_mmq_q4k_plane.argtypes = [p, p, p, p, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
+            L.qk_mmq_q4k_f32.argtypes = [p, p, p, i64, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
+            L.qk_mmq_q6k_f32.argtypes = [p, p, i64, i64, i64, i64, p, p, p, ctypes.c_size_t, u, p]
             L.qk_rmsnorm_q8_1.argtypes = [p, i64, p, p, ctypes.c_float, i64, i64, p, p, p, p, u, p]
             L.qk_swiglu_q8_1.argtypes = [p, i64, i64, i64, p, p, p, u, p]
             L.qk_mmq_q4k_noalloc.argtypes = [p, p, p, i64, i64, i64, p, p, u, p]
@@ -416,6 +418,43 @@ def mmq_q4k_plane(w, plane, codes, scales, N, K, residual=None, y=None, workspac
     _cuda(plane, "plane")
     return _mmq("qk_mmq_q4k_plane", w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile, plane,
                 split_k)
+
+
+def mmq_q4k_f32(w, x, N, K, residual=None, y=None, workspace=None, plane=None, pdl=False, stream=None, tile=None,
+                split_k=False):
+    """mmq_q4k from the f32 activation x [M][K] (row pitch x.stride(0)): the q8_1 quantization is done
+    inside the call, bit-identical to quantize_q8_1 + mmq_q4k (or mmq_q4k_plane with a plane)."""
+    return _mmq_f32("qk_mmq_q4k_f32", w, x, N, K, residual, y, workspace, pdl, stream, tile, plane, split_k)
+
+
+def mmq_q6k_f32(w, x, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None, tile=None):
+    """mmq_q6k from the f32 activation x [M][K] (quantized inside the call, as mmq_q4k_f32)."""
+    return _mmq_f32("qk_mmq_q6k_f32", w, x, N, K, residual, y, workspace, pdl, stream, tile, None, False)
+
+
+def _mmq_f32(fn, w, x, N, K, residual, y, workspace, pdl, stream, tile, plane, split_k):
+    _cuda(w, "w")
+    if x.dtype != torch.float32 or x.dim() != 2 or not x.is_cuda or x.stride(1) != 1:
+        raise ValueError("x must be a float32 [M][K] CUDA tensor with unit stride along K (rows may be strided)")
+    if plane is not None:
+        _cuda(plane, "plane")
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    need = mmq_workspace_bytes(M, N, K)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    flags = (LAUNCH_PDL if pdl else 0) | {None: 0, 256: MMQ_TILE_256, 192: MMQ_TILE_192, 128: MMQ_TILE_128}[tile]
+    flags |= MMQ_SPLIT_K if split_k else 0
+    tail = (M, N, K, _p(residual), y.data_ptr(), _p(workspace), wsb, flags, _stream(stream))
+    with _on(x):
+        if fn == "qk_mmq_q4k_f32":
+            st = lib().qk_mmq_q4k_f32(w.data_ptr(), _p(plane), x.data_ptr(), x.stride(0) if M > 1 else K, *tail)
+        else:
+            st = lib().qk_mmq_q6k_f32(w.data_ptr(), x.data_ptr(), x.stride(0) if M > 1 else K, *tail)
+    _check(st, fn)
+    return y
 
 
 def _mmq(fn, w, codes, scales, N, K, residual, y, workspace, pdl, stream, tile=None, plane=None, split_k=False):

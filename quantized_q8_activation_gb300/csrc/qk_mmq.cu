@@ -345,6 +345,66 @@ __global__ void __launch_bounds__(256) mmq_prep_kernel(const int8_t *__restrict_
     }
 }
 
+// The prep of the f32 entry points (qk_mmq_q4k_f32, qk_mmq_q6k_f32): the f32 activation is quantized
+// to q8_1 on the way, by the library's block quantizer (the codes and binary16 scales of
+// qk_quantize_q8_1, bit for bit; they are not stored), and expanded as mmq_prep_kernel does.  Grid
+// (K/32, M-tiles): CTA (bc, mt) takes 32-value block column bc (K stage bc) of the M-tile's 128 rows,
+// eight lanes a row and four values a lane, four passes of 32 rows.
+__global__ void __launch_bounds__(256) mmq_prep_f32_kernel(const float *__restrict__ x, int64_t ldx, int64_t M,
+                                                           int64_t K, uint8_t *__restrict__ wsA,
+                                                           uint8_t *__restrict__ wsS, unsigned *__restrict__ cnt,
+                                                           int ncnt)
+{
+    qk::pdl_launch_dependents();
+    const int bc = blockIdx.x, mt = blockIdx.y, sb = bc >> 3, j = bc & 7;
+    const int sub = threadIdx.x & 7;
+    const int nit = (int)(K >> 5), B = (int)(K >> 8), nmin = (B + 1) >> 1;
+    qk::pdl_wait();                              // x may come from the previous kernel
+    if (bc == 0 && mt == 0)                      // the split-K tile counters of this call start at zero
+        for (int i = threadIdx.x; i < ncnt; i += 256) cnt[i] = 0;
+    float4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int64_t m = (int64_t)mt * BM + ((threadIdx.x + 256 * i) >> 3);
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m < M) v[i] = *reinterpret_cast<const float4 *>(x + m * ldx + 32 * bc + 4 * sub);
+    }
+    uint8_t *tA = wsA + ((size_t)mt * nit + bc) * ABLOCK;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int row = (threadIdx.x + 256 * i) >> 3;
+        float d;
+        int sum;
+        const uint32_t packed = qk::q81_quant8(v[i], d, sum);      // rows past M: d = 0, codes 0
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        const __half dah = qk::f16_sat(d);                         // the stored q8_1 scale
+        const __half2 d2 = __halves2half2(dah, dah);
+        flag_range(__half2float(dah) * 127.0f > (wsS ? 32000.0f : 65000.0f));
+        uint32_t hi01, lo01, hi23, lo23;
+        conv_a(packed, d2, hi01, lo01, hi23, lo23);
+        // values 4 sub .. 4 sub + 3 of the stage: half (sub & 1) of 16-byte chunk sub / 2 of the row
+        const uint32_t off = sw64(row, sub >> 1) + 8 * (sub & 1);
+        *reinterpret_cast<uint2 *>(tA + off) = make_uint2(hi01, hi23);
+        *reinterpret_cast<uint2 *>(tA + ATILE + off) = make_uint2(lo01, lo23);
+        if (wsS && sub == 0) {
+            // the block's source sum S = d_a * sum(q_a) / 16 as S_hi + S_lo, placed as mmq_prep_kernel does
+            const float S = __half2float(dah) * (float)sum * kSScale;
+            const __half sh = __float2half_rn(S);
+            const __half sl = __float2half_rn(S - __half2float(sh));
+            uint8_t *tS = wsS + ((size_t)mt * nmin + (sb >> 1)) * SBLK;
+            const int e = sb & 1;
+            *reinterpret_cast<__half *>(tS + sw64(row, e) + 2 * j) = sh;
+            *reinterpret_cast<__half *>(tS + sw64(row, 2 + e) + 2 * j) = sl;
+            if (e == 0 && sb + 1 == B) {         // odd B: the last tile's second superblock does not exist
+                *reinterpret_cast<__half *>(tS + sw64(row, 1) + 2 * j) = __ushort_as_half(0);
+                *reinterpret_cast<__half *>(tS + sw64(row, 3) + 2 * j) = __ushort_as_half(0);
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------- main kernel
 
 // Converter state of one half row across K stages.  Q4_K: its 16 code bytes of the current
@@ -1473,17 +1533,21 @@ int launch_mmq(const MmqArgs &args, const MmqMaps &maps, int64_t tiles, cudaStre
 // bytes of the Q4_K min-operand plane of an N x K weight: 64 per row and pair of superblocks
 size_t plane_bytes(int64_t N, int64_t K) { return (size_t)N * (size_t)((K / 256 + 1) / 2) * 64; }
 
-int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const void *scales, int64_t M, int64_t N,
-        int64_t K, const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,
-        void *stream)
+// The activation comes as q8_1 (codes, scales) or, for the f32 entry points, as f32 rows x with row
+// pitch ldx (quantized inside the prep kernel; codes and scales are then null).
+int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const void *scales, const float *x,
+        int64_t ldx, int64_t M, int64_t N, int64_t K, const float *residual, float *y, void *workspace,
+        size_t workspace_bytes, unsigned flags, void *stream)
 {
     // TMA coordinates are signed 32-bit: rows and bytes of a row stay below 2^31
     if (M < 0 || N < 1 || N > 0x7fffffffLL || K < 256 || K % 256 != 0 || M > 0x7fffffffLL || K > 0x7fffffffLL)
         return QK_E_SHAPE;
+    if (x && (ldx < K || ldx > ((int64_t)1 << 40))) return QK_E_SHAPE;
     if (M == 0) return QK_OK;
-    if (!w || !codes || !scales || !y || !workspace) return QK_E_NULL;
+    if (!w || (!x && (!codes || !scales)) || !y || !workspace) return QK_E_NULL;
     if (!qk::aligned(w, 16) || !qk::aligned(codes, 16) || !qk::aligned(scales, 16) || !qk::aligned(y, 4) ||
-        (residual && !qk::aligned(residual, 4)) || !qk::aligned(workspace, 256) || !qk::aligned(plane, 16))
+        (residual && !qk::aligned(residual, 4)) || !qk::aligned(workspace, 256) || !qk::aligned(plane, 16) ||
+        !qk::aligned(x, 16) || (x && ldx % 4 != 0))
         return QK_E_ALIGN;
     const size_t need = ws_bytes(M, K);
     if (workspace_bytes < need) return QK_E_WORKSPACE;
@@ -1505,6 +1569,9 @@ int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const voi
     size_t wbytes = 0;
     qk_repacked_bytes(qt, N, K, &wbytes);
     const size_t ybytes = (size_t)M * N * 4, cbytes = (size_t)M * K, sbytes = (size_t)M * (K / 32) * 4;
+    const size_t xbytes = x ? ((size_t)(M - 1) * (size_t)ldx + (size_t)K) * 4 : 0;
+    if (x && (qk::overlaps(y, ybytes, x, xbytes) || qk::overlaps(workspace, used, x, xbytes)))
+        return QK_E_ALIAS;
     if (qk::overlaps(y, ybytes, w, wbytes) || qk::overlaps(y, ybytes, codes, cbytes) ||
         qk::overlaps(y, ybytes, scales, sbytes) || (residual != y && qk::overlaps(y, ybytes, residual, ybytes)) ||
         qk::overlaps(workspace, used, w, wbytes) || qk::overlaps(workspace, used, codes, cbytes) ||
@@ -1561,9 +1628,12 @@ int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const voi
         part = reinterpret_cast<float *>(wsA + need);
         cnt = reinterpret_cast<unsigned *>(wsA + need + (size_t)plan.tail * 2 * BM * BN * 4);
     }
-    int st = qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, cs,
-                        (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA, wsS,
-                        cnt, plan.split > 1 ? (int)plan.tail : 0);
+    const int ncnt = plan.split > 1 ? (int)plan.tail : 0;
+    int st = x ? qk::launch(mmq_prep_f32_kernel, dim3((unsigned)(K / 32), (unsigned)gx), dim3(256), 0, cs,
+                            (flags & QK_LAUNCH_PDL) != 0, x, ldx, M, K, wsA, wsS, cnt, ncnt)
+               : qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, cs,
+                            (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA,
+                            wsS, cnt, ncnt);
     if (st != QK_OK) return st;
     MmqArgs args{};
     args.wsA = wsA;
@@ -1625,8 +1695,8 @@ extern "C" int qk_mmq_q4k(const void *w, const int8_t *codes, const void *scales
                           const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,
                           void *stream)
 {
-    return mmq(QK_TYPE_Q4_K, w, nullptr, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags,
-               stream);
+    return mmq(QK_TYPE_Q4_K, w, nullptr, codes, scales, nullptr, 0, M, N, K, residual, y, workspace,
+               workspace_bytes, flags, stream);
 }
 
 extern "C" int qk_q4k_min_plane_bytes(int64_t N, int64_t K, size_t *bytes)
@@ -1660,14 +1730,32 @@ extern "C" int qk_mmq_q4k_plane(const void *w, const void *plane, const int8_t *
                                 size_t workspace_bytes, unsigned flags, void *stream)
 {
     if (M > 0 && !plane) return QK_E_NULL;
-    return mmq(QK_TYPE_Q4_K, w, plane, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags,
-               stream);
+    return mmq(QK_TYPE_Q4_K, w, plane, codes, scales, nullptr, 0, M, N, K, residual, y, workspace, workspace_bytes,
+               flags, stream);
+}
+
+extern "C" int qk_mmq_q4k_f32(const void *w, const void *plane, const float *x, int64_t ldx, int64_t M, int64_t N,
+                              int64_t K, const float *residual, float *y, void *workspace, size_t workspace_bytes,
+                              unsigned flags, void *stream)
+{
+    if (M > 0 && !x) return QK_E_NULL;
+    return mmq(QK_TYPE_Q4_K, w, plane, nullptr, nullptr, x, ldx, M, N, K, residual, y, workspace, workspace_bytes,
+               flags, stream);
+}
+
+extern "C" int qk_mmq_q6k_f32(const void *w, const float *x, int64_t ldx, int64_t M, int64_t N, int64_t K,
+                              const float *residual, float *y, void *workspace, size_t workspace_bytes,
+                              unsigned flags, void *stream)
+{
+    if (M > 0 && !x) return QK_E_NULL;
+    return mmq(QK_TYPE_Q6_K, w, nullptr, nullptr, nullptr, x, ldx, M, N, K, residual, y, workspace, workspace_bytes,
+               flags, stream);
 }
 
 extern "C" int qk_mmq_q6k(const void *w, const int8_t *codes, const void *scales, int64_t M, int64_t N, int64_t K,
                           const float *residual, float *y, void *workspace, size_t workspace_bytes, unsigned flags,
                           void *stream)
 {
-    return mmq(QK_TYPE_Q6_K, w, nullptr, codes, scales, M, N, K, residual, y, workspace, workspace_bytes, flags,
-               stream);
+    return mmq(QK_TYPE_Q6_K, w, nullptr, codes, scales, nullptr, 0, M, N, K, residual, y, workspace,
+               workspace_bytes, flags, stream);
 }

@@ -185,6 +185,21 @@ def test_min_plane_size_and_rejects(L):
     assert g(w, ws, c, s, 16, 64, 512, None, y, ws, wsn, 0, None) == E_ALIAS  # plane over the workspace
 
 
+@pytest.mark.parametrize("fn", ["qk_mmq_q4k_f32", "qk_mmq_q6k_f32"])
+def test_mmq_f32_rejects(L, fn):
+    f = getattr(L, fn)
+    w, x, y, ws = P, P + 0x10000000, P + 0x30000000, P + 0x40000000
+    need = qk.mmq_workspace_bytes(16, 64, 256)
+    pre = (w, None) if fn == "qk_mmq_q4k_f32" else (w,)
+    assert f(*pre, x, 256, 0, 64, 256, None, y, None, 0, 0, None) == 0                 # M = 0: nothing to do
+    assert f(*pre, None, 256, 16, 64, 256, None, y, ws, need, 0, None) == E_NULL
+    assert f(*pre, x, 128, 16, 64, 256, None, y, ws, need, 0, None) == E_SHAPE         # ldx < K
+    assert f(*pre, x + 4, 256, 16, 64, 256, None, y, ws, need, 0, None) == E_ALIGN     # x not 16-byte aligned
+    assert f(*pre, x, 258, 16, 64, 256, None, y, ws, need, 0, None) == E_ALIGN         # ldx % 4 != 0
+    assert f(*pre, y, 256, 16, 64, 256, None, y, ws, need, 0, None) == E_ALIAS         # x over y
+    assert f(*pre, ws, 256, 16, 64, 256, None, y, ws, need, 0, None) == E_ALIAS        # x over the workspace
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     with pytest.raises(ValueError):

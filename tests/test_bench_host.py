@@ -5,10 +5,13 @@ import bench
 def test_launches_per_step_match_the_ncu_launch_lists():
     # counts seen in the ncu launch lists of the same workloads (profiles/launches_*.md,
     # profiles/dram_traffic_per_launch.md): decode layer 5 (quantize only in front of down),
-    # prefill 12 (quantize + prep + main per GEMM), M = 4 mix 10 (a quantize per activation)
+    # prefill 8 (prep with the quantizer inside + main per GEMM; 12 with a quantize kernel per
+    # GEMM), M = 4 mix 10 (a quantize per activation)
     assert bench.launches_per_step(bench.CONFIGS[1]) == 5
-    assert bench.launches_per_step(bench.CONFIGS[4]) == 12
-    assert bench.launches_per_step(bench.CONFIGS[5]) == 12
+    assert bench.launches_per_step(bench.CONFIGS[4]) == 8
+    assert bench.launches_per_step(bench.CONFIGS[5]) == 8
+    assert bench.launches_per_step(bench.CONFIGS[4], "unfused") == 12
+    assert bench.launches_per_step(bench.CONFIGS[4], "batched") == 8
     assert bench.launches_per_step(bench.CONFIGS[3]) == 10
     assert bench.launches_per_step(bench.CONFIGS[2]) == 1
     assert bench.launches_per_step(bench.CONFIGS[6]) == 7
