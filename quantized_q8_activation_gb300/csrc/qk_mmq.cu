@@ -269,77 +269,68 @@ __device__ __forceinline__ void sts128(uint8_t *base, uint32_t off, uint32_t x, 
 }
 
 // ------------------------------------------------------------- prep kernel
-// CTA (superblock sb, M-tile mt), 256 threads, 4 items each: item (row, j) is
-// the 32-value q8_1 block j of superblock sb of activation row 128 mt + row.
-// It writes the block's 32 (A_hi, A_lo) pairs into row `row` of the stage
-// block of K stage 8 sb + j; rows past M are written as zeros.
+// Grid (K/32, M-tiles): CTA (bc, mt) takes 32-value block column bc (K stage bc) of the M-tile's
+// 128 rows, eight lanes a row (four codes each), four passes of 32 rows; every load of the four
+// passes is issued before the first conversion.  Each lane writes its four (A_hi, A_lo) pairs into
+// row `row` of the stage block; rows past M are written as zeros.
 __global__ void __launch_bounds__(256) mmq_prep_kernel(const int8_t *__restrict__ codes,
                                                        const __half2 *__restrict__ scales, int64_t M, int64_t K,
                                                        uint8_t *__restrict__ wsA, uint8_t *__restrict__ wsS,
                                                        unsigned *__restrict__ cnt, int ncnt)
 {
     qk::pdl_launch_dependents();
-    qk::pdl_wait();                              // codes may come from the previous kernel
-    const int sb = blockIdx.x, mt = blockIdx.y;
-    if (sb == 0 && mt == 0)                      // the split-K tile counters of this call start at zero
-        for (int i = threadIdx.x; i < ncnt; i += 256) cnt[i] = 0;
+    const int bc = blockIdx.x, mt = blockIdx.y, sb = bc >> 3, j = bc & 7;
+    const int sub = threadIdx.x & 7;
     const int nit = (int)(K >> 5), B = (int)(K >> 8), nmin = (B + 1) >> 1;
-    // every load of the thread's four blocks is issued before any of them is used (the loads of one
-    // block at a time left the kernel waiting on DRAM four times over)
-    uint4 ra0[4], ra1[4];
-    uint32_t rd[4];
+    qk::pdl_wait();                              // codes may come from the previous kernel
+    if (bc == 0 && mt == 0)                      // the split-K tile counters of this call start at zero
+        for (int i = threadIdx.x; i < ncnt; i += 256) cnt[i] = 0;
+    uint32_t rc[4], rd[4];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        const int q = threadIdx.x + 256 * i;
-        const int64_t m = (int64_t)mt * BM + (q >> 3);
-        ra0[i] = ra1[i] = make_uint4(0, 0, 0, 0);
-        rd[i] = 0;
+        const int64_t m = (int64_t)mt * BM + ((threadIdx.x + 256 * i) >> 3);
+        rc[i] = rd[i] = 0;
         if (m < M) {
-            const int8_t *src = codes + m * K + sb * 256 + 32 * (q & 7);
-            ra0[i] = *reinterpret_cast<const uint4 *>(src);
-            ra1[i] = *reinterpret_cast<const uint4 *>(src + 16);
-            rd[i] = *reinterpret_cast<const uint32_t *>(scales + m * (K >> 5) + 8 * sb + (q & 7)) & 0xffffu;
+            rc[i] = *reinterpret_cast<const uint32_t *>(codes + m * K + 32 * bc + 4 * sub);
+            rd[i] = *reinterpret_cast<const uint32_t *>(scales + m * (K >> 5) + bc) & 0xffffu;
         }
     }
+    uint8_t *tA = wsA + ((size_t)mt * nit + bc) * ABLOCK;
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        const int q = threadIdx.x + 256 * i;
-        const int row = q >> 3, j = q & 7;
-        const uint4 a0 = ra0[i], a1 = ra1[i];
-        const uint32_t dbits = rd[i];
-        const __half dah = __ushort_as_half((unsigned short)dbits);
+        const int row = (threadIdx.x + 256 * i) >> 3;
+        const __half dah = __ushort_as_half((unsigned short)rd[i]);
         const __half2 d2 = __halves2half2(dah, dah);
         // value limits of the f16 operands: d_a * 127 (the block's largest |x|) at most 32000 when the
         // sums S / 16 are built (Q4_K), 65000 otherwise (Q6_K); beyond them the result is undefined
         flag_range(__half2float(dah) * 127.0f > (wsS ? 32000.0f : 65000.0f));
-        const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        uint8_t *tA = wsA + ((size_t)mt * nit + 8 * sb + j) * ABLOCK;
-#pragma unroll
-        for (int c = 0; c < 4; c++) {
-            uint32_t hi[4], lo[4];
-            conv_a(aw[2 * c], d2, hi[0], lo[0], hi[1], lo[1]);
-            conv_a(aw[2 * c + 1], d2, hi[2], lo[2], hi[3], lo[3]);
-            sts128(tA, sw64(row, c), hi[0], hi[1], hi[2], hi[3]);
-            sts128(tA + ATILE, sw64(row, c), lo[0], lo[1], lo[2], lo[3]);
-        }
+        uint32_t hi01, lo01, hi23, lo23;
+        conv_a(rc[i], d2, hi01, lo01, hi23, lo23);
+        // values 4 sub .. 4 sub + 3 of the stage: half (sub & 1) of 16-byte chunk sub / 2 of the row
+        const uint32_t off = sw64(row, sub >> 1) + 8 * (sub & 1);
+        *reinterpret_cast<uint2 *>(tA + off) = make_uint2(hi01, hi23);
+        *reinterpret_cast<uint2 *>(tA + ATILE + off) = make_uint2(lo01, lo23);
         if (wsS) {
             // the block's source sum S = d_a * sum(q_a), exact in binary32 (11 x 13 significant bits),
             // scaled by 2^-4 and split into f16 S_hi + S_lo (to 2^-22 of S): sub-block j of superblock
             // sb is column 8 (sb % 2) + j (S_hi) and 16 + 8 (sb % 2) + j (S_lo) of row `row` of the
             // sums tile sb / 2
-            int sum = 0;
-#pragma unroll
-            for (int w = 0; w < 8; w++) sum = __dp4a((int)aw[w], 0x01010101, sum);
-            const float S = __half2float(dah) * (float)sum * kSScale;
-            const __half sh = __float2half_rn(S);
-            const __half sl = __float2half_rn(S - __half2float(sh));
-            uint8_t *tS = wsS + ((size_t)mt * nmin + (sb >> 1)) * SBLK;
-            const int e = sb & 1;
-            *reinterpret_cast<__half *>(tS + sw64(row, e) + 2 * j) = sh;
-            *reinterpret_cast<__half *>(tS + sw64(row, 2 + e) + 2 * j) = sl;
-            if (e == 0 && sb + 1 == B) {         // odd B: the last tile's second superblock does not exist
-                *reinterpret_cast<__half *>(tS + sw64(row, 1) + 2 * j) = __ushort_as_half(0);
-                *reinterpret_cast<__half *>(tS + sw64(row, 3) + 2 * j) = __ushort_as_half(0);
+            int sum = __dp4a((int)rc[i], 0x01010101, 0);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            if (sub == 0) {
+                const float S = __half2float(dah) * (float)sum * kSScale;
+                const __half sh = __float2half_rn(S);
+                const __half sl = __float2half_rn(S - __half2float(sh));
+                uint8_t *tS = wsS + ((size_t)mt * nmin + (sb >> 1)) * SBLK;
+                const int e = sb & 1;
+                *reinterpret_cast<__half *>(tS + sw64(row, e) + 2 * j) = sh;
+                *reinterpret_cast<__half *>(tS + sw64(row, 2 + e) + 2 * j) = sl;
+                if (e == 0 && sb + 1 == B) {     // odd B: the last tile's second superblock does not exist
+                    *reinterpret_cast<__half *>(tS + sw64(row, 1) + 2 * j) = __ushort_as_half(0);
+                    *reinterpret_cast<__half *>(tS + sw64(row, 3) + 2 * j) = __ushort_as_half(0);
+                }
             }
         }
     }
@@ -1631,7 +1622,7 @@ int mmq(int qt, const void *w, const void *plane, const int8_t *codes, const voi
     const int ncnt = plan.split > 1 ? (int)plan.tail : 0;
     int st = x ? qk::launch(mmq_prep_f32_kernel, dim3((unsigned)(K / 32), (unsigned)gx), dim3(256), 0, cs,
                             (flags & QK_LAUNCH_PDL) != 0, x, ldx, M, K, wsA, wsS, cnt, ncnt)
-               : qk::launch(mmq_prep_kernel, dim3((unsigned)B, (unsigned)gx), dim3(256), 0, cs,
+               : qk::launch(mmq_prep_kernel, dim3((unsigned)(K / 32), (unsigned)gx), dim3(256), 0, cs,
                             (flags & QK_LAUNCH_PDL) != 0, codes, static_cast<const __half2 *>(scales), M, K, wsA,
                             wsS, cnt, ncnt);
     if (st != QK_OK) return st;
