@@ -101,15 +101,17 @@ def int_ops(cfg) -> int:
 
 
 def gemm_fused(policy: str, cfg, gemm) -> bool:
-    if cfg["kind"] == "chain":                      # only attn-out reads an f32 activation the chain does not make
+    """Activation path of one GEMM: q8_1 quantization inside the contraction ("fused")
+    or a quantize kernel before its consumers.  Decode: "auto" quantizes inside the GEMV
+    when the activation is small (M*K <= 4096: one float4 or two per thread), where
+    saving the extra kernel and dependency wins; larger activations use the quantize
+    kernel, since the in-GEMV front end repeats the quantization in every CTA.  Prefill:
+    the MMQ's prep kernel quantizes once per call, so every policy but "unfused" fuses.
+    The decode chain fuses only attn-out, the one f32 activation it does not produce."""
+    if cfg["kind"] == "chain":
         return gemm[0] == "attn_out"
-    if cfg["kind"] == "mmq":                        # prefill: the q8_1 quantization inside the MMQ call
+    if cfg["kind"] == "mmq":
         return policy != "unfused"
-    """Decode activation path of one GEMM: q8_1 quantization inside the GEMV ("fused")
-    or a quantize kernel before its consumers.  "auto" quantizes inside the GEMV when the
-    activation is small (M*K <= 4096: one float4 or two per thread), where saving the
-    extra kernel and dependency wins; larger activations use the quantize kernel, since
-    the in-GEMV front end repeats the quantization in every CTA."""
     if cfg["kind"] != "gemv":
         return False
     if policy == "auto":
@@ -129,8 +131,8 @@ TRAFFIC: dict = {
                       "profile": "profiles/gemv_q6k_head_128256x4096.md"},
     (3, "gemv_q6k"): {"bytes_per_launch": 435365376, "digest": "deacd4a9d539f614",
                       "profile": "profiles/gemv_q6k_head_m4_128256x4096.md"},
-    (4, "mmq_q4k"): {"bytes_per_launch": 291980608, "digest": "98dd40edc013c482",
-                     "profile": "profiles/launches_qwen2_7b_prefill_mmq.md"},
+    (4, "mmq_q4k_f32"): {"bytes_per_launch": 332174272, "digest": "7dc433405fca68ba",
+                         "profile": "profiles/launches_qwen2_7b_prefill_mmq.md"},
 }
 
 
@@ -831,7 +833,7 @@ def roofline(cfg, cfg_id, dom, dk, peaks_meas):
         # f16 tensor MMAs the kernel issues per algorithmic integer product: two (A_hi, A_lo against the exact
         # sc*q) plus the min term's K/32-deep contraction (3 MMAs per 16 sub-blocks, ~4.7 % more) for Q4_K;
         # three (hi/lo splits) for Q6_K
-        mma_per_product = (2.0 + 3.0 / 64.0) if dom == "mmq_q4k" else 3.0
+        mma_per_product = (2.0 + 3.0 / 64.0) if dom.startswith("mmq_q4k") else 3.0
         r = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
              "traffic": traffic, "kernel": dom, "algorithmic_ops_per_launch": dk["ops"] / n,
              "avg_launch_us": dk["avg_us"],

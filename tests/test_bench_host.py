@@ -35,3 +35,23 @@ def test_weight_bytes_of_the_headline_workloads():
     assert bench.weight_bytes(bench.CONFIGS[1]) == 122683392
     # Qwen2-7B prefill: 2 M sum(N K) integer ops
     assert bench.int_ops(bench.CONFIGS[4]) == 954556481536
+
+
+def test_mmq_roofline_counts_the_mmas_of_the_kernel_that_ran():
+    # Q4_K: A_hi and A_lo against the exact sc*q operand, plus the min term's 3 MMAs per 64
+    # products; Q6_K: three hi/lo products. The f32-input entry points run the same kernels.
+    dk = {"calls_per_step": 4, "ms_per_step": 1.0, "ops": 1e12, "avg_us": 250.0}
+    peaks = {"tcgen05_f16_tflops": 2000.0}
+    for key, per in (("mmq_q4k", 2.0 + 3.0 / 64.0), ("mmq_q4k_f32", 2.0 + 3.0 / 64.0),
+                     ("mmq_q6k", 3.0), ("mmq_q6k_f32", 3.0)):
+        r = bench.roofline(bench.CONFIGS[4], 4, key, dk, peaks)
+        assert r["f16_mma_per_integer_product"] == per
+        assert abs(r["issued_mma_utilisation"] - 1000.0 * per / 2000.0) < 1e-9
+
+
+def test_prefill_traffic_is_recorded_for_the_default_front_end():
+    # the bench's default prefill line runs the f32-input MMQ; its DRAM figure must be the one
+    # the ncu launch list of that kernel pair measured
+    fused = all(bench.gemm_fused("auto", bench.CONFIGS[4], g) for g in bench.CONFIGS[4]["gemms"])
+    assert fused
+    assert (4, "mmq_q4k_f32") in bench.TRAFFIC
