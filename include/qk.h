@@ -90,6 +90,25 @@ extern "C" {
 #define QK_MMQ_TILE_192 8u
 #define QK_MMQ_SPLIT_K 16u
 
+/*
+ * QK_GEMV_ROWS4 / QK_GEMV_ROWS2 (Q4_K and Q6_K GEMV, M >= 3): force items of
+ * four or of two weight rows.  An item is the slice of weight rows a warp
+ * takes through its shared-memory ring; with four rows one read of the
+ * staged activation serves four rows instead of two, which halves the
+ * activation traffic per weight byte where several activation rows make the
+ * GEMV bound by instruction issue and shared-memory reads.  By default four
+ * rows are taken for Q4_K when the groups of four rows still give every warp
+ * of the grid one group (N >= 4 * 12 warps * SMs) and the ring and the
+ * activation fit in shared memory; QK_GEMV_ROWS4 drops the first condition
+ * and also applies to Q6_K (measured slower there at M = 4: its four-row
+ * kernel runs 12 warps instead of 16).
+ * Results are the same within the stated bound either way (the reduction
+ * order is fixed for a given choice).  Setting both is QK_E_SHAPE for any
+ * GEMV call; the other GEMV formats and the MMQ calls ignore them otherwise.
+ */
+#define QK_GEMV_ROWS4 32u
+#define QK_GEMV_ROWS2 64u
+
 /* Library version (major*10000 + minor*100 + patch). */
 int qk_version(void);
 

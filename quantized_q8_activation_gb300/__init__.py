@@ -42,6 +42,8 @@ MMQ_TILE_256 = 2
 MMQ_TILE_128 = 4
 MMQ_TILE_192 = 8
 MMQ_SPLIT_K = 16
+GEMV_ROWS4 = 32
+GEMV_ROWS2 = 64
 
 ERR_TIMEOUT = 1     # error_flags(): a bounded in-kernel wait gave up
 ERR_RANGE = 2       # error_flags(): an MMQ input was outside the value limits (see include/qk.h)
@@ -274,7 +276,11 @@ def repack(qtype: int, gguf: torch.Tensor, N: int, K: int, out=None, stream=None
     return out
 
 
-def _gemv(fn, name, w, codes, scales, N, K, residual, y, pdl, stream):
+def _rows_flag(rows):
+    return {None: 0, 2: GEMV_ROWS2, 4: GEMV_ROWS4}[rows]
+
+
+def _gemv(fn, name, w, codes, scales, N, K, residual, y, pdl, stream, rows=None, flags=0):
     M = codes.shape[0]
     for t, n in ((w, "w"), (codes, "codes"), (scales, "scales")):
         _cuda(t, n)
@@ -285,42 +291,44 @@ def _gemv(fn, name, w, codes, scales, N, K, residual, y, pdl, stream):
         _cuda(residual, "residual")
     with _on(codes):
         st = fn(w.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, _p(residual), y.data_ptr(),
-                LAUNCH_PDL if pdl else 0, _stream(stream))
+                (LAUNCH_PDL if pdl else 0) | _rows_flag(rows) | flags, _stream(stream))
     _check(st, name)
     return y
 
 
-def gemv_q4k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
-    """y[M][N] = xhat . W^T (+ residual) over a repacked Q4_K weight, 1 <= M <= 8."""
-    return _gemv(lib().qk_gemv_q4k, "qk_gemv_q4k", w, codes, scales, N, K, residual, y, pdl, stream)
+def gemv_q4k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None, rows=None, flags=0):
+    """y[M][N] = xhat . W^T (+ residual) over a repacked Q4_K weight, 1 <= M <= 8.
+
+    rows=4 / rows=2 force items of four or two weight rows (QK_GEMV_ROWS4 / QK_GEMV_ROWS2, M >= 3)."""
+    return _gemv(lib().qk_gemv_q4k, "qk_gemv_q4k", w, codes, scales, N, K, residual, y, pdl, stream, rows, flags)
 
 
-def gemv_q6k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
-    """y[M][N] = xhat . W^T (+ residual) over a repacked Q6_K weight, 1 <= M <= 8."""
-    return _gemv(lib().qk_gemv_q6k, "qk_gemv_q6k", w, codes, scales, N, K, residual, y, pdl, stream)
+def gemv_q6k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None, rows=None, flags=0):
+    """y[M][N] = xhat . W^T (+ residual) over a repacked Q6_K weight, 1 <= M <= 8 (rows: as gemv_q4k)."""
+    return _gemv(lib().qk_gemv_q6k, "qk_gemv_q6k", w, codes, scales, N, K, residual, y, pdl, stream, rows, flags)
 
 
-def gemv_q5k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
+def gemv_q5k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None, flags=0):
     """GEMV over a repacked Q5_K weight, 1 <= M <= 8 activation rows."""
-    return _gemv(lib().qk_gemv_q5k, "qk_gemv_q5k", w, codes, scales, N, K, residual, y, pdl, stream)
+    return _gemv(lib().qk_gemv_q5k, "qk_gemv_q5k", w, codes, scales, N, K, residual, y, pdl, stream, None, flags)
 
 
-def gemv_q8_0(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
+def gemv_q8_0(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None, flags=0):
     """GEMV over a repacked Q8_0 weight, 1 <= M <= 8 activation rows."""
-    return _gemv(lib().qk_gemv_q8_0, "qk_gemv_q8_0", w, codes, scales, N, K, residual, y, pdl, stream)
+    return _gemv(lib().qk_gemv_q8_0, "qk_gemv_q8_0", w, codes, scales, N, K, residual, y, pdl, stream, None, flags)
 
 
-def gemv_q2k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
+def gemv_q2k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None, flags=0):
     """GEMV over a repacked Q2_K weight, 1 <= M <= 8 activation rows."""
-    return _gemv(lib().qk_gemv_q2k, "qk_gemv_q2k", w, codes, scales, N, K, residual, y, pdl, stream)
+    return _gemv(lib().qk_gemv_q2k, "qk_gemv_q2k", w, codes, scales, N, K, residual, y, pdl, stream, None, flags)
 
 
-def gemv_q3k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None):
+def gemv_q3k(w, codes, scales, N, K, residual=None, y=None, pdl=False, stream=None, flags=0):
     """GEMV over a repacked Q3_K weight, 1 <= M <= 8 activation rows."""
-    return _gemv(lib().qk_gemv_q3k, "qk_gemv_q3k", w, codes, scales, N, K, residual, y, pdl, stream)
+    return _gemv(lib().qk_gemv_q3k, "qk_gemv_q3k", w, codes, scales, N, K, residual, y, pdl, stream, None, flags)
 
 
-def _gemv_f32(fn, name, w, x, N, K, residual, y, codes_out, scales_out, pdl, stream):
+def _gemv_f32(fn, name, w, x, N, K, residual, y, codes_out, scales_out, pdl, stream, rows=None, flags=0):
     if x.dim() == 1:
         x = x.view(1, -1)
     if x.dtype != torch.float32 or not x.is_cuda or x.stride(1) != 1:
@@ -334,45 +342,52 @@ def _gemv_f32(fn, name, w, x, N, K, residual, y, codes_out, scales_out, pdl, str
         _cuda(residual, "residual")
     with _on(x):
         st = fn(w.data_ptr(), x.data_ptr(), x.stride(0) if M > 1 else K, M, N, K, _p(residual), y.data_ptr(),
-                _p(codes_out), _p(scales_out), LAUNCH_PDL if pdl else 0, _stream(stream))
+                _p(codes_out), _p(scales_out), (LAUNCH_PDL if pdl else 0) | _rows_flag(rows) | flags,
+                _stream(stream))
     _check(st, name)
     return y
 
 
-def gemv_q4k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+def gemv_q4k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None,
+                 rows=None, flags=0):
     """GEMV over a repacked Q4_K weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
     return _gemv_f32(lib().qk_gemv_q4k_f32, "qk_gemv_q4k_f32", w, x, N, K, residual, y, codes_out, scales_out,
-                     pdl, stream)
+                     pdl, stream, rows, flags)
 
 
-def gemv_q6k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+def gemv_q6k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None,
+                 rows=None, flags=0):
     """GEMV over a repacked Q6_K weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
     return _gemv_f32(lib().qk_gemv_q6k_f32, "qk_gemv_q6k_f32", w, x, N, K, residual, y, codes_out, scales_out,
-                     pdl, stream)
+                     pdl, stream, rows, flags)
 
 
-def gemv_q5k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+def gemv_q5k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None,
+                 rows=None, flags=0):
     """GEMV over a repacked Q5_K weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
     return _gemv_f32(lib().qk_gemv_q5k_f32, "qk_gemv_q5k_f32", w, x, N, K, residual, y, codes_out, scales_out,
-                     pdl, stream)
+                     pdl, stream, rows, flags)
 
 
-def gemv_q8_0_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+def gemv_q8_0_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None,
+                  rows=None, flags=0):
     """GEMV over a repacked Q8_0 weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
     return _gemv_f32(lib().qk_gemv_q8_0_f32, "qk_gemv_q8_0_f32", w, x, N, K, residual, y, codes_out, scales_out,
-                     pdl, stream)
+                     pdl, stream, rows, flags)
 
 
-def gemv_q2k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+def gemv_q2k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None,
+                 rows=None, flags=0):
     """GEMV over a repacked Q2_K weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
     return _gemv_f32(lib().qk_gemv_q2k_f32, "qk_gemv_q2k_f32", w, x, N, K, residual, y, codes_out, scales_out,
-                     pdl, stream)
+                     pdl, stream, rows, flags)
 
 
-def gemv_q3k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None):
+def gemv_q3k_f32(w, x, N, K, residual=None, y=None, codes_out=None, scales_out=None, pdl=False, stream=None,
+                 rows=None, flags=0):
     """GEMV over a repacked Q3_K weight from f32 activations (quantized inside the kernel), 1 <= M <= 8."""
     return _gemv_f32(lib().qk_gemv_q3k_f32, "qk_gemv_q3k_f32", w, x, N, K, residual, y, codes_out, scales_out,
-                     pdl, stream)
+                     pdl, stream, rows, flags)
 
 
 def mmq_q4k(w, codes, scales, N, K, residual=None, y=None, workspace=None, pdl=False, stream=None, tile=None,

@@ -3,10 +3,12 @@
 //
 // Design (GB300, HBM-bound):
 //  - Persistent grid, one CTA of 16 warps per SM.  Warp w of the grid owns
-//    output rows w, w + W, w + 2W, ... and walks each row in steps of up to
-//    8 superblocks (an "item"); in an item every lane copies 16-byte chunks
-//    so a warp covers 512 contiguous bytes of the repacked code plane per
-//    copy instruction (qk.h layout).
+//    groups of P output rows w, w + W, w + 2W, ... and walks each group in
+//    steps of up to 8 superblocks (an "item"); in an item every lane copies
+//    16-byte chunks so a warp covers 512 contiguous bytes of the repacked code
+//    plane per copy instruction (qk.h layout).  P = 2, or P = 4 for Q4_K with
+//    M >= 3 where the groups still fill the grid (12 warps per CTA): one read
+//    of the staged activation then serves four weight rows.
 //  - Each warp streams its items through a private ring of R shared-memory
 //    slots with cp.async (L2 -> SMEM, no register cost), R-1 items in flight
 //    while one is computed; no block-wide barrier inside the loop.  With
@@ -67,14 +69,31 @@ namespace {
 #ifndef QK_GEMV_MINB_SMALL_M
 #define QK_GEMV_MINB_SMALL_M 1         // CTAs per SM the q8_1-input kernels for M <= 2 are compiled for
 #endif
+// four-row items (Q4_K / Q6_K, M >= 3): warps per CTA and ring slots
+#ifndef QK_GEMV_P4_WARPS
+#define QK_GEMV_P4_WARPS 12
+#endif
+#ifndef QK_GEMV_P4_Q4_RING
+#define QK_GEMV_P4_Q4_RING 3
+#endif
+#ifndef QK_GEMV_P4_Q6_RING
+#define QK_GEMV_P4_Q6_RING 2
+#endif
 template <int M, bool FUSED>
 struct Cfg {
     static constexpr int warps = M > 2 ? QK_GEMV_WARPS : FUSED ? QK_GEMV_WARPS_FUSED : QK_GEMV_WARPS_SMALL_M;
     static constexpr int threads = warps * 32;
     static constexpr int minb = M <= 2 ? (FUSED ? QK_GEMV_MINB_FUSED : QK_GEMV_MINB_SMALL_M) : 1;
 };
+// launch shape of a kernel whose items hold PR weight rows
+template <int M, bool FUSED, int PR>
+struct KCfg {
+    static constexpr int warps = PR == 4 ? QK_GEMV_P4_WARPS : Cfg<M, FUSED>::warps;
+    static constexpr int threads = warps * 32;
+    static constexpr int minb = PR == 4 ? 1 : Cfg<M, FUSED>::minb;
+};
 constexpr int kCtasPerSm = QK_GEMV_CTAS_PER_SM;
-constexpr int kRowsPerItem = 2;                                     // rows a lane works on at once
+constexpr int kRowsPerItem = 2;                                     // rows a lane works on at once (default)
 constexpr int Q4_R = QK_GEMV_Q4_RING, Q4_SLOT = kRowsPerItem * (1024 + 128);       // codes + 8 metadata records
 constexpr int Q6_R = QK_GEMV_Q6_RING, Q6_SLOT = kRowsPerItem * (1024 + 512 + 128); // ql + qh + scales
 constexpr int Q5_R = QK_GEMV_Q4_RING, Q5_SLOT = kRowsPerItem * (1024 + 256 + 128);  // codes + fifth bits + metadata
@@ -293,14 +312,17 @@ struct ItemSeq {
     }
 };
 
-constexpr int P = kRowsPerItem;
 // ------------------------------------------------------------------ Q4_K
 // slot: [P][1024] code bytes of the step, then [P][8] 16-byte metadata records
 
 constexpr int Q4_CODES = 1024, Q4_META = 128;
 
-struct Q4Ops {
-    static constexpr int R = Q4_R, SLOT = Q4_SLOT;
+// PR weight rows per item: 2, or 4 for M >= 3 where one activation load then serves four rows
+template <int PR>
+struct Q4OpsT {
+    static constexpr int P = PR;
+    static constexpr int R = PR == 2 ? Q4_R : QK_GEMV_P4_Q4_RING, SLOT = PR * (Q4_CODES + Q4_META);
+    static_assert(R >= 2, "ring needs two slots at least");
     struct LaneConst {
         uint32_t selA, selB;
         int aoff[4];
@@ -394,6 +416,7 @@ struct Q4Ops {
         else stage_act_q4k<M, NT>(a.codes, a.scales, a.K, s_codes, s_side);
     }
 };
+using Q4Ops = Q4OpsT<2>;
 
 // ------------------------------------------------------------------ Q5_K
 // slot: [P][1024] code bytes of the step, [P][256] fifth-bit words, [P][8] 16-byte metadata records.
@@ -403,6 +426,7 @@ struct Q4Ops {
 constexpr int Q5_HB = 256;
 
 struct Q5Ops {
+    static constexpr int P = kRowsPerItem;
     static constexpr int R = Q5_R, SLOT = Q5_SLOT;
     using LaneConst = Q4Ops::LaneConst;
     __device__ static LaneConst lane_const(int lane) { return Q4Ops::lane_const(lane); }
@@ -511,6 +535,7 @@ struct Q5Ops {
 constexpr int Q80_CODES = 2048, Q80_D = 128;
 
 struct Q80Ops {
+    static constexpr int P = kRowsPerItem;
     static constexpr int R = Q80_R, SLOT = Q80_SLOT;
     struct LaneConst {
         int aoff[4];
@@ -600,8 +625,11 @@ struct Q80Ops {
 
 constexpr int Q6_QL = 1024, Q6_QH = 512, Q6_SC = 128;
 
-struct Q6Ops {
-    static constexpr int R = Q6_R, SLOT = Q6_SLOT;
+template <int PR>
+struct Q6OpsT {
+    static constexpr int P = PR;
+    static constexpr int R = PR == 2 ? Q6_R : QK_GEMV_P4_Q6_RING, SLOT = PR * (Q6_QL + Q6_QH + Q6_SC);
+    static_assert(R >= 2, "ring needs two slots at least");
     struct LaneConst {
         int qoff[4], coff[4];
     };
@@ -758,6 +786,7 @@ struct Q6Ops {
         else stage_act_q6k<M, NT>(a.codes, a.scales, a.K, s_codes, s_side);
     }
 };
+using Q6Ops = Q6OpsT<2>;
 
 // ------------------------------------------------------------- Q2_K / Q3_K
 // slot: [P][512] 2-bit codes of the step, Q3_K only [P][256] hmask bytes, then [P][128] scale records.
@@ -772,6 +801,7 @@ struct Q6Ops {
 
 template <int QT>
 struct Q23Ops {
+    static constexpr int P = kRowsPerItem;
     static constexpr bool Q3 = QT == QK_TYPE_Q3_K;
     static constexpr int CODES = 512, HM = Q3 ? 256 : 0, SCR = 128;
     static constexpr int R = Q4_R, SLOT = Q3 ? Q3_SLOT : Q2_SLOT;
@@ -900,10 +930,10 @@ __device__ __forceinline__ void prefetch_activation(const GemvArgs &a)
     }
 }
 
-template <class Ops, int M, bool FUSED>
+template <class Ops, int M, bool FUSED, int kWarps>
 __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
 {
-    constexpr int kWarps = Cfg<M, FUSED>::warps, R = Ops::R;
+    constexpr int R = Ops::R, P = Ops::P, NT = kWarps * 32;
     if (QK_GEMV_TRIGGER == 0) qk::pdl_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t N = a.N;
@@ -943,9 +973,9 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
     // so a line fetched early is updated in place and the reads after the wait see the
     // producer's values; the prefetch only saves the DRAM latency when the activation is
     // not in L2 already.
-    prefetch_activation<M, Cfg<M, FUSED>::threads, FUSED>(a);
+    prefetch_activation<M, NT, FUSED>(a);
     qk::pdl_wait();
-    Ops::template stage<M, Cfg<M, FUSED>::threads, FUSED>(a, s_codes, s_side);
+    Ops::template stage<M, NT, FUSED>(a, s_codes, s_side);
     __syncthreads();
     if (QK_GEMV_TRIGGER == 1) qk::pdl_launch_dependents();
 
@@ -992,46 +1022,48 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
     if (QK_GEMV_TRIGGER == 2) qk::pdl_launch_dependents();
 }
 
-template <int M, bool FUSED>
-__global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q4k_kernel(const GemvArgs a)
+template <int M, bool FUSED, int PR>
+__global__ void __launch_bounds__(KCfg<M, FUSED, PR>::threads, KCfg<M, FUSED, PR>::minb)
+    gemv_q4k_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    gemv_body<Q4Ops, M, FUSED>(a, smem);
+    gemv_body<Q4OpsT<PR>, M, FUSED, KCfg<M, FUSED, PR>::warps>(a, smem);
 }
 
-template <int M, bool FUSED>
-__global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q6k_kernel(const GemvArgs a)
+template <int M, bool FUSED, int PR>
+__global__ void __launch_bounds__(KCfg<M, FUSED, PR>::threads, KCfg<M, FUSED, PR>::minb)
+    gemv_q6k_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    gemv_body<Q6Ops, M, FUSED>(a, smem);
+    gemv_body<Q6OpsT<PR>, M, FUSED, KCfg<M, FUSED, PR>::warps>(a, smem);
 }
 
 template <int M, bool FUSED>
 __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q5k_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    gemv_body<Q5Ops, M, FUSED>(a, smem);
+    gemv_body<Q5Ops, M, FUSED, Cfg<M, FUSED>::warps>(a, smem);
 }
 
 template <int M, bool FUSED>
 __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q80_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    gemv_body<Q80Ops, M, FUSED>(a, smem);
+    gemv_body<Q80Ops, M, FUSED, Cfg<M, FUSED>::warps>(a, smem);
 }
 
 template <int M, bool FUSED>
 __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q2k_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    gemv_body<Q23Ops<QK_TYPE_Q2_K>, M, FUSED>(a, smem);
+    gemv_body<Q23Ops<QK_TYPE_Q2_K>, M, FUSED, Cfg<M, FUSED>::warps>(a, smem);
 }
 
 template <int M, bool FUSED>
 __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) gemv_q3k_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    gemv_body<Q23Ops<QK_TYPE_Q3_K>, M, FUSED>(a, smem);
+    gemv_body<Q23Ops<QK_TYPE_Q3_K>, M, FUSED, Cfg<M, FUSED>::warps>(a, smem);
 }
 
 // ------------------------------------------------------------------ host
@@ -1039,7 +1071,7 @@ __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) g
 typedef void (*gemv_fn)(const GemvArgs);
 
 // per device and kernel: largest dynamic shared memory opted in so far
-std::atomic<int> g_smem_set[qk::kMaxDevices][6][2][8];
+std::atomic<int> g_smem_set[qk::kMaxDevices][6][2][8][2];
 
 int prepare(gemv_fn kern, std::atomic<int> &done, size_t smem)
 {
@@ -1057,12 +1089,12 @@ int prepare(gemv_fn kern, std::atomic<int> &done, size_t smem)
 template <bool FUSED>
 gemv_fn pick(int qtype, int M)
 {
-    static const gemv_fn q4[8] = {gemv_q4k_kernel<1, FUSED>, gemv_q4k_kernel<2, FUSED>, gemv_q4k_kernel<3, FUSED>,
-                                  gemv_q4k_kernel<4, FUSED>, gemv_q4k_kernel<5, FUSED>, gemv_q4k_kernel<6, FUSED>,
-                                  gemv_q4k_kernel<7, FUSED>, gemv_q4k_kernel<8, FUSED>};
-    static const gemv_fn q6[8] = {gemv_q6k_kernel<1, FUSED>, gemv_q6k_kernel<2, FUSED>, gemv_q6k_kernel<3, FUSED>,
-                                  gemv_q6k_kernel<4, FUSED>, gemv_q6k_kernel<5, FUSED>, gemv_q6k_kernel<6, FUSED>,
-                                  gemv_q6k_kernel<7, FUSED>, gemv_q6k_kernel<8, FUSED>};
+    static const gemv_fn q4[8] = {gemv_q4k_kernel<1, FUSED, 2>, gemv_q4k_kernel<2, FUSED, 2>, gemv_q4k_kernel<3, FUSED, 2>,
+                                  gemv_q4k_kernel<4, FUSED, 2>, gemv_q4k_kernel<5, FUSED, 2>, gemv_q4k_kernel<6, FUSED, 2>,
+                                  gemv_q4k_kernel<7, FUSED, 2>, gemv_q4k_kernel<8, FUSED, 2>};
+    static const gemv_fn q6[8] = {gemv_q6k_kernel<1, FUSED, 2>, gemv_q6k_kernel<2, FUSED, 2>, gemv_q6k_kernel<3, FUSED, 2>,
+                                  gemv_q6k_kernel<4, FUSED, 2>, gemv_q6k_kernel<5, FUSED, 2>, gemv_q6k_kernel<6, FUSED, 2>,
+                                  gemv_q6k_kernel<7, FUSED, 2>, gemv_q6k_kernel<8, FUSED, 2>};
     static const gemv_fn q5[8] = {gemv_q5k_kernel<1, FUSED>, gemv_q5k_kernel<2, FUSED>, gemv_q5k_kernel<3, FUSED>,
                                   gemv_q5k_kernel<4, FUSED>, gemv_q5k_kernel<5, FUSED>, gemv_q5k_kernel<6, FUSED>,
                                   gemv_q5k_kernel<7, FUSED>, gemv_q5k_kernel<8, FUSED>};
@@ -1081,6 +1113,19 @@ gemv_fn pick(int qtype, int M)
            : qtype == QK_TYPE_Q2_K ? q2[M - 1]
            : qtype == QK_TYPE_Q3_K ? q3[M - 1]
                                    : q6[M - 1];
+}
+
+// four-row kernels (Q4_K / Q6_K, M = 3..8)
+template <bool FUSED>
+gemv_fn pick4(int qtype, int M)
+{
+    static const gemv_fn q4[6] = {gemv_q4k_kernel<3, FUSED, 4>, gemv_q4k_kernel<4, FUSED, 4>,
+                                  gemv_q4k_kernel<5, FUSED, 4>, gemv_q4k_kernel<6, FUSED, 4>,
+                                  gemv_q4k_kernel<7, FUSED, 4>, gemv_q4k_kernel<8, FUSED, 4>};
+    static const gemv_fn q6[6] = {gemv_q6k_kernel<3, FUSED, 4>, gemv_q6k_kernel<4, FUSED, 4>,
+                                  gemv_q6k_kernel<5, FUSED, 4>, gemv_q6k_kernel<6, FUSED, 4>,
+                                  gemv_q6k_kernel<7, FUSED, 4>, gemv_q6k_kernel<8, FUSED, 4>};
+    return qtype == QK_TYPE_Q4_K ? q4[M - 3] : q6[M - 3];
 }
 
 int warps_for(int M, bool fused)
@@ -1121,24 +1166,41 @@ int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, uns
          (a.residual && (qk::overlaps(a.codes_out, cbytes, a.residual, ybytes) ||
                          qk::overlaps(a.scales_out, sbytes, a.residual, ybytes)))))
         return QK_E_ALIAS;
-    const int warps = warps_for((int)M, fused);
+    if ((flags & QK_GEMV_ROWS4) && (flags & QK_GEMV_ROWS2)) return QK_E_SHAPE;
     // ring | activation codes | side data
     const bool q6side = qtype == QK_TYPE_Q6_K || qtype == QK_TYPE_Q2_K || qtype == QK_TYPE_Q3_K;
-    const size_t smem = (size_t)warps * (qtype == QK_TYPE_Q4_K   ? Q4_R * Q4_SLOT
-                                         : qtype == QK_TYPE_Q5_K ? Q5_R * Q5_SLOT
-                                         : qtype == QK_TYPE_Q8_0 ? Q80_R * Q80_SLOT
-                                         : qtype == QK_TYPE_Q2_K ? Q4_R * Q2_SLOT
-                                         : qtype == QK_TYPE_Q3_K ? Q4_R * Q3_SLOT
-                                                                 : Q6_R * Q6_SLOT) +
-                        (size_t)M * K + (size_t)M * (K / 32) * (q6side ? 16 : 8);
+    const size_t act = (size_t)M * K + (size_t)M * (K / 32) * (q6side ? 16 : 8);
+    // four-row items: one activation load serves four weight rows (Q4_K / Q6_K, M >= 3).  Taken
+    // when the row groups of four still give every warp of the grid one at least, or on request,
+    // and only where the ring and the activation fit in shared memory.
+    // (by default for Q4_K only: the Q6_K head measured slower with four-row items, 12 warps)
+    const bool q46 = qtype == QK_TYPE_Q4_K || (qtype == QK_TYPE_Q6_K && (flags & QK_GEMV_ROWS4));
+    const size_t smem4 = (size_t)QK_GEMV_P4_WARPS * (qtype == QK_TYPE_Q4_K ? Q4OpsT<4>::R * Q4OpsT<4>::SLOT
+                                                                            : Q6OpsT<4>::R * Q6OpsT<4>::SLOT) +
+                         act;
+    const int64_t groups4 = (N + 3) / 4;
+    const bool p4 = q46 && M >= 3 && !(flags & QK_GEMV_ROWS2) && smem4 <= qk::max_smem_optin() &&
+                    ((flags & QK_GEMV_ROWS4) ||
+                     groups4 >= (int64_t)QK_GEMV_P4_WARPS * kCtasPerSm * qk::sm_count());
+    const int rows = p4 ? 4 : kRowsPerItem;
+    const int warps = p4 ? QK_GEMV_P4_WARPS : warps_for((int)M, fused);
+    const size_t smem = p4 ? smem4
+                           : (size_t)warps * (qtype == QK_TYPE_Q4_K   ? Q4_R * Q4_SLOT
+                                              : qtype == QK_TYPE_Q5_K ? Q5_R * Q5_SLOT
+                                              : qtype == QK_TYPE_Q8_0 ? Q80_R * Q80_SLOT
+                                              : qtype == QK_TYPE_Q2_K ? Q4_R * Q2_SLOT
+                                              : qtype == QK_TYPE_Q3_K ? Q4_R * Q3_SLOT
+                                                                      : Q6_R * Q6_SLOT) +
+                                 act;
     if (smem > qk::max_smem_optin()) return QK_E_SHAPE;
-    gemv_fn kern = fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M);
+    gemv_fn kern = p4 ? (fused ? pick4<true>(qtype, (int)M) : pick4<false>(qtype, (int)M))
+                      : (fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M));
     const int dev = qk::device_slot();
     if (dev < 0) return QK_E_CUDA;
-    int st = prepare(kern, g_smem_set[dev][qtype - 1][fused ? 1 : 0][M - 1], smem);
+    int st = prepare(kern, g_smem_set[dev][qtype - 1][fused ? 1 : 0][M - 1][p4 ? 1 : 0], smem);
     if (st != QK_OK) return st;
     int64_t grid = (int64_t)kCtasPerSm * qk::sm_count();
-    const int64_t groups = (N + kRowsPerItem - 1) / kRowsPerItem;
+    const int64_t groups = (N + rows - 1) / rows;
     const int64_t need = (groups + warps - 1) / warps;              // CTAs that get a group in the first round
     if (grid > need) grid = need;
     a.N = N;

@@ -160,6 +160,72 @@ def test_gemv_partial_last_round(qt, K, frac, front):
     check(y, y_ref, ab, what=f"{qt} {front} M={M} N={N} K={K}")
 
 
+# Items of four weight rows (Q4_K / Q6_K, M >= 3), forced at small shapes: a ragged last
+# group (N not a multiple of 4), one to eleven superblocks per row, both front ends, with a
+# residual added in place.  The same call with two-row items forced must also be within the
+# bound, and each choice must give the same bits on a second run.
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+@pytest.mark.parametrize("M", [3, 4, 5, 8])
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 2304), (301, 4096), (130, 256 * 11)])
+@pytest.mark.parametrize("front", ["q8", "f32"])
+def test_gemv_rows4_parity(qt, M, N, K, front):
+    if M * K > {"q4k": 81920, "q6k": 40960}[qt]:
+        pytest.skip("activation larger than the GEMV's staging limit")
+    w, wr = weights(qt, N, K, seed=3 * M + N + K)
+    x = synth.activations(M, K, seed=N + 5)
+    r = synth.residual(M, N, seed=M + 9)
+    outs = {}
+    for rows in (4, 2, 4):
+        rt = dev(r)
+        if front == "q8":
+            codes, scales = q8(x)
+            y = gemv(qt, wr, codes, scales, N, K, residual=rt, y=rt, rows=rows)
+        else:
+            codes, scales = qk.empty_q8_1(M, K)
+            f = qk.gemv_q4k_f32 if qt == "q4k" else qk.gemv_q6k_f32
+            y = f(wr, dev(x), N, K, residual=rt, y=rt, codes_out=codes, scales_out=scales, rows=rows)
+        c, d = q8_host(codes, scales)
+        y = y.cpu().numpy()
+        if rows in outs:
+            assert np.array_equal(outs[rows], y), f"{qt} rows={rows}: second run differs"
+        else:
+            y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d, residual=r)
+            check(y, y_ref, ab, r, what=f"{qt} {front} rows={rows} M={M} N={N} K={K}")
+            outs[rows] = y
+
+
+# The default choice takes four-row items once the groups of four fill every warp: a shape
+# just past that point, with a partial last round and a ragged last group, every row checked.
+@pytest.mark.parametrize("qt", ["q4k", "q6k"])
+@pytest.mark.parametrize("front", ["q8", "f32"])
+def test_gemv_rows4_default_partial_round(qt, front):
+    W4 = torch.cuda.get_device_properties(0).multi_processor_count * 12
+    N = 4 * (W4 + W4 // 8) - 3
+    M, K = 4, 4096
+    w, wr = weights(qt, N, K, seed=N + 1)
+    x = synth.activations(M, K, seed=N + 2)
+    if front == "q8":
+        codes, scales = q8(x)
+        y = gemv(qt, wr, codes, scales, N, K).cpu().numpy()
+    else:
+        codes, scales = qk.empty_q8_1(M, K)
+        f = qk.gemv_q4k_f32 if qt == "q4k" else qk.gemv_q6k_f32
+        y = f(wr, dev(x), N, K, codes_out=codes, scales_out=scales).cpu().numpy()
+    c, d = q8_host(codes, scales)
+    y_ref, ab = oracle.gemm(QT[qt][1], w, N, K, c, d)
+    check(y, y_ref, ab, what=f"{qt} {front} default rows M={M} N={N}")
+
+
+def test_gemv_rows_flags_exclusive():
+    M, N, K = 4, 64, 256
+    w, wr = weights("q4k", N, K, seed=1)
+    codes, scales = q8(synth.activations(M, K, seed=2))
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    st = qk.lib().qk_gemv_q4k(wr.data_ptr(), codes.data_ptr(), scales.data_ptr(), M, N, K, None, y.data_ptr(),
+                              qk.GEMV_ROWS4 | qk.GEMV_ROWS2, None)
+    assert qk.STATUS[st] == "QK_E_SHAPE"
+
+
 @pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 @pytest.mark.parametrize("mode", ["separate", "inplace", "pdl"])
 def test_gemv_residual(qt, mode):
