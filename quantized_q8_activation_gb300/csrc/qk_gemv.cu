@@ -2,7 +2,8 @@
 // over a repacked k-quant (Q2_K, Q3_K, Q4_K, Q5_K, Q6_K) or Q8_0 weight.
 //
 // Design (GB300, HBM-bound):
-//  - Persistent grid, one CTA of 16 warps per SM.  Warp w of the grid owns
+//  - Persistent grid, one CTA of 16 warps per SM (20 for the Q6_K kernels with M <= 2
+//    where the ring fits, 12 for four-row items).  Warp w of the grid owns
 //    groups of P output rows w, w + W, w + 2W, ... and walks each group in
 //    steps of up to 8 superblocks (an "item"); in an item every lane copies
 //    16-byte chunks so a warp covers 512 contiguous bytes of the repacked code
@@ -69,6 +70,12 @@ namespace {
 #ifndef QK_GEMV_MINB_SMALL_M
 #define QK_GEMV_MINB_SMALL_M 1         // CTAs per SM the q8_1-input kernels for M <= 2 are compiled for
 #endif
+// warps per CTA of the wide Q6_K kernels for M <= 2, taken where their ring and the activation fit
+// in shared memory (their registers leave room for 20 warps; the Q4_K kernels keep 16, which the
+// chained decode layer measured faster)
+#ifndef QK_GEMV_WARPS_Q6_SMALL_M
+#define QK_GEMV_WARPS_Q6_SMALL_M 20
+#endif
 // four-row items (Q4_K / Q6_K, M >= 3): warps per CTA and ring slots
 #ifndef QK_GEMV_P4_WARPS
 #define QK_GEMV_P4_WARPS 12
@@ -85,10 +92,10 @@ struct Cfg {
     static constexpr int threads = warps * 32;
     static constexpr int minb = M <= 2 ? (FUSED ? QK_GEMV_MINB_FUSED : QK_GEMV_MINB_SMALL_M) : 1;
 };
-// launch shape of a kernel whose items hold PR weight rows
-template <int M, bool FUSED, int PR>
+// launch shape of a kernel whose items hold PR weight rows (WIDE: the 20-warp Q6_K kernels, M <= 2)
+template <int M, bool FUSED, int PR, bool WIDE = false>
 struct KCfg {
-    static constexpr int warps = PR == 4 ? QK_GEMV_P4_WARPS : Cfg<M, FUSED>::warps;
+    static constexpr int warps = PR == 4 ? QK_GEMV_P4_WARPS : WIDE ? QK_GEMV_WARPS_Q6_SMALL_M : Cfg<M, FUSED>::warps;
     static constexpr int threads = warps * 32;
     static constexpr int minb = PR == 4 ? 1 : Cfg<M, FUSED>::minb;
 };
@@ -1030,12 +1037,12 @@ __global__ void __launch_bounds__(KCfg<M, FUSED, PR>::threads, KCfg<M, FUSED, PR
     gemv_body<Q4OpsT<PR>, M, FUSED, KCfg<M, FUSED, PR>::warps>(a, smem);
 }
 
-template <int M, bool FUSED, int PR>
-__global__ void __launch_bounds__(KCfg<M, FUSED, PR>::threads, KCfg<M, FUSED, PR>::minb)
+template <int M, bool FUSED, int PR, bool WIDE = false>
+__global__ void __launch_bounds__(KCfg<M, FUSED, PR, WIDE>::threads, KCfg<M, FUSED, PR, WIDE>::minb)
     gemv_q6k_kernel(const GemvArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem[];
-    gemv_body<Q6OpsT<PR>, M, FUSED, KCfg<M, FUSED, PR>::warps>(a, smem);
+    gemv_body<Q6OpsT<PR>, M, FUSED, KCfg<M, FUSED, PR, WIDE>::warps>(a, smem);
 }
 
 template <int M, bool FUSED>
@@ -1071,7 +1078,7 @@ __global__ void __launch_bounds__(Cfg<M, FUSED>::threads, Cfg<M, FUSED>::minb) g
 typedef void (*gemv_fn)(const GemvArgs);
 
 // per device and kernel: largest dynamic shared memory opted in so far
-std::atomic<int> g_smem_set[qk::kMaxDevices][6][2][8][2];
+std::atomic<int> g_smem_set[qk::kMaxDevices][6][2][8][3];
 
 int prepare(gemv_fn kern, std::atomic<int> &done, size_t smem)
 {
@@ -1126,6 +1133,14 @@ gemv_fn pick4(int qtype, int M)
                                   gemv_q6k_kernel<5, FUSED, 4>, gemv_q6k_kernel<6, FUSED, 4>,
                                   gemv_q6k_kernel<7, FUSED, 4>, gemv_q6k_kernel<8, FUSED, 4>};
     return qtype == QK_TYPE_Q4_K ? q4[M - 3] : q6[M - 3];
+}
+
+// the wide (20-warp) Q6_K kernels, M = 1, 2
+template <bool FUSED>
+gemv_fn pick_q6_wide(int M)
+{
+    static const gemv_fn q6[2] = {gemv_q6k_kernel<1, FUSED, 2, true>, gemv_q6k_kernel<2, FUSED, 2, true>};
+    return q6[M - 1];
 }
 
 int warps_for(int M, bool fused)
@@ -1183,7 +1198,10 @@ int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, uns
                     ((flags & QK_GEMV_ROWS4) ||
                      groups4 >= (int64_t)QK_GEMV_P4_WARPS * kCtasPerSm * qk::sm_count());
     const int rows = p4 ? 4 : kRowsPerItem;
-    const int warps = p4 ? QK_GEMV_P4_WARPS : warps_for((int)M, fused);
+    // Q6_K with M <= 2: the 20-warp kernel where its ring and the activation fit
+    const bool wide = !p4 && qtype == QK_TYPE_Q6_K && M <= 2 &&
+                      (size_t)QK_GEMV_WARPS_Q6_SMALL_M * Q6_R * Q6_SLOT + act <= qk::max_smem_optin();
+    const int warps = p4 ? QK_GEMV_P4_WARPS : wide ? QK_GEMV_WARPS_Q6_SMALL_M : warps_for((int)M, fused);
     const size_t smem = p4 ? smem4
                            : (size_t)warps * (qtype == QK_TYPE_Q4_K   ? Q4_R * Q4_SLOT
                                               : qtype == QK_TYPE_Q5_K ? Q5_R * Q5_SLOT
@@ -1193,11 +1211,12 @@ int gemv(int qtype, bool fused, GemvArgs a, int64_t M, int64_t N, int64_t K, uns
                                                                       : Q6_R * Q6_SLOT) +
                                  act;
     if (smem > qk::max_smem_optin()) return QK_E_SHAPE;
-    gemv_fn kern = p4 ? (fused ? pick4<true>(qtype, (int)M) : pick4<false>(qtype, (int)M))
-                      : (fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M));
+    gemv_fn kern = p4     ? (fused ? pick4<true>(qtype, (int)M) : pick4<false>(qtype, (int)M))
+                   : wide ? (fused ? pick_q6_wide<true>((int)M) : pick_q6_wide<false>((int)M))
+                          : (fused ? pick<true>(qtype, (int)M) : pick<false>(qtype, (int)M));
     const int dev = qk::device_slot();
     if (dev < 0) return QK_E_CUDA;
-    int st = prepare(kern, g_smem_set[dev][qtype - 1][fused ? 1 : 0][M - 1][p4 ? 1 : 0], smem);
+    int st = prepare(kern, g_smem_set[dev][qtype - 1][fused ? 1 : 0][M - 1][p4 ? 1 : wide ? 2 : 0], smem);
     if (st != QK_OK) return st;
     int64_t grid = (int64_t)kCtasPerSm * qk::sm_count();
     const int64_t groups = (N + rows - 1) / rows;

@@ -276,6 +276,28 @@ def test_gemv_max_activation(qt):
     check(y, y_ref, ab, what="max M*K")
 
 
+# Q6_K with M <= 2 runs 20 warps per CTA where the ring and the activation fit in shared memory and
+# 16 beyond (M*K over about 21.8K values): both sides of the choice, a partial last round of row
+# pairs for 20 warps, both front ends, every row checked.
+@pytest.mark.parametrize("M,K", [(1, 4096), (2, 8192), (1, 20480), (1, 40960), (2, 20480)])
+@pytest.mark.parametrize("front", ["q8", "f32"])
+def test_gemv_q6k_small_m_warp_choice(M, K, front):
+    W = torch.cuda.get_device_properties(0).multi_processor_count * 20
+    N = 2 * (W + W // 9) - 1 if K <= 8192 else 301
+    w, wr = weights("q6k", N, K, seed=N + K + M)
+    x = synth.activations(M, K, seed=K + 11)
+    r = synth.residual(M, N, seed=M + 12)
+    if front == "q8":
+        codes, scales = q8(x)
+        y = qk.gemv_q6k(wr, codes, scales, N, K, residual=dev(r)).cpu().numpy()
+    else:
+        codes, scales = qk.empty_q8_1(M, K)
+        y = qk.gemv_q6k_f32(wr, dev(x), N, K, residual=dev(r), codes_out=codes, scales_out=scales).cpu().numpy()
+    c, d = q8_host(codes, scales)
+    y_ref, ab = oracle.gemm(oracle.Q6_K, w, N, K, c, d, residual=r)
+    check(y, y_ref, ab, r, what=f"q6k {front} M={M} N={N} K={K}")
+
+
 @pytest.mark.parametrize("qt", ["q4k", "q5k", "q6k", "q80", "q2k", "q3k"])
 def test_gemv_deterministic_and_guard_band(qt):
     M, N, K = 3, 1000, 4096
