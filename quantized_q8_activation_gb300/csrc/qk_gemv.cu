@@ -300,6 +300,33 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// Fixed-order reduce-scatter of 2^L per-lane values over the warp: at each of the first L xor
+// steps (offsets 16, 8, ...) every lane keeps one half of its values and adds its partner's copy
+// of that half, then the remaining 5 - L steps add up the one value left.  Lane l ends with the
+// warp total of value l >> (5 - L).  Per group of outputs it takes about a third of the shuffles
+// and adds of one xor tree per value.
+template <int L>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[1 << L], int lane)
+{
+#pragma unroll
+    for (int k = 0; k < L; k++) {
+        const int o = 16 >> k, h = (1 << L) >> (k + 1);
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; i++) {
+            const float send = up ? v[i] : v[i + h];
+            const float keep = up ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int o = 16 >> L; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+
+__host__ __device__ constexpr int ceil_log2(int v) { return v <= 1 ? 0 : 1 + ceil_log2((v + 1) / 2); }
+
 // ------------------------------------------------------------ work split
 // Rows are taken in groups of P consecutive rows; an item is (group, step s),
 // the step-s bytes of the group's rows.  Groups are dealt round robin over
@@ -1004,19 +1031,42 @@ __device__ __forceinline__ void gemv_body(const GemvArgs &a, uint8_t *smem)
         Ops::template compute<M>(ring + slot * Ops::SLOT, rd.s, B, lane, reg[0], lc, s_codes, s_side, K, acc);
         __syncwarp();
         if (rd.s == nsteps - 1) {
-            // fixed xor tree over the lanes, then lane m writes output m of each row of the group
+            if constexpr (M >= 3) {
+                // the group's P x M sums by a fixed-order reduce-scatter: lane (j << (5 - LV))
+                // holds sum j = r M + m and writes output m of row r
+                constexpr int V = P * M, LV = ceil_log2(V);
+                float v[1 << LV];
 #pragma unroll
-            for (int r = 0; r < P; r++)
+                for (int j = 0; j < (1 << LV); j++) v[j] = j < V ? acc[j / M][j % M] : 0.0f;
 #pragma unroll
-                for (int m = 0; m < M; m++) {
-                    const float v = warp_sum(acc[r][m]);
-                    acc[r][m] = 0.0f;
+                for (int r = 0; r < P; r++)
+#pragma unroll
+                    for (int m = 0; m < M; m++) acc[r][m] = 0.0f;
+                const float t = warp_reduce_scatter<LV>(v, lane);
+                const int j = lane >> (5 - LV);
+                if ((lane & ((1 << (5 - LV)) - 1)) == 0 && j < V) {
+                    const int r = j / M, m = j - r * M;
                     const int64_t n = P * rd.g + r;
-                    if (lane == m && n < N) {
+                    if (n < N) {
                         const size_t o = (size_t)m * N + n;
-                        a.y[o] = a.residual ? __fadd_rn(v, a.residual[o]) : v;
+                        a.y[o] = a.residual ? __fadd_rn(t, a.residual[o]) : t;
                     }
                 }
+            } else {
+                // fixed xor tree over the lanes, then lane m writes output m of each row of the group
+#pragma unroll
+                for (int r = 0; r < P; r++)
+#pragma unroll
+                    for (int m = 0; m < M; m++) {
+                        const float v = warp_sum(acc[r][m]);
+                        acc[r][m] = 0.0f;
+                        const int64_t n = P * rd.g + r;
+                        if (lane == m && n < N) {
+                            const size_t o = (size_t)m * N + n;
+                            a.y[o] = a.residual ? __fadd_rn(v, a.residual[o]) : v;
+                        }
+                    }
+            }
         }
         rd.next(nsteps);
 #pragma unroll
